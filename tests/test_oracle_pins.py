@@ -1,0 +1,331 @@
+"""Pins of the fp64 oracle against things other than itself.
+
+Each test ties one oracle function to a closed form, a library routine, a
+value the pages print, brute force, or finite differences, chosen so that a
+plausible slip (a dropped term, a wrong sign or index, a transposed operand,
+an off-by-one scale exponent) fails at least one of them.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as fm
+from oracle import moe
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ formats
+
+def test_bf16_rounding_matches_torch_cast():
+    rng = np.random.default_rng(0)
+    v = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, 20000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.01171875, -3.3e-39]]).astype(np.float32)
+    ours = fm.round_bf16(v.astype(np.float64))
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(ours, ref)
+
+
+def test_fp32_rounding_matches_numpy_cast():
+    rng = np.random.default_rng(1)
+    v = rng.standard_normal(20000) * 10.0 ** rng.integers(-40, 38, 20000)
+    np.testing.assert_array_equal(fm.round_fp32(v), v.astype(np.float32).astype(np.float64))
+
+
+def test_e4m3_all_codes_round_trip():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = fm.e4m3_decode(codes)
+    finite = ~np.isnan(vals)
+    assert finite.sum() == 254          # 0x7F and 0xFF are NaN
+    assert np.nanmax(vals) == 448.0 and np.nanmin(vals) == -448.0
+    assert vals[1] == 2.0 ** -9         # smallest subnormal
+    np.testing.assert_array_equal(fm.round_e4m3(vals[finite]), vals[finite])
+    back = fm.e4m3_encode(vals[finite])
+    # +0 and -0 are distinct codes with equal value; compare values for those
+    np.testing.assert_array_equal(fm.e4m3_decode(back), vals[finite])
+    np.testing.assert_array_equal(back[codes[finite] != 0x80], codes[finite][codes[finite] != 0x80])
+
+
+def test_e4m3_rounding_matches_torch_cast_in_range():
+    rng = np.random.default_rng(2)
+    v = rng.uniform(-464, 464, 50000) * 2.0 ** rng.integers(-14, 1, 50000)
+    v = v.astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(fm.round_e4m3(v), ref)
+
+
+def test_e4m3_hand_cases(golden_dir):
+    for c in _load(golden_dir, "e4m3_hand_cases.json")["cases"]:
+        r = float(fm.round_e4m3(c["value"]))
+        assert r == c["rounded"], c
+        assert int(fm.e4m3_encode(r)) == c["code"], c
+
+
+def test_e8m0_decode():
+    assert fm.e8m0_decode(127) == 1.0
+    assert fm.e8m0_decode(0) == 2.0 ** -127
+    assert fm.e8m0_decode(254) == 2.0 ** 127
+    assert np.isnan(fm.e8m0_decode(255))
+
+
+def test_mx_hand_blocks(golden_dir):
+    for b in _load(golden_dir, "mx_hand_blocks.json")["blocks"]:
+        v = np.full(32, b["fill"])
+        for i, x in b["set"].items():
+            v[int(i)] = x
+        q, e = fm.mx_quantize(v[None, :])
+        assert int(e[0, 0]) + 127 == b["scale_byte"], b["name"]
+        qx = np.full(32, b["q_fill"])
+        for i, x in b["q_set"].items():
+            qx[int(i)] = x
+        np.testing.assert_array_equal(q[0], qx, err_msg=b["name"])
+        d = np.full(32, b["deq_fill"])
+        for i, x in b["deq_set"].items():
+            d[int(i)] = x
+        np.testing.assert_array_equal(fm.mx_dequantize(q, e)[0], d, err_msg=b["name"])
+
+
+def test_mx_axis_and_block_alignment():
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal((64, 96)) * np.exp(rng.standard_normal((64, 96)))
+    # along rows: blocks are rows [0,32) and [32,64), quantised independently
+    full = fm.mx_fake_quant(v, axis=0)
+    top = fm.mx_fake_quant(v[:32], axis=0)
+    np.testing.assert_array_equal(full[:32], top)
+    # along rows == along columns of the transpose
+    np.testing.assert_array_equal(full, fm.mx_fake_quant(v.T, axis=-1).T)
+    # elements in E4M3's normal range lie within half an ulp (2^-4 relative)
+    # of v; elements scaled past 448 saturate (the OCP rule lets the block
+    # maximum land in [256, 512))
+    q, e = fm.mx_quantize(v, axis=0)
+    y = v * np.repeat(np.ldexp(1.0, -e), 32, axis=0)
+    normal = (np.abs(y) >= 2.0 ** -6) & (np.abs(y) < 448)
+    rel = np.abs(full - v) / np.abs(v)
+    assert np.all(rel[normal] <= 2.0 ** -4 + 1e-12)
+    sat = np.abs(y) >= 464
+    assert np.all(np.abs(q[sat]) == 448.0)
+    assert np.all(np.sign(full[full != 0]) == np.sign(v[full != 0]))
+
+
+def test_mx_weight_32x32_single_scale_per_tile():
+    rng = np.random.default_rng(4)
+    w = rng.standard_normal((2, 64, 96))
+    w[0, 5, 70] = 1000.0
+    q, e = fm.mx_quantize_weight_32x32(w)
+    assert e.shape == (2, 2, 3)
+    assert e[0, 0, 2] == int(math.floor(math.log2(1000.0))) - 8
+    # the tile's one scale equals the row-wise scale of the tile's whole content
+    tile = w[0, 0:32, 64:96].reshape(1, -1)[:, :32 * 32]
+    amax = np.abs(tile).max()
+    assert e[0, 0, 2] == fm.mx_shared_exponent(amax)
+    # same exponent drives the transpose: quantising w^T with the tile rule gives q^T
+    qT, eT = fm.mx_quantize_weight_32x32(np.swapaxes(w, 1, 2))
+    np.testing.assert_array_equal(qT, np.swapaxes(q, 1, 2))
+    np.testing.assert_array_equal(eT, np.swapaxes(e, 1, 2))
+
+
+# -------------------------------------------------------------------- SiLU
+
+def test_silu_closed_form(golden_dir):
+    g = _load(golden_dir, "silu_closed_form.json")
+    for z, v in g["silu"]:
+        assert moe.silu(z) == pytest.approx(v, rel=1e-15, abs=1e-300)
+    for z, v in g["silu_grad"]:
+        assert moe.silu_grad(z) == pytest.approx(v, rel=1e-14)
+
+
+def test_silu_grad_is_derivative():
+    z = np.linspace(-8, 8, 161)
+    h = 1e-6
+    fd = (moe.silu(z + h) - moe.silu(z - h)) / (2 * h)
+    np.testing.assert_allclose(moe.silu_grad(z), fd, rtol=1e-8, atol=1e-9)
+
+
+# ------------------------------------------------------------------ routing
+
+def test_offsets_worked_example(golden_dir):
+    g = _load(golden_dir, "offsets_worked_example.json")
+    counts = g["counts"]
+    ids = np.concatenate([np.full(c, e) for e, c in enumerate(counts)])
+    ids = np.random.default_rng(5).permutation(ids).reshape(-1, 1)
+    rt = moe.route(ids, len(counts), pad=1)
+    assert rt.counts.tolist() == counts
+    assert rt.offsets.tolist() == g["offsets"]
+    for e, (a, b) in enumerate(g["expert_row_ranges"]):
+        assert np.all(ids.reshape(-1)[rt.perm[a:b]] == e)
+
+
+@pytest.mark.parametrize("T,K,E,pad", [(1, 1, 1, 32), (37, 3, 5, 32), (200, 6, 64, 32), (50, 2, 8, 1)])
+def test_route_matches_stable_argsort(T, K, E, pad):
+    rng = np.random.default_rng(T * 7 + E)
+    ids = rng.integers(-1, E, size=(T, K))
+    ids[0, 0] = E + 3          # out of range -> inactive + flagged
+    if T > 1:
+        ids[1, :] = -1         # an all-inactive token
+    rt = moe.route(ids, E, pad)
+    flat = ids.reshape(-1)
+    active = (flat >= 0) & (flat < E)
+    assert rt.counts.sum() == active.sum() == rt.num_active
+    assert rt.bad_ids.tolist() == ((flat < -1) | (flat >= E)).tolist()
+    # expected order: stable argsort of the IDs over the active routes
+    act_idx = np.nonzero(active)[0]
+    order = act_idx[np.argsort(flat[act_idx], kind="stable")]
+    got = rt.perm[rt.perm >= 0]
+    np.testing.assert_array_equal(got, order)
+    assert np.all(np.diff(rt.poffsets) % pad == 0)
+    assert np.all(np.diff(rt.poffsets) - rt.counts < pad)
+    for e in range(E):
+        a = rt.poffsets[e]
+        seg = rt.perm[a:rt.poffsets[e + 1]]
+        assert np.all(seg[:rt.counts[e]] >= 0) and np.all(seg[rt.counts[e]:] == -1)
+    # inverse permutation
+    assert np.all(rt.inv[~active] == -1)
+    np.testing.assert_array_equal(rt.perm[rt.inv[active]], act_idx)
+
+
+# ------------------------------------------------------------------ forward
+
+def _case(T, D, F, E, K, seed, inactive=0.1):
+    rng = np.random.default_rng(seed)
+    x = fm.round_bf16(rng.standard_normal((T, D)))
+    w13 = fm.round_bf16(rng.standard_normal((E, 2 * F, D)) / np.sqrt(D))
+    w2 = fm.round_bf16(rng.standard_normal((E, D, F)) / np.sqrt(F))
+    ids = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int64)
+    s = rng.uniform(0.05, 1.0, (T, K)).astype(np.float32)
+    off = rng.uniform(size=(T, K)) < inactive
+    ids[off] = -1
+    s[off] = 0.0
+    return x, ids, s, w13, w2
+
+
+@pytest.mark.parametrize("precision", ["f64", "bf16", "mxfp8"])
+def test_routed_forward_matches_per_token_loop(precision):
+    x, ids, s, w13, w2 = _case(40, 64, 96, 6, 3, 11)
+    ids[7, :] = -1
+    init = fm.round_bf16(np.random.default_rng(12).standard_normal(x.shape))
+    st = moe.forward(x, ids, s, w13, w2, precision, out_init=init)
+    ref = moe.forward_per_token(x, ids, s, w13, w2, precision, out_init=init)
+    ref = np.stack([ref[t] for t in range(x.shape[0])])
+    tol = 1e-12 if precision == "f64" else 1e-2
+    err = np.max(np.abs(st["out"] - ref)) / np.max(np.abs(ref))
+    assert err <= tol
+    if precision != "f64":
+        # rounding points make most outputs identical, not just close
+        assert np.mean(st["out"] == ref) > 0.97
+
+
+def test_single_expert_is_dense_swiglu():
+    """E=1, K=1, score=1 reduces to the dense SwiGLU FFN W2 (SiLU(Wg x) * (Wu x))."""
+    x, _, _, w13, w2 = _case(9, 32, 48, 1, 1, 13)
+    ids = np.zeros((9, 1), np.int64)
+    for score in (1.0, 0.5):
+        s = np.full((9, 1), score, np.float32)
+        out = moe.forward(x, ids, s, w13, w2, "f64")["out"]
+        wg, wu = w13[0][:48], w13[0][48:]
+        g = x @ wg.T
+        u = x @ wu.T
+        h = g / (1 + np.exp(-g)) * u
+        np.testing.assert_allclose(out, score * (h @ w2[0].T), rtol=1e-12, atol=1e-14)
+
+
+def test_inactive_routes_contribute_nothing():
+    x, ids, s, w13, w2 = _case(16, 32, 32, 4, 2, 14, inactive=0.0)
+    ids[3, :] = -1
+    s[3, :] = 0.0
+    for p in ("f64", "bf16", "mxfp8"):
+        st = moe.forward(x, ids, s, w13, w2, p)
+        assert np.all(st["out"][3] == 0.0)
+    # a -1 route is ignored whatever score it carries
+    ids2, s2 = ids.copy(), s.copy()
+    ids2[5, 1] = -1
+    s2[5, 1] = 0.7
+    s3 = s2.copy()
+    s3[5, 1] = 0.0
+    a = moe.forward(x, ids2, s2, w13, w2, "bf16")["out"]
+    b = moe.forward(x, ids2, s3, w13, w2, "bf16")["out"]
+    np.testing.assert_array_equal(a, b)
+
+
+def test_expert_relabelling_is_equivariant():
+    x, ids, s, w13, w2 = _case(24, 32, 32, 5, 2, 15)
+    p = np.array([3, 0, 4, 1, 2])           # new label of old expert e is p[e]
+    ids2 = np.where(ids >= 0, p[np.maximum(ids, 0)], -1)
+    w13b = np.empty_like(w13)
+    w2b = np.empty_like(w2)
+    w13b[p], w2b[p] = w13, w2
+    for prec in ("bf16", "mxfp8"):
+        a = moe.forward(x, ids, s, w13, w2, prec)["out"]
+        b = moe.forward(x, ids2, s, w13b, w2b, prec)["out"]
+        np.testing.assert_array_equal(a, b)
+
+
+# ----------------------------------------------------------------- backward
+
+def test_backward_matches_finite_differences():
+    T, D, F, E, K = 6, 5, 4, 3, 2
+    x, ids, s, w13, w2 = _case(T, D, F, E, K, 16, inactive=0.0)
+    ids[2, 1] = -1
+    s[2, 1] = 0.0
+    rng = np.random.default_rng(17)
+    dY = rng.standard_normal((T, D))
+
+    def loss(x_, w13_, w2_):
+        return float(np.sum(dY * moe.forward(x_, ids, s, w13_, w2_, "f64")["out"]))
+
+    st = moe.forward(x, ids, s, w13, w2, "f64")
+    g = moe.backward(st, dY, w13, w2)
+    h = 1e-6
+
+    def fd(arr, idx, which):
+        a1, a2 = arr.copy(), arr.copy()
+        a1[idx] += h
+        a2[idx] -= h
+        args1 = {"x": (a1, w13, w2), "w13": (x, a1, w2), "w2": (x, w13, a1)}[which]
+        args2 = {"x": (a2, w13, w2), "w13": (x, a2, w2), "w2": (x, w13, a2)}[which]
+        return (loss(*args1) - loss(*args2)) / (2 * h)
+
+    for idx in np.ndindex(x.shape):
+        assert g["dX"][idx] == pytest.approx(fd(x, idx, "x"), rel=1e-6, abs=1e-8)
+    for idx in list(np.ndindex(w13.shape))[::3]:
+        assert g["dW13"][idx] == pytest.approx(fd(w13, idx, "w13"), rel=1e-6, abs=1e-8)
+    for idx in list(np.ndindex(w2.shape))[::2]:
+        assert g["dW2"][idx] == pytest.approx(fd(w2, idx, "w2"), rel=1e-6, abs=1e-8)
+
+
+def test_backward_inactive_routes_get_no_gradient():
+    x, ids, s, w13, w2 = _case(20, 32, 32, 5, 2, 18, inactive=0.0)
+    ids[ids == 4] = 0            # expert 4 is reached by no active route...
+    ids[9, :] = [4, -1]          # ...except one that we then disable
+    ids[9, 0] = -1
+    s[9, :] = 0.0
+    dY = np.random.default_rng(19).standard_normal(x.shape)
+    for p in ("f64", "bf16", "mxfp8"):
+        st = moe.forward(x, ids, s, w13, w2, p)
+        g = moe.backward(st, dY, w13, w2)
+        assert np.all(g["dX"][9] == 0.0)
+        assert np.all(g["dW13"][4] == 0.0) and np.all(g["dW2"][4] == 0.0)
+
+
+@pytest.mark.parametrize("precision", ["bf16", "mxfp8"])
+def test_rounded_backward_tracks_exact_backward(precision):
+    x, ids, s, w13, w2 = _case(64, 64, 64, 4, 2, 20)
+    dY = fm.round_bf16(np.random.default_rng(21).standard_normal(x.shape))
+    ex = moe.backward(moe.forward(x, ids, s, w13, w2, "f64"), dY, w13, w2)
+    rd = moe.backward(moe.forward(x, ids, s, w13, w2, precision), dY, w13, w2)
+    # MXFP8: the OCP scale rule puts a block's maximum in [256, 512) after
+    # scaling, so a maximum scaled past 448 is clipped by up to 12.5%; a
+    # weight gradient dominated by one row inherits that clipping.
+    tol = 0.02 if precision == "bf16" else 0.15
+    for k in ("dX", "dW13", "dW2"):
+        err = np.max(np.abs(rd[k] - ex[k])) / np.max(np.abs(ex[k]))
+        assert err < tol, (k, err)
