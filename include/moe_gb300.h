@@ -1,0 +1,300 @@
+/*
+ * moe_gb300.h -- C ABI of the dropless routed-expert MoE layer on one GB300.
+ *
+ * One GPU holds all E experts (no expert parallelism, no peer buffers).  The
+ * caller supplies top-K expert IDs and scores per token; the library routes
+ * and permutes the token rows by expert, runs a grouped W13 (gate + up) GEMM
+ * with a fused SwiGLU epilogue and a grouped W2 GEMM on the tcgen05 tensor
+ * cores, and sums each token's K score-weighted expert outputs in a fixed
+ * order.  The backward pass produces dX, dW13 and dW2.
+ *
+ * Sources (page title, section):
+ *   [DM]   "Dist-MoE: Speed-of-light distributed Mixture-of-Experts kernels",
+ *          visual explainer (meta-pytorch.org/dist_moe).
+ *   [BLOG] "Mixture of Experts: How Routing Becomes GPU Computation"
+ *          (g-u-n.github.io).
+ *   [NEWS] "Meta Dist-MoE: Open-Source Fused MoE Kernels for Blackwell"
+ *          (explainx.ai).
+ *
+ * Conventions that hold for every call below
+ *   - All tensors are row-major and contiguous; device pointers unless a
+ *     parameter says "host".  Every device pointer must be 16-byte aligned.
+ *   - Calls that take a cudaStream_t only enqueue work on that stream.  They
+ *     never allocate, never synchronise and never read device memory on the
+ *     host, so a sequence of them can be captured in a CUDA graph; the
+ *     addresses the context owns never change after moe_ctx_create.
+ *   - Host-detectable errors (NULL pointers, sizes above the context's
+ *     capacity, shape or precision mismatches, misaligned pointers) return a
+ *     status synchronously and enqueue nothing.
+ *   - Errors the GPU detects (IDs outside [-1, E), an ID of -1 carrying a
+ *     nonzero score when MOE_DEBUG_CHECKS is set, a device wait that ran out
+ *     of time) never trap: the kernel sets a bit in the context's error word
+ *     and carries on (a bad ID is treated as inactive).  moe_ctx_get_error
+ *     reads and clears the word.
+ *   - A context is reusable sequentially but not reentrant: calls that may
+ *     overlap on the GPU need separate contexts ([DM] section 04, last
+ *     paragraph of "Save and Recompute Decisions"; [NEWS] "How the execution
+ *     model works").
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* NULL/misaligned pointer, bad size or shape */
+  MOE_ERR_CAPACITY = 2,      /* T above the context's max_tokens           */
+  MOE_ERR_BAD_ROUTE = 3,     /* reserved: routes are checked on the GPU    */
+  MOE_ERR_UNSUPPORTED = 4,   /* shape the kernels do not tile (see below)  */
+  MOE_ERR_CUDA = 5,          /* a CUDA runtime call failed                 */
+  MOE_ERR_TIMEOUT = 6        /* reserved: device timeouts set an error bit */
+} moe_status;
+
+/* Bits of the device error word (moe_ctx_get_error). */
+#define MOE_DEV_ERR_BAD_ID          0x1u  /* an ID outside [-1, E) was seen     */
+#define MOE_DEV_ERR_INACTIVE_SCORE  0x2u  /* ID -1 with score != 0 (debug only) */
+#define MOE_DEV_ERR_TIMEOUT         0x4u  /* a bounded device wait expired      */
+
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
+
+/* moe_config.flags */
+#define MOE_TRAINING      0x1u  /* forward saves state; backward is allowed   */
+#define MOE_DEBUG_CHECKS  0x2u  /* also flag ID -1 routes with nonzero score */
+
+/* call_flags of moe_forward */
+#define MOE_ACCUMULATE_OUT 0x1u /* out = round(out + sum_k s*h3) (shared expert first) */
+/* call_flags of moe_backward */
+#define MOE_ACCUMULATE_DX  0x1u /* dx  = round(dx + sum_k dxr)                 */
+#define MOE_DW_FP32        0x2u /* dW13/dW2 are float32 instead of BF16        */
+#define MOE_DW_ACCUMULATE  0x4u /* dW += new gradient (in the dW dtype)        */
+
+/*
+ * Layer shape and precision.  The kernels tile D and F in steps of 128, so
+ * d_model % 128 == 0 and d_ff % 128 == 0 are required (MOE_ERR_UNSUPPORTED
+ * otherwise); num_experts <= 1024, top_k <= 32.
+ *   BF16:  BF16 operands, FP32 accumulation, BF16 stored intermediates.
+ *   MXFP8: E4M3 operands with one E8M0 scale per 32 values along the
+ *          contraction axis ([DM] section 02, "Block-Scaled Quantization"),
+ *          FP32 accumulation, BF16 h1/h3.
+ */
+typedef struct {
+  int32_t max_tokens;     /* T_max: largest T any call will pass            */
+  int32_t d_model;        /* D                                              */
+  int32_t d_ff;           /* F (h1 has 2F columns: gate then up)            */
+  int32_t num_experts;    /* E                                              */
+  int32_t top_k;          /* K routes per token                             */
+  moe_precision precision;
+  uint32_t flags;         /* MOE_TRAINING | MOE_DEBUG_CHECKS                */
+} moe_config;
+
+/*
+ * One stacked expert weight [E, N, K] (K contiguous) as the GEMMs read it.
+ *   W13: N = 2F, K = D (rows 0..F-1 gate, F..2F-1 up; [DM] section 01
+ *        "Inputs, shapes, and inactive routes", [BLOG] section 2
+ *        grouped_swiglu_forward_combined).
+ *   W2:  N = D,  K = F.
+ * BF16:  data = the caller's BF16 tensor; scale = scale_t = NULL; data_t =
+ *        BF16 [E, K, N] transposed copy (needed by moe_backward only).
+ * MXFP8: data = E4M3 codes [E, N, K], scale = E8M0 [E, N, K/32];
+ *        data_t = E4M3 codes [E, K, N], scale_t = E8M0 [E, K, N/32]
+ *        (backward only).  Filled by prepare_block_scaled_weight.
+ * The struct is read on the host at call time; the pointers are not owned.
+ */
+typedef struct {
+  moe_precision precision;
+  int32_t E, N, K;
+  const void* data;
+  const uint8_t* scale;
+  const void* data_t;
+  const uint8_t* scale_t;
+} moe_weight;
+
+typedef struct moe_ctx moe_ctx;
+
+/*
+ * Create a context: checks the config, allocates all scratch once (every
+ * later call reuses it, so its addresses are stable for graph capture) and
+ * creates no stream.  Scratch is sized for max_tokens*top_k routes plus 31
+ * pad rows per expert, which bounds every routing, so a call can never
+ * overflow it ([NEWS] "scratch is a hard limit" -- here it is sized so the
+ * limit cannot be reached).  Must be called with the target device current.
+ * Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_CUDA; *out is
+ * set only on MOE_OK.
+ */
+MOE_API moe_status moe_ctx_create(const moe_config* cfg, moe_ctx** out);
+
+/* Free the context's scratch.  The caller must make sure no enqueued work
+ * that uses it is still running (synchronise first). */
+MOE_API moe_status moe_ctx_destroy(moe_ctx* ctx);
+
+/* Bytes of device scratch a context with this config allocates (0 if the
+ * config is invalid). */
+MOE_API size_t moe_ctx_scratch_bytes(const moe_config* cfg);
+
+/*
+ * Bytes of the per-layer saved state that a training forward writes and the
+ * matching backward reads: routing arrays, a copy of the scores, BF16 h1
+ * [R_cap, 2F] and the WGRAD column bundles of x and h2 ([DM] section 04,
+ * "Activation Lifetimes and Backward Readers": MXFP8 full-save keeps the x/h2
+ * column bundles and dense h1).  The caller allocates it (16-byte aligned)
+ * and keeps one per live layer.  0 for an invalid config.
+ */
+MOE_API size_t moe_saved_state_bytes(const moe_config* cfg);
+
+/* Saved-state fields, for inspection by tests (moe_saved_state_field). */
+typedef enum {
+  MOE_SAVED_HEADER = 0,     /* int32[16]: [0] T, [1] num_blocks, [2] rows used */
+  MOE_SAVED_COUNTS = 1,     /* int32[E]     active routes per expert           */
+  MOE_SAVED_OFFSETS = 2,    /* int32[E+1]   exclusive prefix of counts         */
+  MOE_SAVED_POFFSETS = 3,   /* int32[E+1]   same with counts padded to 32      */
+  MOE_SAVED_PERM = 4,       /* int32[R_cap] route t*K+k of each row, -1 = pad  */
+  MOE_SAVED_INV = 5,        /* int32[T_max*K] row of each route, -1 = inactive */
+  MOE_SAVED_BLOCKS = 6,     /* int32[4*B_cap] (expert, first row, rows, 0)     */
+  MOE_SAVED_SCORES = 7,     /* float[T_max*K] scores, 0 for inactive routes    */
+  MOE_SAVED_H1 = 8,         /* bf16[R_cap, 2F]                                 */
+  MOE_SAVED_XCOL = 9,       /* x column bundle: bf16 [D, R_cap] or e4m3 codes  */
+  MOE_SAVED_XCOL_SCALE = 10,/* e8m0 [D, R_cap/32] (MXFP8 only)                 */
+  MOE_SAVED_H2COL = 11,     /* h2 column bundle: bf16 [F, R_cap] or e4m3       */
+  MOE_SAVED_H2COL_SCALE = 12,/* e8m0 [F, R_cap/32] (MXFP8 only)                */
+  MOE_SAVED_NUM_FIELDS = 13
+} moe_saved_field;
+
+/* Offset and size in bytes of one saved-state field; the row capacity
+ * R_cap used by the layouts above is returned by moe_row_capacity. */
+MOE_API moe_status moe_saved_state_field(const moe_config* cfg, int field, size_t* offset, size_t* bytes);
+
+/* R_cap: rows of every per-route buffer = max_tokens*top_k + 31*E rounded
+ * up to a multiple of 128 (0 for an invalid config). */
+MOE_API int64_t moe_row_capacity(const moe_config* cfg);
+
+/*
+ * Prepare one stacked expert weight once, outside any timed region
+ * ([NEWS] "Supported modes": prepare_block_scaled_weight quantises expert
+ * weights once with 32x32 blocks for MXFP8 training; [DM] section 02: with
+ * 32x32 blocks the forward and input-gradient GEMMs share qdata with
+ * distinct scale orientations).
+ *   w       BF16 [E, N, K] (device).  N % 32 == 0 and K % 32 == 0.
+ *   MXFP8:  one E8M0 scale per 32x32 tile (OCP MX rule: floor(log2 amax) - 8,
+ *           values rounded to nearest-even E4M3 and saturated at 448) is
+ *           written to scale [E,N,K/32] and, when data_t != NULL, the
+ *           transposed codes to data_t [E,K,N] with scale_t [E,K,N/32].
+ *           data may not be NULL.
+ *   BF16:   data and scale must be NULL; data_t (BF16 [E,K,N]) receives the
+ *           transpose used by the input-gradient GEMMs.
+ * The outputs are caller-owned device buffers.  Enqueued on `stream`.
+ */
+MOE_API moe_status prepare_block_scaled_weight(const void* w, int32_t E, int32_t N, int32_t K,
+                                       moe_precision precision, void* data, uint8_t* scale,
+                                       void* data_t, uint8_t* scale_t, cudaStream_t stream);
+
+/*
+ * Forward of the routed layer ([BLOG] section 2 "SwiGLU forward: compute
+ * and combine expert outputs"; [DM] sections 01-02):
+ *   x          bf16 [T, D]
+ *   topk_ids   int32 [T, K]  expert of each route; -1 marks an inactive route
+ *   topk_scores float [T, K] route weight; an inactive route's score is ignored
+ *   W13, W2    prepared weights of the context's precision (see moe_weight)
+ *   out        bf16 [T, D]   out[t] = bf16(sum_k s*h3), summed in FP32 in
+ *                            k order; a token with no active route gets 0.
+ *                            With MOE_ACCUMULATE_OUT the old out is added
+ *                            first (one rounding at the end).
+ *   saved      NULL for inference; for a training context, a buffer of
+ *              moe_saved_state_bytes that the matching moe_backward reads.
+ * T may be 0 (nothing is enqueued).  T > max_tokens gives MOE_ERR_CAPACITY.
+ */
+MOE_API moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* topk_ids,
+                       const float* topk_scores, const moe_weight* W13, const moe_weight* W2,
+                       void* out, void* saved, uint32_t call_flags, cudaStream_t stream);
+
+/*
+ * Backward of the routed layer ([BLOG] section 2 "SwiGLU backward: the
+ * complete expert path"; [DM] section 05 "Kernel Pipelines": W2 DGRAD and
+ * WGRAD, then SwiGLU backward with row and column grad_h1, then W13 DGRAD and
+ * WGRAD, then the K-reduction of the input gradients):
+ *   saved   the state written by the matching training forward
+ *   dout    bf16 [T, D]   gradient of out (T as in that forward)
+ *   W13,W2  prepared weights including data_t (and scale_t for MXFP8)
+ *   dx      bf16 [T, D]   dx[t] = bf16(sum_k dxr); MOE_ACCUMULATE_DX adds the
+ *                         old dx first
+ *   dW13    [E, 2F, D], dW2 [E, D, F]: BF16, or float with MOE_DW_FP32;
+ *           MOE_DW_ACCUMULATE adds into them.  An expert no active route
+ *           reaches gets exact zeros (or is left as is when accumulating).
+ */
+MOE_API moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout,
+                        const moe_weight* W13, const moe_weight* W2, void* dx, void* dW13,
+                        void* dW2, uint32_t call_flags, cudaStream_t stream);
+
+/* Synchronise the device, return the error word's bits in *bits and clear
+ * it.  Not for use inside graph capture. */
+MOE_API moe_status moe_ctx_get_error(moe_ctx* ctx, uint32_t* bits);
+
+/* Copy `bytes` from device memory to host memory (synchronous).  A helper
+ * for tests that inspect scratch; not part of the hot path. */
+MOE_API moe_status moe_debug_copy_to_host(void* host_dst, const void* dev_src, size_t bytes);
+
+/* Scratch regions of a context, for inspection by tests. */
+typedef enum {
+  MOE_BUF_XROW = 0,        /* gathered x row bundle: bf16 [R_cap, D] or e4m3  */
+  MOE_BUF_XROW_SCALE = 1,  /* e8m0 [R_cap, D/32]                               */
+  MOE_BUF_H2ROW = 2,       /* h2 row bundle: bf16 [R_cap, F] or e4m3           */
+  MOE_BUF_H2ROW_SCALE = 3, /* e8m0 [R_cap, F/32]                               */
+  MOE_BUF_H3 = 4,          /* bf16 [R_cap, D]                                  */
+  MOE_BUF_DH3ROW = 5,      /* bf16 [R_cap, D] or e4m3                          */
+  MOE_BUF_DH3ROW_SCALE = 6,
+  MOE_BUF_DH3COL = 7,      /* bf16 [D, R_cap] or e4m3                          */
+  MOE_BUF_DH3COL_SCALE = 8,/* e8m0 [D, R_cap/32]                               */
+  MOE_BUF_DH1ROW = 9,      /* bf16 [R_cap, 2F] or e4m3                         */
+  MOE_BUF_DH1ROW_SCALE = 10,
+  MOE_BUF_DH1COL = 11,     /* bf16 [2F, R_cap] or e4m3                         */
+  MOE_BUF_DH1COL_SCALE = 12,
+  MOE_BUF_DXR = 13,        /* bf16 [R_cap, D]                                  */
+  MOE_BUF_ROUTING = 14,    /* inference routing state (same layout as saved)   */
+  MOE_BUF_ERROR = 15,      /* uint32 error word                                */
+  MOE_BUF_NUM = 16
+} moe_buffer;
+
+MOE_API moe_status moe_ctx_buffer(moe_ctx* ctx, int which, void** dev_ptr, size_t* bytes);
+
+/*
+ * Stage timing, for measurement.  When enabled, moe_forward and moe_backward
+ * record a CUDA event on their stream before their first launch and after
+ * each stage (inside stream capture the records become event nodes of the
+ * graph, so replays re-time them).  moe_ctx_stage_times waits for the events
+ * of the last forward (pass 0) or backward (pass 1) and returns each stage's
+ * duration in milliseconds:
+ *   forward  (MOE_FWD_STAGES): route, gather x rows, gather x columns
+ *            (training only, else ~0), W13 + SwiGLU GEMM, W2 GEMM, combine
+ *   backward (MOE_BWD_STAGES): gather dh3 rows, gather dh3 columns, W2 DGRAD +
+ *            SwiGLU backward GEMM, W2 WGRAD GEMM, W13 DGRAD GEMM, W13 WGRAD
+ *            GEMM, dX reduction
+ * Enabling creates the events (call it outside capture, after create).
+ */
+#define MOE_FWD_STAGES 6
+#define MOE_BWD_STAGES 7
+MOE_API moe_status moe_ctx_enable_stage_timing(moe_ctx* ctx, int enable);
+MOE_API moe_status moe_ctx_stage_times(moe_ctx* ctx, int pass, float* ms, int n);
+
+/* Number of kernels this context has enqueued so far (host-side count; a
+ * captured call counts once at capture time). */
+MOE_API uint64_t moe_ctx_launch_count(const moe_ctx* ctx);
+
+/* Library version string. */
+MOE_API const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

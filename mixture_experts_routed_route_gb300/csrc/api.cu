@@ -1,0 +1,645 @@
+// C ABI of the MoE layer: context (fixed scratch), saved-state layout,
+// weight preparation, and the forward/backward launch sequences.
+//
+// Forward (one stream, no host synchronisation):
+//   route -> gather x (row bundle; + column bundle when training)
+//   -> W13 GEMM with fused SwiGLU -> W2 GEMM -> combine.
+// Backward:
+//   dh3 gather (row + column bundles) -> W2 DGRAD with fused SwiGLU backward
+//   -> W2 WGRAD -> W13 DGRAD -> W13 WGRAD -> K-reduction of dX.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "kernels.cuh"
+#include "moe_gb300.h"
+
+using namespace moe;
+
+struct moe_ctx {
+  moe_config cfg;
+  int device;
+  int num_sms;
+  int64_t r_cap;
+  int64_t b_cap;
+  uint8_t* base;
+  size_t bytes;
+  void* buf[MOE_BUF_NUM];
+  size_t buf_bytes[MOE_BUF_NUM];
+  uint32_t* err;
+  bool timing;
+  cudaEvent_t ev[2][8];
+  uint64_t launches;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool config_ok(const moe_config* c) {
+  if (!c) return false;
+  if (c->max_tokens < 1 || c->top_k < 1 || c->top_k > 32) return false;
+  if (c->num_experts < 1 || c->num_experts > 1024) return false;
+  if (c->d_model < 128 || c->d_ff < 128) return false;
+  if (c->precision != MOE_BF16 && c->precision != MOE_MXFP8) return false;
+  const int64_t routes = static_cast<int64_t>(c->max_tokens) * c->top_k;
+  if (routes + 31LL * c->num_experts > (1LL << 28)) return false;
+  return true;
+}
+
+bool config_tileable(const moe_config* c) { return c->d_model % 128 == 0 && c->d_ff % 128 == 0; }
+
+int64_t row_cap(const moe_config* c) {
+  const int64_t r = static_cast<int64_t>(c->max_tokens) * c->top_k + 31LL * c->num_experts;
+  return static_cast<int64_t>(align_up(static_cast<size_t>(r), 128)) + 128;  // +128: slack for the last stage
+}
+
+int64_t block_cap(const moe_config* c) {
+  const int64_t r = static_cast<int64_t>(c->max_tokens) * c->top_k + 31LL * c->num_experts;
+  return r / 128 + c->num_experts + 1;
+}
+
+struct SavedLayout {
+  size_t off[MOE_SAVED_NUM_FIELDS];
+  size_t size[MOE_SAVED_NUM_FIELDS];
+  size_t routing_bytes;  // header .. scores
+  size_t total;
+};
+
+SavedLayout saved_layout(const moe_config* c) {
+  SavedLayout L{};
+  const int64_t R = row_cap(c), B = block_cap(c);
+  const int64_t E = c->num_experts, TK = static_cast<int64_t>(c->max_tokens) * c->top_k;
+  const int64_t D = c->d_model, F = c->d_ff;
+  const bool mx = c->precision == MOE_MXFP8;
+  const size_t esz = mx ? 1 : 2;
+  size_t sz[MOE_SAVED_NUM_FIELDS] = {};
+  sz[MOE_SAVED_HEADER] = 16 * sizeof(int);
+  sz[MOE_SAVED_COUNTS] = E * sizeof(int);
+  sz[MOE_SAVED_OFFSETS] = (E + 1) * sizeof(int);
+  sz[MOE_SAVED_POFFSETS] = (E + 1) * sizeof(int);
+  sz[MOE_SAVED_PERM] = R * sizeof(int);
+  sz[MOE_SAVED_INV] = TK * sizeof(int);
+  sz[MOE_SAVED_BLOCKS] = B * 4 * sizeof(int);
+  sz[MOE_SAVED_SCORES] = TK * sizeof(float);
+  sz[MOE_SAVED_H1] = R * 2 * F * 2;
+  sz[MOE_SAVED_XCOL] = D * R * esz;
+  sz[MOE_SAVED_XCOL_SCALE] = mx ? D * (R / 32) + kAlign : 0;
+  sz[MOE_SAVED_H2COL] = F * R * esz;
+  sz[MOE_SAVED_H2COL_SCALE] = mx ? F * (R / 32) + kAlign : 0;
+  size_t off = 0;
+  for (int i = 0; i < MOE_SAVED_NUM_FIELDS; ++i) {
+    L.off[i] = off;
+    L.size[i] = sz[i];
+    off += align_up(sz[i], kAlign);
+    if (i == MOE_SAVED_SCORES) L.routing_bytes = off;
+  }
+  L.total = off;
+  return L;
+}
+
+struct ScratchLayout {
+  size_t off[MOE_BUF_NUM];
+  size_t size[MOE_BUF_NUM];
+  size_t total;
+};
+
+ScratchLayout scratch_layout(const moe_config* c) {
+  ScratchLayout L{};
+  const int64_t R = row_cap(c);
+  const int64_t D = c->d_model, F = c->d_ff;
+  const bool mx = c->precision == MOE_MXFP8;
+  const bool train = (c->flags & MOE_TRAINING) != 0;
+  const size_t esz = mx ? 1 : 2;
+  size_t sz[MOE_BUF_NUM] = {};
+  sz[MOE_BUF_XROW] = R * D * esz;
+  sz[MOE_BUF_XROW_SCALE] = mx ? R * (D / 32) + kAlign : 0;
+  sz[MOE_BUF_H2ROW] = R * F * esz;
+  sz[MOE_BUF_H2ROW_SCALE] = mx ? R * (F / 32) + kAlign : 0;
+  sz[MOE_BUF_H3] = R * D * 2;
+  if (train) {
+    sz[MOE_BUF_DH3ROW] = R * D * esz;
+    sz[MOE_BUF_DH3ROW_SCALE] = mx ? R * (D / 32) + kAlign : 0;
+    sz[MOE_BUF_DH3COL] = D * R * esz;
+    sz[MOE_BUF_DH3COL_SCALE] = mx ? D * (R / 32) + kAlign : 0;
+    sz[MOE_BUF_DH1ROW] = R * 2 * F * esz;
+    sz[MOE_BUF_DH1ROW_SCALE] = mx ? R * (2 * F / 32) + kAlign : 0;
+    sz[MOE_BUF_DH1COL] = 2 * F * R * esz;
+    sz[MOE_BUF_DH1COL_SCALE] = mx ? 2 * F * (R / 32) + kAlign : 0;
+    sz[MOE_BUF_DXR] = R * D * 2;
+  }
+  sz[MOE_BUF_ROUTING] = saved_layout(c).routing_bytes;
+  sz[MOE_BUF_ERROR] = 16;
+  size_t off = 0;
+  for (int i = 0; i < MOE_BUF_NUM; ++i) {
+    L.off[i] = off;
+    L.size[i] = sz[i];
+    off += align_up(sz[i], kAlign);
+  }
+  L.total = off;
+  return L;
+}
+
+RoutingPtrs routing_ptrs(uint8_t* base, const SavedLayout& L) {
+  RoutingPtrs r;
+  r.hdr = reinterpret_cast<int*>(base + L.off[MOE_SAVED_HEADER]);
+  r.counts = reinterpret_cast<int*>(base + L.off[MOE_SAVED_COUNTS]);
+  r.offsets = reinterpret_cast<int*>(base + L.off[MOE_SAVED_OFFSETS]);
+  r.poffsets = reinterpret_cast<int*>(base + L.off[MOE_SAVED_POFFSETS]);
+  r.perm = reinterpret_cast<int*>(base + L.off[MOE_SAVED_PERM]);
+  r.inv = reinterpret_cast<int*>(base + L.off[MOE_SAVED_INV]);
+  r.blocks = reinterpret_cast<int4*>(base + L.off[MOE_SAVED_BLOCKS]);
+  r.scores = reinterpret_cast<float*>(base + L.off[MOE_SAVED_SCORES]);
+  return r;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// ------------------------------------------------------------ tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D operand map over a row-major [rows, cols] matrix; boxes are 128 bytes
+// wide (64 BF16 or 128 E4M3 elements) and `box_rows` tall, 128-byte swizzle.
+bool make_tmap(CUtensorMap* tm, const void* base, bool mx, int64_t rows, int64_t cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int esz = mx ? 1 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esz)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(x)                          \
+  do {                                      \
+    const cudaError_t _e = (x);             \
+    if (_e != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+bool weight_ok(const moe_weight* w, moe_precision prec, int E, int N, int K, bool need_t) {
+  if (!w || w->precision != prec || w->E != E || w->N != N || w->K != K) return false;
+  if (!w->data || !aligned16(w->data)) return false;
+  if (prec == MOE_MXFP8 && (!w->scale || !aligned16(w->scale))) return false;
+  if (need_t) {
+    if (!w->data_t || !aligned16(w->data_t)) return false;
+    if (prec == MOE_MXFP8 && (!w->scale_t || !aligned16(w->scale_t))) return false;
+  }
+  return true;
+}
+
+uint8_t* B(moe_ctx* c, int which) { return static_cast<uint8_t*>(c->buf[which]); }
+
+// Record stage event `idx` of `pass` (0 forward, 1 backward) when timing is on.
+cudaError_t stage_mark(moe_ctx* c, int pass, int idx, cudaStream_t s) {
+  if (!c->timing) return cudaSuccess;
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &st);
+  if (e != cudaSuccess) return e;
+  if (st == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(c->ev[pass][idx], s, cudaEventRecordExternal);
+  return cudaEventRecord(c->ev[pass][idx], s);
+}
+
+}  // namespace
+
+// =================================================================== ABI
+
+extern "C" {
+
+const char* moe_version(void) { return "moe_gb300 0.1 (sm_103a)"; }
+
+int64_t moe_row_capacity(const moe_config* cfg) { return config_ok(cfg) ? row_cap(cfg) : 0; }
+
+size_t moe_saved_state_bytes(const moe_config* cfg) { return config_ok(cfg) ? saved_layout(cfg).total : 0; }
+
+moe_status moe_saved_state_field(const moe_config* cfg, int field, size_t* offset, size_t* bytes) {
+  if (!config_ok(cfg) || field < 0 || field >= MOE_SAVED_NUM_FIELDS || !offset || !bytes)
+    return MOE_ERR_INVALID_ARG;
+  const SavedLayout L = saved_layout(cfg);
+  *offset = L.off[field];
+  *bytes = L.size[field];
+  return MOE_OK;
+}
+
+size_t moe_ctx_scratch_bytes(const moe_config* cfg) { return config_ok(cfg) ? scratch_layout(cfg).total : 0; }
+
+moe_status moe_ctx_create(const moe_config* cfg, moe_ctx** out) {
+  if (!out || !config_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  if (!config_tileable(cfg)) return MOE_ERR_UNSUPPORTED;
+  if (!encode_fn()) return MOE_ERR_CUDA;
+  moe_ctx* c = new moe_ctx();
+  c->cfg = *cfg;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return MOE_ERR_CUDA;
+  }
+  c->r_cap = row_cap(cfg);
+  c->b_cap = block_cap(cfg);
+  const ScratchLayout L = scratch_layout(cfg);
+  c->bytes = L.total;
+  if (cudaMalloc(&c->base, c->bytes) != cudaSuccess) {
+    delete c;
+    return MOE_ERR_CUDA;
+  }
+  if (cudaMemset(c->base, 0, c->bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(c->base);
+    delete c;
+    return MOE_ERR_CUDA;
+  }
+  for (int i = 0; i < MOE_BUF_NUM; ++i) {
+    c->buf[i] = L.size[i] ? c->base + L.off[i] : nullptr;
+    c->buf_bytes[i] = L.size[i];
+  }
+  c->err = reinterpret_cast<uint32_t*>(c->buf[MOE_BUF_ERROR]);
+  *out = c;
+  return MOE_OK;
+}
+
+moe_status moe_ctx_enable_stage_timing(moe_ctx* ctx, int enable) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (enable && !ctx->timing) {
+    for (int p = 0; p < 2; ++p)
+      for (int i = 0; i < 8; ++i) MOE_TRY(cudaEventCreate(&ctx->ev[p][i]));
+    ctx->timing = true;
+  } else if (!enable && ctx->timing) {
+    for (int p = 0; p < 2; ++p)
+      for (int i = 0; i < 8; ++i) cudaEventDestroy(ctx->ev[p][i]);
+    ctx->timing = false;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_ctx_stage_times(moe_ctx* ctx, int pass, float* ms, int n) {
+  if (!ctx || !ms || pass < 0 || pass > 1 || !ctx->timing) return MOE_ERR_INVALID_ARG;
+  const int stages = pass == 0 ? MOE_FWD_STAGES : MOE_BWD_STAGES;
+  if (n < stages) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(cudaEventSynchronize(ctx->ev[pass][stages]));
+  for (int i = 0; i < stages; ++i) MOE_TRY(cudaEventElapsedTime(&ms[i], ctx->ev[pass][i], ctx->ev[pass][i + 1]));
+  return MOE_OK;
+}
+
+uint64_t moe_ctx_launch_count(const moe_ctx* ctx) { return ctx ? ctx->launches : 0; }
+
+moe_status moe_ctx_destroy(moe_ctx* ctx) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  moe_ctx_enable_stage_timing(ctx, 0);
+  const cudaError_t e = cudaFree(ctx->base);
+  delete ctx;
+  return cuda_status(e);
+}
+
+moe_status moe_ctx_buffer(moe_ctx* ctx, int which, void** dev_ptr, size_t* bytes) {
+  if (!ctx || which < 0 || which >= MOE_BUF_NUM || !dev_ptr || !bytes) return MOE_ERR_INVALID_ARG;
+  *dev_ptr = ctx->buf[which];
+  *bytes = ctx->buf_bytes[which];
+  return MOE_OK;
+}
+
+moe_status moe_ctx_get_error(moe_ctx* ctx, uint32_t* bits) {
+  if (!ctx || !bits) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(cudaDeviceSynchronize());
+  MOE_TRY(cudaMemcpy(bits, ctx->err, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  MOE_TRY(cudaMemset(ctx->err, 0, sizeof(uint32_t)));
+  MOE_TRY(cudaDeviceSynchronize());
+  return MOE_OK;
+}
+
+moe_status moe_debug_copy_to_host(void* host_dst, const void* dev_src, size_t bytes) {
+  if (!host_dst || !dev_src) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(cudaDeviceSynchronize());
+  MOE_TRY(cudaMemcpy(host_dst, dev_src, bytes, cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+moe_status prepare_block_scaled_weight(const void* w, int32_t E, int32_t N, int32_t K, moe_precision precision,
+                                       void* data, uint8_t* scale, void* data_t, uint8_t* scale_t,
+                                       cudaStream_t stream) {
+  if (!w || !aligned16(w) || E < 1 || N < 32 || K < 32 || N % 32 || K % 32) return MOE_ERR_INVALID_ARG;
+  if (precision == MOE_MXFP8) {
+    if (!data || !scale || !aligned16(data)) return MOE_ERR_INVALID_ARG;
+    if ((data_t == nullptr) != (scale_t == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (data_t && !aligned16(data_t)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_prep_mx_weight(w, E, N, K, static_cast<uint8_t*>(data), scale,
+                                             static_cast<uint8_t*>(data_t), scale_t, stream));
+  }
+  if (precision == MOE_BF16) {
+    if (data || scale || scale_t || !data_t || !aligned16(data_t)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_transpose_bf16(w, E, N, K, data_t, stream));
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* topk_ids, const float* topk_scores,
+                       const moe_weight* W13, const moe_weight* W2, void* out, void* saved, uint32_t call_flags,
+                       cudaStream_t stream) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  const moe_config& c = ctx->cfg;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > c.max_tokens) return MOE_ERR_CAPACITY;
+  const int D = c.d_model, F = c.d_ff, E = c.num_experts, K = c.top_k;
+  const bool mx = c.precision == MOE_MXFP8;
+  const bool train = saved != nullptr;
+  if (train && !(c.flags & MOE_TRAINING)) return MOE_ERR_INVALID_ARG;
+  if (!weight_ok(W13, c.precision, E, 2 * F, D, false) || !weight_ok(W2, c.precision, E, D, F, false))
+    return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !topk_ids || !topk_scores || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || (saved && !aligned16(saved))) return MOE_ERR_INVALID_ARG;
+  if (call_flags & ~MOE_ACCUMULATE_OUT) return MOE_ERR_INVALID_ARG;
+
+  const SavedLayout SL = saved_layout(&c);
+  uint8_t* sv = static_cast<uint8_t*>(saved);
+  const RoutingPtrs rp = routing_ptrs(train ? sv : B(ctx, MOE_BUF_ROUTING), SL);
+  const int64_t R = ctx->r_cap;
+  const int sms = ctx->num_sms;
+
+  MOE_TRY(stage_mark(ctx, 0, 0, stream));
+  MOE_TRY(launch_route(topk_ids, topk_scores, T, K, E, static_cast<int>(R), (c.flags & MOE_DEBUG_CHECKS) ? 1 : 0,
+                       rp, ctx->err, stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 0, 1, stream));
+  MOE_TRY(launch_gather_rows(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
+                             static_cast<int>(R), sms, stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 0, 2, stream));
+  if (train) {
+    MOE_TRY(launch_gather_cols(mx, false, x, D, K, rp, sv + SL.off[MOE_SAVED_XCOL],
+                               mx ? sv + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr, static_cast<int>(R), stream));
+    ctx->launches += 1;
+  }
+  MOE_TRY(stage_mark(ctx, 0, 3, stream));
+
+  // ---- W13 + SwiGLU
+  GemmLaunch g1{};
+  g1.mx = mx;
+  g1.na = 2;
+  g1.epi = kEpiSwigluFwd;
+  g1.mode = kGroupedM;
+  if (!make_tmap(&g1.tmA, W13->data, mx, static_cast<int64_t>(E) * 2 * F, D, 128) ||
+      !make_tmap(&g1.tmB, B(ctx, MOE_BUF_XROW), mx, R, D, 32))
+    return MOE_ERR_CUDA;
+  GemmParams& p1 = g1.p;
+  p1.hdr = rp.hdr;
+  p1.blocks = rp.blocks;
+  p1.poffsets = rp.poffsets;
+  p1.E = E;
+  p1.n_tiles = F / 128;
+  p1.K = D;
+  p1.a_rows_per_expert = 2 * F;
+  p1.a_up_offset = F;
+  p1.sfa = W13->scale;
+  p1.sfa_pitch = D / 32;
+  p1.sfb = B(ctx, MOE_BUF_XROW_SCALE);
+  p1.sfb_pitch = D / 32;
+  p1.out0 = B(ctx, MOE_BUF_H2ROW);
+  p1.out0_pitch = F;
+  p1.out0_sf = B(ctx, MOE_BUF_H2ROW_SCALE);
+  p1.out0_sf_pitch = F / 32;
+  if (train) {
+    p1.out1 = sv + SL.off[MOE_SAVED_H2COL];
+    p1.out1_pitch = R;
+    p1.out1_sf = mx ? sv + SL.off[MOE_SAVED_H2COL_SCALE] : nullptr;
+    p1.out1_sf_pitch = R / 32;
+    p1.h1 = reinterpret_cast<__nv_bfloat16*>(sv + SL.off[MOE_SAVED_H1]);
+    p1.h1_pitch = 2 * F;
+  }
+  p1.F = F;
+  p1.save_h1 = train ? 1 : 0;
+  p1.want_col = train ? 1 : 0;
+  p1.err = ctx->err;
+  g1.max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
+  MOE_TRY(launch_gemm(g1, sms, stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 0, 4, stream));
+
+  // ---- W2
+  GemmLaunch g2{};
+  g2.mx = mx;
+  g2.na = 1;
+  g2.epi = kEpiStore;
+  g2.mode = kGroupedM;
+  if (!make_tmap(&g2.tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128) ||
+      !make_tmap(&g2.tmB, B(ctx, MOE_BUF_H2ROW), mx, R, F, 32))
+    return MOE_ERR_CUDA;
+  GemmParams& p2 = g2.p;
+  p2.hdr = rp.hdr;
+  p2.blocks = rp.blocks;
+  p2.poffsets = rp.poffsets;
+  p2.E = E;
+  p2.n_tiles = D / 128;
+  p2.K = F;
+  p2.a_rows_per_expert = D;
+  p2.sfa = W2->scale;
+  p2.sfa_pitch = F / 32;
+  p2.sfb = B(ctx, MOE_BUF_H2ROW_SCALE);
+  p2.sfb_pitch = F / 32;
+  p2.out0 = B(ctx, MOE_BUF_H3);
+  p2.out0_pitch = D;
+  p2.F = F;
+  p2.err = ctx->err;
+  g2.max_tiles = static_cast<int>(ctx->b_cap * (D / 128));
+  MOE_TRY(launch_gemm(g2, sms, stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 0, 5, stream));
+
+  // ---- combine
+  MOE_TRY(launch_combine(B(ctx, MOE_BUF_H3), D, K, rp.inv, rp.scores, out, T,
+                         (call_flags & MOE_ACCUMULATE_OUT) != 0, sms, stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 0, 6, stream));
+  return MOE_OK;
+}
+
+moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const moe_weight* W13,
+                        const moe_weight* W2, void* dx, void* dW13, void* dW2, uint32_t call_flags,
+                        cudaStream_t stream) {
+  if (!ctx || !saved || !dout || !dx || !dW13 || !dW2) return MOE_ERR_INVALID_ARG;
+  const moe_config& c = ctx->cfg;
+  if (!(c.flags & MOE_TRAINING)) return MOE_ERR_INVALID_ARG;
+  const int D = c.d_model, F = c.d_ff, E = c.num_experts, K = c.top_k;
+  const bool mx = c.precision == MOE_MXFP8;
+  if (!weight_ok(W13, c.precision, E, 2 * F, D, true) || !weight_ok(W2, c.precision, E, D, F, true))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(saved) || !aligned16(dout) || !aligned16(dx) || !aligned16(dW13) || !aligned16(dW2))
+    return MOE_ERR_INVALID_ARG;
+  if (call_flags & ~(MOE_ACCUMULATE_DX | MOE_DW_FP32 | MOE_DW_ACCUMULATE)) return MOE_ERR_INVALID_ARG;
+
+  const SavedLayout SL = saved_layout(&c);
+  uint8_t* sv = static_cast<uint8_t*>(const_cast<void*>(saved));
+  const RoutingPtrs rp = routing_ptrs(sv, SL);
+  const int64_t R = ctx->r_cap;
+  const int sms = ctx->num_sms;
+  const int dw_fp32 = (call_flags & MOE_DW_FP32) ? 1 : 0;
+  const int dw_acc = (call_flags & MOE_DW_ACCUMULATE) ? 1 : 0;
+
+  // ---- dh3 = s * dY: row bundle (W2 DGRAD) and column bundle (W2 WGRAD)
+  MOE_TRY(stage_mark(ctx, 1, 0, stream));
+  MOE_TRY(launch_gather_rows(mx, true, dout, D, K, rp, B(ctx, MOE_BUF_DH3ROW), B(ctx, MOE_BUF_DH3ROW_SCALE),
+                             static_cast<int>(R), sms, stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 1, 1, stream));
+  MOE_TRY(launch_gather_cols(mx, true, dout, D, K, rp, B(ctx, MOE_BUF_DH3COL), B(ctx, MOE_BUF_DH3COL_SCALE),
+                             static_cast<int>(R), stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 1, 2, stream));
+
+  // ---- W2 DGRAD + SwiGLU backward -> dh1 row and column bundles
+  GemmLaunch g1{};
+  g1.mx = mx;
+  g1.na = 1;
+  g1.epi = kEpiSwigluBwd;
+  g1.mode = kGroupedM;
+  if (!make_tmap(&g1.tmA, W2->data_t, mx, static_cast<int64_t>(E) * F, D, 128) ||
+      !make_tmap(&g1.tmB, B(ctx, MOE_BUF_DH3ROW), mx, R, D, 32))
+    return MOE_ERR_CUDA;
+  GemmParams& p1 = g1.p;
+  p1.hdr = rp.hdr;
+  p1.blocks = rp.blocks;
+  p1.poffsets = rp.poffsets;
+  p1.E = E;
+  p1.n_tiles = F / 128;
+  p1.K = D;
+  p1.a_rows_per_expert = F;
+  p1.sfa = W2->scale_t;
+  p1.sfa_pitch = D / 32;
+  p1.sfb = B(ctx, MOE_BUF_DH3ROW_SCALE);
+  p1.sfb_pitch = D / 32;
+  p1.h1 = reinterpret_cast<__nv_bfloat16*>(sv + SL.off[MOE_SAVED_H1]);
+  p1.h1_pitch = 2 * F;
+  p1.out0 = B(ctx, MOE_BUF_DH1ROW);
+  p1.out0_pitch = 2 * F;
+  p1.out0_sf = B(ctx, MOE_BUF_DH1ROW_SCALE);
+  p1.out0_sf_pitch = 2 * F / 32;
+  p1.out1 = B(ctx, MOE_BUF_DH1COL);
+  p1.out1_pitch = R;
+  p1.out1_sf = B(ctx, MOE_BUF_DH1COL_SCALE);
+  p1.out1_sf_pitch = R / 32;
+  p1.F = F;
+  p1.err = ctx->err;
+  g1.max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
+  MOE_TRY(launch_gemm(g1, sms, stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 1, 3, stream));
+
+  // ---- W2 WGRAD: dW2[e] = dh3_e^T h2_e   ([D, F] per expert)
+  GemmLaunch g2{};
+  g2.mx = mx;
+  g2.na = 1;
+  g2.epi = kEpiWgrad;
+  g2.mode = kGroupedK;
+  if (!make_tmap(&g2.tmA, B(ctx, MOE_BUF_DH3COL), mx, D, R, 128) ||
+      !make_tmap(&g2.tmB, sv + SL.off[MOE_SAVED_H2COL], mx, F, R, 32))
+    return MOE_ERR_CUDA;
+  GemmParams& p2 = g2.p;
+  p2.hdr = rp.hdr;
+  p2.blocks = rp.blocks;
+  p2.poffsets = rp.poffsets;
+  p2.E = E;
+  p2.m_tiles = D / 128;
+  p2.n_tiles = F / 128;
+  p2.sfa = B(ctx, MOE_BUF_DH3COL_SCALE);
+  p2.sfa_pitch = R / 32;
+  p2.sfb = mx ? sv + SL.off[MOE_SAVED_H2COL_SCALE] : nullptr;
+  p2.sfb_pitch = R / 32;
+  p2.out0 = dW2;
+  p2.out0_pitch = F;
+  p2.dw_fp32 = dw_fp32;
+  p2.dw_accum = dw_acc;
+  p2.err = ctx->err;
+  g2.max_tiles = E * (D / 128) * (F / 128);
+  MOE_TRY(launch_gemm(g2, sms, stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 1, 4, stream));
+
+  // ---- W13 DGRAD: dxr = dh1 W13[e]
+  GemmLaunch g3{};
+  g3.mx = mx;
+  g3.na = 1;
+  g3.epi = kEpiStore;
+  g3.mode = kGroupedM;
+  if (!make_tmap(&g3.tmA, W13->data_t, mx, static_cast<int64_t>(E) * D, 2 * F, 128) ||
+      !make_tmap(&g3.tmB, B(ctx, MOE_BUF_DH1ROW), mx, R, 2 * F, 32))
+    return MOE_ERR_CUDA;
+  GemmParams& p3 = g3.p;
+  p3.hdr = rp.hdr;
+  p3.blocks = rp.blocks;
+  p3.poffsets = rp.poffsets;
+  p3.E = E;
+  p3.n_tiles = D / 128;
+  p3.K = 2 * F;
+  p3.a_rows_per_expert = D;
+  p3.sfa = W13->scale_t;
+  p3.sfa_pitch = 2 * F / 32;
+  p3.sfb = B(ctx, MOE_BUF_DH1ROW_SCALE);
+  p3.sfb_pitch = 2 * F / 32;
+  p3.out0 = B(ctx, MOE_BUF_DXR);
+  p3.out0_pitch = D;
+  p3.F = F;
+  p3.err = ctx->err;
+  g3.max_tiles = static_cast<int>(ctx->b_cap * (D / 128));
+  MOE_TRY(launch_gemm(g3, sms, stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 1, 5, stream));
+
+  // ---- W13 WGRAD: dW13[e] = dh1_e^T x_e   ([2F, D] per expert)
+  GemmLaunch g4{};
+  g4.mx = mx;
+  g4.na = 1;
+  g4.epi = kEpiWgrad;
+  g4.mode = kGroupedK;
+  if (!make_tmap(&g4.tmA, B(ctx, MOE_BUF_DH1COL), mx, 2 * F, R, 128) ||
+      !make_tmap(&g4.tmB, sv + SL.off[MOE_SAVED_XCOL], mx, D, R, 32))
+    return MOE_ERR_CUDA;
+  GemmParams& p4 = g4.p;
+  p4.hdr = rp.hdr;
+  p4.blocks = rp.blocks;
+  p4.poffsets = rp.poffsets;
+  p4.E = E;
+  p4.m_tiles = 2 * F / 128;
+  p4.n_tiles = D / 128;
+  p4.sfa = B(ctx, MOE_BUF_DH1COL_SCALE);
+  p4.sfa_pitch = R / 32;
+  p4.sfb = mx ? sv + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr;
+  p4.sfb_pitch = R / 32;
+  p4.out0 = dW13;
+  p4.out0_pitch = D;
+  p4.dw_fp32 = dw_fp32;
+  p4.dw_accum = dw_acc;
+  p4.err = ctx->err;
+  g4.max_tiles = E * (2 * F / 128) * (D / 128);
+  MOE_TRY(launch_gemm(g4, sms, stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 1, 6, stream));
+
+  // ---- dX[t] = sum_k dxr(t,k)
+  MOE_TRY(launch_combine(B(ctx, MOE_BUF_DXR), D, K, rp.inv, nullptr, dx, c.max_tokens,
+                         (call_flags & MOE_ACCUMULATE_DX) != 0, sms, stream, rp.hdr));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 1, 7, stream));
+  return MOE_OK;
+}
+
+}  // extern "C"

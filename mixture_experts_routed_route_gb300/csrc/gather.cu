@@ -1,0 +1,200 @@
+// F1 / B0: gather token rows into expert-major order, optionally scaled by
+// the route's score, as BF16 or as MXFP8 (E4M3 + one E8M0 scale per 32
+// values).
+//
+// Dist-MoE explainer section 02, "Quantization Axes for Forward and
+// Backward": FPROP/DGRAD operands are scaled along the feature axis (row
+// bundles, launch_gather_rows); WGRAD contracts over token rows and needs a
+// separately quantised column-oriented bundle (launch_gather_cols, stored
+// transposed [D, r_cap] so the GEMM reads it K-major).  MXFP8 training
+// quantises after the gather ("MXFP8 training publishes BF16 source rows and
+// quantizes after peer gather"); row quantisation depends only on the row,
+// so quantising after the gather is exact.  Pad rows (route -1) are zero.
+//
+// The dh3 prep of the backward ("Mixture of Experts: How Routing Becomes GPU
+// Computation", section 2, "SwiGLU backward: the complete expert path":
+// dH = p * dY) is the same gather with use_scores: the FP32 product of the
+// score and the BF16 dY is what gets rounded or quantised.
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&v)[8]) {
+  v[0] = bf16_lo(u.x);
+  v[1] = bf16_hi(u.x);
+  v[2] = bf16_lo(u.y);
+  v[3] = bf16_hi(u.y);
+  v[4] = bf16_lo(u.z);
+  v[5] = bf16_hi(u.z);
+  v[6] = bf16_lo(u.w);
+  v[7] = bf16_hi(u.w);
+}
+
+// One warp per row; each lane moves 8 values (16 bytes) per step, 4 lanes
+// cover one 32-value MX block.
+template <bool MX, bool SCALE>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ src, int D, int K,
+                                                          const int* __restrict__ hdr, const int* __restrict__ perm,
+                                                          const float* __restrict__ scores, void* __restrict__ dst,
+                                                          uint8_t* __restrict__ dst_sf) {
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  const int rows = hdr[2];
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+    const int route = perm[r];
+    const __nv_bfloat16* srow = nullptr;
+    float s = 1.0f;
+    if (route >= 0) {
+      srow = src + static_cast<long long>(route / K) * D;
+      if (SCALE) s = scores[route];
+    }
+    for (int base = 0; base < D; base += 256) {
+      const int c = base + lane * 8;
+      const bool act = c < D;
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (act && srow) u = __ldg(reinterpret_cast<const uint4*>(srow + c));
+      if (!MX) {
+        if (SCALE) {
+          float v[8];
+          unpack8(u, v);
+          u.x = pack_bf16x2(s * v[0], s * v[1]);
+          u.y = pack_bf16x2(s * v[2], s * v[3]);
+          u.z = pack_bf16x2(s * v[4], s * v[5]);
+          u.w = pack_bf16x2(s * v[6], s * v[7]);
+        }
+        if (act) *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + static_cast<long long>(r) * D + c) = u;
+      } else {
+        float v[8];
+        unpack8(u, v);
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (SCALE) v[j] = s * v[j];
+          amax = fmaxf(amax, fabsf(v[j]));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        const int e = mx_shared_exp(amax);
+        const float inv = exp2_int(-e);
+        uint2 q;
+        q.x = cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
+        q.y = cvt_e4m3x2(v[4] * inv, v[5] * inv) | (cvt_e4m3x2(v[6] * inv, v[7] * inv) << 16);
+        if (act) {
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(dst) + static_cast<long long>(r) * D + c) = q;
+          if ((lane & 3) == 0) dst_sf[static_cast<long long>(r) * (D / 32) + c / 32] = static_cast<uint8_t>(e + 127);
+        }
+      }
+    }
+  }
+}
+
+// One CTA per (32-row group, 256-column slab): load the 32 gathered rows
+// into shared memory, then each thread owns one column d and writes its 32
+// row values contiguously to dstT[d][r0 .. r0+31] (one MX block along rows).
+template <bool MX, bool SCALE>
+__global__ void __launch_bounds__(256) gather_cols_kernel(const __nv_bfloat16* __restrict__ src, int D, int K,
+                                                          const int* __restrict__ hdr, const int* __restrict__ perm,
+                                                          const float* __restrict__ scores, void* __restrict__ dstT,
+                                                          uint8_t* __restrict__ dstT_sf, int r_cap) {
+  __shared__ float tile[32][257];
+  const int rows = hdr[2];
+  const int c0 = blockIdx.x * 256;
+  const int tid = threadIdx.x;
+  for (int rg = blockIdx.y; rg * 32 < rows; rg += gridDim.y) {
+    const int r0 = rg * 32;
+    for (int i = tid; i < 32 * 32; i += 256) {
+      const int row = i >> 5, chunk = i & 31;
+      const int c = c0 + chunk * 8;
+      float v[8];
+      const int route = perm[r0 + row];
+      if (route >= 0 && c < D) {
+        unpack8(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(route / K) * D + c)), v);
+        if (SCALE) {
+          const float s = scores[route];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = s * v[j];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tile[row][chunk * 8 + j] = v[j];
+    }
+    __syncthreads();
+    const int d = c0 + tid;
+    if (d < D) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = tile[i][tid];
+      if (!MX) {
+        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dstT) + static_cast<long long>(d) * r_cap + r0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          o[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+      } else {
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const int e = mx_shared_exp(amax);
+        const float inv = exp2_int(-e);
+        uint32_t w[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
+        uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dstT) + static_cast<long long>(d) * r_cap + r0);
+        o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        dstT_sf[static_cast<long long>(d) * (r_cap / 32) + rg] = static_cast<uint8_t>(e + 127);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <bool MX, bool SCALE>
+cudaError_t rows_impl(const void* src, int D, int K, const RoutingPtrs& rp, void* dst, uint8_t* dst_sf, int r_cap,
+                      int num_sms, cudaStream_t stream) {
+  const int warps_needed = r_cap;
+  int blocks = (warps_needed + 7) / 8;
+  blocks = min(blocks, num_sms * 8);
+  gather_rows_kernel<MX, SCALE><<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr,
+                                                            rp.perm, rp.scores, dst, dst_sf);
+  return cudaGetLastError();
+}
+
+template <bool MX, bool SCALE>
+cudaError_t cols_impl(const void* src, int D, int K, const RoutingPtrs& rp, void* dstT, uint8_t* dstT_sf, int r_cap,
+                      cudaStream_t stream) {
+  dim3 grid((D + 255) / 256, r_cap / 32);
+  gather_cols_kernel<MX, SCALE><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr,
+                                                          rp.perm, rp.scores, dstT, dstT_sf, r_cap);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gather_rows(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
+                               void* dst, uint8_t* dst_sf, int r_cap, int num_sms, cudaStream_t stream) {
+  if (mx) {
+    return use_scores ? rows_impl<true, true>(src, D, K, rp, dst, dst_sf, r_cap, num_sms, stream)
+                      : rows_impl<true, false>(src, D, K, rp, dst, dst_sf, r_cap, num_sms, stream);
+  }
+  return use_scores ? rows_impl<false, true>(src, D, K, rp, dst, dst_sf, r_cap, num_sms, stream)
+                    : rows_impl<false, false>(src, D, K, rp, dst, dst_sf, r_cap, num_sms, stream);
+}
+
+cudaError_t launch_gather_cols(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
+                               void* dstT, uint8_t* dstT_sf, int r_cap, cudaStream_t stream) {
+  if (mx) {
+    return use_scores ? cols_impl<true, true>(src, D, K, rp, dstT, dstT_sf, r_cap, stream)
+                      : cols_impl<true, false>(src, D, K, rp, dstT, dstT_sf, r_cap, stream);
+  }
+  return use_scores ? cols_impl<false, true>(src, D, K, rp, dstT, dstT_sf, r_cap, stream)
+                    : cols_impl<false, false>(src, D, K, rp, dstT, dstT_sf, r_cap, stream);
+}
+
+}  // namespace moe

@@ -1,0 +1,530 @@
+// Grouped GEMMs of the MoE layer on the 5th-generation tensor cores
+// (tcgen05.mma, FP32 accumulators in tensor memory, operands staged by TMA).
+//
+// "Mixture of Experts: How Routing Becomes GPU Computation", section 2,
+// "Grouped GEMM": each expert e computes C_e = A_e B_e^T over its own ragged
+// row range, with weights stacked [E, N, K]; "Grouped GEMM backward":
+// dA_e = dC_e B_e and dB_e = dC_e^T A_e.  Dist-MoE explainer section 05,
+// "GPU Kernels: Tiles and Warp Roles": a persistent scheduler hands each CTA
+// an expert's row/output tile, TMA stages operand tiles into shared memory,
+// MMA accumulates in FP32 tensor memory, and an epilogue drains it; tails are
+// masked.
+//
+// Two ways of walking the experts:
+//  * grouped-M (forward W13 and W2, input-gradient DGRAD): the weight is the
+//    A operand (128 output features per tile, M = 128) and the expert's token
+//    rows are the B operand (N = the row block's 32..128 rows).  Experts get
+//    only ~32 rows at the 384-expert shape, so putting weights on the
+//    128-wide M side keeps the MMA from computing padding and reads each
+//    weight tile once per row block.
+//  * grouped-K (WGRAD): dW_e[m, n] = sum over the expert's rows of
+//    colA[m, r] colB[n, r]; both operands are column bundles stored
+//    [features, rows], so the contraction runs over the expert's row range.
+//
+// Epilogues: fused SwiGLU forward (h1 -> h2 row/column bundles), plain BF16
+// store (h3, input-gradient rows), fused SwiGLU backward (dh2 -> dh1 row and
+// column bundles) and weight-gradient store (BF16/FP32, optional add).
+//
+// Warp roles (one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer (one thread)
+//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warps 2-5   epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
+//   warps 6-9   MXFP8 only: load the E8M0 scales of each stage and write
+//               them to tensor memory with tcgen05.st
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kABytes = 128 * 128;  // one 128-row x 128-byte operand tile
+constexpr int kBBytes = 128 * 128;
+
+struct Tile {
+  int e;
+  int a_row[2];
+  int b_row0;
+  int b_rows;    // rows of B = MMA N
+  int k0;        // first contraction element
+  int kstages;
+  int klast;     // contraction elements of the last stage
+  int out_row0;
+  int out_col0;
+};
+
+template <int MODE, int BK>
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int nblk) {
+  Tile t;
+  if (MODE == kGroupedM) {
+    const int n = tile / nblk, b = tile - n * nblk;
+    const int4 blk = p.blocks[b];
+    t.e = blk.x;
+    t.a_row[0] = blk.x * p.a_rows_per_expert + n * 128;
+    t.a_row[1] = t.a_row[0] + p.a_up_offset;
+    t.b_row0 = blk.y;
+    t.b_rows = blk.z;
+    t.k0 = 0;
+    t.kstages = p.K / BK;
+    t.klast = BK;
+    t.out_row0 = blk.y;
+    t.out_col0 = n * 128;
+  } else {
+    const int per_e = p.m_tiles * p.n_tiles;
+    const int e = tile / per_e, rem = tile - e * per_e;
+    const int m = rem / p.n_tiles, n = rem - m * p.n_tiles;
+    const int k0 = p.poffsets[e], klen = p.poffsets[e + 1] - k0;
+    t.e = e;
+    t.a_row[0] = m * 128;
+    t.a_row[1] = 0;
+    t.b_row0 = n * 128;
+    t.b_rows = 128;
+    t.k0 = k0;
+    t.kstages = (klen + BK - 1) / BK;
+    t.klast = klen - (t.kstages - 1) * BK;
+    t.out_row0 = m * 128;
+    t.out_col0 = n * 128;
+  }
+  return t;
+}
+
+// Four consecutive scale bytes starting at any byte address, little-endian.
+__device__ __forceinline__ uint32_t load_sf4(const uint8_t* ptr) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~static_cast<uintptr_t>(3));
+  const uint32_t sh = static_cast<uint32_t>(a & 3) * 8;
+  const uint32_t lo = __ldg(w);
+  if (sh == 0) return lo;
+  return __funnelshift_r(lo, __ldg(w + 1), sh);
+}
+
+// A final bounded wait that ignores the abort flag (used only to drain work
+// already in flight before the CTA releases its resources).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitTimeoutCycles / 8) return;
+  }
+}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// ------------------------------------------------------------- epilogues
+
+// h3 / input-gradient rows: out[row][feature] = bf16(acc).
+__device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow) {
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0);
+  const int f = t.out_col0 + lrow;
+  for (int c0 = 0; c0 < t.b_rows; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(tbase + c0, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      out[static_cast<long long>(t.out_row0 + c0 + i) * p.out0_pitch + f] = __float2bfloat16_rn(u2f(v[i]));
+  }
+}
+
+// Row bundle of one 32-feature block held across the warp's lanes (MXFP8:
+// the block's amax is a warp reduction), and column bundle of 32 rows held
+// in one thread's registers.
+template <bool MX>
+__device__ __forceinline__ void store_row_val(const GemmParams& p, void* out, uint8_t* out_sf, long long pitch,
+                                              long long sf_pitch, long long row, int col, float v, int lane) {
+  if (!MX) {
+    static_cast<__nv_bfloat16*>(out)[row * pitch + col] = __float2bfloat16_rn(v);
+  } else {
+    const float amax = warp_max(fabsf(v));
+    const int e = mx_shared_exp(amax);
+    const uint32_t code = cvt_e4m3x2(v * exp2_int(-e), 0.0f) & 0xFFu;
+    static_cast<uint8_t*>(out)[row * pitch + col] = static_cast<uint8_t>(code);
+    if (lane == 0) out_sf[row * sf_pitch + col / 32] = static_cast<uint8_t>(e + 127);
+  }
+}
+
+template <bool MX>
+__device__ __forceinline__ void store_col32(void* outT, uint8_t* outT_sf, long long pitch, long long sf_pitch,
+                                            long long feat, long long row0, const float (&v)[32]) {
+  if (!MX) {
+    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(outT) + feat * pitch + row0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      o[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                        pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+  } else {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int e = mx_shared_exp(amax);
+    const float inv = exp2_int(-e);
+    uint32_t w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
+    uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(outT) + feat * pitch + row0);
+    o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    outT_sf[feat * sf_pitch + row0 / 32] = static_cast<uint8_t>(e + 127);
+  }
+}
+
+// Fused SwiGLU forward: g, u from the two accumulators, rounded to BF16
+// (the stored h1), h2 = SiLU(g) * u in FP32, then the h2 row bundle (W2's
+// operand) and, for training, the h2 column bundle (W2 WGRAD's operand).
+template <bool MX>
+__device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow,
+                                               int lane) {
+  const int f = t.out_col0 + lrow;
+  for (int c0 = 0; c0 < t.b_rows; c0 += 32) {
+    uint32_t vg[32], vu[32];
+    tmem_ld32(tbase + c0, vg);
+    tmem_ld32(tbase + 128 + c0, vu);
+    tmem_ld_wait();
+    float h[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const long long row = t.out_row0 + c0 + i;
+      const __nv_bfloat16 gb = __float2bfloat16_rn(u2f(vg[i]));
+      const __nv_bfloat16 ub = __float2bfloat16_rn(u2f(vu[i]));
+      if (p.save_h1) {
+        p.h1[row * p.h1_pitch + f] = gb;
+        p.h1[row * p.h1_pitch + p.F + f] = ub;
+      }
+      const float g = __bfloat162float(gb), u = __bfloat162float(ub);
+      h[i] = silu_f(g) * u;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      store_row_val<MX>(p, p.out0, p.out0_sf, p.out0_pitch, p.out0_sf_pitch, t.out_row0 + c0 + i, f, h[i], lane);
+    if (p.want_col) store_col32<MX>(p.out1, p.out1_sf, p.out1_pitch, p.out1_sf_pitch, f, t.out_row0 + c0, h);
+  }
+}
+
+// Fused SwiGLU backward: dh2 from the accumulator (W2 DGRAD), g and u from
+// the saved BF16 h1, dg = dh2 u SiLU'(g), du = dh2 SiLU(g), written as the
+// dh1 row bundle (W13 DGRAD's operand) and column bundle (W13 WGRAD's).
+template <bool MX>
+__device__ __forceinline__ void epi_swiglu_bwd(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow,
+                                               int lane) {
+  const int f = t.out_col0 + lrow;
+  for (int c0 = 0; c0 < t.b_rows; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(tbase + c0, v);
+    tmem_ld_wait();
+    float dg[32], du[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const long long row = t.out_row0 + c0 + i;
+      const float g = __bfloat162float(p.h1[row * p.h1_pitch + f]);
+      const float u = __bfloat162float(p.h1[row * p.h1_pitch + p.F + f]);
+      const float dh2 = u2f(v[i]);
+      const float s = sigmoid_f(g);
+      dg[i] = dh2 * u * (s * (1.0f + g * (1.0f - s)));
+      du[i] = dh2 * (g * s);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const long long row = t.out_row0 + c0 + i;
+      store_row_val<MX>(p, p.out0, p.out0_sf, p.out0_pitch, p.out0_sf_pitch, row, f, dg[i], lane);
+      store_row_val<MX>(p, p.out0, p.out0_sf, p.out0_pitch, p.out0_sf_pitch, row, p.F + f, du[i], lane);
+    }
+    store_col32<MX>(p.out1, p.out1_sf, p.out1_pitch, p.out1_sf_pitch, f, t.out_row0 + c0, dg);
+    store_col32<MX>(p.out1, p.out1_sf, p.out1_pitch, p.out1_sf_pitch, p.F + f, t.out_row0 + c0, du);
+  }
+}
+
+// Weight gradient: dW[e][m][n0 .. n0+127], BF16 or FP32, optional add.  An
+// expert without rows (no MMA issued) gets zeros, or is left as is when
+// adding.
+__device__ __forceinline__ void epi_wgrad(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow) {
+  if (t.kstages == 0 && p.dw_accum) return;
+  const long long M = static_cast<long long>(p.m_tiles) * 128;
+  const long long row = static_cast<long long>(t.e) * M + t.out_row0 + lrow;
+  for (int c0 = 0; c0 < 128; c0 += 32) {
+    float v[32];
+    if (t.kstages > 0) {
+      uint32_t r[32];
+      tmem_ld32(tbase + c0, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    }
+    const long long off = row * p.out0_pitch + t.out_col0 + c0;
+    if (p.dw_fp32) {
+      float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out0) + off);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 x = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        if (p.dw_accum) {
+          const float4 y = o[q];
+          x.x += y.x;
+          x.y += y.y;
+          x.z += y.z;
+          x.w += y.w;
+        }
+        o[q] = x;
+      }
+    } else {
+      uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out0) + off);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (p.dw_accum) {
+          const uint4 y = o[q];
+          v[8 * q + 0] += bf16_lo(y.x);
+          v[8 * q + 1] += bf16_hi(y.x);
+          v[8 * q + 2] += bf16_lo(y.y);
+          v[8 * q + 3] += bf16_hi(y.y);
+          v[8 * q + 4] += bf16_lo(y.z);
+          v[8 * q + 5] += bf16_hi(y.z);
+          v[8 * q + 6] += bf16_lo(y.w);
+          v[8 * q + 7] += bf16_hi(y.w);
+        }
+        o[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                          pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <bool MX, int NA>
+struct Cfg {
+  static constexpr int S = (NA == 2) ? 4 : 6;          // pipeline stages
+  static constexpr int STAGE = NA * kABytes + kBBytes;
+  static constexpr int ACC_BUFS = (NA == 1) ? 2 : 1;   // accumulator buffers
+  static constexpr int ACC_COLS = NA * 128;
+  static constexpr int SF_COLS = (NA + 1) * 4;         // scale columns per stage
+  static constexpr uint32_t SF_COL0 = ACC_BUFS * ACC_COLS;
+  static constexpr int BK = MX ? 128 : 64;             // contraction elements per stage
+  static constexpr int KMMA = MX ? 32 : 16;            // contraction elements per MMA
+  static constexpr int MMAS = BK / KMMA;
+  static constexpr int THREADS = MX ? 320 : 192;
+  static constexpr int SMEM = 1024 + S * STAGE + 256;
+};
+
+template <bool MX, int NA, int EPI, int MODE>
+__global__ void __launch_bounds__(Cfg<MX, NA>::THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmParams p) {
+  using C = Cfg<MX, NA>;
+  constexpr int S = C::S;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + C::ACC_BUFS;
+  uint64_t* drain = tempty + C::ACC_BUFS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1 + (MX ? 4 : 0));
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < C::ACC_BUFS; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+    tma_prefetch(&tmA);
+    tma_prefetch(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int nblk = (MODE == kGroupedM) ? p.hdr[1] : 0;
+  const int num_tiles = (MODE == kGroupedM) ? nblk * p.n_tiles : p.E * p.m_tiles * p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk);
+        for (int ks = 0; ks < t.kstages; ++ks, ++it) {
+          const uint32_t slot = it % S, ph = (it / S) & 1;
+          if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + slot * C::STAGE;
+          uint8_t* sb = sa + NA * kABytes;
+          mbar_arrive_expect_tx(&full[slot], NA * kABytes + t.b_rows * 128);
+          const int kx = t.k0 + ks * C::BK;
+#pragma unroll
+          for (int j = 0; j < NA; ++j) tma_load_2d(sa + j * kABytes, &tmA, &full[slot], kx, t.a_row[j]);
+          for (int c = 0; c < t.b_rows / 32; ++c)
+            tma_load_2d(sb + c * 4096, &tmB, &full[slot], kx, t.b_row0 + 32 * c);
+        }
+      }
+      // no load may still be landing in shared memory when the CTA exits
+      const uint32_t pend = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
+      for (uint32_t j = 0; j < pend; ++j) {
+        const uint32_t i2 = it - 1 - j;
+        drain_wait(&full[i2 % S], (i2 / S) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, tc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++tc) {
+        const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk);
+        const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
+        if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * C::ACC_COLS;
+        for (int ks = 0; ks < t.kstages; ++ks, ++it) {
+          const uint32_t slot = it % S, ph = (it / S) & 1;
+          if (!mbar_wait(&full[slot], ph, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + slot * C::STAGE);
+          const uint64_t bdesc0 = sdesc_k_sw128(sa + NA * kABytes);
+          const int nmma = (ks == t.kstages - 1) ? t.klast / C::KMMA : C::MMAS;
+          for (int k = 0; k < nmma; ++k) {
+            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(2 * k);   // +32 bytes along K
+            const uint32_t accum = (ks | k) ? 1u : 0u;
+#pragma unroll
+            for (int j = 0; j < NA; ++j) {
+              const uint64_t adesc = sdesc_k_sw128(sa + j * kABytes) + static_cast<uint64_t>(2 * k);
+              if (MX) {
+                const uint32_t sfcol = tmem + C::SF_COL0 + slot * C::SF_COLS;
+                mma_mxf8(d_tmem + j * 128, adesc, bdesc, idesc_mxf8(t.b_rows, k, k), sfcol + j * 4,
+                         sfcol + NA * 4, accum);
+              } else {
+                mma_bf16(d_tmem + j * 128, adesc, bdesc, idesc_bf16(t.b_rows), accum);
+              }
+            }
+          }
+          tc_commit(&empty[slot]);
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+      }
+      // every MMA issued here must be complete before TMEM is released
+      tc_commit(drain);
+      drain_wait(drain, 0);
+    }
+  } else if (warp < 6) {
+    // --------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int lrow = q * 32 + lane;
+    uint32_t tc = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
+      const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk);
+      const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull[acc], aph, abort_flag, p.err))) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
+      if (EPI == kEpiStore) epi_store(p, t, tbase, lrow);
+      else if (EPI == kEpiSwigluFwd) epi_swiglu_fwd<MX>(p, t, tbase, lrow, lane);
+      else if (EPI == kEpiSwigluBwd) epi_swiglu_bwd<MX>(p, t, tbase, lrow, lane);
+      else epi_wgrad(p, t, tbase, lrow);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  } else if (MX) {
+    // ----------------------------------------- scale factors -> TMEM
+    // TMEM scale layout for M = 128 with one scale per 32 values: column j
+    // (of 4) at lane i holds the scales of row 32*j + i, byte l = K-block l
+    // of the stage (selected per MMA by the scale-factor id).  Every warp
+    // writes the same words into its own lane quadrant.
+    const int q = warp & 3;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk);
+      for (int ks = 0; ks < t.kstages; ++ks, ++it) {
+        const uint32_t slot = it % S, ph = (it / S) & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[slot], ph ^ 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        const int kb0 = (t.k0 + ks * C::BK) >> 5;
+        uint32_t wa[NA][4], wb[4];
+#pragma unroll
+        for (int j = 0; j < NA; ++j)
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            wa[j][c] = load_sf4(p.sfa + static_cast<long long>(t.a_row[j] + 32 * c + lane) * p.sfa_pitch + kb0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          wb[c] = (32 * c < t.b_rows)
+                      ? load_sf4(p.sfb + static_cast<long long>(t.b_row0 + 32 * c + lane) * p.sfb_pitch + kb0)
+                      : 0u;
+        const uint32_t col = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::SF_COL0 + slot * C::SF_COLS;
+#pragma unroll
+        for (int j = 0; j < NA; ++j) tmem_st4(col + j * 4, wa[j][0], wa[j][1], wa[j][2], wa[j][3]);
+        tmem_st4(col + NA * 4, wb[0], wb[1], wb[2], wb[3]);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[slot]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool MX, int NA, int EPI, int MODE>
+cudaError_t launch_impl(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
+  using C = Cfg<MX, NA>;
+  auto kern = gemm_kernel<MX, NA, EPI, MODE>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int grid = max(1, min(num_sms, g.max_tiles));
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
+  if (g.max_tiles <= 0) return cudaSuccess;
+#define MOE_GEMM_CASE(MXV, NAV, EPIV, MODEV)                                         \
+  if (g.mx == MXV && g.na == NAV && g.epi == EPIV && g.mode == MODEV)                \
+    return launch_impl<MXV, NAV, EPIV, MODEV>(g, num_sms, stream);
+  MOE_GEMM_CASE(false, 2, kEpiSwigluFwd, kGroupedM)
+  MOE_GEMM_CASE(true, 2, kEpiSwigluFwd, kGroupedM)
+  MOE_GEMM_CASE(false, 1, kEpiStore, kGroupedM)
+  MOE_GEMM_CASE(true, 1, kEpiStore, kGroupedM)
+  MOE_GEMM_CASE(false, 1, kEpiSwigluBwd, kGroupedM)
+  MOE_GEMM_CASE(true, 1, kEpiSwigluBwd, kGroupedM)
+  MOE_GEMM_CASE(false, 1, kEpiWgrad, kGroupedK)
+  MOE_GEMM_CASE(true, 1, kEpiWgrad, kGroupedK)
+#undef MOE_GEMM_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,100 @@
+// Launch interface of the MoE kernels (internal to the library).
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// Device view of one routing state (the saved-state prefix or the
+// context's inference copy).  Layout and meaning of every array are those of
+// moe_saved_field in moe_gb300.h.
+struct RoutingPtrs {
+  int* hdr;       // [0] T, [1] blocks, [2] padded rows used, [3] active routes
+  int* counts;    // [E]
+  int* offsets;   // [E+1]
+  int* poffsets;  // [E+1]
+  int* perm;      // [r_cap]
+  int* inv;       // [T_max*K]
+  int4* blocks;   // [b_cap] (expert, first row, rows, 0)
+  float* scores;  // [T_max*K]
+};
+
+constexpr int kPad = 32;        // rows of every expert are padded to this
+constexpr int kBlockRows = 128; // rows per GEMM row block (MMA N <= 128)
+
+cudaError_t launch_route(const int32_t* ids, const float* scores, int T, int K, int E, int r_cap, int debug,
+                         const RoutingPtrs& rp, uint32_t* err, cudaStream_t stream);
+
+// Row bundle: dst[r] = q(s * src[perm[r] / K]) for every used row r (s = the
+// route's score when `use_scores`, else 1; zero rows for padding).
+cudaError_t launch_gather_rows(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
+                               void* dst, uint8_t* dst_sf, int r_cap, int num_sms, cudaStream_t stream);
+
+// Column bundle: dstT[d][r] = the same values transposed to [D, r_cap]; MXFP8
+// quantises along rows in 32-row blocks (WGRAD contracts over rows).
+cudaError_t launch_gather_cols(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
+                               void* dstT, uint8_t* dstT_sf, int r_cap, cudaStream_t stream);
+
+// out[t] = bf16((accumulate ? out[t] : 0) + sum_k s(t,k) * h[inv(t,k)]),
+// FP32, k in order; s = 1 when `scores` is NULL.  The token count is T, or
+// hdr[0] (read on the device, at most T) when `hdr` is given.
+cudaError_t launch_combine(const void* h, int D, int K, const int* inv, const float* scores, void* out, int T,
+                           bool accumulate, int num_sms, cudaStream_t stream, const int* hdr = nullptr);
+
+cudaError_t launch_prep_mx_weight(const void* w, int E, int N, int K, uint8_t* q, uint8_t* sf, uint8_t* qT,
+                                  uint8_t* sfT, cudaStream_t stream);
+cudaError_t launch_transpose_bf16(const void* w, int E, int N, int K, void* wT, cudaStream_t stream);
+
+// ------------------------------------------------------------- grouped GEMM
+
+enum GemmMode { kGroupedM = 0, kGroupedK = 1 };
+enum GemmEpi { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2, kEpiWgrad = 3 };
+
+struct GemmParams {
+  // routing
+  const int* hdr;
+  const int4* blocks;
+  const int* poffsets;
+  int E;
+  int n_tiles;            // grouped-M: 128-wide output tiles per expert; grouped-K: N/128
+  int m_tiles;            // grouped-K: M/128
+  int K;                  // grouped-M: contraction length
+  int a_rows_per_expert;  // grouped-M: rows of A per expert
+  int a_up_offset;        // SwiGLU forward: row offset of the up half (F)
+  // MXFP8 scale factors: byte arrays with a row pitch in bytes
+  const uint8_t* sfa;
+  long long sfa_pitch;
+  const uint8_t* sfb;
+  long long sfb_pitch;
+  // epilogue outputs (pitches in elements)
+  void* out0;
+  long long out0_pitch;
+  uint8_t* out0_sf;
+  long long out0_sf_pitch;
+  void* out1;
+  long long out1_pitch;
+  uint8_t* out1_sf;
+  long long out1_sf_pitch;
+  __nv_bfloat16* h1;      // SwiGLU forward: written when save_h1; backward: read
+  long long h1_pitch;
+  int F;
+  int save_h1;
+  int want_col;
+  int dw_fp32;
+  int dw_accum;
+  uint32_t* err;
+};
+
+struct GemmLaunch {
+  bool mx;
+  int na;                 // A tiles per B tile (2 for the fused SwiGLU forward)
+  GemmEpi epi;
+  GemmMode mode;
+  CUtensorMap tmA, tmB;
+  GemmParams p;
+  int max_tiles;          // upper bound of the tile count (grid sizing)
+};
+
+cudaError_t launch_gemm(const GemmLaunch& g, int num_sms, cudaStream_t stream);
+
+}  // namespace moe

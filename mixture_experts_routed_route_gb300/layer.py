@@ -1,0 +1,122 @@
+"""Torch-facing wrapper of the C ABI: device buffers come from torch, every
+computation runs in the CUDA library.
+
+``PreparedWeight`` holds one stacked expert weight in the form the GEMMs read
+(``prepare_block_scaled_weight``); ``MoELayer`` owns one context and offers
+``forward`` / ``backward`` on torch tensors.
+"""
+
+import numpy as np
+import torch
+
+from . import abi
+
+_DT = {"bf16": abi.MOE_BF16, "mxfp8": abi.MOE_MXFP8}
+
+
+def precision_code(precision):
+    return _DT[precision] if isinstance(precision, str) else int(precision)
+
+
+class PreparedWeight:
+    """One stacked weight [E, N, K] prepared for the GEMMs.
+
+    BF16: ``data`` is the caller's tensor, ``data_t`` its transpose
+    [E, K, N] (for the input-gradient GEMMs).  MXFP8: E4M3 codes with one
+    E8M0 scale per 32x32 tile, in both orientations."""
+
+    def __init__(self, w, precision, with_transpose=True, stream=None):
+        assert w.dtype == torch.bfloat16 and w.is_cuda and w.dim() == 3
+        w = w.contiguous()
+        self.precision = precision_code(precision)
+        E, N, K = w.shape
+        self.shape = (E, N, K)
+        dev = w.device
+        self.data_t = self.scale = self.scale_t = None
+        if self.precision == abi.MOE_MXFP8:
+            self.data = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
+            self.scale = torch.empty(E * N * (K // 32) + 16, dtype=torch.uint8, device=dev)
+            if with_transpose:
+                self.data_t = torch.empty((E, K, N), dtype=torch.uint8, device=dev)
+                self.scale_t = torch.empty(E * K * (N // 32) + 16, dtype=torch.uint8, device=dev)
+            abi.prepare_block_scaled_weight(w, E, N, K, self.precision, self.data, self.scale, self.data_t,
+                                            self.scale_t, stream)
+        else:
+            self.data = w
+            if with_transpose:
+                self.data_t = torch.empty((E, K, N), dtype=torch.bfloat16, device=dev)
+                abi.prepare_block_scaled_weight(w, E, N, K, self.precision, None, None, self.data_t, None, stream)
+        self.struct = abi.moe_weight(self.precision, E, N, K, abi._ptr(self.data), abi._ptr(self.scale),
+                                     abi._ptr(self.data_t), abi._ptr(self.scale_t))
+
+
+class MoELayer:
+    """One routed MoE layer bound to a context (fixed scratch)."""
+
+    def __init__(self, max_tokens, d_model, d_ff, num_experts, top_k, precision, training=False, debug=False,
+                 device="cuda"):
+        flags = (abi.MOE_TRAINING if training else 0) | (abi.MOE_DEBUG_CHECKS if debug else 0)
+        self.cfg = abi.make_config(max_tokens, d_model, d_ff, num_experts, top_k, precision_code(precision), flags)
+        self.device = torch.device(device)
+        self.D, self.F, self.E, self.K = d_model, d_ff, num_experts, top_k
+        self.training = training
+        self.ctx = abi.moe_ctx_create(self.cfg)
+        self.r_cap = abi.moe_row_capacity(self.cfg)
+
+    def close(self):
+        if self.ctx is not None:
+            torch.cuda.synchronize(self.device)
+            abi.moe_ctx_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------- state
+    def new_saved(self):
+        return torch.empty(abi.moe_saved_state_bytes(self.cfg), dtype=torch.uint8, device=self.device)
+
+    def saved_field(self, saved, field, dtype, shape):
+        off, nb = abi.moe_saved_state_field(self.cfg, field)
+        esz = torch.empty((), dtype=dtype).element_size()
+        n = int(np.prod(shape))
+        assert n * esz <= nb
+        return saved[off:off + n * esz].view(dtype).view(*shape)
+
+    def read_buffer(self, which, dtype, shape):
+        """Copy one scratch region to host memory (tests only)."""
+        ptr, nb = abi.moe_ctx_buffer(self.ctx, which)
+        out = np.empty(shape, dtype=dtype)
+        assert out.nbytes <= nb
+        abi.moe_debug_copy_to_host(out.ctypes.data, ptr, out.nbytes)
+        return out
+
+    def error_bits(self):
+        return abi.moe_ctx_get_error(self.ctx)
+
+    # ----------------------------------------------------------- compute
+    def forward(self, x, ids, scores, W13, W2, out=None, saved=None, accumulate=False, stream=None):
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty((T, self.D), dtype=torch.bfloat16, device=self.device)
+        abi.moe_forward(self.ctx, T, x, ids, scores, W13.struct, W2.struct, out, saved,
+                        abi.MOE_ACCUMULATE_OUT if accumulate else 0, stream)
+        return out
+
+    def backward(self, saved, dout, W13, W2, dx=None, dW13=None, dW2=None, accumulate_dx=False, dw_fp32=False,
+                 dw_accumulate=False, stream=None):
+        T = dout.shape[0]
+        dt = torch.float32 if dw_fp32 else torch.bfloat16
+        if dx is None:
+            dx = torch.empty((T, self.D), dtype=torch.bfloat16, device=self.device)
+        if dW13 is None:
+            dW13 = torch.empty((self.E, 2 * self.F, self.D), dtype=dt, device=self.device)
+        if dW2 is None:
+            dW2 = torch.empty((self.E, self.D, self.F), dtype=dt, device=self.device)
+        flags = ((abi.MOE_ACCUMULATE_DX if accumulate_dx else 0) | (abi.MOE_DW_FP32 if dw_fp32 else 0)
+                 | (abi.MOE_DW_ACCUMULATE if dw_accumulate else 0))
+        abi.moe_backward(self.ctx, saved, dout, W13.struct, W2.struct, dx, dW13, dW2, flags, stream)
+        return dx, dW13, dW2

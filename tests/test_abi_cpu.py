@@ -1,0 +1,81 @@
+"""The C-ABI library loads and exports every function include/moe_gb300.h
+declares, and the binding's structs match the header (no GPU needed: no
+compute call is made)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+
+def _declared_functions():
+    names = []
+    for inc in os.listdir(os.path.join(ROOT, "include")):
+        if not inc.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", inc)).read()
+        names += re.findall(r"^MOE_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_routed_route_gb300 import build
+    path = os.path.join(build.OUT_DIR, build.LIB_NAME)
+    if not os.path.exists(path):
+        build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = set(_declared_functions())
+    for required in ("moe_ctx_create", "moe_ctx_destroy", "moe_forward", "moe_backward",
+                     "prepare_block_scaled_weight", "moe_saved_state_bytes", "moe_ctx_get_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_declared_symbol(lib):
+    from mixture_experts_routed_route_gb300 import abi
+    for name in _declared_functions():
+        assert name in abi._SIGNATURES, name
+        assert callable(getattr(abi, name)), name
+
+
+def test_struct_layouts_match_header():
+    from mixture_experts_routed_route_gb300 import abi
+    assert ctypes.sizeof(abi.moe_config) == 7 * 4
+    assert ctypes.sizeof(abi.moe_weight) == 16 + 4 * 8
+    assert abi.moe_weight.data.offset == 16
+
+
+def test_host_side_sizes_without_gpu(lib):
+    """Pure host calls: capacity and layout arithmetic."""
+    from mixture_experts_routed_route_gb300 import abi
+    cfg = abi.make_config(2048, 7168, 2048, 384, 6, abi.MOE_MXFP8, abi.MOE_TRAINING)
+    r = abi.moe_row_capacity(cfg)
+    assert r % 128 == 0 and r >= 2048 * 6 + 31 * 384 + 128
+    sb = abi.moe_saved_state_bytes(cfg)
+    off_prev = -1
+    for f in range(abi.MOE_SAVED_NUM_FIELDS):
+        off, nb = abi.moe_saved_state_field(cfg, f)
+        assert off % 256 == 0 and off > off_prev and off + nb <= sb
+        off_prev = off
+    assert abi.moe_saved_state_field(cfg, abi.MOE_SAVED_H1)[1] == r * 2 * 2048 * 2
+    bad = abi.make_config(2048, 7168, 2048, 2000, 6, abi.MOE_MXFP8, 0)
+    assert abi.moe_row_capacity(bad) == 0 and abi.moe_saved_state_bytes(bad) == 0
+    with pytest.raises(abi.MoEError) as ei:
+        abi.moe_ctx_create(bad)
+    assert ei.value.status == abi.MOE_ERR_INVALID_ARG
+    odd = abi.make_config(64, 200, 256, 8, 2, abi.MOE_BF16, 0)
+    with pytest.raises(abi.MoEError) as ei:
+        abi.moe_ctx_create(odd)
+    assert ei.value.status in (abi.MOE_ERR_INVALID_ARG, abi.MOE_ERR_UNSUPPORTED)
