@@ -1,0 +1,514 @@
+"""Benchmark of the routed-expert MoE layer on GB300.
+
+One step = one pass of the whole hot path over one synthetic batch:
+shared-expert forward (BF16, dense), routed forward (route, gather/quantise,
+W13 + SwiGLU, W2, combine, accumulated onto the shared output) and, for the
+training workloads, the routed and shared backward (dh3 bundles, W2 DGRAD +
+SwiGLU backward, W2 WGRAD, W13 DGRAD, W13 WGRAD, dX reduction).  The step is
+captured once in a CUDA graph and replayed.
+
+Metric: useful TFLOP/s of the routed expert GEMMs (6 R D F forward, 12 R D F
+backward, R = active routes; padding, the shared expert and the router are
+not counted, as on the Dist-MoE explainer's "Performance Metrics" panel),
+plus tokens/s and the fraction of the dense tensor peak.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       python bench.py --impl reference ...   (the fp64 oracle on host cores)
+Under torchrun each rank runs an independent replica (weak scaling) and the
+slowest rank's time is reported.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "useful TFLOP/s and tokens/s per GB300 (fraction of FP8/BF16 tensor peak)"
+DEFAULT_WORKLOAD = "e384_mxfp8_zipf_train"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-sample-experts", type=int, default=3)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            ids = [v.strip() for v in vis.split(",") if v.strip()]
+            if self.index < len(ids):
+                self.index = ids[self.index]
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------- algorithmic bytes
+
+def stage_bytes(w, rows_padded, routes, precision, train):
+    """Unique bytes each stage must move (read once + written once), per launch.
+
+    rows_padded = sum of expert row counts padded to 32; routes = active
+    routes.  MXFP8 operands cost 1 + 1/32 bytes per element (E4M3 + E8M0)."""
+    T, D, F, E = w.T, w.D, w.F, w.E
+    q = (1 + 1 / 32) if precision == "mxfp8" else 2.0
+    Rp, R = rows_padded, routes
+    fwd = {
+        "route": T * w.K * 8 + (Rp + 2 * T * w.K) * 4,
+        "gather_x_rows": T * D * 2 + Rp * D * q,
+        "gather_x_cols": (T * D * 2 + Rp * D * q) if train else 0,
+        "gemm_w13_swiglu": E * 2 * F * D * q + Rp * D * q + Rp * F * q + (Rp * 2 * F * 2 + Rp * F * q if train else 0),
+        "gemm_w2": E * D * F * q + Rp * F * q + Rp * D * 2,
+        "combine": R * D * 2 + T * D * 2 * 2,
+    }
+    bwd = {
+        "gather_dh3_rows": T * D * 2 + Rp * D * q,
+        "gather_dh3_cols": T * D * 2 + Rp * D * q,
+        "gemm_w2_dgrad_swiglu_bwd": E * D * F * q + Rp * D * q + Rp * 2 * F * 2 + 2 * Rp * 2 * F * q,
+        "gemm_w2_wgrad": D * Rp * q + F * Rp * q + E * D * F * 2,
+        "gemm_w13_dgrad": E * 2 * F * D * q + Rp * 2 * F * q + Rp * D * 2,
+        "gemm_w13_wgrad": 2 * F * Rp * q + D * Rp * q + E * 2 * F * D * 2,
+        "reduce_dx": R * D * 2 + T * D * 2 * 2,
+    }
+    return fwd, bwd
+
+
+def traffic_record(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if its kernel
+    source is unchanged since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "mixture_experts_routed_route_gb300", "csrc", "gemm.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        line = line.strip()
+        if not line.startswith("{"):
+            continue
+        rec = json.loads(line)
+        if rec.get("stage") == kernel and rec.get("workload") == workload and rec.get("gemm_src") == digest:
+            return rec.get("dram_bytes_per_launch_full")
+    return None
+
+
+# ------------------------------------------------------------ our arm (GPU)
+
+class Step:
+    """Inputs, weights, contexts and the captured CUDA graph of one step."""
+
+    def __init__(self, w, device):
+        import torch
+        from mixture_experts_routed_route_gb300 import synth
+        from mixture_experts_routed_route_gb300.layer import MoELayer, PreparedWeight
+
+        self.w = w
+        self.dev = device
+        self.train = w.train
+        T, D, F, E, K = w.T, w.D, w.F, w.E, w.K
+        ids, scores = synth.make_routing(w)
+        self.ids_np, self.scores_np = ids, scores
+        self.x = synth.make_tokens(w, device)
+        self.dy = synth.make_grad_out(w, device)
+        self.ids = torch.from_numpy(ids).to(device)
+        self.scores = torch.from_numpy(scores).to(device)
+        w13, w2 = synth.make_weights(w, device)
+        self.sample_experts = None
+        self.W13 = PreparedWeight(w13, w.precision, with_transpose=self.train)
+        self.W2 = PreparedWeight(w2, w.precision, with_transpose=self.train)
+        self.w13_bf16, self.w2_bf16 = w13, w2   # kept only until the oracle sample is taken
+        self.layer = MoELayer(T, D, F, E, K, w.precision, training=self.train, device=device)
+        self.saved = self.layer.new_saved() if self.train else None
+        self.shared = None
+        if w.shared_F:
+            sw13, sw2 = synth.make_shared_weights(w, device)
+            self.sW13 = PreparedWeight(sw13, "bf16", with_transpose=self.train)
+            self.sW2 = PreparedWeight(sw2, "bf16", with_transpose=self.train)
+            self.shared = MoELayer(T, D, w.shared_F, 1, 1, "bf16", training=self.train, device=device)
+            self.s_ids = torch.zeros((T, 1), dtype=torch.int32, device=device)
+            self.s_scores = torch.ones((T, 1), dtype=torch.float32, device=device)
+            self.s_saved = self.shared.new_saved() if self.train else None
+        self.out = torch.empty((T, D), dtype=torch.bfloat16, device=device)
+        if self.train:
+            self.dx = torch.empty((T, D), dtype=torch.bfloat16, device=device)
+            self.dW13 = torch.empty((E, 2 * F, D), dtype=torch.bfloat16, device=device)
+            self.dW2 = torch.empty((E, D, F), dtype=torch.bfloat16, device=device)
+            if self.shared:
+                self.sdW13 = torch.empty((1, 2 * w.shared_F, D), dtype=torch.bfloat16, device=device)
+                self.sdW2 = torch.empty((1, D, w.shared_F), dtype=torch.bfloat16, device=device)
+        self.graph = None
+
+    def layers(self):
+        return [l for l in (self.layer, self.shared) if l is not None]
+
+    def enqueue(self):
+        """The step, through the public C ABI (enqueue only, no host sync)."""
+        acc = False
+        if self.shared:
+            self.shared.forward(self.x, self.s_ids, self.s_scores, self.sW13, self.sW2, out=self.out,
+                                saved=self.s_saved)
+            acc = True
+        self.layer.forward(self.x, self.ids, self.scores, self.W13, self.W2, out=self.out, saved=self.saved,
+                           accumulate=acc)
+        if self.train:
+            acc = False
+            if self.shared:
+                self.shared.backward(self.s_saved, self.dy, self.sW13, self.sW2, dx=self.dx, dW13=self.sdW13,
+                                     dW2=self.sdW2)
+                acc = True
+            self.layer.backward(self.saved, self.dy, self.W13, self.W2, dx=self.dx, dW13=self.dW13, dW2=self.dW2,
+                                accumulate_dx=acc)
+
+    def capture(self):
+        import torch
+        from mixture_experts_routed_route_gb300 import abi
+        before = sum(abi.moe_ctx_launch_count(l.ctx) for l in self.layers())
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.enqueue()
+        self.launches_per_step = sum(abi.moe_ctx_launch_count(l.ctx) for l in self.layers()) - before
+
+    def rows_used(self):
+        from mixture_experts_routed_route_gb300 import abi
+        import torch
+        if self.train:
+            hdr = self.layer.saved_field(self.saved, abi.MOE_SAVED_HEADER, torch.int32, (16,)).cpu().numpy()
+        else:
+            hdr = self.layer.read_buffer(abi.MOE_BUF_ROUTING, np.int32, (16,))
+        return int(hdr[2]), int(hdr[3])
+
+
+def cpu_sample(w, ids, scores, x_cpu, dy_cpu, w13_sub, w2_sub, experts):
+    """Time the oracle on a bounded sample (the routes of a few experts)."""
+    from oracle import sample as osample
+    f64 = lambda t: t.to("cpu").double().numpy()
+    xs, dys = f64(x_cpu), (f64(dy_cpu) if w.train else None)
+    a13, a2 = f64(w13_sub), f64(w2_sub)
+    t0 = time.perf_counter()
+    osample.run(xs, ids, scores, a13, a2, experts, w.precision, dY=dys)
+    dt = time.perf_counter() - t0
+    sub_ids = osample.restrict_routes(ids, experts)
+    flops = osample.useful_flops(sub_ids, w.D, w.F, w.train)
+    return dt, flops, int(np.sum(sub_ids >= 0))
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def pick_sample_experts(w, ids, n):
+    rng = np.random.default_rng(12345)
+    present = sorted(set(int(e) for e in np.asarray(ids).reshape(-1) if e >= 0))
+    order = [present[i] for i in rng.permutation(len(present))]
+    return sorted(order[:n])
+
+
+def run_ours(args, rank, world):
+    import torch
+    from mixture_experts_routed_route_gb300 import abi, synth
+
+    w = synth.WORKLOADS[args.workload]
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    st = Step(w, dev)
+
+    # eager warm-up (configures kernels), then correctness guard: no device error
+    st.enqueue()
+    torch.cuda.synchronize(dev)
+    for l in st.layers():
+        bits = l.error_bits()
+        if bits:
+            raise RuntimeError(f"device error bits {bits:#x} in warm-up")
+    rows_padded, routes = st.rows_used()
+
+    # oracle sample weights (host copies) before the BF16 masters are dropped
+    sample = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        experts = pick_sample_experts(w, st.ids_np, args.cpu_sample_experts)
+        sample = (experts, st.w13_bf16[experts].cpu(), st.w2_bf16[experts].cpu(), st.x.cpu(), st.dy.cpu())
+    st.w13_bf16 = st.w2_bf16 = None
+    torch.cuda.empty_cache()
+
+    for l in st.layers():
+        abi.moe_ctx_enable_stage_timing(l.ctx, True)
+    st.capture()
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        st.graph.replay()
+    torch.cuda.synchronize(dev)
+
+    # ---------------- timed region: K graph replays
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        st.graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # ---------------- per-stage durations (CUDA events inside the graph)
+    fwd_t = {n: [] for n in abi.FWD_STAGE_NAMES}
+    bwd_t = {n: [] for n in abi.BWD_STAGE_NAMES}
+    for _ in range(max(3, min(args.steps, 10))):
+        st.graph.replay()
+        torch.cuda.synchronize(dev)
+        for n, v in zip(abi.FWD_STAGE_NAMES, abi.moe_ctx_stage_times(st.layer.ctx, 0)):
+            fwd_t[n].append(v)
+        if st.train:
+            for n, v in zip(abi.BWD_STAGE_NAMES, abi.moe_ctx_stage_times(st.layer.ctx, 1)):
+                bwd_t[n].append(v)
+    stage_ms = {k: statistics.mean(v) for k, v in list(fwd_t.items()) + list(bwd_t.items()) if v}
+    fb, bb = stage_bytes(w, rows_padded, routes, w.precision, st.train)
+    sbytes = {**fb, **(bb if st.train else {})}
+    dom = max(stage_ms, key=lambda k: stage_ms[k])
+    achieved = sbytes[dom] / (stage_ms[dom] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic_record(dom, w.name),
+            "algorithmic_bytes": int(sbytes[dom]), "avg_launch_ms": round(stage_ms[dom], 4),
+            "peak_source": pk["source"]}
+    stages = {k: {"ms": round(v, 4), "GB/s": round(sbytes[k] / (v * 1e-3) / 1e9, 1) if v > 0 else None}
+              for k, v in stage_ms.items()}
+
+    # ---------------- metric
+    flops = 6.0 * routes * w.D * w.F * (3.0 if st.train else 1.0)
+    tflops = flops / (ms * 1e-3) / 1e12 * world
+    fp8_peak = pk["bf16_tflops"] * 2.0
+    peak_t = fp8_peak if w.precision == "mxfp8" else pk["bf16_tflops"]
+    shared_flops = (6.0 * w.T * w.D * w.shared_F * (3.0 if st.train else 1.0)) if w.shared_F else 0.0
+
+    # ---------------- end to end through the ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = st.x.cpu().pin_memory()
+        hids = st.ids.cpu().pin_memory()
+        hsc = st.scores.cpu().pin_memory()
+        hdy = st.dy.cpu().pin_memory() if st.train else None
+        hout = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+        hdx = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() if st.train else None
+        h2d = hx.numel() * 2 + hids.numel() * 4 + hsc.numel() * 4 + (hdy.numel() * 2 if st.train else 0)
+        d2h = hout.numel() * 2 + (hdx.numel() * 2 if st.train else 0)
+
+        def e2e_step():
+            st.x.copy_(hx, non_blocking=True)
+            st.ids.copy_(hids, non_blocking=True)
+            st.scores.copy_(hsc, non_blocking=True)
+            if st.train:
+                st.dy.copy_(hdy, non_blocking=True)
+            st.enqueue()
+            hout.copy_(st.out, non_blocking=True)
+            if st.train:
+                hdx.copy_(st.dx, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, args.steps // 2)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            tt = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            ems = float(tt.item())
+        e2e = {"value": round(flops / (ems * 1e-3) / 1e12 * world, 3), "unit": "TFLOP/s",
+               "ms_per_step": round(ems, 4), "tokens_per_s": round(w.T * world / (ems * 1e-3), 1),
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    # ---------------- oracle baseline on host cores (rank 0, N = 1)
+    cpu = None
+    if sample is not None:
+        experts, s13, s2, xc, dyc = sample
+        dt, sflops, sroutes = cpu_sample(w, st.ids_np, st.scores_np, xc, dyc, s13, s2, experts)
+        cpu = {"value": round(sflops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"fp64 numpy oracle, {'forward+backward' if w.train else 'forward'} of the {sroutes} "
+                         f"routes of {len(experts)} of {w.E} experts (all {w.T} tokens), {dt:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.precision, "data": "synthetic",
+        "tokens_per_s": round(w.T * world / (ms * 1e-3), 1),
+        "tensor_frac": round(tflops / world / peak_t, 4),
+        "tensor_peak_tflops": round(peak_t, 1),
+        "config": {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "K": w.K,
+                   "routing": w.routing, "inactive_frac": w.inactive_frac, "shared_F": w.shared_F,
+                   "train": w.train, "active_routes": routes, "padded_rows": rows_padded,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (expert weights stream from HBM every step)",
+                   "graph": "one CUDA graph per step, replayed"},
+        "roofline": roof, "stages": stages,
+        "shared_expert_tflops": round(shared_flops / (ms * 1e-3) / 1e12, 3) if shared_flops else None,
+        "clocks": clk, "gpu_launches": int(st.launches_per_step * args.steps),
+        "e2e": e2e, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------ reference arm (CPU)
+
+def run_reference(args, rank, world):
+    """The fp64 oracle timed on the host cores, on bounded samples of the
+    same workload (each step = the oracle on the routes of a few experts)."""
+    if rank != 0:
+        return
+    import torch
+    from mixture_experts_routed_route_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    ids, scores = synth.make_routing(w)
+    x = synth.make_tokens(w, "cpu")
+    dy = synth.make_grad_out(w, "cpu")
+    experts = pick_sample_experts(w, ids, args.cpu_sample_experts)
+    w13s, w2s = synth.make_weights(w, "cpu", experts=experts)
+    for _ in range(min(args.warmup, 1)):
+        cpu_sample(w, ids, scores, x, dy, w13s, w2s, experts)
+    times, fl = [], 0.0
+    steps = max(1, min(args.steps, 3))
+    for _ in range(steps):
+        dt, fl, sroutes = cpu_sample(w, ids, scores, x, dy, w13s, w2s, experts)
+        times.append(dt)
+    dt = statistics.median(times)
+    val = fl / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": steps, "warmup": min(args.warmup, 1), "ms_per_step": round(dt * 1e3, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "K": w.K, "train": w.train},
+        "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"fp64 numpy oracle, routes of {len(experts)} of {w.E} experts per step "
+                                   f"({sroutes} routes, all {w.T} tokens)"},
+        "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

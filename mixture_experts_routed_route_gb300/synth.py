@@ -133,19 +133,23 @@ def make_grad_out(w: Workload, device="cpu", layer: int = 0):
     return make_tokens(w, device, layer, salt=5)
 
 
-def make_weights(w: Workload, device="cpu", layer: int = 0, E=None, F=None):
+def make_weights(w: Workload, device="cpu", layer: int = 0, E=None, F=None, experts=None):
     """W13 [E,2F,D] ~ N(0,1/D) and W2 [E,D,F] ~ N(0,1/F), BF16.
 
     Rows 0..F-1 of W13 are the gate projection, rows F..2F-1 the up
-    projection."""
+    projection.  Each expert has its own seed, so ``experts`` (a list of
+    expert indices) draws exactly those experts' weights of the full set."""
     E = w.E if E is None else E
     F = w.F if F is None else F
-    g = _gen(device, 20_000 * w.seed + 97 * layer + E + 3)
-    w13 = torch.empty((E, 2 * F, w.D), device=device, dtype=torch.bfloat16)
-    w2 = torch.empty((E, w.D, F), device=device, dtype=torch.bfloat16)
-    for e in range(E):     # per expert keeps the fp32 temporaries small
-        w13[e] = (torch.randn((2 * F, w.D), generator=g, device=device) * w.D ** -0.5).to(torch.bfloat16)
-        w2[e] = (torch.randn((w.D, F), generator=g, device=device) * F ** -0.5).to(torch.bfloat16)
+    experts = list(range(E)) if experts is None else list(experts)
+    n = len(experts)
+    w13 = torch.empty((n, 2 * F, w.D), device=device, dtype=torch.bfloat16)
+    w2 = torch.empty((n, w.D, F), device=device, dtype=torch.bfloat16)
+    g = torch.Generator(device=device)
+    for i, e in enumerate(experts):
+        g.manual_seed(20_000 * w.seed + 97 * layer + 1_000_003 * (E + 3) + 7919 * e)
+        w13[i] = (torch.randn((2 * F, w.D), generator=g, device=device) * w.D ** -0.5).to(torch.bfloat16)
+        w2[i] = (torch.randn((w.D, F), generator=g, device=device) * F ** -0.5).to(torch.bfloat16)
     return w13, w2
 
 
