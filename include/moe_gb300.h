@@ -291,6 +291,41 @@ MOE_API moe_status moe_ctx_stage_times(moe_ctx* ctx, int pass, float* ms, int n)
  * captured call counts once at capture time). */
 MOE_API uint64_t moe_ctx_launch_count(const moe_ctx* ctx);
 
+/*
+ * Allocation-free inference forward.  The pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory when
+ * they need the layer -- an inference engine that gives all free HBM to its
+ * KV cache at start-up, a plugin handed a stream but no allocator, or a
+ * latency-critical loop that must not call cudaMalloc because it can
+ * synchronise the whole device.  It runs the same kernels as an inference
+ * moe_forward (no saved state) without a context: every intermediate lives
+ * in one file-scope device array of MOE_STATIC_SCRATCH_BYTES, which every GPU
+ * that loads this library holds until the process exits.  It calls no
+ * cudaMalloc/cudaFree and no allocating library routine.
+ *   cfg         host struct: d_model, d_ff, num_experts, top_k, precision
+ *               (max_tokens and MOE_TRAINING are ignored; MOE_DEBUG_CHECKS
+ *               is honoured)
+ *   T, x, topk_ids, topk_scores, W13, W2, out, call_flags: as moe_forward
+ *   device_error_word  device uint32 that receives the MOE_DEV_ERR_* bits
+ *               (ORed in, never cleared here); NULL uses a word inside the
+ *               static array that each call clears and nobody reads.
+ * Returns MOE_ERR_CAPACITY when the call's buffers do not fit the array.
+ * They need about R*(D + F + 2D) bytes for MXFP8 (R*(2D + 2F + 2D) for BF16),
+ * with R = T*top_k + 31*num_experts rounded up to 128, plus 128, plus
+ * routing arrays of a few bytes per route.
+ * The first call on a device takes the array's device address
+ * (cudaGetSymbolAddress) and sets kernel attributes, so make it before any
+ * stream capture.  Every call shares the array and finds the previous call's
+ * contents there: calls that may overlap on the GPU race and must be
+ * ordered (one stream, or events) by the caller.
+ */
+#define MOE_STATIC_SCRATCH_BYTES (64ull << 20)
+MOE_API moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t T, const void* x,
+                                              const int32_t* topk_ids, const float* topk_scores,
+                                              const moe_weight* W13, const moe_weight* W2, void* out,
+                                              uint32_t call_flags, uint32_t* device_error_word,
+                                              cudaStream_t stream);
+
 /* Library version string. */
 MOE_API const char* moe_version(void);
 

@@ -92,7 +92,12 @@ _SIGNATURES = {
     "moe_ctx_enable_stage_timing": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_ctx_stage_times": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.c_int]),
     "moe_ctx_launch_count": (ctypes.c_uint64, [_P]),
+    "moe_forward_static_scratch": (ctypes.c_int, [ctypes.POINTER(moe_config), ctypes.c_int32, _P, _P, _P,
+                                                  ctypes.POINTER(moe_weight), ctypes.POINTER(moe_weight), _P,
+                                                  ctypes.c_uint32, _P, _P]),
 }
+
+MOE_STATIC_SCRATCH_BYTES = 64 << 20
 
 MOE_FWD_STAGES = 6
 MOE_BWD_STAGES = 7
@@ -218,6 +223,14 @@ def moe_ctx_stage_times(ctx, pass_):
 
 def moe_ctx_launch_count(ctx):
     return LIB.moe_ctx_launch_count(ctx)
+
+
+def moe_forward_static_scratch(cfg, T, x, topk_ids, topk_scores, W13, W2, out, call_flags=0,
+                               device_error_word=None, stream=None):
+    _check("moe_forward_static_scratch",
+           LIB.moe_forward_static_scratch(ctypes.byref(cfg), T, _ptr(x), _ptr(topk_ids), _ptr(topk_scores),
+                                          ctypes.byref(W13), ctypes.byref(W2), _ptr(out), call_flags,
+                                          _ptr(device_error_word), _stream(stream)))
 
 
 def moe_backward(ctx, saved, dout, W13, W2, dx, dW13, dW2, call_flags=0, stream=None):

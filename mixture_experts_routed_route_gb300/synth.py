@@ -20,6 +20,8 @@ Workloads (names used by tests and the benchmark):
   K=8, each layer Zipf(s ~ U[0.8, 1.5]) with its own seed.
 * ``e6_dense``    diagnostic: the e384 shapes with E=6, K=6, so every
   token visits every expert (2048 rows per expert).
+* ``profile_e24`` the e384 per-expert shape with 24 experts and T=128, a
+  small case for hardware-counter captures.
 
 Weights are N(0, 1/D) for W13 and N(0, 1/F) for W2, tokens and output
 gradients N(0, 1), all rounded to BF16.
@@ -61,6 +63,11 @@ WORKLOADS = {
     "ten_layer_graph": Workload("ten_layer_graph", 4096, 7168, 2048, 384, 8, "mxfp8",
                                 "zipf", train=True, layers=10, seed=5),
     "e6_dense": Workload("e6_dense", 2048, 7168, 2048, 6, 6, "mxfp8", "uniform", seed=6),
+    # profiling case: the e384 per-expert shape (about 32 rows per expert, D=7168,
+    # F=2048) with 24 experts, so a full ncu capture holds a few GB, while the
+    # weight gradients (1.4 GB for W13) still exceed L2
+    "profile_e24": Workload("profile_e24", 128, 7168, 2048, 24, 6, "mxfp8", "zipf", inactive_frac=0.10,
+                            zipf_s=1.2, train=True, seed=7),
 }
 
 
