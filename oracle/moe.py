@@ -178,12 +178,14 @@ def forward(x, ids, scores, w13, w2, precision, out_init=None, pad=PAD):
     h1 = np.zeros((Rp, 2 * F))
     h2 = np.zeros((Rp, F))
     h3 = np.zeros((Rp, D))
+    h1_exact = np.zeros((Rp, 2 * F))
     for e in range(E):
         a, b = rt.poffsets[e], rt.poffsets[e + 1]
         if a == b:
             continue
         w13e = prepare_weight(w13[e], precision)
-        h1[a:b] = _round_out(xq[a:b] @ w13e.T, precision)
+        h1_exact[a:b] = xq[a:b] @ w13e.T
+        h1[a:b] = _round_out(h1_exact[a:b], precision)
     g, u = h1[:, :F], h1[:, F:]
     h2 = silu(g) * u
     h2q = _q_row(h2, precision)
@@ -194,7 +196,7 @@ def forward(x, ids, scores, w13, w2, precision, out_init=None, pad=PAD):
         w2e = prepare_weight(w2[e], precision)
         h3[a:b] = _round_out(h2q[a:b] @ w2e.T, precision)
     out = combine(h3, rt.inv.reshape(T, K), scores, out_init, precision)
-    return dict(out=out, routing=rt, xg=xg, xq=xq, h1=h1, h2=h2, h2q=h2q,
+    return dict(out=out, routing=rt, xg=xg, xq=xq, h1=h1, h1_exact=h1_exact, h2=h2, h2q=h2q,
                 h3=h3, ids=np.asarray(ids), scores=np.asarray(scores, np.float32),
                 precision=precision, T=T, D=D, F=F, E=E, K=K)
 

@@ -95,3 +95,82 @@ def run_oracle(case, precision=None, out_init=None, dx_init=None, dw_fp32=False,
         g = moe.backward(st, to_f64(case.dy), w13, w2, dx_init=dx_init, dw_fp32=dw_fp32)
         res.update(dx=g["dX"], dW13=g["dW13"], dW2=g["dW2"], grads=g)
     return res
+
+
+# ------------------------------------------------------------------------
+# MXFP8 weight gradients: codes that two correct computations may round
+# differently.
+#
+# The WGRAD operands h2 and dh1 are quantised (along rows, 32-row blocks)
+# from values each side computes in its own precision: the GPU accumulates
+# the GEMM in FP32, the oracle exactly.  Where such a value lies within the
+# FP32 spread of a rounding decision (an E4M3 midpoint, a block-scale power
+# of two, or the BF16 rounding of the h1 it is built from), both codes are
+# correct, and one differing code moves a whole dW row by one E4M3 step.
+# The check below compares what is unique with the stated tolerance and
+# allows, on top of it, exactly the contribution of the undecided codes, all
+# derived from oracle values.  EPS_ACC = 3 sqrt(K) 2^-24 for K = 7168 (the
+# relative spread of an FP32 sum of K random-sign terms, three sigma).
+
+EPS_ACC = 2.0 ** -16
+
+
+def _bf16_candidates(v_exact, eps):
+    """BF16 rounding of each exact value, and the other neighbour where the
+    exact value lies within eps (relative) of a rounding midpoint."""
+    from oracle import formats as fm
+    r = fm.round_bf16(v_exact)
+    lo = fm.round_bf16(v_exact * (1 - eps))
+    hi = fm.round_bf16(v_exact * (1 + eps))
+    return r, np.where(lo != r, lo, np.where(hi != r, hi, r))
+
+
+def _mx_col_spread(cands, eps):
+    """Per element, the spread of the dequantised MXFP8 column-bundle value
+    over the admissible pre-quantisation values (each candidate scaled by
+    1 - eps, 1, 1 + eps); zero where the code is decided."""
+    from oracle import formats as fm
+    lo = hi = None
+    for c in cands:
+        for f in (1 - eps, 1.0, 1 + eps):
+            q = fm.mx_fake_quant(c * f, axis=0)
+            lo = q if lo is None else np.minimum(lo, q)
+            hi = q if hi is None else np.maximum(hi, q)
+    return hi - lo
+
+
+def check_mx_wgrad(dW13_gpu, dW2_gpu, state, grads, experts=None, tol=TOL["mxfp8"], max_undecided=5e-3):
+    """Assert dW13/dW2 of the listed experts (indices into the oracle's
+    expert axis; dW*_gpu indexed the same way) against the oracle with the
+    undecided-code allowance.  Returns the per-expert plain errors."""
+    from oracle import moe as omoe
+    rt = state["routing"]
+    F = state["F"]
+    experts = range(len(grads["dW13"])) if experts is None else experts
+    errs = []
+    for i in experts:
+        a, b = int(rt.poffsets[i]), int(rt.poffsets[i + 1])
+        ref13, ref2 = grads["dW13"][i], grads["dW2"][i]
+        got13, got2 = np.asarray(dW13_gpu[i], np.float64), np.asarray(dW2_gpu[i], np.float64)
+        if a == b:
+            assert np.all(got13 == 0) and np.all(got2 == 0)
+            errs.append((0.0, 0.0))
+            continue
+        h1x = state["h1_exact"][a:b]
+        g, ga = _bf16_candidates(h1x[:, :F], EPS_ACC)
+        u, ua = _bf16_candidates(h1x[:, F:], EPS_ACC)
+        dh2 = grads["dh2"][a:b]
+        combos = [(g, u), (ga, u), (g, ua), (ga, ua)]
+        dh1_c = [np.concatenate([dh2 * uu * omoe.silu_grad(gg), dh2 * omoe.silu(gg)], axis=1) for gg, uu in combos]
+        h2_c = [omoe.silu(gg) * uu for gg, uu in combos]
+        s13 = _mx_col_spread(dh1_c, EPS_ACC)
+        s2 = _mx_col_spread(h2_c, EPS_ACC)
+        assert (s13 > 0).mean() <= max_undecided and (s2 > 0).mean() <= max_undecided
+        allow13 = 2.0 * s13.T @ np.abs(grads["x_col"][a:b])
+        allow2 = 2.0 * np.abs(grads["dh3_col"][a:b]).T @ s2
+        for got, ref, allow, name in ((got13, ref13, allow13, "dW13"), (got2, ref2, allow2, "dW2")):
+            bound = tol * np.max(np.abs(ref)) + allow
+            bad = np.abs(got - ref) > bound
+            assert not bad.any(), (name, i, int(bad.sum()), rel_err(got, ref))
+        errs.append((rel_err(got13, ref13), rel_err(got2, ref2)))
+    return errs
