@@ -108,9 +108,10 @@ typedef struct {
  *   W2:  N = D,  K = F.
  * BF16:  data = the caller's BF16 tensor; scale = scale_t = NULL; data_t =
  *        BF16 [E, K, N] transposed copy (needed by moe_backward only).
- * MXFP8: data = E4M3 codes [E, N, K], scale = E8M0 [E, N, K/32];
- *        data_t = E4M3 codes [E, K, N], scale_t = E8M0 [E, K, N/32]
- *        (backward only).  Filled by prepare_block_scaled_weight.
+ * MXFP8: data = E4M3 codes [E, N, K], scale = E8M0 atoms [E*N/128][K/128];
+ *        data_t = E4M3 codes [E, K, N], scale_t = E8M0 atoms [E*K/128][N/128]
+ *        (backward only; both E*N*K/32 bytes, see the atom layout below).
+ *        N % 128 == 0 and K % 128 == 0.  Filled by prepare_block_scaled_weight.
  * The struct is read on the host at call time; the pointers are not owned.
  */
 typedef struct {
@@ -154,22 +155,43 @@ MOE_API size_t moe_ctx_scratch_bytes(const moe_config* cfg);
  */
 MOE_API size_t moe_saved_state_bytes(const moe_config* cfg);
 
-/* Saved-state fields, for inspection by tests (moe_saved_state_field). */
+/*
+ * Layout of every MXFP8 scale array (weights, row bundles, column bundles):
+ * 512-byte atoms, each holding the E8M0 scales of 128 operand rows x 4
+ * consecutive 32-value blocks along the contraction axis.  Row p (0..127) of
+ * the atom and block l (0..3) sit at byte (p % 32) * 16 + (p / 32) * 4 + l,
+ * the order in which tcgen05.cp 32x128b.warpx4 lays a row's scales into
+ * tensor memory, so a GEMM stage moves its scales with one bulk copy.
+ *   weight scale    atoms [E*N/128][K/128]   (rows = weight rows)
+ *   weight scale_t  atoms [E*K/128][N/128]
+ *   row bundles     atoms [B_cap][Kdim/128]  (rows = rows of routing block b,
+ *                   counted from the block's first row)
+ *   column bundles  atoms [Dim/128][B_cap]   (rows = features; block l = the
+ *                   32-row group l of routing block b)
+ * B_cap = (max_tokens*top_k + 31*E)/128 + E + 1 row blocks.
+ */
+
+/* Saved-state fields, for inspection by tests (moe_saved_state_field).  The
+ * routing fields come first in memory (HEADER..SCORES, BSTART, ROWBLOCK),
+ * then H1 and the column bundles. */
 typedef enum {
-  MOE_SAVED_HEADER = 0,     /* int32[16]: [0] T, [1] num_blocks, [2] rows used */
+  MOE_SAVED_HEADER = 0,     /* int32[16]: [0] T, [1] row blocks, [2] rows used, [3] active routes */
   MOE_SAVED_COUNTS = 1,     /* int32[E]     active routes per expert           */
   MOE_SAVED_OFFSETS = 2,    /* int32[E+1]   exclusive prefix of counts         */
   MOE_SAVED_POFFSETS = 3,   /* int32[E+1]   same with counts padded to 32      */
   MOE_SAVED_PERM = 4,       /* int32[R_cap] route t*K+k of each row, -1 = pad  */
   MOE_SAVED_INV = 5,        /* int32[T_max*K] row of each route, -1 = inactive */
-  MOE_SAVED_BLOCKS = 6,     /* int32[4*B_cap] (expert, first row, rows, 0)     */
+  MOE_SAVED_BLOCKS = 6,     /* int32[4*B_cap] (expert, first row, rows, 0): each
+                               expert's padded rows cut into blocks of <=128   */
   MOE_SAVED_SCORES = 7,     /* float[T_max*K] scores, 0 for inactive routes    */
   MOE_SAVED_H1 = 8,         /* bf16[R_cap, 2F]                                 */
   MOE_SAVED_XCOL = 9,       /* x column bundle: bf16 [D, R_cap] or e4m3 codes  */
-  MOE_SAVED_XCOL_SCALE = 10,/* e8m0 [D, R_cap/32] (MXFP8 only)                 */
+  MOE_SAVED_XCOL_SCALE = 10,/* e8m0 column-bundle atoms [D/128][B_cap] (MXFP8) */
   MOE_SAVED_H2COL = 11,     /* h2 column bundle: bf16 [F, R_cap] or e4m3       */
-  MOE_SAVED_H2COL_SCALE = 12,/* e8m0 [F, R_cap/32] (MXFP8 only)                */
-  MOE_SAVED_NUM_FIELDS = 13
+  MOE_SAVED_H2COL_SCALE = 12,/* e8m0 column-bundle atoms [F/128][B_cap]        */
+  MOE_SAVED_BSTART = 13,    /* int32[E+1]   first row block of each expert     */
+  MOE_SAVED_ROWBLOCK = 14,  /* int32[R_cap/32] row block of each 32-row group  */
+  MOE_SAVED_NUM_FIELDS = 15
 } moe_saved_field;
 
 /* Offset and size in bytes of one saved-state field; the row capacity
@@ -177,7 +199,7 @@ typedef enum {
 MOE_API moe_status moe_saved_state_field(const moe_config* cfg, int field, size_t* offset, size_t* bytes);
 
 /* R_cap: rows of every per-route buffer = max_tokens*top_k + 31*E rounded
- * up to a multiple of 128 (0 for an invalid config). */
+ * up to a multiple of 128, plus 128 (0 for an invalid config). */
 MOE_API int64_t moe_row_capacity(const moe_config* cfg);
 
 /*
@@ -186,12 +208,13 @@ MOE_API int64_t moe_row_capacity(const moe_config* cfg);
  * weights once with 32x32 blocks for MXFP8 training; [DM] section 02: with
  * 32x32 blocks the forward and input-gradient GEMMs share qdata with
  * distinct scale orientations).
- *   w       BF16 [E, N, K] (device).  N % 32 == 0 and K % 32 == 0.
+ *   w       BF16 [E, N, K] (device).  N % 32 == 0 and K % 32 == 0 (BF16),
+ *           N % 128 == 0 and K % 128 == 0 (MXFP8).
  *   MXFP8:  one E8M0 scale per 32x32 tile (OCP MX rule: floor(log2 amax) - 8,
  *           values rounded to nearest-even E4M3 and saturated at 448) is
- *           written to scale [E,N,K/32] and, when data_t != NULL, the
- *           transposed codes to data_t [E,K,N] with scale_t [E,K,N/32].
- *           data may not be NULL.
+ *           written to the scale atoms [E*N/128][K/128] and, when
+ *           data_t != NULL, the transposed codes to data_t [E,K,N] with
+ *           scale atoms [E*K/128][N/128] in scale_t.  data may not be NULL.
  *   BF16:   data and scale must be NULL; data_t (BF16 [E,K,N]) receives the
  *           transpose used by the input-gradient GEMMs.
  * The outputs are caller-owned device buffers.  Enqueued on `stream`.
@@ -248,18 +271,18 @@ MOE_API moe_status moe_debug_copy_to_host(void* host_dst, const void* dev_src, s
 /* Scratch regions of a context, for inspection by tests. */
 typedef enum {
   MOE_BUF_XROW = 0,        /* gathered x row bundle: bf16 [R_cap, D] or e4m3  */
-  MOE_BUF_XROW_SCALE = 1,  /* e8m0 [R_cap, D/32]                               */
+  MOE_BUF_XROW_SCALE = 1,  /* e8m0 row-bundle atoms [B_cap][D/128]             */
   MOE_BUF_H2ROW = 2,       /* h2 row bundle: bf16 [R_cap, F] or e4m3           */
-  MOE_BUF_H2ROW_SCALE = 3, /* e8m0 [R_cap, F/32]                               */
+  MOE_BUF_H2ROW_SCALE = 3, /* e8m0 row-bundle atoms [B_cap][F/128]             */
   MOE_BUF_H3 = 4,          /* bf16 [R_cap, D]                                  */
   MOE_BUF_DH3ROW = 5,      /* bf16 [R_cap, D] or e4m3                          */
-  MOE_BUF_DH3ROW_SCALE = 6,
+  MOE_BUF_DH3ROW_SCALE = 6,/* e8m0 row-bundle atoms [B_cap][D/128]            */
   MOE_BUF_DH3COL = 7,      /* bf16 [D, R_cap] or e4m3                          */
-  MOE_BUF_DH3COL_SCALE = 8,/* e8m0 [D, R_cap/32]                               */
+  MOE_BUF_DH3COL_SCALE = 8,/* e8m0 column-bundle atoms [D/128][B_cap]         */
   MOE_BUF_DH1ROW = 9,      /* bf16 [R_cap, 2F] or e4m3                         */
-  MOE_BUF_DH1ROW_SCALE = 10,
+  MOE_BUF_DH1ROW_SCALE = 10,/* e8m0 row-bundle atoms [B_cap][2F/128]          */
   MOE_BUF_DH1COL = 11,     /* bf16 [2F, R_cap] or e4m3                         */
-  MOE_BUF_DH1COL_SCALE = 12,
+  MOE_BUF_DH1COL_SCALE = 12,/* e8m0 column-bundle atoms [2F/128][B_cap]       */
   MOE_BUF_DXR = 13,        /* bf16 [R_cap, D]                                  */
   MOE_BUF_ROUTING = 14,    /* inference routing state (same layout as saved)   */
   MOE_BUF_ERROR = 15,      /* uint32 error word                                */

@@ -41,8 +41,8 @@ MOE_DW_ACCUMULATE = 0x4
 # moe_saved_field
 (MOE_SAVED_HEADER, MOE_SAVED_COUNTS, MOE_SAVED_OFFSETS, MOE_SAVED_POFFSETS, MOE_SAVED_PERM, MOE_SAVED_INV,
  MOE_SAVED_BLOCKS, MOE_SAVED_SCORES, MOE_SAVED_H1, MOE_SAVED_XCOL, MOE_SAVED_XCOL_SCALE, MOE_SAVED_H2COL,
- MOE_SAVED_H2COL_SCALE) = range(13)
-MOE_SAVED_NUM_FIELDS = 13
+ MOE_SAVED_H2COL_SCALE, MOE_SAVED_BSTART, MOE_SAVED_ROWBLOCK) = range(15)
+MOE_SAVED_NUM_FIELDS = 15
 
 # moe_buffer
 (MOE_BUF_XROW, MOE_BUF_XROW_SCALE, MOE_BUF_H2ROW, MOE_BUF_H2ROW_SCALE, MOE_BUF_H3, MOE_BUF_DH3ROW,

@@ -85,17 +85,25 @@ SavedLayout saved_layout(const moe_config* c) {
   sz[MOE_SAVED_INV] = TK * sizeof(int);
   sz[MOE_SAVED_BLOCKS] = B * 4 * sizeof(int);
   sz[MOE_SAVED_SCORES] = TK * sizeof(float);
+  sz[MOE_SAVED_BSTART] = (E + 1) * sizeof(int);
+  sz[MOE_SAVED_ROWBLOCK] = (R / 32) * sizeof(int);
   sz[MOE_SAVED_H1] = R * 2 * F * 2;
   sz[MOE_SAVED_XCOL] = D * R * esz;
-  sz[MOE_SAVED_XCOL_SCALE] = mx ? D * (R / 32) + kAlign : 0;
+  sz[MOE_SAVED_XCOL_SCALE] = mx ? (D / 128) * B * 512 : 0;
   sz[MOE_SAVED_H2COL] = F * R * esz;
-  sz[MOE_SAVED_H2COL_SCALE] = mx ? F * (R / 32) + kAlign : 0;
+  sz[MOE_SAVED_H2COL_SCALE] = mx ? (F / 128) * B * 512 : 0;
+  // routing fields first (the inference copy in the context holds just these)
+  static const int order[MOE_SAVED_NUM_FIELDS] = {
+      MOE_SAVED_HEADER, MOE_SAVED_COUNTS, MOE_SAVED_OFFSETS, MOE_SAVED_POFFSETS, MOE_SAVED_PERM,
+      MOE_SAVED_INV,    MOE_SAVED_BLOCKS, MOE_SAVED_SCORES,  MOE_SAVED_BSTART,   MOE_SAVED_ROWBLOCK,
+      MOE_SAVED_H1,     MOE_SAVED_XCOL,   MOE_SAVED_XCOL_SCALE, MOE_SAVED_H2COL, MOE_SAVED_H2COL_SCALE};
   size_t off = 0;
-  for (int i = 0; i < MOE_SAVED_NUM_FIELDS; ++i) {
+  for (int k = 0; k < MOE_SAVED_NUM_FIELDS; ++k) {
+    const int i = order[k];
     L.off[i] = off;
     L.size[i] = sz[i];
     off += align_up(sz[i], kAlign);
-    if (i == MOE_SAVED_SCORES) L.routing_bytes = off;
+    if (i == MOE_SAVED_ROWBLOCK) L.routing_bytes = off;
   }
   L.total = off;
   return L;
@@ -109,26 +117,26 @@ struct ScratchLayout {
 
 ScratchLayout scratch_layout(const moe_config* c) {
   ScratchLayout L{};
-  const int64_t R = row_cap(c);
+  const int64_t R = row_cap(c), B = block_cap(c);
   const int64_t D = c->d_model, F = c->d_ff;
   const bool mx = c->precision == MOE_MXFP8;
   const bool train = (c->flags & MOE_TRAINING) != 0;
   const size_t esz = mx ? 1 : 2;
   size_t sz[MOE_BUF_NUM] = {};
   sz[MOE_BUF_XROW] = R * D * esz;
-  sz[MOE_BUF_XROW_SCALE] = mx ? R * (D / 32) + kAlign : 0;
+  sz[MOE_BUF_XROW_SCALE] = mx ? B * (D / 128) * 512 : 0;
   sz[MOE_BUF_H2ROW] = R * F * esz;
-  sz[MOE_BUF_H2ROW_SCALE] = mx ? R * (F / 32) + kAlign : 0;
+  sz[MOE_BUF_H2ROW_SCALE] = mx ? B * (F / 128) * 512 : 0;
   sz[MOE_BUF_H3] = R * D * 2;
   if (train) {
     sz[MOE_BUF_DH3ROW] = R * D * esz;
-    sz[MOE_BUF_DH3ROW_SCALE] = mx ? R * (D / 32) + kAlign : 0;
+    sz[MOE_BUF_DH3ROW_SCALE] = mx ? B * (D / 128) * 512 : 0;
     sz[MOE_BUF_DH3COL] = D * R * esz;
-    sz[MOE_BUF_DH3COL_SCALE] = mx ? D * (R / 32) + kAlign : 0;
+    sz[MOE_BUF_DH3COL_SCALE] = mx ? (D / 128) * B * 512 : 0;
     sz[MOE_BUF_DH1ROW] = R * 2 * F * esz;
-    sz[MOE_BUF_DH1ROW_SCALE] = mx ? R * (2 * F / 32) + kAlign : 0;
+    sz[MOE_BUF_DH1ROW_SCALE] = mx ? B * (2 * F / 128) * 512 : 0;
     sz[MOE_BUF_DH1COL] = 2 * F * R * esz;
-    sz[MOE_BUF_DH1COL_SCALE] = mx ? 2 * F * (R / 32) + kAlign : 0;
+    sz[MOE_BUF_DH1COL_SCALE] = mx ? (2 * F / 128) * B * 512 : 0;
     sz[MOE_BUF_DXR] = R * D * 2;
   }
   sz[MOE_BUF_ROUTING] = saved_layout(c).routing_bytes;
@@ -153,6 +161,8 @@ RoutingPtrs routing_ptrs(uint8_t* base, const SavedLayout& L) {
   r.inv = reinterpret_cast<int*>(base + L.off[MOE_SAVED_INV]);
   r.blocks = reinterpret_cast<int4*>(base + L.off[MOE_SAVED_BLOCKS]);
   r.scores = reinterpret_cast<float*>(base + L.off[MOE_SAVED_SCORES]);
+  r.bstart = reinterpret_cast<int*>(base + L.off[MOE_SAVED_BSTART]);
+  r.row_block = reinterpret_cast<int*>(base + L.off[MOE_SAVED_ROWBLOCK]);
   return r;
 }
 
@@ -189,6 +199,20 @@ bool make_tmap(CUtensorMap* tm, const void* base, bool mx, int64_t rows, int64_t
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Output map of a BF16 weight gradient [rows, cols]: boxes of 64 columns
+// (128 bytes) x 128 rows in the 128-byte swizzle the epilogue stages.
+bool make_out_tmap(CUtensorMap* tm, void* base, int64_t rows, int64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -339,7 +363,7 @@ moe_status prepare_block_scaled_weight(const void* w, int32_t E, int32_t N, int3
                                        cudaStream_t stream) {
   if (!w || !aligned16(w) || E < 1 || N < 32 || K < 32 || N % 32 || K % 32) return MOE_ERR_INVALID_ARG;
   if (precision == MOE_MXFP8) {
-    if (!data || !scale || !aligned16(data)) return MOE_ERR_INVALID_ARG;
+    if (N % 128 || K % 128 || !data || !scale || !aligned16(data)) return MOE_ERR_INVALID_ARG;
     if ((data_t == nullptr) != (scale_t == nullptr)) return MOE_ERR_INVALID_ARG;
     if (data_t && !aligned16(data_t)) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_prep_mx_weight(w, E, N, K, static_cast<uint8_t*>(data), scale,
@@ -387,7 +411,8 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   MOE_TRY(stage_mark(ctx, 0, 2, stream));
   if (train) {
     MOE_TRY(launch_gather_cols(mx, false, x, D, K, rp, sv + SL.off[MOE_SAVED_XCOL],
-                               mx ? sv + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr, static_cast<int>(R), stream));
+                               mx ? sv + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr, static_cast<int>(R),
+                               static_cast<int>(ctx->b_cap), stream));
     ctx->launches += 1;
   }
   MOE_TRY(stage_mark(ctx, 0, 3, stream));
@@ -411,18 +436,18 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   p1.a_rows_per_expert = 2 * F;
   p1.a_up_offset = F;
   p1.sfa = W13->scale;
-  p1.sfa_pitch = D / 32;
+  p1.sfa_ts = D / 128;
   p1.sfb = B(ctx, MOE_BUF_XROW_SCALE);
-  p1.sfb_pitch = D / 32;
+  p1.sfb_ts = D / 128;
   p1.out0 = B(ctx, MOE_BUF_H2ROW);
   p1.out0_pitch = F;
   p1.out0_sf = B(ctx, MOE_BUF_H2ROW_SCALE);
-  p1.out0_sf_pitch = F / 32;
+  p1.out0_sf_kg = F / 128;
+  p1.b_cap = static_cast<int>(ctx->b_cap);
   if (train) {
     p1.out1 = sv + SL.off[MOE_SAVED_H2COL];
     p1.out1_pitch = R;
     p1.out1_sf = mx ? sv + SL.off[MOE_SAVED_H2COL_SCALE] : nullptr;
-    p1.out1_sf_pitch = R / 32;
     p1.h1 = reinterpret_cast<__nv_bfloat16*>(sv + SL.off[MOE_SAVED_H1]);
     p1.h1_pitch = 2 * F;
   }
@@ -453,9 +478,9 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   p2.K = F;
   p2.a_rows_per_expert = D;
   p2.sfa = W2->scale;
-  p2.sfa_pitch = F / 32;
+  p2.sfa_ts = F / 128;
   p2.sfb = B(ctx, MOE_BUF_H2ROW_SCALE);
-  p2.sfb_pitch = F / 32;
+  p2.sfb_ts = F / 128;
   p2.out0 = B(ctx, MOE_BUF_H3);
   p2.out0_pitch = D;
   p2.F = F;
@@ -502,7 +527,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 1, 1, stream));
   MOE_TRY(launch_gather_cols(mx, true, dout, D, K, rp, B(ctx, MOE_BUF_DH3COL), B(ctx, MOE_BUF_DH3COL_SCALE),
-                             static_cast<int>(R), stream));
+                             static_cast<int>(R), static_cast<int>(ctx->b_cap), stream));
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 1, 2, stream));
 
@@ -524,19 +549,19 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p1.K = D;
   p1.a_rows_per_expert = F;
   p1.sfa = W2->scale_t;
-  p1.sfa_pitch = D / 32;
+  p1.sfa_ts = D / 128;
   p1.sfb = B(ctx, MOE_BUF_DH3ROW_SCALE);
-  p1.sfb_pitch = D / 32;
+  p1.sfb_ts = D / 128;
   p1.h1 = reinterpret_cast<__nv_bfloat16*>(sv + SL.off[MOE_SAVED_H1]);
   p1.h1_pitch = 2 * F;
   p1.out0 = B(ctx, MOE_BUF_DH1ROW);
   p1.out0_pitch = 2 * F;
   p1.out0_sf = B(ctx, MOE_BUF_DH1ROW_SCALE);
-  p1.out0_sf_pitch = 2 * F / 32;
+  p1.out0_sf_kg = 2 * F / 128;
   p1.out1 = B(ctx, MOE_BUF_DH1COL);
   p1.out1_pitch = R;
   p1.out1_sf = B(ctx, MOE_BUF_DH1COL_SCALE);
-  p1.out1_sf_pitch = R / 32;
+  p1.b_cap = static_cast<int>(ctx->b_cap);
   p1.F = F;
   p1.err = ctx->err;
   g1.max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
@@ -560,14 +585,17 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p2.E = E;
   p2.m_tiles = D / 128;
   p2.n_tiles = F / 128;
+  p2.bstart = rp.bstart;
   p2.sfa = B(ctx, MOE_BUF_DH3COL_SCALE);
-  p2.sfa_pitch = R / 32;
+  p2.sfa_ts = ctx->b_cap;
   p2.sfb = mx ? sv + SL.off[MOE_SAVED_H2COL_SCALE] : nullptr;
-  p2.sfb_pitch = R / 32;
+  p2.sfb_ts = ctx->b_cap;
   p2.out0 = dW2;
   p2.out0_pitch = F;
   p2.dw_fp32 = dw_fp32;
   p2.dw_accum = dw_acc;
+  p2.tma_store = (!dw_fp32 && !dw_acc) ? 1 : 0;
+  if (p2.tma_store && !make_out_tmap(&g2.tmC, dW2, static_cast<int64_t>(E) * D, F)) return MOE_ERR_CUDA;
   p2.err = ctx->err;
   g2.max_tiles = E * (D / 128) * (F / 128);
   MOE_TRY(launch_gemm(g2, sms, stream));
@@ -592,9 +620,9 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p3.K = 2 * F;
   p3.a_rows_per_expert = D;
   p3.sfa = W13->scale_t;
-  p3.sfa_pitch = 2 * F / 32;
+  p3.sfa_ts = 2 * F / 128;
   p3.sfb = B(ctx, MOE_BUF_DH1ROW_SCALE);
-  p3.sfb_pitch = 2 * F / 32;
+  p3.sfb_ts = 2 * F / 128;
   p3.out0 = B(ctx, MOE_BUF_DXR);
   p3.out0_pitch = D;
   p3.F = F;
@@ -620,14 +648,17 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p4.E = E;
   p4.m_tiles = 2 * F / 128;
   p4.n_tiles = D / 128;
+  p4.bstart = rp.bstart;
   p4.sfa = B(ctx, MOE_BUF_DH1COL_SCALE);
-  p4.sfa_pitch = R / 32;
+  p4.sfa_ts = ctx->b_cap;
   p4.sfb = mx ? sv + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr;
-  p4.sfb_pitch = R / 32;
+  p4.sfb_ts = ctx->b_cap;
   p4.out0 = dW13;
   p4.out0_pitch = D;
   p4.dw_fp32 = dw_fp32;
   p4.dw_accum = dw_acc;
+  p4.tma_store = (!dw_fp32 && !dw_acc) ? 1 : 0;
+  if (p4.tma_store && !make_out_tmap(&g4.tmC, dW13, static_cast<int64_t>(E) * 2 * F, D)) return MOE_ERR_CUDA;
   p4.err = ctx->err;
   g4.max_tiles = E * (2 * F / 128) * (D / 128);
   MOE_TRY(launch_gemm(g4, sms, stream));

@@ -38,7 +38,9 @@ template <bool MX, bool SCALE>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ src, int D, int K,
                                                           const int* __restrict__ hdr, const int* __restrict__ perm,
                                                           const float* __restrict__ scores, void* __restrict__ dst,
-                                                          uint8_t* __restrict__ dst_sf) {
+                                                          uint8_t* __restrict__ dst_sf,
+                                                          const int* __restrict__ row_block,
+                                                          const int4* __restrict__ blocks) {
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
   const int rows = hdr[2];
@@ -46,6 +48,14 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
     const int route = perm[r];
     const __nv_bfloat16* srow = nullptr;
     float s = 1.0f;
+    // scale atoms of this row: routing block b, row p within it
+    long long atom_row = 0;
+    int p = 0;
+    if (MX) {
+      const int b = row_block[r >> 5];
+      p = r - blocks[b].y;
+      atom_row = static_cast<long long>(b) * (D / 128);
+    }
     if (route >= 0) {
       srow = src + static_cast<long long>(route / K) * D;
       if (SCALE) s = scores[route];
@@ -83,7 +93,10 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
         q.y = cvt_e4m3x2(v[4] * inv, v[5] * inv) | (cvt_e4m3x2(v[6] * inv, v[7] * inv) << 16);
         if (act) {
           *reinterpret_cast<uint2*>(static_cast<uint8_t*>(dst) + static_cast<long long>(r) * D + c) = q;
-          if ((lane & 3) == 0) dst_sf[static_cast<long long>(r) * (D / 32) + c / 32] = static_cast<uint8_t>(e + 127);
+          if ((lane & 3) == 0) {
+            const int kb = c >> 5;
+            dst_sf[(atom_row + (kb >> 2)) * 512 + sf_atom_byte(p, kb & 3)] = static_cast<uint8_t>(e + 127);
+          }
         }
       }
     }
@@ -97,7 +110,9 @@ template <bool MX, bool SCALE>
 __global__ void __launch_bounds__(256) gather_cols_kernel(const __nv_bfloat16* __restrict__ src, int D, int K,
                                                           const int* __restrict__ hdr, const int* __restrict__ perm,
                                                           const float* __restrict__ scores, void* __restrict__ dstT,
-                                                          uint8_t* __restrict__ dstT_sf, int r_cap) {
+                                                          uint8_t* __restrict__ dstT_sf, int r_cap, int b_cap,
+                                                          const int* __restrict__ row_block,
+                                                          const int4* __restrict__ blocks) {
   __shared__ float tile[32][257];
   const int rows = hdr[2];
   const int c0 = blockIdx.x * 256;
@@ -148,11 +163,133 @@ __global__ void __launch_bounds__(256) gather_cols_kernel(const __nv_bfloat16* _
         uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dstT) + static_cast<long long>(d) * r_cap + r0);
         o[0] = make_uint4(w[0], w[1], w[2], w[3]);
         o[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        dstT_sf[static_cast<long long>(d) * (r_cap / 32) + rg] = static_cast<uint8_t>(e + 127);
+        const int b = row_block[rg];
+        const int l = rg - (blocks[b].y >> 5);
+        dstT_sf[(static_cast<long long>(d >> 7) * b_cap + b) * 512 + sf_atom_byte(d & 127, l)] =
+            static_cast<uint8_t>(e + 127);
       }
     }
     __syncthreads();
   }
+}
+
+// Both bundles in one pass (training): one CTA per (32-row group, 256-column
+// slab) loads the gathered rows into shared memory once, then writes the row
+// bundle (warp w: rows 4w..4w+3, lane l: columns 8l..8l+7, 4 lanes per MX
+// block) and the transposed column bundle (thread d: one column, 32 rows).
+template <bool MX, bool SCALE>
+__global__ void __launch_bounds__(256) gather_both_kernel(const __nv_bfloat16* __restrict__ src, int D, int K,
+                                                          const int* __restrict__ hdr, const int* __restrict__ perm,
+                                                          const float* __restrict__ scores, void* __restrict__ dst,
+                                                          uint8_t* __restrict__ dst_sf, void* __restrict__ dstT,
+                                                          uint8_t* __restrict__ dstT_sf, int r_cap, int b_cap,
+                                                          const int* __restrict__ row_block,
+                                                          const int4* __restrict__ blocks) {
+  __shared__ float tile[32][257];
+  const int rows = hdr[2];
+  const int c0 = blockIdx.x * 256;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int rg = blockIdx.y; rg * 32 < rows; rg += gridDim.y) {
+    const int r0 = rg * 32;
+    const int b = MX ? row_block[rg] : 0;
+    const int p0 = MX ? r0 - blocks[b].y : 0;   // first row of the group within its block
+    for (int i = tid; i < 32 * 32; i += 256) {
+      const int row = i >> 5, chunk = i & 31;
+      const int c = c0 + chunk * 8;
+      float v[8];
+      const int route = perm[r0 + row];
+      if (route >= 0 && c < D) {
+        unpack8(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(route / K) * D + c)), v);
+        if (SCALE) {
+          const float s = scores[route];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = s * v[j];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tile[row][chunk * 8 + j] = v[j];
+    }
+    __syncthreads();
+    // ---- row bundle
+    const int c = c0 + lane * 8;
+    for (int rr = 0; rr < 4; ++rr) {
+      const int row = warp * 4 + rr;
+      const long long r = r0 + row;
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = tile[row][lane * 8 + j];
+      if (!MX) {
+        if (c < D)
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + r * D + c) =
+              make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                         pack_bf16x2(v[6], v[7]));
+      } else {
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        const int e = mx_shared_exp(amax);
+        const float inv = exp2_int(-e);
+        uint2 q;
+        q.x = cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
+        q.y = cvt_e4m3x2(v[4] * inv, v[5] * inv) | (cvt_e4m3x2(v[6] * inv, v[7] * inv) << 16);
+        if (c < D) {
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(dst) + r * D + c) = q;
+          if ((lane & 3) == 0) {
+            const int kb = c >> 5;
+            dst_sf[(static_cast<long long>(b) * (D / 128) + (kb >> 2)) * 512 + sf_atom_byte(p0 + row, kb & 3)] =
+                static_cast<uint8_t>(e + 127);
+          }
+        }
+      }
+    }
+    // ---- column bundle
+    const int d = c0 + tid;
+    if (d < D) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = tile[i][tid];
+      if (!MX) {
+        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dstT) + static_cast<long long>(d) * r_cap + r0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          o[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+      } else {
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const int e = mx_shared_exp(amax);
+        const float inv = exp2_int(-e);
+        uint32_t w[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
+        uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dstT) + static_cast<long long>(d) * r_cap + r0);
+        o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        dstT_sf[(static_cast<long long>(d >> 7) * b_cap + b) * 512 + sf_atom_byte(d & 127, p0 >> 5)] =
+            static_cast<uint8_t>(e + 127);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <bool MX, bool SCALE>
+cudaError_t both_impl(const void* src, int D, int K, const RoutingPtrs& rp, void* dst, uint8_t* dst_sf, void* dstT,
+                      uint8_t* dstT_sf, int r_cap, int b_cap, int num_sms, cudaStream_t stream) {
+  const int xs = (D + 255) / 256;
+  const int ys = max(1, min(r_cap / 32, (num_sms * 8 + xs - 1) / xs));
+  dim3 grid(xs, ys);
+  gather_both_kernel<MX, SCALE><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr,
+                                                          rp.perm, rp.scores, dst, dst_sf, dstT, dstT_sf, r_cap,
+                                                          b_cap, rp.row_block, rp.blocks);
+  return cudaGetLastError();
 }
 
 template <bool MX, bool SCALE>
@@ -162,16 +299,18 @@ cudaError_t rows_impl(const void* src, int D, int K, const RoutingPtrs& rp, void
   int blocks = (warps_needed + 7) / 8;
   blocks = min(blocks, num_sms * 8);
   gather_rows_kernel<MX, SCALE><<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr,
-                                                            rp.perm, rp.scores, dst, dst_sf);
+                                                            rp.perm, rp.scores, dst, dst_sf, rp.row_block,
+                                                            rp.blocks);
   return cudaGetLastError();
 }
 
 template <bool MX, bool SCALE>
 cudaError_t cols_impl(const void* src, int D, int K, const RoutingPtrs& rp, void* dstT, uint8_t* dstT_sf, int r_cap,
-                      cudaStream_t stream) {
+                      int b_cap, cudaStream_t stream) {
   dim3 grid((D + 255) / 256, r_cap / 32);
   gather_cols_kernel<MX, SCALE><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr,
-                                                          rp.perm, rp.scores, dstT, dstT_sf, r_cap);
+                                                          rp.perm, rp.scores, dstT, dstT_sf, r_cap, b_cap,
+                                                          rp.row_block, rp.blocks);
   return cudaGetLastError();
 }
 
@@ -188,13 +327,24 @@ cudaError_t launch_gather_rows(bool mx, bool use_scores, const void* src, int D,
 }
 
 cudaError_t launch_gather_cols(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
-                               void* dstT, uint8_t* dstT_sf, int r_cap, cudaStream_t stream) {
+                               void* dstT, uint8_t* dstT_sf, int r_cap, int b_cap, cudaStream_t stream) {
   if (mx) {
-    return use_scores ? cols_impl<true, true>(src, D, K, rp, dstT, dstT_sf, r_cap, stream)
-                      : cols_impl<true, false>(src, D, K, rp, dstT, dstT_sf, r_cap, stream);
+    return use_scores ? cols_impl<true, true>(src, D, K, rp, dstT, dstT_sf, r_cap, b_cap, stream)
+                      : cols_impl<true, false>(src, D, K, rp, dstT, dstT_sf, r_cap, b_cap, stream);
   }
-  return use_scores ? cols_impl<false, true>(src, D, K, rp, dstT, dstT_sf, r_cap, stream)
-                    : cols_impl<false, false>(src, D, K, rp, dstT, dstT_sf, r_cap, stream);
+  return use_scores ? cols_impl<false, true>(src, D, K, rp, dstT, dstT_sf, r_cap, b_cap, stream)
+                    : cols_impl<false, false>(src, D, K, rp, dstT, dstT_sf, r_cap, b_cap, stream);
+}
+
+cudaError_t launch_gather_both(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
+                               void* dst, uint8_t* dst_sf, void* dstT, uint8_t* dstT_sf, int r_cap, int b_cap,
+                               int num_sms, cudaStream_t stream) {
+  if (mx) {
+    return use_scores ? both_impl<true, true>(src, D, K, rp, dst, dst_sf, dstT, dstT_sf, r_cap, b_cap, num_sms, stream)
+                      : both_impl<true, false>(src, D, K, rp, dst, dst_sf, dstT, dstT_sf, r_cap, b_cap, num_sms, stream);
+  }
+  return use_scores ? both_impl<false, true>(src, D, K, rp, dst, dst_sf, dstT, dstT_sf, r_cap, b_cap, num_sms, stream)
+                    : both_impl<false, false>(src, D, K, rp, dst, dst_sf, dstT, dstT_sf, r_cap, b_cap, num_sms, stream);
 }
 
 }  // namespace moe

@@ -12,25 +12,30 @@
 //
 // Two ways of walking the experts:
 //  * grouped-M (forward W13 and W2, input-gradient DGRAD): the weight is the
-//    A operand (128 output features per tile, M = 128) and the expert's token
-//    rows are the B operand (N = the row block's 32..128 rows).  Experts get
-//    only ~32 rows at the 384-expert shape, so putting weights on the
-//    128-wide M side keeps the MMA from computing padding and reads each
-//    weight tile once per row block.
+//    A operand (128 output features per tile, M = 128) and one routing row
+//    block of the expert (32..128 rows) is the B operand (N = its rows).
+//    Experts get only ~32 rows at the 384-expert shape, so putting weights
+//    on the 128-wide M side keeps the MMA from computing padding and reads
+//    each weight tile once per row block.
 //  * grouped-K (WGRAD): dW_e[m, n] = sum over the expert's rows of
 //    colA[m, r] colB[n, r]; both operands are column bundles stored
 //    [features, rows], so the contraction runs over the expert's row range.
 //
+// MXFP8 scales travel with the operand tiles: the TMA producer bulk-copies
+// one 512-byte scale atom per operand per stage into the stage's shared
+// memory, and the MMA thread moves it to tensor memory with tcgen05.cp ahead
+// of the block-scaled MMAs (same thread, so the tensor pipe keeps the order).
+//
 // Epilogues: fused SwiGLU forward (h1 -> h2 row/column bundles), plain BF16
 // store (h3, input-gradient rows), fused SwiGLU backward (dh2 -> dh1 row and
-// column bundles) and weight-gradient store (BF16/FP32, optional add).
+// column bundles) and weight-gradient store (BF16 through shared memory and
+// TMA; FP32 or accumulate with plain stores).
 //
 // Warp roles (one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (one thread)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2-5   epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
-//   warps 6-9   MXFP8 only: load the E8M0 scales of each stage and write
-//               them to tensor memory with tcgen05.st
+//   warps 2-9   epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and the
+//               32-column chunks 2i + (w-2)/4 of the accumulator
 #include "kernels.cuh"
 
 namespace moe {
@@ -39,9 +44,14 @@ namespace {
 
 constexpr int kABytes = 128 * 128;  // one 128-row x 128-byte operand tile
 constexpr int kBBytes = 128 * 128;
+constexpr int kAtom = 512;          // one scale atom
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kEpiBarrier = 1;      // named barrier of the epilogue warps
 
 struct Tile {
   int e;
+  int blk;       // grouped-M: routing row block
   int a_row[2];
   int b_row0;
   int b_rows;    // rows of B = MMA N
@@ -50,6 +60,8 @@ struct Tile {
   int klast;     // contraction elements of the last stage
   int out_row0;
   int out_col0;
+  long long sfa_atom[2];  // atom index of stage 0 for each A tile
+  long long sfb_atom;     // atom index of stage 0 for B
 };
 
 template <int MODE, int BK>
@@ -59,6 +71,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int n
     const int n = tile / nblk, b = tile - n * nblk;
     const int4 blk = p.blocks[b];
     t.e = blk.x;
+    t.blk = b;
     t.a_row[0] = blk.x * p.a_rows_per_expert + n * 128;
     t.a_row[1] = t.a_row[0] + p.a_up_offset;
     t.b_row0 = blk.y;
@@ -68,12 +81,16 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int n
     t.klast = BK;
     t.out_row0 = blk.y;
     t.out_col0 = n * 128;
+    t.sfa_atom[0] = static_cast<long long>(t.a_row[0] >> 7) * p.sfa_ts;
+    t.sfa_atom[1] = static_cast<long long>(t.a_row[1] >> 7) * p.sfa_ts;
+    t.sfb_atom = static_cast<long long>(b) * p.sfb_ts;
   } else {
     const int per_e = p.m_tiles * p.n_tiles;
     const int e = tile / per_e, rem = tile - e * per_e;
     const int m = rem / p.n_tiles, n = rem - m * p.n_tiles;
     const int k0 = p.poffsets[e], klen = p.poffsets[e + 1] - k0;
     t.e = e;
+    t.blk = 0;
     t.a_row[0] = m * 128;
     t.a_row[1] = 0;
     t.b_row0 = n * 128;
@@ -83,18 +100,12 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int n
     t.klast = klen - (t.kstages - 1) * BK;
     t.out_row0 = m * 128;
     t.out_col0 = n * 128;
+    const int b0 = (p.bstart != nullptr) ? p.bstart[e] : 0;
+    t.sfa_atom[0] = static_cast<long long>(m) * p.sfa_ts + b0;
+    t.sfa_atom[1] = 0;
+    t.sfb_atom = static_cast<long long>(n) * p.sfb_ts + b0;
   }
   return t;
-}
-
-// Four consecutive scale bytes starting at any byte address, little-endian.
-__device__ __forceinline__ uint32_t load_sf4(const uint8_t* ptr) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~static_cast<uintptr_t>(3));
-  const uint32_t sh = static_cast<uint32_t>(a & 3) * 8;
-  const uint32_t lo = __ldg(w);
-  if (sh == 0) return lo;
-  return __funnelshift_r(lo, __ldg(w + 1), sh);
 }
 
 // A final bounded wait that ignores the abort flag (used only to drain work
@@ -108,28 +119,12 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
-// ------------------------------------------------------------- epilogues
-
-// h3 / input-gradient rows: out[row][feature] = bf16(acc).
-__device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow) {
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0);
-  const int f = t.out_col0 + lrow;
-  for (int c0 = 0; c0 < t.b_rows; c0 += 32) {
-    uint32_t v[32];
-    tmem_ld32(tbase + c0, v);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      out[static_cast<long long>(t.out_row0 + c0 + i) * p.out0_pitch + f] = __float2bfloat16_rn(u2f(v[i]));
-  }
-}
-
 // Row bundle of one 32-feature block held across the warp's lanes (MXFP8:
-// the block's amax is a warp reduction), and column bundle of 32 rows held
-// in one thread's registers.
+// the block's amax is a warp reduction; the scale goes to the row-bundle
+// atom of routing block `blk`, row `prow` within it).
 template <bool MX>
-__device__ __forceinline__ void store_row_val(const GemmParams& p, void* out, uint8_t* out_sf, long long pitch,
-                                              long long sf_pitch, long long row, int col, float v, int lane) {
+__device__ __forceinline__ void store_row_val(const GemmParams& p, void* out, long long pitch, long long row,
+                                              int col, float v, int lane, int blk, int prow) {
   if (!MX) {
     static_cast<__nv_bfloat16*>(out)[row * pitch + col] = __float2bfloat16_rn(v);
   } else {
@@ -137,15 +132,22 @@ __device__ __forceinline__ void store_row_val(const GemmParams& p, void* out, ui
     const int e = mx_shared_exp(amax);
     const uint32_t code = cvt_e4m3x2(v * exp2_int(-e), 0.0f) & 0xFFu;
     static_cast<uint8_t*>(out)[row * pitch + col] = static_cast<uint8_t>(code);
-    if (lane == 0) out_sf[row * sf_pitch + col / 32] = static_cast<uint8_t>(e + 127);
+    if (lane == 0) {
+      const int kb = col >> 5;
+      p.out0_sf[(static_cast<long long>(blk) * p.out0_sf_kg + (kb >> 2)) * kAtom + sf_atom_byte(prow, kb & 3)] =
+          static_cast<uint8_t>(e + 127);
+    }
   }
 }
 
+// Column bundle: 32 rows of one feature in one thread's registers, written
+// contiguously to outT[feat][row0 ..]; MXFP8 scale to the column-bundle atom
+// (feature tile feat/128, routing block blk, 32-row group l).
 template <bool MX>
-__device__ __forceinline__ void store_col32(void* outT, uint8_t* outT_sf, long long pitch, long long sf_pitch,
-                                            long long feat, long long row0, const float (&v)[32]) {
+__device__ __forceinline__ void store_col32(const GemmParams& p, long long feat, long long row0, int blk, int l,
+                                            const float (&v)[32]) {
   if (!MX) {
-    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(outT) + feat * pitch + row0);
+    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out1) + feat * p.out1_pitch + row0);
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       o[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
@@ -160,10 +162,28 @@ __device__ __forceinline__ void store_col32(void* outT, uint8_t* outT_sf, long l
 #pragma unroll
     for (int q = 0; q < 8; ++q)
       w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
-    uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(outT) + feat * pitch + row0);
+    uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out1) + feat * p.out1_pitch + row0);
     o[0] = make_uint4(w[0], w[1], w[2], w[3]);
     o[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    outT_sf[feat * sf_pitch + row0 / 32] = static_cast<uint8_t>(e + 127);
+    p.out1_sf[((feat >> 7) * p.b_cap + blk) * kAtom + sf_atom_byte(static_cast<int>(feat & 127), l)] =
+        static_cast<uint8_t>(e + 127);
+  }
+}
+
+// ------------------------------------------------------------- epilogues
+// Each takes the warp's column half `h`: it drains chunks c0 = 32*(2i + h).
+
+// h3 / input-gradient rows: out[row][feature] = bf16(acc).
+__device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow, int h) {
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0);
+  const int f = t.out_col0 + lrow;
+  for (int c0 = 32 * h; c0 < t.b_rows; c0 += 64) {
+    uint32_t v[32];
+    tmem_ld32(tbase + c0, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      out[static_cast<long long>(t.out_row0 + c0 + i) * p.out0_pitch + f] = __float2bfloat16_rn(u2f(v[i]));
   }
 }
 
@@ -172,14 +192,14 @@ __device__ __forceinline__ void store_col32(void* outT, uint8_t* outT_sf, long l
 // operand) and, for training, the h2 column bundle (W2 WGRAD's operand).
 template <bool MX>
 __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow,
-                                               int lane) {
+                                               int lane, int h) {
   const int f = t.out_col0 + lrow;
-  for (int c0 = 0; c0 < t.b_rows; c0 += 32) {
+  for (int c0 = 32 * h; c0 < t.b_rows; c0 += 64) {
     uint32_t vg[32], vu[32];
     tmem_ld32(tbase + c0, vg);
     tmem_ld32(tbase + 128 + c0, vu);
     tmem_ld_wait();
-    float h[32];
+    float hv[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const long long row = t.out_row0 + c0 + i;
@@ -190,12 +210,12 @@ __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& 
         p.h1[row * p.h1_pitch + p.F + f] = ub;
       }
       const float g = __bfloat162float(gb), u = __bfloat162float(ub);
-      h[i] = silu_f(g) * u;
+      hv[i] = silu_f(g) * u;
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      store_row_val<MX>(p, p.out0, p.out0_sf, p.out0_pitch, p.out0_sf_pitch, t.out_row0 + c0 + i, f, h[i], lane);
-    if (p.want_col) store_col32<MX>(p.out1, p.out1_sf, p.out1_pitch, p.out1_sf_pitch, f, t.out_row0 + c0, h);
+      store_row_val<MX>(p, p.out0, p.out0_pitch, t.out_row0 + c0 + i, f, hv[i], lane, t.blk, c0 + i);
+    if (p.want_col) store_col32<MX>(p, f, t.out_row0 + c0, t.blk, c0 >> 5, hv);
   }
 }
 
@@ -204,9 +224,9 @@ __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& 
 // dh1 row bundle (W13 DGRAD's operand) and column bundle (W13 WGRAD's).
 template <bool MX>
 __device__ __forceinline__ void epi_swiglu_bwd(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow,
-                                               int lane) {
+                                               int lane, int h) {
   const int f = t.out_col0 + lrow;
-  for (int c0 = 0; c0 < t.b_rows; c0 += 32) {
+  for (int c0 = 32 * h; c0 < t.b_rows; c0 += 64) {
     uint32_t v[32];
     tmem_ld32(tbase + c0, v);
     tmem_ld_wait();
@@ -224,22 +244,22 @@ __device__ __forceinline__ void epi_swiglu_bwd(const GemmParams& p, const Tile& 
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const long long row = t.out_row0 + c0 + i;
-      store_row_val<MX>(p, p.out0, p.out0_sf, p.out0_pitch, p.out0_sf_pitch, row, f, dg[i], lane);
-      store_row_val<MX>(p, p.out0, p.out0_sf, p.out0_pitch, p.out0_sf_pitch, row, p.F + f, du[i], lane);
+      store_row_val<MX>(p, p.out0, p.out0_pitch, row, f, dg[i], lane, t.blk, c0 + i);
+      store_row_val<MX>(p, p.out0, p.out0_pitch, row, p.F + f, du[i], lane, t.blk, c0 + i);
     }
-    store_col32<MX>(p.out1, p.out1_sf, p.out1_pitch, p.out1_sf_pitch, f, t.out_row0 + c0, dg);
-    store_col32<MX>(p.out1, p.out1_sf, p.out1_pitch, p.out1_sf_pitch, p.F + f, t.out_row0 + c0, du);
+    store_col32<MX>(p, f, t.out_row0 + c0, t.blk, c0 >> 5, dg);
+    store_col32<MX>(p, p.F + f, t.out_row0 + c0, t.blk, c0 >> 5, du);
   }
 }
 
-// Weight gradient: dW[e][m][n0 .. n0+127], BF16 or FP32, optional add.  An
-// expert without rows (no MMA issued) gets zeros, or is left as is when
-// adding.
-__device__ __forceinline__ void epi_wgrad(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow) {
+// Weight gradient with plain stores: dW[e][m][n0 ..], FP32 or accumulate.
+// An expert without rows gets zeros, or is left as is when adding.
+__device__ __forceinline__ void epi_wgrad_direct(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow,
+                                                 int h) {
   if (t.kstages == 0 && p.dw_accum) return;
   const long long M = static_cast<long long>(p.m_tiles) * 128;
   const long long row = static_cast<long long>(t.e) * M + t.out_row0 + lrow;
-  for (int c0 = 0; c0 < 128; c0 += 32) {
+  for (int c0 = 32 * h; c0 < 128; c0 += 64) {
     float v[32];
     if (t.kstages > 0) {
       uint32_t r[32];
@@ -288,54 +308,92 @@ __device__ __forceinline__ void epi_wgrad(const GemmParams& p, const Tile& t, ui
   }
 }
 
+// Weight gradient (BF16, overwrite) through shared memory: the 128 x 128
+// tile is written into a 32 KB staging buffer as two 128-row x 128-byte
+// boxes in the 128-byte swizzle (16-byte chunk j of row m at chunk
+// j ^ (m % 8), so 8 consecutive rows hit 8 different bank groups), then one
+// thread stores both boxes with TMA.  Returns after the TMEM reads, so the
+// caller can release the accumulator before the smem write-out.
+__device__ __forceinline__ void epi_wgrad_stage(const Tile& t, uint32_t tbase, int lrow, int h, uint8_t* stg) {
+  for (int c0 = 32 * h; c0 < 128; c0 += 64) {
+    float v[32];
+    if (t.kstages > 0) {
+      uint32_t r[32];
+      tmem_ld32(tbase + c0, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    }
+    uint8_t* box = stg + (c0 >> 6) * 16384 + lrow * 128;
+    const int j0 = (c0 & 63) >> 3;  // first 16-byte chunk of these 32 columns
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int phys = (j0 + q) ^ (lrow & 7);
+      *reinterpret_cast<uint4*>(box + phys * 16) =
+          make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                     pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    }
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 
-template <bool MX, int NA>
+template <bool MX, int NA, int MODE>
 struct Cfg {
-  static constexpr int S = (NA == 2) ? 4 : 6;          // pipeline stages
-  static constexpr int STAGE = NA * kABytes + kBBytes;
-  static constexpr int ACC_BUFS = (NA == 1) ? 2 : 1;   // accumulator buffers
+  static constexpr bool WGRAD = MODE == kGroupedK;
+  static constexpr int SF_BYTES = MX ? (NA + 1) * kAtom : 0;
+  static constexpr int STAGE = ((NA * kABytes + kBBytes + SF_BYTES) + 1023) / 1024 * 1024;
+  static constexpr int S = WGRAD ? 4 : ((NA == 2) ? 4 : 6);  // pipeline stages
+  static constexpr int STAGING = WGRAD ? 2 * 32768 : 0;    // weight-gradient store buffers
+  static constexpr int ACC_BUFS = (NA == 1) ? 2 : 1;       // accumulator buffers
   static constexpr int ACC_COLS = NA * 128;
-  static constexpr int SF_COLS = (NA + 1) * 4;         // scale columns per stage
+  static constexpr int SF_COLS = (NA + 1) * 4;             // scale columns per stage
   static constexpr uint32_t SF_COL0 = ACC_BUFS * ACC_COLS;
-  static constexpr int BK = MX ? 128 : 64;             // contraction elements per stage
-  static constexpr int KMMA = MX ? 32 : 16;            // contraction elements per MMA
+  static constexpr int BK = MX ? 128 : 64;                 // contraction elements per stage
+  static constexpr int KMMA = MX ? 32 : 16;                // contraction elements per MMA
   static constexpr int MMAS = BK / KMMA;
-  static constexpr int THREADS = MX ? 320 : 192;
-  static constexpr int SMEM = 1024 + S * STAGE + 256;
+  static constexpr int THREADS = 64 + kEpiThreads;
+  static constexpr int SMEM = 1024 + S * STAGE + STAGING + 256;
 };
 
 template <bool MX, int NA, int EPI, int MODE>
-__global__ void __launch_bounds__(Cfg<MX, NA>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmParams p) {
-  using C = Cfg<MX, NA>;
+                const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  using C = Cfg<MX, NA, MODE>;
   constexpr int S = C::S;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE);
+  uint8_t* staging = smem + S * C::STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::STAGING);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + C::ACC_BUFS;
   uint64_t* drain = tempty + C::ACC_BUFS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* epi_abort = abort_flag + 1;  // epilogue warps leave together
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1 + (MX ? 4 : 0));
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < C::ACC_BUFS; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *epi_abort = 0;
     mbar_fence_init();
     tma_prefetch(&tmA);
     tma_prefetch(&tmB);
+    if (C::WGRAD && p.tma_store) tma_prefetch(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -364,12 +422,19 @@ __global__ void __launch_bounds__(Cfg<MX, NA>::THREADS, 1)
           }
           uint8_t* sa = smem + slot * C::STAGE;
           uint8_t* sb = sa + NA * kABytes;
-          mbar_arrive_expect_tx(&full[slot], NA * kABytes + t.b_rows * 128);
+          uint8_t* ssf = sb + kBBytes;
+          mbar_arrive_expect_tx(&full[slot], NA * kABytes + t.b_rows * 128 + C::SF_BYTES);
           const int kx = t.k0 + ks * C::BK;
 #pragma unroll
           for (int j = 0; j < NA; ++j) tma_load_2d(sa + j * kABytes, &tmA, &full[slot], kx, t.a_row[j]);
           for (int c = 0; c < t.b_rows / 32; ++c)
             tma_load_2d(sb + c * 4096, &tmB, &full[slot], kx, t.b_row0 + 32 * c);
+          if (MX) {
+#pragma unroll
+            for (int j = 0; j < NA; ++j)
+              bulk_load(ssf + j * kAtom, p.sfa + (t.sfa_atom[j] + ks) * kAtom, kAtom, &full[slot]);
+            bulk_load(ssf + NA * kAtom, p.sfb + (t.sfb_atom + ks) * kAtom, kAtom, &full[slot]);
+          }
         }
       }
       // no load may still be landing in shared memory when the CTA exits
@@ -398,7 +463,13 @@ __global__ void __launch_bounds__(Cfg<MX, NA>::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + slot * C::STAGE);
-          const uint64_t bdesc0 = sdesc_k_sw128(sa + NA * kABytes);
+          const uint32_t sb = sa + NA * kABytes;
+          const uint32_t sfcol = tmem + C::SF_COL0 + slot * C::SF_COLS;
+          if (MX) {
+#pragma unroll
+            for (int j = 0; j <= NA; ++j) tc_cp_sf(sfcol + j * 4, sdesc_sf_atom(sb + kBBytes + j * kAtom));
+          }
+          const uint64_t bdesc0 = sdesc_k_sw128(sb);
           const int nmma = (ks == t.kstages - 1) ? t.klast / C::KMMA : C::MMAS;
           for (int k = 0; k < nmma; ++k) {
             const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(2 * k);   // +32 bytes along K
@@ -407,9 +478,8 @@ __global__ void __launch_bounds__(Cfg<MX, NA>::THREADS, 1)
             for (int j = 0; j < NA; ++j) {
               const uint64_t adesc = sdesc_k_sw128(sa + j * kABytes) + static_cast<uint64_t>(2 * k);
               if (MX) {
-                const uint32_t sfcol = tmem + C::SF_COL0 + slot * C::SF_COLS;
-                mma_mxf8(d_tmem + j * 128, adesc, bdesc, idesc_mxf8(t.b_rows, k, k), sfcol + j * 4,
-                         sfcol + NA * 4, accum);
+                mma_mxf8(d_tmem + j * 128, adesc, bdesc, idesc_mxf8(t.b_rows, k, k), sfcol + j * 4, sfcol + NA * 4,
+                         accum);
               } else {
                 mma_bf16(d_tmem + j * 128, adesc, bdesc, idesc_bf16(t.b_rows), accum);
               }
@@ -424,64 +494,53 @@ __global__ void __launch_bounds__(Cfg<MX, NA>::THREADS, 1)
       tc_commit(drain);
       drain_wait(drain, 0);
     }
-  } else if (warp < 6) {
+  } else {
     // --------------------------------------------------------- epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;              // TMEM lane quadrant of this warp
+    const int h = (warp - 2) >> 2;       // which 32-column chunks it drains
     const int lrow = q * 32 + lane;
+    const int etid = threadIdx.x - 64;   // 0 .. kEpiThreads-1
+    const bool staged = C::WGRAD && p.tma_store;
     uint32_t tc = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
       const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk);
       const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull[acc], aph, abort_flag, p.err))) break;
+      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&tfull[acc], aph, abort_flag, p.err));
+      uint8_t* stg = staging + (tc & 1) * 32768;
+      if (staged) {
+        // Every epilogue warp reaches this barrier once per tile whether its
+        // (bounded) wait succeeded or not, so a warp that gives up cannot
+        // leave the others blocked in it: they all see the flag and leave.
+        if (!ok && lane == 0) *epi_abort = 1;
+        // the buffer used two tiles ago must have been read by its TMA store
+        if (etid == 0) bulk_wait_read<1>();
+        named_bar_sync(kEpiBarrier, kEpiThreads);
+        if (*epi_abort) break;
+      } else if (!ok) {
+        break;
+      }
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
-      if (EPI == kEpiStore) epi_store(p, t, tbase, lrow);
-      else if (EPI == kEpiSwigluFwd) epi_swiglu_fwd<MX>(p, t, tbase, lrow, lane);
-      else if (EPI == kEpiSwigluBwd) epi_swiglu_bwd<MX>(p, t, tbase, lrow, lane);
-      else epi_wgrad(p, t, tbase, lrow);
+      if (EPI == kEpiStore) epi_store(p, t, tbase, lrow, h);
+      else if (EPI == kEpiSwigluFwd) epi_swiglu_fwd<MX>(p, t, tbase, lrow, lane, h);
+      else if (EPI == kEpiSwigluBwd) epi_swiglu_bwd<MX>(p, t, tbase, lrow, lane, h);
+      else if (staged) epi_wgrad_stage(t, tbase, lrow, h, stg);
+      else epi_wgrad_direct(p, t, tbase, lrow, h);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
-    }
-  } else if (MX) {
-    // ----------------------------------------- scale factors -> TMEM
-    // TMEM scale layout for M = 128 with one scale per 32 values: column j
-    // (of 4) at lane i holds the scales of row 32*j + i, byte l = K-block l
-    // of the stage (selected per MMA by the scale-factor id).  Every warp
-    // writes the same words into its own lane quadrant.
-    const int q = warp & 3;
-    uint32_t it = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk);
-      for (int ks = 0; ks < t.kstages; ++ks, ++it) {
-        const uint32_t slot = it % S, ph = (it / S) & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[slot], ph ^ 1, abort_flag, p.err))) {
-          ok = false;
-          break;
+      if (staged) {
+        fence_proxy_async_smem();
+        named_bar_sync(kEpiBarrier, kEpiThreads);
+        if (etid == 0) {
+          const int y = t.e * p.m_tiles * 128 + t.out_row0;
+          tma_store_2d(&tmC, stg, t.out_col0, y);
+          tma_store_2d(&tmC, stg + 16384, t.out_col0 + 64, y);
+          bulk_commit();
         }
-        const int kb0 = (t.k0 + ks * C::BK) >> 5;
-        uint32_t wa[NA][4], wb[4];
-#pragma unroll
-        for (int j = 0; j < NA; ++j)
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            wa[j][c] = load_sf4(p.sfa + static_cast<long long>(t.a_row[j] + 32 * c + lane) * p.sfa_pitch + kb0);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          wb[c] = (32 * c < t.b_rows)
-                      ? load_sf4(p.sfb + static_cast<long long>(t.b_row0 + 32 * c + lane) * p.sfb_pitch + kb0)
-                      : 0u;
-        const uint32_t col = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::SF_COL0 + slot * C::SF_COLS;
-#pragma unroll
-        for (int j = 0; j < NA; ++j) tmem_st4(col + j * 4, wa[j][0], wa[j][1], wa[j][2], wa[j][3]);
-        tmem_st4(col + NA * 4, wb[0], wb[1], wb[2], wb[3]);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[slot]);
       }
     }
+    if (staged && etid == 0) bulk_wait<0>();
   }
 
   tc_fence_before();
@@ -495,7 +554,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA>::THREADS, 1)
 
 template <bool MX, int NA, int EPI, int MODE>
 cudaError_t launch_impl(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
-  using C = Cfg<MX, NA>;
+  using C = Cfg<MX, NA, MODE>;
   auto kern = gemm_kernel<MX, NA, EPI, MODE>;
   static bool configured = false;
   if (!configured) {
@@ -504,7 +563,7 @@ cudaError_t launch_impl(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
     configured = true;
   }
   const int grid = max(1, min(num_sms, g.max_tiles));
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.p);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.tmC, g.p);
   return cudaGetLastError();
 }
 

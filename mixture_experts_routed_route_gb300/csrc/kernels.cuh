@@ -17,7 +17,16 @@ struct RoutingPtrs {
   int* inv;       // [T_max*K]
   int4* blocks;   // [b_cap] (expert, first row, rows, 0)
   float* scores;  // [T_max*K]
+  int* bstart;    // [E+1] first row block of each expert
+  int* row_block; // [r_cap/32] row block of each 32-row group
 };
+
+// MXFP8 scale atoms: 128 operand rows x 4 consecutive 32-value blocks, 512
+// bytes, row p / block l at byte (p % 32) * 16 + (p / 32) * 4 + l (the order
+// tcgen05.cp 32x128b.warpx4 lays scales into tensor memory).
+__host__ __device__ __forceinline__ long long sf_atom_byte(int p, int l) {
+  return (p & 31) * 16 + (p >> 5) * 4 + l;
+}
 
 constexpr int kPad = 32;        // rows of every expert are padded to this
 constexpr int kBlockRows = 128; // rows per GEMM row block (MMA N <= 128)
@@ -33,7 +42,12 @@ cudaError_t launch_gather_rows(bool mx, bool use_scores, const void* src, int D,
 // Column bundle: dstT[d][r] = the same values transposed to [D, r_cap]; MXFP8
 // quantises along rows in 32-row blocks (WGRAD contracts over rows).
 cudaError_t launch_gather_cols(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
-                               void* dstT, uint8_t* dstT_sf, int r_cap, cudaStream_t stream);
+                               void* dstT, uint8_t* dstT_sf, int r_cap, int b_cap, cudaStream_t stream);
+
+// Row and column bundles of the same gathered rows in one pass (training).
+cudaError_t launch_gather_both(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
+                               void* dst, uint8_t* dst_sf, void* dstT, uint8_t* dstT_sf, int r_cap, int b_cap,
+                               int num_sms, cudaStream_t stream);
 
 // out[t] = bf16((accumulate ? out[t] : 0) + sum_k s(t,k) * h[inv(t,k)]),
 // FP32, k in order; s = 1 when `scores` is NULL.  The token count is T, or
@@ -55,26 +69,30 @@ struct GemmParams {
   const int* hdr;
   const int4* blocks;
   const int* poffsets;
+  const int* bstart;      // grouped-K: first row block of each expert
   int E;
   int n_tiles;            // grouped-M: 128-wide output tiles per expert; grouped-K: N/128
   int m_tiles;            // grouped-K: M/128
   int K;                  // grouped-M: contraction length
   int a_rows_per_expert;  // grouped-M: rows of A per expert
   int a_up_offset;        // SwiGLU forward: row offset of the up half (F)
-  // MXFP8 scale factors: byte arrays with a row pitch in bytes
+  // MXFP8 scale atoms of the operands (512 bytes each).  Atom of an A tile:
+  // grouped-M (A row / 128) * sfa_ts + stage, grouped-K m_tile * sfa_ts +
+  // (first block of the expert + stage); B likewise with the row block
+  // (grouped-M) or n_tile (grouped-K).
   const uint8_t* sfa;
-  long long sfa_pitch;
+  long long sfa_ts;
   const uint8_t* sfb;
-  long long sfb_pitch;
+  long long sfb_ts;
   // epilogue outputs (pitches in elements)
   void* out0;
   long long out0_pitch;
-  uint8_t* out0_sf;
-  long long out0_sf_pitch;
+  uint8_t* out0_sf;       // row-bundle scale atoms [b_cap][out0_sf_kg]
+  int out0_sf_kg;
   void* out1;
   long long out1_pitch;
-  uint8_t* out1_sf;
-  long long out1_sf_pitch;
+  uint8_t* out1_sf;       // column-bundle scale atoms [features/128][b_cap]
+  int b_cap;
   __nv_bfloat16* h1;      // SwiGLU forward: written when save_h1; backward: read
   long long h1_pitch;
   int F;
@@ -82,6 +100,7 @@ struct GemmParams {
   int want_col;
   int dw_fp32;
   int dw_accum;
+  int tma_store;          // weight gradient written through shared memory + TMA
   uint32_t* err;
 };
 
@@ -90,7 +109,7 @@ struct GemmLaunch {
   int na;                 // A tiles per B tile (2 for the fused SwiGLU forward)
   GemmEpi epi;
   GemmMode mode;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmC;  // tmC: weight-gradient output (TMA store)
   GemmParams p;
   int max_tiles;          // upper bound of the tile count (grid sizing)
 };

@@ -99,7 +99,7 @@ bool weight_matches(const moe_weight* w, moe_precision prec, int E, int N, int K
 
 // Offsets of the call's buffers inside the static array.
 struct StaticLayout {
-  size_t hdr, counts, offsets, poffsets, perm, inv, blocks, scores;
+  size_t hdr, counts, offsets, poffsets, perm, inv, blocks, scores, bstart, row_block;
   size_t xrow, xrow_sf, h2row, h2row_sf, h3, err, total;
   int64_t r_cap, b_cap;
 };
@@ -125,10 +125,12 @@ StaticLayout static_layout(int T, int D, int F, int E, int K, bool mx) {
   L.inv = take(routes * sizeof(int));
   L.blocks = take(L.b_cap * 4 * sizeof(int));
   L.scores = take(routes * sizeof(float));
+  L.bstart = take((E + 1) * sizeof(int));
+  L.row_block = take((L.r_cap / 32) * sizeof(int));
   L.xrow = take(L.r_cap * D * esz);
-  L.xrow_sf = mx ? take(L.r_cap * (D / 32) + kAl) : 0;
+  L.xrow_sf = mx ? take(L.b_cap * (D / 128) * 512) : 0;
   L.h2row = take(L.r_cap * F * esz);
-  L.h2row_sf = mx ? take(L.r_cap * (F / 32) + kAl) : 0;
+  L.h2row_sf = mx ? take(L.b_cap * (F / 128) * 512) : 0;
   L.h3 = take(L.r_cap * D * 2);
   L.err = take(16);
   L.total = o;
@@ -175,6 +177,8 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   rp.inv = reinterpret_cast<int*>(S + L.inv);
   rp.blocks = reinterpret_cast<int4*>(S + L.blocks);
   rp.scores = reinterpret_cast<float*>(S + L.scores);
+  rp.bstart = reinterpret_cast<int*>(S + L.bstart);
+  rp.row_block = reinterpret_cast<int*>(S + L.row_block);
   const int R = static_cast<int>(L.r_cap);
   uint8_t* xrow = S + L.xrow;
   uint8_t* xsf = mx ? S + L.xrow_sf : nullptr;
@@ -204,13 +208,14 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   g1.p.a_rows_per_expert = 2 * F;
   g1.p.a_up_offset = F;
   g1.p.sfa = W13->scale;
-  g1.p.sfa_pitch = D / 32;
+  g1.p.sfa_ts = D / 128;
   g1.p.sfb = xsf;
-  g1.p.sfb_pitch = D / 32;
+  g1.p.sfb_ts = D / 128;
   g1.p.out0 = h2;
   g1.p.out0_pitch = F;
   g1.p.out0_sf = h2sf;
-  g1.p.out0_sf_pitch = F / 32;
+  g1.p.out0_sf_kg = F / 128;
+  g1.p.b_cap = static_cast<int>(L.b_cap);
   g1.p.F = F;
   g1.p.err = err;
   g1.max_tiles = static_cast<int>(L.b_cap * (F / 128));
@@ -232,9 +237,9 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   g2.p.K = F;
   g2.p.a_rows_per_expert = D;
   g2.p.sfa = W2->scale;
-  g2.p.sfa_pitch = F / 32;
+  g2.p.sfa_ts = F / 128;
   g2.p.sfb = h2sf;
-  g2.p.sfb_pitch = F / 32;
+  g2.p.sfb_ts = F / 128;
   g2.p.out0 = h3;
   g2.p.out0_pitch = D;
   g2.p.F = F;

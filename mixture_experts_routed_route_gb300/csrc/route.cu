@@ -145,13 +145,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       hist[w * E + tid] = run;
       run += h;
     }
-    // row blocks of this expert
-    for (int b = 0; b < nb; ++b)
-      rp.blocks[eb + b] = make_int4(tid, ep + b * kBlockRows, min(kBlockRows, pc - b * kBlockRows), 0);
+    // row blocks of this expert, and the block of each of its 32-row groups
+    rp.bstart[tid] = eb;
+    for (int b = 0; b < nb; ++b) {
+      const int rows_b = min(kBlockRows, pc - b * kBlockRows);
+      rp.blocks[eb + b] = make_int4(tid, ep + b * kBlockRows, rows_b, 0);
+      for (int g = 0; g < rows_b / kPad; ++g) rp.row_block[(ep + b * kBlockRows) / kPad + g] = eb + b;
+    }
   }
   if (tid == 0) {
     rp.offsets[E] = to;
     rp.poffsets[E] = tp;
+    rp.bstart[E] = tb;
     s_poff[E] = tp;
     rp.hdr[0] = T;
     rp.hdr[1] = tb;

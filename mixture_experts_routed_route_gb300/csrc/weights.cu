@@ -8,7 +8,8 @@
 // values with distinct scale orientations.  Here the one scale of each tile
 // is written in both orientations ([E,N,K/32] and [E,K,N/32]) and the codes
 // once more transposed ([E,K,N]), so the input-gradient GEMM also reads a
-// K-major operand.
+// K-major operand.  The scales are written in the GEMMs' 512-byte atom
+// layout (kernels.cuh: sf_atom_byte), so a GEMM stage copies them in bulk.
 #include "kernels.cuh"
 
 namespace moe {
@@ -61,9 +62,16 @@ __global__ void __launch_bounds__(256) prep_mx_kernel(const __nv_bfloat16* __res
       qt[r][col] = static_cast<uint8_t>(two & 0xFF);
       qt[r + 1][col] = static_cast<uint8_t>(two >> 8);
     }
-    // scale in both orientations: row n of the tile / column k of the tile
-    sf[(static_cast<long long>(e) * N + n0 + lane) * (K / 32) + kc / 32] = sbyte;
-    if (sfT) sfT[(static_cast<long long>(e) * K + kc + lane) * (N / 32) + nb] = sbyte;
+    // the one scale in both orientations, as 512-byte atoms: row n of the
+    // tile (K-block kc/32) in [E*N/128][K/128], and row k of the transposed
+    // tile (N-block nb) in [E*K/128][N/128]
+    const long long nrow = static_cast<long long>(e) * N + n0 + lane;
+    const int kb = kc / 32;
+    sf[((nrow >> 7) * (K / 128) + (kb >> 2)) * 512 + sf_atom_byte(static_cast<int>(nrow & 127), kb & 3)] = sbyte;
+    if (sfT) {
+      const long long krow = static_cast<long long>(e) * K + kc + lane;
+      sfT[((krow >> 7) * (N / 128) + (nb >> 2)) * 512 + sf_atom_byte(static_cast<int>(krow & 127), nb & 3)] = sbyte;
+    }
   }
   __syncthreads();
   // codes, row-major [E,N,K]

@@ -174,3 +174,49 @@ def check_mx_wgrad(dW13_gpu, dW2_gpu, state, grads, experts=None, tol=TOL["mxfp8
             assert not bad.any(), (name, i, int(bad.sum()), rel_err(got, ref))
         errs.append((rel_err(got13, ref13), rel_err(got2, ref2)))
     return errs
+
+
+# ------------------------------------------------------------------------
+# MXFP8 scale layouts (include/moe_gb300.h): 512-byte atoms of 128 rows x 4
+# consecutive 32-value blocks, row p / block l at byte (p%32)*16 + (p//32)*4 + l.
+
+def atom_byte(p, l):
+    return (p % 32) * 16 + (p // 32) * 4 + l
+
+
+def unpack_row_sf(atoms, blocks, rows, K):
+    """[rows, K/32] scale bytes of a row bundle stored as atoms [B_cap][K/128]."""
+    atoms = np.asarray(atoms).reshape(-1)
+    out = np.zeros((rows, K // 32), np.uint8)
+    kb = np.arange(K // 32)[None, :]
+    for b, (_, r0, n, _) in enumerate(np.asarray(blocks).reshape(-1, 4)):
+        p = np.arange(n)[:, None]
+        out[r0:r0 + n] = atoms[(b * (K // 128) + kb // 4) * 512 + atom_byte(p, kb % 4)]
+    return out
+
+
+def unpack_col_sf(atoms, blocks, dim, rows, b_cap):
+    """[dim, rows/32] scale bytes of a column bundle stored as atoms [dim/128][B_cap]."""
+    atoms = np.asarray(atoms).reshape(-1)
+    out = np.zeros((dim, rows // 32), np.uint8)
+    d = np.arange(dim)
+    for b, (_, r0, n, _) in enumerate(np.asarray(blocks).reshape(-1, 4)):
+        for l in range(n // 32):
+            out[:, r0 // 32 + l] = atoms[((d // 128) * b_cap + b) * 512 + atom_byte(d % 128, l)]
+    return out
+
+
+def unpack_weight_sf(atoms, rows, K):
+    """[rows, K/32] scale bytes of a weight stored as atoms [rows/128][K/128]."""
+    atoms = np.asarray(atoms).reshape(-1)
+    r = np.arange(rows)[:, None]
+    kb = np.arange(K // 32)[None, :]
+    return atoms[((r // 128) * (K // 128) + kb // 4) * 512 + atom_byte(r % 128, kb % 4)]
+
+
+def saved_blocks(layer, saved):
+    """Row blocks (expert, first row, rows, 0) of the routing in `saved`."""
+    from mixture_experts_routed_route_gb300 import abi
+    hdr = layer.saved_field(saved, abi.MOE_SAVED_HEADER, torch.int32, (16,)).cpu().numpy()
+    nb = int(hdr[1])
+    return layer.saved_field(saved, abi.MOE_SAVED_BLOCKS, torch.int32, (4 * nb,)).cpu().numpy().reshape(nb, 4)

@@ -64,11 +64,16 @@ def test_host_side_sizes_without_gpu(lib):
     r = abi.moe_row_capacity(cfg)
     assert r % 128 == 0 and r >= 2048 * 6 + 31 * 384 + 128
     sb = abi.moe_saved_state_bytes(cfg)
-    off_prev = -1
+    spans = []
     for f in range(abi.MOE_SAVED_NUM_FIELDS):
         off, nb = abi.moe_saved_state_field(cfg, f)
-        assert off % 256 == 0 and off > off_prev and off + nb <= sb
-        off_prev = off
+        assert off % 256 == 0 and off + nb <= sb
+        spans.append((off, off + nb))
+    spans.sort()
+    assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))     # fields do not overlap
+    # routing fields come first, then h1 and the column bundles
+    routing = [abi.moe_saved_state_field(cfg, f)[0] for f in (abi.MOE_SAVED_BSTART, abi.MOE_SAVED_ROWBLOCK)]
+    assert max(routing) < abi.moe_saved_state_field(cfg, abi.MOE_SAVED_H1)[0]
     assert abi.moe_saved_state_field(cfg, abi.MOE_SAVED_H1)[1] == r * 2 * 2048 * 2
     bad = abi.make_config(2048, 7168, 2048, 2000, 6, abi.MOE_MXFP8, 0)
     assert abi.moe_row_capacity(bad) == 0 and abi.moe_saved_state_bytes(bad) == 0

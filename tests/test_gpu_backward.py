@@ -9,7 +9,8 @@ import torch
 from mixture_experts_routed_route_gb300 import synth
 from oracle import formats as fm
 
-from moe_cases import TOL, Case, check_mx_wgrad, rel_err, run_gpu, run_oracle, to_f64
+from moe_cases import (TOL, Case, check_mx_wgrad, rel_err, run_gpu, run_oracle, saved_blocks, to_f64,
+                        unpack_col_sf, unpack_row_sf)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,13 +73,18 @@ def test_dh3_bundles_bit_exact(name):
         col = layer.read_buffer(abi.MOE_BUF_DH3COL, np.uint16, (D, R))[:, :rows]
         np.testing.assert_array_equal(fm.bf16_bits_to_f64(col).T, gr["dh3_col"])
     else:
+        blocks = saved_blocks(layer, g["saved"])
         row = layer.read_buffer(abi.MOE_BUF_DH3ROW, np.uint8, (rows, D))
-        rs = layer.read_buffer(abi.MOE_BUF_DH3ROW_SCALE, np.uint8, (rows, D // 32)).astype(np.int64) - 127
+        _, nb_row = abi.moe_ctx_buffer(layer.ctx, abi.MOE_BUF_DH3ROW_SCALE)
+        rs = unpack_row_sf(layer.read_buffer(abi.MOE_BUF_DH3ROW_SCALE, np.uint8, (nb_row,)), blocks, rows, D)
+        rs = rs.astype(np.int64) - 127
         q, e = fm.mx_quantize(gr["dh3"], axis=-1)
         np.testing.assert_array_equal(fm.e4m3_decode(row), q)
         np.testing.assert_array_equal(rs, e)
         col = layer.read_buffer(abi.MOE_BUF_DH3COL, np.uint8, (D, R))[:, :rows]
-        cs = layer.read_buffer(abi.MOE_BUF_DH3COL_SCALE, np.uint8, (D, R // 32))[:, : rows // 32]
+        _, nb_col = abi.moe_ctx_buffer(layer.ctx, abi.MOE_BUF_DH3COL_SCALE)
+        b_cap = nb_col // ((D // 128) * 512)
+        cs = unpack_col_sf(layer.read_buffer(abi.MOE_BUF_DH3COL_SCALE, np.uint8, (nb_col,)), blocks, D, rows, b_cap)
         q, e = fm.mx_quantize(gr["dh3"], axis=0)
         np.testing.assert_array_equal(fm.e4m3_decode(col).T, q)
         np.testing.assert_array_equal(cs.astype(np.int64).T - 127, e)

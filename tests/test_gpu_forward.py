@@ -11,7 +11,8 @@ from mixture_experts_routed_route_gb300 import synth
 from oracle import formats as fm
 from oracle import moe as omoe
 
-from moe_cases import TOL, Case, rel_err, run_gpu, run_oracle, to_f64
+from moe_cases import (TOL, Case, rel_err, run_gpu, run_oracle, saved_blocks, to_f64, unpack_row_sf,
+                        unpack_weight_sf)
 
 pytestmark = pytest.mark.gpu
 
@@ -67,7 +68,9 @@ def test_forward_stages(name):
         np.testing.assert_array_equal(fm.bf16_bits_to_f64(xr), st["xq"])
     else:
         xr = layer.read_buffer(abi.MOE_BUF_XROW, np.uint8, (rows, D))
-        xs = layer.read_buffer(abi.MOE_BUF_XROW_SCALE, np.uint8, (rows, D // 32))
+        _, nbytes = abi.moe_ctx_buffer(layer.ctx, abi.MOE_BUF_XROW_SCALE)
+        atoms = layer.read_buffer(abi.MOE_BUF_XROW_SCALE, np.uint8, (nbytes,))
+        xs = unpack_row_sf(atoms, saved_blocks(layer, g["saved"]), rows, D)
         q, e = fm.mx_quantize(st["xg"], axis=-1)
         np.testing.assert_array_equal(fm.e4m3_decode(xr), q)
         np.testing.assert_array_equal(xs.astype(np.int64) - 127, e)
@@ -110,10 +113,10 @@ def test_weight_prep_mx_bit_exact():
     q, e = fm.mx_quantize_weight_32x32(to_f64(w13))
     E, N, K = w13.shape
     np.testing.assert_array_equal(fm.e4m3_decode(pw.data.cpu().numpy()), q)
-    sf = pw.scale[: E * N * (K // 32)].cpu().numpy().reshape(E, N, K // 32).astype(np.int64) - 127
+    sf = unpack_weight_sf(pw.scale.cpu().numpy(), E * N, K).reshape(E, N, K // 32).astype(np.int64) - 127
     np.testing.assert_array_equal(sf, np.repeat(e, 32, axis=1))
     np.testing.assert_array_equal(fm.e4m3_decode(pw.data_t.cpu().numpy()), np.swapaxes(q, 1, 2))
-    sft = pw.scale_t[: E * K * (N // 32)].cpu().numpy().reshape(E, K, N // 32).astype(np.int64) - 127
+    sft = unpack_weight_sf(pw.scale_t.cpu().numpy(), E * K, N).reshape(E, K, N // 32).astype(np.int64) - 127
     np.testing.assert_array_equal(sft, np.repeat(np.swapaxes(e, 1, 2), 32, axis=1))
 
 

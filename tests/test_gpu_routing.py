@@ -71,6 +71,13 @@ def test_routing_bit_exact(name):
         for b in range((pc + 127) // 128):
             exp.append([e, int(rt.poffsets[e]) + 128 * b, min(128, pc - 128 * b), 0])
     np.testing.assert_array_equal(blocks, np.array(exp, dtype=np.int32).reshape(-1, 4))
+    # first block of each expert, and the block of every 32-row group
+    nb = np.array([(int(rt.poffsets[e + 1] - rt.poffsets[e]) + 127) // 128 for e in range(E)])
+    np.testing.assert_array_equal(field(abi.MOE_SAVED_BSTART, torch.int32, E + 1),
+                                  np.concatenate([[0], np.cumsum(nb)]))
+    rb = field(abi.MOE_SAVED_ROWBLOCK, torch.int32, rows // 32)
+    for b, (_, r0, n, _) in enumerate(exp):
+        assert np.all(rb[r0 // 32:(r0 + n) // 32] == b)
     # error word: bad IDs flagged; an inactive route with a score flagged in debug mode
     bits = res["err_bits"]
     assert bool(bits & abi.MOE_DEV_ERR_BAD_ID) == bool(rt.bad_ids.any())
