@@ -132,15 +132,13 @@ def stage_bytes(w, rows_padded, routes, precision, train):
     Rp, R = rows_padded, routes
     fwd = {
         "route": T * w.K * 8 + (Rp + 2 * T * w.K) * 4,
-        "gather_x_rows": T * D * 2 + Rp * D * q,
-        "gather_x_cols": (T * D * 2 + Rp * D * q) if train else 0,
+        "gather_x": T * D * 2 + Rp * D * q * (2 if train else 1),
         "gemm_w13_swiglu": E * 2 * F * D * q + Rp * D * q + Rp * F * q + (Rp * 2 * F * 2 + Rp * F * q if train else 0),
         "gemm_w2": E * D * F * q + Rp * F * q + Rp * D * 2,
         "combine": R * D * 2 + T * D * 2 * 2,
     }
     bwd = {
-        "gather_dh3_rows": T * D * 2 + Rp * D * q,
-        "gather_dh3_cols": T * D * 2 + Rp * D * q,
+        "gather_dh3": T * D * 2 + 2 * Rp * D * q,
         "gemm_w2_dgrad_swiglu_bwd": E * D * F * q + Rp * D * q + Rp * 2 * F * 2 + 2 * Rp * 2 * F * q,
         "gemm_w2_wgrad": D * Rp * q + F * Rp * q + E * D * F * 2,
         "gemm_w13_dgrad": E * 2 * F * D * q + Rp * 2 * F * q + Rp * D * 2,

@@ -148,9 +148,9 @@ MOE_API size_t moe_ctx_scratch_bytes(const moe_config* cfg);
 /*
  * Bytes of the per-layer saved state that a training forward writes and the
  * matching backward reads: routing arrays, a copy of the scores, BF16 h1
- * [R_cap, 2F] and the WGRAD column bundles of x and h2 ([DM] section 04,
- * "Activation Lifetimes and Backward Readers": MXFP8 full-save keeps the x/h2
- * column bundles and dense h1).  The caller allocates it (16-byte aligned)
+ * [R_cap, 2F], the WGRAD column bundles of x and h2 and BF16 h3 [R_cap, D]
+ * ([DM] section 04, "Activation Lifetimes and Backward Readers": MXFP8
+ * full-save keeps the x/h2 column bundles, dense h1 and h3).  The caller allocates it (16-byte aligned)
  * and keeps one per live layer.  0 for an invalid config.
  */
 MOE_API size_t moe_saved_state_bytes(const moe_config* cfg);
@@ -173,7 +173,7 @@ MOE_API size_t moe_saved_state_bytes(const moe_config* cfg);
 
 /* Saved-state fields, for inspection by tests (moe_saved_state_field).  The
  * routing fields come first in memory (HEADER..SCORES, BSTART, ROWBLOCK),
- * then H1 and the column bundles. */
+ * then H1, the column bundles and H3. */
 typedef enum {
   MOE_SAVED_HEADER = 0,     /* int32[16]: [0] T, [1] row blocks, [2] rows used, [3] active routes */
   MOE_SAVED_COUNTS = 1,     /* int32[E]     active routes per expert           */
@@ -191,7 +191,8 @@ typedef enum {
   MOE_SAVED_H2COL_SCALE = 12,/* e8m0 column-bundle atoms [F/128][B_cap]        */
   MOE_SAVED_BSTART = 13,    /* int32[E+1]   first row block of each expert     */
   MOE_SAVED_ROWBLOCK = 14,  /* int32[R_cap/32] row block of each 32-row group  */
-  MOE_SAVED_NUM_FIELDS = 15
+  MOE_SAVED_H3 = 15,        /* bf16[R_cap, D] route outputs (score gradient)   */
+  MOE_SAVED_NUM_FIELDS = 16
 } moe_saved_field;
 
 /* Offset and size in bytes of one saved-state field; the row capacity
@@ -255,10 +256,15 @@ MOE_API moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int
  *   dW13    [E, 2F, D], dW2 [E, D, F]: BF16, or float with MOE_DW_FP32;
  *           MOE_DW_ACCUMULATE adds into them.  An expert no active route
  *           reaches gets exact zeros (or is left as is when accumulating).
+ *   d_scores float [T, K] or NULL: the score gradient
+ *           dp(t,k) = <h3(t,k), dout[t]> summed in FP32 in a fixed order
+ *           ([BLOG] section 2 "SwiGLU backward": the routing-weight gradient
+ *           of the weighted combine, which the caller's router backward
+ *           consumes); 0 for inactive routes.
  */
 MOE_API moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout,
                         const moe_weight* W13, const moe_weight* W2, void* dx, void* dW13,
-                        void* dW2, uint32_t call_flags, cudaStream_t stream);
+                        void* dW2, float* d_scores, uint32_t call_flags, cudaStream_t stream);
 
 /* Synchronise the device, return the error word's bits in *bits and clear
  * it.  Not for use inside graph capture. */
@@ -298,15 +304,16 @@ MOE_API moe_status moe_ctx_buffer(moe_ctx* ctx, int which, void** dev_ptr, size_
  * graph, so replays re-time them).  moe_ctx_stage_times waits for the events
  * of the last forward (pass 0) or backward (pass 1) and returns each stage's
  * duration in milliseconds:
- *   forward  (MOE_FWD_STAGES): route, gather x rows, gather x columns
- *            (training only, else ~0), W13 + SwiGLU GEMM, W2 GEMM, combine
- *   backward (MOE_BWD_STAGES): gather dh3 rows, gather dh3 columns, W2 DGRAD +
- *            SwiGLU backward GEMM, W2 WGRAD GEMM, W13 DGRAD GEMM, W13 WGRAD
+ *   forward  (MOE_FWD_STAGES): route, gather x (row bundle, and the column
+ *            bundle in the same pass when training), W13 + SwiGLU GEMM, W2
+ *            GEMM, combine
+ *   backward (MOE_BWD_STAGES): gather dh3 (row and column bundles), W2 DGRAD
+ *            + SwiGLU backward GEMM, W2 WGRAD GEMM, W13 DGRAD GEMM, W13 WGRAD
  *            GEMM, dX reduction
  * Enabling creates the events (call it outside capture, after create).
  */
-#define MOE_FWD_STAGES 6
-#define MOE_BWD_STAGES 7
+#define MOE_FWD_STAGES 5
+#define MOE_BWD_STAGES 6
 MOE_API moe_status moe_ctx_enable_stage_timing(moe_ctx* ctx, int enable);
 MOE_API moe_status moe_ctx_stage_times(moe_ctx* ctx, int pass, float* ms, int n);
 

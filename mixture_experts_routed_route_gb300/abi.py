@@ -41,8 +41,8 @@ MOE_DW_ACCUMULATE = 0x4
 # moe_saved_field
 (MOE_SAVED_HEADER, MOE_SAVED_COUNTS, MOE_SAVED_OFFSETS, MOE_SAVED_POFFSETS, MOE_SAVED_PERM, MOE_SAVED_INV,
  MOE_SAVED_BLOCKS, MOE_SAVED_SCORES, MOE_SAVED_H1, MOE_SAVED_XCOL, MOE_SAVED_XCOL_SCALE, MOE_SAVED_H2COL,
- MOE_SAVED_H2COL_SCALE, MOE_SAVED_BSTART, MOE_SAVED_ROWBLOCK) = range(15)
-MOE_SAVED_NUM_FIELDS = 15
+ MOE_SAVED_H2COL_SCALE, MOE_SAVED_BSTART, MOE_SAVED_ROWBLOCK, MOE_SAVED_H3) = range(16)
+MOE_SAVED_NUM_FIELDS = 16
 
 # moe_buffer
 (MOE_BUF_XROW, MOE_BUF_XROW_SCALE, MOE_BUF_H2ROW, MOE_BUF_H2ROW_SCALE, MOE_BUF_H3, MOE_BUF_DH3ROW,
@@ -88,7 +88,7 @@ _SIGNATURES = {
     "moe_forward": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, _P, ctypes.POINTER(moe_weight),
                                    ctypes.POINTER(moe_weight), _P, _P, ctypes.c_uint32, _P]),
     "moe_backward": (ctypes.c_int, [_P, _P, _P, ctypes.POINTER(moe_weight), ctypes.POINTER(moe_weight), _P, _P,
-                                    _P, ctypes.c_uint32, _P]),
+                                    _P, _P, ctypes.c_uint32, _P]),
     "moe_ctx_enable_stage_timing": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_ctx_stage_times": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.c_int]),
     "moe_ctx_launch_count": (ctypes.c_uint64, [_P]),
@@ -99,11 +99,11 @@ _SIGNATURES = {
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
 
-MOE_FWD_STAGES = 6
-MOE_BWD_STAGES = 7
-FWD_STAGE_NAMES = ("route", "gather_x_rows", "gather_x_cols", "gemm_w13_swiglu", "gemm_w2", "combine")
-BWD_STAGE_NAMES = ("gather_dh3_rows", "gather_dh3_cols", "gemm_w2_dgrad_swiglu_bwd", "gemm_w2_wgrad",
-                   "gemm_w13_dgrad", "gemm_w13_wgrad", "reduce_dx")
+MOE_FWD_STAGES = 5
+MOE_BWD_STAGES = 6
+FWD_STAGE_NAMES = ("route", "gather_x", "gemm_w13_swiglu", "gemm_w2", "combine")
+BWD_STAGE_NAMES = ("gather_dh3", "gemm_w2_dgrad_swiglu_bwd", "gemm_w2_wgrad", "gemm_w13_dgrad", "gemm_w13_wgrad",
+                   "reduce_dx")
 
 
 def _load():
@@ -233,6 +233,7 @@ def moe_forward_static_scratch(cfg, T, x, topk_ids, topk_scores, W13, W2, out, c
                                           _ptr(device_error_word), _stream(stream)))
 
 
-def moe_backward(ctx, saved, dout, W13, W2, dx, dW13, dW2, call_flags=0, stream=None):
+def moe_backward(ctx, saved, dout, W13, W2, dx, dW13, dW2, d_scores=None, call_flags=0, stream=None):
     _check("moe_backward", LIB.moe_backward(ctx, _ptr(saved), _ptr(dout), ctypes.byref(W13), ctypes.byref(W2),
-                                            _ptr(dx), _ptr(dW13), _ptr(dW2), call_flags, _stream(stream)))
+                                            _ptr(dx), _ptr(dW13), _ptr(dW2), _ptr(d_scores), call_flags,
+                                            _stream(stream)))

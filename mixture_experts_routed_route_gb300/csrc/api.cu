@@ -92,11 +92,13 @@ SavedLayout saved_layout(const moe_config* c) {
   sz[MOE_SAVED_XCOL_SCALE] = mx ? (D / 128) * B * 512 : 0;
   sz[MOE_SAVED_H2COL] = F * R * esz;
   sz[MOE_SAVED_H2COL_SCALE] = mx ? (F / 128) * B * 512 : 0;
+  sz[MOE_SAVED_H3] = R * D * 2;
   // routing fields first (the inference copy in the context holds just these)
   static const int order[MOE_SAVED_NUM_FIELDS] = {
       MOE_SAVED_HEADER, MOE_SAVED_COUNTS, MOE_SAVED_OFFSETS, MOE_SAVED_POFFSETS, MOE_SAVED_PERM,
       MOE_SAVED_INV,    MOE_SAVED_BLOCKS, MOE_SAVED_SCORES,  MOE_SAVED_BSTART,   MOE_SAVED_ROWBLOCK,
-      MOE_SAVED_H1,     MOE_SAVED_XCOL,   MOE_SAVED_XCOL_SCALE, MOE_SAVED_H2COL, MOE_SAVED_H2COL_SCALE};
+      MOE_SAVED_H1,     MOE_SAVED_XCOL,   MOE_SAVED_XCOL_SCALE, MOE_SAVED_H2COL, MOE_SAVED_H2COL_SCALE,
+      MOE_SAVED_H3};
   size_t off = 0;
   for (int k = 0; k < MOE_SAVED_NUM_FIELDS; ++k) {
     const int i = order[k];
@@ -405,17 +407,17 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
                        rp, ctx->err, stream));
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 0, 1, stream));
-  MOE_TRY(launch_gather_rows(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
-                             static_cast<int>(R), sms, stream));
+  if (train) {
+    // row bundle (W13 operand) and column bundle (W13 WGRAD operand) in one pass
+    MOE_TRY(launch_gather_both(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
+                               sv + SL.off[MOE_SAVED_XCOL], mx ? sv + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr,
+                               static_cast<int>(R), static_cast<int>(ctx->b_cap), sms, stream));
+  } else {
+    MOE_TRY(launch_gather_rows(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
+                               static_cast<int>(R), sms, stream));
+  }
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 0, 2, stream));
-  if (train) {
-    MOE_TRY(launch_gather_cols(mx, false, x, D, K, rp, sv + SL.off[MOE_SAVED_XCOL],
-                               mx ? sv + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr, static_cast<int>(R),
-                               static_cast<int>(ctx->b_cap), stream));
-    ctx->launches += 1;
-  }
-  MOE_TRY(stage_mark(ctx, 0, 3, stream));
 
   // ---- W13 + SwiGLU
   GemmLaunch g1{};
@@ -431,6 +433,7 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   p1.blocks = rp.blocks;
   p1.poffsets = rp.poffsets;
   p1.E = E;
+  p1.b_box_rows = 32;
   p1.n_tiles = F / 128;
   p1.K = D;
   p1.a_rows_per_expert = 2 * F;
@@ -458,7 +461,7 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   g1.max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
   MOE_TRY(launch_gemm(g1, sms, stream));
   ctx->launches += 1;
-  MOE_TRY(stage_mark(ctx, 0, 4, stream));
+  MOE_TRY(stage_mark(ctx, 0, 3, stream));
 
   // ---- W2
   GemmLaunch g2{};
@@ -474,6 +477,7 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   p2.blocks = rp.blocks;
   p2.poffsets = rp.poffsets;
   p2.E = E;
+  p2.b_box_rows = 32;
   p2.n_tiles = D / 128;
   p2.K = F;
   p2.a_rows_per_expert = D;
@@ -481,25 +485,26 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   p2.sfa_ts = F / 128;
   p2.sfb = B(ctx, MOE_BUF_H2ROW_SCALE);
   p2.sfb_ts = F / 128;
-  p2.out0 = B(ctx, MOE_BUF_H3);
+  uint8_t* h3 = train ? sv + SL.off[MOE_SAVED_H3] : B(ctx, MOE_BUF_H3);   // saved for the score gradient
+  p2.out0 = h3;
   p2.out0_pitch = D;
   p2.F = F;
   p2.err = ctx->err;
   g2.max_tiles = static_cast<int>(ctx->b_cap * (D / 128));
   MOE_TRY(launch_gemm(g2, sms, stream));
   ctx->launches += 1;
-  MOE_TRY(stage_mark(ctx, 0, 5, stream));
+  MOE_TRY(stage_mark(ctx, 0, 4, stream));
 
   // ---- combine
-  MOE_TRY(launch_combine(B(ctx, MOE_BUF_H3), D, K, rp.inv, rp.scores, out, T,
+  MOE_TRY(launch_combine(h3, D, K, rp.inv, rp.scores, out, T,
                          (call_flags & MOE_ACCUMULATE_OUT) != 0, sms, stream));
   ctx->launches += 1;
-  MOE_TRY(stage_mark(ctx, 0, 6, stream));
+  MOE_TRY(stage_mark(ctx, 0, 5, stream));
   return MOE_OK;
 }
 
 moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const moe_weight* W13,
-                        const moe_weight* W2, void* dx, void* dW13, void* dW2, uint32_t call_flags,
+                        const moe_weight* W2, void* dx, void* dW13, void* dW2, float* d_scores, uint32_t call_flags,
                         cudaStream_t stream) {
   if (!ctx || !saved || !dout || !dx || !dW13 || !dW2) return MOE_ERR_INVALID_ARG;
   const moe_config& c = ctx->cfg;
@@ -522,14 +527,11 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
 
   // ---- dh3 = s * dY: row bundle (W2 DGRAD) and column bundle (W2 WGRAD)
   MOE_TRY(stage_mark(ctx, 1, 0, stream));
-  MOE_TRY(launch_gather_rows(mx, true, dout, D, K, rp, B(ctx, MOE_BUF_DH3ROW), B(ctx, MOE_BUF_DH3ROW_SCALE),
-                             static_cast<int>(R), sms, stream));
+  MOE_TRY(launch_gather_both(mx, true, dout, D, K, rp, B(ctx, MOE_BUF_DH3ROW), B(ctx, MOE_BUF_DH3ROW_SCALE),
+                             B(ctx, MOE_BUF_DH3COL), B(ctx, MOE_BUF_DH3COL_SCALE), static_cast<int>(R),
+                             static_cast<int>(ctx->b_cap), sms, stream));
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 1, 1, stream));
-  MOE_TRY(launch_gather_cols(mx, true, dout, D, K, rp, B(ctx, MOE_BUF_DH3COL), B(ctx, MOE_BUF_DH3COL_SCALE),
-                             static_cast<int>(R), static_cast<int>(ctx->b_cap), stream));
-  ctx->launches += 1;
-  MOE_TRY(stage_mark(ctx, 1, 2, stream));
 
   // ---- W2 DGRAD + SwiGLU backward -> dh1 row and column bundles
   GemmLaunch g1{};
@@ -545,6 +547,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p1.blocks = rp.blocks;
   p1.poffsets = rp.poffsets;
   p1.E = E;
+  p1.b_box_rows = 32;
   p1.n_tiles = F / 128;
   p1.K = D;
   p1.a_rows_per_expert = F;
@@ -567,7 +570,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g1.max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
   MOE_TRY(launch_gemm(g1, sms, stream));
   ctx->launches += 1;
-  MOE_TRY(stage_mark(ctx, 1, 3, stream));
+  MOE_TRY(stage_mark(ctx, 1, 2, stream));
 
   // ---- W2 WGRAD: dW2[e] = dh3_e^T h2_e   ([D, F] per expert)
   GemmLaunch g2{};
@@ -576,13 +579,14 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g2.epi = kEpiWgrad;
   g2.mode = kGroupedK;
   if (!make_tmap(&g2.tmA, B(ctx, MOE_BUF_DH3COL), mx, D, R, 128) ||
-      !make_tmap(&g2.tmB, sv + SL.off[MOE_SAVED_H2COL], mx, F, R, 32))
+      !make_tmap(&g2.tmB, sv + SL.off[MOE_SAVED_H2COL], mx, F, R, 128))
     return MOE_ERR_CUDA;
   GemmParams& p2 = g2.p;
   p2.hdr = rp.hdr;
   p2.blocks = rp.blocks;
   p2.poffsets = rp.poffsets;
   p2.E = E;
+  p2.b_box_rows = 128;
   p2.m_tiles = D / 128;
   p2.n_tiles = F / 128;
   p2.bstart = rp.bstart;
@@ -600,7 +604,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g2.max_tiles = E * (D / 128) * (F / 128);
   MOE_TRY(launch_gemm(g2, sms, stream));
   ctx->launches += 1;
-  MOE_TRY(stage_mark(ctx, 1, 4, stream));
+  MOE_TRY(stage_mark(ctx, 1, 3, stream));
 
   // ---- W13 DGRAD: dxr = dh1 W13[e]
   GemmLaunch g3{};
@@ -616,6 +620,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p3.blocks = rp.blocks;
   p3.poffsets = rp.poffsets;
   p3.E = E;
+  p3.b_box_rows = 32;
   p3.n_tiles = D / 128;
   p3.K = 2 * F;
   p3.a_rows_per_expert = D;
@@ -630,7 +635,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g3.max_tiles = static_cast<int>(ctx->b_cap * (D / 128));
   MOE_TRY(launch_gemm(g3, sms, stream));
   ctx->launches += 1;
-  MOE_TRY(stage_mark(ctx, 1, 5, stream));
+  MOE_TRY(stage_mark(ctx, 1, 4, stream));
 
   // ---- W13 WGRAD: dW13[e] = dh1_e^T x_e   ([2F, D] per expert)
   GemmLaunch g4{};
@@ -639,13 +644,14 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g4.epi = kEpiWgrad;
   g4.mode = kGroupedK;
   if (!make_tmap(&g4.tmA, B(ctx, MOE_BUF_DH1COL), mx, 2 * F, R, 128) ||
-      !make_tmap(&g4.tmB, sv + SL.off[MOE_SAVED_XCOL], mx, D, R, 32))
+      !make_tmap(&g4.tmB, sv + SL.off[MOE_SAVED_XCOL], mx, D, R, 128))
     return MOE_ERR_CUDA;
   GemmParams& p4 = g4.p;
   p4.hdr = rp.hdr;
   p4.blocks = rp.blocks;
   p4.poffsets = rp.poffsets;
   p4.E = E;
+  p4.b_box_rows = 128;
   p4.m_tiles = 2 * F / 128;
   p4.n_tiles = D / 128;
   p4.bstart = rp.bstart;
@@ -663,13 +669,18 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g4.max_tiles = E * (2 * F / 128) * (D / 128);
   MOE_TRY(launch_gemm(g4, sms, stream));
   ctx->launches += 1;
-  MOE_TRY(stage_mark(ctx, 1, 6, stream));
+  MOE_TRY(stage_mark(ctx, 1, 5, stream));
 
   // ---- dX[t] = sum_k dxr(t,k)
   MOE_TRY(launch_combine(B(ctx, MOE_BUF_DXR), D, K, rp.inv, nullptr, dx, c.max_tokens,
                          (call_flags & MOE_ACCUMULATE_DX) != 0, sms, stream, rp.hdr));
   ctx->launches += 1;
-  MOE_TRY(stage_mark(ctx, 1, 7, stream));
+  MOE_TRY(stage_mark(ctx, 1, 6, stream));
+  if (d_scores) {
+    MOE_TRY(launch_score_grad(sv + SL.off[MOE_SAVED_H3], dout, D, K, rp.inv, d_scores, c.max_tokens, sms, stream,
+                              rp.hdr));
+    ctx->launches += 1;
+  }
   return MOE_OK;
 }
 

@@ -57,7 +57,51 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
   }
 }
 
+// Score gradient ("Mixture of Experts: How Routing Becomes GPU Computation",
+// section 2, "SwiGLU backward": dp(t,e) = <H(t,e), dY(t)>): one warp per
+// route, each lane sums its 8-value slices in order, then a fixed xor tree.
+__global__ void __launch_bounds__(256) score_grad_kernel(const __nv_bfloat16* __restrict__ h3,
+                                                         const __nv_bfloat16* __restrict__ dY, int D, int K,
+                                                         const int* __restrict__ inv, float* __restrict__ dp, int T,
+                                                         const int* __restrict__ hdr) {
+  if (hdr) T = min(T, hdr[0]);
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < T * K; i += warps) {
+    const int r = inv[i];
+    float acc = 0.0f;
+    if (r >= 0) {
+      const __nv_bfloat16* a = h3 + static_cast<long long>(r) * D;
+      const __nv_bfloat16* b = dY + static_cast<long long>(i / K) * D;
+      for (int c = lane * 8; c < D; c += 256) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(a + c));
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(b + c));
+        acc = fmaf(bf16_lo(u.x), bf16_lo(v.x), acc);
+        acc = fmaf(bf16_hi(u.x), bf16_hi(v.x), acc);
+        acc = fmaf(bf16_lo(u.y), bf16_lo(v.y), acc);
+        acc = fmaf(bf16_hi(u.y), bf16_hi(v.y), acc);
+        acc = fmaf(bf16_lo(u.z), bf16_lo(v.z), acc);
+        acc = fmaf(bf16_hi(u.z), bf16_hi(v.z), acc);
+        acc = fmaf(bf16_lo(u.w), bf16_lo(v.w), acc);
+        acc = fmaf(bf16_hi(u.w), bf16_hi(v.w), acc);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    }
+    if (lane == 0) dp[i] = acc;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_score_grad(const void* h3, const void* dY, int D, int K, const int* inv, float* dp, int T,
+                              int num_sms, cudaStream_t stream, const int* hdr) {
+  if (T <= 0) return cudaSuccess;
+  const int blocks = max(1, min((T * K + 7) / 8, num_sms * 8));
+  score_grad_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(h3),
+                                                static_cast<const __nv_bfloat16*>(dY), D, K, inv, dp, T, hdr);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const void* h, int D, int K, const int* inv, const float* scores, void* out, int T,
                            bool accumulate, int num_sms, cudaStream_t stream, const int* hdr) {

@@ -5,8 +5,9 @@
 // Dist-MoE explainer section 02, "Quantization Axes for Forward and
 // Backward": FPROP/DGRAD operands are scaled along the feature axis (row
 // bundles, launch_gather_rows); WGRAD contracts over token rows and needs a
-// separately quantised column-oriented bundle (launch_gather_cols, stored
-// transposed [D, r_cap] so the GEMM reads it K-major).  MXFP8 training
+// separately quantised column-oriented bundle (stored transposed [D, r_cap]
+// so the GEMM reads it K-major); launch_gather_both writes both bundles of
+// the same rows in one pass when training.  MXFP8 training
 // quantises after the gather ("MXFP8 training publishes BF16 source rows and
 // quantizes after peer gather"); row quantisation depends only on the row,
 // so quantising after the gather is exact.  Pad rows (route -1) are zero.
@@ -103,80 +104,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
   }
 }
 
-// One CTA per (32-row group, 256-column slab): load the 32 gathered rows
-// into shared memory, then each thread owns one column d and writes its 32
-// row values contiguously to dstT[d][r0 .. r0+31] (one MX block along rows).
-template <bool MX, bool SCALE>
-__global__ void __launch_bounds__(256) gather_cols_kernel(const __nv_bfloat16* __restrict__ src, int D, int K,
-                                                          const int* __restrict__ hdr, const int* __restrict__ perm,
-                                                          const float* __restrict__ scores, void* __restrict__ dstT,
-                                                          uint8_t* __restrict__ dstT_sf, int r_cap, int b_cap,
-                                                          const int* __restrict__ row_block,
-                                                          const int4* __restrict__ blocks) {
-  __shared__ float tile[32][257];
-  const int rows = hdr[2];
-  const int c0 = blockIdx.x * 256;
-  const int tid = threadIdx.x;
-  for (int rg = blockIdx.y; rg * 32 < rows; rg += gridDim.y) {
-    const int r0 = rg * 32;
-    for (int i = tid; i < 32 * 32; i += 256) {
-      const int row = i >> 5, chunk = i & 31;
-      const int c = c0 + chunk * 8;
-      float v[8];
-      const int route = perm[r0 + row];
-      if (route >= 0 && c < D) {
-        unpack8(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(route / K) * D + c)), v);
-        if (SCALE) {
-          const float s = scores[route];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = s * v[j];
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) tile[row][chunk * 8 + j] = v[j];
-    }
-    __syncthreads();
-    const int d = c0 + tid;
-    if (d < D) {
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = tile[i][tid];
-      if (!MX) {
-        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dstT) + static_cast<long long>(d) * r_cap + r0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          o[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-      } else {
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        const int e = mx_shared_exp(amax);
-        const float inv = exp2_int(-e);
-        uint32_t w[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
-        uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dstT) + static_cast<long long>(d) * r_cap + r0);
-        o[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        o[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        const int b = row_block[rg];
-        const int l = rg - (blocks[b].y >> 5);
-        dstT_sf[(static_cast<long long>(d >> 7) * b_cap + b) * 512 + sf_atom_byte(d & 127, l)] =
-            static_cast<uint8_t>(e + 127);
-      }
-    }
-    __syncthreads();
-  }
-}
+// Both bundles in one pass (training).  One CTA per (128-row tile,
+// 128-column slab): the gathered rows go through shared memory once, then
+//  * row bundle: warp w writes rows 16w .. 16w+15, lane l columns 4l .. 4l+3
+//    (8 lanes per MX block; 128 contiguous bytes per row and warp);
+//  * column bundle: thread (c, half) writes feature c0+c for rows
+//    64*half .. +63, i.e. 64 contiguous bytes (two MX blocks) per thread, so
+//    two threads fill each 128-byte line of dstT[feature][rows] at once.
+constexpr int kBothRows = 128, kBothCols = 128, kBothPitch = kBothCols + 4;
+constexpr int kBothSmem = kBothRows * kBothPitch * 4;
 
-// Both bundles in one pass (training): one CTA per (32-row group, 256-column
-// slab) loads the gathered rows into shared memory once, then writes the row
-// bundle (warp w: rows 4w..4w+3, lane l: columns 8l..8l+7, 4 lanes per MX
-// block) and the transposed column bundle (thread d: one column, 32 rows).
 template <bool MX, bool SCALE>
 __global__ void __launch_bounds__(256) gather_both_kernel(const __nv_bfloat16* __restrict__ src, int D, int K,
                                                           const int* __restrict__ hdr, const int* __restrict__ perm,
@@ -185,76 +122,78 @@ __global__ void __launch_bounds__(256) gather_both_kernel(const __nv_bfloat16* _
                                                           uint8_t* __restrict__ dstT_sf, int r_cap, int b_cap,
                                                           const int* __restrict__ row_block,
                                                           const int4* __restrict__ blocks) {
-  __shared__ float tile[32][257];
+  extern __shared__ float4 smem_f4[];
+  float* tile = reinterpret_cast<float*>(smem_f4);  // [128][kBothPitch]
   const int rows = hdr[2];
-  const int c0 = blockIdx.x * 256;
+  const int r0 = blockIdx.y * kBothRows;
+  if (r0 >= rows) return;
+  const int c0 = blockIdx.x * kBothCols;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int rg = blockIdx.y; rg * 32 < rows; rg += gridDim.y) {
-    const int r0 = rg * 32;
-    const int b = MX ? row_block[rg] : 0;
-    const int p0 = MX ? r0 - blocks[b].y : 0;   // first row of the group within its block
-    for (int i = tid; i < 32 * 32; i += 256) {
-      const int row = i >> 5, chunk = i & 31;
-      const int c = c0 + chunk * 8;
-      float v[8];
-      const int route = perm[r0 + row];
-      if (route >= 0 && c < D) {
-        unpack8(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(route / K) * D + c)), v);
-        if (SCALE) {
-          const float s = scores[route];
+  // ---- load 128 gathered rows x 128 columns (16 chunks of 8 values per row)
+  for (int i = tid; i < kBothRows * 16; i += 256) {
+    const int row = i >> 4, chunk = i & 15;
+    const int c = c0 + chunk * 8;
+    float v[8];
+    const int route = (r0 + row < r_cap) ? perm[r0 + row] : -1;
+    if (route >= 0 && c < D) {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(route / K) * D + c)), v);
+      if (SCALE) {
+        const float s = scores[route];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = s * v[j];
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+        for (int j = 0; j < 8; ++j) v[j] = s * v[j];
       }
+    } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) tile[row][chunk * 8 + j] = v[j];
+      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
     }
-    __syncthreads();
-    // ---- row bundle
-    const int c = c0 + lane * 8;
-    for (int rr = 0; rr < 4; ++rr) {
-      const int row = warp * 4 + rr;
-      const long long r = r0 + row;
-      float v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = tile[row][lane * 8 + j];
-      if (!MX) {
-        if (c < D)
-          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + r * D + c) =
-              make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                         pack_bf16x2(v[6], v[7]));
-      } else {
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-        const int e = mx_shared_exp(amax);
-        const float inv = exp2_int(-e);
-        uint2 q;
-        q.x = cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
-        q.y = cvt_e4m3x2(v[4] * inv, v[5] * inv) | (cvt_e4m3x2(v[6] * inv, v[7] * inv) << 16);
-        if (c < D) {
-          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(dst) + r * D + c) = q;
-          if ((lane & 3) == 0) {
-            const int kb = c >> 5;
-            dst_sf[(static_cast<long long>(b) * (D / 128) + (kb >> 2)) * 512 + sf_atom_byte(p0 + row, kb & 3)] =
-                static_cast<uint8_t>(e + 127);
-          }
+    float4* t4 = reinterpret_cast<float4*>(tile + row * kBothPitch + chunk * 8);
+    t4[0] = make_float4(v[0], v[1], v[2], v[3]);
+    t4[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+  __syncthreads();
+  // ---- row bundle
+  const int c = c0 + lane * 4;
+  for (int rr = 0; rr < 16; ++rr) {
+    const int row = warp * 16 + rr;
+    const int r = r0 + row;
+    const float4 x4 = *reinterpret_cast<const float4*>(tile + row * kBothPitch + lane * 4);
+    if (!MX) {
+      if (c < D && r < rows)
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dst) + static_cast<long long>(r) * D + c) =
+            make_uint2(pack_bf16x2(x4.x, x4.y), pack_bf16x2(x4.z, x4.w));
+    } else {
+      float amax = fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w)));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+      const int e = mx_shared_exp(amax);
+      const float inv = exp2_int(-e);
+      const uint32_t q = cvt_e4m3x2(x4.x * inv, x4.y * inv) | (cvt_e4m3x2(x4.z * inv, x4.w * inv) << 16);
+      if (c < D && r < rows) {
+        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(dst) + static_cast<long long>(r) * D + c) = q;
+        if ((lane & 7) == 0) {
+          const int b = row_block[r >> 5];
+          const int kb = c >> 5;
+          dst_sf[(static_cast<long long>(b) * (D / 128) + (kb >> 2)) * 512 + sf_atom_byte(r - blocks[b].y, kb & 3)] =
+              static_cast<uint8_t>(e + 127);
         }
       }
     }
-    // ---- column bundle
-    const int d = c0 + tid;
-    if (d < D) {
+  }
+  // ---- column bundle
+  const int cc = tid & 127, half = tid >> 7;
+  const int d = c0 + cc;
+  if (d < D) {
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const int rl = half * 64 + g * 32;   // first row of this 32-row group within the tile
+      const int rg = (r0 + rl) >> 5;
+      if (r0 + rl >= rows) break;
       float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = tile[i][tid];
+      for (int i = 0; i < 32; ++i) v[i] = tile[(rl + i) * kBothPitch + cc];
       if (!MX) {
-        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dstT) + static_cast<long long>(d) * r_cap + r0);
+        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dstT) + static_cast<long long>(d) * r_cap + r0 + rl);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           o[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
@@ -269,26 +208,30 @@ __global__ void __launch_bounds__(256) gather_both_kernel(const __nv_bfloat16* _
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
-        uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dstT) + static_cast<long long>(d) * r_cap + r0);
+        uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dstT) + static_cast<long long>(d) * r_cap + r0 + rl);
         o[0] = make_uint4(w[0], w[1], w[2], w[3]);
         o[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        dstT_sf[(static_cast<long long>(d >> 7) * b_cap + b) * 512 + sf_atom_byte(d & 127, p0 >> 5)] =
+        const int b = row_block[rg];
+        dstT_sf[(static_cast<long long>(d >> 7) * b_cap + b) * 512 + sf_atom_byte(d & 127, rg - (blocks[b].y >> 5))] =
             static_cast<uint8_t>(e + 127);
       }
     }
-    __syncthreads();
   }
 }
 
 template <bool MX, bool SCALE>
 cudaError_t both_impl(const void* src, int D, int K, const RoutingPtrs& rp, void* dst, uint8_t* dst_sf, void* dstT,
-                      uint8_t* dstT_sf, int r_cap, int b_cap, int num_sms, cudaStream_t stream) {
-  const int xs = (D + 255) / 256;
-  const int ys = max(1, min(r_cap / 32, (num_sms * 8 + xs - 1) / xs));
-  dim3 grid(xs, ys);
-  gather_both_kernel<MX, SCALE><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr,
-                                                          rp.perm, rp.scores, dst, dst_sf, dstT, dstT_sf, r_cap,
-                                                          b_cap, rp.row_block, rp.blocks);
+                      uint8_t* dstT_sf, int r_cap, int b_cap, int /*num_sms*/, cudaStream_t stream) {
+  auto kern = gather_both_kernel<MX, SCALE>;
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBothSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid((D + kBothCols - 1) / kBothCols, (r_cap + kBothRows - 1) / kBothRows);
+  kern<<<grid, 256, kBothSmem, stream>>>(static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr, rp.perm, rp.scores,
+                                         dst, dst_sf, dstT, dstT_sf, r_cap, b_cap, rp.row_block, rp.blocks);
   return cudaGetLastError();
 }
 
@@ -304,16 +247,6 @@ cudaError_t rows_impl(const void* src, int D, int K, const RoutingPtrs& rp, void
   return cudaGetLastError();
 }
 
-template <bool MX, bool SCALE>
-cudaError_t cols_impl(const void* src, int D, int K, const RoutingPtrs& rp, void* dstT, uint8_t* dstT_sf, int r_cap,
-                      int b_cap, cudaStream_t stream) {
-  dim3 grid((D + 255) / 256, r_cap / 32);
-  gather_cols_kernel<MX, SCALE><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr,
-                                                          rp.perm, rp.scores, dstT, dstT_sf, r_cap, b_cap,
-                                                          rp.row_block, rp.blocks);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 cudaError_t launch_gather_rows(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
@@ -324,16 +257,6 @@ cudaError_t launch_gather_rows(bool mx, bool use_scores, const void* src, int D,
   }
   return use_scores ? rows_impl<false, true>(src, D, K, rp, dst, dst_sf, r_cap, num_sms, stream)
                     : rows_impl<false, false>(src, D, K, rp, dst, dst_sf, r_cap, num_sms, stream);
-}
-
-cudaError_t launch_gather_cols(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
-                               void* dstT, uint8_t* dstT_sf, int r_cap, int b_cap, cudaStream_t stream) {
-  if (mx) {
-    return use_scores ? cols_impl<true, true>(src, D, K, rp, dstT, dstT_sf, r_cap, b_cap, stream)
-                      : cols_impl<true, false>(src, D, K, rp, dstT, dstT_sf, r_cap, b_cap, stream);
-  }
-  return use_scores ? cols_impl<false, true>(src, D, K, rp, dstT, dstT_sf, r_cap, b_cap, stream)
-                    : cols_impl<false, false>(src, D, K, rp, dstT, dstT_sf, r_cap, b_cap, stream);
 }
 
 cudaError_t launch_gather_both(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,

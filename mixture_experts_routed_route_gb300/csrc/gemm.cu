@@ -34,8 +34,9 @@
 // Warp roles (one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (one thread)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2-9   epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and the
-//               32-column chunks 2i + (w-2)/4 of the accumulator
+//   warps 2..    epilogue (8 warps; 16 for the weight-gradient store):
+//               warp w reads TMEM lanes 32*(w%4) .. +31 and every
+//               (EPI_WARPS/4)-th 32-column chunk of the accumulator
 #include "kernels.cuh"
 
 namespace moe {
@@ -45,9 +46,13 @@ namespace {
 constexpr int kABytes = 128 * 128;  // one 128-row x 128-byte operand tile
 constexpr int kBBytes = 128 * 128;
 constexpr int kAtom = 512;          // one scale atom
-constexpr int kEpiWarps = 8;
-constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kEpiBarrier = 1;      // named barrier of the epilogue warps
+// Tile metadata cached in shared memory at kernel start, so no role pays a
+// dependent global load per tile: the routing's row blocks (grouped-M, the
+// first kCacheBlocks of them) or the experts' row offsets and first blocks
+// (grouped-K, E <= 1024).
+constexpr int kCacheBlocks = 1024;
+constexpr int kCacheBytes = 16384;
 
 struct Tile {
   int e;
@@ -64,12 +69,18 @@ struct Tile {
   long long sfb_atom;     // atom index of stage 0 for B
 };
 
+struct MetaCache {
+  const int4* blocks;   // grouped-M: s_blocks[b] for b < kCacheBlocks
+  const int* poff;      // grouped-K: poffsets[0..E]
+  const int* bstart;    // grouped-K: bstart[0..E]
+};
+
 template <int MODE, int BK>
-__device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int nblk) {
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int nblk, const MetaCache& mc) {
   Tile t;
   if (MODE == kGroupedM) {
     const int n = tile / nblk, b = tile - n * nblk;
-    const int4 blk = p.blocks[b];
+    const int4 blk = (b < kCacheBlocks) ? mc.blocks[b] : p.blocks[b];
     t.e = blk.x;
     t.blk = b;
     t.a_row[0] = blk.x * p.a_rows_per_expert + n * 128;
@@ -88,7 +99,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int n
     const int per_e = p.m_tiles * p.n_tiles;
     const int e = tile / per_e, rem = tile - e * per_e;
     const int m = rem / p.n_tiles, n = rem - m * p.n_tiles;
-    const int k0 = p.poffsets[e], klen = p.poffsets[e + 1] - k0;
+    const int k0 = mc.poff[e], klen = mc.poff[e + 1] - k0;
     t.e = e;
     t.blk = 0;
     t.a_row[0] = m * 128;
@@ -100,7 +111,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int n
     t.klast = klen - (t.kstages - 1) * BK;
     t.out_row0 = m * 128;
     t.out_col0 = n * 128;
-    const int b0 = (p.bstart != nullptr) ? p.bstart[e] : 0;
+    const int b0 = mc.bstart[e];
     t.sfa_atom[0] = static_cast<long long>(m) * p.sfa_ts + b0;
     t.sfa_atom[1] = 0;
     t.sfb_atom = static_cast<long long>(n) * p.sfb_ts + b0;
@@ -171,7 +182,8 @@ __device__ __forceinline__ void store_col32(const GemmParams& p, long long feat,
 }
 
 // ------------------------------------------------------------- epilogues
-// Each takes the warp's column half `h`: it drains chunks c0 = 32*(2i + h).
+// Each takes the warp's chunk index `h` (0..EPI_WARPS/4-1) and drains the
+// 32-column chunks c0 = 32h, 32h + 32*(EPI_WARPS/4), ...
 
 // h3 / input-gradient rows: out[row][feature] = bf16(acc).
 __device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow, int h) {
@@ -222,20 +234,36 @@ __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& 
 // Fused SwiGLU backward: dh2 from the accumulator (W2 DGRAD), g and u from
 // the saved BF16 h1, dg = dh2 u SiLU'(g), du = dh2 SiLU(g), written as the
 // dh1 row bundle (W13 DGRAD's operand) and column bundle (W13 WGRAD's).
+// h1 does not depend on the MMA, so the caller issues the loads of the
+// warp's first chunk before it waits for the accumulator.
+__device__ __forceinline__ void load_h1_chunk(const GemmParams& p, const Tile& t, int f, int c0,
+                                              uint32_t (&hp)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    hp[i] = 0;
+    if (c0 + i < t.b_rows) {
+      const long long row = t.out_row0 + c0 + i;
+      const uint32_t g = __bfloat16_as_ushort(p.h1[row * p.h1_pitch + f]);
+      const uint32_t u = __bfloat16_as_ushort(p.h1[row * p.h1_pitch + p.F + f]);
+      hp[i] = g | (u << 16);
+    }
+  }
+}
+
 template <bool MX>
 __device__ __forceinline__ void epi_swiglu_bwd(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow,
-                                               int lane, int h) {
+                                               int lane, int h, uint32_t (&hp)[32]) {
   const int f = t.out_col0 + lrow;
   for (int c0 = 32 * h; c0 < t.b_rows; c0 += 64) {
+    if (c0 != 32 * h) load_h1_chunk(p, t, f, c0, hp);   // the first chunk was prefetched
     uint32_t v[32];
     tmem_ld32(tbase + c0, v);
     tmem_ld_wait();
     float dg[32], du[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const long long row = t.out_row0 + c0 + i;
-      const float g = __bfloat162float(p.h1[row * p.h1_pitch + f]);
-      const float u = __bfloat162float(p.h1[row * p.h1_pitch + p.F + f]);
+      const float g = bf16_lo(hp[i]);
+      const float u = bf16_hi(hp[i]);
       const float dh2 = u2f(v[i]);
       const float s = sigmoid_f(g);
       dg[i] = dh2 * u * (s * (1.0f + g * (1.0f - s)));
@@ -255,11 +283,11 @@ __device__ __forceinline__ void epi_swiglu_bwd(const GemmParams& p, const Tile& 
 // Weight gradient with plain stores: dW[e][m][n0 ..], FP32 or accumulate.
 // An expert without rows gets zeros, or is left as is when adding.
 __device__ __forceinline__ void epi_wgrad_direct(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow,
-                                                 int h) {
+                                                 int h, int step) {
   if (t.kstages == 0 && p.dw_accum) return;
   const long long M = static_cast<long long>(p.m_tiles) * 128;
   const long long row = static_cast<long long>(t.e) * M + t.out_row0 + lrow;
-  for (int c0 = 32 * h; c0 < 128; c0 += 64) {
+  for (int c0 = 32 * h; c0 < 128; c0 += step) {
     float v[32];
     if (t.kstages > 0) {
       uint32_t r[32];
@@ -312,30 +340,19 @@ __device__ __forceinline__ void epi_wgrad_direct(const GemmParams& p, const Tile
 // tile is written into a 32 KB staging buffer as two 128-row x 128-byte
 // boxes in the 128-byte swizzle (16-byte chunk j of row m at chunk
 // j ^ (m % 8), so 8 consecutive rows hit 8 different bank groups), then one
-// thread stores both boxes with TMA.  Returns after the TMEM reads, so the
-// caller can release the accumulator before the smem write-out.
-__device__ __forceinline__ void epi_wgrad_stage(const Tile& t, uint32_t tbase, int lrow, int h, uint8_t* stg) {
-  for (int c0 = 32 * h; c0 < 128; c0 += 64) {
-    float v[32];
-    if (t.kstages > 0) {
-      uint32_t r[32];
-      tmem_ld32(tbase + c0, r);
-      tmem_ld_wait();
+// thread stores both boxes with TMA.  The warp's two 32-column chunks
+// (c0 = 32h and 32h + 64) arrive already loaded from TMEM in r0 / r1.
+__device__ __forceinline__ void stage_chunk(const uint32_t (&r)[32], bool zero, int c0, int lrow, uint8_t* stg) {
+  uint8_t* box = stg + (c0 >> 6) * 16384 + lrow * 128;
+  const int j0 = (c0 & 63) >> 3;  // first 16-byte chunk of these 32 columns
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-    }
-    uint8_t* box = stg + (c0 >> 6) * 16384 + lrow * 128;
-    const int j0 = (c0 & 63) >> 3;  // first 16-byte chunk of these 32 columns
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int phys = (j0 + q) ^ (lrow & 7);
-      *reinterpret_cast<uint4*>(box + phys * 16) =
-          make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                     pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-    }
+  for (int q = 0; q < 4; ++q) {
+    const int phys = (j0 + q) ^ (lrow & 7);
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (!zero)
+      w = make_uint4(pack_bf16x2(u2f(r[8 * q + 0]), u2f(r[8 * q + 1])), pack_bf16x2(u2f(r[8 * q + 2]), u2f(r[8 * q + 3])),
+                     pack_bf16x2(u2f(r[8 * q + 4]), u2f(r[8 * q + 5])), pack_bf16x2(u2f(r[8 * q + 6]), u2f(r[8 * q + 7])));
+    *reinterpret_cast<uint4*>(box + phys * 16) = w;
   }
 }
 
@@ -355,8 +372,13 @@ struct Cfg {
   static constexpr int BK = MX ? 128 : 64;                 // contraction elements per stage
   static constexpr int KMMA = MX ? 32 : 16;                // contraction elements per MMA
   static constexpr int MMAS = BK / KMMA;
-  static constexpr int THREADS = 64 + kEpiThreads;
-  static constexpr int SMEM = 1024 + S * STAGE + STAGING + 256;
+  // epilogue warps: 8 (two per TMEM lane quadrant, alternate 32-column
+  // chunks); the weight-gradient store has 16 (one chunk each), since its
+  // per-tile work is almost all epilogue
+  static constexpr int EPI_WARPS = WGRAD ? 16 : 8;
+  static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int THREADS = 64 + EPI_THREADS;
+  static constexpr int SMEM = 1024 + S * STAGE + STAGING + 256 + kCacheBytes;
 };
 
 template <bool MX, int NA, int EPI, int MODE>
@@ -376,6 +398,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_abort = abort_flag + 1;  // epilogue warps leave together
+  uint8_t* cache = staging + C::STAGING + 256;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -385,7 +408,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     }
     for (int a = 0; a < C::ACC_BUFS; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps);
+      mbar_init(&tempty[a], C::EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -406,6 +429,21 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
 
   const int nblk = (MODE == kGroupedM) ? p.hdr[1] : 0;
   const int num_tiles = (MODE == kGroupedM) ? nblk * p.n_tiles : p.E * p.m_tiles * p.n_tiles;
+  MetaCache mc;
+  mc.blocks = reinterpret_cast<const int4*>(cache);
+  mc.poff = reinterpret_cast<const int*>(cache);
+  mc.bstart = reinterpret_cast<const int*>(cache) + 1028;
+  if (MODE == kGroupedM) {
+    int4* sb = reinterpret_cast<int4*>(cache);
+    for (int i = threadIdx.x; i < min(nblk, kCacheBlocks); i += blockDim.x) sb[i] = p.blocks[i];
+  } else {
+    int* sp = reinterpret_cast<int*>(cache);
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+      sp[i] = p.poffsets[i];
+      sp[1028 + i] = (p.bstart != nullptr) ? p.bstart[i] : 0;
+    }
+  }
+  __syncthreads();
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -413,7 +451,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk);
+        const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk, mc);
         for (int ks = 0; ks < t.kstages; ++ks, ++it) {
           const uint32_t slot = it % S, ph = (it / S) & 1;
           if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag, p.err)) {
@@ -427,8 +465,8 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
           const int kx = t.k0 + ks * C::BK;
 #pragma unroll
           for (int j = 0; j < NA; ++j) tma_load_2d(sa + j * kABytes, &tmA, &full[slot], kx, t.a_row[j]);
-          for (int c = 0; c < t.b_rows / 32; ++c)
-            tma_load_2d(sb + c * 4096, &tmB, &full[slot], kx, t.b_row0 + 32 * c);
+          for (int c = 0; c < t.b_rows / p.b_box_rows; ++c)
+            tma_load_2d(sb + c * p.b_box_rows * 128, &tmB, &full[slot], kx, t.b_row0 + p.b_box_rows * c);
           if (MX) {
 #pragma unroll
             for (int j = 0; j < NA; ++j)
@@ -450,7 +488,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       uint32_t it = 0, tc = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++tc) {
-        const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk);
+        const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk, mc);
         const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
@@ -499,46 +537,55 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     const int q = warp & 3;              // TMEM lane quadrant of this warp
     const int h = (warp - 2) >> 2;       // which 32-column chunks it drains
     const int lrow = q * 32 + lane;
-    const int etid = threadIdx.x - 64;   // 0 .. kEpiThreads-1
+    const int etid = threadIdx.x - 64;   // 0 .. EPI_THREADS-1
     const bool staged = C::WGRAD && p.tma_store;
     uint32_t tc = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
-      const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk);
+      const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk, mc);
       const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
+      uint32_t hp[32];
+      if (EPI == kEpiSwigluBwd && 32 * h < t.b_rows) load_h1_chunk(p, t, t.out_col0 + lrow, 32 * h, hp);
       const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&tfull[acc], aph, abort_flag, p.err));
-      uint8_t* stg = staging + (tc & 1) * 32768;
-      if (staged) {
-        // Every epilogue warp reaches this barrier once per tile whether its
-        // (bounded) wait succeeded or not, so a warp that gives up cannot
-        // leave the others blocked in it: they all see the flag and leave.
-        if (!ok && lane == 0) *epi_abort = 1;
-        // the buffer used two tiles ago must have been read by its TMA store
-        if (etid == 0) bulk_wait_read<1>();
-        named_bar_sync(kEpiBarrier, kEpiThreads);
-        if (*epi_abort) break;
-      } else if (!ok) {
-        break;
-      }
+      if (!staged && !ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
-      if (EPI == kEpiStore) epi_store(p, t, tbase, lrow, h);
-      else if (EPI == kEpiSwigluFwd) epi_swiglu_fwd<MX>(p, t, tbase, lrow, lane, h);
-      else if (EPI == kEpiSwigluBwd) epi_swiglu_bwd<MX>(p, t, tbase, lrow, lane, h);
-      else if (staged) epi_wgrad_stage(t, tbase, lrow, h, stg);
-      else epi_wgrad_direct(p, t, tbase, lrow, h);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
       if (staged) {
+        uint8_t* stg = staging + (tc & 1) * 32768;
+        // start both TMEM reads, then (while they are in flight) make sure the
+        // staging buffer's previous TMA store has finished reading it.  Every
+        // epilogue warp reaches the barrier once per tile whether its bounded
+        // wait succeeded or not, so a warp that gives up cannot leave the
+        // others blocked in it: they all see the flag and leave together.
+        // one 32-column chunk per warp (16 epilogue warps)
+        uint32_t r0[32];
+        const bool has = ok && t.kstages > 0;
+        if (has) tmem_ld32(tbase + 32 * h, r0);
+        if (!ok && lane == 0) *epi_abort = 1;
+        if (etid == 0) bulk_wait_read<1>();
+        named_bar_sync(kEpiBarrier, C::EPI_THREADS);
+        tmem_ld_wait();
+        if (*epi_abort) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        stage_chunk(r0, !has, 32 * h, lrow, stg);
         fence_proxy_async_smem();
-        named_bar_sync(kEpiBarrier, kEpiThreads);
+        named_bar_sync(kEpiBarrier, C::EPI_THREADS);
         if (etid == 0) {
           const int y = t.e * p.m_tiles * 128 + t.out_row0;
           tma_store_2d(&tmC, stg, t.out_col0, y);
           tma_store_2d(&tmC, stg + 16384, t.out_col0 + 64, y);
           bulk_commit();
         }
+        continue;
       }
+      if (EPI == kEpiStore) epi_store(p, t, tbase, lrow, h);
+      else if (EPI == kEpiSwigluFwd) epi_swiglu_fwd<MX>(p, t, tbase, lrow, lane, h);
+      else if (EPI == kEpiSwigluBwd) epi_swiglu_bwd<MX>(p, t, tbase, lrow, lane, h, hp);
+      else epi_wgrad_direct(p, t, tbase, lrow, h, 32 * (C::EPI_WARPS / 4));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
     }
     if (staged && etid == 0) bulk_wait<0>();
   }
@@ -571,6 +618,8 @@ cudaError_t launch_impl(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
 
 cudaError_t launch_gemm(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   if (g.max_tiles <= 0) return cudaSuccess;
+  // B boxes must tile every row block (32-row multiples) or the 128-row K-mode tile
+  if (g.p.b_box_rows != 32 && !(g.p.b_box_rows == 128 && g.mode == kGroupedK)) return cudaErrorInvalidValue;
 #define MOE_GEMM_CASE(MXV, NAV, EPIV, MODEV)                                         \
   if (g.mx == MXV && g.na == NAV && g.epi == EPIV && g.mode == MODEV)                \
     return launch_impl<MXV, NAV, EPIV, MODEV>(g, num_sms, stream);

@@ -39,12 +39,9 @@ cudaError_t launch_route(const int32_t* ids, const float* scores, int T, int K, 
 cudaError_t launch_gather_rows(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
                                void* dst, uint8_t* dst_sf, int r_cap, int num_sms, cudaStream_t stream);
 
-// Column bundle: dstT[d][r] = the same values transposed to [D, r_cap]; MXFP8
-// quantises along rows in 32-row blocks (WGRAD contracts over rows).
-cudaError_t launch_gather_cols(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
-                               void* dstT, uint8_t* dstT_sf, int r_cap, int b_cap, cudaStream_t stream);
-
-// Row and column bundles of the same gathered rows in one pass (training).
+// Row bundle and column bundle of the same gathered rows in one pass
+// (training): dstT[d][r] holds the rows transposed to [D, r_cap]; MXFP8
+// quantises it along rows in 32-row blocks (WGRAD contracts over rows).
 cudaError_t launch_gather_both(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
                                void* dst, uint8_t* dst_sf, void* dstT, uint8_t* dstT_sf, int r_cap, int b_cap,
                                int num_sms, cudaStream_t stream);
@@ -54,6 +51,11 @@ cudaError_t launch_gather_both(bool mx, bool use_scores, const void* src, int D,
 // hdr[0] (read on the device, at most T) when `hdr` is given.
 cudaError_t launch_combine(const void* h, int D, int K, const int* inv, const float* scores, void* out, int T,
                            bool accumulate, int num_sms, cudaStream_t stream, const int* hdr = nullptr);
+
+// dp[t*K+k] = <h3[inv(t,k)], dY[t]> in FP32 (fixed order), 0 if inactive;
+// tokens t < min(T, hdr[0]).
+cudaError_t launch_score_grad(const void* h3, const void* dY, int D, int K, const int* inv, float* dp, int T,
+                              int num_sms, cudaStream_t stream, const int* hdr);
 
 cudaError_t launch_prep_mx_weight(const void* w, int E, int N, int K, uint8_t* q, uint8_t* sf, uint8_t* qT,
                                   uint8_t* sfT, cudaStream_t stream);
@@ -76,6 +78,7 @@ struct GemmParams {
   int K;                  // grouped-M: contraction length
   int a_rows_per_expert;  // grouped-M: rows of A per expert
   int a_up_offset;        // SwiGLU forward: row offset of the up half (F)
+  int b_box_rows;         // rows of one B tensor-map box (32, or 128 in grouped-K)
   // MXFP8 scale atoms of the operands (512 bytes each).  Atom of an A tile:
   // grouped-M (A row / 128) * sfa_ts + stage, grouped-K m_tile * sfa_ts +
   // (first block of the expert + stage); B likewise with the row block

@@ -203,6 +203,7 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   g1.p.blocks = rp.blocks;
   g1.p.poffsets = rp.poffsets;
   g1.p.E = E;
+  g1.p.b_box_rows = 32;
   g1.p.n_tiles = F / 128;
   g1.p.K = D;
   g1.p.a_rows_per_expert = 2 * F;
@@ -233,6 +234,7 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   g2.p.blocks = rp.blocks;
   g2.p.poffsets = rp.poffsets;
   g2.p.E = E;
+  g2.p.b_box_rows = 32;
   g2.p.n_tiles = D / 128;
   g2.p.K = F;
   g2.p.a_rows_per_expert = D;

@@ -107,7 +107,7 @@ class MoELayer:
         return out
 
     def backward(self, saved, dout, W13, W2, dx=None, dW13=None, dW2=None, accumulate_dx=False, dw_fp32=False,
-                 dw_accumulate=False, stream=None):
+                 dw_accumulate=False, d_scores=None, stream=None):
         T = dout.shape[0]
         dt = torch.float32 if dw_fp32 else torch.bfloat16
         if dx is None:
@@ -118,5 +118,5 @@ class MoELayer:
             dW2 = torch.empty((self.E, self.D, self.F), dtype=dt, device=self.device)
         flags = ((abi.MOE_ACCUMULATE_DX if accumulate_dx else 0) | (abi.MOE_DW_FP32 if dw_fp32 else 0)
                  | (abi.MOE_DW_ACCUMULATE if dw_accumulate else 0))
-        abi.moe_backward(self.ctx, saved, dout, W13.struct, W2.struct, dx, dW13, dW2, flags, stream)
+        abi.moe_backward(self.ctx, saved, dout, W13.struct, W2.struct, dx, dW13, dW2, d_scores, flags, stream)
         return dx, dW13, dW2

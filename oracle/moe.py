@@ -26,6 +26,7 @@ op order W2 DGRAD/WGRAD, SwiGLU backward, W13 DGRAD/WGRAD, K-reduction):
     dxr = R( q(dh1)_row . W13[e] ),   dX[t] = R( init[t] + sum_k dxr(t,k) )
     dW2[e]  = Rw( sum_rows dh3_colT . h2_col )
     dW13[e] = Rw( sum_rows dh1_colT . x_col )
+    dp(t,k) = <h3(t,k), dY[t]>        (score gradient, unrounded)
 
 Readings of the pages (each also listed in the design notes)
 ------------------------------------------------------------
@@ -219,8 +220,8 @@ def combine(h3, inv, scores, out_init, precision):
 def backward(state, dY, w13, w2, dx_init=None, dw_fp32=False):
     """Backward of ``forward`` (see module docstring).
 
-    Returns dict with dX [T,D], dW13 [E,2F,D], dW2 [E,D,F] and the
-    intermediates dh3/dh2/dh1/dxr per padded row.
+    Returns dict with dX [T,D], dp [T,K] (score gradient), dW13 [E,2F,D],
+    dW2 [E,D,F] and the intermediates dh3/dh2/dh1/dxr per padded row.
     """
     p = state["precision"]
     rt = state["routing"]
@@ -271,7 +272,14 @@ def backward(state, dY, w13, w2, dx_init=None, dw_fp32=False):
         on = inv[:, k] >= 0
         acc[on] += dxr[inv[on, k]]
     dX = _round_out(acc, p)
-    return dict(dX=dX, dW13=dW13, dW2=dW2, dh3=dh3, dh3_row=dh3_row,
+    # score gradient dp(t,k) = <h3(t,k), dY[t]> (blog section 2, "SwiGLU
+    # backward": the routing-weight gradient of the weighted combine); zero for
+    # inactive routes
+    dp = np.zeros((T, K))
+    for k in range(K):
+        on = inv[:, k] >= 0
+        dp[on, k] = np.sum(state["h3"][inv[on, k]] * dY[on], axis=1)
+    return dict(dX=dX, dp=dp, dW13=dW13, dW2=dW2, dh3=dh3, dh3_row=dh3_row,
                 dh3_col=dh3_col, dh2=dh2, dh1=dh1, dh1_row=dh1_row,
                 dh1_col=dh1_col, dxr=dxr, h2_col=h2_col, x_col=x_col)
 

@@ -77,9 +77,10 @@ def run_gpu(case, precision=None, training=True, debug=False, out_init=None, max
         dx = torch.zeros((T, w.D), dtype=torch.bfloat16, device=dev)
         if dx_init is not None:
             dx.copy_(dx_init)
+        dp = torch.full((T, w.K), float("nan"), dtype=torch.float32, device=dev)
         dx, dW13, dW2 = layer.backward(saved, dy, W13, W2, dx=dx, accumulate_dx=dx_init is not None,
-                                       dw_fp32=dw_fp32)
-        res.update(dx=to_f64(dx), dW13=to_f64(dW13), dW2=to_f64(dW2))
+                                       dw_fp32=dw_fp32, d_scores=dp)
+        res.update(dx=to_f64(dx), dW13=to_f64(dW13), dW2=to_f64(dW2), dp=to_f64(dp))
     torch.cuda.synchronize()
     res["err_bits"] = layer.error_bits()
     return res
@@ -93,7 +94,7 @@ def run_oracle(case, precision=None, out_init=None, dx_init=None, dw_fp32=False,
     res = {"state": st, "out": st["out"]}
     if backward:
         g = moe.backward(st, to_f64(case.dy), w13, w2, dx_init=dx_init, dw_fp32=dw_fp32)
-        res.update(dx=g["dX"], dW13=g["dW13"], dW2=g["dW2"], grads=g)
+        res.update(dx=g["dX"], dW13=g["dW13"], dW2=g["dW2"], dp=g["dp"], grads=g)
     return res
 
 

@@ -44,8 +44,9 @@ def test_backward_matches_oracle(name):
     g = run_gpu(case)
     o = run_oracle(case)
     assert g["err_bits"] == 0
-    for k in ("out", "dx") if p == "mxfp8" else ("out", "dx", "dW13", "dW2"):
+    for k in ("out", "dx", "dp") if p == "mxfp8" else ("out", "dx", "dp", "dW13", "dW2"):
         assert rel_err(g[k], o[k]) <= TOL[p], k
+    assert np.all(g["dp"][case.ids < 0] == 0.0)      # inactive routes get no score gradient
     if p == "mxfp8":
         check_mx_wgrad(g["dW13"], g["dW2"], o["state"], o["grads"])
     dead = np.all(case.ids < 0, axis=1)

@@ -300,6 +300,15 @@ def test_backward_matches_finite_differences():
         assert g["dW13"][idx] == pytest.approx(fd(w13, idx, "w13"), rel=1e-6, abs=1e-8)
     for idx in list(np.ndindex(w2.shape))[::2]:
         assert g["dW2"][idx] == pytest.approx(fd(w2, idx, "w2"), rel=1e-6, abs=1e-8)
+    # score gradient: d loss / d s(t,k); inactive routes get none
+    for t, k in np.ndindex(s.shape):
+        s1, s2 = s.astype(np.float64).copy(), s.astype(np.float64).copy()
+        s1[t, k] += h
+        s2[t, k] -= h
+        f1 = float(np.sum(dY * moe.forward(x, ids, s1, w13, w2, "f64")["out"]))
+        f2 = float(np.sum(dY * moe.forward(x, ids, s2, w13, w2, "f64")["out"]))
+        assert g["dp"][t, k] == pytest.approx((f1 - f2) / (2 * h), rel=1e-6, abs=1e-8)
+    assert g["dp"][2, 1] == 0.0
 
 
 def test_backward_inactive_routes_get_no_gradient():
