@@ -186,21 +186,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D operand map over a row-major [rows, cols] matrix; boxes are 128 bytes
-// wide (64 BF16 or 128 E4M3 elements) and `box_rows` tall, 128-byte swizzle.
-bool make_tmap(CUtensorMap* tm, const void* base, bool mx, int64_t rows, int64_t cols, int box_rows) {
+// 2D operand map over a row-major [rows, cols] matrix; boxes are
+// `row_bytes` (128, 64 or 32) wide with the matching swizzle and `box_rows`
+// tall.
+bool make_tmap(CUtensorMap* tm, const void* base, bool mx, int64_t rows, int64_t cols, int box_rows,
+               int row_bytes = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int esz = mx ? 1 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esz)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes / esz), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : (row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
   const CUresult r = fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// The narrow-box maps a weight-gradient GEMM uses for a short last stage.
+bool make_narrow_tmaps(GemmLaunch* g, const void* a, int64_t a_rows, const void* b, int64_t b_rows, bool mx,
+                       int64_t cols) {
+  return make_tmap(&g->tmA64, a, mx, a_rows, cols, 128, 64) && make_tmap(&g->tmB64, b, mx, b_rows, cols, 128, 64) &&
+         make_tmap(&g->tmA32, a, mx, a_rows, cols, 128, 32) && make_tmap(&g->tmB32, b, mx, b_rows, cols, 128, 32);
 }
 
 // Output map of a BF16 weight gradient [rows, cols]: boxes of 64 columns
@@ -579,7 +589,8 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g2.epi = kEpiWgrad;
   g2.mode = kGroupedK;
   if (!make_tmap(&g2.tmA, B(ctx, MOE_BUF_DH3COL), mx, D, R, 128) ||
-      !make_tmap(&g2.tmB, sv + SL.off[MOE_SAVED_H2COL], mx, F, R, 128))
+      !make_tmap(&g2.tmB, sv + SL.off[MOE_SAVED_H2COL], mx, F, R, 128) ||
+      !make_narrow_tmaps(&g2, B(ctx, MOE_BUF_DH3COL), D, sv + SL.off[MOE_SAVED_H2COL], F, mx, R))
     return MOE_ERR_CUDA;
   GemmParams& p2 = g2.p;
   p2.hdr = rp.hdr;
@@ -644,7 +655,8 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g4.epi = kEpiWgrad;
   g4.mode = kGroupedK;
   if (!make_tmap(&g4.tmA, B(ctx, MOE_BUF_DH1COL), mx, 2 * F, R, 128) ||
-      !make_tmap(&g4.tmB, sv + SL.off[MOE_SAVED_XCOL], mx, D, R, 128))
+      !make_tmap(&g4.tmB, sv + SL.off[MOE_SAVED_XCOL], mx, D, R, 128) ||
+      !make_narrow_tmaps(&g4, B(ctx, MOE_BUF_DH1COL), 2 * F, sv + SL.off[MOE_SAVED_XCOL], D, mx, R))
     return MOE_ERR_CUDA;
   GemmParams& p4 = g4.p;
   p4.hdr = rp.hdr;

@@ -178,6 +178,20 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
   return d;
 }
 
+// Same for a K-major tile whose rows are `row_bytes` = 128, 64 or 32 bytes
+// wide, stored with the matching TMA swizzle (128B, 64B, 32B): groups of 8
+// rows are 8 * row_bytes apart; swizzle modes 2 (128B), 4 (64B), 6 (32B).
+__device__ __forceinline__ uint64_t sdesc_k_sw(uint32_t saddr, int row_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>((8 * row_bytes) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  const uint64_t mode = row_bytes == 128 ? 2 : (row_bytes == 64 ? 4 : 6);
+  d |= mode << 61;
+  return d;
+}
+
 // Shared-memory descriptor of one scale atom for tcgen05.cp: a K-major
 // matrix of 32 rows x 16 bytes without swizzle, i.e. four 8-row x 16-byte
 // core matrices 128 bytes apart (stride byte offset 128).

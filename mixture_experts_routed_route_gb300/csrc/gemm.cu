@@ -119,6 +119,17 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int n
   return t;
 }
 
+// Width in bytes of the K-major rows a stage loads: 128 (a full stage), or
+// for the last stage of a weight-gradient tile only as much as it holds
+// (32 or 64 bytes when that is enough), so short experts do not stream
+// unused columns through TMA and shared memory.
+template <int MODE, int BK, int ESZ>
+__device__ __forceinline__ int stage_row_bytes(const Tile& t, int ks) {
+  if (MODE != kGroupedK || ks != t.kstages - 1) return 128;
+  const int b = t.klast * ESZ;
+  return b <= 32 ? 32 : (b <= 64 ? 64 : 128);
+}
+
 // A final bounded wait that ignores the abort flag (used only to drain work
 // already in flight before the CTA releases its resources).
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
@@ -384,7 +395,9 @@ struct Cfg {
 template <bool MX, int NA, int EPI, int MODE>
 __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA64,
+                const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmA32,
+                const __grid_constant__ CUtensorMap tmB32, const GemmParams p) {
   using C = Cfg<MX, NA, MODE>;
   constexpr int S = C::S;
   extern __shared__ uint8_t smem_raw[];
@@ -417,6 +430,12 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     tma_prefetch(&tmA);
     tma_prefetch(&tmB);
     if (C::WGRAD && p.tma_store) tma_prefetch(&tmC);
+    if (C::WGRAD) {
+      tma_prefetch(&tmA64);
+      tma_prefetch(&tmB64);
+      tma_prefetch(&tmA32);
+      tma_prefetch(&tmB32);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -461,12 +480,15 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
           uint8_t* sa = smem + slot * C::STAGE;
           uint8_t* sb = sa + NA * kABytes;
           uint8_t* ssf = sb + kBBytes;
-          mbar_arrive_expect_tx(&full[slot], NA * kABytes + t.b_rows * 128 + C::SF_BYTES);
+          const int rb = stage_row_bytes<MODE, C::BK, MX ? 1 : 2>(t, ks);
+          mbar_arrive_expect_tx(&full[slot], (NA * 128 + t.b_rows) * rb + C::SF_BYTES);
           const int kx = t.k0 + ks * C::BK;
+          const CUtensorMap* ta = rb == 128 ? &tmA : (rb == 64 ? &tmA64 : &tmA32);
+          const CUtensorMap* tb = rb == 128 ? &tmB : (rb == 64 ? &tmB64 : &tmB32);
 #pragma unroll
-          for (int j = 0; j < NA; ++j) tma_load_2d(sa + j * kABytes, &tmA, &full[slot], kx, t.a_row[j]);
+          for (int j = 0; j < NA; ++j) tma_load_2d(sa + j * kABytes, ta, &full[slot], kx, t.a_row[j]);
           for (int c = 0; c < t.b_rows / p.b_box_rows; ++c)
-            tma_load_2d(sb + c * p.b_box_rows * 128, &tmB, &full[slot], kx, t.b_row0 + p.b_box_rows * c);
+            tma_load_2d(sb + c * p.b_box_rows * rb, tb, &full[slot], kx, t.b_row0 + p.b_box_rows * c);
           if (MX) {
 #pragma unroll
             for (int j = 0; j < NA; ++j)
@@ -507,14 +529,15 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
 #pragma unroll
             for (int j = 0; j <= NA; ++j) tc_cp_sf(sfcol + j * 4, sdesc_sf_atom(sb + kBBytes + j * kAtom));
           }
-          const uint64_t bdesc0 = sdesc_k_sw128(sb);
+          const int rb = stage_row_bytes<MODE, C::BK, MX ? 1 : 2>(t, ks);
+          const uint64_t bdesc0 = sdesc_k_sw(sb, rb);
           const int nmma = (ks == t.kstages - 1) ? t.klast / C::KMMA : C::MMAS;
           for (int k = 0; k < nmma; ++k) {
             const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(2 * k);   // +32 bytes along K
             const uint32_t accum = (ks | k) ? 1u : 0u;
 #pragma unroll
             for (int j = 0; j < NA; ++j) {
-              const uint64_t adesc = sdesc_k_sw128(sa + j * kABytes) + static_cast<uint64_t>(2 * k);
+              const uint64_t adesc = sdesc_k_sw(sa + j * kABytes, rb) + static_cast<uint64_t>(2 * k);
               if (MX) {
                 mma_mxf8(d_tmem + j * 128, adesc, bdesc, idesc_mxf8(t.b_rows, k, k), sfcol + j * 4, sfcol + NA * 4,
                          accum);
@@ -610,7 +633,7 @@ cudaError_t launch_impl(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
     configured = true;
   }
   const int grid = max(1, min(num_sms, g.max_tiles));
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.tmC, g.p);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.tmC, g.tmA64, g.tmB64, g.tmA32, g.tmB32, g.p);
   return cudaGetLastError();
 }
 

@@ -113,6 +113,9 @@ struct GemmLaunch {
   GemmEpi epi;
   GemmMode mode;
   CUtensorMap tmA, tmB, tmC;  // tmC: weight-gradient output (TMA store)
+  // grouped-K: maps of A and B with 64- and 32-byte wide boxes (64B / 32B
+  // swizzle) for a last stage that holds only 32 or 64 bytes of each row
+  CUtensorMap tmA64, tmB64, tmA32, tmB32;
   GemmParams p;
   int max_tiles;          // upper bound of the tile count (grid sizing)
 };
