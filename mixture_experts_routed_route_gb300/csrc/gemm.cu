@@ -34,9 +34,11 @@
 // Warp roles (one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (one thread)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2..    epilogue (8 warps; 16 for the weight-gradient store):
-//               warp w reads TMEM lanes 32*(w%4) .. +31 and every
-//               (EPI_WARPS/4)-th 32-column chunk of the accumulator
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and the
+//               32-column chunks 32h and 32h + 64 (h = (w-2)/4) of the
+//               accumulator
+//   warps 10..17  weight gradient only: a second epilogue group of 8 warps;
+//               the two groups take alternate tiles
 #include "kernels.cuh"
 
 namespace moe {
@@ -46,7 +48,7 @@ namespace {
 constexpr int kABytes = 128 * 128;  // one 128-row x 128-byte operand tile
 constexpr int kBBytes = 128 * 128;
 constexpr int kAtom = 512;          // one scale atom
-constexpr int kEpiBarrier = 1;      // named barrier of the epilogue warps
+constexpr int kEpiBarrier = 1;      // named barriers 1, 2: one per epilogue group
 // Tile metadata cached in shared memory at kernel start, so no role pays a
 // dependent global load per tile: the routing's row blocks (grouped-M, the
 // first kCacheBlocks of them) or the experts' row offsets and first blocks
@@ -193,8 +195,8 @@ __device__ __forceinline__ void store_col32(const GemmParams& p, long long feat,
 }
 
 // ------------------------------------------------------------- epilogues
-// Each takes the warp's chunk index `h` (0..EPI_WARPS/4-1) and drains the
-// 32-column chunks c0 = 32h, 32h + 32*(EPI_WARPS/4), ...
+// Each takes the warp's chunk index `h` (0 or 1) and drains the 32-column
+// chunks c0 = 32h and 32h + 64.
 
 // h3 / input-gradient rows: out[row][feature] = bf16(acc).
 __device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow, int h) {
@@ -351,8 +353,8 @@ __device__ __forceinline__ void epi_wgrad_direct(const GemmParams& p, const Tile
 // tile is written into a 32 KB staging buffer as two 128-row x 128-byte
 // boxes in the 128-byte swizzle (16-byte chunk j of row m at chunk
 // j ^ (m % 8), so 8 consecutive rows hit 8 different bank groups), then one
-// thread stores both boxes with TMA.  The warp's two 32-column chunks
-// (c0 = 32h and 32h + 64) arrive already loaded from TMEM in r0 / r1.
+// thread stores both boxes with TMA.  `r` holds the 32 columns from c0 of
+// row lrow, already loaded from TMEM.
 __device__ __forceinline__ void stage_chunk(const uint32_t (&r)[32], bool zero, int c0, int lrow, uint8_t* stg) {
   uint8_t* box = stg + (c0 >> 6) * 16384 + lrow * 128;
   const int j0 = (c0 & 63) >> 3;  // first 16-byte chunk of these 32 columns
@@ -384,10 +386,15 @@ struct Cfg {
   static constexpr int KMMA = MX ? 32 : 16;                // contraction elements per MMA
   static constexpr int MMAS = BK / KMMA;
   // epilogue warps: 8 (two per TMEM lane quadrant, alternate 32-column
-  // chunks); the weight-gradient store has 16 (one chunk each), since its
-  // per-tile work is almost all epilogue
-  static constexpr int EPI_WARPS = WGRAD ? 16 : 8;
+  // chunks).  The weight-gradient GEMM, whose per-tile work is almost all
+  // epilogue, has two such groups of 8 that take alternate tiles (one
+  // accumulator buffer, staging buffer and named barrier each), so the
+  // TMEM-load -> stage -> store chains of two tiles overlap.
+  static constexpr int EPI_GROUPS = WGRAD ? 2 : 1;
+  static constexpr int EPI_WARPS = 8 * EPI_GROUPS;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int GROUP_THREADS = EPI_THREADS / EPI_GROUPS;
+  static_assert(!WGRAD || (NA == 1 && ACC_BUFS == EPI_GROUPS), "one accumulator buffer per epilogue group");
   static constexpr int THREADS = 64 + EPI_THREADS;
   static constexpr int SMEM = 1024 + S * STAGE + STAGING + 256 + kCacheBytes;
 };
@@ -410,7 +417,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   uint64_t* drain = tempty + C::ACC_BUFS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* epi_abort = abort_flag + 1;  // epilogue warps leave together
+  volatile int* epi_abort = abort_flag + 1;  // [EPI_GROUPS]: a group's warps leave together
   uint8_t* cache = staging + C::STAGING + 256;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -421,11 +428,11 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     }
     for (int a = 0; a < C::ACC_BUFS; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], C::EPI_WARPS);
+      mbar_init(&tempty[a], C::EPI_WARPS / C::EPI_GROUPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
-    *epi_abort = 0;
+    for (int g = 0; g < C::EPI_GROUPS; ++g) epi_abort[g] = 0;
     mbar_fence_init();
     tma_prefetch(&tmA);
     tma_prefetch(&tmB);
@@ -558,12 +565,15 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   } else {
     // --------------------------------------------------------- epilogue
     const int q = warp & 3;              // TMEM lane quadrant of this warp
-    const int h = (warp - 2) >> 2;       // which 32-column chunks it drains
+    const int hw = (warp - 2) >> 2;      // 0 .. EPI_WARPS/4 - 1
+    const int grp = hw / 2 % C::EPI_GROUPS;   // weight gradient: group of this warp
+    const int h = C::EPI_GROUPS > 1 ? (hw & 1) : hw;  // which 32-column chunks it drains
     const int lrow = q * 32 + lane;
-    const int etid = threadIdx.x - 64;   // 0 .. EPI_THREADS-1
+    const int gtid = (threadIdx.x - 64) % C::GROUP_THREADS;   // thread index within the group
     const bool staged = C::WGRAD && p.tma_store;
-    uint32_t tc = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
+    uint32_t tc = grp;
+    for (int tile = blockIdx.x + grp * gridDim.x; tile < num_tiles;
+         tile += C::EPI_GROUPS * gridDim.x, tc += C::EPI_GROUPS) {
       const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk, mc);
       const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
       uint32_t hp[32];
@@ -573,28 +583,35 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
       if (staged) {
-        uint8_t* stg = staging + (tc & 1) * 32768;
-        // start both TMEM reads, then (while they are in flight) make sure the
-        // staging buffer's previous TMA store has finished reading it.  Every
-        // epilogue warp reaches the barrier once per tile whether its bounded
-        // wait succeeded or not, so a warp that gives up cannot leave the
-        // others blocked in it: they all see the flag and leave together.
-        // one 32-column chunk per warp (16 epilogue warps)
-        uint32_t r0[32];
+        // The group's 8 warps drain the 128 x 128 accumulator, two 32-column
+        // chunks each (c0 = 32h and 32h + 64), into the group's staging
+        // buffer.  The first TMEM read starts first; while it is in flight
+        // the group's store thread makes sure its previous TMA store has
+        // finished reading the buffer.  Every warp of the group reaches the
+        // barrier once per tile whether its bounded wait succeeded or not, so
+        // a warp that gives up cannot leave the others blocked in it: they
+        // all see the group's flag and leave together.
+        uint8_t* stg = staging + grp * 32768;
+        uint32_t r[32];
         const bool has = ok && t.kstages > 0;
-        if (has) tmem_ld32(tbase + 32 * h, r0);
-        if (!ok && lane == 0) *epi_abort = 1;
-        if (etid == 0) bulk_wait_read<1>();
-        named_bar_sync(kEpiBarrier, C::EPI_THREADS);
+        if (has) tmem_ld32(tbase + 32 * h, r);
+        if (!ok && lane == 0) epi_abort[grp] = 1;
+        if (gtid == 0) bulk_wait_read<0>();
+        named_bar_sync(kEpiBarrier + grp, C::GROUP_THREADS);
         tmem_ld_wait();
-        if (*epi_abort) break;
+        if (epi_abort[grp]) break;
+        stage_chunk(r, !has, 32 * h, lrow, stg);
+        if (has) {
+          tmem_ld32(tbase + 32 * h + 64, r);
+          tmem_ld_wait();
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
-        stage_chunk(r0, !has, 32 * h, lrow, stg);
+        stage_chunk(r, !has, 32 * h + 64, lrow, stg);
         fence_proxy_async_smem();
-        named_bar_sync(kEpiBarrier, C::EPI_THREADS);
-        if (etid == 0) {
+        named_bar_sync(kEpiBarrier + grp, C::GROUP_THREADS);
+        if (gtid == 0) {
           const int y = t.e * p.m_tiles * 128 + t.out_row0;
           tma_store_2d(&tmC, stg, t.out_col0, y);
           tma_store_2d(&tmC, stg + 16384, t.out_col0 + 64, y);
@@ -605,12 +622,12 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       if (EPI == kEpiStore) epi_store(p, t, tbase, lrow, h);
       else if (EPI == kEpiSwigluFwd) epi_swiglu_fwd<MX>(p, t, tbase, lrow, lane, h);
       else if (EPI == kEpiSwigluBwd) epi_swiglu_bwd<MX>(p, t, tbase, lrow, lane, h, hp);
-      else epi_wgrad_direct(p, t, tbase, lrow, h, 32 * (C::EPI_WARPS / 4));
+      else epi_wgrad_direct(p, t, tbase, lrow, h, 64);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
     }
-    if (staged && etid == 0) bulk_wait<0>();
+    if (staged && gtid == 0) bulk_wait<0>();
   }
 
   tc_fence_before();
