@@ -206,6 +206,12 @@ bool make_tmap(CUtensorMap* tm, const void* base, bool mx, int64_t rows, int64_t
   return r == CUDA_SUCCESS;
 }
 
+// Weight tiles per stage of a grouped-M store GEMM whose output has `n`
+// features: two adjacent 128-row tiles share each loaded
+// activation box and its scales (half the activation traffic per weight
+// byte) when n is a multiple of 256, else one.
+int pair_tiles(int64_t n) { return n % 256 == 0 ? 2 : 1; }
+
 // The narrow-box maps a weight-gradient GEMM uses for a short last stage.
 bool make_narrow_tmaps(GemmLaunch* g, const void* a, int64_t a_rows, const void* b, int64_t b_rows, bool mx,
                        int64_t cols) {
@@ -476,7 +482,7 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   // ---- W2
   GemmLaunch g2{};
   g2.mx = mx;
-  g2.na = 1;
+  g2.na = pair_tiles(D);
   g2.epi = kEpiStore;
   g2.mode = kGroupedM;
   if (!make_tmap(&g2.tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128) ||
@@ -488,7 +494,7 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   p2.poffsets = rp.poffsets;
   p2.E = E;
   p2.b_box_rows = 32;
-  p2.n_tiles = D / 128;
+  p2.n_tiles = D / (128 * g2.na);
   p2.K = F;
   p2.a_rows_per_expert = D;
   p2.sfa = W2->scale;
@@ -500,7 +506,7 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   p2.out0_pitch = D;
   p2.F = F;
   p2.err = ctx->err;
-  g2.max_tiles = static_cast<int>(ctx->b_cap * (D / 128));
+  g2.max_tiles = static_cast<int>(ctx->b_cap * p2.n_tiles);
   MOE_TRY(launch_gemm(g2, sms, stream));
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 0, 4, stream));
@@ -546,7 +552,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   // ---- W2 DGRAD + SwiGLU backward -> dh1 row and column bundles
   GemmLaunch g1{};
   g1.mx = mx;
-  g1.na = 1;
+  g1.na = 1;   // the SwiGLU-backward epilogue needs two accumulator buffers
   g1.epi = kEpiSwigluBwd;
   g1.mode = kGroupedM;
   if (!make_tmap(&g1.tmA, W2->data_t, mx, static_cast<int64_t>(E) * F, D, 128) ||
@@ -558,7 +564,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p1.poffsets = rp.poffsets;
   p1.E = E;
   p1.b_box_rows = 32;
-  p1.n_tiles = F / 128;
+  p1.n_tiles = F / (128 * g1.na);
   p1.K = D;
   p1.a_rows_per_expert = F;
   p1.sfa = W2->scale_t;
@@ -577,7 +583,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p1.b_cap = static_cast<int>(ctx->b_cap);
   p1.F = F;
   p1.err = ctx->err;
-  g1.max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
+  g1.max_tiles = static_cast<int>(ctx->b_cap * p1.n_tiles);
   MOE_TRY(launch_gemm(g1, sms, stream));
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 1, 2, stream));
@@ -620,7 +626,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   // ---- W13 DGRAD: dxr = dh1 W13[e]
   GemmLaunch g3{};
   g3.mx = mx;
-  g3.na = 1;
+  g3.na = pair_tiles(D);
   g3.epi = kEpiStore;
   g3.mode = kGroupedM;
   if (!make_tmap(&g3.tmA, W13->data_t, mx, static_cast<int64_t>(E) * D, 2 * F, 128) ||
@@ -632,7 +638,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p3.poffsets = rp.poffsets;
   p3.E = E;
   p3.b_box_rows = 32;
-  p3.n_tiles = D / 128;
+  p3.n_tiles = D / (128 * g3.na);
   p3.K = 2 * F;
   p3.a_rows_per_expert = D;
   p3.sfa = W13->scale_t;
@@ -643,7 +649,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p3.out0_pitch = D;
   p3.F = F;
   p3.err = ctx->err;
-  g3.max_tiles = static_cast<int>(ctx->b_cap * (D / 128));
+  g3.max_tiles = static_cast<int>(ctx->b_cap * p3.n_tiles);
   MOE_TRY(launch_gemm(g3, sms, stream));
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 1, 4, stream));

@@ -77,7 +77,10 @@ struct MetaCache {
   const int* bstart;    // grouped-K: bstart[0..E]
 };
 
-template <int MODE, int BK>
+// STEP: weight rows per grouped-M output tile: 128, or 256 when the two A
+// tiles of an NA = 2 store tile are adjacent 128-row blocks (the SwiGLU
+// forward's second A tile is the up half, F rows on).
+template <int MODE, int BK, int STEP>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int nblk, const MetaCache& mc) {
   Tile t;
   if (MODE == kGroupedM) {
@@ -85,15 +88,15 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int n
     const int4 blk = (b < kCacheBlocks) ? mc.blocks[b] : p.blocks[b];
     t.e = blk.x;
     t.blk = b;
-    t.a_row[0] = blk.x * p.a_rows_per_expert + n * 128;
-    t.a_row[1] = t.a_row[0] + p.a_up_offset;
+    t.a_row[0] = blk.x * p.a_rows_per_expert + n * STEP;
+    t.a_row[1] = t.a_row[0] + (STEP == 256 ? 128 : p.a_up_offset);
     t.b_row0 = blk.y;
     t.b_rows = blk.z;
     t.k0 = 0;
     t.kstages = p.K / BK;
     t.klast = BK;
     t.out_row0 = blk.y;
-    t.out_col0 = n * 128;
+    t.out_col0 = n * STEP;
     t.sfa_atom[0] = static_cast<long long>(t.a_row[0] >> 7) * p.sfa_ts;
     t.sfa_atom[1] = static_cast<long long>(t.a_row[1] >> 7) * p.sfa_ts;
     t.sfb_atom = static_cast<long long>(b) * p.sfb_ts;
@@ -196,19 +199,38 @@ __device__ __forceinline__ void store_col32(const GemmParams& p, long long feat,
 
 // ------------------------------------------------------------- epilogues
 // Each takes the warp's chunk index `h` (0 or 1) and drains the 32-column
-// chunks c0 = 32h and 32h + 64.
+// chunks c0 = 32h and 32h + 64.  The store and SwiGLU-forward epilogues hand
+// the accumulator back (`tempty`) as soon as their last TMEM read has
+// landed, before the stores, so the next tile's MMAs overlap the store work
+// (with two A tiles per stage there is a single 256-column accumulator).
+
+// This warp is done reading the accumulator.
+__device__ __forceinline__ void release_acc(uint64_t* tempty, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(tempty);
+}
 
 // h3 / input-gradient rows: out[row][feature] = bf16(acc).
-__device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow, int h) {
+// With NA = 2 the two accumulators hold features out_col0 + [0, 128) and
+// out_col0 + [128, 256).
+template <int NA>
+__device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow, int lane,
+                                          int h, uint64_t* tempty) {
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0);
-  const int f = t.out_col0 + lrow;
-  for (int c0 = 32 * h; c0 < t.b_rows; c0 += 64) {
-    uint32_t v[32];
-    tmem_ld32(tbase + c0, v);
-    tmem_ld_wait();
+  if (32 * h >= t.b_rows) release_acc(tempty, lane);
+#pragma unroll 1
+  for (int j = 0; j < NA; ++j) {
+    const int f = t.out_col0 + j * 128 + lrow;
+    for (int c0 = 32 * h; c0 < t.b_rows; c0 += 64) {
+      uint32_t v[32];
+      tmem_ld32(tbase + j * 128 + c0, v);
+      tmem_ld_wait();
+      if (j == NA - 1 && c0 + 64 >= t.b_rows) release_acc(tempty, lane);
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      out[static_cast<long long>(t.out_row0 + c0 + i) * p.out0_pitch + f] = __float2bfloat16_rn(u2f(v[i]));
+      for (int i = 0; i < 32; ++i)
+        out[static_cast<long long>(t.out_row0 + c0 + i) * p.out0_pitch + f] = __float2bfloat16_rn(u2f(v[i]));
+    }
   }
 }
 
@@ -217,13 +239,15 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, ui
 // operand) and, for training, the h2 column bundle (W2 WGRAD's operand).
 template <bool MX>
 __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow,
-                                               int lane, int h) {
+                                               int lane, int h, uint64_t* tempty) {
   const int f = t.out_col0 + lrow;
+  if (32 * h >= t.b_rows) release_acc(tempty, lane);
   for (int c0 = 32 * h; c0 < t.b_rows; c0 += 64) {
     uint32_t vg[32], vu[32];
     tmem_ld32(tbase + c0, vg);
     tmem_ld32(tbase + 128 + c0, vu);
     tmem_ld_wait();
+    if (c0 + 64 >= t.b_rows) release_acc(tempty, lane);
     float hv[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -407,6 +431,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
                 const __grid_constant__ CUtensorMap tmB32, const GemmParams p) {
   using C = Cfg<MX, NA, MODE>;
   constexpr int S = C::S;
+  constexpr int kStep = (NA == 2 && EPI != kEpiSwigluFwd) ? 256 : 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + S * C::STAGE;
@@ -471,19 +496,23 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   }
   __syncthreads();
 
+  // The producer and MMA warps walk their loops with all 32 lanes, so the
+  // loop state and the descriptors stay warp-uniform; lane 0 alone issues
+  // the copies and the tensor-core instructions (and the commits, which
+  // track the issuing thread's operations).
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      uint32_t it = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk, mc);
-        for (int ks = 0; ks < t.kstages; ++ks, ++it) {
-          const uint32_t slot = it % S, ph = (it / S) & 1;
-          if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE, C::BK, kStep>(p, tile, nblk, mc);
+      for (int ks = 0; ks < t.kstages; ++ks, ++it) {
+        const uint32_t slot = it % S, ph = (it / S) & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[slot], ph ^ 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
           uint8_t* sa = smem + slot * C::STAGE;
           uint8_t* sb = sa + NA * kABytes;
           uint8_t* ssf = sb + kBBytes;
@@ -503,65 +532,82 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
             bulk_load(ssf + NA * kAtom, p.sfb + (t.sfb_atom + ks) * kAtom, kAtom, &full[slot]);
           }
         }
+        __syncwarp();
       }
-      // no load may still be landing in shared memory when the CTA exits
+    }
+    // no load may still be landing in shared memory when the CTA exits
+    if (lane == 0) {
       const uint32_t pend = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
       for (uint32_t j = 0; j < pend; ++j) {
         const uint32_t i2 = it - 1 - j;
         drain_wait(&full[i2 % S], (i2 / S) & 1);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      uint32_t it = 0, tc = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++tc) {
-        const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk, mc);
-        const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
-        if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, p.err)) break;
+    uint32_t it = 0, tc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++tc) {
+      const Tile t = decode_tile<MODE, C::BK, kStep>(p, tile, nblk, mc);
+      const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty[acc], aph ^ 1, abort_flag, p.err))) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + acc * C::ACC_COLS;
+      const uint32_t idesc = MX ? idesc_mxf8(t.b_rows, 0, 0) : idesc_bf16(t.b_rows);
+      for (int ks = 0; ks < t.kstages; ++ks, ++it) {
+        const uint32_t slot = it % S, ph = (it / S) & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], ph, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * C::ACC_COLS;
-        for (int ks = 0; ks < t.kstages; ++ks, ++it) {
-          const uint32_t slot = it % S, ph = (it / S) & 1;
-          if (!mbar_wait(&full[slot], ph, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + slot * C::STAGE);
-          const uint32_t sb = sa + NA * kABytes;
-          const uint32_t sfcol = tmem + C::SF_COL0 + slot * C::SF_COLS;
+        const uint32_t sa = smem_u32(smem + slot * C::STAGE);
+        const uint32_t sb = sa + NA * kABytes;
+        const uint32_t sfcol = tmem + C::SF_COL0 + slot * C::SF_COLS;
+        const int rb = stage_row_bytes<MODE, C::BK, MX ? 1 : 2>(t, ks);
+        const uint64_t bdesc0 = sdesc_k_sw(sb, rb);
+        uint64_t adesc0[NA];
+#pragma unroll
+        for (int j = 0; j < NA; ++j) adesc0[j] = sdesc_k_sw(sa + j * kABytes, rb);
+        const int nmma = (ks == t.kstages - 1) ? t.klast / C::KMMA : C::MMAS;
+        if (lane == 0) {
           if (MX) {
 #pragma unroll
             for (int j = 0; j <= NA; ++j) tc_cp_sf(sfcol + j * 4, sdesc_sf_atom(sb + kBBytes + j * kAtom));
           }
-          const int rb = stage_row_bytes<MODE, C::BK, MX ? 1 : 2>(t, ks);
-          const uint64_t bdesc0 = sdesc_k_sw(sb, rb);
-          const int nmma = (ks == t.kstages - 1) ? t.klast / C::KMMA : C::MMAS;
-          for (int k = 0; k < nmma; ++k) {
-            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(2 * k);   // +32 bytes along K
-            const uint32_t accum = (ks | k) ? 1u : 0u;
 #pragma unroll
-            for (int j = 0; j < NA; ++j) {
-              const uint64_t adesc = sdesc_k_sw(sa + j * kABytes, rb) + static_cast<uint64_t>(2 * k);
-              if (MX) {
-                mma_mxf8(d_tmem + j * 128, adesc, bdesc, idesc_mxf8(t.b_rows, k, k), sfcol + j * 4, sfcol + NA * 4,
-                         accum);
-              } else {
-                mma_bf16(d_tmem + j * 128, adesc, bdesc, idesc_bf16(t.b_rows), accum);
+          for (int k = 0; k < C::MMAS; ++k) {
+            if (k < nmma) {
+              const uint64_t koff = static_cast<uint64_t>(2 * k);   // +32 bytes along K
+              const uint32_t accum = (ks | k) ? 1u : 0u;
+#pragma unroll
+              for (int j = 0; j < NA; ++j) {
+                if (MX) {
+                  // scale byte k of the 4 per row (one per 32-element block)
+                  mma_mxf8(d_tmem + j * 128, adesc0[j] + koff, bdesc0 + koff,
+                           idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29), sfcol + j * 4,
+                           sfcol + NA * 4, accum);
+                } else {
+                  mma_bf16(d_tmem + j * 128, adesc0[j] + koff, bdesc0 + koff, idesc, accum);
+                }
               }
             }
           }
           tc_commit(&empty[slot]);
         }
-        if (!ok) break;
-        tc_commit(&tfull[acc]);
+        __syncwarp();
       }
-      // every MMA issued here must be complete before TMEM is released
+      if (!ok) break;
+      if (lane == 0) tc_commit(&tfull[acc]);
+      __syncwarp();
+    }
+    // every MMA issued here must be complete before TMEM is released
+    if (lane == 0) {
       tc_commit(drain);
       drain_wait(drain, 0);
     }
+    __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue
     const int q = warp & 3;              // TMEM lane quadrant of this warp
@@ -574,7 +620,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     uint32_t tc = grp;
     for (int tile = blockIdx.x + grp * gridDim.x; tile < num_tiles;
          tile += C::EPI_GROUPS * gridDim.x, tc += C::EPI_GROUPS) {
-      const Tile t = decode_tile<MODE, C::BK>(p, tile, nblk, mc);
+      const Tile t = decode_tile<MODE, C::BK, kStep>(p, tile, nblk, mc);
       const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
       uint32_t hp[32];
       if (EPI == kEpiSwigluBwd && 32 * h < t.b_rows) load_h1_chunk(p, t, t.out_col0 + lrow, 32 * h, hp);
@@ -619,13 +665,16 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
         }
         continue;
       }
-      if (EPI == kEpiStore) epi_store(p, t, tbase, lrow, h);
-      else if (EPI == kEpiSwigluFwd) epi_swiglu_fwd<MX>(p, t, tbase, lrow, lane, h);
-      else if (EPI == kEpiSwigluBwd) epi_swiglu_bwd<MX>(p, t, tbase, lrow, lane, h, hp);
-      else epi_wgrad_direct(p, t, tbase, lrow, h, 64);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (EPI == kEpiStore) epi_store<NA>(p, t, tbase, lrow, lane, h, &tempty[acc]);
+      else if (EPI == kEpiSwigluFwd) epi_swiglu_fwd<MX>(p, t, tbase, lrow, lane, h, &tempty[acc]);
+      else if (EPI == kEpiSwigluBwd) {
+        // its two accumulator buffers cover this (heavier) epilogue: release at the end
+        epi_swiglu_bwd<MX>(p, t, tbase, lrow, lane, h, hp);
+        release_acc(&tempty[acc], lane);
+      } else {
+        epi_wgrad_direct(p, t, tbase, lrow, h, 64);
+        release_acc(&tempty[acc], lane);
+      }
     }
     if (staged && gtid == 0) bulk_wait<0>();
   }
@@ -667,6 +716,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   MOE_GEMM_CASE(true, 2, kEpiSwigluFwd, kGroupedM)
   MOE_GEMM_CASE(false, 1, kEpiStore, kGroupedM)
   MOE_GEMM_CASE(true, 1, kEpiStore, kGroupedM)
+  MOE_GEMM_CASE(false, 2, kEpiStore, kGroupedM)
+  MOE_GEMM_CASE(true, 2, kEpiStore, kGroupedM)
   MOE_GEMM_CASE(false, 1, kEpiSwigluBwd, kGroupedM)
   MOE_GEMM_CASE(true, 1, kEpiSwigluBwd, kGroupedM)
   MOE_GEMM_CASE(false, 1, kEpiWgrad, kGroupedK)

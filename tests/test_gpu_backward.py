@@ -29,11 +29,22 @@ def _mx_skewed():
                           seed=33)
 
 
+def _mx_d384():
+    # D and F not multiples of 256: the store and SwiGLU-backward GEMMs take one weight tile per stage
+    return synth.Workload("mx_d384", 200, 384, 384, 8, 3, "mxfp8", "zipf", inactive_frac=0.05, zipf_s=1.2, seed=34)
+
+
+def _bf16_d384():
+    return synth.Workload("bf16_d384", 200, 384, 384, 8, 3, "bf16", "zipf", inactive_frac=0.05, zipf_s=1.2, seed=35)
+
+
 CASES = {
     "tiny_bf16": lambda: synth.WORKLOADS["tiny_bf16"],
     "bf16_skewed": _bf16_skewed,
     "mx_tiny": _mx_tiny,
     "mx_skewed": _mx_skewed,
+    "mx_d384": _mx_d384,
+    "bf16_d384": _bf16_d384,
 }
 
 
