@@ -6,10 +6,12 @@
 // section 02, "Quantization Axes for Forward and Backward": with 32x32
 // blocks the forward and the input-gradient GEMMs use the same quantised
 // values with distinct scale orientations.  Here the one scale of each tile
-// is written in both orientations ([E,N,K/32] and [E,K,N/32]) and the codes
-// once more transposed ([E,K,N]), so the input-gradient GEMM also reads a
-// K-major operand.  The scales are written in the GEMMs' 512-byte atom
-// layout (kernels.cuh: sf_atom_byte), so a GEMM stage copies them in bulk.
+// is written for both orientations and the codes once more transposed
+// ([E,K,N]), so the input-gradient GEMM also reads a K-major operand.  The
+// scales are written in the GEMMs' 512-byte atom layout (kernels.cuh:
+// sf_atom_byte): atom (r/128, k/128) of the [E*N, K] orientation and atom
+// (k/128, r/128) of the [E*K, N] one each hold 128 rows x 4 blocks of 32, so
+// a GEMM stage copies one atom per operand tile in bulk.
 #include "kernels.cuh"
 
 namespace moe {
