@@ -425,9 +425,13 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   MOE_TRY(stage_mark(ctx, 0, 1, stream));
   if (train) {
     // row bundle (W13 operand) and column bundle (W13 WGRAD operand) in one pass
+    CUtensorMap tr, tc;
+    if (mx && (!make_tmap(&tr, B(ctx, MOE_BUF_XROW), true, R, D, 128) ||
+               !make_tmap(&tc, sv + SL.off[MOE_SAVED_XCOL], true, D, R, 128)))
+      return MOE_ERR_CUDA;
     MOE_TRY(launch_gather_both(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
                                sv + SL.off[MOE_SAVED_XCOL], mx ? sv + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr,
-                               static_cast<int>(R), static_cast<int>(ctx->b_cap), sms, stream));
+                               static_cast<int>(R), static_cast<int>(ctx->b_cap), sms, stream, &tr, &tc));
   } else {
     MOE_TRY(launch_gather_rows(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
                                static_cast<int>(R), sms, stream));
@@ -543,9 +547,13 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
 
   // ---- dh3 = s * dY: row bundle (W2 DGRAD) and column bundle (W2 WGRAD)
   MOE_TRY(stage_mark(ctx, 1, 0, stream));
+  CUtensorMap tr, tc;
+  if (mx && (!make_tmap(&tr, B(ctx, MOE_BUF_DH3ROW), true, R, D, 128) ||
+             !make_tmap(&tc, B(ctx, MOE_BUF_DH3COL), true, D, R, 128)))
+    return MOE_ERR_CUDA;
   MOE_TRY(launch_gather_both(mx, true, dout, D, K, rp, B(ctx, MOE_BUF_DH3ROW), B(ctx, MOE_BUF_DH3ROW_SCALE),
                              B(ctx, MOE_BUF_DH3COL), B(ctx, MOE_BUF_DH3COL_SCALE), static_cast<int>(R),
-                             static_cast<int>(ctx->b_cap), sms, stream));
+                             static_cast<int>(ctx->b_cap), sms, stream, &tr, &tc));
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 1, 1, stream));
 

@@ -61,11 +61,20 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
       srow = src + static_cast<long long>(route / K) * D;
       if (SCALE) s = scores[route];
     }
-    for (int base = 0; base < D; base += 256) {
-      const int c = base + lane * 8;
+    // four 16-byte loads in flight per lane before any is used
+    for (int base = 0; base < D; base += 1024) {
+      uint4 ub[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cq = base + q * 256 + lane * 8;
+        ub[q] = make_uint4(0, 0, 0, 0);
+        if (cq < D && srow) ub[q] = __ldg(reinterpret_cast<const uint4*>(srow + cq));
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+      const int c = base + q * 256 + lane * 8;
       const bool act = c < D;
-      uint4 u = make_uint4(0, 0, 0, 0);
-      if (act && srow) u = __ldg(reinterpret_cast<const uint4*>(srow + c));
+      uint4 u = ub[q];
       if (!MX) {
         if (SCALE) {
           float v[8];
@@ -100,28 +109,25 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
           }
         }
       }
+      }
     }
   }
 }
 
-// Both bundles in one pass (training).  One CTA per (128-row tile,
+// Both bundles in one pass (training), BF16.  One CTA per (128-row tile,
 // 128-column slab): the gathered rows go through shared memory once, then
-//  * row bundle: warp w writes rows 16w .. 16w+15, lane l columns 4l .. 4l+3
-//    (8 lanes per MX block; 128 contiguous bytes per row and warp);
+//  * row bundle: warp w writes rows 16w .. 16w+15, lane l columns 4l .. 4l+3;
 //  * column bundle: thread (c, half) writes feature c0+c for rows
-//    64*half .. +63, i.e. 64 contiguous bytes (two MX blocks) per thread, so
-//    two threads fill each 128-byte line of dstT[feature][rows] at once.
+//    64*half .. +63 (128 contiguous bytes per thread).
 constexpr int kBothRows = 128, kBothCols = 128, kBothPitch = kBothCols + 4;
 constexpr int kBothSmem = kBothRows * kBothPitch * 4;
 
-template <bool MX, bool SCALE>
+template <bool SCALE>
 __global__ void __launch_bounds__(256) gather_both_kernel(const __nv_bfloat16* __restrict__ src, int D, int K,
                                                           const int* __restrict__ hdr, const int* __restrict__ perm,
-                                                          const float* __restrict__ scores, void* __restrict__ dst,
-                                                          uint8_t* __restrict__ dst_sf, void* __restrict__ dstT,
-                                                          uint8_t* __restrict__ dstT_sf, int r_cap, int b_cap,
-                                                          const int* __restrict__ row_block,
-                                                          const int4* __restrict__ blocks) {
+                                                          const float* __restrict__ scores,
+                                                          __nv_bfloat16* __restrict__ dst,
+                                                          __nv_bfloat16* __restrict__ dstT, int r_cap) {
   extern __shared__ float4 smem_f4[];
   float* tile = reinterpret_cast<float*>(smem_f4);  // [128][kBothPitch]
   const int rows = hdr[2];
@@ -129,26 +135,42 @@ __global__ void __launch_bounds__(256) gather_both_kernel(const __nv_bfloat16* _
   if (r0 >= rows) return;
   const int c0 = blockIdx.x * kBothCols;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // ---- load 128 gathered rows x 128 columns (16 chunks of 8 values per row)
-  for (int i = tid; i < kBothRows * 16; i += 256) {
-    const int row = i >> 4, chunk = i & 15;
-    const int c = c0 + chunk * 8;
-    float v[8];
-    const int route = (r0 + row < r_cap) ? perm[r0 + row] : -1;
-    if (route >= 0 && c < D) {
-      unpack8(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(route / K) * D + c)), v);
-      if (SCALE) {
-        const float s = scores[route];
+  // ---- load 128 gathered rows x 128 columns (16 chunks of 8 values per row):
+  // thread t moves chunk t%16 of rows t/16 + 16j, j = 0..7.  All route
+  // lookups are issued first, then all eight row loads, so a thread waits for
+  // two memory latencies, not sixteen.
+  {
+    constexpr int kPer = kBothRows * 16 / 256;
+    const int chunk = tid & 15, c = c0 + chunk * 8;
+    int route[kPer];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = s * v[j];
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+    for (int j = 0; j < kPer; ++j) {
+      const int r = r0 + (tid >> 4) + 16 * j;
+      route[j] = (r < r_cap) ? perm[r] : -1;
     }
-    float4* t4 = reinterpret_cast<float4*>(tile + row * kBothPitch + chunk * 8);
-    t4[0] = make_float4(v[0], v[1], v[2], v[3]);
-    t4[1] = make_float4(v[4], v[5], v[6], v[7]);
+    uint4 u[kPer];
+    float s[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      u[j] = make_uint4(0, 0, 0, 0);
+      s[j] = 1.0f;
+      if (route[j] >= 0 && c < D) {
+        u[j] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(route[j] / K) * D + c));
+        if (SCALE) s[j] = scores[route[j]];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      float v[8];
+      unpack8(u[j], v);
+      if (SCALE) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = s[j] * v[q];
+      }
+      float4* t4 = reinterpret_cast<float4*>(tile + ((tid >> 4) + 16 * j) * kBothPitch + chunk * 8);
+      t4[0] = make_float4(v[0], v[1], v[2], v[3]);
+      t4[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
   }
   __syncthreads();
   // ---- row bundle
@@ -157,28 +179,9 @@ __global__ void __launch_bounds__(256) gather_both_kernel(const __nv_bfloat16* _
     const int row = warp * 16 + rr;
     const int r = r0 + row;
     const float4 x4 = *reinterpret_cast<const float4*>(tile + row * kBothPitch + lane * 4);
-    if (!MX) {
-      if (c < D && r < rows)
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dst) + static_cast<long long>(r) * D + c) =
-            make_uint2(pack_bf16x2(x4.x, x4.y), pack_bf16x2(x4.z, x4.w));
-    } else {
-      float amax = fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w)));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-      const int e = mx_shared_exp(amax);
-      const float inv = exp2_int(-e);
-      const uint32_t q = cvt_e4m3x2(x4.x * inv, x4.y * inv) | (cvt_e4m3x2(x4.z * inv, x4.w * inv) << 16);
-      if (c < D && r < rows) {
-        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(dst) + static_cast<long long>(r) * D + c) = q;
-        if ((lane & 7) == 0) {
-          const int b = row_block[r >> 5];
-          const int kb = c >> 5;
-          dst_sf[(static_cast<long long>(b) * (D / 128) + (kb >> 2)) * 512 + sf_atom_byte(r - blocks[b].y, kb & 3)] =
-              static_cast<uint8_t>(e + 127);
-        }
-      }
-    }
+    if (c < D && r < rows)
+      *reinterpret_cast<uint2*>(dst + static_cast<long long>(r) * D + c) =
+          make_uint2(pack_bf16x2(x4.x, x4.y), pack_bf16x2(x4.z, x4.w));
   }
   // ---- column bundle
   const int cc = tid & 127, half = tid >> 7;
@@ -187,42 +190,23 @@ __global__ void __launch_bounds__(256) gather_both_kernel(const __nv_bfloat16* _
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
       const int rl = half * 64 + g * 32;   // first row of this 32-row group within the tile
-      const int rg = (r0 + rl) >> 5;
       if (r0 + rl >= rows) break;
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = tile[(rl + i) * kBothPitch + cc];
-      if (!MX) {
-        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dstT) + static_cast<long long>(d) * r_cap + r0 + rl);
+      uint4* o = reinterpret_cast<uint4*>(dstT + static_cast<long long>(d) * r_cap + r0 + rl);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          o[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-      } else {
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        const int e = mx_shared_exp(amax);
-        const float inv = exp2_int(-e);
-        uint32_t w[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
-        uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dstT) + static_cast<long long>(d) * r_cap + r0 + rl);
-        o[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        o[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        const int b = row_block[rg];
-        dstT_sf[(static_cast<long long>(d >> 7) * b_cap + b) * 512 + sf_atom_byte(d & 127, rg - (blocks[b].y >> 5))] =
-            static_cast<uint8_t>(e + 127);
-      }
+      for (int q = 0; q < 4; ++q)
+        o[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                          pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
     }
   }
 }
 
-template <bool MX, bool SCALE>
-cudaError_t both_impl(const void* src, int D, int K, const RoutingPtrs& rp, void* dst, uint8_t* dst_sf, void* dstT,
-                      uint8_t* dstT_sf, int r_cap, int b_cap, int /*num_sms*/, cudaStream_t stream) {
-  auto kern = gather_both_kernel<MX, SCALE>;
+template <bool SCALE>
+cudaError_t both_impl(const void* src, int D, int K, const RoutingPtrs& rp, void* dst, void* dstT, int r_cap,
+                      cudaStream_t stream) {
+  auto kern = gather_both_kernel<SCALE>;
   static bool configured = false;
   if (!configured) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBothSmem);
@@ -231,7 +215,161 @@ cudaError_t both_impl(const void* src, int D, int K, const RoutingPtrs& rp, void
   }
   dim3 grid((D + kBothCols - 1) / kBothCols, (r_cap + kBothRows - 1) / kBothRows);
   kern<<<grid, 256, kBothSmem, stream>>>(static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr, rp.perm, rp.scores,
-                                         dst, dst_sf, dstT, dstT_sf, r_cap, b_cap, rp.row_block, rp.blocks);
+                                         static_cast<__nv_bfloat16*>(dst), static_cast<__nv_bfloat16*>(dstT), r_cap);
+  return cudaGetLastError();
+}
+
+// MXFP8 variant of the same pass.  The gathered BF16 rows are staged once
+// (272-byte row pitch: conflict-free 16-byte writes and row reads), both
+// quantised bundles are built in shared memory as 128 x 128-byte tiles in
+// the 128-byte swizzle (16-byte chunk j of line m at chunk j ^ (m % 8)) and
+// leave with two TMA stores: row bundle lines are token rows
+// (dst[r][c0 ..]), column bundle lines are features (dstT[d][r0 ..]).  A row
+// scale (4 blocks of this slab) is one 32-bit word of the row's atom.  Rows
+// past the routed rows are written as zeros; nothing reads them.
+constexpr int kMxPitchB = 2 * kBothCols + 16;
+constexpr int kMxSmem = 1024 + 2 * 16384 + kBothRows * kMxPitchB + kBothRows * 4;
+
+template <bool SCALE>
+__global__ void __launch_bounds__(256) gather_both_mx_kernel(const __grid_constant__ CUtensorMap tm_row,
+                                                             const __grid_constant__ CUtensorMap tm_col,
+                                                             const __nv_bfloat16* __restrict__ src, int D, int K,
+                                                             const int* __restrict__ hdr, const int* __restrict__ perm,
+                                                             const float* __restrict__ scores,
+                                                             uint8_t* __restrict__ dst_sf, uint8_t* __restrict__ dstT_sf,
+                                                             int b_cap, const int* __restrict__ row_block,
+                                                             const int4* __restrict__ blocks) {
+  extern __shared__ uint8_t gmx_smem_raw[];
+  uint8_t* rb = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gmx_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* cb = rb + 16384;
+  uint8_t* xs = cb + 16384;
+  float* s_row = reinterpret_cast<float*>(xs + kBothRows * kMxPitchB);
+  __shared__ int s_blk[kBothRows / 32], s_b0[kBothRows / 32];
+  const int rows = hdr[2];
+  const int r0 = blockIdx.y * kBothRows;
+  if (r0 >= rows) return;
+  const int c0 = blockIdx.x * kBothCols;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < kBothRows / 32) {
+    const bool in = r0 + 32 * tid < rows;
+    const int b = in ? row_block[(r0 >> 5) + tid] : 0;
+    s_blk[tid] = b;
+    s_b0[tid] = in ? blocks[b].y : 0;
+  }
+  // ---- load: thread t moves chunk t%16 (8 values) of rows t/16 + 16j; all
+  // route lookups first, then all eight row loads
+  {
+    constexpr int kPer = kBothRows * 16 / 256;
+    const int chunk = tid & 15, c = c0 + chunk * 8;
+    int route[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int r = r0 + (tid >> 4) + 16 * j;
+      route[j] = (r < rows) ? perm[r] : -1;
+    }
+    uint4 u[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      u[j] = make_uint4(0, 0, 0, 0);
+      if (route[j] >= 0 && c < D)
+        u[j] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(route[j] / K) * D + c));
+    }
+    if (SCALE && chunk == 0) {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) s_row[(tid >> 4) + 16 * j] = route[j] >= 0 ? scores[route[j]] : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      *reinterpret_cast<uint4*>(xs + ((tid >> 4) + 16 * j) * kMxPitchB + chunk * 16) = u[j];
+  }
+  __syncthreads();
+  // ---- row bundle: warp w builds rows 16w .. 16w+15, lane l columns 4l .. 4l+3
+  for (int rr = 0; rr < 16; ++rr) {
+    const int row = warp * 16 + rr;
+    const int r = r0 + row;
+    const uint2 raw = *reinterpret_cast<const uint2*>(xs + row * kMxPitchB + lane * 8);
+    float x0 = bf16_lo(raw.x), x1 = bf16_hi(raw.x), x2 = bf16_lo(raw.y), x3 = bf16_hi(raw.y);
+    if (SCALE) {
+      const float sc = s_row[row];
+      x0 *= sc;
+      x1 *= sc;
+      x2 *= sc;
+      x3 *= sc;
+    }
+    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+    const int e = mx_shared_exp(amax);
+    const float inv = exp2_int(-e);
+    const uint32_t q = cvt_e4m3x2(x0 * inv, x1 * inv) | (cvt_e4m3x2(x2 * inv, x3 * inv) << 16);
+    *reinterpret_cast<uint32_t*>(rb + row * 128 + (((lane >> 2) ^ (row & 7)) << 4) + (lane & 3) * 4) = q;
+    const uint32_t eb = static_cast<uint32_t>(e + 127);
+    const uint32_t w = __shfl_sync(0xFFFFFFFFu, eb, 0) | (__shfl_sync(0xFFFFFFFFu, eb, 8) << 8) |
+                       (__shfl_sync(0xFFFFFFFFu, eb, 16) << 16) | (__shfl_sync(0xFFFFFFFFu, eb, 24) << 24);
+    if (lane == 0 && r < rows) {
+      const int p = r - s_b0[row >> 5];
+      *reinterpret_cast<uint32_t*>(dst_sf + (static_cast<long long>(s_blk[row >> 5]) * (D / 128) + (c0 >> 7)) * 512 +
+                                   (p & 31) * 16 + (p >> 5) * 4) = w;
+    }
+  }
+  // ---- column bundle: thread (cc, half) builds feature c0+cc, rows 64*half .. +63
+  {
+    const int cc = tid & 127, half = tid >> 7;
+    const int d = c0 + cc;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const int rl = half * 64 + g * 32;   // first row of this 32-row group within the tile
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const uint16_t h = *reinterpret_cast<const uint16_t*>(xs + (rl + i) * kMxPitchB + cc * 2);
+        v[i] = __uint_as_float(static_cast<uint32_t>(h) << 16);
+        if (SCALE) v[i] *= s_row[rl + i];
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      const int e = mx_shared_exp(amax);
+      const float inv = exp2_int(-e);
+      uint32_t w[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
+      const int j0 = rl >> 4;
+      *reinterpret_cast<uint4*>(cb + cc * 128 + ((j0 ^ (cc & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(cb + cc * 128 + (((j0 + 1) ^ (cc & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+      if (r0 + rl < rows) {
+        const int rg = (r0 + rl) >> 5;
+        dstT_sf[(static_cast<long long>(d >> 7) * b_cap + s_blk[rl >> 5]) * 512 +
+                sf_atom_byte(d & 127, rg - (s_b0[rl >> 5] >> 5))] = static_cast<uint8_t>(e + 127);
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    tma_store_2d(&tm_row, rb, c0, r0);
+    tma_store_2d(&tm_col, cb, r0, c0);
+    bulk_commit();
+    bulk_wait_read<0>();   // the staging must outlive the stores' reads
+  }
+}
+
+template <bool SCALE>
+cudaError_t both_mx_impl(const CUtensorMap* tm_row, const CUtensorMap* tm_col, const void* src, int D, int K,
+                         const RoutingPtrs& rp, uint8_t* dst_sf, uint8_t* dstT_sf, int r_cap, int b_cap,
+                         cudaStream_t stream) {
+  auto kern = gather_both_mx_kernel<SCALE>;
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(D / kBothCols, r_cap / kBothRows);
+  kern<<<grid, 256, kMxSmem, stream>>>(*tm_row, *tm_col, static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr,
+                                       rp.perm, rp.scores, dst_sf, dstT_sf, b_cap, rp.row_block, rp.blocks);
   return cudaGetLastError();
 }
 
@@ -261,13 +399,15 @@ cudaError_t launch_gather_rows(bool mx, bool use_scores, const void* src, int D,
 
 cudaError_t launch_gather_both(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
                                void* dst, uint8_t* dst_sf, void* dstT, uint8_t* dstT_sf, int r_cap, int b_cap,
-                               int num_sms, cudaStream_t stream) {
+                               int num_sms, cudaStream_t stream, const CUtensorMap* tm_row,
+                               const CUtensorMap* tm_col) {
   if (mx) {
-    return use_scores ? both_impl<true, true>(src, D, K, rp, dst, dst_sf, dstT, dstT_sf, r_cap, b_cap, num_sms, stream)
-                      : both_impl<true, false>(src, D, K, rp, dst, dst_sf, dstT, dstT_sf, r_cap, b_cap, num_sms, stream);
+    if (!tm_row || !tm_col || D % kBothCols != 0 || r_cap % kBothRows != 0) return cudaErrorInvalidValue;
+    return use_scores ? both_mx_impl<true>(tm_row, tm_col, src, D, K, rp, dst_sf, dstT_sf, r_cap, b_cap, stream)
+                      : both_mx_impl<false>(tm_row, tm_col, src, D, K, rp, dst_sf, dstT_sf, r_cap, b_cap, stream);
   }
-  return use_scores ? both_impl<false, true>(src, D, K, rp, dst, dst_sf, dstT, dstT_sf, r_cap, b_cap, num_sms, stream)
-                    : both_impl<false, false>(src, D, K, rp, dst, dst_sf, dstT, dstT_sf, r_cap, b_cap, num_sms, stream);
+  return use_scores ? both_impl<true>(src, D, K, rp, dst, dstT, r_cap, stream)
+                    : both_impl<false>(src, D, K, rp, dst, dstT, r_cap, stream);
 }
 
 }  // namespace moe

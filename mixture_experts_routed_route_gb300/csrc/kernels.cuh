@@ -42,9 +42,12 @@ cudaError_t launch_gather_rows(bool mx, bool use_scores, const void* src, int D,
 // Row bundle and column bundle of the same gathered rows in one pass
 // (training): dstT[d][r] holds the rows transposed to [D, r_cap]; MXFP8
 // quantises it along rows in 32-row blocks (WGRAD contracts over rows).
+// MXFP8 needs tm_row / tm_col: 128 x 128-byte boxes, 128-byte swizzle, over
+// dst [r_cap, D] and dstT [D, r_cap] (the bundles leave by TMA store).
 cudaError_t launch_gather_both(bool mx, bool use_scores, const void* src, int D, int K, const RoutingPtrs& rp,
                                void* dst, uint8_t* dst_sf, void* dstT, uint8_t* dstT_sf, int r_cap, int b_cap,
-                               int num_sms, cudaStream_t stream);
+                               int num_sms, cudaStream_t stream, const CUtensorMap* tm_row = nullptr,
+                               const CUtensorMap* tm_col = nullptr);
 
 // out[t] = bf16((accumulate ? out[t] : 0) + sum_k s(t,k) * h[inv(t,k)]),
 // FP32, k in order; s = 1 when `scores` is NULL.  The token count is T, or

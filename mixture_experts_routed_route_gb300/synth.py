@@ -68,6 +68,11 @@ WORKLOADS = {
     # weight gradients (1.4 GB for W13) still exceed L2
     "profile_e24": Workload("profile_e24", 128, 7168, 2048, 24, 6, "mxfp8", "zipf", inactive_frac=0.10,
                             zipf_s=1.2, train=True, seed=7),
+    # profiling case for the row-sized kernels (gathers, combine): the e384
+    # token count and width (T=2048, D=7168, K=6, so about 12 K routed rows)
+    # with 32 experts, about 10 GB on the device
+    "profile_e32": Workload("profile_e32", 2048, 7168, 2048, 32, 6, "mxfp8", "zipf", inactive_frac=0.10,
+                            zipf_s=1.2, train=True, seed=8),
 }
 
 
