@@ -213,53 +213,83 @@ __device__ __forceinline__ void release_acc(uint64_t* tempty, int lane) {
 
 // h3 / input-gradient rows: out[row][feature] = bf16(acc).
 // With NA = 2 the two accumulators hold features out_col0 + [0, 128) and
-// out_col0 + [128, 256).
+// out_col0 + [128, 256).  Every chunk is read from TMEM first, rounded to
+// BF16 pairs at once (the stored value), and the accumulator handed back
+// before the first store.
 template <int NA>
 __device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow, int lane,
                                           int h, uint64_t* tempty) {
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0);
-  if (32 * h >= t.b_rows) release_acc(tempty, lane);
-#pragma unroll 1
-  for (int j = 0; j < NA; ++j) {
-    const int f = t.out_col0 + j * 128 + lrow;
-    for (int c0 = 32 * h; c0 < t.b_rows; c0 += 64) {
-      uint32_t v[32];
-      tmem_ld32(tbase + j * 128 + c0, v);
-      tmem_ld_wait();
-      if (j == NA - 1 && c0 + 64 >= t.b_rows) release_acc(tempty, lane);
+  uint32_t pk[NA][2][16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        out[static_cast<long long>(t.out_row0 + c0 + i) * p.out0_pitch + f] = __float2bfloat16_rn(u2f(v[i]));
+  for (int j = 0; j < NA; ++j)
+#pragma unroll
+    for (int ci = 0; ci < 2; ++ci) {
+      const int c0 = 32 * h + 64 * ci;
+      if (c0 < t.b_rows) {
+        uint32_t v[32];
+        tmem_ld32(tbase + j * 128 + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 16; ++q) pk[j][ci][q] = pack_bf16x2(u2f(v[2 * q]), u2f(v[2 * q + 1]));
+      }
     }
-  }
+  release_acc(tempty, lane);
+#pragma unroll
+  for (int j = 0; j < NA; ++j)
+#pragma unroll
+    for (int ci = 0; ci < 2; ++ci) {
+      const int c0 = 32 * h + 64 * ci;
+      if (c0 < t.b_rows) {
+        __nv_bfloat16* o = out + static_cast<long long>(t.out_row0 + c0) * p.out0_pitch + t.out_col0 + j * 128 + lrow;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t w = pk[j][ci][i >> 1];
+          o[static_cast<long long>(i) * p.out0_pitch] =
+              __ushort_as_bfloat16(static_cast<unsigned short>((i & 1) ? (w >> 16) : (w & 0xFFFFu)));
+        }
+      }
+    }
 }
 
 // Fused SwiGLU forward: g, u from the two accumulators, rounded to BF16
 // (the stored h1), h2 = SiLU(g) * u in FP32, then the h2 row bundle (W2's
 // operand) and, for training, the h2 column bundle (W2 WGRAD's operand).
+// Both chunks are read from TMEM first, as BF16 (g, u) pairs (the stored
+// h1 and the SwiGLU's inputs), and the accumulator handed back before any
+// store.
 template <bool MX>
 __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow,
                                                int lane, int h, uint64_t* tempty) {
   const int f = t.out_col0 + lrow;
-  if (32 * h >= t.b_rows) release_acc(tempty, lane);
-  for (int c0 = 32 * h; c0 < t.b_rows; c0 += 64) {
-    uint32_t vg[32], vu[32];
-    tmem_ld32(tbase + c0, vg);
-    tmem_ld32(tbase + 128 + c0, vu);
-    tmem_ld_wait();
-    if (c0 + 64 >= t.b_rows) release_acc(tempty, lane);
+  uint32_t gu[2][32];
+#pragma unroll
+  for (int ci = 0; ci < 2; ++ci) {
+    const int c0 = 32 * h + 64 * ci;
+    if (c0 < t.b_rows) {
+      uint32_t vg[32], vu[32];
+      tmem_ld32(tbase + c0, vg);
+      tmem_ld32(tbase + 128 + c0, vu);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) gu[ci][i] = pack_bf16x2(u2f(vg[i]), u2f(vu[i]));
+    }
+  }
+  release_acc(tempty, lane);
+#pragma unroll
+  for (int ci = 0; ci < 2; ++ci) {
+    const int c0 = 32 * h + 64 * ci;
+    if (c0 >= t.b_rows) continue;
     float hv[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const long long row = t.out_row0 + c0 + i;
-      const __nv_bfloat16 gb = __float2bfloat16_rn(u2f(vg[i]));
-      const __nv_bfloat16 ub = __float2bfloat16_rn(u2f(vu[i]));
+      const uint32_t w = gu[ci][i];
       if (p.save_h1) {
-        p.h1[row * p.h1_pitch + f] = gb;
-        p.h1[row * p.h1_pitch + p.F + f] = ub;
+        p.h1[row * p.h1_pitch + f] = __ushort_as_bfloat16(static_cast<unsigned short>(w & 0xFFFFu));
+        p.h1[row * p.h1_pitch + p.F + f] = __ushort_as_bfloat16(static_cast<unsigned short>(w >> 16));
       }
-      const float g = __bfloat162float(gb), u = __bfloat162float(ub);
-      hv[i] = silu_f(g) * u;
+      hv[i] = silu_f(bf16_lo(w)) * bf16_hi(w);
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i)
