@@ -215,8 +215,66 @@ int pair_tiles(int64_t n) { return n % 256 == 0 ? 2 : 1; }
 // The narrow-box maps a weight-gradient GEMM uses for a short last stage.
 bool make_narrow_tmaps(GemmLaunch* g, const void* a, int64_t a_rows, const void* b, int64_t b_rows, bool mx,
                        int64_t cols) {
-  return make_tmap(&g->tmA64, a, mx, a_rows, cols, 128, 64) && make_tmap(&g->tmB64, b, mx, b_rows, cols, 128, 64) &&
-         make_tmap(&g->tmA32, a, mx, a_rows, cols, 128, 32) && make_tmap(&g->tmB32, b, mx, b_rows, cols, 128, 32);
+  return make_tmap(&g->aux[0], a, mx, a_rows, cols, 128, 64) && make_tmap(&g->aux[1], b, mx, b_rows, cols, 128, 64) &&
+         make_tmap(&g->aux[2], a, mx, a_rows, cols, 128, 32) && make_tmap(&g->aux[3], b, mx, b_rows, cols, 128, 32);
+}
+
+// A tensor map of any rank (dims / box innermost first, byte strides of
+// dims 1..rank-1), no interleave.
+bool make_tmap_nd(CUtensorMap* tm, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+                  const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(tm, dt, rank, const_cast<void*>(base), const_cast<cuuint64_t*>(dims), const_cast<cuuint64_t*>(strides),
+            const_cast<cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The larger boxes a grouped-M GEMM loads with (fewer copies per stage for
+// the producer thread to issue):
+//  * both A tiles of a stage in one copy: a 256-row box when they are
+//    adjacent (store GEMMs with two tiles per stage), a 3D box over
+//    [2E halves][F rows][K] when they are W13's gate and up halves
+//    (`halves_f` = F), and likewise their two MXFP8 scale atoms, read as
+//    [row tiles][K/128][128 words] (adjacent) or [2E][F/128][K/128][128]
+//    (halves) from `a_sf`;
+//  * a full 128-row routing block of B in one box.
+bool make_grouped_m_boxes(GemmLaunch* g, const void* a, int64_t a_rows, const void* a_sf, const void* b,
+                          int64_t b_rows, bool mx, int64_t cols, int64_t halves_f = 0) {
+  const int esz = mx ? 1 : 2;
+  const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const cuuint64_t ks = static_cast<cuuint64_t>(cols / 128), atom = 512;
+  if (g->na == 2 && g->epi == kEpiStore) {
+    if (!make_tmap(&g->aux[0], a, mx, a_rows, cols, 256)) return false;
+    if (mx) {
+      const cuuint64_t d[3] = {128, ks, static_cast<cuuint64_t>(a_rows / 128)};
+      const cuuint64_t st[2] = {atom, ks * atom};
+      const cuuint32_t bx[3] = {128, 1, 2};
+      if (!make_tmap_nd(&g->aux[2], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a_sf, d, st, bx, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return false;
+    }
+    g->p.a_pair_box = 1;
+  } else if (g->na == 2 && g->epi == kEpiSwigluFwd && halves_f > 0 && halves_f % 128 == 0) {
+    const cuuint64_t d[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(halves_f),
+                             static_cast<cuuint64_t>(a_rows / halves_f)};
+    const cuuint64_t st[2] = {static_cast<cuuint64_t>(cols * esz), static_cast<cuuint64_t>(halves_f * cols * esz)};
+    const cuuint32_t bx[3] = {static_cast<cuuint32_t>(128 / esz), 128, 2};
+    if (!make_tmap_nd(&g->aux[0], dt, 3, a, d, st, bx, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
+    if (mx) {
+      const cuuint64_t ft = static_cast<cuuint64_t>(halves_f / 128);
+      const cuuint64_t d4[4] = {128, ks, ft, static_cast<cuuint64_t>(a_rows / halves_f)};
+      const cuuint64_t st4[3] = {atom, ks * atom, ft * ks * atom};
+      const cuuint32_t bx4[4] = {128, 1, 1, 2};
+      if (!make_tmap_nd(&g->aux[2], CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, a_sf, d4, st4, bx4,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+        return false;
+    }
+    g->p.a_pair_box = 2;
+  }
+  if (!make_tmap(&g->aux[1], b, mx, b_rows, cols, 128)) return false;
+  g->p.b_full_box = 1;
+  return true;
 }
 
 // Output map of a BF16 weight gradient [rows, cols]: boxes of 64 columns
@@ -446,7 +504,9 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   g1.epi = kEpiSwigluFwd;
   g1.mode = kGroupedM;
   if (!make_tmap(&g1.tmA, W13->data, mx, static_cast<int64_t>(E) * 2 * F, D, 128) ||
-      !make_tmap(&g1.tmB, B(ctx, MOE_BUF_XROW), mx, R, D, 32))
+      !make_tmap(&g1.tmB, B(ctx, MOE_BUF_XROW), mx, R, D, 32) ||
+      !make_grouped_m_boxes(&g1, W13->data, static_cast<int64_t>(E) * 2 * F, W13->scale, B(ctx, MOE_BUF_XROW), R,
+                            mx, D, F))
     return MOE_ERR_CUDA;
   GemmParams& p1 = g1.p;
   p1.hdr = rp.hdr;
@@ -490,7 +550,8 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   g2.epi = kEpiStore;
   g2.mode = kGroupedM;
   if (!make_tmap(&g2.tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128) ||
-      !make_tmap(&g2.tmB, B(ctx, MOE_BUF_H2ROW), mx, R, F, 32))
+      !make_tmap(&g2.tmB, B(ctx, MOE_BUF_H2ROW), mx, R, F, 32) ||
+      !make_grouped_m_boxes(&g2, W2->data, static_cast<int64_t>(E) * D, W2->scale, B(ctx, MOE_BUF_H2ROW), R, mx, F))
     return MOE_ERR_CUDA;
   GemmParams& p2 = g2.p;
   p2.hdr = rp.hdr;
@@ -564,7 +625,9 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g1.epi = kEpiSwigluBwd;
   g1.mode = kGroupedM;
   if (!make_tmap(&g1.tmA, W2->data_t, mx, static_cast<int64_t>(E) * F, D, 128) ||
-      !make_tmap(&g1.tmB, B(ctx, MOE_BUF_DH3ROW), mx, R, D, 32))
+      !make_tmap(&g1.tmB, B(ctx, MOE_BUF_DH3ROW), mx, R, D, 32) ||
+      !make_grouped_m_boxes(&g1, W2->data_t, static_cast<int64_t>(E) * F, W2->scale_t, B(ctx, MOE_BUF_DH3ROW), R,
+                            mx, D))
     return MOE_ERR_CUDA;
   GemmParams& p1 = g1.p;
   p1.hdr = rp.hdr;
@@ -638,7 +701,9 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g3.epi = kEpiStore;
   g3.mode = kGroupedM;
   if (!make_tmap(&g3.tmA, W13->data_t, mx, static_cast<int64_t>(E) * D, 2 * F, 128) ||
-      !make_tmap(&g3.tmB, B(ctx, MOE_BUF_DH1ROW), mx, R, 2 * F, 32))
+      !make_tmap(&g3.tmB, B(ctx, MOE_BUF_DH1ROW), mx, R, 2 * F, 32) ||
+      !make_grouped_m_boxes(&g3, W13->data_t, static_cast<int64_t>(E) * D, W13->scale_t, B(ctx, MOE_BUF_DH1ROW), R,
+                            mx, 2 * F))
     return MOE_ERR_CUDA;
   GemmParams& p3 = g3.p;
   p3.hdr = rp.hdr;

@@ -456,9 +456,9 @@ struct Cfg {
 template <bool MX, int NA, int EPI, int MODE>
 __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA64,
-                const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmA32,
-                const __grid_constant__ CUtensorMap tmB32, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap aux0,
+                const __grid_constant__ CUtensorMap aux1, const __grid_constant__ CUtensorMap aux2,
+                const __grid_constant__ CUtensorMap aux3, const GemmParams p) {
   using C = Cfg<MX, NA, MODE>;
   constexpr int S = C::S;
   constexpr int kStep = (NA == 2 && EPI != kEpiSwigluFwd) ? 256 : 128;
@@ -493,10 +493,16 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     tma_prefetch(&tmB);
     if (C::WGRAD && p.tma_store) tma_prefetch(&tmC);
     if (C::WGRAD) {
-      tma_prefetch(&tmA64);
-      tma_prefetch(&tmB64);
-      tma_prefetch(&tmA32);
-      tma_prefetch(&tmB32);
+      tma_prefetch(&aux0);
+      tma_prefetch(&aux1);
+      tma_prefetch(&aux2);
+      tma_prefetch(&aux3);
+    } else {
+      if (p.a_pair_box) {
+        tma_prefetch(&aux0);
+        if (MX) tma_prefetch(&aux2);
+      }
+      if (p.b_full_box) tma_prefetch(&aux1);
     }
   }
   if (warp == 1) {
@@ -549,16 +555,41 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
           const int rb = stage_row_bytes<MODE, C::BK, MX ? 1 : 2>(t, ks);
           mbar_arrive_expect_tx(&full[slot], (NA * 128 + t.b_rows) * rb + C::SF_BYTES);
           const int kx = t.k0 + ks * C::BK;
-          const CUtensorMap* ta = rb == 128 ? &tmA : (rb == 64 ? &tmA64 : &tmA32);
-          const CUtensorMap* tb = rb == 128 ? &tmB : (rb == 64 ? &tmB64 : &tmB32);
+          if (MODE == kGroupedK) {
+            const CUtensorMap* ta = rb == 128 ? &tmA : (rb == 64 ? &aux0 : &aux2);
+            const CUtensorMap* tb = rb == 128 ? &tmB : (rb == 64 ? &aux1 : &aux3);
 #pragma unroll
-          for (int j = 0; j < NA; ++j) tma_load_2d(sa + j * kABytes, ta, &full[slot], kx, t.a_row[j]);
-          for (int c = 0; c < t.b_rows / p.b_box_rows; ++c)
-            tma_load_2d(sb + c * p.b_box_rows * rb, tb, &full[slot], kx, t.b_row0 + p.b_box_rows * c);
+            for (int j = 0; j < NA; ++j) tma_load_2d(sa + j * kABytes, ta, &full[slot], kx, t.a_row[j]);
+            for (int c = 0; c < t.b_rows / p.b_box_rows; ++c)
+              tma_load_2d(sb + c * p.b_box_rows * rb, tb, &full[slot], kx, t.b_row0 + p.b_box_rows * c);
+          } else {
+            // fewer, larger copies: the issue rate of the producer thread
+            // bounds compute-bound shapes
+            if (NA == 2 && p.a_pair_box == 1) {
+              tma_load_2d(sa, &aux0, &full[slot], kx, t.a_row[0]);   // rows a_row[0] .. +255
+            } else if (NA == 2 && p.a_pair_box == 2) {
+              tma_load_3d(sa, &aux0, &full[slot], kx, t.out_col0, 2 * t.e);   // gate, then up
+            } else {
+#pragma unroll
+              for (int j = 0; j < NA; ++j) tma_load_2d(sa + j * kABytes, &tmA, &full[slot], kx, t.a_row[j]);
+            }
+            if (t.b_rows == 128 && p.b_full_box) {
+              tma_load_2d(sb, &aux1, &full[slot], kx, t.b_row0);
+            } else {
+              for (int c = 0; c < t.b_rows / p.b_box_rows; ++c)
+                tma_load_2d(sb + c * p.b_box_rows * 128, &tmB, &full[slot], kx, t.b_row0 + p.b_box_rows * c);
+            }
+          }
           if (MX) {
+            if (MODE == kGroupedM && NA == 2 && p.a_pair_box == 1) {
+              tma_load_3d(ssf, &aux2, &full[slot], 0, ks, t.a_row[0] >> 7);
+            } else if (MODE == kGroupedM && NA == 2 && p.a_pair_box == 2) {
+              tma_load_4d(ssf, &aux2, &full[slot], 0, ks, t.out_col0 >> 7, 2 * t.e);
+            } else {
 #pragma unroll
-            for (int j = 0; j < NA; ++j)
-              bulk_load(ssf + j * kAtom, p.sfa + (t.sfa_atom[j] + ks) * kAtom, kAtom, &full[slot]);
+              for (int j = 0; j < NA; ++j)
+                bulk_load(ssf + j * kAtom, p.sfa + (t.sfa_atom[j] + ks) * kAtom, kAtom, &full[slot]);
+            }
             bulk_load(ssf + NA * kAtom, p.sfb + (t.sfb_atom + ks) * kAtom, kAtom, &full[slot]);
           }
         }
@@ -729,7 +760,7 @@ cudaError_t launch_impl(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
     configured = true;
   }
   const int grid = max(1, min(num_sms, g.max_tiles));
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.tmC, g.tmA64, g.tmB64, g.tmA32, g.tmB32, g.p);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.tmC, g.aux[0], g.aux[1], g.aux[2], g.aux[3], g.p);
   return cudaGetLastError();
 }
 

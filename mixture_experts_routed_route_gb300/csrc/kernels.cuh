@@ -107,18 +107,29 @@ struct GemmParams {
   int dw_fp32;
   int dw_accum;
   int tma_store;          // weight gradient written through shared memory + TMA
+  // grouped-M, both A tiles of a stage in one copy: aux[0] holds their data
+  // (1: adjacent 128-row tiles, a 256-row box; 2: gate and up halves F rows
+  // apart, a 3D [halves][F][K] box) and aux[2] their two scale atoms (1:
+  // adjacent tiles, 3D atom view; 2: halves, 4D atom view)
+  int a_pair_box;
+  int b_full_box;         // grouped-M: aux[1] loads a full 128-row block in one box
   uint32_t* err;
 };
 
 struct GemmLaunch {
   bool mx;
-  int na;                 // A tiles per B tile (2 for the fused SwiGLU forward)
+  int na;                 // A tiles per stage (gate + up, or two adjacent weight tiles)
   GemmEpi epi;
   GemmMode mode;
   CUtensorMap tmA, tmB, tmC;  // tmC: weight-gradient output (TMA store)
-  // grouped-K: maps of A and B with 64- and 32-byte wide boxes (64B / 32B
-  // swizzle) for a last stage that holds only 32 or 64 bytes of each row
-  CUtensorMap tmA64, tmB64, tmA32, tmB32;
+  // auxiliary maps, by mode:
+  //  grouped-K: aux[0] / aux[1] = A / B with 64-byte wide boxes (64B swizzle),
+  //             aux[2] / aux[3] = A / B with 32-byte wide boxes (32B swizzle),
+  //             for a last stage that holds only 64 or 32 bytes of each row;
+  //  grouped-M: aux[0] = both A tiles of a stage in one box (a_pair_box),
+  //             aux[1] = B with 128-row boxes (b_full_box),
+  //             aux[2] = the A tiles' two scale atoms in one box (a_pair_box).
+  CUtensorMap aux[4];
   GemmParams p;
   int max_tiles;          // upper bound of the tile count (grid sizing)
 };
