@@ -449,7 +449,10 @@ struct Cfg {
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int GROUP_THREADS = EPI_THREADS / EPI_GROUPS;
   static_assert(!WGRAD || (NA == 1 && ACC_BUFS == EPI_GROUPS), "one accumulator buffer per epilogue group");
-  static constexpr int THREADS = 64 + EPI_THREADS;
+  // MXFP8: one more warp copies each stage's scale atoms to TMEM, so the
+  // MMA thread issues nothing but MMAs and commits
+  static constexpr int SF_WARPS = MX ? 1 : 0;
+  static constexpr int THREADS = 64 + EPI_THREADS + 32 * SF_WARPS;
   static constexpr int SMEM = 1024 + S * STAGE + STAGING + 256 + kCacheBytes;
 };
 
@@ -470,7 +473,9 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + C::ACC_BUFS;
   uint64_t* drain = tempty + C::ACC_BUFS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sf_full = drain + 1;            // [S]: a stage's scale atoms are in TMEM (MXFP8)
+  uint64_t* sf_drain = sf_full + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_abort = abort_flag + 1;  // [EPI_GROUPS]: a group's warps leave together
   uint8_t* cache = staging + C::STAGING + 256;
@@ -486,6 +491,8 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       mbar_init(&tempty[a], C::EPI_WARPS / C::EPI_GROUPS);
     }
     mbar_init(drain, 1);
+    for (int s2 = 0; s2 < S; ++s2) mbar_init(&sf_full[s2], 1);
+    mbar_init(sf_drain, 1);
     *abort_flag = 0;
     for (int g = 0; g < C::EPI_GROUPS; ++g) epi_abort[g] = 0;
     mbar_fence_init();
@@ -618,7 +625,9 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       const uint32_t idesc = MX ? idesc_mxf8(t.b_rows, 0, 0) : idesc_bf16(t.b_rows);
       for (int ks = 0; ks < t.kstages; ++ks, ++it) {
         const uint32_t slot = it % S, ph = (it / S) & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], ph, abort_flag, p.err))) {
+        // MXFP8: the scale warp's commit for this stage follows its own wait
+        // for the stage's data, so it covers both
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(MX ? &sf_full[slot] : &full[slot], ph, abort_flag, p.err))) {
           ok = false;
           break;
         }
@@ -633,10 +642,6 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
         for (int j = 0; j < NA; ++j) adesc0[j] = sdesc_k_sw(sa + j * kABytes, rb);
         const int nmma = (ks == t.kstages - 1) ? t.klast / C::KMMA : C::MMAS;
         if (lane == 0) {
-          if (MX) {
-#pragma unroll
-            for (int j = 0; j <= NA; ++j) tc_cp_sf(sfcol + j * 4, sdesc_sf_atom(sb + kBBytes + j * kAtom));
-          }
 #pragma unroll
           for (int k = 0; k < C::MMAS; ++k) {
             if (k < nmma) {
@@ -667,6 +672,39 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     if (lane == 0) {
       tc_commit(drain);
       drain_wait(drain, 0);
+    }
+    __syncwarp();
+  } else if (MX && warp == 2 + C::EPI_WARPS) {
+    // ------------------------------------------------- scale-atom copier
+    // Each stage's scale atoms go from shared memory to the stage's TMEM
+    // columns once its data has landed; the commit tells the MMA thread.
+    // A slot's columns are rewritten only after the producer refilled the
+    // slot, i.e. after the MMAs that read them completed.
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE, C::BK, kStep>(p, tile, nblk, mc);
+      for (int ks = 0; ks < t.kstages; ++ks, ++it) {
+        const uint32_t slot = it % S, ph = (it / S) & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], ph, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t ssf = smem_u32(smem + slot * C::STAGE) + NA * kABytes + kBBytes;
+          const uint32_t sfcol = tmem + C::SF_COL0 + slot * C::SF_COLS;
+#pragma unroll
+          for (int j = 0; j <= NA; ++j) tc_cp_sf(sfcol + j * 4, sdesc_sf_atom(ssf + j * kAtom));
+          tc_commit(&sf_full[slot]);
+        }
+        __syncwarp();
+      }
+    }
+    // every copy issued here must be complete before TMEM is released
+    if (lane == 0) {
+      tc_commit(sf_drain);
+      drain_wait(sf_drain, 0);
     }
     __syncwarp();
   } else {
