@@ -222,18 +222,19 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, ui
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0);
   uint32_t pk[NA][2][16];
 #pragma unroll
-  for (int j = 0; j < NA; ++j)
+  for (int ci = 0; ci < 2; ++ci) {
+    const int c0 = 32 * h + 64 * ci;
+    if (c0 < t.b_rows) {
+      uint32_t v[NA][32];   // both accumulators' chunk, one wait
 #pragma unroll
-    for (int ci = 0; ci < 2; ++ci) {
-      const int c0 = 32 * h + 64 * ci;
-      if (c0 < t.b_rows) {
-        uint32_t v[32];
-        tmem_ld32(tbase + j * 128 + c0, v);
-        tmem_ld_wait();
+      for (int j = 0; j < NA; ++j) tmem_ld32(tbase + j * 128 + c0, v[j]);
+      tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 16; ++q) pk[j][ci][q] = pack_bf16x2(u2f(v[2 * q]), u2f(v[2 * q + 1]));
-      }
+      for (int j = 0; j < NA; ++j)
+#pragma unroll
+        for (int q = 0; q < 16; ++q) pk[j][ci][q] = pack_bf16x2(u2f(v[j][2 * q]), u2f(v[j][2 * q + 1]));
     }
+  }
   release_acc(tempty, lane);
 #pragma unroll
   for (int j = 0; j < NA; ++j)
