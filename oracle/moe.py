@@ -45,6 +45,16 @@ Readings of the pages (each also listed in the design notes)
   precision as on the GPU.
 * MXFP8 WGRAD operands are column bundles: the unquantised source quantised
   in 32-row blocks aligned to each expert's first row.
+* Clamped SwiGLU ("Meta Dist-MoE: Open-Source Fused MoE Kernels for
+  Blackwell", "Supported modes", lists plain and clamped SwiGLU without
+  defining the clamp): with a limit L > 0, g is clamped from above and u on
+  both sides before the plain SwiGLU, h2 = SiLU(min(g, L)) * clamp(u, -L, L),
+  on the BF16-rounded h1; the backward passes a gradient where the input lies
+  inside the clamp range, bounds included (the convention of a clamp's
+  subgradient).  L = 0 is the plain SwiGLU.
+* Inference weights with 1x32 blocks (same section: "32x32 blocks for MXFP8
+  training-compatible values or 1x32 for inference"): one scale per 32
+  consecutive values of a weight row along the contraction axis.
 """
 
 from collections import namedtuple
@@ -144,18 +154,45 @@ def _q_col(v, precision):
     return fm.mx_fake_quant(v, axis=0)
 
 
-def prepare_weight(w_e, precision):
-    """One expert's weight as the GEMMs consume it (MXFP8: 32x32 blocks)."""
+def prepare_weight(w_e, precision, blocks="32x32"):
+    """One expert's weight [N, K] as the GEMMs consume it: MXFP8 with 32x32
+    blocks (training) or 1x32 blocks along K (inference)."""
     w_e = np.asarray(w_e, dtype=np.float64)
     if precision == "mxfp8":
+        if blocks == "1x32":
+            return fm.mx_fake_quant(w_e, axis=-1)
         q, e = fm.mx_quantize_weight_32x32(w_e)
         return fm.mx_dequantize_weight_32x32(q, e)
     return w_e
 
 
+def swiglu(g, u, limit=0.0):
+    """h2 = SiLU(g) * u, with g clamped to <= limit and u to [-limit, limit]
+    when limit > 0 (clamped SwiGLU, reading in the module docstring)."""
+    if limit > 0:
+        g = np.minimum(g, limit)
+        u = np.clip(u, -limit, limit)
+    return silu(g) * u
+
+
+def swiglu_grad(g, u, dh, limit=0.0):
+    """(dg, du) of ``swiglu`` at (g, u) for the upstream gradient dh."""
+    if limit > 0:
+        gc, uc = np.minimum(g, limit), np.clip(u, -limit, limit)
+        return dh * uc * silu_grad(gc) * (g <= limit), dh * silu(gc) * (np.abs(u) <= limit)
+    return dh * u * silu_grad(g), dh * silu(g)
+
+
+def clip_counts(h1, F, limit):
+    """Numbers of gate and up values the clamp changes (clip statistics)."""
+    if limit <= 0:
+        return 0, 0
+    return int(np.sum(h1[:, :F] > limit)), int(np.sum(np.abs(h1[:, F:]) > limit))
+
+
 # ------------------------------------------------------------------ forward
 
-def forward(x, ids, scores, w13, w2, precision, out_init=None, pad=PAD):
+def forward(x, ids, scores, w13, w2, precision, out_init=None, pad=PAD, swiglu_limit=0.0, weight_blocks="32x32"):
     """Routed forward (see module docstring).
 
     x [T,D] (BF16 values as float64), ids [T,K] int, scores [T,K] float32,
@@ -184,22 +221,23 @@ def forward(x, ids, scores, w13, w2, precision, out_init=None, pad=PAD):
         a, b = rt.poffsets[e], rt.poffsets[e + 1]
         if a == b:
             continue
-        w13e = prepare_weight(w13[e], precision)
+        w13e = prepare_weight(w13[e], precision, weight_blocks)
         h1_exact[a:b] = xq[a:b] @ w13e.T
         h1[a:b] = _round_out(h1_exact[a:b], precision)
     g, u = h1[:, :F], h1[:, F:]
-    h2 = silu(g) * u
+    h2 = swiglu(g, u, swiglu_limit)
     h2q = _q_row(h2, precision)
     for e in range(E):
         a, b = rt.poffsets[e], rt.poffsets[e + 1]
         if a == b:
             continue
-        w2e = prepare_weight(w2[e], precision)
+        w2e = prepare_weight(w2[e], precision, weight_blocks)
         h3[a:b] = _round_out(h2q[a:b] @ w2e.T, precision)
     out = combine(h3, rt.inv.reshape(T, K), scores, out_init, precision)
     return dict(out=out, routing=rt, xg=xg, xq=xq, h1=h1, h1_exact=h1_exact, h2=h2, h2q=h2q,
                 h3=h3, ids=np.asarray(ids), scores=np.asarray(scores, np.float32),
-                precision=precision, T=T, D=D, F=F, E=E, K=K)
+                precision=precision, T=T, D=D, F=F, E=E, K=K, swiglu_limit=swiglu_limit,
+                clip=clip_counts(h1, F, swiglu_limit))
 
 
 def combine(h3, inv, scores, out_init, precision):
@@ -246,8 +284,7 @@ def backward(state, dY, w13, w2, dx_init=None, dw_fp32=False):
         if a == b:
             continue
         dh2[a:b] = dh3_row[a:b] @ prepare_weight(w2[e], p)
-    dg = dh2 * u * silu_grad(g)
-    du = dh2 * silu(g)
+    dg, du = swiglu_grad(g, u, dh2, state.get("swiglu_limit", 0.0))
     dh1 = np.concatenate([dg, du], axis=1)
     dh1_row = _q_row(dh1, p)
     dh1_col = _q_col(dh1, p)
@@ -286,7 +323,8 @@ def backward(state, dY, w13, w2, dx_init=None, dw_fp32=False):
 
 # ------------------------------------------------- brute-force per-token forward
 
-def forward_per_token(x, ids, scores, w13, w2, precision, out_init=None, tokens=None):
+def forward_per_token(x, ids, scores, w13, w2, precision, out_init=None, tokens=None, swiglu_limit=0.0,
+                      weight_blocks="32x32"):
     """Forward without any permutation: for each token, loop over its K
     routes and run that expert's SwiGLU FFN on the single row.
 
@@ -302,7 +340,8 @@ def forward_per_token(x, ids, scores, w13, w2, precision, out_init=None, tokens=
 
     def wts(e):
         if e not in cache:
-            cache[e] = (prepare_weight(w13[e], precision), prepare_weight(w2[e], precision))
+            cache[e] = (prepare_weight(w13[e], precision, weight_blocks),
+                        prepare_weight(w2[e], precision, weight_blocks))
         return cache[e]
 
     out = {}
@@ -316,7 +355,7 @@ def forward_per_token(x, ids, scores, w13, w2, precision, out_init=None, tokens=
             w13e, w2e = wts(e)
             F = w13e.shape[0] // 2
             h1 = _round_out(w13e @ xt, precision)
-            h2 = _q_row((silu(h1[:F]) * h1[F:])[None, :], precision)[0]
+            h2 = _q_row(swiglu(h1[:F], h1[F:], swiglu_limit)[None, :], precision)[0]
             h3 = _round_out(w2e @ h2, precision)
             acc = acc + np.float64(np.float32(scores[t, k])) * h3
         out[t] = _round_out(acc, precision)

@@ -32,10 +32,11 @@ def useful_flops(ids, D, F, backward):
     return 6.0 * R * D * F * (3.0 if backward else 1.0)
 
 
-def run(x, ids, scores, w13_sub, w2_sub, experts, precision, dY=None):
-    """Oracle forward (and backward when dY is given) of the sample."""
+def run(x, ids, scores, w13_sub, w2_sub, experts, precision, dY=None, **variant):
+    """Oracle forward (and backward when dY is given) of the sample;
+    ``variant`` passes swiglu_limit / weight_blocks to the forward."""
     sub_ids = restrict_routes(ids, experts)
-    st = moe.forward(x, sub_ids, scores, w13_sub, w2_sub, precision)
+    st = moe.forward(x, sub_ids, scores, w13_sub, w2_sub, precision, **variant)
     res = {"state": st, "ids": sub_ids, "out": st["out"]}
     if dY is not None:
         res["grads"] = moe.backward(st, dY, w13_sub, w2_sub)

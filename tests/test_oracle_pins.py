@@ -338,3 +338,88 @@ def test_rounded_backward_tracks_exact_backward(precision):
     for k in ("dX", "dW13", "dW2"):
         err = np.max(np.abs(rd[k] - ex[k])) / np.max(np.abs(ex[k]))
         assert err < tol, (k, err)
+
+
+# ------------------------------------------------------ clamped SwiGLU, 1x32 weights
+# "Meta Dist-MoE: Open-Source Fused MoE Kernels for Blackwell", "Supported
+# modes": plain and clamped SwiGLU; 1x32 weight blocks for inference.
+
+def test_clamped_swiglu_closed_form():
+    # SiLU(1) = 1 / (1 + e^-1) = 0.7310585786300049; SiLU(-5) = -5 / (1 + e^5)
+    g = np.array([2.0, -5.0, 0.5, 3.0])
+    u = np.array([3.0, -10.0, 0.25, -0.5])
+    h = moe.swiglu(g, u, limit=1.0)
+    assert h[0] == pytest.approx(0.7310585786300049 * 1.0, rel=1e-15)      # g -> 1, u -> 1
+    assert h[1] == pytest.approx((-5.0 / (1.0 + np.exp(5.0))) * -1.0, rel=1e-15)   # u -> -1
+    assert h[2] == pytest.approx(0.5 / (1.0 + np.exp(-0.5)) * 0.25, rel=1e-15)    # inside: unchanged
+    assert h[3] == pytest.approx(0.7310585786300049 * -0.5, rel=1e-15)     # only g clamped
+    # limit 0 is the plain SwiGLU, and a limit above every value changes nothing
+    assert np.array_equal(moe.swiglu(g, u, 0.0), moe.silu(g) * u)
+    assert np.array_equal(moe.swiglu(g, u, 100.0), moe.silu(g) * u)
+
+
+def test_clamped_swiglu_grad_matches_finite_differences():
+    rng = np.random.default_rng(31)
+    L = 0.8
+    g = rng.uniform(-3, 3, 200)
+    u = rng.uniform(-3, 3, 200)
+    keep = (np.abs(g - L) > 1e-3) & (np.abs(np.abs(u) - L) > 1e-3)   # away from the kinks
+    g, u = g[keep], u[keep]
+    dh = rng.standard_normal(g.shape)
+    dg, du = moe.swiglu_grad(g, u, dh, L)
+    h = 1e-7
+    fd_g = (moe.swiglu(g + h, u, L) - moe.swiglu(g - h, u, L)) / (2 * h) * dh
+    fd_u = (moe.swiglu(g, u + h, L) - moe.swiglu(g, u - h, L)) / (2 * h) * dh
+    assert np.allclose(dg, fd_g, rtol=1e-6, atol=1e-9)
+    assert np.allclose(du, fd_u, rtol=1e-6, atol=1e-9)
+    assert np.all(dg[g > L] == 0.0) and np.all(du[np.abs(u) > L] == 0.0)
+
+
+def test_clamped_layer_backward_matches_finite_differences():
+    T, D, F, E, K = 6, 5, 4, 3, 2
+    x, ids, s, w13, w2 = _case(T, D, F, E, K, 16, inactive=0.0)
+    x = x * 3.0                   # large enough that some gate / up values clip
+    L = 0.3
+    dY = np.random.default_rng(33).standard_normal((T, D))
+    st = moe.forward(x, ids, s, w13, w2, "f64", swiglu_limit=L)
+    F_ = st["F"]
+    g1, u1 = st["h1"][:, :F_], st["h1"][:, F_:]
+    assert st["clip"][0] > 0 and st["clip"][1] > 0
+    assert np.min(np.abs(g1 - L)) > 1e-5 and np.min(np.abs(np.abs(u1) - L)) > 1e-5
+    grads = moe.backward(st, dY, w13, w2)
+    h = 1e-7
+
+    def loss(x_):
+        return float(np.sum(dY * moe.forward(x_, ids, s, w13, w2, "f64", swiglu_limit=L)["out"]))
+
+    for idx in np.ndindex(x.shape):
+        a1, a2 = x.copy(), x.copy()
+        a1[idx] += h
+        a2[idx] -= h
+        assert grads["dX"][idx] == pytest.approx((loss(a1) - loss(a2)) / (2 * h), rel=1e-5, abs=1e-8)
+
+
+def test_clip_counts_count_the_clamped_values():
+    h1 = np.array([[0.5, 2.0, -3.0, 0.1], [1.5, -1.0, 0.2, -1.5]])   # F = 2: gate cols 0-1, up cols 2-3
+    assert moe.clip_counts(h1, 2, 1.0) == (2, 2)    # gate > 1: 2.0, 1.5; |up| > 1: -3.0, -1.5
+    assert moe.clip_counts(h1, 2, 0.0) == (0, 0)
+
+
+def test_weight_1x32_blocks_are_per_row():
+    rng = np.random.default_rng(35)
+    w = rng.standard_normal((64, 128))
+    q = moe.prepare_weight(w, "mxfp8", "1x32")
+    w2 = w.copy()
+    w2[5, 40] = 1e4               # an outlier in row 5, block 1
+    q2 = moe.prepare_weight(w2, "mxfp8", "1x32")
+    changed = np.argwhere(q2 != q)
+    # only that row's 32-value block is affected (1x32), not its 32x32 tile
+    assert set(map(tuple, changed[:, :1].tolist())) == {(5,)}
+    assert changed[:, 1].min() >= 32 and changed[:, 1].max() < 64
+    t1, t2 = moe.prepare_weight(w, "mxfp8"), moe.prepare_weight(w2, "mxfp8")
+    assert len(set(np.argwhere(t2 != t1)[:, 0].tolist())) > 1     # 32x32: the whole tile moves
+    # every 1x32 block of every row is the MX quantisation of that block alone
+    for r in (0, 5, 63):
+        for b in range(4):
+            blk = w[r, 32 * b:32 * (b + 1)][None, :]
+            assert np.array_equal(q[r, 32 * b:32 * (b + 1)], fm.mx_fake_quant(blk, axis=-1)[0])
