@@ -68,7 +68,12 @@ typedef enum {
 #define MOE_DEV_ERR_INACTIVE_SCORE  0x2u  /* ID -1 with score != 0 (debug only) */
 #define MOE_DEV_ERR_TIMEOUT         0x4u  /* a bounded device wait expired      */
 
-typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
+/* MOE_MXFP8_1X32 is a weight preparation, not a layer precision: MXFP8
+ * weights with one scale per 1x32 block along K ("Meta Dist-MoE:
+ * Open-Source Fused MoE Kernels for Blackwell", "Supported modes": 32x32
+ * blocks for training-compatible values, 1x32 for inference).  Such a
+ * weight feeds moe_forward of an MXFP8 context; moe_backward rejects it. */
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_MXFP8_1X32 = 2 } moe_precision;
 
 /* moe_config.flags */
 #define MOE_TRAINING      0x1u  /* forward saves state; backward is allowed   */
@@ -96,8 +101,13 @@ typedef struct {
   int32_t d_ff;           /* F (h1 has 2F columns: gate then up)            */
   int32_t num_experts;    /* E                                              */
   int32_t top_k;          /* K routes per token                             */
-  moe_precision precision;
+  moe_precision precision; /* MOE_BF16 or MOE_MXFP8                         */
   uint32_t flags;         /* MOE_TRAINING | MOE_DEBUG_CHECKS                */
+  float swiglu_limit;     /* 0: plain SwiGLU.  L > 0: clamped SwiGLU ("Meta
+                           * Dist-MoE...", "Supported modes"), h2 =
+                           * SiLU(min(g, L)) * clamp(u, -L, L) on the BF16 h1;
+                           * the backward's gradient is zero where g > L
+                           * (for g) or |u| > L (for u).  Finite, >= 0.   */
 } moe_config;
 
 /*
@@ -216,6 +226,10 @@ MOE_API int64_t moe_row_capacity(const moe_config* cfg);
  *           written to the scale atoms [E*N/128][K/128] and, when
  *           data_t != NULL, the transposed codes to data_t [E,K,N] with
  *           scale atoms [E*K/128][N/128] in scale_t.  data may not be NULL.
+ *   MXFP8_1X32: inference weights, one E8M0 scale per 32 consecutive values
+ *           of a row along K (same rule), codes to data [E,N,K] and scales
+ *           to the atoms [E*N/128][K/128]; data_t and scale_t must be NULL.
+ *           Use the result with moe_weight.precision = MOE_MXFP8_1X32.
  *   BF16:   data and scale must be NULL; data_t (BF16 [E,K,N]) receives the
  *           transpose used by the input-gradient GEMMs.
  * The outputs are caller-owned device buffers.  Enqueued on `stream`.
@@ -269,6 +283,16 @@ MOE_API moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dou
 /* Synchronise the device, return the error word's bits in *bits and clear
  * it.  Not for use inside graph capture. */
 MOE_API moe_status moe_ctx_get_error(moe_ctx* ctx, uint32_t* bits);
+
+/* Clip statistics of the clamped SwiGLU ("Meta Dist-MoE: Open-Source Fused
+ * MoE Kernels for Blackwell", "Supported modes" lists clip statistics; the
+ * page does not define them, so these are the counts of the clamp): the
+ * numbers of gate values above swiglu_limit (counts[0]) and of up values
+ * outside [-limit, limit] (counts[1]) that every moe_forward since the last
+ * call of this function clamped, over routed rows (pad rows never clip).
+ * Zero with swiglu_limit == 0.  Synchronises the device, then clears the
+ * counters.  Not for use inside graph capture. */
+MOE_API moe_status moe_ctx_clip_stats(moe_ctx* ctx, uint64_t* counts);
 
 /* Copy `bytes` from device memory to host memory (synchronous).  A helper
  * for tests that inspect scratch; not part of the hot path. */

@@ -30,6 +30,7 @@ MOE_DEV_ERR_TIMEOUT = 0x4
 
 MOE_BF16 = 0
 MOE_MXFP8 = 1
+MOE_MXFP8_1X32 = 2    # weight preparation only: 1x32 inference blocks
 
 MOE_TRAINING = 0x1
 MOE_DEBUG_CHECKS = 0x2
@@ -54,7 +55,7 @@ MOE_BUF_NUM = 16
 class moe_config(ctypes.Structure):
     _fields_ = [("max_tokens", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32), ("precision", ctypes.c_int),
-                ("flags", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("swiglu_limit", ctypes.c_float)]
 
 
 class moe_weight(ctypes.Structure):
@@ -82,6 +83,7 @@ _SIGNATURES = {
     "moe_ctx_destroy": (ctypes.c_int, [_P]),
     "moe_ctx_buffer": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
     "moe_ctx_get_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_ctx_clip_stats": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
     "moe_debug_copy_to_host": (ctypes.c_int, [_P, _P, ctypes.c_size_t]),
     "prepare_block_scaled_weight": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
                                                    _P, _P, _P, _P, _P]),
@@ -144,8 +146,8 @@ def _check(fn, status):
         raise MoEError(fn, status)
 
 
-def make_config(max_tokens, d_model, d_ff, num_experts, top_k, precision, flags=0):
-    return moe_config(max_tokens, d_model, d_ff, num_experts, top_k, precision, flags)
+def make_config(max_tokens, d_model, d_ff, num_experts, top_k, precision, flags=0, swiglu_limit=0.0):
+    return moe_config(max_tokens, d_model, d_ff, num_experts, top_k, precision, flags, swiglu_limit)
 
 
 # ------------------------------------------------------------- C functions
@@ -187,6 +189,13 @@ def moe_ctx_buffer(ctx, which):
     p, nb = ctypes.c_void_p(), ctypes.c_size_t()
     _check("moe_ctx_buffer", LIB.moe_ctx_buffer(ctx, which, ctypes.byref(p), ctypes.byref(nb)))
     return p.value, nb.value
+
+
+def moe_ctx_clip_stats(ctx):
+    """(clamped gate count, clamped up count) since the last call; clears them."""
+    counts = (ctypes.c_uint64 * 2)()
+    _check("moe_ctx_clip_stats", LIB.moe_ctx_clip_stats(ctx, counts))
+    return int(counts[0]), int(counts[1])
 
 
 def moe_ctx_get_error(ctx):

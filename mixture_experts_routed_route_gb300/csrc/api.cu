@@ -28,6 +28,7 @@ struct moe_ctx {
   void* buf[MOE_BUF_NUM];
   size_t buf_bytes[MOE_BUF_NUM];
   uint32_t* err;
+  unsigned long long* clip;   // [2] clamped gate / up counts (clip statistics)
   bool timing;
   cudaEvent_t ev[2][8];
   uint64_t launches;
@@ -45,6 +46,7 @@ bool config_ok(const moe_config* c) {
   if (c->num_experts < 1 || c->num_experts > 1024) return false;
   if (c->d_model < 128 || c->d_ff < 128) return false;
   if (c->precision != MOE_BF16 && c->precision != MOE_MXFP8) return false;
+  if (!(c->swiglu_limit >= 0.0f) || c->swiglu_limit > 3.0e38f) return false;   // also rejects NaN
   const int64_t routes = static_cast<int64_t>(c->max_tokens) * c->top_k;
   if (routes + 31LL * c->num_experts > (1LL << 28)) return false;
   return true;
@@ -142,7 +144,7 @@ ScratchLayout scratch_layout(const moe_config* c) {
     sz[MOE_BUF_DXR] = R * D * 2;
   }
   sz[MOE_BUF_ROUTING] = saved_layout(c).routing_bytes;
-  sz[MOE_BUF_ERROR] = 16;
+  sz[MOE_BUF_ERROR] = 32;   // error word at 0, clip counters at 16
   size_t off = 0;
   for (int i = 0; i < MOE_BUF_NUM; ++i) {
     L.off[i] = off;
@@ -299,8 +301,12 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
     if (_e != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
+// need_t: the backward's transposed copy is needed (which a 1x32 inference
+// weight does not have); an MXFP8 context's forward also takes 1x32 weights.
 bool weight_ok(const moe_weight* w, moe_precision prec, int E, int N, int K, bool need_t) {
-  if (!w || w->precision != prec || w->E != E || w->N != N || w->K != K) return false;
+  if (!w || w->E != E || w->N != N || w->K != K) return false;
+  const bool row32 = prec == MOE_MXFP8 && !need_t && w->precision == MOE_MXFP8_1X32;
+  if (w->precision != prec && !row32) return false;
   if (!w->data || !aligned16(w->data)) return false;
   if (prec == MOE_MXFP8 && (!w->scale || !aligned16(w->scale))) return false;
   if (need_t) {
@@ -374,6 +380,7 @@ moe_status moe_ctx_create(const moe_config* cfg, moe_ctx** out) {
     c->buf_bytes[i] = L.size[i];
   }
   c->err = reinterpret_cast<uint32_t*>(c->buf[MOE_BUF_ERROR]);
+  c->clip = reinterpret_cast<unsigned long long*>(B(c, MOE_BUF_ERROR) + 16);
   *out = c;
   return MOE_OK;
 }
@@ -427,6 +434,15 @@ moe_status moe_ctx_get_error(moe_ctx* ctx, uint32_t* bits) {
   return MOE_OK;
 }
 
+moe_status moe_ctx_clip_stats(moe_ctx* ctx, uint64_t* counts) {
+  if (!ctx || !counts) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(cudaDeviceSynchronize());
+  MOE_TRY(cudaMemcpy(counts, ctx->clip, 2 * sizeof(uint64_t), cudaMemcpyDeviceToHost));
+  MOE_TRY(cudaMemset(ctx->clip, 0, 2 * sizeof(uint64_t)));
+  MOE_TRY(cudaDeviceSynchronize());
+  return MOE_OK;
+}
+
 moe_status moe_debug_copy_to_host(void* host_dst, const void* dev_src, size_t bytes) {
   if (!host_dst || !dev_src) return MOE_ERR_INVALID_ARG;
   MOE_TRY(cudaDeviceSynchronize());
@@ -438,6 +454,10 @@ moe_status prepare_block_scaled_weight(const void* w, int32_t E, int32_t N, int3
                                        void* data, uint8_t* scale, void* data_t, uint8_t* scale_t,
                                        cudaStream_t stream) {
   if (!w || !aligned16(w) || E < 1 || N < 32 || K < 32 || N % 32 || K % 32) return MOE_ERR_INVALID_ARG;
+  if (precision == MOE_MXFP8_1X32) {
+    if (N % 128 || K % 128 || !data || !scale || !aligned16(data) || data_t || scale_t) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_prep_mx_weight_row32(w, E, N, K, static_cast<uint8_t*>(data), scale, stream));
+  }
   if (precision == MOE_MXFP8) {
     if (N % 128 || K % 128 || !data || !scale || !aligned16(data)) return MOE_ERR_INVALID_ARG;
     if ((data_t == nullptr) != (scale_t == nullptr)) return MOE_ERR_INVALID_ARG;
@@ -537,6 +557,8 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   p1.F = F;
   p1.save_h1 = train ? 1 : 0;
   p1.want_col = train ? 1 : 0;
+  p1.swiglu_limit = c.swiglu_limit;
+  p1.clip = c.swiglu_limit > 0.0f ? ctx->clip : nullptr;
   p1.err = ctx->err;
   g1.max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
   MOE_TRY(launch_gemm(g1, sms, stream));
@@ -653,6 +675,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p1.out1_sf = B(ctx, MOE_BUF_DH1COL_SCALE);
   p1.b_cap = static_cast<int>(ctx->b_cap);
   p1.F = F;
+  p1.swiglu_limit = c.swiglu_limit;
   p1.err = ctx->err;
   g1.max_tiles = static_cast<int>(ctx->b_cap * p1.n_tiles);
   MOE_TRY(launch_gemm(g1, sms, stream));

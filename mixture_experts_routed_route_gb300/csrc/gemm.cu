@@ -258,7 +258,11 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, ui
 // operand) and, for training, the h2 column bundle (W2 WGRAD's operand).
 // Both chunks are read from TMEM first, as BF16 (g, u) pairs (the stored
 // h1 and the SwiGLU's inputs), and the accumulator handed back before any
-// store.
+// store.  With a limit L > 0 (clamped SwiGLU, "Meta Dist-MoE: Open-Source
+// Fused MoE Kernels for Blackwell", "Supported modes") g is clamped to <= L
+// and u to [-L, L] first; the warp counts the values it clamps (clip
+// statistics) and adds them to p.clip once per chunk.  h1 keeps the
+// unclamped values, which the backward needs for its masks.
 template <bool MX>
 __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow,
                                                int lane, int h, uint64_t* tempty) {
@@ -282,6 +286,8 @@ __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& 
     const int c0 = 32 * h + 64 * ci;
     if (c0 >= t.b_rows) continue;
     float hv[32];
+    const float L = p.swiglu_limit;
+    int cg = 0, cu = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const long long row = t.out_row0 + c0 + i;
@@ -290,7 +296,25 @@ __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& 
         p.h1[row * p.h1_pitch + f] = __ushort_as_bfloat16(static_cast<unsigned short>(w & 0xFFFFu));
         p.h1[row * p.h1_pitch + p.F + f] = __ushort_as_bfloat16(static_cast<unsigned short>(w >> 16));
       }
-      hv[i] = silu_f(bf16_lo(w)) * bf16_hi(w);
+      float g = bf16_lo(w), u = bf16_hi(w);
+      if (L > 0.0f) {
+        cg += g > L;
+        cu += fabsf(u) > L;
+        g = fminf(g, L);
+        u = fminf(fmaxf(u, -L), L);
+      }
+      hv[i] = silu_f(g) * u;
+    }
+    if (L > 0.0f && p.clip != nullptr) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        cg += __shfl_xor_sync(0xFFFFFFFFu, cg, o);
+        cu += __shfl_xor_sync(0xFFFFFFFFu, cu, o);
+      }
+      if (lane == 0) {
+        if (cg) atomicAdd(&p.clip[0], static_cast<unsigned long long>(cg));
+        if (cu) atomicAdd(&p.clip[1], static_cast<unsigned long long>(cu));
+      }
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i)
@@ -302,6 +326,8 @@ __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& 
 // Fused SwiGLU backward: dh2 from the accumulator (W2 DGRAD), g and u from
 // the saved BF16 h1, dg = dh2 u SiLU'(g), du = dh2 SiLU(g), written as the
 // dh1 row bundle (W13 DGRAD's operand) and column bundle (W13 WGRAD's).
+// With a clamp limit L, g and u are clamped first and dg (du) is zero where
+// g > L (|u| > L).
 // h1 does not depend on the MMA, so the caller issues the loads of the
 // warp's first chunk before it waits for the accumulator.
 __device__ __forceinline__ void load_h1_chunk(const GemmParams& p, const Tile& t, int f, int c0,
@@ -328,14 +354,22 @@ __device__ __forceinline__ void epi_swiglu_bwd(const GemmParams& p, const Tile& 
     tmem_ld32(tbase + c0, v);
     tmem_ld_wait();
     float dg[32], du[32];
+    const float L = p.swiglu_limit;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float g = bf16_lo(hp[i]);
-      const float u = bf16_hi(hp[i]);
+      float g = bf16_lo(hp[i]);
+      float u = bf16_hi(hp[i]);
       const float dh2 = u2f(v[i]);
+      float mg = 1.0f, mu = 1.0f;   // clamped SwiGLU: gradient only inside the clamp range
+      if (L > 0.0f) {
+        mg = g <= L ? 1.0f : 0.0f;
+        mu = fabsf(u) <= L ? 1.0f : 0.0f;
+        g = fminf(g, L);
+        u = fminf(fmaxf(u, -L), L);
+      }
       const float s = sigmoid_f(g);
-      dg[i] = dh2 * u * (s * (1.0f + g * (1.0f - s)));
-      du[i] = dh2 * (g * s);
+      dg[i] = dh2 * u * (s * (1.0f + g * (1.0f - s))) * mg;
+      du[i] = dh2 * (g * s) * mu;
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i) {

@@ -62,6 +62,10 @@ cudaError_t launch_score_grad(const void* h3, const void* dY, int D, int K, cons
 
 cudaError_t launch_prep_mx_weight(const void* w, int E, int N, int K, uint8_t* q, uint8_t* sf, uint8_t* qT,
                                   uint8_t* sfT, cudaStream_t stream);
+// 1x32 blocks along K (inference weights): codes [E,N,K] and scale atoms
+// [E*N/128][K/128], no transposed copy.
+cudaError_t launch_prep_mx_weight_row32(const void* w, int E, int N, int K, uint8_t* q, uint8_t* sf,
+                                        cudaStream_t stream);
 cudaError_t launch_transpose_bf16(const void* w, int E, int N, int K, void* wT, cudaStream_t stream);
 
 // ------------------------------------------------------------- grouped GEMM
@@ -112,6 +116,8 @@ struct GemmParams {
   // apart, a 3D [halves][F][K] box) and aux[2] their two scale atoms (1:
   // adjacent tiles, 3D atom view; 2: halves, 4D atom view)
   int a_pair_box;
+  float swiglu_limit;     // SwiGLU epilogues: clamp g <= L and |u| <= L when L > 0
+  unsigned long long* clip;  // SwiGLU forward with a limit: [2] counts of clamped g, u (or null)
   int b_full_box;         // grouped-M: aux[1] loads a full 128-row block in one box
   uint32_t* err;
 };

@@ -93,7 +93,8 @@ bool operand_map(CUtensorMap* tm, const void* base, bool mx, int64_t rows, int64
 bool is16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 bool weight_matches(const moe_weight* w, moe_precision prec, int E, int N, int K) {
-  return w && w->precision == prec && w->E == E && w->N == N && w->K == K && w->data && is16(w->data) &&
+  const bool prec_ok = w && (w->precision == prec || (prec == MOE_MXFP8 && w->precision == MOE_MXFP8_1X32));
+  return prec_ok && w->E == E && w->N == N && w->K == K && w->data && is16(w->data) &&
          (prec != MOE_MXFP8 || (w->scale && is16(w->scale)));
 }
 
@@ -148,6 +149,7 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   const int D = cfg->d_model, F = cfg->d_ff, E = cfg->num_experts, K = cfg->top_k;
   if (K < 1 || K > 32 || E < 1 || E > 1024 || D < 128 || F < 128) return MOE_ERR_INVALID_ARG;
   if (cfg->precision != MOE_BF16 && cfg->precision != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (!(cfg->swiglu_limit >= 0.0f) || cfg->swiglu_limit > 3.0e38f) return MOE_ERR_INVALID_ARG;
   if (D % 128 || F % 128) return MOE_ERR_UNSUPPORTED;
   if (call_flags & ~MOE_ACCUMULATE_OUT) return MOE_ERR_INVALID_ARG;
   const bool mx = cfg->precision == MOE_MXFP8;
@@ -218,6 +220,7 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   g1.p.out0_sf_kg = F / 128;
   g1.p.b_cap = static_cast<int>(L.b_cap);
   g1.p.F = F;
+  g1.p.swiglu_limit = cfg->swiglu_limit;   // clamped SwiGLU (no clip counters here)
   g1.p.err = err;
   g1.max_tiles = static_cast<int>(L.b_cap * (F / 128));
   if (launch_gemm(g1, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;

@@ -100,6 +100,49 @@ __global__ void __launch_bounds__(256) prep_mx_kernel(const __nv_bfloat16* __res
   }
 }
 
+// 1x32 blocks (inference weights, "Meta Dist-MoE: Open-Source Fused MoE
+// Kernels for Blackwell", "Supported modes"): thread b quantises block b of
+// the flattened [rows, K/32] grid, 32 consecutive values of one row along K,
+// with its own scale (same OCP rule), into the same codes / atom layout the
+// 32x32 preparation writes.
+__global__ void __launch_bounds__(256) prep_mx_row32_kernel(const __nv_bfloat16* __restrict__ w, long long rows,
+                                                            int K, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  const int kbs = K / 32;
+  const long long nb = rows * kbs;
+  for (long long b = blockIdx.x * 256LL + threadIdx.x; b < nb; b += static_cast<long long>(gridDim.x) * 256) {
+    const long long row = b / kbs;
+    const int kb = static_cast<int>(b - row * kbs);
+    const uint4* src = reinterpret_cast<const uint4*>(w + row * K + kb * 32);
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 u = __ldg(src + j);
+      v[8 * j + 0] = bf16_lo(u.x);
+      v[8 * j + 1] = bf16_hi(u.x);
+      v[8 * j + 2] = bf16_lo(u.y);
+      v[8 * j + 3] = bf16_hi(u.y);
+      v[8 * j + 4] = bf16_lo(u.z);
+      v[8 * j + 5] = bf16_hi(u.z);
+      v[8 * j + 6] = bf16_lo(u.w);
+      v[8 * j + 7] = bf16_hi(u.w);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int ex = mx_shared_exp(amax);
+    const float inv = exp2_int(-ex);
+    uint32_t c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      c[i] = cvt_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) | (cvt_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+    uint4* dst = reinterpret_cast<uint4*>(q + row * K + kb * 32);
+    dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+    dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+    sf[((row >> 7) * (K / 128) + (kb >> 2)) * 512 + sf_atom_byte(static_cast<int>(row & 127), kb & 3)] =
+        static_cast<uint8_t>(ex + 127);
+  }
+}
+
 // BF16 [E,N,K] -> [E,K,N] through 32x32 shared-memory tiles.
 __global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ w, int N, int K,
                                                              __nv_bfloat16* __restrict__ wT) {
@@ -121,6 +164,15 @@ cudaError_t launch_prep_mx_weight(const void* w, int E, int N, int K, uint8_t* q
   const int slabs = (K + 255) / 256;
   dim3 grid((N / 32) * slabs, E);
   prep_mx_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(w), N, K, q, sf, qT, sfT);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_mx_weight_row32(const void* w, int E, int N, int K, uint8_t* q, uint8_t* sf,
+                                        cudaStream_t stream) {
+  const long long rows = static_cast<long long>(E) * N;
+  const long long blocks = (rows * (K / 32) + 255) / 256;
+  const int grid = static_cast<int>(blocks < 65535 * 16 ? blocks : 65535 * 16);
+  prep_mx_row32_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(w), rows, K, q, sf);
   return cudaGetLastError();
 }
 

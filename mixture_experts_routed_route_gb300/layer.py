@@ -11,7 +11,7 @@ import torch
 
 from . import abi
 
-_DT = {"bf16": abi.MOE_BF16, "mxfp8": abi.MOE_MXFP8}
+_DT = {"bf16": abi.MOE_BF16, "mxfp8": abi.MOE_MXFP8, "mxfp8_1x32": abi.MOE_MXFP8_1X32}
 
 
 def precision_code(precision):
@@ -23,7 +23,8 @@ class PreparedWeight:
 
     BF16: ``data`` is the caller's tensor, ``data_t`` its transpose
     [E, K, N] (for the input-gradient GEMMs).  MXFP8: E4M3 codes with one
-    E8M0 scale per 32x32 tile, in both orientations."""
+    E8M0 scale per 32x32 tile, in both orientations.  "mxfp8_1x32": forward
+    only, one scale per 1x32 block of a row along K."""
 
     def __init__(self, w, precision, with_transpose=True, stream=None):
         assert w.dtype == torch.bfloat16 and w.is_cuda and w.dim() == 3
@@ -33,7 +34,11 @@ class PreparedWeight:
         self.shape = (E, N, K)
         dev = w.device
         self.data_t = self.scale = self.scale_t = None
-        if self.precision == abi.MOE_MXFP8:
+        if self.precision == abi.MOE_MXFP8_1X32:
+            self.data = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
+            self.scale = torch.empty(E * N * (K // 32) + 16, dtype=torch.uint8, device=dev)
+            abi.prepare_block_scaled_weight(w, E, N, K, self.precision, self.data, self.scale, None, None, stream)
+        elif self.precision == abi.MOE_MXFP8:
             self.data = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
             self.scale = torch.empty(E * N * (K // 32) + 16, dtype=torch.uint8, device=dev)
             if with_transpose:
@@ -54,9 +59,10 @@ class MoELayer:
     """One routed MoE layer bound to a context (fixed scratch)."""
 
     def __init__(self, max_tokens, d_model, d_ff, num_experts, top_k, precision, training=False, debug=False,
-                 device="cuda"):
+                 device="cuda", swiglu_limit=0.0):
         flags = (abi.MOE_TRAINING if training else 0) | (abi.MOE_DEBUG_CHECKS if debug else 0)
-        self.cfg = abi.make_config(max_tokens, d_model, d_ff, num_experts, top_k, precision_code(precision), flags)
+        self.cfg = abi.make_config(max_tokens, d_model, d_ff, num_experts, top_k, precision_code(precision), flags,
+                                   swiglu_limit)
         self.device = torch.device(device)
         self.D, self.F, self.E, self.K = d_model, d_ff, num_experts, top_k
         self.training = training
@@ -96,6 +102,9 @@ class MoELayer:
 
     def error_bits(self):
         return abi.moe_ctx_get_error(self.ctx)
+
+    def clip_stats(self):
+        return abi.moe_ctx_clip_stats(self.ctx)
 
     # ----------------------------------------------------------- compute
     def forward(self, x, ids, scores, W13, W2, out=None, saved=None, accumulate=False, stream=None):

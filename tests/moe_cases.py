@@ -50,18 +50,20 @@ class Case:
 
 
 def run_gpu(case, precision=None, training=True, debug=False, out_init=None, max_tokens=None,
-            dx_init=None, dw_fp32=False, backward=True):
+            dx_init=None, dw_fp32=False, backward=True, swiglu_limit=0.0, weight_prec=None):
     """Forward (and backward) of a case through the C ABI; returns a dict of
-    host arrays plus the layer object for further inspection."""
+    host arrays plus the layer object for further inspection.  weight_prec
+    overrides the weights' preparation (e.g. "mxfp8_1x32")."""
     from mixture_experts_routed_route_gb300.layer import MoELayer, PreparedWeight
 
     w = case.w
     precision = precision or w.precision
     dev = torch.device("cuda")
     T = case.T
-    layer = MoELayer(max_tokens or max(T, 1), w.D, w.F, w.E, w.K, precision, training=training, debug=debug)
-    W13 = PreparedWeight(case.w13.to(dev), precision, with_transpose=training)
-    W2 = PreparedWeight(case.w2.to(dev), precision, with_transpose=training)
+    layer = MoELayer(max_tokens or max(T, 1), w.D, w.F, w.E, w.K, precision, training=training, debug=debug,
+                     swiglu_limit=swiglu_limit)
+    W13 = PreparedWeight(case.w13.to(dev), weight_prec or precision, with_transpose=training)
+    W2 = PreparedWeight(case.w2.to(dev), weight_prec or precision, with_transpose=training)
     x = case.x.to(dev)
     ids = torch.from_numpy(case.ids).to(dev)
     sc = torch.from_numpy(case.scores).to(dev)
@@ -86,11 +88,13 @@ def run_gpu(case, precision=None, training=True, debug=False, out_init=None, max
     return res
 
 
-def run_oracle(case, precision=None, out_init=None, dx_init=None, dw_fp32=False, backward=True):
+def run_oracle(case, precision=None, out_init=None, dx_init=None, dw_fp32=False, backward=True, swiglu_limit=0.0,
+               weight_blocks="32x32"):
     from oracle import moe
     precision = precision or case.w.precision
     x, ids, s, w13, w2 = case.oracle_inputs()
-    st = moe.forward(x, ids, s, w13, w2, precision, out_init=out_init)
+    st = moe.forward(x, ids, s, w13, w2, precision, out_init=out_init, swiglu_limit=swiglu_limit,
+                     weight_blocks=weight_blocks)
     res = {"state": st, "out": st["out"]}
     if backward:
         g = moe.backward(st, to_f64(case.dy), w13, w2, dx_init=dx_init, dw_fp32=dw_fp32)
@@ -161,9 +165,10 @@ def check_mx_wgrad(dW13_gpu, dW2_gpu, state, grads, experts=None, tol=TOL["mxfp8
         g, ga = _bf16_candidates(h1x[:, :F], EPS_ACC)
         u, ua = _bf16_candidates(h1x[:, F:], EPS_ACC)
         dh2 = grads["dh2"][a:b]
+        lim = state.get("swiglu_limit", 0.0)
         combos = [(g, u), (ga, u), (g, ua), (ga, ua)]
-        dh1_c = [np.concatenate([dh2 * uu * omoe.silu_grad(gg), dh2 * omoe.silu(gg)], axis=1) for gg, uu in combos]
-        h2_c = [omoe.silu(gg) * uu for gg, uu in combos]
+        dh1_c = [np.concatenate(omoe.swiglu_grad(gg, uu, dh2, lim), axis=1) for gg, uu in combos]
+        h2_c = [omoe.swiglu(gg, uu, lim) for gg, uu in combos]
         s13 = _mx_col_spread(dh1_c, EPS_ACC)
         s2 = _mx_col_spread(h2_c, EPS_ACC)
         assert (s13 > 0).mean() <= max_undecided and (s2 > 0).mean() <= max_undecided

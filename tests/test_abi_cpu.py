@@ -52,7 +52,7 @@ def test_binding_covers_every_declared_symbol(lib):
 
 def test_struct_layouts_match_header():
     from mixture_experts_routed_route_gb300 import abi
-    assert ctypes.sizeof(abi.moe_config) == 7 * 4
+    assert ctypes.sizeof(abi.moe_config) == 8 * 4
     assert ctypes.sizeof(abi.moe_weight) == 16 + 4 * 8
     assert abi.moe_weight.data.offset == 16
 
@@ -80,6 +80,10 @@ def test_host_side_sizes_without_gpu(lib):
     with pytest.raises(abi.MoEError) as ei:
         abi.moe_ctx_create(bad)
     assert ei.value.status == abi.MOE_ERR_INVALID_ARG
+    # the clamp limit must be finite and non-negative
+    for lim in (float("nan"), -1.0, float("inf")):
+        assert abi.moe_row_capacity(abi.make_config(2048, 7168, 2048, 384, 6, abi.MOE_MXFP8, 0, lim)) == 0
+    assert abi.moe_row_capacity(abi.make_config(2048, 7168, 2048, 384, 6, abi.MOE_MXFP8, 0, 7.0)) == r
     odd = abi.make_config(64, 200, 256, 8, 2, abi.MOE_BF16, 0)
     with pytest.raises(abi.MoEError) as ei:
         abi.moe_ctx_create(odd)
