@@ -324,10 +324,10 @@ __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u 
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  return v;
+// Maximum over the warp of non-negative finite values: such floats order
+// like their bit patterns, so one integer reduction (redux.sync) does it.
+__device__ __forceinline__ float warp_max_nonneg(float v) {
+  return __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(v)));
 }
 
 // SiLU(z) = z / (1 + e^-z) and its derivative s (1 + z (1 - s)).

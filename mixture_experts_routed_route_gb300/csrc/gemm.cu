@@ -155,7 +155,7 @@ __device__ __forceinline__ void store_row_val(const GemmParams& p, void* out, lo
   if (!MX) {
     static_cast<__nv_bfloat16*>(out)[row * pitch + col] = __float2bfloat16_rn(v);
   } else {
-    const float amax = warp_max(fabsf(v));
+    const float amax = warp_max_nonneg(fabsf(v));
     const int e = mx_shared_exp(amax);
     const uint32_t code = cvt_e4m3x2(v * exp2_int(-e), 0.0f) & 0xFFu;
     static_cast<uint8_t*>(out)[row * pitch + col] = static_cast<uint8_t>(code);
@@ -306,11 +306,8 @@ __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& 
       hv[i] = silu_f(g) * u;
     }
     if (L > 0.0f && p.clip != nullptr) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        cg += __shfl_xor_sync(0xFFFFFFFFu, cg, o);
-        cu += __shfl_xor_sync(0xFFFFFFFFu, cu, o);
-      }
+      cg = __reduce_add_sync(0xFFFFFFFFu, cg);
+      cu = __reduce_add_sync(0xFFFFFFFFu, cu);
       if (lane == 0) {
         if (cg) atomicAdd(&p.clip[0], static_cast<unsigned long long>(cg));
         if (cu) atomicAdd(&p.clip[1], static_cast<unsigned long long>(cu));

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(256) prep_mx_kernel(const __nv_bfloat16* __res
     float amax = 0.0f;
 #pragma unroll
     for (int r = 0; r < 32; ++r) amax = fmaxf(amax, fabsf(tile[r][col]));
-    amax = warp_max(amax);
+    amax = warp_max_nonneg(amax);
     const int ex = mx_shared_exp(amax);
     const float inv = exp2_int(-ex);
     const uint8_t sbyte = static_cast<uint8_t>(ex + 127);
