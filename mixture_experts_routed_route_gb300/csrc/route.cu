@@ -25,6 +25,9 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+// Routes per lane held in registers for both passes (read once, with all
+// loads in flight together): up to kWarps * 32 * kHold = 16384 routes.
+constexpr int kHold = 16;
 
 // Exclusive block-wide scan of three ints per thread (one thread per slot).
 __device__ void block_scan3(int a, int b, int c, int& ea, int& eb, int& ec, int& ta, int& tb, int& tc,
@@ -103,22 +106,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- pass 1: per-warp histograms (and validation of the IDs)
   int* myh = hist + warp * E;
   unsigned my_err = 0;
-  for (int base = beg; base < end; base += 32) {
-    const int i = base + lane;
-    int e = -1;
-    if (i < end) {
-      const int id = ids[i];
-      if (id >= 0 && id < E) {
-        e = id;
-      } else if (id != -1) {
-        my_err |= kErrBadId;
-      } else if (debug && scores[i] != 0.0f) {
-        my_err |= kErrInactiveScore;
-      }
+  const bool held = seg <= 32 * kHold;
+  int idr[kHold];
+  if (held) {
+#pragma unroll
+    for (int j = 0; j < kHold; ++j) {
+      const int i = beg + 32 * j + lane;
+      idr[j] = i < end ? ids[i] : -1;
     }
+  }
+  // expert of route i with id `id` (-1: inactive), flagging bad IDs
+  auto classify = [&](int i, int id) {
+    if (id >= 0 && id < E) return id;
+    if (id != -1) my_err |= kErrBadId;
+    else if (debug && scores[i] != 0.0f) my_err |= kErrInactiveScore;
+    return -1;
+  };
+  auto count = [&](int e) {
     const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
     if (e >= 0 && lane == __ffs(grp) - 1) myh[e] += __popc(grp);
     __syncwarp();
+  };
+  if (held) {
+#pragma unroll
+    for (int j = 0; j < kHold; ++j) {
+      if (beg + 32 * j < end) {
+        const int i = beg + 32 * j + lane;
+        count(i < end ? classify(i, idr[j]) : -1);
+      }
+    }
+  } else {
+    for (int base = beg; base < end; base += 32) {
+      const int i = base + lane;
+      count(i < end ? classify(i, ids[i]) : -1);
+    }
   }
   if (my_err) atomicOr(&s_err, my_err);
   __syncthreads();
@@ -166,13 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 
   // ---- pass 3: stable scatter of each route to its row
-  for (int base = beg; base < end; base += 32) {
-    const int i = base + lane;
-    int e = -1;
-    if (i < end) {
-      const int id = ids[i];
-      if (id >= 0 && id < E) e = id;
-    }
+  auto scatter = [&](int i, int id) {
+    const int e = (i < end && id >= 0 && id < E) ? id : -1;
     const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
     const unsigned lower = grp & ((1u << lane) - 1u);
     if (e >= 0) {
@@ -187,6 +203,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (e >= 0 && lane == __ffs(grp) - 1) myh[e] += __popc(grp);
     __syncwarp();
+  };
+  if (held) {
+#pragma unroll
+    for (int j = 0; j < kHold; ++j)
+      if (beg + 32 * j < end) scatter(beg + 32 * j + lane, idr[j]);
+  } else {
+    for (int base = beg; base < end; base += 32) {
+      const int i = base + lane;
+      scatter(i, i < end ? ids[i] : -1);
+    }
   }
 
   // ---- pass 4: pad rows and the unused tail of the row capacity
