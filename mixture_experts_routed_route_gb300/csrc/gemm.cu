@@ -21,24 +21,27 @@
 //    colA[m, r] colB[n, r]; both operands are column bundles stored
 //    [features, rows], so the contraction runs over the expert's row range.
 //
-// MXFP8 scales travel with the operand tiles: the TMA producer bulk-copies
-// one 512-byte scale atom per operand per stage into the stage's shared
-// memory, and the MMA thread moves it to tensor memory with tcgen05.cp ahead
-// of the block-scaled MMAs (same thread, so the tensor pipe keeps the order).
+// MXFP8 scales travel with the operand tiles: the TMA producer copies one
+// 512-byte scale atom per operand per stage into the stage's shared memory,
+// a scale warp moves them to tensor memory with tcgen05.cp and commits them
+// to the stage's sf_full barrier, and the MMA thread, which waits on that
+// barrier, issues the block-scaled MMAs.
 //
 // Epilogues: fused SwiGLU forward (h1 -> h2 row/column bundles), plain BF16
 // store (h3, input-gradient rows), fused SwiGLU backward (dh2 -> dh1 row and
 // column bundles) and weight-gradient store (BF16 through shared memory and
 // TMA; FP32 or accumulate with plain stores).
 //
-// Warp roles (one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer (one thread)
-//   warp 1      TMEM allocator and MMA issuer (one thread)
+// Warp roles (one CTA per SM, persistent over tiles; warps 0, 1 and the
+// scale warp run their loops converged and lane 0 issues):
+//   warp 0      TMA producer
+//   warp 1      TMEM allocator and MMA issuer
 //   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and the
 //               32-column chunks 32h and 32h + 64 (h = (w-2)/4) of the
 //               accumulator
 //   warps 10..17  weight gradient only: a second epilogue group of 8 warps;
 //               the two groups take alternate tiles
+//   last warp   MXFP8 only: scale-atom copier (tcgen05.cp)
 #include "kernels.cuh"
 
 namespace moe {
