@@ -234,6 +234,8 @@ class Step:
                                 accumulate_dx=acc)
 
     def capture(self):
+        """Two graphs of the same step: the timed one, and one that also
+        records the library's per-stage events (kept out of the timed one)."""
         import torch
         from mixture_experts_routed_route_gb300 import abi
         before = sum(abi.moe_ctx_launch_count(l.ctx) for l in self.layers())
@@ -241,6 +243,13 @@ class Step:
         with torch.cuda.graph(self.graph):
             self.enqueue()
         self.launches_per_step = sum(abi.moe_ctx_launch_count(l.ctx) for l in self.layers()) - before
+        for l in self.layers():
+            abi.moe_ctx_enable_stage_timing(l.ctx, True)
+        self.stage_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.stage_graph):
+            self.enqueue()
+        for l in self.layers():
+            abi.moe_ctx_enable_stage_timing(l.ctx, False)
 
     def rows_used(self):
         from mixture_experts_routed_route_gb300 import abi
@@ -312,8 +321,6 @@ def run_ours(args, rank, world):
     st.w13_bf16 = st.w2_bf16 = None
     torch.cuda.empty_cache()
 
-    for l in st.layers():
-        abi.moe_ctx_enable_stage_timing(l.ctx, True)
     st.capture()
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -347,7 +354,7 @@ def run_ours(args, rank, world):
     fwd_t = {n: [] for n in abi.FWD_STAGE_NAMES}
     bwd_t = {n: [] for n in abi.BWD_STAGE_NAMES}
     for _ in range(max(3, min(args.steps, 10))):
-        st.graph.replay()
+        st.stage_graph.replay()
         torch.cuda.synchronize(dev)
         for n, v in zip(abi.FWD_STAGE_NAMES, abi.moe_ctx_stage_times(st.layer.ctx, 0)):
             fwd_t[n].append(v)

@@ -334,7 +334,10 @@ MOE_API moe_status moe_ctx_buffer(moe_ctx* ctx, int which, void** dev_ptr, size_
  *   backward (MOE_BWD_STAGES): gather dh3 (row and column bundles), W2 DGRAD
  *            + SwiGLU backward GEMM, W2 WGRAD GEMM, W13 DGRAD GEMM, W13 WGRAD
  *            GEMM, dX reduction
- * Enabling creates the events (call it outside capture, after create).
+ * The first enable creates the events (call it outside capture); they live
+ * until moe_ctx_destroy, so disabling only stops later calls from recording
+ * and a graph captured with timing on can still be replayed and read.
+ * Destroy the context only after the last replay of such a graph.
  */
 #define MOE_FWD_STAGES 5
 #define MOE_BWD_STAGES 6

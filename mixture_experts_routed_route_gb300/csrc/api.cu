@@ -29,7 +29,8 @@ struct moe_ctx {
   size_t buf_bytes[MOE_BUF_NUM];
   uint32_t* err;
   unsigned long long* clip;   // [2] clamped gate / up counts (clip statistics)
-  bool timing;
+  bool timing;          // calls record the stage events
+  bool events;          // the stage events exist (created once, destroyed with the context)
   cudaEvent_t ev[2][8];
   uint64_t launches;
 };
@@ -387,20 +388,19 @@ moe_status moe_ctx_create(const moe_config* cfg, moe_ctx** out) {
 
 moe_status moe_ctx_enable_stage_timing(moe_ctx* ctx, int enable) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
-  if (enable && !ctx->timing) {
+  if (enable && !ctx->events) {
     for (int p = 0; p < 2; ++p)
       for (int i = 0; i < 8; ++i) MOE_TRY(cudaEventCreate(&ctx->ev[p][i]));
-    ctx->timing = true;
-  } else if (!enable && ctx->timing) {
-    for (int p = 0; p < 2; ++p)
-      for (int i = 0; i < 8; ++i) cudaEventDestroy(ctx->ev[p][i]);
-    ctx->timing = false;
+    ctx->events = true;
   }
+  // disabling only stops the recording: a graph captured with timing on
+  // still records into these events, so they live until moe_ctx_destroy
+  ctx->timing = enable != 0;
   return MOE_OK;
 }
 
 moe_status moe_ctx_stage_times(moe_ctx* ctx, int pass, float* ms, int n) {
-  if (!ctx || !ms || pass < 0 || pass > 1 || !ctx->timing) return MOE_ERR_INVALID_ARG;
+  if (!ctx || !ms || pass < 0 || pass > 1 || !ctx->events) return MOE_ERR_INVALID_ARG;
   const int stages = pass == 0 ? MOE_FWD_STAGES : MOE_BWD_STAGES;
   if (n < stages) return MOE_ERR_INVALID_ARG;
   MOE_TRY(cudaEventSynchronize(ctx->ev[pass][stages]));
@@ -412,7 +412,10 @@ uint64_t moe_ctx_launch_count(const moe_ctx* ctx) { return ctx ? ctx->launches :
 
 moe_status moe_ctx_destroy(moe_ctx* ctx) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
-  moe_ctx_enable_stage_timing(ctx, 0);
+  if (ctx->events) {
+    for (int p = 0; p < 2; ++p)
+      for (int i = 0; i < 8; ++i) cudaEventDestroy(ctx->ev[p][i]);
+  }
   const cudaError_t e = cudaFree(ctx->base);
   delete ctx;
   return cuda_status(e);
