@@ -145,3 +145,35 @@ def test_zero_tokens_is_a_no_op():
         abi.moe_forward(layer.ctx, 17, x, ids, sc, W13.struct, W2.struct, out)
     assert ei.value.status == abi.MOE_ERR_CAPACITY
     assert layer.error_bits() == 0
+
+
+def test_stage_timing_graph_survives_disable():
+    """A graph captured with stage timing on keeps recording into the
+    context's events after timing is disabled (they live until the context
+    is destroyed), so it can be replayed and its stage times read."""
+    from mixture_experts_routed_route_gb300 import abi
+    from mixture_experts_routed_route_gb300.layer import MoELayer, PreparedWeight
+    w = synth.WORKLOADS["tiny_bf16"]
+    case = Case(w)
+    dev = torch.device("cuda")
+    layer = MoELayer(w.T, w.D, w.F, w.E, w.K, "bf16")
+    W13 = PreparedWeight(case.w13.to(dev), "bf16", with_transpose=False)
+    W2 = PreparedWeight(case.w2.to(dev), "bf16", with_transpose=False)
+    x = case.x.to(dev)
+    ids = torch.from_numpy(case.ids).to(dev)
+    sc = torch.from_numpy(case.scores).to(dev)
+    out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
+    layer.forward(x, ids, sc, W13, W2, out=out)        # eager once (kernel attributes)
+    torch.cuda.synchronize()
+    abi.moe_ctx_enable_stage_timing(layer.ctx, True)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(x, ids, sc, W13, W2, out=out)
+    abi.moe_ctx_enable_stage_timing(layer.ctx, False)
+    for _ in range(2):
+        graph.replay()
+        torch.cuda.synchronize()
+        times = abi.moe_ctx_stage_times(layer.ctx, 0)
+        assert len(times) == abi.MOE_FWD_STAGES and all(t >= 0 for t in times)
+    del graph
+    layer.close()
