@@ -467,7 +467,9 @@ struct Cfg {
   static constexpr int STAGE = ((NA * kABytes + kBBytes + SF_BYTES) + 1023) / 1024 * 1024;
   static constexpr int S = WGRAD ? 4 : ((NA == 2) ? 4 : 6);  // pipeline stages
   static constexpr int STAGING = WGRAD ? 2 * 32768 : 0;    // weight-gradient store buffers
-  static constexpr int ACC_BUFS = (NA == 1) ? 2 : 1;       // accumulator buffers
+  // accumulator buffers: two, except with two MXFP8 A tiles (2 x 256
+  // columns leave no room in TMEM's 512 for the stages' scale columns)
+  static constexpr int ACC_BUFS = (NA == 1 || !MX) ? 2 : 1;
   static constexpr int ACC_COLS = NA * 128;
   static constexpr int SF_COLS = (NA + 1) * 4;             // scale columns per stage
   static constexpr uint32_t SF_COL0 = ACC_BUFS * ACC_COLS;
