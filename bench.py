@@ -46,7 +46,9 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-sample-experts", type=int, default=3)
+    ap.add_argument("--cpu-sample-experts", type=int, default=3)        # reference arm: experts per step
+    ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)   # cpu_baseline: oracle work to time
+    ap.add_argument("--cpu-sample-max-experts", type=int, default=16)
     return ap.parse_args()
 
 
@@ -287,10 +289,32 @@ def blas_threads():
 
 
 def pick_sample_experts(w, ids, n):
+    """The first n routed experts of a fixed seeded order (prefixes nest)."""
     rng = np.random.default_rng(12345)
     present = sorted(set(int(e) for e in np.asarray(ids).reshape(-1) if e >= 0))
     order = [present[i] for i in rng.permutation(len(present))]
-    return sorted(order[:n])
+    return order[:n]
+
+
+def timed_cpu_sample(w, ids, scores, x, dy, w13s, w2s, experts, target_s):
+    """The oracle timed on a sample sized to about target_s seconds: one run on
+    the first two experts calibrates the cost of an expert (mostly fixed: its
+    weight preparation and full weight gradient), then the longest prefix of
+    `experts` predicted to fit is run and reported (or the calibration run
+    itself when nothing more fits).  An added expert is predicted to cost the
+    calibration average, scaled up if it has more routes than they had."""
+    n0 = min(2, len(experts))
+    t0, f0, r0 = cpu_sample(w, ids, scores, x, dy, w13s[:n0], w2s[:n0], experts[:n0])
+    per_expert, mean_routes = t0 / n0, max(r0 / n0, 1.0)
+    counts = [int(np.sum(np.asarray(ids) == e)) for e in experts]
+    n, pred = n0, t0
+    while n < len(experts) and pred + per_expert * max(1.0, counts[n] / mean_routes) <= target_s:
+        pred += per_expert * max(1.0, counts[n] / mean_routes)
+        n += 1
+    if n == n0:
+        return t0, f0, r0, n0
+    dt, fl, r = cpu_sample(w, ids, scores, x, dy, w13s[:n], w2s[:n], experts[:n])
+    return dt, fl, r, n
 
 
 def run_ours(args, rank, world):
@@ -316,7 +340,7 @@ def run_ours(args, rank, world):
     # oracle sample weights (host copies) before the BF16 masters are dropped
     sample = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        experts = pick_sample_experts(w, st.ids_np, args.cpu_sample_experts)
+        experts = pick_sample_experts(w, st.ids_np, args.cpu_sample_max_experts)
         sample = (experts, st.w13_bf16[experts].cpu(), st.w2_bf16[experts].cpu(), st.x.cpu(), st.dy.cpu())
     st.w13_bf16 = st.w2_bf16 = None
     torch.cuda.empty_cache()
@@ -429,10 +453,11 @@ def run_ours(args, rank, world):
     cpu = None
     if sample is not None:
         experts, s13, s2, xc, dyc = sample
-        dt, sflops, sroutes = cpu_sample(w, st.ids_np, st.scores_np, xc, dyc, s13, s2, experts)
+        dt, sflops, sroutes, n = timed_cpu_sample(w, st.ids_np, st.scores_np, xc, dyc, s13, s2, experts,
+                                                  args.cpu_sample_seconds)
         cpu = {"value": round(sflops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"fp64 numpy oracle, {'forward+backward' if w.train else 'forward'} of the {sroutes} "
-                         f"routes of {len(experts)} of {w.E} experts (all {w.T} tokens), {dt:.1f} s"}
+                         f"routes of {n} of {w.E} experts (all {w.T} tokens), {dt:.1f} s"}
 
     line = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
