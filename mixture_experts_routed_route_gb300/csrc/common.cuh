@@ -331,8 +331,11 @@ __device__ __forceinline__ float warp_max_nonneg(float v) {
   return __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(v)));
 }
 
-// SiLU(z) = z / (1 + e^-z) and its derivative s (1 + z (1 - s)).
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
-__device__ __forceinline__ float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
+// SiLU(z) = z / (1 + e^-z) and sigmoid, with the fast exponential and
+// division intrinsics (a few FP32 ulps; the results are rounded to BF16 or
+// MXFP8 next).  For very negative z, e^-z overflows to inf and the quotient
+// is 0, the limit.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+__device__ __forceinline__ float sigmoid_f(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 }  // namespace moe
