@@ -109,3 +109,23 @@ def test_accumulate_dx_and_fp32_dw():
     o = run_oracle(case, dx_init=to_f64(init), dw_fp32=True)
     for k in ("dx", "dW13", "dW2"):
         assert rel_err(g[k], o[k]) <= TOL["bf16"], k
+
+
+@pytest.mark.parametrize("precision", ["bf16", "mxfp8"])
+def test_all_routes_inactive(precision):
+    """Every route ID -1: no expert gets a row, every GEMM has zero tiles, and
+    out, dX, dW13, dW2 and the score gradient are exact zeros (the old out /
+    dX with the accumulate flags)."""
+    w = synth.Workload("all_inactive", 96, 256, 256, 8, 2, precision, "uniform", seed=51)
+    ids = np.full((96, 2), -1, np.int32)
+    scores = np.zeros((96, 2), np.float32)
+    case = Case(w, ids=ids, scores=scores)
+    g = run_gpu(case)
+    assert g["err_bits"] == 0
+    for k in ("out", "dx", "dW13", "dW2", "dp"):
+        assert np.all(g[k] == 0.0), k
+    o = run_oracle(case)
+    assert np.all(o["out"] == 0.0) and np.all(o["dx"] == 0.0)
+    init = torch.full((96, w.D), 0.5, dtype=torch.bfloat16)
+    ga = run_gpu(case, out_init=init.cuda(), dx_init=init.cuda())
+    assert np.all(ga["out"] == 0.5) and np.all(ga["dx"] == 0.5)
