@@ -297,24 +297,17 @@ def pick_sample_experts(w, ids, n):
 
 
 def timed_cpu_sample(w, ids, scores, x, dy, w13s, w2s, experts, target_s):
-    """The oracle timed on a sample sized to about target_s seconds: one run on
-    the first two experts calibrates the cost of an expert (mostly fixed: its
-    weight preparation and full weight gradient), then the longest prefix of
-    `experts` predicted to fit is run and reported (or the calibration run
-    itself when nothing more fits).  An added expert is predicted to cost the
-    calibration average, scaled up if it has more routes than they had."""
-    n0 = min(2, len(experts))
-    t0, f0, r0 = cpu_sample(w, ids, scores, x, dy, w13s[:n0], w2s[:n0], experts[:n0])
-    per_expert, mean_routes = t0 / n0, max(r0 / n0, 1.0)
-    counts = [int(np.sum(np.asarray(ids) == e)) for e in experts]
-    n, pred = n0, t0
-    while n < len(experts) and pred + per_expert * max(1.0, counts[n] / mean_routes) <= target_s:
-        pred += per_expert * max(1.0, counts[n] / mean_routes)
-        n += 1
-    if n == n0:
-        return t0, f0, r0, n0
-    dt, fl, r = cpu_sample(w, ids, scores, x, dy, w13s[:n], w2s[:n], experts[:n])
-    return dt, fl, r, n
+    """The oracle timed on a sample of about target_s seconds: the experts of
+    `experts` (a seeded order) are run one oracle call each, in that order,
+    until the calls' total time reaches target_s.  No cost prediction: an
+    expert's cost is mostly fixed (its weight preparation and full weight
+    gradient), so route counts say little about it.  Returns the totals of
+    time, useful FLOPs and routes, and the number of experts run."""
+    tot_t, tot_f, tot_r, n = 0.0, 0.0, 0, 0
+    while n < len(experts) and (n == 0 or tot_t < target_s):
+        dt, fl, r = cpu_sample(w, ids, scores, x, dy, w13s[n:n + 1], w2s[n:n + 1], experts[n:n + 1])
+        tot_t, tot_f, tot_r, n = tot_t + dt, tot_f + fl, tot_r + r, n + 1
+    return tot_t, tot_f, tot_r, n
 
 
 def run_ours(args, rank, world):
@@ -457,7 +450,7 @@ def run_ours(args, rank, world):
                                                   args.cpu_sample_seconds)
         cpu = {"value": round(sflops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"fp64 numpy oracle, {'forward+backward' if w.train else 'forward'} of the {sroutes} "
-                         f"routes of {n} of {w.E} experts (all {w.T} tokens), {dt:.1f} s"}
+                         f"routes of {n} of {w.E} experts, one oracle call per expert (all {w.T} tokens), {dt:.1f} s"}
 
     line = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
