@@ -48,7 +48,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-experts", type=int, default=3)        # reference arm: experts per step
     ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)   # cpu_baseline: oracle work to time
-    ap.add_argument("--cpu-sample-max-experts", type=int, default=16)
+    ap.add_argument("--cpu-sample-max-experts", type=int, default=384)
+    ap.add_argument("--cpu-sample-max-gb", type=float, default=2.0)      # host copy of the sampled BF16 weights
     return ap.parse_args()
 
 
@@ -217,22 +218,29 @@ class Step:
     def layers(self):
         return [l for l in (self.layer, self.shared) if l is not None]
 
-    def enqueue(self):
-        """The step, through the public C ABI (enqueue only, no host sync)."""
+    def io_set(self):
+        """The step's per-step inputs and outputs (the ones a host feeds and reads)."""
+        return {"x": self.x, "ids": self.ids, "scores": self.scores, "dy": self.dy if self.train else None,
+                "out": self.out, "dx": self.dx if self.train else None}
+
+    def enqueue(self, io=None):
+        """The step, through the public C ABI (enqueue only, no host sync), on
+        the step's own buffers or on another set of the same shapes."""
+        io = io or self.io_set()
+        x, out, dx = io["x"], io["out"], io["dx"]
         acc = False
         if self.shared:
-            self.shared.forward(self.x, self.s_ids, self.s_scores, self.sW13, self.sW2, out=self.out,
-                                saved=self.s_saved)
+            self.shared.forward(x, self.s_ids, self.s_scores, self.sW13, self.sW2, out=out, saved=self.s_saved)
             acc = True
-        self.layer.forward(self.x, self.ids, self.scores, self.W13, self.W2, out=self.out, saved=self.saved,
+        self.layer.forward(x, io["ids"], io["scores"], self.W13, self.W2, out=out, saved=self.saved,
                            accumulate=acc)
         if self.train:
             acc = False
             if self.shared:
-                self.shared.backward(self.s_saved, self.dy, self.sW13, self.sW2, dx=self.dx, dW13=self.sdW13,
+                self.shared.backward(self.s_saved, io["dy"], self.sW13, self.sW2, dx=dx, dW13=self.sdW13,
                                      dW2=self.sdW2)
                 acc = True
-            self.layer.backward(self.saved, self.dy, self.W13, self.W2, dx=self.dx, dW13=self.dW13, dW2=self.dW2,
+            self.layer.backward(self.saved, io["dy"], self.W13, self.W2, dx=dx, dW13=self.dW13, dW2=self.dW2,
                                 accumulate_dx=acc)
 
     def capture(self):
@@ -333,7 +341,9 @@ def run_ours(args, rank, world):
     # oracle sample weights (host copies) before the BF16 masters are dropped
     sample = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        experts = pick_sample_experts(w, st.ids_np, args.cpu_sample_max_experts)
+        per_expert = 3 * w.F * w.D * 2          # W13 + W2 of one expert, BF16
+        cap = max(1, min(args.cpu_sample_max_experts, int(args.cpu_sample_max_gb * 1e9) // per_expert))
+        experts = pick_sample_experts(w, st.ids_np, cap)
         sample = (experts, st.w13_bf16[experts].cpu(), st.w2_bf16[experts].cpu(), st.x.cpu(), st.dy.cpu())
     st.w13_bf16 = st.w2_bf16 = None
     torch.cuda.empty_cache()
@@ -398,30 +408,49 @@ def run_ours(args, rank, world):
     shared_flops = (6.0 * w.T * w.D * w.shared_F * (3.0 if st.train else 1.0)) if w.shared_F else 0.0
 
     # ---------------- end to end through the ABI with host buffers
+    # Every step uploads its inputs from pinned host memory and downloads its
+    # outputs.  Two device buffer sets and two copy streams pipeline the
+    # steps: step i+1's upload and step i-1's download run on the copy
+    # engines while step i's kernels run.  The timed region spans the first
+    # upload to the last download.
     e2e = None
     if not args.no_e2e:
-        hx = st.x.cpu().pin_memory()
-        hids = st.ids.cpu().pin_memory()
-        hsc = st.scores.cpu().pin_memory()
-        hdy = st.dy.cpu().pin_memory() if st.train else None
-        hout = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-        hdx = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() if st.train else None
-        h2d = hx.numel() * 2 + hids.numel() * 4 + hsc.numel() * 4 + (hdy.numel() * 2 if st.train else 0)
-        d2h = hout.numel() * 2 + (hdx.numel() * 2 if st.train else 0)
+        io0 = st.io_set()
+        ios = [io0, {k: (torch.empty_like(v) if v is not None else None) for k, v in io0.items()}]
+        h_in = {k: io0[k].cpu().pin_memory() for k in ("x", "ids", "scores", "dy") if io0[k] is not None}
+        h_out = [{k: torch.empty(io0[k].shape, dtype=io0[k].dtype).pin_memory() for k in ("out", "dx")
+                  if io0[k] is not None} for _ in range(2)]
+        h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        uploaded = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        downloaded = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step():
-            st.x.copy_(hx, non_blocking=True)
-            st.ids.copy_(hids, non_blocking=True)
-            st.scores.copy_(hsc, non_blocking=True)
-            if st.train:
-                st.dy.copy_(hdy, non_blocking=True)
-            st.enqueue()
-            hout.copy_(st.out, non_blocking=True)
-            if st.train:
-                hdx.copy_(st.dx, non_blocking=True)
+        def e2e_steps(n):
+            for i in range(n):
+                j = i % 2
+                io = ios[j]
+                with torch.cuda.stream(up):
+                    if i >= 2:
+                        up.wait_event(computed[j])        # step i-2 has read this set's inputs
+                    for k, t in h_in.items():
+                        io[k].copy_(t, non_blocking=True)
+                    uploaded[j].record(up)
+                stream.wait_event(uploaded[j])
+                if i >= 2:
+                    stream.wait_event(downloaded[j])      # step i-2's outputs have left this set
+                st.enqueue(io)
+                computed[j].record(stream)
+                with torch.cuda.stream(down):
+                    down.wait_event(computed[j])
+                    for k, t in h_out[j].items():
+                        t.copy_(io[k], non_blocking=True)
+                    downloaded[j].record(down)
+            for j in range(min(n, 2)):
+                stream.wait_event(downloaded[j])
 
-        for _ in range(2):
-            e2e_step()
+        e2e_steps(2)
         torch.cuda.synchronize(dev)
         if world > 1:
             torch.distributed.barrier()
@@ -429,8 +458,8 @@ def run_ours(args, rank, world):
         e1 = torch.cuda.Event(enable_timing=True)
         n_e2e = max(3, args.steps // 2)
         e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
+        up.wait_event(e0)
+        e2e_steps(n_e2e)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         ems = e0.elapsed_time(e1) / n_e2e
@@ -440,7 +469,8 @@ def run_ours(args, rank, world):
             ems = float(tt.item())
         e2e = {"value": round(flops / (ems * 1e-3) / 1e12 * world, 3), "unit": "TFLOP/s",
                "ms_per_step": round(ems, 4), "tokens_per_s": round(w.T * world / (ems * 1e-3), 1),
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "pipelined": "2 buffer sets; uploads and downloads overlap the neighbouring steps' kernels"}
 
     # ---------------- oracle baseline on host cores (rank 0, N = 1)
     cpu = None
