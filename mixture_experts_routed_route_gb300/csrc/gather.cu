@@ -219,26 +219,50 @@ cudaError_t both_impl(const void* src, int D, int K, const RoutingPtrs& rp, void
   return cudaGetLastError();
 }
 
-// MXFP8 variant of the same pass.  The gathered BF16 rows are staged once
-// (272-byte row pitch: conflict-free 16-byte writes and row reads), both
-// quantised bundles are built in shared memory as 128 x 128-byte tiles in
+// MXFP8 variant of the same pass, one CTA per 128-row x 128-column tile.
+//  * Row pass: thread t owns row t/2 and 64 contiguous columns (two MX
+//    blocks) of it, so each block's scale comes from the thread's own
+//    registers; the row's four scales are one 32-bit word of its atom.  The
+//    BF16 values also go to shared memory for the column pass: row pitch
+//    288 bytes, the two halves of a row 144 bytes apart, so the 16-byte
+//    stores of a quarter-warp (4 rows x 2 halves) hit distinct banks.
+//  * Column pass: thread (pair q, group g) builds features 2q and 2q+1 for
+//    rows 32g .. 32g+31 from 32-bit reads (a warp reads 128 contiguous
+//    bytes of one row).
+// Both quantised tiles are built in shared memory as 128 x 128-byte tiles in
 // the 128-byte swizzle (16-byte chunk j of line m at chunk j ^ (m % 8)) and
 // leave with two TMA stores: row bundle lines are token rows
-// (dst[r][c0 ..]), column bundle lines are features (dstT[d][r0 ..]).  A row
-// scale (4 blocks of this slab) is one 32-bit word of the row's atom.  Rows
+// (dst[r][c0 ..]), column bundle lines are features (dstT[d][r0 ..]).  Rows
 // past the routed rows are written as zeros; nothing reads them.
-constexpr int kMxPitchB = 2 * kBothCols + 16;
+constexpr int kMxPitchB = 288, kMxHalfB = 144;
 constexpr int kMxSmem = 1024 + 2 * 16384 + kBothRows * kMxPitchB + kBothRows * 4;
 
+// e4m3 codes of 32 values scaled by 2^-e, low byte first
+__device__ __forceinline__ void mx_codes32(const float (&v)[32], int e, uint32_t (&w)[8]) {
+  const float inv = exp2_int(-e);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    w[k] = cvt_e4m3x2(v[4 * k] * inv, v[4 * k + 1] * inv) | (cvt_e4m3x2(v[4 * k + 2] * inv, v[4 * k + 3] * inv) << 16);
+}
+
+__device__ __forceinline__ float amax32(const float (&v)[32]) {
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));
+  return a;
+}
+
 template <bool SCALE>
-__global__ void __launch_bounds__(256) gather_both_mx_kernel(const __grid_constant__ CUtensorMap tm_row,
-                                                             const __grid_constant__ CUtensorMap tm_col,
-                                                             const __nv_bfloat16* __restrict__ src, int D, int K,
-                                                             const int* __restrict__ hdr, const int* __restrict__ perm,
-                                                             const float* __restrict__ scores,
-                                                             uint8_t* __restrict__ dst_sf, uint8_t* __restrict__ dstT_sf,
-                                                             int b_cap, const int* __restrict__ row_block,
-                                                             const int4* __restrict__ blocks) {
+__global__ void __launch_bounds__(256, 3) gather_both_mx_kernel(const __grid_constant__ CUtensorMap tm_row,
+                                                                const __grid_constant__ CUtensorMap tm_col,
+                                                                const __nv_bfloat16* __restrict__ src, int D, int K,
+                                                                const int* __restrict__ hdr,
+                                                                const int* __restrict__ perm,
+                                                                const float* __restrict__ scores,
+                                                                uint8_t* __restrict__ dst_sf,
+                                                                uint8_t* __restrict__ dstT_sf, int b_cap,
+                                                                const int* __restrict__ row_block,
+                                                                const int4* __restrict__ blocks) {
   extern __shared__ uint8_t gmx_smem_raw[];
   uint8_t* rb = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gmx_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* cb = rb + 16384;
@@ -249,100 +273,97 @@ __global__ void __launch_bounds__(256) gather_both_mx_kernel(const __grid_consta
   const int r0 = blockIdx.y * kBothRows;
   if (r0 >= rows) return;
   const int c0 = blockIdx.x * kBothCols;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   if (tid < kBothRows / 32) {
     const bool in = r0 + 32 * tid < rows;
     const int b = in ? row_block[(r0 >> 5) + tid] : 0;
     s_blk[tid] = b;
     s_b0[tid] = in ? blocks[b].y : 0;
   }
-  // ---- load: thread t moves chunk t%16 (8 values) of rows t/16 + 16j; all
-  // route lookups first, then all eight row loads
+  // ---- row pass
+  const int row = tid >> 1, h = tid & 1;
+  const int r = r0 + row;
+  uint32_t sword;   // this thread's two block scales (bytes 0, 1)
   {
-    constexpr int kPer = kBothRows * 16 / 256;
-    const int chunk = tid & 15, c = c0 + chunk * 8;
-    int route[kPer];
+    const int route = r < rows ? perm[r] : -1;
+    uint4 u[8];
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int r = r0 + (tid >> 4) + 16 * j;
-      route[j] = (r < rows) ? perm[r] : -1;
+    for (int j = 0; j < 8; ++j) u[j] = make_uint4(0, 0, 0, 0);
+    float sc = 1.0f;
+    if (route >= 0) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src + static_cast<long long>(route / K) * D + c0 + 64 * h);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) u[j] = __ldg(s4 + j);
+      if (SCALE) sc = scores[route];
+    } else if (SCALE) {
+      sc = 0.0f;
     }
-    uint4 u[kPer];
+    if (SCALE && h == 0) s_row[row] = sc;
+    uint8_t* xrow = xs + row * kMxPitchB + h * kMxHalfB;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      u[j] = make_uint4(0, 0, 0, 0);
-      if (route[j] >= 0 && c < D)
-        u[j] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(route[j] / K) * D + c));
+    for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(xrow + j * 16) = u[j];
+    sword = 0;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w4 = u[4 * blk + q];
+        const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[8 * q + 2 * k] = bf16_lo(ww[k]);
+          v[8 * q + 2 * k + 1] = bf16_hi(ww[k]);
+        }
+      }
+      if (SCALE) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= sc;
+      }
+      const int e = mx_shared_exp(amax32(v));
+      uint32_t w[8];
+      mx_codes32(v, e, w);
+      // bytes 32 (2h + blk) .. +31 of the row's line: chunks 2 (2h + blk) and +1
+      const int ch = 2 * (2 * h + blk);
+      *reinterpret_cast<uint4*>(rb + row * 128 + ((ch ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(rb + row * 128 + (((ch + 1) ^ (row & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+      sword |= static_cast<uint32_t>(e + 127) << (8 * blk);
     }
-    if (SCALE && chunk == 0) {
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) s_row[(tid >> 4) + 16 * j] = route[j] >= 0 ? scores[route[j]] : 0.0f;
-    }
-#pragma unroll
-    for (int j = 0; j < kPer; ++j)
-      *reinterpret_cast<uint4*>(xs + ((tid >> 4) + 16 * j) * kMxPitchB + chunk * 16) = u[j];
+    sword |= __shfl_xor_sync(0xFFFFFFFFu, sword, 1) << 16;   // h = 0: blocks 2, 3 from its partner
   }
   __syncthreads();
-  // ---- row bundle: warp w builds rows 16w .. 16w+15, lane l columns 4l .. 4l+3
-  for (int rr = 0; rr < 16; ++rr) {
-    const int row = warp * 16 + rr;
-    const int r = r0 + row;
-    const uint2 raw = *reinterpret_cast<const uint2*>(xs + row * kMxPitchB + lane * 8);
-    float x0 = bf16_lo(raw.x), x1 = bf16_hi(raw.x), x2 = bf16_lo(raw.y), x3 = bf16_hi(raw.y);
-    if (SCALE) {
-      const float sc = s_row[row];
-      x0 *= sc;
-      x1 *= sc;
-      x2 *= sc;
-      x3 *= sc;
-    }
-    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-    const int e = mx_shared_exp(amax);
-    const float inv = exp2_int(-e);
-    const uint32_t q = cvt_e4m3x2(x0 * inv, x1 * inv) | (cvt_e4m3x2(x2 * inv, x3 * inv) << 16);
-    *reinterpret_cast<uint32_t*>(rb + row * 128 + (((lane >> 2) ^ (row & 7)) << 4) + (lane & 3) * 4) = q;
-    const uint32_t eb = static_cast<uint32_t>(e + 127);
-    const uint32_t w = __shfl_sync(0xFFFFFFFFu, eb, 0) | (__shfl_sync(0xFFFFFFFFu, eb, 8) << 8) |
-                       (__shfl_sync(0xFFFFFFFFu, eb, 16) << 16) | (__shfl_sync(0xFFFFFFFFu, eb, 24) << 24);
-    if (lane == 0 && r < rows) {
-      const int p = r - s_b0[row >> 5];
-      *reinterpret_cast<uint32_t*>(dst_sf + (static_cast<long long>(s_blk[row >> 5]) * (D / 128) + (c0 >> 7)) * 512 +
-                                   (p & 31) * 16 + (p >> 5) * 4) = w;
-    }
+  if (h == 0 && r < rows) {
+    const int p = r - s_b0[row >> 5];
+    *reinterpret_cast<uint32_t*>(dst_sf + (static_cast<long long>(s_blk[row >> 5]) * (D / 128) + (c0 >> 7)) * 512 +
+                                 (p & 31) * 16 + (p >> 5) * 4) = sword;
   }
-  // ---- column bundle: thread (cc, half) builds feature c0+cc, rows 64*half .. +63
+  // ---- column pass
   {
-    const int cc = tid & 127, half = tid >> 7;
-    const int d = c0 + cc;
+    const int q = tid & 63, g = tid >> 6;
+    const int rl = 32 * g;   // first row of the group within the tile
+    const uint8_t* xcol = xs + (q >> 5) * kMxHalfB + (q & 31) * 4;
+    uint32_t pr[32];
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      const int rl = half * 64 + g * 32;   // first row of this 32-row group within the tile
+    for (int i = 0; i < 32; ++i) pr[i] = *reinterpret_cast<const uint32_t*>(xcol + (rl + i) * kMxPitchB);
+#pragma unroll
+    for (int f = 0; f < 2; ++f) {
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const uint16_t h = *reinterpret_cast<const uint16_t*>(xs + (rl + i) * kMxPitchB + cc * 2);
-        v[i] = __uint_as_float(static_cast<uint32_t>(h) << 16);
+        v[i] = f == 0 ? bf16_lo(pr[i]) : bf16_hi(pr[i]);
         if (SCALE) v[i] *= s_row[rl + i];
       }
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-      const int e = mx_shared_exp(amax);
-      const float inv = exp2_int(-e);
+      const int e = mx_shared_exp(amax32(v));
       uint32_t w[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        w[q] = cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) | (cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
-      const int j0 = rl >> 4;
-      *reinterpret_cast<uint4*>(cb + cc * 128 + ((j0 ^ (cc & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(cb + cc * 128 + (((j0 + 1) ^ (cc & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+      mx_codes32(v, e, w);
+      const int cc = 2 * q + f;   // feature within the slab
+      *reinterpret_cast<uint4*>(cb + cc * 128 + (((2 * g) ^ (cc & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(cb + cc * 128 + (((2 * g + 1) ^ (cc & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
       if (r0 + rl < rows) {
+        const int d = c0 + cc;
         const int rg = (r0 + rl) >> 5;
-        dstT_sf[(static_cast<long long>(d >> 7) * b_cap + s_blk[rl >> 5]) * 512 +
-                sf_atom_byte(d & 127, rg - (s_b0[rl >> 5] >> 5))] = static_cast<uint8_t>(e + 127);
+        dstT_sf[(static_cast<long long>(d >> 7) * b_cap + s_blk[g]) * 512 + sf_atom_byte(d & 127, rg - (s_b0[g] >> 5))] =
+            static_cast<uint8_t>(e + 127);
       }
     }
   }
