@@ -83,11 +83,19 @@ struct MetaCache {
 // STEP: weight rows per grouped-M output tile: 128, or 256 when the two A
 // tiles of an NA = 2 store tile are adjacent 128-row blocks (the SwiGLU
 // forward's second A tile is the up half, F rows on).
+//
+// Grouped-M tiles run routing block by routing block, all output slices of
+// a block together: the resident CTAs then cover a few blocks at a time,
+// each block's activation rows come from DRAM once and are shared in L2 by
+// the CTAs of its slices, and the blocks of one expert (adjacent in block
+// order) still read the same weight slices at about the same time.  Slice
+// by slice instead, the weight stream evicts every activation bundle larger
+// than a few tens of MB from L2 before the next slice comes back to it.
 template <int MODE, int BK, int STEP>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int nblk, const MetaCache& mc) {
   Tile t;
   if (MODE == kGroupedM) {
-    const int n = tile / nblk, b = tile - n * nblk;
+    const int b = tile / p.n_tiles, n = tile - b * p.n_tiles;
     const int4 blk = (b < kCacheBlocks) ? mc.blocks[b] : p.blocks[b];
     t.e = blk.x;
     t.blk = b;
