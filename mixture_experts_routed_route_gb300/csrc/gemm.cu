@@ -91,11 +91,43 @@ struct MetaCache {
 // order) still read the same weight slices at about the same time.  Slice
 // by slice instead, the weight stream evicts every activation bundle larger
 // than a few tens of MB from L2 before the next slice comes back to it.
+//
+// A CTA's tiles are tile0, tile0 + step, ...: the walk keeps their
+// coordinates (grouped-M: block m and slice n, tile = m * n_tiles + n;
+// grouped-K: expert e, m, n, tile = (e * m_tiles + m) * n_tiles + n) and
+// advances them by the step's own coordinates with carries, so no role
+// divides per tile.  (Weight-gradient tiles are mostly one stage deep, and
+// two integer divisions per tile sat on the MMA thread's serial path.)
+template <int MODE>
+struct TileWalk {
+  int tile, n, m, e;
+  // the walk's step comes from p.walk (parameter space, no registers)
+  __device__ __forceinline__ void start(const GemmParams& p, int tile0) {
+    tile = tile0;
+    n = tile0 % p.n_tiles;
+    const int q = tile0 / p.n_tiles;
+    m = MODE == kGroupedM ? q : q % p.m_tiles;
+    e = MODE == kGroupedM ? 0 : q / p.m_tiles;
+  }
+  __device__ __forceinline__ void advance(const GemmParams& p) {
+    tile += p.walk[0];
+    n += p.walk[1];
+    const int c = n >= p.n_tiles;
+    n -= c ? p.n_tiles : 0;
+    m += p.walk[2] + c;
+    if (MODE == kGroupedK) {
+      const int c2 = m >= p.m_tiles;
+      m -= c2 ? p.m_tiles : 0;
+      e += p.walk[3] + c2;
+    }
+  }
+};
+
 template <int MODE, int BK, int STEP>
-__device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int nblk, const MetaCache& mc) {
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, const TileWalk<MODE>& w, const MetaCache& mc) {
   Tile t;
   if (MODE == kGroupedM) {
-    const int b = tile / p.n_tiles, n = tile - b * p.n_tiles;
+    const int b = w.m, n = w.n;
     const int4 blk = (b < kCacheBlocks) ? mc.blocks[b] : p.blocks[b];
     t.e = blk.x;
     t.blk = b;
@@ -112,9 +144,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int tile, int n
     t.sfa_atom[1] = static_cast<long long>(t.a_row[1] >> 7) * p.sfa_ts;
     t.sfb_atom = static_cast<long long>(b) * p.sfb_ts;
   } else {
-    const int per_e = p.m_tiles * p.n_tiles;
-    const int e = tile / per_e, rem = tile - e * per_e;
-    const int m = rem / p.n_tiles, n = rem - m * p.n_tiles;
+    const int e = w.e, m = w.m, n = w.n;
     const int k0 = mc.poff[e], klen = mc.poff[e + 1] - k0;
     t.e = e;
     t.blk = 0;
@@ -592,8 +622,10 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     // ------------------------------------------------------ TMA producer
     uint32_t it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE, C::BK, kStep>(p, tile, nblk, mc);
+    TileWalk<MODE> w;
+    w.start(p, blockIdx.x);
+    for (; ok && w.tile < num_tiles; w.advance(p)) {
+      const Tile t = decode_tile<MODE, C::BK, kStep>(p, w, mc);
       for (int ks = 0; ks < t.kstages; ++ks, ++it) {
         const uint32_t slot = it % S, ph = (it / S) & 1;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[slot], ph ^ 1, abort_flag, p.err))) {
@@ -661,8 +693,10 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     // ------------------------------------------------------- MMA issuer
     uint32_t it = 0, tc = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++tc) {
-      const Tile t = decode_tile<MODE, C::BK, kStep>(p, tile, nblk, mc);
+    TileWalk<MODE> w;
+    w.start(p, blockIdx.x);
+    for (; ok && w.tile < num_tiles; w.advance(p), ++tc) {
+      const Tile t = decode_tile<MODE, C::BK, kStep>(p, w, mc);
       const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty[acc], aph ^ 1, abort_flag, p.err))) break;
       tc_fence_after();
@@ -727,8 +761,10 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     // slot, i.e. after the MMAs that read them completed.
     uint32_t it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE, C::BK, kStep>(p, tile, nblk, mc);
+    TileWalk<MODE> w;
+    w.start(p, blockIdx.x);
+    for (; ok && w.tile < num_tiles; w.advance(p)) {
+      const Tile t = decode_tile<MODE, C::BK, kStep>(p, w, mc);
       for (int ks = 0; ks < t.kstages; ++ks, ++it) {
         const uint32_t slot = it % S, ph = (it / S) & 1;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], ph, abort_flag, p.err))) {
@@ -762,9 +798,13 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     const int gtid = (threadIdx.x - 64) % C::GROUP_THREADS;   // thread index within the group
     const bool staged = C::WGRAD && p.tma_store;
     uint32_t tc = grp;
+    // (the epilogue has slack: it decodes each tile from its index, which
+    // keeps the walk's registers out of its register-bound loop)
     for (int tile = blockIdx.x + grp * gridDim.x; tile < num_tiles;
          tile += C::EPI_GROUPS * gridDim.x, tc += C::EPI_GROUPS) {
-      const Tile t = decode_tile<MODE, C::BK, kStep>(p, tile, nblk, mc);
+      TileWalk<MODE> w;
+      w.start(p, tile);
+      const Tile t = decode_tile<MODE, C::BK, kStep>(p, w, mc);
       const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
       uint32_t hp[32];
       if (EPI == kEpiSwigluBwd && 32 * h < t.b_rows) load_h1_chunk(p, t, t.out_col0 + lrow, 32 * h, hp);
@@ -843,7 +883,13 @@ cudaError_t launch_impl(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
     configured = true;
   }
   const int grid = max(1, min(num_sms, g.max_tiles));
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.tmC, g.aux[0], g.aux[1], g.aux[2], g.aux[3], g.p);
+  GemmParams p = g.p;
+  const int q = grid / p.n_tiles;
+  p.walk[0] = grid;
+  p.walk[1] = grid % p.n_tiles;
+  p.walk[2] = MODE == kGroupedM ? q : q % p.m_tiles;
+  p.walk[3] = MODE == kGroupedM ? 0 : q / p.m_tiles;
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.tmC, g.aux[0], g.aux[1], g.aux[2], g.aux[3], p);
   return cudaGetLastError();
 }
 
