@@ -94,6 +94,7 @@ _SIGNATURES = {
     "moe_ctx_enable_stage_timing": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_ctx_stage_times": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.c_int]),
     "moe_ctx_launch_count": (ctypes.c_uint64, [_P]),
+    "moe_ctx_set_max_ctas": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_forward_static_scratch": (ctypes.c_int, [ctypes.POINTER(moe_config), ctypes.c_int32, _P, _P, _P,
                                                   ctypes.POINTER(moe_weight), ctypes.POINTER(moe_weight), _P,
                                                   ctypes.c_uint32, _P, _P]),
@@ -232,6 +233,10 @@ def moe_ctx_stage_times(ctx, pass_):
 
 def moe_ctx_launch_count(ctx):
     return LIB.moe_ctx_launch_count(ctx)
+
+
+def moe_ctx_set_max_ctas(ctx, max_ctas):
+    _check("moe_ctx_set_max_ctas", LIB.moe_ctx_set_max_ctas(ctx, max_ctas))
 
 
 def moe_forward_static_scratch(cfg, T, x, topk_ids, topk_scores, W13, W2, out, call_flags=0,

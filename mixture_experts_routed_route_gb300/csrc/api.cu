@@ -9,6 +9,7 @@
 //   -> W2 WGRAD -> W13 DGRAD -> W13 WGRAD -> K-reduction of dX.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -21,6 +22,7 @@ struct moe_ctx {
   moe_config cfg;
   int device;
   int num_sms;
+  int max_ctas = 0;   // moe_ctx_set_max_ctas (0: num_sms)
   int64_t r_cap;
   int64_t b_cap;
   uint8_t* base;
@@ -410,6 +412,12 @@ moe_status moe_ctx_stage_times(moe_ctx* ctx, int pass, float* ms, int n) {
 
 uint64_t moe_ctx_launch_count(const moe_ctx* ctx) { return ctx ? ctx->launches : 0; }
 
+moe_status moe_ctx_set_max_ctas(moe_ctx* ctx, int max_ctas) {
+  if (!ctx || max_ctas < 0) return MOE_ERR_INVALID_ARG;
+  ctx->max_ctas = max_ctas;
+  return MOE_OK;
+}
+
 moe_status moe_ctx_destroy(moe_ctx* ctx) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
   if (ctx->events) {
@@ -497,7 +505,7 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   uint8_t* sv = static_cast<uint8_t*>(saved);
   const RoutingPtrs rp = routing_ptrs(train ? sv : B(ctx, MOE_BUF_ROUTING), SL);
   const int64_t R = ctx->r_cap;
-  const int sms = ctx->num_sms;
+  const int sms = ctx->max_ctas > 0 ? std::min(ctx->max_ctas, ctx->num_sms) : ctx->num_sms;
 
   MOE_TRY(stage_mark(ctx, 0, 0, stream));
   MOE_TRY(launch_route(topk_ids, topk_scores, T, K, E, static_cast<int>(R), (c.flags & MOE_DEBUG_CHECKS) ? 1 : 0,
@@ -627,7 +635,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   uint8_t* sv = static_cast<uint8_t*>(const_cast<void*>(saved));
   const RoutingPtrs rp = routing_ptrs(sv, SL);
   const int64_t R = ctx->r_cap;
-  const int sms = ctx->num_sms;
+  const int sms = ctx->max_ctas > 0 ? std::min(ctx->max_ctas, ctx->num_sms) : ctx->num_sms;
   const int dw_fp32 = (call_flags & MOE_DW_FP32) ? 1 : 0;
   const int dw_acc = (call_flags & MOE_DW_ACCUMULATE) ? 1 : 0;
 

@@ -50,10 +50,12 @@ class Case:
 
 
 def run_gpu(case, precision=None, training=True, debug=False, out_init=None, max_tokens=None,
-            dx_init=None, dw_fp32=False, backward=True, swiglu_limit=0.0, weight_prec=None):
+            dx_init=None, dw_fp32=False, backward=True, swiglu_limit=0.0, weight_prec=None, max_ctas=0):
     """Forward (and backward) of a case through the C ABI; returns a dict of
     host arrays plus the layer object for further inspection.  weight_prec
-    overrides the weights' preparation (e.g. "mxfp8_1x32")."""
+    overrides the weights' preparation (e.g. "mxfp8_1x32"); max_ctas caps
+    the persistent grids (moe_ctx_set_max_ctas)."""
+    from mixture_experts_routed_route_gb300 import abi
     from mixture_experts_routed_route_gb300.layer import MoELayer, PreparedWeight
 
     w = case.w
@@ -62,6 +64,8 @@ def run_gpu(case, precision=None, training=True, debug=False, out_init=None, max
     T = case.T
     layer = MoELayer(max_tokens or max(T, 1), w.D, w.F, w.E, w.K, precision, training=training, debug=debug,
                      swiglu_limit=swiglu_limit)
+    if max_ctas:
+        abi.moe_ctx_set_max_ctas(layer.ctx, max_ctas)
     W13 = PreparedWeight(case.w13.to(dev), weight_prec or precision, with_transpose=training)
     W2 = PreparedWeight(case.w2.to(dev), weight_prec or precision, with_transpose=training)
     x = case.x.to(dev)

@@ -88,3 +88,10 @@ def test_host_side_sizes_without_gpu(lib):
     with pytest.raises(abi.MoEError) as ei:
         abi.moe_ctx_create(odd)
     assert ei.value.status in (abi.MOE_ERR_INVALID_ARG, abi.MOE_ERR_UNSUPPORTED)
+
+
+def test_context_setters_reject_null_context(lib):
+    """Host-side argument checks that need no device."""
+    from mixture_experts_routed_route_gb300 import abi
+    assert abi.LIB.moe_ctx_set_max_ctas(None, 4) == abi.MOE_ERR_INVALID_ARG
+    assert abi.LIB.moe_ctx_enable_stage_timing(None, 1) == abi.MOE_ERR_INVALID_ARG
