@@ -13,10 +13,10 @@
 //
 // One CTA of 32 warps.  Warp w owns the contiguous route segment
 // [w*seg, (w+1)*seg); within a warp, routes are taken 32 at a time in
-// order, and lanes holding the same expert are grouped with match.any, so
-// each route's rank within its expert is (earlier warps' count) + (earlier
-// batches of this warp) + (lower lanes of its group): exactly the stable
-// order by flat index t*K+k.
+// order, and lanes holding the same expert are grouped (one ballot per bit
+// of the expert id), so each route's rank within its expert is (earlier
+// warps' count) + (earlier batches of this warp) + (lower lanes of its
+// group): exactly the stable order by flat index t*K+k.
 #include "kernels.cuh"
 
 namespace moe {
@@ -28,6 +28,22 @@ constexpr int kWarps = kThreads / 32;
 // Routes per lane held in registers for both passes (read once, with all
 // loads in flight together): up to kWarps * 32 * kHold = 16384 routes.
 constexpr int kHold = 16;
+
+// Lanes of the warp whose expert equals this lane's (e = -1: inactive).
+// One ballot per bit of the id plus one for activity, so the cost does not
+// grow with the number of distinct experts among the 32 routes, as
+// match.any's does (with 64..384 experts nearly every lane differs).
+__device__ __forceinline__ unsigned same_expert_lanes(int e, int nbits) {
+  const bool act = e >= 0;
+  const unsigned ba = __ballot_sync(0xFFFFFFFFu, act);
+  unsigned m = act ? ba : ~ba;
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (e >> b) & 1;
+    const unsigned bb = __ballot_sync(0xFFFFFFFFu, bit);
+    m &= bit ? bb : ~bb;
+  }
+  return m;
+}
 
 // Exclusive block-wide scan of three ints per thread (one thread per slot).
 __device__ void block_scan3(int a, int b, int c, int& ea, int& eb, int& ec, int& ta, int& tb, int& tc,
@@ -115,6 +131,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       idr[j] = i < end ? ids[i] : -1;
     }
   }
+  // the saved copy of the scores, while the ID loads are in flight: 16-byte
+  // vectors, every load issued at once (pass 3 zeroes the inactive routes'
+  // entries after the barriers below), so the scatter issues no loads
+  if ((reinterpret_cast<uintptr_t>(scores) & 15) == 0) {   // the caller's scores need only 4-byte alignment
+    const int n4 = TK / 4;
+    const float4* s4 = reinterpret_cast<const float4*>(scores);
+    float4* d4 = reinterpret_cast<float4*>(rp.scores);
+    for (int q = tid; q < n4; q += kThreads) d4[q] = s4[q];
+    if (tid < TK - 4 * n4) rp.scores[4 * n4 + tid] = scores[4 * n4 + tid];
+  } else {
+    for (int i = tid; i < TK; i += kThreads) rp.scores[i] = scores[i];
+  }
   // expert of route i with id `id` (-1: inactive), flagging bad IDs
   auto classify = [&](int i, int id) {
     if (id >= 0 && id < E) return id;
@@ -122,10 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     else if (debug && scores[i] != 0.0f) my_err |= kErrInactiveScore;
     return -1;
   };
+  // counts need no order: one shared-memory atomic per active route
   auto count = [&](int e) {
-    const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
-    if (e >= 0 && lane == __ffs(grp) - 1) myh[e] += __popc(grp);
-    __syncwarp();
+    if (e >= 0) atomicAdd(&myh[e], 1);
   };
   if (held) {
 #pragma unroll
@@ -187,15 +214,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 
   // ---- pass 3: stable scatter of each route to its row
+  const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
   auto scatter = [&](int i, int id) {
     const int e = (i < end && id >= 0 && id < E) ? id : -1;
-    const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
+    const unsigned grp = same_expert_lanes(e, nbits);
     const unsigned lower = grp & ((1u << lane) - 1u);
     if (e >= 0) {
       const int row = myh[e] + __popc(lower);
       rp.perm[row] = i;
       rp.inv[i] = row;
-      rp.scores[i] = scores[i];
     } else if (i < end) {
       rp.inv[i] = -1;
       rp.scores[i] = 0.0f;
