@@ -502,7 +502,17 @@ template <bool MX, int NA, int MODE>
 struct Cfg {
   static constexpr bool WGRAD = MODE == kGroupedK;
   static constexpr int SF_BYTES = MX ? (NA + 1) * kAtom : 0;
-  static constexpr int STAGE = ((NA * kABytes + kBBytes + SF_BYTES) + 1023) / 1024 * 1024;
+  // Scale-atom groups (MXFP8, grouped-M, one A tile): the atoms of GS
+  // consecutive stages of a tile are consecutive in memory for the weight
+  // and for the row block, so they come in two copies per group into a
+  // ring of their own instead of two per stage (each TMA copy has a fixed
+  // cost well above its 512 bytes; this GEMM streams only 16 KB of weights
+  // per stage).
+  static constexpr bool SFG = MX && MODE == kGroupedM && NA == 1;
+  static constexpr int GS = 4, SFR = 2;
+  static constexpr int GROUP_BYTES = GS * (NA + 1) * kAtom;
+  static constexpr int SFG_BYTES = SFG ? SFR * GROUP_BYTES : 0;
+  static constexpr int STAGE = ((NA * kABytes + kBBytes + (SFG ? 0 : SF_BYTES)) + 1023) / 1024 * 1024;
   static constexpr int S = WGRAD ? 4 : ((NA == 2) ? 4 : 6);  // pipeline stages
   static constexpr int STAGING = WGRAD ? 2 * 32768 : 0;    // weight-gradient store buffers
   // accumulator buffers: two, except with two MXFP8 A tiles (2 x 256
@@ -528,7 +538,7 @@ struct Cfg {
   // MMA thread issues nothing but MMAs and commits
   static constexpr int SF_WARPS = MX ? 1 : 0;
   static constexpr int THREADS = 64 + EPI_THREADS + 32 * SF_WARPS;
-  static constexpr int SMEM = 1024 + S * STAGE + STAGING + 256 + kCacheBytes;
+  static constexpr int SMEM = 1024 + S * STAGE + STAGING + SFG_BYTES + 256 + kCacheBytes;
 };
 
 template <bool MX, int NA, int EPI, int MODE>
@@ -543,17 +553,20 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + S * C::STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::STAGING);
+  uint8_t* sfg = staging + C::STAGING;     // [SFR][GROUP_BYTES]: scale-atom groups (SFG)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sfg + C::SFG_BYTES);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + C::ACC_BUFS;
   uint64_t* drain = tempty + C::ACC_BUFS;
   uint64_t* sf_full = drain + 1;            // [S]: a stage's scale atoms are in TMEM (MXFP8)
   uint64_t* sf_drain = sf_full + S;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
+  uint64_t* sfg_full = sf_drain + 1;        // [SFR]: a scale-atom group has landed
+  uint64_t* sfg_empty = sfg_full + C::SFR;  // [SFR]: its atoms are in TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfg_empty + C::SFR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_abort = abort_flag + 1;  // [EPI_GROUPS]: a group's warps leave together
-  uint8_t* cache = staging + C::STAGING + 256;
+  uint8_t* cache = staging + C::STAGING + C::SFG_BYTES + 256;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -568,6 +581,10 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     mbar_init(drain, 1);
     for (int s2 = 0; s2 < S; ++s2) mbar_init(&sf_full[s2], 1);
     mbar_init(sf_drain, 1);
+    for (int g = 0; g < C::SFR; ++g) {
+      mbar_init(&sfg_full[g], 1);
+      mbar_init(&sfg_empty[g], 1);
+    }
     *abort_flag = 0;
     for (int g = 0; g < C::EPI_GROUPS; ++g) epi_abort[g] = 0;
     mbar_fence_init();
@@ -620,7 +637,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   // track the issuing thread's operations).
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
-    uint32_t it = 0;
+    uint32_t it = 0, gc = 0;   // gc: scale-atom groups issued (SFG)
     bool ok = true;
     TileWalk<MODE> w;
     w.start(p, blockIdx.x);
@@ -628,6 +645,23 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       const Tile t = decode_tile<MODE, C::BK, kStep>(p, w, mc);
       for (int ks = 0; ks < t.kstages; ++ks, ++it) {
         const uint32_t slot = it % S, ph = (it / S) & 1;
+        if (C::SFG && ks % C::GS == 0) {
+          // the group's atoms (weight, then row block), once the scale warp
+          // has moved the group that last used the buffer into TMEM
+          const uint32_t g = gc % C::SFR, gph = (gc / C::SFR) & 1;
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sfg_empty[g], gph ^ 1, abort_flag, p.err))) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const int n = min(C::GS, t.kstages - ks);
+            uint8_t* dst = sfg + g * C::GROUP_BYTES;
+            mbar_arrive_expect_tx(&sfg_full[g], 2 * n * kAtom);
+            bulk_load(dst, p.sfa + (t.sfa_atom[0] + ks) * kAtom, n * kAtom, &sfg_full[g]);
+            bulk_load(dst + C::GS * kAtom, p.sfb + (t.sfb_atom + ks) * kAtom, n * kAtom, &sfg_full[g]);
+          }
+          ++gc;
+        }
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[slot], ph ^ 1, abort_flag, p.err))) {
           ok = false;
           break;
@@ -637,7 +671,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
           uint8_t* sb = sa + NA * kABytes;
           uint8_t* ssf = sb + kBBytes;
           const int rb = stage_row_bytes<MODE, C::BK, MX ? 1 : 2>(t, ks);
-          mbar_arrive_expect_tx(&full[slot], (NA * 128 + t.b_rows) * rb + C::SF_BYTES);
+          mbar_arrive_expect_tx(&full[slot], (NA * 128 + t.b_rows) * rb + (C::SFG ? 0 : C::SF_BYTES));
           const int kx = t.k0 + ks * C::BK;
           if (MODE == kGroupedK) {
             const CUtensorMap* ta = rb == 128 ? &tmA : (rb == 64 ? &aux0 : &aux2);
@@ -664,7 +698,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
                 tma_load_2d(sb + c * p.b_box_rows * 128, &tmB, &full[slot], kx, t.b_row0 + p.b_box_rows * c);
             }
           }
-          if (MX) {
+          if (MX && !C::SFG) {
             if (MODE == kGroupedM && NA == 2 && p.a_pair_box == 1) {
               tma_load_3d(ssf, &aux2, &full[slot], 0, ks, t.a_row[0] >> 7);
             } else if (MODE == kGroupedM && NA == 2 && p.a_pair_box == 2) {
@@ -686,6 +720,11 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       for (uint32_t j = 0; j < pend; ++j) {
         const uint32_t i2 = it - 1 - j;
         drain_wait(&full[i2 % S], (i2 / S) & 1);
+      }
+      const uint32_t gpend = gc < static_cast<uint32_t>(C::SFR) ? gc : static_cast<uint32_t>(C::SFR);
+      for (uint32_t j = 0; j < gpend; ++j) {
+        const uint32_t i2 = gc - 1 - j;
+        drain_wait(&sfg_full[i2 % C::SFR], (i2 / C::SFR) & 1);
       }
     }
     __syncwarp();
@@ -759,7 +798,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     // columns once its data has landed; the commit tells the MMA thread.
     // A slot's columns are rewritten only after the producer refilled the
     // slot, i.e. after the MMAs that read them completed.
-    uint32_t it = 0;
+    uint32_t it = 0, gc = 0, cur = 0;   // scale-atom groups (SFG): next, and the current one
     bool ok = true;
     TileWalk<MODE> w;
     w.start(p, blockIdx.x);
@@ -771,12 +810,28 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
           ok = false;
           break;
         }
+        if (C::SFG && ks % C::GS == 0) {
+          cur = gc++;
+          if (!__all_sync(0xFFFFFFFFu,
+                          mbar_wait(&sfg_full[cur % C::SFR], (cur / C::SFR) & 1, abort_flag, p.err))) {
+            ok = false;
+            break;
+          }
+        }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t ssf = smem_u32(smem + slot * C::STAGE) + NA * kABytes + kBBytes;
           const uint32_t sfcol = tmem + C::SF_COL0 + slot * C::SF_COLS;
+          if (C::SFG) {
+            const uint32_t grp = smem_u32(sfg + (cur % C::SFR) * C::GROUP_BYTES) + (ks % C::GS) * kAtom;
+            tc_cp_sf(sfcol, sdesc_sf_atom(grp));
+            tc_cp_sf(sfcol + 4, sdesc_sf_atom(grp + C::GS * kAtom));
+            // the group's last stage: its buffer may be refilled once these copies completed
+            if (ks % C::GS == C::GS - 1 || ks == t.kstages - 1) tc_commit(&sfg_empty[cur % C::SFR]);
+          } else {
+            const uint32_t ssf = smem_u32(smem + slot * C::STAGE) + NA * kABytes + kBBytes;
 #pragma unroll
-          for (int j = 0; j <= NA; ++j) tc_cp_sf(sfcol + j * 4, sdesc_sf_atom(ssf + j * kAtom));
+            for (int j = 0; j <= NA; ++j) tc_cp_sf(sfcol + j * 4, sdesc_sf_atom(ssf + j * kAtom));
+          }
           tc_commit(&sf_full[slot]);
         }
         __syncwarp();
