@@ -35,10 +35,23 @@ def _routing_case(name):
     if name == "one_token":
         w = synth.Workload("one", 1, 128, 128, 4, 2, "bf16", "uniform", seed=10)
         return Case(w)
+    if name == "e1024":
+        # the largest expert count: ids need all 10 bits the lane grouping compares
+        w = synth.Workload("e1024", 256, 128, 128, 1024, 8, "bf16", "uniform", inactive_frac=0.1, seed=11)
+        return Case(w)
+    if name == "top_id_and_inactive":
+        # E = 64: id 63 has every compared bit set, like -1; the grouping must still keep them apart,
+        # and repeated ids inside one token count as separate routes
+        w = synth.Workload("top", 128, 128, 128, 64, 6, "bf16", "uniform", seed=12)
+        rng = np.random.default_rng(12)
+        ids = rng.choice(np.array([63, 63, -1, 62, 0, 31], np.int32), size=(128, 6))
+        s = rng.random((128, 6)).astype(np.float32)
+        s[ids < 0] = 0.0
+        return Case(w, ids=ids, scores=s)
     raise ValueError(name)
 
 
-@pytest.mark.parametrize("name", ["tiny", "skewed", "bad_ids", "dense", "one_token"])
+@pytest.mark.parametrize("name", ["tiny", "skewed", "bad_ids", "dense", "one_token", "e1024", "top_id_and_inactive"])
 def test_routing_bit_exact(name):
     case = _routing_case(name)
     w = case.w
