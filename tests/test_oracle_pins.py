@@ -423,3 +423,84 @@ def test_weight_1x32_blocks_are_per_row():
         for b in range(4):
             blk = w[r, 32 * b:32 * (b + 1)][None, :]
             assert np.array_equal(q[r, 32 * b:32 * (b + 1)], fm.mx_fake_quant(blk, axis=-1)[0])
+
+
+# ---------------------------------------------------------- post-expert RMSNorm
+
+def test_post_norm_constant_row_closed_form():
+    """A row of equal values a: mean(x^2) = a^2, so y = gamma * a / sqrt(a^2 + eps)
+    whatever D is."""
+    from oracle import post_norm as pn
+    rng = np.random.default_rng(5)
+    for D in (8, 96):
+        gamma = rng.normal(size=D)
+        for a, eps in ((0.75, 1e-6), (-3.0, 0.5), (2.0 ** -10, 1e-3)):
+            y, r = pn.forward(np.full((1, D), a), gamma, eps, rounding=False)
+            np.testing.assert_allclose(y[0], gamma * a / math.sqrt(a * a + eps), rtol=1e-14, atol=0)
+            assert r[0] == pytest.approx(1.0 / math.sqrt(a * a + eps), rel=1e-14)
+
+
+def test_post_norm_zero_row():
+    """An all-zero row (every route inactive, no shared expert) stays zero, and
+    its gradient is gamma * dy / sqrt(eps) (c = 0)."""
+    from oracle import post_norm as pn
+    D, eps = 16, 1e-5
+    gamma = np.linspace(-1.0, 1.5, D)
+    dy = np.linspace(0.3, -0.7, D)[None, :]
+    y, _ = pn.forward(np.zeros((1, D)), gamma, eps, rounding=False)
+    assert np.all(y == 0.0)
+    dx, dg = pn.backward(np.zeros((1, D)), gamma, eps, dy, rounding=False)
+    np.testing.assert_allclose(dx[0], gamma * dy[0] / math.sqrt(eps), rtol=1e-14)
+    assert np.all(dg == 0.0)
+
+
+def test_post_norm_scale_invariant_without_eps():
+    """With eps = 0 the map forgets the row's scale: y(alpha x) = y(x)."""
+    from oracle import post_norm as pn
+    rng = np.random.default_rng(6)
+    x = rng.normal(size=(3, 24))
+    gamma = rng.normal(size=24)
+    y1, _ = pn.forward(x, gamma, 0.0, rounding=False)
+    for alpha in (1e-3, 7.0, 2.0 ** 20):
+        y2, _ = pn.forward(alpha * x, gamma, 0.0, rounding=False)
+        np.testing.assert_allclose(y2, y1, rtol=1e-12)
+
+
+def test_post_norm_backward_matches_finite_differences():
+    """dx and dgamma against central differences of L = sum(dy * y) in fp64."""
+    from oracle import post_norm as pn
+    rng = np.random.default_rng(7)
+    T, D, eps = 3, 8, 1e-3
+    x = rng.normal(size=(T, D))
+    gamma = rng.normal(size=D)
+    dy = rng.normal(size=(T, D))
+    dx, dg = pn.backward(x, gamma, eps, dy, rounding=False)
+
+    def loss(xv, gv):
+        return float(np.sum(dy * pn.forward(xv, gv, eps, rounding=False)[0]))
+
+    h = 1e-6
+    num_dx = np.zeros_like(x)
+    for t in range(T):
+        for d in range(D):
+            e = np.zeros_like(x)
+            e[t, d] = h
+            num_dx[t, d] = (loss(x + e, gamma) - loss(x - e, gamma)) / (2 * h)
+    num_dg = np.zeros(D)
+    for d in range(D):
+        e = np.zeros(D)
+        e[d] = h
+        num_dg[d] = (loss(x, gamma + e) - loss(x, gamma - e)) / (2 * h)
+    np.testing.assert_allclose(dx, num_dx, rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dg, num_dg, rtol=1e-6, atol=1e-8)
+
+
+def test_post_norm_rounds_outputs_to_bf16():
+    from oracle import post_norm as pn
+    rng = np.random.default_rng(8)
+    x = fm.round_bf16(rng.normal(size=(4, 32)))
+    gamma = fm.round_bf16(rng.normal(size=32))
+    y, _ = pn.forward(x, gamma, 1e-6)
+    np.testing.assert_array_equal(y, fm.round_bf16(y))
+    yx, _ = pn.forward(x, gamma, 1e-6, rounding=False)
+    assert np.max(np.abs(y - yx) / np.maximum(np.abs(yx), 1e-30)) <= 2.0 ** -8
