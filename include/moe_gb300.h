@@ -78,6 +78,9 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_MXFP8_1X32 = 2 } moe_precision;
 /* moe_config.flags */
 #define MOE_TRAINING      0x1u  /* forward saves state; backward is allowed   */
 #define MOE_DEBUG_CHECKS  0x2u  /* also flag ID -1 routes with nonzero score */
+#define MOE_POST_NORM     0x4u  /* the layer ends with the post-expert RMSNorm
+                                   (moe_ctx_set_post_norm); training saves the
+                                   pre-norm output for moe_post_norm_backward */
 
 /* call_flags of moe_forward */
 #define MOE_ACCUMULATE_OUT 0x1u /* out = round(out + sum_k s*h3) (shared expert first) */
@@ -140,8 +143,8 @@ typedef struct moe_ctx moe_ctx;
  * later call reuses it, so its addresses are stable for graph capture) and
  * creates no stream.  Scratch is sized for max_tokens*top_k routes plus 31
  * pad rows per expert, which bounds every routing, so a call can never
- * overflow it ([NEWS] "scratch is a hard limit" -- here it is sized so the
- * limit cannot be reached).  Must be called with the target device current.
+ * overflow it ([NEWS] "How the execution model works" treats running out of
+ * scratch as fatal; here it is sized so that cannot happen).  Must be called with the target device current.
  * Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_CUDA; *out is
  * set only on MOE_OK.
  */
@@ -202,7 +205,9 @@ typedef enum {
   MOE_SAVED_BSTART = 13,    /* int32[E+1]   first row block of each expert     */
   MOE_SAVED_ROWBLOCK = 14,  /* int32[R_cap/32] row block of each 32-row group  */
   MOE_SAVED_H3 = 15,        /* bf16[R_cap, D] route outputs (score gradient)   */
-  MOE_SAVED_NUM_FIELDS = 16
+  MOE_SAVED_PRENORM = 16,   /* bf16[T_max, D] layer output before the post-expert
+                               RMSNorm (MOE_POST_NORM only, else 0 bytes)     */
+  MOE_SAVED_NUM_FIELDS = 17
 } moe_saved_field;
 
 /* Offset and size in bytes of one saved-state field; the row capacity
@@ -316,7 +321,9 @@ typedef enum {
   MOE_BUF_DXR = 13,        /* bf16 [R_cap, D]                                  */
   MOE_BUF_ROUTING = 14,    /* inference routing state (same layout as saved)   */
   MOE_BUF_ERROR = 15,      /* uint32 error word                                */
-  MOE_BUF_NUM = 16
+  MOE_BUF_NORM = 16,       /* MOE_POST_NORM training: float r[T_max], then the
+                              dgamma partial sums [ceil(T_max/64)][D]          */
+  MOE_BUF_NUM = 17
 } moe_buffer;
 
 MOE_API moe_status moe_ctx_buffer(moe_ctx* ctx, int which, void** dev_ptr, size_t* bytes);
@@ -343,6 +350,39 @@ MOE_API moe_status moe_ctx_buffer(moe_ctx* ctx, int which, void** dev_ptr, size_
 #define MOE_BWD_STAGES 6
 MOE_API moe_status moe_ctx_enable_stage_timing(moe_ctx* ctx, int enable);
 MOE_API moe_status moe_ctx_stage_times(moe_ctx* ctx, int pass, float* ms, int n);
+
+/*
+ * Post-expert RMSNorm ("Meta Dist-MoE: Open-Source Fused MoE Kernels for
+ * Blackwell", "Supported modes", names a fused post-expert RMSNorm without
+ * defining it; this library's reading).  With MOE_POST_NORM in the
+ * configuration, the combine that writes the layer output x[t] (the BF16
+ * row of the score-weighted K-sum, after adding `out` under
+ * MOE_ACCUMULATE_OUT) normalises it over D in the same pass:
+ *   r[t] = 1 / sqrt(mean_d x[t,d]^2 + eps),  out[t,d] = bf16(gamma[d] x[t,d] r[t])
+ * with r and the products in FP32.  A training forward also writes x to the
+ * saved field MOE_SAVED_PRENORM.
+ *
+ * moe_ctx_set_post_norm: gamma is a device pointer to bf16[D] (16-byte
+ *   aligned, not owned, read by every later forward and post-norm backward;
+ *   keep it alive and unchanged while they run); eps finite and > 0.  A
+ *   forward with MOE_POST_NORM and no gamma set returns MOE_ERR_INVALID_ARG.
+ *   Errors: MOE_ERR_INVALID_ARG (null context or gamma, eps not finite and
+ *   positive, context without MOE_POST_NORM).
+ *
+ * moe_post_norm_backward: from dout = dL/dout (bf16 [T,D], the tokens of
+ *   the forward that wrote `saved`) computes, with g = gamma * dout and
+ *   c[t] = mean_d g[t,d] x[t,d],
+ *     dx_pre[t,d] = bf16(r[t] g[t,d] - x[t,d] r[t]^3 c[t])   (bf16 [T,D])
+ *     dgamma[d]   = sum_t dout[t,d] x[t,d] r[t]               (float [D])
+ *   in FP32, sums in fixed orders (bitwise reproducible).  dx_pre is the
+ *   gradient to pass as `dout` to moe_backward (and to the shared expert's).
+ *   dgamma is overwritten.  Enqueue only.  Errors: MOE_ERR_INVALID_ARG
+ *   (null or misaligned pointer, context without MOE_TRAINING and
+ *   MOE_POST_NORM, or no gamma set).
+ */
+MOE_API moe_status moe_ctx_set_post_norm(moe_ctx* ctx, const void* gamma, float eps);
+MOE_API moe_status moe_post_norm_backward(moe_ctx* ctx, const void* saved, const void* dout, void* dx_pre,
+                                          float* dgamma, cudaStream_t stream);
 
 /* Number of kernels this context has enqueued so far (host-side count; a
  * captured call counts once at capture time). */
@@ -373,7 +413,8 @@ MOE_API moe_status moe_ctx_set_max_ctas(moe_ctx* ctx, int max_ctas);
  * cudaMalloc/cudaFree and no allocating library routine.
  *   cfg         host struct: d_model, d_ff, num_experts, top_k, precision
  *               (max_tokens and MOE_TRAINING are ignored; MOE_DEBUG_CHECKS
- *               is honoured)
+ *               is honoured; MOE_POST_NORM, whose gamma lives in a context,
+ *               returns MOE_ERR_UNSUPPORTED)
  *   T, x, topk_ids, topk_scores, W13, W2, out, call_flags: as moe_forward
  *   device_error_word  device uint32 that receives the MOE_DEV_ERR_* bits
  *               (ORed in, never cleared here); NULL uses a word inside the

@@ -34,6 +34,7 @@ MOE_MXFP8_1X32 = 2    # weight preparation only: 1x32 inference blocks
 
 MOE_TRAINING = 0x1
 MOE_DEBUG_CHECKS = 0x2
+MOE_POST_NORM = 0x4
 MOE_ACCUMULATE_OUT = 0x1
 MOE_ACCUMULATE_DX = 0x1
 MOE_DW_FP32 = 0x2
@@ -42,14 +43,14 @@ MOE_DW_ACCUMULATE = 0x4
 # moe_saved_field
 (MOE_SAVED_HEADER, MOE_SAVED_COUNTS, MOE_SAVED_OFFSETS, MOE_SAVED_POFFSETS, MOE_SAVED_PERM, MOE_SAVED_INV,
  MOE_SAVED_BLOCKS, MOE_SAVED_SCORES, MOE_SAVED_H1, MOE_SAVED_XCOL, MOE_SAVED_XCOL_SCALE, MOE_SAVED_H2COL,
- MOE_SAVED_H2COL_SCALE, MOE_SAVED_BSTART, MOE_SAVED_ROWBLOCK, MOE_SAVED_H3) = range(16)
-MOE_SAVED_NUM_FIELDS = 16
+ MOE_SAVED_H2COL_SCALE, MOE_SAVED_BSTART, MOE_SAVED_ROWBLOCK, MOE_SAVED_H3, MOE_SAVED_PRENORM) = range(17)
+MOE_SAVED_NUM_FIELDS = 17
 
 # moe_buffer
 (MOE_BUF_XROW, MOE_BUF_XROW_SCALE, MOE_BUF_H2ROW, MOE_BUF_H2ROW_SCALE, MOE_BUF_H3, MOE_BUF_DH3ROW,
  MOE_BUF_DH3ROW_SCALE, MOE_BUF_DH3COL, MOE_BUF_DH3COL_SCALE, MOE_BUF_DH1ROW, MOE_BUF_DH1ROW_SCALE,
- MOE_BUF_DH1COL, MOE_BUF_DH1COL_SCALE, MOE_BUF_DXR, MOE_BUF_ROUTING, MOE_BUF_ERROR) = range(16)
-MOE_BUF_NUM = 16
+ MOE_BUF_DH1COL, MOE_BUF_DH1COL_SCALE, MOE_BUF_DXR, MOE_BUF_ROUTING, MOE_BUF_ERROR, MOE_BUF_NORM) = range(17)
+MOE_BUF_NUM = 17
 
 
 class moe_config(ctypes.Structure):
@@ -95,6 +96,8 @@ _SIGNATURES = {
     "moe_ctx_stage_times": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.c_int]),
     "moe_ctx_launch_count": (ctypes.c_uint64, [_P]),
     "moe_ctx_set_max_ctas": (ctypes.c_int, [_P, ctypes.c_int]),
+    "moe_ctx_set_post_norm": (ctypes.c_int, [_P, _P, ctypes.c_float]),
+    "moe_post_norm_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "moe_forward_static_scratch": (ctypes.c_int, [ctypes.POINTER(moe_config), ctypes.c_int32, _P, _P, _P,
                                                   ctypes.POINTER(moe_weight), ctypes.POINTER(moe_weight), _P,
                                                   ctypes.c_uint32, _P, _P]),
@@ -237,6 +240,15 @@ def moe_ctx_launch_count(ctx):
 
 def moe_ctx_set_max_ctas(ctx, max_ctas):
     _check("moe_ctx_set_max_ctas", LIB.moe_ctx_set_max_ctas(ctx, max_ctas))
+
+
+def moe_ctx_set_post_norm(ctx, gamma, eps):
+    _check("moe_ctx_set_post_norm", LIB.moe_ctx_set_post_norm(ctx, _ptr(gamma), eps))
+
+
+def moe_post_norm_backward(ctx, saved, dout, dx_pre, dgamma, stream=None):
+    _check("moe_post_norm_backward",
+           LIB.moe_post_norm_backward(ctx, _ptr(saved), _ptr(dout), _ptr(dx_pre), _ptr(dgamma), _stream(stream)))
 
 
 def moe_forward_static_scratch(cfg, T, x, topk_ids, topk_scores, W13, W2, out, call_flags=0,

@@ -23,6 +23,8 @@ struct moe_ctx {
   int device;
   int num_sms;
   int max_ctas = 0;   // moe_ctx_set_max_ctas (0: num_sms)
+  const void* norm_gamma = nullptr;   // moe_ctx_set_post_norm (MOE_POST_NORM)
+  float norm_eps = 0.0f;
   int64_t r_cap;
   int64_t b_cap;
   uint8_t* base;
@@ -98,12 +100,13 @@ SavedLayout saved_layout(const moe_config* c) {
   sz[MOE_SAVED_H2COL] = F * R * esz;
   sz[MOE_SAVED_H2COL_SCALE] = mx ? (F / 128) * B * 512 : 0;
   sz[MOE_SAVED_H3] = R * D * 2;
+  sz[MOE_SAVED_PRENORM] = (c->flags & MOE_POST_NORM) ? static_cast<int64_t>(c->max_tokens) * D * 2 : 0;
   // routing fields first (the inference copy in the context holds just these)
   static const int order[MOE_SAVED_NUM_FIELDS] = {
       MOE_SAVED_HEADER, MOE_SAVED_COUNTS, MOE_SAVED_OFFSETS, MOE_SAVED_POFFSETS, MOE_SAVED_PERM,
       MOE_SAVED_INV,    MOE_SAVED_BLOCKS, MOE_SAVED_SCORES,  MOE_SAVED_BSTART,   MOE_SAVED_ROWBLOCK,
       MOE_SAVED_H1,     MOE_SAVED_XCOL,   MOE_SAVED_XCOL_SCALE, MOE_SAVED_H2COL, MOE_SAVED_H2COL_SCALE,
-      MOE_SAVED_H3};
+      MOE_SAVED_H3,     MOE_SAVED_PRENORM};
   size_t off = 0;
   for (int k = 0; k < MOE_SAVED_NUM_FIELDS; ++k) {
     const int i = order[k];
@@ -145,6 +148,10 @@ ScratchLayout scratch_layout(const moe_config* c) {
     sz[MOE_BUF_DH1COL] = 2 * F * R * esz;
     sz[MOE_BUF_DH1COL_SCALE] = mx ? (2 * F / 128) * B * 512 : 0;
     sz[MOE_BUF_DXR] = R * D * 2;
+  }
+  if (train && (c->flags & MOE_POST_NORM)) {   // r[T_max], then the dgamma slab partials
+    const int64_t Tm = c->max_tokens;
+    sz[MOE_BUF_NORM] = (Tm + (Tm + kPostNormSlab - 1) / kPostNormSlab * D) * sizeof(float);
   }
   sz[MOE_BUF_ROUTING] = saved_layout(c).routing_bytes;
   sz[MOE_BUF_ERROR] = 32;   // error word at 0, clip counters at 16
@@ -412,6 +419,31 @@ moe_status moe_ctx_stage_times(moe_ctx* ctx, int pass, float* ms, int n) {
 
 uint64_t moe_ctx_launch_count(const moe_ctx* ctx) { return ctx ? ctx->launches : 0; }
 
+moe_status moe_ctx_set_post_norm(moe_ctx* ctx, const void* gamma, float eps) {
+  if (!ctx || !gamma || !aligned16(gamma) || !(eps > 0.0f) || eps > 3.0e38f) return MOE_ERR_INVALID_ARG;
+  if (!(ctx->cfg.flags & MOE_POST_NORM)) return MOE_ERR_INVALID_ARG;
+  ctx->norm_gamma = gamma;
+  ctx->norm_eps = eps;
+  return MOE_OK;
+}
+
+moe_status moe_post_norm_backward(moe_ctx* ctx, const void* saved, const void* dout, void* dx_pre, float* dgamma,
+                                  cudaStream_t stream) {
+  if (!ctx || !saved || !dout || !dx_pre || !dgamma) return MOE_ERR_INVALID_ARG;
+  const moe_config& c = ctx->cfg;
+  if (!(c.flags & MOE_TRAINING) || !(c.flags & MOE_POST_NORM) || !ctx->norm_gamma) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(saved) || !aligned16(dout) || !aligned16(dx_pre) || !aligned16(dgamma)) return MOE_ERR_INVALID_ARG;
+  const SavedLayout SL = saved_layout(&c);
+  const uint8_t* sv = static_cast<const uint8_t*>(saved);
+  const int* hdr = reinterpret_cast<const int*>(sv + SL.off[MOE_SAVED_HEADER]);
+  float* nb = reinterpret_cast<float*>(B(ctx, MOE_BUF_NORM));
+  const int sms = ctx->max_ctas > 0 ? std::min(ctx->max_ctas, ctx->num_sms) : ctx->num_sms;
+  MOE_TRY(launch_post_norm_backward(sv + SL.off[MOE_SAVED_PRENORM], ctx->norm_gamma, dout, c.d_model, ctx->norm_eps,
+                                    dx_pre, nb, nb + c.max_tokens, dgamma, c.max_tokens, sms, stream, hdr));
+  ctx->launches += 3;
+  return MOE_OK;
+}
+
 moe_status moe_ctx_set_max_ctas(moe_ctx* ctx, int max_ctas) {
   if (!ctx || max_ctas < 0) return MOE_ERR_INVALID_ARG;
   ctx->max_ctas = max_ctas;
@@ -500,6 +532,8 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   if (!x || !topk_ids || !topk_scores || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(out) || (saved && !aligned16(saved))) return MOE_ERR_INVALID_ARG;
   if (call_flags & ~MOE_ACCUMULATE_OUT) return MOE_ERR_INVALID_ARG;
+  const bool norm = (c.flags & MOE_POST_NORM) != 0;
+  if (norm && !ctx->norm_gamma) return MOE_ERR_INVALID_ARG;
 
   const SavedLayout SL = saved_layout(&c);
   uint8_t* sv = static_cast<uint8_t*>(saved);
@@ -610,8 +644,9 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   MOE_TRY(stage_mark(ctx, 0, 4, stream));
 
   // ---- combine
-  MOE_TRY(launch_combine(h3, D, K, rp.inv, rp.scores, out, T,
-                         (call_flags & MOE_ACCUMULATE_OUT) != 0, sms, stream));
+  MOE_TRY(launch_combine(h3, D, K, rp.inv, rp.scores, out, T, (call_flags & MOE_ACCUMULATE_OUT) != 0, sms, stream,
+                         nullptr, norm ? ctx->norm_gamma : nullptr, ctx->norm_eps,
+                         (norm && train) ? sv + SL.off[MOE_SAVED_PRENORM] : nullptr));
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 0, 5, stream));
   return MOE_OK;

@@ -7,10 +7,10 @@
 // bundles, launch_gather_rows); WGRAD contracts over token rows and needs a
 // separately quantised column-oriented bundle (stored transposed [D, r_cap]
 // so the GEMM reads it K-major); launch_gather_both writes both bundles of
-// the same rows in one pass when training.  MXFP8 training
-// quantises after the gather ("MXFP8 training publishes BF16 source rows and
-// quantizes after peer gather"); row quantisation depends only on the row,
-// so quantising after the gather is exact.  Pad rows (route -1) are zero.
+// the same rows in one pass when training.  In MXFP8 training the rows
+// travel as BF16 and are quantised where they land (same section); row
+// quantisation depends only on the row, so quantising after the gather is
+// exact.  Pad rows (route -1) are zero.
 //
 // The dh3 prep of the backward ("Mixture of Experts: How Routing Becomes GPU
 // Computation", section 2, "SwiGLU backward: the complete expert path":

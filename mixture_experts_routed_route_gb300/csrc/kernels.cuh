@@ -51,9 +51,22 @@ cudaError_t launch_gather_both(bool mx, bool use_scores, const void* src, int D,
 
 // out[t] = bf16((accumulate ? out[t] : 0) + sum_k s(t,k) * h[inv(t,k)]),
 // FP32, k in order; s = 1 when `scores` is NULL.  The token count is T, or
-// hdr[0] (read on the device, at most T) when `hdr` is given.
+// hdr[0] (read on the device, at most T) when `hdr` is given.  With `gamma`
+// (bf16 [D]) that row x is then normalised: out[t] = bf16(gamma x r),
+// r = 1/sqrt(mean x^2 + eps); x is kept in `xsave` (bf16 [T, D]) if given.
 cudaError_t launch_combine(const void* h, int D, int K, const int* inv, const float* scores, void* out, int T,
-                           bool accumulate, int num_sms, cudaStream_t stream, const int* hdr = nullptr);
+                           bool accumulate, int num_sms, cudaStream_t stream, const int* hdr = nullptr,
+                           const void* gamma = nullptr, float eps = 0.0f, void* xsave = nullptr);
+
+// Tokens per dgamma partial sum of the post-norm backward.
+constexpr int kPostNormSlab = 64;
+
+// Post-norm backward for tokens t < min(T, hdr[0]): dx = bf16(r g - x r^3 c)
+// with g = gamma dy, c = mean_d(g x), r from x (also written to rstd[T]);
+// dgamma[d] = sum_t dy x r through partial[ceil(T/kPostNormSlab)][D] slab sums.
+cudaError_t launch_post_norm_backward(const void* x, const void* gamma, const void* dy, int D, float eps, void* dx,
+                                      float* rstd, float* partial, float* dgamma, int T, int num_sms,
+                                      cudaStream_t stream, const int* hdr);
 
 // dp[t*K+k] = <h3[inv(t,k)], dY[t]> in FP32 (fixed order), 0 if inactive;
 // tokens t < min(T, hdr[0]).

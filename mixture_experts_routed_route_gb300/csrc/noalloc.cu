@@ -151,6 +151,7 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   if (cfg->precision != MOE_BF16 && cfg->precision != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
   if (!(cfg->swiglu_limit >= 0.0f) || cfg->swiglu_limit > 3.0e38f) return MOE_ERR_INVALID_ARG;
   if (D % 128 || F % 128) return MOE_ERR_UNSUPPORTED;
+  if (cfg->flags & MOE_POST_NORM) return MOE_ERR_UNSUPPORTED;   // its gamma lives in a context
   if (call_flags & ~MOE_ACCUMULATE_OUT) return MOE_ERR_INVALID_ARG;
   const bool mx = cfg->precision == MOE_MXFP8;
   if (!weight_matches(W13, cfg->precision, E, 2 * F, D) || !weight_matches(W2, cfg->precision, E, D, F))

@@ -59,8 +59,9 @@ class MoELayer:
     """One routed MoE layer bound to a context (fixed scratch)."""
 
     def __init__(self, max_tokens, d_model, d_ff, num_experts, top_k, precision, training=False, debug=False,
-                 device="cuda", swiglu_limit=0.0):
-        flags = (abi.MOE_TRAINING if training else 0) | (abi.MOE_DEBUG_CHECKS if debug else 0)
+                 device="cuda", swiglu_limit=0.0, post_norm=False):
+        flags = ((abi.MOE_TRAINING if training else 0) | (abi.MOE_DEBUG_CHECKS if debug else 0)
+                 | (abi.MOE_POST_NORM if post_norm else 0))
         self.cfg = abi.make_config(max_tokens, d_model, d_ff, num_experts, top_k, precision_code(precision), flags,
                                    swiglu_limit)
         self.device = torch.device(device)
@@ -105,6 +106,21 @@ class MoELayer:
 
     def clip_stats(self):
         return abi.moe_ctx_clip_stats(self.ctx)
+
+    def set_post_norm(self, gamma, eps):
+        """gamma: bf16 [D] on the device, kept referenced while the layer uses it."""
+        abi.moe_ctx_set_post_norm(self.ctx, gamma, eps)
+        self._gamma = gamma
+
+    def post_norm_backward(self, saved, dout, dx_pre=None, dgamma=None, stream=None):
+        """dout = dL/d(normalised output) -> (dL/d(pre-norm output), dL/dgamma)."""
+        T = dout.shape[0]
+        if dx_pre is None:
+            dx_pre = torch.empty((T, self.D), dtype=torch.bfloat16, device=self.device)
+        if dgamma is None:
+            dgamma = torch.empty((self.D,), dtype=torch.float32, device=self.device)
+        abi.moe_post_norm_backward(self.ctx, saved, dout, dx_pre, dgamma, stream)
+        return dx_pre, dgamma
 
     # ----------------------------------------------------------- compute
     def forward(self, x, ids, scores, W13, W2, out=None, saved=None, accumulate=False, stream=None):
