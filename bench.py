@@ -125,26 +125,29 @@ class ClockSampler:
 
 # --------------------------------------------------------- algorithmic bytes
 
-def stage_bytes(w, rows_padded, routes, precision, train):
+def stage_bytes(w, rows_padded, routes, precision, train, experts_used=None):
     """Unique bytes each stage must move (read once + written once), per launch.
 
     rows_padded = sum of expert row counts padded to 32; routes = active
-    routes.  MXFP8 operands cost 1 + 1/32 bytes per element (E4M3 + E8M0)."""
+    routes; experts_used = experts with at least one route (the GEMMs read
+    only their weights; the weight gradients write dW of every expert).
+    MXFP8 operands cost 1 + 1/32 bytes per element (E4M3 + E8M0)."""
     T, D, F, E = w.T, w.D, w.F, w.E
+    Eu = w.E if experts_used is None else experts_used
     q = (1 + 1 / 32) if precision == "mxfp8" else 2.0
     Rp, R = rows_padded, routes
     fwd = {
         "route": T * w.K * 8 + (Rp + 2 * T * w.K) * 4,
         "gather_x": T * D * 2 + Rp * D * q * (2 if train else 1),
-        "gemm_w13_swiglu": E * 2 * F * D * q + Rp * D * q + Rp * F * q + (Rp * 2 * F * 2 + Rp * F * q if train else 0),
-        "gemm_w2": E * D * F * q + Rp * F * q + Rp * D * 2,
+        "gemm_w13_swiglu": Eu * 2 * F * D * q + Rp * D * q + Rp * F * q + (Rp * 2 * F * 2 + Rp * F * q if train else 0),
+        "gemm_w2": Eu * D * F * q + Rp * F * q + Rp * D * 2,
         "combine": R * D * 2 + T * D * 2 * 2,
     }
     bwd = {
         "gather_dh3": T * D * 2 + 2 * Rp * D * q,
-        "gemm_w2_dgrad_swiglu_bwd": E * D * F * q + Rp * D * q + Rp * 2 * F * 2 + 2 * Rp * 2 * F * q,
+        "gemm_w2_dgrad_swiglu_bwd": Eu * D * F * q + Rp * D * q + Rp * 2 * F * 2 + 2 * Rp * 2 * F * q,
         "gemm_w2_wgrad": D * Rp * q + F * Rp * q + E * D * F * 2,
-        "gemm_w13_dgrad": E * 2 * F * D * q + Rp * 2 * F * q + Rp * D * 2,
+        "gemm_w13_dgrad": Eu * 2 * F * D * q + Rp * 2 * F * q + Rp * D * 2,
         "gemm_w13_wgrad": 2 * F * Rp * q + D * Rp * q + E * 2 * F * D * 2,
         "reduce_dx": R * D * 2 + T * D * 2 * 2,
     }
@@ -389,7 +392,9 @@ def run_ours(args, rank, world):
             for n, v in zip(abi.BWD_STAGE_NAMES, abi.moe_ctx_stage_times(st.layer.ctx, 1)):
                 bwd_t[n].append(v)
     stage_ms = {k: statistics.mean(v) for k, v in list(fwd_t.items()) + list(bwd_t.items()) if v}
-    fb, bb = stage_bytes(w, rows_padded, routes, w.precision, st.train)
+    ids = np.asarray(st.ids_np)
+    used = int(np.unique(ids[(ids >= 0) & (ids < w.E)]).size)
+    fb, bb = stage_bytes(w, rows_padded, routes, w.precision, st.train, experts_used=used)
     sbytes = {**fb, **(bb if st.train else {})}
     dom = max(stage_ms, key=lambda k: stage_ms[k])
     achieved = sbytes[dom] / (stage_ms[dom] * 1e-3) / 1e9

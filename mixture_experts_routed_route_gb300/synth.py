@@ -68,6 +68,10 @@ WORKLOADS = {
     # weight gradients (1.4 GB for W13) still exceed L2
     "profile_e24": Workload("profile_e24", 128, 7168, 2048, 24, 6, "mxfp8", "zipf", inactive_frac=0.10,
                             zipf_s=1.2, train=True, seed=7),
+    # decode-sized steps (diagnostic): the e384 MXFP8 inference shapes with 1
+    # and 16 tokens, no shared expert; only the routed experts' weights stream
+    "decode_e384_t1": Workload("decode_e384_t1", 1, 7168, 2048, 384, 6, "mxfp8", "uniform", seed=9),
+    "decode_e384_t16": Workload("decode_e384_t16", 16, 7168, 2048, 384, 6, "mxfp8", "uniform", seed=10),
     # profiling case for the row-sized kernels (gathers, combine): the e384
     # token count and width (T=2048, D=7168, K=6, so about 12 K routed rows)
     # with 32 experts, about 10 GB on the device
