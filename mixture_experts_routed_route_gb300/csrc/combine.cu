@@ -81,19 +81,30 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
       }
-      for (int k = 0; k < K; ++k) {
-        const int r = inv[t * K + k];
-        if (r < 0) continue;
-        const float s = scores ? scores[t * K + k] : 1.0f;
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(h + static_cast<long long>(r) * D + c));
-        acc[0] = fmaf(s, bf16_lo(u.x), acc[0]);
-        acc[1] = fmaf(s, bf16_hi(u.x), acc[1]);
-        acc[2] = fmaf(s, bf16_lo(u.y), acc[2]);
-        acc[3] = fmaf(s, bf16_hi(u.y), acc[3]);
-        acc[4] = fmaf(s, bf16_lo(u.z), acc[4]);
-        acc[5] = fmaf(s, bf16_hi(u.z), acc[5]);
-        acc[6] = fmaf(s, bf16_lo(u.w), acc[6]);
-        acc[7] = fmaf(s, bf16_hi(u.w), acc[7]);
+      // up to 8 routes at a time: every row load in flight before the FMAs,
+      // which still run in ascending k (inactive routes skipped)
+      for (int k0 = 0; k0 < K; k0 += 8) {
+        int r[8];
+        uint4 u[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          r[j] = k0 + j < K ? inv[t * K + k0 + j] : -1;
+          u[j] = make_uint4(0, 0, 0, 0);
+          if (r[j] >= 0) u[j] = __ldg(reinterpret_cast<const uint4*>(h + static_cast<long long>(r[j]) * D + c));
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (r[j] < 0) continue;
+          const float s = scores ? scores[t * K + k0 + j] : 1.0f;
+          acc[0] = fmaf(s, bf16_lo(u[j].x), acc[0]);
+          acc[1] = fmaf(s, bf16_hi(u[j].x), acc[1]);
+          acc[2] = fmaf(s, bf16_lo(u[j].y), acc[2]);
+          acc[3] = fmaf(s, bf16_hi(u[j].y), acc[3]);
+          acc[4] = fmaf(s, bf16_lo(u[j].z), acc[4]);
+          acc[5] = fmaf(s, bf16_hi(u[j].z), acc[5]);
+          acc[6] = fmaf(s, bf16_lo(u[j].w), acc[6]);
+          acc[7] = fmaf(s, bf16_hi(u[j].w), acc[7]);
+        }
       }
       const uint4 xv = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                                   pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
