@@ -32,9 +32,9 @@ pytestmark = pytest.mark.gpu
 W = synth.WORKLOADS["ten_layer_graph"]
 
 
-def _layer_inputs(layer, round_):
-    """Seeded inputs of one layer for one replay round (round 1 = changed inputs)."""
-    w = synth.scaled(W, seed=W.seed + 100 * round_)
+def _layer_inputs(layer, replay):
+    """Seeded inputs of one layer for one replay (replay 1 = changed inputs)."""
+    w = synth.scaled(W, seed=W.seed + 100 * replay)
     s = synth.layer_zipf_s(w, layer)
     ids, scores = synth.make_routing(w, layer=layer, zipf_s=s)
     x = synth.make_tokens(w, "cpu", layer=layer)
@@ -61,7 +61,7 @@ def test_ten_layer_graph_changed_inputs():
     dW13 = torch.empty((E, 2 * F, D), dtype=torch.float32, device=dev)
     dW2 = torch.empty((E, D, F), dtype=torch.float32, device=dev)
 
-    def load_round(r):
+    def load_replay(r):
         host = [_layer_inputs(l, r) for l in range(L)]
         for l, (i, s, xx, yy) in enumerate(host):
             ids[l].copy_(torch.from_numpy(i))
@@ -77,7 +77,7 @@ def test_ten_layer_graph_changed_inputs():
             layer.backward(saved[l], dy[l], W13, W2, dx=dx[l], dW13=dW13, dW2=dW2, dw_fp32=True,
                            dw_accumulate=n > 0)
 
-    load_round(0)
+    load_replay(0)
     step()                                     # eager once: kernel attributes, warm-up
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
@@ -86,7 +86,7 @@ def test_ten_layer_graph_changed_inputs():
 
     rng = np.random.default_rng(77)
     for r in (0, 1):
-        host = load_round(r)
+        host = load_replay(r)
         graph.replay()
         torch.cuda.synchronize()
         assert layer.error_bits() == 0
