@@ -22,10 +22,11 @@
 //    [features, rows], so the contraction runs over the expert's row range.
 //
 // MXFP8 scales travel with the operand tiles: the TMA producer copies one
-// 512-byte scale atom per operand per stage into the stage's shared memory,
-// a scale warp moves them to tensor memory with tcgen05.cp and commits them
-// to the stage's sf_full barrier, and the MMA thread, which waits on that
-// barrier, issues the block-scaled MMAs.
+// 512-byte scale atom per operand per stage into the stage's shared memory
+// (the one-A-tile grouped-M GEMMs: four stages' atoms per copy, into a ring
+// of their own), a scale warp moves them to tensor memory with tcgen05.cp
+// and commits them to the stage's sf_full barrier, and the MMA thread,
+// which waits on that barrier, issues the block-scaled MMAs.
 //
 // Epilogues: fused SwiGLU forward (h1 -> h2 row/column bundles), plain BF16
 // store (h3, input-gradient rows), fused SwiGLU backward (dh2 -> dh1 row and
