@@ -1,0 +1,44 @@
+"""Host-side accounting of bench.py (no GPU): the algorithmic bytes a stage
+is charged and the oracle sample's bounds."""
+
+import numpy as np
+
+import bench
+from mixture_experts_routed_route_gb300 import synth
+
+
+def test_gemm_weight_bytes_count_only_routed_experts():
+    w = synth.WORKLOADS["e384_mxfp8_zipf_train"]
+    q = 1 + 1 / 32
+    Rp, R = 20000, 11059
+    full_f, full_b = bench.stage_bytes(w, Rp, R, w.precision, True)
+    used_f, used_b = bench.stage_bytes(w, Rp, R, w.precision, True, experts_used=381)
+    D, F = w.D, w.F
+    # the weight-streaming GEMMs lose exactly the three idle experts' weights
+    assert full_f["gemm_w13_swiglu"] - used_f["gemm_w13_swiglu"] == 3 * 2 * F * D * q
+    assert full_f["gemm_w2"] - used_f["gemm_w2"] == 3 * D * F * q
+    assert full_b["gemm_w13_dgrad"] - used_b["gemm_w13_dgrad"] == 3 * 2 * F * D * q
+    assert full_b["gemm_w2_dgrad_swiglu_bwd"] - used_b["gemm_w2_dgrad_swiglu_bwd"] == 3 * D * F * q
+    # the weight gradients still write every expert's dW (zeros for idle ones)
+    assert used_b["gemm_w13_wgrad"] == full_b["gemm_w13_wgrad"]
+    assert used_b["gemm_w2_wgrad"] == full_b["gemm_w2_wgrad"]
+    assert used_b["gemm_w13_wgrad"] >= w.E * 2 * F * D * 2
+
+
+def test_one_token_step_charges_six_experts():
+    w = synth.WORKLOADS["decode_e384_t1"]
+    ids, _ = synth.make_routing(w)
+    used = int(np.unique(np.asarray(ids)[np.asarray(ids) >= 0]).size)
+    assert used == w.K == 6
+    f, _ = bench.stage_bytes(w, 32 * used, used, w.precision, False, experts_used=used)
+    assert f["gemm_w13_swiglu"] < 0.2e9 and f["gemm_w2"] < 0.1e9
+
+
+def test_sample_experts_are_a_nested_seeded_prefix():
+    w = synth.WORKLOADS["e384_mxfp8_zipf_train"]
+    ids, _ = synth.make_routing(w)
+    a = bench.pick_sample_experts(w, ids, 6)
+    b = bench.pick_sample_experts(w, ids, 16)
+    assert b[:6] == a and len(set(b)) == 16
+    present = set(int(e) for e in np.asarray(ids).reshape(-1) if e >= 0)
+    assert set(b) <= present
