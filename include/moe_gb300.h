@@ -81,13 +81,24 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_MXFP8_1X32 = 2 } moe_precision;
 #define MOE_POST_NORM     0x4u  /* the layer ends with the post-expert RMSNorm
                                    (moe_ctx_set_post_norm); training saves the
                                    pre-norm output for moe_post_norm_backward */
+#define MOE_REPLAY        0x8u  /* (with MOE_TRAINING) the context also holds
+                                   the scratch a backward uses to rebuild the
+                                   expert state of a forward that saved only
+                                   its input (MOE_SAVE_INPUT_ONLY); see
+                                   "Activation slots" below                 */
 
 /* call_flags of moe_forward */
 #define MOE_ACCUMULATE_OUT 0x1u /* out = round(out + sum_k s*h3) (shared expert first) */
+#define MOE_SAVE_INPUT_ONLY 0x2u /* training: `saved` is an input-only state of
+                                    moe_saved_input_bytes (routing, scores, a
+                                    copy of x); needs a MOE_REPLAY context    */
 /* call_flags of moe_backward */
 #define MOE_ACCUMULATE_DX  0x1u /* dx  = round(dx + sum_k dxr)                 */
 #define MOE_DW_FP32        0x2u /* dW13/dW2 are float32 instead of BF16        */
 #define MOE_DW_ACCUMULATE  0x4u /* dW += new gradient (in the dW dtype)        */
+#define MOE_REPLAY_FORWARD 0x8u /* `saved` was written with MOE_SAVE_INPUT_ONLY:
+                                   rebuild the expert state first (must match
+                                   the forward's choice)                      */
 
 /*
  * Layer shape and precision.  The kernels tile D and F in steps of 128, so
@@ -184,9 +195,11 @@ MOE_API size_t moe_saved_state_bytes(const moe_config* cfg);
  * B_cap = (max_tokens*top_k + 31*E)/128 + E + 1 row blocks.
  */
 
-/* Saved-state fields, for inspection by tests (moe_saved_state_field).  The
- * routing fields come first in memory (HEADER..SCORES, BSTART, ROWBLOCK),
- * then H1, the column bundles and H3. */
+/* Saved-state fields, for inspection by tests (moe_saved_state_field,
+ * moe_saved_input_field).  The routing fields come first in memory
+ * (HEADER..SCORES, BSTART, ROWBLOCK), then PRENORM, then H1, the column
+ * bundles and H3 of a full state or X of an input-only state.  The routing
+ * fields and PRENORM sit at the same offsets in both layouts. */
 typedef enum {
   MOE_SAVED_HEADER = 0,     /* int32[16]: [0] T, [1] row blocks, [2] rows used, [3] active routes */
   MOE_SAVED_COUNTS = 1,     /* int32[E]     active routes per expert           */
@@ -207,7 +220,9 @@ typedef enum {
   MOE_SAVED_H3 = 15,        /* bf16[R_cap, D] route outputs (score gradient)   */
   MOE_SAVED_PRENORM = 16,   /* bf16[T_max, D] layer output before the post-expert
                                RMSNorm (MOE_POST_NORM only, else 0 bytes)     */
-  MOE_SAVED_NUM_FIELDS = 17
+  MOE_SAVED_X = 17,         /* bf16[T_max, D] the layer input x (input-only
+                               states; 0 bytes in a full state)               */
+  MOE_SAVED_NUM_FIELDS = 18
 } moe_saved_field;
 
 /* Offset and size in bytes of one saved-state field; the row capacity
@@ -256,6 +271,10 @@ MOE_API moe_status prepare_block_scaled_weight(const void* w, int32_t E, int32_t
  *                            first (one rounding at the end).
  *   saved      NULL for inference; for a training context, a buffer of
  *              moe_saved_state_bytes that the matching moe_backward reads.
+ *              With MOE_SAVE_INPUT_ONLY (MOE_REPLAY context) a buffer of
+ *              moe_saved_input_bytes instead: the forward keeps its routing,
+ *              scores and a copy of x there and nothing of the expert
+ *              state, which the backward rebuilds.
  * T may be 0 (nothing is enqueued).  T > max_tokens gives MOE_ERR_CAPACITY.
  */
 MOE_API moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* topk_ids,
@@ -280,6 +299,17 @@ MOE_API moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int
  *           ([BLOG] section 2 "SwiGLU backward": the routing-weight gradient
  *           of the weighted combine, which the caller's router backward
  *           consumes); 0 for inactive routes.
+ *   MOE_REPLAY_FORWARD: `saved` is an input-only state.  Before the steps
+ *           above the backward replays the forward's gather and W13 +
+ *           SwiGLU GEMM (and its W2 GEMM when d_scores is requested) on the
+ *           saved x and routing, writing the state into the context's
+ *           MOE_BUF_REPLAY scratch, and reads it from there.  The replayed
+ *           kernels and inputs are the forward's, so the gradients equal
+ *           those of a full-state backward bit for bit.  The flag must
+ *           match the forward's MOE_SAVE_INPUT_ONLY (moe_slot keeps it): the
+ *           context remembers, per `saved` pointer, the last of its
+ *           forwards that wrote there, and a mismatch returns
+ *           MOE_ERR_INVALID_ARG.
  */
 MOE_API moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout,
                         const moe_weight* W13, const moe_weight* W2, void* dx, void* dW13,
@@ -323,7 +353,9 @@ typedef enum {
   MOE_BUF_ERROR = 15,      /* uint32 error word                                */
   MOE_BUF_NORM = 16,       /* MOE_POST_NORM training: float r[T_max], then the
                               dgamma partial sums [ceil(T_max/64)][D]          */
-  MOE_BUF_NUM = 17
+  MOE_BUF_REPLAY = 17,     /* MOE_REPLAY: a full saved state (same layout) that
+                              a backward with MOE_REPLAY_FORWARD rebuilds       */
+  MOE_BUF_NUM = 18
 } moe_buffer;
 
 MOE_API moe_status moe_ctx_buffer(moe_ctx* ctx, int which, void** dev_ptr, size_t* bytes);
@@ -435,6 +467,62 @@ MOE_API moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t T, 
                                               const moe_weight* W13, const moe_weight* W2, void* out,
                                               uint32_t call_flags, uint32_t* device_error_word,
                                               cudaStream_t stream);
+
+/*
+ * Activation slots: several layers' saved states packed into one buffer,
+ * with save-or-replay decisions ("Dist-MoE: Speed-of-light distributed
+ * Mixture-of-Experts kernels", section 04 "Activation Packing and Dynamic
+ * Recompute").  The caller allocates one device buffer of `capacity` bytes;
+ * each training forward of a stack takes its saved state at
+ * base + offset from moe_slot_push, and the backwards, in reverse order,
+ * give the offsets back with moe_slot_pop.
+ *
+ * Decision for a layer with `remaining_layers` layers still to come after
+ * it in the slot, each of which needs `input_bytes` at least:
+ *   full  = full_bytes, input = input_bytes, each rounded up to 128 bytes
+ *           (for a layer of this library: moe_saved_state_bytes and
+ *           moe_saved_input_bytes of its configuration)
+ *   cursor + full + remaining_layers * input <= capacity
+ *       -> full state (forward call flags 0)
+ *   else cursor + input + remaining_layers * input <= capacity
+ *       -> input only (*forward_flags = MOE_SAVE_INPUT_ONLY; the backward
+ *          passes MOE_REPLAY_FORWARD and rebuilds the state)
+ *   else MOE_ERR_CAPACITY (the slot cannot keep every layer's input).
+ * The page's planner takes the decision on the device from the routed
+ * rows of the step; here the state sizes use the row capacity R_cap (the
+ * saved fields' addresses enter tensor maps encoded on the host), so a
+ * layer's decision depends only on its configuration and is the same on
+ * every step and every graph replay.
+ *
+ * moe_slot_init: capacity >= 0, 1 <= max_layers <= MOE_SLOT_MAX_LAYERS.
+ * moe_slot_push: errors MOE_ERR_INVALID_ARG (null pointer, negative or
+ *   above 2^50 byte counts, remaining_layers outside [0,
+ *   MOE_SLOT_MAX_LAYERS], a slot struct not in a state moe_slot_init and
+ *   push/pop leave), MOE_ERR_CAPACITY (no room, or max_layers layers already
+ *   in the slot).  An input-only layer needs a MOE_REPLAY context.
+ * moe_slot_pop: `offset` must be the most recent push still in the slot
+ *   (MOE_ERR_INVALID_ARG otherwise); the cursor returns to it.
+ * Host-only bookkeeping: no CUDA call, no device access.
+ */
+#define MOE_SLOT_MAX_LAYERS 64
+typedef struct {
+  int64_t capacity;                      /* bytes of the slot buffer           */
+  int64_t cursor;                        /* next free byte (multiple of 128)   */
+  int32_t layers;                        /* saved states now in the slot       */
+  int32_t max_layers;                    /* bound on `layers`                   */
+  int64_t offset[MOE_SLOT_MAX_LAYERS];   /* offset of each stacked state        */
+  uint32_t flags[MOE_SLOT_MAX_LAYERS];   /* its forward call flags              */
+} moe_slot;
+
+/* Bytes of an input-only saved state (routing fields, scores, the
+ * pre-norm output under MOE_POST_NORM, and x) and one field's place in it. */
+MOE_API size_t moe_saved_input_bytes(const moe_config* cfg);
+MOE_API moe_status moe_saved_input_field(const moe_config* cfg, int field, size_t* offset, size_t* bytes);
+
+MOE_API moe_status moe_slot_init(moe_slot* slot, int64_t capacity, int32_t max_layers);
+MOE_API moe_status moe_slot_push(moe_slot* slot, int64_t full_bytes, int64_t input_bytes, int32_t remaining_layers,
+                                 int64_t* offset, uint32_t* forward_flags);
+MOE_API moe_status moe_slot_pop(moe_slot* slot, int64_t offset);
 
 /* Library version string. */
 MOE_API const char* moe_version(void);

@@ -35,22 +35,27 @@ MOE_MXFP8_1X32 = 2    # weight preparation only: 1x32 inference blocks
 MOE_TRAINING = 0x1
 MOE_DEBUG_CHECKS = 0x2
 MOE_POST_NORM = 0x4
+MOE_REPLAY = 0x8
 MOE_ACCUMULATE_OUT = 0x1
+MOE_SAVE_INPUT_ONLY = 0x2
 MOE_ACCUMULATE_DX = 0x1
 MOE_DW_FP32 = 0x2
 MOE_DW_ACCUMULATE = 0x4
+MOE_REPLAY_FORWARD = 0x8
 
 # moe_saved_field
 (MOE_SAVED_HEADER, MOE_SAVED_COUNTS, MOE_SAVED_OFFSETS, MOE_SAVED_POFFSETS, MOE_SAVED_PERM, MOE_SAVED_INV,
  MOE_SAVED_BLOCKS, MOE_SAVED_SCORES, MOE_SAVED_H1, MOE_SAVED_XCOL, MOE_SAVED_XCOL_SCALE, MOE_SAVED_H2COL,
- MOE_SAVED_H2COL_SCALE, MOE_SAVED_BSTART, MOE_SAVED_ROWBLOCK, MOE_SAVED_H3, MOE_SAVED_PRENORM) = range(17)
-MOE_SAVED_NUM_FIELDS = 17
+ MOE_SAVED_H2COL_SCALE, MOE_SAVED_BSTART, MOE_SAVED_ROWBLOCK, MOE_SAVED_H3, MOE_SAVED_PRENORM,
+ MOE_SAVED_X) = range(18)
+MOE_SAVED_NUM_FIELDS = 18
 
 # moe_buffer
 (MOE_BUF_XROW, MOE_BUF_XROW_SCALE, MOE_BUF_H2ROW, MOE_BUF_H2ROW_SCALE, MOE_BUF_H3, MOE_BUF_DH3ROW,
  MOE_BUF_DH3ROW_SCALE, MOE_BUF_DH3COL, MOE_BUF_DH3COL_SCALE, MOE_BUF_DH1ROW, MOE_BUF_DH1ROW_SCALE,
- MOE_BUF_DH1COL, MOE_BUF_DH1COL_SCALE, MOE_BUF_DXR, MOE_BUF_ROUTING, MOE_BUF_ERROR, MOE_BUF_NORM) = range(17)
-MOE_BUF_NUM = 17
+ MOE_BUF_DH1COL, MOE_BUF_DH1COL_SCALE, MOE_BUF_DXR, MOE_BUF_ROUTING, MOE_BUF_ERROR, MOE_BUF_NORM,
+ MOE_BUF_REPLAY) = range(18)
+MOE_BUF_NUM = 18
 
 
 class moe_config(ctypes.Structure):
@@ -63,6 +68,15 @@ class moe_weight(ctypes.Structure):
     _fields_ = [("precision", ctypes.c_int), ("E", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32),
                 ("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("data_t", ctypes.c_void_p),
                 ("scale_t", ctypes.c_void_p)]
+
+
+MOE_SLOT_MAX_LAYERS = 64
+
+
+class moe_slot(ctypes.Structure):
+    _fields_ = [("capacity", ctypes.c_int64), ("cursor", ctypes.c_int64), ("layers", ctypes.c_int32),
+                ("max_layers", ctypes.c_int32), ("offset", ctypes.c_int64 * MOE_SLOT_MAX_LAYERS),
+                ("flags", ctypes.c_uint32 * MOE_SLOT_MAX_LAYERS)]
 
 
 class MoEError(RuntimeError):
@@ -98,6 +112,13 @@ _SIGNATURES = {
     "moe_ctx_set_max_ctas": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_ctx_set_post_norm": (ctypes.c_int, [_P, _P, ctypes.c_float]),
     "moe_post_norm_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
+    "moe_saved_input_bytes": (ctypes.c_size_t, [ctypes.POINTER(moe_config)]),
+    "moe_saved_input_field": (ctypes.c_int, [ctypes.POINTER(moe_config), ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]),
+    "moe_slot_init": (ctypes.c_int, [ctypes.POINTER(moe_slot), ctypes.c_int64, ctypes.c_int32]),
+    "moe_slot_push": (ctypes.c_int, [ctypes.POINTER(moe_slot), ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                     ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_slot_pop": (ctypes.c_int, [ctypes.POINTER(moe_slot), ctypes.c_int64]),
     "moe_forward_static_scratch": (ctypes.c_int, [ctypes.POINTER(moe_config), ctypes.c_int32, _P, _P, _P,
                                                   ctypes.POINTER(moe_weight), ctypes.POINTER(moe_weight), _P,
                                                   ctypes.c_uint32, _P, _P]),
@@ -173,6 +194,36 @@ def moe_saved_state_field(cfg, field):
     _check("moe_saved_state_field", LIB.moe_saved_state_field(ctypes.byref(cfg), field, ctypes.byref(off),
                                                               ctypes.byref(nb)))
     return off.value, nb.value
+
+
+def moe_saved_input_bytes(cfg):
+    return LIB.moe_saved_input_bytes(ctypes.byref(cfg))
+
+
+def moe_saved_input_field(cfg, field):
+    off, nb = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("moe_saved_input_field", LIB.moe_saved_input_field(ctypes.byref(cfg), field, ctypes.byref(off),
+                                                              ctypes.byref(nb)))
+    return off.value, nb.value
+
+
+def moe_slot_init(capacity, max_layers):
+    """A new moe_slot of `capacity` bytes holding at most `max_layers` states."""
+    slot = moe_slot()
+    _check("moe_slot_init", LIB.moe_slot_init(ctypes.byref(slot), capacity, max_layers))
+    return slot
+
+
+def moe_slot_push(slot, full_bytes, input_bytes, remaining_layers):
+    """(offset, forward call flags) of the next layer's saved state."""
+    off, fl = ctypes.c_int64(), ctypes.c_uint32()
+    _check("moe_slot_push", LIB.moe_slot_push(ctypes.byref(slot), full_bytes, input_bytes, remaining_layers,
+                                              ctypes.byref(off), ctypes.byref(fl)))
+    return off.value, fl.value
+
+
+def moe_slot_pop(slot, offset):
+    _check("moe_slot_pop", LIB.moe_slot_pop(ctypes.byref(slot), offset))
 
 
 def moe_ctx_scratch_bytes(cfg):

@@ -5,6 +5,8 @@
 //   route -> gather x (row bundle; + column bundle when training)
 //   -> W13 GEMM with fused SwiGLU -> W2 GEMM -> combine.
 // Backward:
+//   [replay: gather x -> W13 GEMM (-> W2 GEMM) into the context's replay
+//   scratch, for a forward that saved only its input]
 //   dh3 gather (row + column bundles) -> W2 DGRAD with fused SwiGLU backward
 //   -> W2 WGRAD -> W13 DGRAD -> W13 WGRAD -> K-reduction of dX.
 #include <cudaTypedefs.h>
@@ -12,6 +14,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "kernels.cuh"
 #include "moe_gb300.h"
@@ -37,6 +40,9 @@ struct moe_ctx {
   bool events;          // the stage events exist (created once, destroyed with the context)
   cudaEvent_t ev[2][8];
   uint64_t launches;
+  // saved-state pointer -> written input-only (MOE_SAVE_INPUT_ONLY) by the
+  // last forward of this context that wrote there
+  std::unordered_map<const void*, bool> saved_input_only;
 };
 
 namespace {
@@ -76,7 +82,10 @@ struct SavedLayout {
   size_t total;
 };
 
-SavedLayout saved_layout(const moe_config* c) {
+// The full state (input_only false) or the input-only state a forward with
+// MOE_SAVE_INPUT_ONLY writes: the same routing fields and PRENORM at the
+// same offsets, then the expert state or the copy of x.
+SavedLayout saved_layout(const moe_config* c, bool input_only = false) {
   SavedLayout L{};
   const int64_t R = row_cap(c), B = block_cap(c);
   const int64_t E = c->num_experts, TK = static_cast<int64_t>(c->max_tokens) * c->top_k;
@@ -101,12 +110,18 @@ SavedLayout saved_layout(const moe_config* c) {
   sz[MOE_SAVED_H2COL_SCALE] = mx ? (F / 128) * B * 512 : 0;
   sz[MOE_SAVED_H3] = R * D * 2;
   sz[MOE_SAVED_PRENORM] = (c->flags & MOE_POST_NORM) ? static_cast<int64_t>(c->max_tokens) * D * 2 : 0;
+  if (input_only) {
+    for (int f : {MOE_SAVED_H1, MOE_SAVED_XCOL, MOE_SAVED_XCOL_SCALE, MOE_SAVED_H2COL, MOE_SAVED_H2COL_SCALE,
+                  MOE_SAVED_H3})
+      sz[f] = 0;
+    sz[MOE_SAVED_X] = static_cast<int64_t>(c->max_tokens) * D * 2;
+  }
   // routing fields first (the inference copy in the context holds just these)
   static const int order[MOE_SAVED_NUM_FIELDS] = {
-      MOE_SAVED_HEADER, MOE_SAVED_COUNTS, MOE_SAVED_OFFSETS, MOE_SAVED_POFFSETS, MOE_SAVED_PERM,
-      MOE_SAVED_INV,    MOE_SAVED_BLOCKS, MOE_SAVED_SCORES,  MOE_SAVED_BSTART,   MOE_SAVED_ROWBLOCK,
-      MOE_SAVED_H1,     MOE_SAVED_XCOL,   MOE_SAVED_XCOL_SCALE, MOE_SAVED_H2COL, MOE_SAVED_H2COL_SCALE,
-      MOE_SAVED_H3,     MOE_SAVED_PRENORM};
+      MOE_SAVED_HEADER,   MOE_SAVED_COUNTS, MOE_SAVED_OFFSETS, MOE_SAVED_POFFSETS,   MOE_SAVED_PERM,
+      MOE_SAVED_INV,      MOE_SAVED_BLOCKS, MOE_SAVED_SCORES,  MOE_SAVED_BSTART,     MOE_SAVED_ROWBLOCK,
+      MOE_SAVED_PRENORM,  MOE_SAVED_H1,     MOE_SAVED_XCOL,    MOE_SAVED_XCOL_SCALE, MOE_SAVED_H2COL,
+      MOE_SAVED_H2COL_SCALE, MOE_SAVED_H3,  MOE_SAVED_X};
   size_t off = 0;
   for (int k = 0; k < MOE_SAVED_NUM_FIELDS; ++k) {
     const int i = order[k];
@@ -153,6 +168,7 @@ ScratchLayout scratch_layout(const moe_config* c) {
     const int64_t Tm = c->max_tokens;
     sz[MOE_BUF_NORM] = (Tm + (Tm + kPostNormSlab - 1) / kPostNormSlab * D) * sizeof(float);
   }
+  if (train && (c->flags & MOE_REPLAY)) sz[MOE_BUF_REPLAY] = saved_layout(c).total;
   sz[MOE_BUF_ROUTING] = saved_layout(c).routing_bytes;
   sz[MOE_BUF_ERROR] = 32;   // error word at 0, clip counters at 16
   size_t off = 0;
@@ -311,6 +327,12 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
     if (_e != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
+#define MOE_PASS(x)                         \
+  do {                                      \
+    const moe_status _s = (x);              \
+    if (_s != MOE_OK) return _s;            \
+  } while (0)
+
 // need_t: the backward's transposed copy is needed (which a 1x32 inference
 // weight does not have); an MXFP8 context's forward also takes 1x32 weights.
 bool weight_ok(const moe_weight* w, moe_precision prec, int E, int N, int K, bool need_t) {
@@ -338,6 +360,123 @@ cudaError_t stage_mark(moe_ctx* c, int pass, int idx, cudaStream_t s) {
   return cudaEventRecord(c->ev[pass][idx], s);
 }
 
+// Gather x (the row bundle; with `act`, also the column bundle into act's
+// XCOL fields) and run the W13 + SwiGLU GEMM (with `act`, h1 and the h2
+// column bundle into act's fields).  `act` is a full saved state (a
+// training forward's, or the context's replay scratch) or null (inference,
+// input-only states).  `marks`: record the forward's stage events and count
+// clip statistics (off when a backward replays these stages).
+moe_status run_gather_w13(moe_ctx* ctx, const void* x, const RoutingPtrs& rp, const moe_weight* W13, uint8_t* act,
+                          const SavedLayout& SL, bool marks, int sms, cudaStream_t stream) {
+  const moe_config& c = ctx->cfg;
+  const int D = c.d_model, F = c.d_ff, E = c.num_experts, K = c.top_k;
+  const bool mx = c.precision == MOE_MXFP8;
+  const int64_t R = ctx->r_cap;
+  if (act) {
+    // row bundle (W13 operand) and column bundle (W13 WGRAD operand) in one pass
+    CUtensorMap tr, tc;
+    if (mx && (!make_tmap(&tr, B(ctx, MOE_BUF_XROW), true, R, D, 128) ||
+               !make_tmap(&tc, act + SL.off[MOE_SAVED_XCOL], true, D, R, 128)))
+      return MOE_ERR_CUDA;
+    MOE_TRY(launch_gather_both(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
+                               act + SL.off[MOE_SAVED_XCOL], mx ? act + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr,
+                               static_cast<int>(R), static_cast<int>(ctx->b_cap), sms, stream, &tr, &tc));
+  } else {
+    MOE_TRY(launch_gather_rows(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
+                               static_cast<int>(R), sms, stream));
+  }
+  ctx->launches += 1;
+  if (marks) MOE_TRY(stage_mark(ctx, 0, 2, stream));
+
+  // ---- W13 + SwiGLU
+  GemmLaunch g1{};
+  g1.mx = mx;
+  g1.na = 2;
+  g1.epi = kEpiSwigluFwd;
+  g1.mode = kGroupedM;
+  if (!make_tmap(&g1.tmA, W13->data, mx, static_cast<int64_t>(E) * 2 * F, D, 128) ||
+      !make_tmap(&g1.tmB, B(ctx, MOE_BUF_XROW), mx, R, D, 32) ||
+      !make_grouped_m_boxes(&g1, W13->data, static_cast<int64_t>(E) * 2 * F, W13->scale, B(ctx, MOE_BUF_XROW), R,
+                            mx, D, F))
+    return MOE_ERR_CUDA;
+  GemmParams& p1 = g1.p;
+  p1.hdr = rp.hdr;
+  p1.blocks = rp.blocks;
+  p1.poffsets = rp.poffsets;
+  p1.E = E;
+  p1.b_box_rows = 32;
+  p1.n_tiles = F / 128;
+  p1.K = D;
+  p1.a_rows_per_expert = 2 * F;
+  p1.a_up_offset = F;
+  p1.sfa = W13->scale;
+  p1.sfa_ts = D / 128;
+  p1.sfb = B(ctx, MOE_BUF_XROW_SCALE);
+  p1.sfb_ts = D / 128;
+  p1.out0 = B(ctx, MOE_BUF_H2ROW);
+  p1.out0_pitch = F;
+  p1.out0_sf = B(ctx, MOE_BUF_H2ROW_SCALE);
+  p1.out0_sf_kg = F / 128;
+  p1.b_cap = static_cast<int>(ctx->b_cap);
+  if (act) {
+    p1.out1 = act + SL.off[MOE_SAVED_H2COL];
+    p1.out1_pitch = R;
+    p1.out1_sf = mx ? act + SL.off[MOE_SAVED_H2COL_SCALE] : nullptr;
+    p1.h1 = reinterpret_cast<__nv_bfloat16*>(act + SL.off[MOE_SAVED_H1]);
+    p1.h1_pitch = 2 * F;
+  }
+  p1.F = F;
+  p1.save_h1 = act ? 1 : 0;
+  p1.want_col = act ? 1 : 0;
+  p1.swiglu_limit = c.swiglu_limit;
+  p1.clip = (marks && c.swiglu_limit > 0.0f) ? ctx->clip : nullptr;   // a replay counts no clips again
+  p1.err = ctx->err;
+  g1.max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
+  MOE_TRY(launch_gemm(g1, sms, stream));
+  ctx->launches += 1;
+  if (marks) MOE_TRY(stage_mark(ctx, 0, 3, stream));
+  return MOE_OK;
+}
+
+// The W2 GEMM: h3 = h2 W2[e]^T from the h2 row bundle in scratch.
+moe_status run_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uint8_t* h3, int sms,
+                  cudaStream_t stream) {
+  const moe_config& c = ctx->cfg;
+  const int D = c.d_model, F = c.d_ff, E = c.num_experts;
+  const bool mx = c.precision == MOE_MXFP8;
+  const int64_t R = ctx->r_cap;
+  // ---- W2
+  GemmLaunch g2{};
+  g2.mx = mx;
+  g2.na = pair_tiles(D);
+  g2.epi = kEpiStore;
+  g2.mode = kGroupedM;
+  if (!make_tmap(&g2.tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128) ||
+      !make_tmap(&g2.tmB, B(ctx, MOE_BUF_H2ROW), mx, R, F, 32) ||
+      !make_grouped_m_boxes(&g2, W2->data, static_cast<int64_t>(E) * D, W2->scale, B(ctx, MOE_BUF_H2ROW), R, mx, F))
+    return MOE_ERR_CUDA;
+  GemmParams& p2 = g2.p;
+  p2.hdr = rp.hdr;
+  p2.blocks = rp.blocks;
+  p2.poffsets = rp.poffsets;
+  p2.E = E;
+  p2.b_box_rows = 32;
+  p2.n_tiles = D / (128 * g2.na);
+  p2.K = F;
+  p2.a_rows_per_expert = D;
+  p2.sfa = W2->scale;
+  p2.sfa_ts = F / 128;
+  p2.sfb = B(ctx, MOE_BUF_H2ROW_SCALE);
+  p2.sfb_ts = F / 128;
+  p2.out0 = h3;
+  p2.out0_pitch = D;
+  p2.F = F;
+  p2.err = ctx->err;
+  g2.max_tiles = static_cast<int>(ctx->b_cap * p2.n_tiles);
+  MOE_TRY(launch_gemm(g2, sms, stream));
+  ctx->launches += 1;
+  return MOE_OK;
+}
 }  // namespace
 
 // =================================================================== ABI
@@ -359,10 +498,73 @@ moe_status moe_saved_state_field(const moe_config* cfg, int field, size_t* offse
   return MOE_OK;
 }
 
+size_t moe_saved_input_bytes(const moe_config* cfg) { return config_ok(cfg) ? saved_layout(cfg, true).total : 0; }
+
+moe_status moe_saved_input_field(const moe_config* cfg, int field, size_t* offset, size_t* bytes) {
+  if (!config_ok(cfg) || field < 0 || field >= MOE_SAVED_NUM_FIELDS || !offset || !bytes)
+    return MOE_ERR_INVALID_ARG;
+  const SavedLayout L = saved_layout(cfg, true);
+  *offset = L.off[field];
+  *bytes = L.size[field];
+  return MOE_OK;
+}
+
+// ---- activation slots: host bookkeeping of the save-or-replay decisions
+
+moe_status moe_slot_init(moe_slot* slot, int64_t capacity, int32_t max_layers) {
+  if (!slot || capacity < 0 || max_layers < 1 || max_layers > MOE_SLOT_MAX_LAYERS) return MOE_ERR_INVALID_ARG;
+  std::memset(slot, 0, sizeof(*slot));
+  slot->capacity = capacity;
+  slot->max_layers = max_layers;
+  return MOE_OK;
+}
+
+moe_status moe_slot_push(moe_slot* slot, int64_t full_bytes, int64_t input_bytes, int32_t remaining_layers,
+                         int64_t* offset, uint32_t* forward_flags) {
+  if (!slot || !offset || !forward_flags || full_bytes < 0 || input_bytes < 0 || remaining_layers < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (full_bytes > (int64_t{1} << 50) || input_bytes > (int64_t{1} << 50) || remaining_layers > MOE_SLOT_MAX_LAYERS)
+    return MOE_ERR_INVALID_ARG;   // keeps the sums below far from overflow
+  if (slot->layers < 0 || slot->max_layers < 1 || slot->max_layers > MOE_SLOT_MAX_LAYERS ||
+      slot->layers > slot->max_layers || slot->cursor < 0 || slot->cursor > slot->capacity)
+    return MOE_ERR_INVALID_ARG;
+  if (slot->layers == slot->max_layers) return MOE_ERR_CAPACITY;
+  const int64_t full = static_cast<int64_t>(align_up(static_cast<size_t>(full_bytes), 128));
+  const int64_t input = static_cast<int64_t>(align_up(static_cast<size_t>(input_bytes), 128));
+  const int64_t reserve = static_cast<int64_t>(remaining_layers) * input;   // the later layers' inputs
+  int64_t take;
+  uint32_t flags;
+  if (slot->cursor + full + reserve <= slot->capacity) {
+    take = full;
+    flags = 0;
+  } else if (slot->cursor + input + reserve <= slot->capacity) {
+    take = input;
+    flags = MOE_SAVE_INPUT_ONLY;
+  } else {
+    return MOE_ERR_CAPACITY;
+  }
+  slot->offset[slot->layers] = slot->cursor;
+  slot->flags[slot->layers] = flags;
+  slot->layers += 1;
+  *offset = slot->cursor;
+  *forward_flags = flags;
+  slot->cursor += take;
+  return MOE_OK;
+}
+
+moe_status moe_slot_pop(moe_slot* slot, int64_t offset) {
+  if (!slot || slot->layers < 1 || slot->layers > MOE_SLOT_MAX_LAYERS) return MOE_ERR_INVALID_ARG;
+  if (slot->offset[slot->layers - 1] != offset) return MOE_ERR_INVALID_ARG;   // not the most recent push
+  slot->layers -= 1;
+  slot->cursor = offset;
+  return MOE_OK;
+}
+
 size_t moe_ctx_scratch_bytes(const moe_config* cfg) { return config_ok(cfg) ? scratch_layout(cfg).total : 0; }
 
 moe_status moe_ctx_create(const moe_config* cfg, moe_ctx** out) {
   if (!out || !config_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  if ((cfg->flags & MOE_REPLAY) && !(cfg->flags & MOE_TRAINING)) return MOE_ERR_INVALID_ARG;
   if (!config_tileable(cfg)) return MOE_ERR_UNSUPPORTED;
   if (!encode_fn()) return MOE_ERR_CUDA;
   moe_ctx* c = new moe_ctx();
@@ -523,20 +725,25 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (T > c.max_tokens) return MOE_ERR_CAPACITY;
   const int D = c.d_model, F = c.d_ff, E = c.num_experts, K = c.top_k;
-  const bool mx = c.precision == MOE_MXFP8;
   const bool train = saved != nullptr;
   if (train && !(c.flags & MOE_TRAINING)) return MOE_ERR_INVALID_ARG;
   if (!weight_ok(W13, c.precision, E, 2 * F, D, false) || !weight_ok(W2, c.precision, E, D, F, false))
     return MOE_ERR_INVALID_ARG;
+  if (call_flags & ~(MOE_ACCUMULATE_OUT | MOE_SAVE_INPUT_ONLY)) return MOE_ERR_INVALID_ARG;
+  const bool input_only = (call_flags & MOE_SAVE_INPUT_ONLY) != 0;
+  if (input_only && (!train || !(c.flags & MOE_REPLAY))) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !topk_ids || !topk_scores || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(out) || (saved && !aligned16(saved))) return MOE_ERR_INVALID_ARG;
-  if (call_flags & ~MOE_ACCUMULATE_OUT) return MOE_ERR_INVALID_ARG;
   const bool norm = (c.flags & MOE_POST_NORM) != 0;
   if (norm && !ctx->norm_gamma) return MOE_ERR_INVALID_ARG;
 
-  const SavedLayout SL = saved_layout(&c);
+  const SavedLayout SL = saved_layout(&c, input_only);
   uint8_t* sv = static_cast<uint8_t*>(saved);
+  if (train) ctx->saved_input_only[saved] = input_only;
+  if (input_only)   // the backward replays from this copy of x
+    MOE_TRY(cudaMemcpyAsync(sv + SL.off[MOE_SAVED_X], x, static_cast<size_t>(T) * D * 2, cudaMemcpyDeviceToDevice,
+                            stream));
   const RoutingPtrs rp = routing_ptrs(train ? sv : B(ctx, MOE_BUF_ROUTING), SL);
   const int64_t R = ctx->r_cap;
   const int sms = ctx->max_ctas > 0 ? std::min(ctx->max_ctas, ctx->num_sms) : ctx->num_sms;
@@ -546,101 +753,10 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
                        rp, ctx->err, stream));
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 0, 1, stream));
-  if (train) {
-    // row bundle (W13 operand) and column bundle (W13 WGRAD operand) in one pass
-    CUtensorMap tr, tc;
-    if (mx && (!make_tmap(&tr, B(ctx, MOE_BUF_XROW), true, R, D, 128) ||
-               !make_tmap(&tc, sv + SL.off[MOE_SAVED_XCOL], true, D, R, 128)))
-      return MOE_ERR_CUDA;
-    MOE_TRY(launch_gather_both(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
-                               sv + SL.off[MOE_SAVED_XCOL], mx ? sv + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr,
-                               static_cast<int>(R), static_cast<int>(ctx->b_cap), sms, stream, &tr, &tc));
-  } else {
-    MOE_TRY(launch_gather_rows(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
-                               static_cast<int>(R), sms, stream));
-  }
-  ctx->launches += 1;
-  MOE_TRY(stage_mark(ctx, 0, 2, stream));
-
-  // ---- W13 + SwiGLU
-  GemmLaunch g1{};
-  g1.mx = mx;
-  g1.na = 2;
-  g1.epi = kEpiSwigluFwd;
-  g1.mode = kGroupedM;
-  if (!make_tmap(&g1.tmA, W13->data, mx, static_cast<int64_t>(E) * 2 * F, D, 128) ||
-      !make_tmap(&g1.tmB, B(ctx, MOE_BUF_XROW), mx, R, D, 32) ||
-      !make_grouped_m_boxes(&g1, W13->data, static_cast<int64_t>(E) * 2 * F, W13->scale, B(ctx, MOE_BUF_XROW), R,
-                            mx, D, F))
-    return MOE_ERR_CUDA;
-  GemmParams& p1 = g1.p;
-  p1.hdr = rp.hdr;
-  p1.blocks = rp.blocks;
-  p1.poffsets = rp.poffsets;
-  p1.E = E;
-  p1.b_box_rows = 32;
-  p1.n_tiles = F / 128;
-  p1.K = D;
-  p1.a_rows_per_expert = 2 * F;
-  p1.a_up_offset = F;
-  p1.sfa = W13->scale;
-  p1.sfa_ts = D / 128;
-  p1.sfb = B(ctx, MOE_BUF_XROW_SCALE);
-  p1.sfb_ts = D / 128;
-  p1.out0 = B(ctx, MOE_BUF_H2ROW);
-  p1.out0_pitch = F;
-  p1.out0_sf = B(ctx, MOE_BUF_H2ROW_SCALE);
-  p1.out0_sf_kg = F / 128;
-  p1.b_cap = static_cast<int>(ctx->b_cap);
-  if (train) {
-    p1.out1 = sv + SL.off[MOE_SAVED_H2COL];
-    p1.out1_pitch = R;
-    p1.out1_sf = mx ? sv + SL.off[MOE_SAVED_H2COL_SCALE] : nullptr;
-    p1.h1 = reinterpret_cast<__nv_bfloat16*>(sv + SL.off[MOE_SAVED_H1]);
-    p1.h1_pitch = 2 * F;
-  }
-  p1.F = F;
-  p1.save_h1 = train ? 1 : 0;
-  p1.want_col = train ? 1 : 0;
-  p1.swiglu_limit = c.swiglu_limit;
-  p1.clip = c.swiglu_limit > 0.0f ? ctx->clip : nullptr;
-  p1.err = ctx->err;
-  g1.max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
-  MOE_TRY(launch_gemm(g1, sms, stream));
-  ctx->launches += 1;
-  MOE_TRY(stage_mark(ctx, 0, 3, stream));
-
-  // ---- W2
-  GemmLaunch g2{};
-  g2.mx = mx;
-  g2.na = pair_tiles(D);
-  g2.epi = kEpiStore;
-  g2.mode = kGroupedM;
-  if (!make_tmap(&g2.tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128) ||
-      !make_tmap(&g2.tmB, B(ctx, MOE_BUF_H2ROW), mx, R, F, 32) ||
-      !make_grouped_m_boxes(&g2, W2->data, static_cast<int64_t>(E) * D, W2->scale, B(ctx, MOE_BUF_H2ROW), R, mx, F))
-    return MOE_ERR_CUDA;
-  GemmParams& p2 = g2.p;
-  p2.hdr = rp.hdr;
-  p2.blocks = rp.blocks;
-  p2.poffsets = rp.poffsets;
-  p2.E = E;
-  p2.b_box_rows = 32;
-  p2.n_tiles = D / (128 * g2.na);
-  p2.K = F;
-  p2.a_rows_per_expert = D;
-  p2.sfa = W2->scale;
-  p2.sfa_ts = F / 128;
-  p2.sfb = B(ctx, MOE_BUF_H2ROW_SCALE);
-  p2.sfb_ts = F / 128;
-  uint8_t* h3 = train ? sv + SL.off[MOE_SAVED_H3] : B(ctx, MOE_BUF_H3);   // saved for the score gradient
-  p2.out0 = h3;
-  p2.out0_pitch = D;
-  p2.F = F;
-  p2.err = ctx->err;
-  g2.max_tiles = static_cast<int>(ctx->b_cap * p2.n_tiles);
-  MOE_TRY(launch_gemm(g2, sms, stream));
-  ctx->launches += 1;
+  uint8_t* act = (train && !input_only) ? sv : nullptr;   // where the expert state is saved
+  MOE_PASS(run_gather_w13(ctx, x, rp, W13, act, SL, true, sms, stream));
+  uint8_t* h3 = act ? act + SL.off[MOE_SAVED_H3] : B(ctx, MOE_BUF_H3);   // saved for the score gradient
+  MOE_PASS(run_w2(ctx, rp, W2, h3, sms, stream));
   MOE_TRY(stage_mark(ctx, 0, 4, stream));
 
   // ---- combine
@@ -664,15 +780,32 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(saved) || !aligned16(dout) || !aligned16(dx) || !aligned16(dW13) || !aligned16(dW2))
     return MOE_ERR_INVALID_ARG;
-  if (call_flags & ~(MOE_ACCUMULATE_DX | MOE_DW_FP32 | MOE_DW_ACCUMULATE)) return MOE_ERR_INVALID_ARG;
+  if (call_flags & ~(MOE_ACCUMULATE_DX | MOE_DW_FP32 | MOE_DW_ACCUMULATE | MOE_REPLAY_FORWARD))
+    return MOE_ERR_INVALID_ARG;
+  const bool replay = (call_flags & MOE_REPLAY_FORWARD) != 0;
+  if (replay && !(c.flags & MOE_REPLAY)) return MOE_ERR_INVALID_ARG;
+  const auto known = ctx->saved_input_only.find(saved);
+  if (known != ctx->saved_input_only.end() && known->second != replay) return MOE_ERR_INVALID_ARG;
 
-  const SavedLayout SL = saved_layout(&c);
+  const SavedLayout SL = saved_layout(&c);   // the expert-state fields (in `sa`)
   uint8_t* sv = static_cast<uint8_t*>(const_cast<void*>(saved));
-  const RoutingPtrs rp = routing_ptrs(sv, SL);
+  const RoutingPtrs rp = routing_ptrs(sv, SL);   // same offsets in an input-only state
   const int64_t R = ctx->r_cap;
   const int sms = ctx->max_ctas > 0 ? std::min(ctx->max_ctas, ctx->num_sms) : ctx->num_sms;
   const int dw_fp32 = (call_flags & MOE_DW_FP32) ? 1 : 0;
   const int dw_acc = (call_flags & MOE_DW_ACCUMULATE) ? 1 : 0;
+
+  // ---- replay: rebuild the expert state of an input-only forward from its
+  // saved x and routing, with the forward's own kernels, in the context's
+  // replay scratch ([DM] section 04: the backward republishes x and rebuilds
+  // the expert state in scratch)
+  uint8_t* sa = sv;
+  if (replay) {
+    sa = B(ctx, MOE_BUF_REPLAY);
+    const SavedLayout SI = saved_layout(&c, true);
+    MOE_PASS(run_gather_w13(ctx, sv + SI.off[MOE_SAVED_X], rp, W13, sa, SL, false, sms, stream));
+    if (d_scores) MOE_PASS(run_w2(ctx, rp, W2, sa + SL.off[MOE_SAVED_H3], sms, stream));
+  }
 
   // ---- dh3 = s * dY: row bundle (W2 DGRAD) and column bundle (W2 WGRAD)
   MOE_TRY(stage_mark(ctx, 1, 0, stream));
@@ -710,7 +843,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p1.sfa_ts = D / 128;
   p1.sfb = B(ctx, MOE_BUF_DH3ROW_SCALE);
   p1.sfb_ts = D / 128;
-  p1.h1 = reinterpret_cast<__nv_bfloat16*>(sv + SL.off[MOE_SAVED_H1]);
+  p1.h1 = reinterpret_cast<__nv_bfloat16*>(sa + SL.off[MOE_SAVED_H1]);
   p1.h1_pitch = 2 * F;
   p1.out0 = B(ctx, MOE_BUF_DH1ROW);
   p1.out0_pitch = 2 * F;
@@ -735,8 +868,8 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g2.epi = kEpiWgrad;
   g2.mode = kGroupedK;
   if (!make_tmap(&g2.tmA, B(ctx, MOE_BUF_DH3COL), mx, D, R, 128) ||
-      !make_tmap(&g2.tmB, sv + SL.off[MOE_SAVED_H2COL], mx, F, R, 128) ||
-      !make_narrow_tmaps(&g2, B(ctx, MOE_BUF_DH3COL), D, sv + SL.off[MOE_SAVED_H2COL], F, mx, R))
+      !make_tmap(&g2.tmB, sa + SL.off[MOE_SAVED_H2COL], mx, F, R, 128) ||
+      !make_narrow_tmaps(&g2, B(ctx, MOE_BUF_DH3COL), D, sa + SL.off[MOE_SAVED_H2COL], F, mx, R))
     return MOE_ERR_CUDA;
   GemmParams& p2 = g2.p;
   p2.hdr = rp.hdr;
@@ -749,7 +882,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p2.bstart = rp.bstart;
   p2.sfa = B(ctx, MOE_BUF_DH3COL_SCALE);
   p2.sfa_ts = ctx->b_cap;
-  p2.sfb = mx ? sv + SL.off[MOE_SAVED_H2COL_SCALE] : nullptr;
+  p2.sfb = mx ? sa + SL.off[MOE_SAVED_H2COL_SCALE] : nullptr;
   p2.sfb_ts = ctx->b_cap;
   p2.out0 = dW2;
   p2.out0_pitch = F;
@@ -803,8 +936,8 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g4.epi = kEpiWgrad;
   g4.mode = kGroupedK;
   if (!make_tmap(&g4.tmA, B(ctx, MOE_BUF_DH1COL), mx, 2 * F, R, 128) ||
-      !make_tmap(&g4.tmB, sv + SL.off[MOE_SAVED_XCOL], mx, D, R, 128) ||
-      !make_narrow_tmaps(&g4, B(ctx, MOE_BUF_DH1COL), 2 * F, sv + SL.off[MOE_SAVED_XCOL], D, mx, R))
+      !make_tmap(&g4.tmB, sa + SL.off[MOE_SAVED_XCOL], mx, D, R, 128) ||
+      !make_narrow_tmaps(&g4, B(ctx, MOE_BUF_DH1COL), 2 * F, sa + SL.off[MOE_SAVED_XCOL], D, mx, R))
     return MOE_ERR_CUDA;
   GemmParams& p4 = g4.p;
   p4.hdr = rp.hdr;
@@ -817,7 +950,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p4.bstart = rp.bstart;
   p4.sfa = B(ctx, MOE_BUF_DH1COL_SCALE);
   p4.sfa_ts = ctx->b_cap;
-  p4.sfb = mx ? sv + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr;
+  p4.sfb = mx ? sa + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr;
   p4.sfb_ts = ctx->b_cap;
   p4.out0 = dW13;
   p4.out0_pitch = D;
@@ -837,7 +970,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 1, 6, stream));
   if (d_scores) {
-    MOE_TRY(launch_score_grad(sv + SL.off[MOE_SAVED_H3], dout, D, K, rp.inv, d_scores, c.max_tokens, sms, stream,
+    MOE_TRY(launch_score_grad(sa + SL.off[MOE_SAVED_H3], dout, D, K, rp.inv, d_scores, c.max_tokens, sms, stream,
                               rp.hdr));
     ctx->launches += 1;
   }

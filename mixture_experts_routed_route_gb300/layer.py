@@ -3,7 +3,9 @@ computation runs in the CUDA library.
 
 ``PreparedWeight`` holds one stacked expert weight in the form the GEMMs read
 (``prepare_block_scaled_weight``); ``MoELayer`` owns one context and offers
-``forward`` / ``backward`` on torch tensors.
+``forward`` / ``backward`` on torch tensors; ``ActivationSlot`` packs several
+layers' saved states into one buffer and decides which of them keep only
+their input (``moe_slot_*``).
 """
 
 import numpy as np
@@ -59,9 +61,9 @@ class MoELayer:
     """One routed MoE layer bound to a context (fixed scratch)."""
 
     def __init__(self, max_tokens, d_model, d_ff, num_experts, top_k, precision, training=False, debug=False,
-                 device="cuda", swiglu_limit=0.0, post_norm=False):
+                 device="cuda", swiglu_limit=0.0, post_norm=False, replay=False):
         flags = ((abi.MOE_TRAINING if training else 0) | (abi.MOE_DEBUG_CHECKS if debug else 0)
-                 | (abi.MOE_POST_NORM if post_norm else 0))
+                 | (abi.MOE_POST_NORM if post_norm else 0) | (abi.MOE_REPLAY if replay else 0))
         self.cfg = abi.make_config(max_tokens, d_model, d_ff, num_experts, top_k, precision_code(precision), flags,
                                    swiglu_limit)
         self.device = torch.device(device)
@@ -83,11 +85,12 @@ class MoELayer:
             pass
 
     # ------------------------------------------------------------- state
-    def new_saved(self):
-        return torch.empty(abi.moe_saved_state_bytes(self.cfg), dtype=torch.uint8, device=self.device)
+    def new_saved(self, input_only=False):
+        nb = abi.moe_saved_input_bytes(self.cfg) if input_only else abi.moe_saved_state_bytes(self.cfg)
+        return torch.empty(nb, dtype=torch.uint8, device=self.device)
 
-    def saved_field(self, saved, field, dtype, shape):
-        off, nb = abi.moe_saved_state_field(self.cfg, field)
+    def saved_field(self, saved, field, dtype, shape, input_only=False):
+        off, nb = (abi.moe_saved_input_field if input_only else abi.moe_saved_state_field)(self.cfg, field)
         esz = torch.empty((), dtype=dtype).element_size()
         n = int(np.prod(shape))
         assert n * esz <= nb
@@ -123,16 +126,17 @@ class MoELayer:
         return dx_pre, dgamma
 
     # ----------------------------------------------------------- compute
-    def forward(self, x, ids, scores, W13, W2, out=None, saved=None, accumulate=False, stream=None):
+    def forward(self, x, ids, scores, W13, W2, out=None, saved=None, accumulate=False, save_input_only=False,
+                stream=None):
         T = x.shape[0]
         if out is None:
             out = torch.empty((T, self.D), dtype=torch.bfloat16, device=self.device)
-        abi.moe_forward(self.ctx, T, x, ids, scores, W13.struct, W2.struct, out, saved,
-                        abi.MOE_ACCUMULATE_OUT if accumulate else 0, stream)
+        flags = (abi.MOE_ACCUMULATE_OUT if accumulate else 0) | (abi.MOE_SAVE_INPUT_ONLY if save_input_only else 0)
+        abi.moe_forward(self.ctx, T, x, ids, scores, W13.struct, W2.struct, out, saved, flags, stream)
         return out
 
     def backward(self, saved, dout, W13, W2, dx=None, dW13=None, dW2=None, accumulate_dx=False, dw_fp32=False,
-                 dw_accumulate=False, d_scores=None, stream=None):
+                 dw_accumulate=False, d_scores=None, replay=False, stream=None):
         T = dout.shape[0]
         dt = torch.float32 if dw_fp32 else torch.bfloat16
         if dx is None:
@@ -142,6 +146,29 @@ class MoELayer:
         if dW2 is None:
             dW2 = torch.empty((self.E, self.D, self.F), dtype=dt, device=self.device)
         flags = ((abi.MOE_ACCUMULATE_DX if accumulate_dx else 0) | (abi.MOE_DW_FP32 if dw_fp32 else 0)
-                 | (abi.MOE_DW_ACCUMULATE if dw_accumulate else 0))
+                 | (abi.MOE_DW_ACCUMULATE if dw_accumulate else 0) | (abi.MOE_REPLAY_FORWARD if replay else 0))
         abi.moe_backward(self.ctx, saved, dout, W13.struct, W2.struct, dx, dW13, dW2, d_scores, flags, stream)
         return dx, dW13, dW2
+
+
+class ActivationSlot:
+    """One device buffer of `capacity` bytes holding the saved states of a
+    stack of layers ("Dist-MoE: Speed-of-light distributed Mixture-of-Experts
+    kernels", section 04 "Activation Packing and Dynamic Recompute").
+    ``push`` gives the next layer its state (a view of the buffer) and tells
+    whether it keeps only its input; ``pop`` returns it, in reverse order."""
+
+    def __init__(self, capacity, max_layers=abi.MOE_SLOT_MAX_LAYERS, device="cuda"):
+        self.buf = torch.empty(capacity, dtype=torch.uint8, device=device)
+        self.slot = abi.moe_slot_init(capacity, max_layers)
+
+    def push(self, layer, remaining_layers):
+        """(saved view, input_only) for `layer`, with `remaining_layers`
+        layers of the same size still to come after it in this slot."""
+        full, inp = abi.moe_saved_state_bytes(layer.cfg), abi.moe_saved_input_bytes(layer.cfg)
+        off, flags = abi.moe_slot_push(self.slot, full, inp, remaining_layers)
+        input_only = bool(flags & abi.MOE_SAVE_INPUT_ONLY)
+        return self.buf[off:off + (inp if input_only else full)], input_only
+
+    def pop(self, saved):
+        abi.moe_slot_pop(self.slot, saved.data_ptr() - self.buf.data_ptr())

@@ -55,6 +55,8 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(abi.moe_config) == 8 * 4
     assert ctypes.sizeof(abi.moe_weight) == 16 + 4 * 8
     assert abi.moe_weight.data.offset == 16
+    assert ctypes.sizeof(abi.moe_slot) == 8 + 8 + 4 + 4 + abi.MOE_SLOT_MAX_LAYERS * (8 + 4)
+    assert abi.moe_slot.offset.offset == 24
 
 
 def test_host_side_sizes_without_gpu(lib):
