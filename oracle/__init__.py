@@ -8,12 +8,17 @@ holds none of the method's arithmetic.
 
 Modules
 -------
-formats  -- BF16 / FP32 / E4M3 / E8M0 rounding and the MX block quantisers.
-moe      -- routing (counting sort), forward, backward, and the brute-force
-            per-token forward used to pin the routed forward.
+formats    -- BF16 / FP32 / E4M3 / E8M0 rounding and the MX block quantisers.
+moe        -- routing (counting sort), forward, backward, and the brute-force
+              per-token forward used to pin the routed forward.
+sample     -- bounded samples of a workload (routes of chosen experts).
+post_norm  -- the post-expert RMSNorm and its backward.
+slot_plan  -- the activation-slot save-or-replay decision rule.
 
-Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-against closed forms, library routines, brute force or finite differences.
+Parity status: every function here is pinned, by ``tests/test_oracle_pins.py``
+(closed forms, library routines, brute force, finite differences) or, for
+the slot planner, by ``tests/test_slot_plan_cpu.py`` (the worked example the
+page prints and brute-force properties).
 """
 
 from . import formats, moe  # noqa: F401
