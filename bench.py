@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--replay", action="store_true")   # training: the routed layer saves only its input and
+                                                       # its backward replays the forward (activation slots)
     ap.add_argument("--cpu-sample-experts", type=int, default=3)        # reference arm: experts per step
     ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)   # cpu_baseline: oracle work to time
     ap.add_argument("--cpu-sample-max-experts", type=int, default=384)
@@ -177,7 +179,7 @@ def traffic_record(kernel, workload):
 class Step:
     """Inputs, weights, contexts and the captured CUDA graph of one step."""
 
-    def __init__(self, w, device):
+    def __init__(self, w, device, replay=False):
         import torch
         from mixture_experts_routed_route_gb300 import synth
         from mixture_experts_routed_route_gb300.layer import MoELayer, PreparedWeight
@@ -197,8 +199,9 @@ class Step:
         self.W13 = PreparedWeight(w13, w.precision, with_transpose=self.train)
         self.W2 = PreparedWeight(w2, w.precision, with_transpose=self.train)
         self.w13_bf16, self.w2_bf16 = w13, w2   # kept only until the oracle sample is taken
-        self.layer = MoELayer(T, D, F, E, K, w.precision, training=self.train, device=device)
-        self.saved = self.layer.new_saved() if self.train else None
+        self.replay = bool(replay and self.train)
+        self.layer = MoELayer(T, D, F, E, K, w.precision, training=self.train, device=device, replay=self.replay)
+        self.saved = self.layer.new_saved(input_only=self.replay) if self.train else None
         self.shared = None
         if w.shared_F:
             sw13, sw2 = synth.make_shared_weights(w, device)
@@ -236,7 +239,7 @@ class Step:
             self.shared.forward(x, self.s_ids, self.s_scores, self.sW13, self.sW2, out=out, saved=self.s_saved)
             acc = True
         self.layer.forward(x, io["ids"], io["scores"], self.W13, self.W2, out=out, saved=self.saved,
-                           accumulate=acc)
+                           accumulate=acc, save_input_only=self.replay)
         if self.train:
             acc = False
             if self.shared:
@@ -244,7 +247,7 @@ class Step:
                                      dW2=self.sdW2)
                 acc = True
             self.layer.backward(self.saved, io["dy"], self.W13, self.W2, dx=dx, dW13=self.dW13, dW2=self.dW2,
-                                accumulate_dx=acc)
+                                accumulate_dx=acc, replay=self.replay)
 
     def capture(self):
         """Two graphs of the same step: the timed one, and one that also
@@ -268,7 +271,8 @@ class Step:
         from mixture_experts_routed_route_gb300 import abi
         import torch
         if self.train:
-            hdr = self.layer.saved_field(self.saved, abi.MOE_SAVED_HEADER, torch.int32, (16,)).cpu().numpy()
+            hdr = self.layer.saved_field(self.saved, abi.MOE_SAVED_HEADER, torch.int32, (16,),
+                                         input_only=self.replay).cpu().numpy()
         else:
             hdr = self.layer.read_buffer(abi.MOE_BUF_ROUTING, np.int32, (16,))
         return int(hdr[2]), int(hdr[3])
@@ -330,7 +334,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk = peaks()
-    st = Step(w, dev)
+    st = Step(w, dev, replay=args.replay)
 
     # eager warm-up (configures kernels), then correctness guard: no device error
     st.enqueue()
@@ -499,7 +503,10 @@ def run_ours(args, rank, world):
                    "train": w.train, "active_routes": routes, "padded_rows": rows_padded,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (expert weights stream from HBM every step)",
-                   "graph": "one CUDA graph per step, replayed"},
+                   "graph": "one CUDA graph per step, replayed",
+                   **({"saved_state": ("input only: the backward replays the gather, W13 and W2 GEMMs "
+                                       "(their FLOPs not counted as useful)") if st.replay else "full"}
+                      if st.train else {})},
         "roofline": roof, "stages": stages,
         "shared_expert_tflops": round(shared_flops / (ms * 1e-3) / 1e12, 3) if shared_flops else None,
         "clocks": clk, "gpu_launches": int(st.launches_per_step * args.steps),
