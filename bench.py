@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--replay", action="store_true")   # training: the routed layer saves only its input and
                                                        # its backward replays the forward (activation slots)
+    ap.add_argument("--slot-gb", type=float, default=0.0)   # layer stacks: one activation slot of this size
+                                                            # holds every layer's saved state (0: full states)
     ap.add_argument("--cpu-sample-experts", type=int, default=3)        # reference arm: experts per step
     ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)   # cpu_baseline: oracle work to time
     ap.add_argument("--cpu-sample-max-experts", type=int, default=384)
@@ -127,13 +129,15 @@ class ClockSampler:
 
 # --------------------------------------------------------- algorithmic bytes
 
-def stage_bytes(w, rows_padded, routes, precision, train, experts_used=None):
+def stage_bytes(w, rows_padded, routes, precision, train, experts_used=None, dw_bytes=2):
     """Unique bytes each stage must move (read once + written once), per launch.
 
     rows_padded = sum of expert row counts padded to 32; routes = active
     routes; experts_used = experts with at least one route (the GEMMs read
     only their weights; the weight gradients write dW of every expert).
-    MXFP8 operands cost 1 + 1/32 bytes per element (E4M3 + E8M0)."""
+    MXFP8 operands cost 1 + 1/32 bytes per element (E4M3 + E8M0).
+    dw_bytes = bytes moved per weight-gradient element: 2 (BF16 written),
+    4 (FP32 written), 8 (FP32 read and written back when accumulating)."""
     T, D, F, E = w.T, w.D, w.F, w.E
     Eu = w.E if experts_used is None else experts_used
     q = (1 + 1 / 32) if precision == "mxfp8" else 2.0
@@ -148,9 +152,9 @@ def stage_bytes(w, rows_padded, routes, precision, train, experts_used=None):
     bwd = {
         "gather_dh3": T * D * 2 + 2 * Rp * D * q,
         "gemm_w2_dgrad_swiglu_bwd": Eu * D * F * q + Rp * D * q + Rp * 2 * F * 2 + 2 * Rp * 2 * F * q,
-        "gemm_w2_wgrad": D * Rp * q + F * Rp * q + E * D * F * 2,
+        "gemm_w2_wgrad": D * Rp * q + F * Rp * q + E * D * F * dw_bytes,
         "gemm_w13_dgrad": Eu * 2 * F * D * q + Rp * 2 * F * q + Rp * D * 2,
-        "gemm_w13_wgrad": 2 * F * Rp * q + D * Rp * q + E * 2 * F * D * 2,
+        "gemm_w13_wgrad": 2 * F * Rp * q + D * Rp * q + E * 2 * F * D * dw_bytes,
         "reduce_dx": R * D * 2 + T * D * 2 * 2,
     }
     return fwd, bwd
@@ -276,6 +280,74 @@ class Step:
         else:
             hdr = self.layer.read_buffer(abi.MOE_BUF_ROUTING, np.int32, (16,))
         return int(hdr[2]), int(hdr[3])
+
+
+class StackStep:
+    """A stack of `w.layers` training layers on one context with one (tied)
+    expert weight set: every layer's forward in order, then the backwards in
+    reverse, captured as one CUDA graph.  Each layer has its own routing
+    (Zipf with a per-layer exponent), tokens and output gradient.  The weight
+    gradients of the layers accumulate in one FP32 buffer (the first backward
+    writes it).  With `slot_bytes`, the saved states share one activation
+    slot and the planner decides which layers keep only their input."""
+
+    def __init__(self, w, device, slot_bytes=0):
+        import torch
+        from mixture_experts_routed_route_gb300 import synth
+        from mixture_experts_routed_route_gb300.layer import ActivationSlot, MoELayer, PreparedWeight
+
+        self.w, self.dev, self.train = w, device, True
+        T, D, F, E, K, L = w.T, w.D, w.F, w.E, w.K, w.layers
+        w13, w2 = synth.make_weights(w, device)
+        self.W13 = PreparedWeight(w13, w.precision, with_transpose=True)
+        self.W2 = PreparedWeight(w2, w.precision, with_transpose=True)
+        del w13, w2
+        self.layer = MoELayer(T, D, F, E, K, w.precision, training=True, device=device, replay=slot_bytes > 0)
+        self.ids_np, self.io = [], []
+        for l in range(L):
+            ids, scores = synth.make_routing(w, layer=l, zipf_s=synth.layer_zipf_s(w, l))
+            self.ids_np.append(ids)
+            self.io.append({"ids": torch.from_numpy(ids).to(device), "scores": torch.from_numpy(scores).to(device),
+                            "x": synth.make_tokens(w, device, layer=l), "dy": synth.make_grad_out(w, device, layer=l),
+                            "out": torch.empty((T, D), dtype=torch.bfloat16, device=device),
+                            "dx": torch.empty((T, D), dtype=torch.bfloat16, device=device)})
+        self.dW13 = torch.empty((E, 2 * F, D), dtype=torch.float32, device=device)
+        self.dW2 = torch.empty((E, D, F), dtype=torch.float32, device=device)
+        self.slot = None
+        if slot_bytes > 0:
+            # the decisions depend only on the sizes, so they are taken once
+            # here and hold for every replay of the captured graph
+            self.slot = ActivationSlot(slot_bytes, max_layers=L, device=device)
+            self.states = [self.slot.push(self.layer, L - 1 - l) for l in range(L)]
+        else:
+            self.states = [(self.layer.new_saved(), False) for _ in range(L)]
+        self.graph = None
+
+    def layers(self):
+        return [self.layer]
+
+    def enqueue(self):
+        for l, io in enumerate(self.io):
+            saved, input_only = self.states[l]
+            self.layer.forward(io["x"], io["ids"], io["scores"], self.W13, self.W2, out=io["out"], saved=saved,
+                               save_input_only=input_only)
+        for n, l in enumerate(reversed(range(len(self.io)))):
+            saved, input_only = self.states[l]
+            self.layer.backward(saved, self.io[l]["dy"], self.W13, self.W2, dx=self.io[l]["dx"], dW13=self.dW13,
+                                dW2=self.dW2, dw_fp32=True, dw_accumulate=n > 0, replay=input_only)
+
+    capture = Step.capture
+
+    def rows_used(self):
+        """(padded rows, active routes) of every layer."""
+        import torch
+        from mixture_experts_routed_route_gb300 import abi
+        out = []
+        for saved, input_only in self.states:
+            hdr = self.layer.saved_field(saved, abi.MOE_SAVED_HEADER, torch.int32, (16,),
+                                         input_only=input_only).cpu().numpy()
+            out.append((int(hdr[2]), int(hdr[3])))
+        return out
 
 
 def cpu_sample(w, ids, scores, x_cpu, dy_cpu, w13_sub, w2_sub, experts):
@@ -516,6 +588,117 @@ def run_ours(args, rank, world):
         print(json.dumps(line), flush=True)
 
 
+def run_stack(args, rank, world):
+    """A layer stack (the ten-layer MXFP8 graph): every layer's forward, then
+    the backwards in reverse, replayed as one CUDA graph; one JSON line."""
+    import torch
+    from mixture_experts_routed_route_gb300 import abi, synth
+
+    w = synth.WORKLOADS[args.workload]
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    st = StackStep(w, dev, slot_bytes=int(args.slot_gb * 1e9))
+    st.enqueue()
+    torch.cuda.synchronize(dev)
+    bits = st.layer.error_bits()
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x} in warm-up")
+    rows = st.rows_used()
+    torch.cuda.empty_cache()
+    st.capture()
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        st.graph.replay()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        st.graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    if st.layer.error_bits():
+        raise RuntimeError("device error bits set in the timed replays")
+
+    # stage events keep the last call's records: the last layer's forward
+    # and the first layer's backward (the last in reverse order, accumulating
+    # into the FP32 weight gradients)
+    fwd_t = {n: [] for n in abi.FWD_STAGE_NAMES}
+    bwd_t = {n: [] for n in abi.BWD_STAGE_NAMES}
+    for _ in range(3):
+        st.stage_graph.replay()
+        torch.cuda.synchronize(dev)
+        for n, v in zip(abi.FWD_STAGE_NAMES, abi.moe_ctx_stage_times(st.layer.ctx, 0)):
+            fwd_t[n].append(v)
+        for n, v in zip(abi.BWD_STAGE_NAMES, abi.moe_ctx_stage_times(st.layer.ctx, 1)):
+            bwd_t[n].append(v)
+    stage_ms = {k: statistics.mean(v) for k, v in list(fwd_t.items()) + list(bwd_t.items())}
+
+    def used(l):
+        ids = np.asarray(st.ids_np[l])
+        return int(np.unique(ids[(ids >= 0) & (ids < w.E)]).size)
+
+    fb, _ = stage_bytes(w, rows[-1][0], rows[-1][1], w.precision, True, experts_used=used(len(rows) - 1))
+    _, bb = stage_bytes(w, rows[0][0], rows[0][1], w.precision, True, experts_used=used(0), dw_bytes=8)
+    sbytes = {**fb, **bb}
+    dom = max(stage_ms, key=lambda k: stage_ms[k])
+    achieved = sbytes[dom] / (stage_ms[dom] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+            "algorithmic_bytes": int(sbytes[dom]), "avg_launch_ms": round(stage_ms[dom], 4),
+            "peak_source": pk["source"]}
+    stages = {k: {"ms": round(v, 4), "GB/s": round(sbytes[k] / (v * 1e-3) / 1e9, 1) if v > 0 else None}
+              for k, v in stage_ms.items()}
+    routes = sum(r for _, r in rows)
+    flops = 6.0 * routes * w.D * w.F * 3.0
+    tflops = flops / (ms * 1e-3) / 1e12 * world
+    peak_t = pk["bf16_tflops"] * 2.0
+    replayed = [l for l, (_, input_only) in enumerate(st.states) if input_only]
+    line = {
+        "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.precision, "data": "synthetic",
+        "tokens_per_s": round(w.T * w.layers * world / (ms * 1e-3), 1),
+        "tensor_frac": round(tflops / world / peak_t, 4), "tensor_peak_tflops": round(peak_t, 1),
+        "config": {"workload": w.name, "layers": w.layers, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "K": w.K,
+                   "routing": "Zipf, exponent per layer in [0.8, 1.5]", "active_routes": routes,
+                   "padded_rows": [r for r, _ in rows], "train": True,
+                   "weights": "one MXFP8 weight set shared by the layers (tied); dW13/dW2 FP32, accumulated "
+                              "over the layers",
+                   "saved_state": ("full, one buffer per layer" if st.slot is None else
+                                   f"one {args.slot_gb:g} GB activation slot; layers {replayed} keep only their "
+                                   f"input and replay (their replay FLOPs not counted as useful)"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2", "graph": "the whole stack in one CUDA graph, replayed"},
+        "roofline": roof, "stages": stages,
+        "stage_note": "stage times of the last layer's forward and the first layer's backward",
+        "clocks": clk, "gpu_launches": int(st.launches_per_step * args.steps),
+        "e2e": None, "cpu_baseline": None,
+    }
+    if st.slot is not None:
+        for saved, _ in reversed(st.states):
+            st.slot.pop(saved)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------ reference arm (CPU)
 
 def run_reference(args, rank, world):
@@ -568,7 +751,8 @@ def main():
         if args.impl == "reference":
             run_reference(args, rank, world)
         else:
-            run_ours(args, rank, world)
+            from mixture_experts_routed_route_gb300 import synth
+            (run_stack if synth.WORKLOADS[args.workload].layers > 1 else run_ours)(args, rank, world)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -422,58 +422,59 @@ __device__ __forceinline__ void epi_swiglu_bwd(const GemmParams& p, const Tile& 
 }
 
 // Weight gradient with plain stores: dW[e][m][n0 ..], FP32 or accumulate.
-// An expert without rows gets zeros, or is left as is when adding.
-__device__ __forceinline__ void epi_wgrad_direct(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow,
-                                                 int h, int step) {
+// An expert without rows gets zeros, or is left as is when adding.  A lane
+// holds one row of each 32 x 32 chunk it drains; the warp turns the chunk
+// around in its own 4 KB of the group's staging buffer (float4 slots
+// XOR-swizzled by row: conflict-free writes and reads) so that each global
+// load and store covers 4 rows x 32 consecutive columns instead of 32 rows.
+__device__ __forceinline__ void epi_wgrad_direct(const GemmParams& p, const Tile& t, uint32_t tbase, int q, int lane,
+                                                 int h, int step, float* ws) {
   if (t.kstages == 0 && p.dw_accum) return;
   const long long M = static_cast<long long>(p.m_tiles) * 128;
-  const long long row = static_cast<long long>(t.e) * M + t.out_row0 + lrow;
+  const long long row0 = static_cast<long long>(t.e) * M + t.out_row0 + q * 32;   // the warp's first row
+  const int rr = lane >> 3, j = lane & 7;   // read-back: rows rr, rr + 4, ...; float4 slot j of each
   for (int c0 = 32 * h; c0 < 128; c0 += step) {
-    float v[32];
+    uint32_t r[32];   // FP32 bits of the chunk's row
     if (t.kstages > 0) {
-      uint32_t r[32];
       tmem_ld32(tbase + c0, r);
       tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]);
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+      for (int i = 0; i < 32; ++i) r[i] = 0u;
     }
-    const long long off = row * p.out0_pitch + t.out_col0 + c0;
-    if (p.dw_fp32) {
-      float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out0) + off);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 x = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    for (int s4 = 0; s4 < 8; ++s4)
+      *reinterpret_cast<uint4*>(ws + lane * 32 + ((s4 ^ (lane & 7)) << 2)) =
+          make_uint4(r[4 * s4], r[4 * s4 + 1], r[4 * s4 + 2], r[4 * s4 + 3]);
+    __syncwarp();
+#pragma unroll 2
+    for (int it = 0; it < 8; ++it) {
+      const int r = 4 * it + rr;
+      float4 a = *reinterpret_cast<const float4*>(ws + r * 32 + ((j ^ (r & 7)) << 2));
+      const long long off = (row0 + r) * p.out0_pitch + t.out_col0 + c0 + 4 * j;
+      if (p.dw_fp32) {
+        float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out0) + off);
         if (p.dw_accum) {
-          const float4 y = o[q];
-          x.x += y.x;
-          x.y += y.y;
-          x.z += y.z;
-          x.w += y.w;
+          const float4 y = *o;
+          a.x += y.x;
+          a.y += y.y;
+          a.z += y.z;
+          a.w += y.w;
         }
-        o[q] = x;
-      }
-    } else {
-      uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out0) + off);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
+        *o = a;
+      } else {
+        uint2* o = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out0) + off);
         if (p.dw_accum) {
-          const uint4 y = o[q];
-          v[8 * q + 0] += bf16_lo(y.x);
-          v[8 * q + 1] += bf16_hi(y.x);
-          v[8 * q + 2] += bf16_lo(y.y);
-          v[8 * q + 3] += bf16_hi(y.y);
-          v[8 * q + 4] += bf16_lo(y.z);
-          v[8 * q + 5] += bf16_hi(y.z);
-          v[8 * q + 6] += bf16_lo(y.w);
-          v[8 * q + 7] += bf16_hi(y.w);
+          const uint2 y = *o;
+          a.x += bf16_lo(y.x);
+          a.y += bf16_hi(y.x);
+          a.z += bf16_lo(y.y);
+          a.w += bf16_hi(y.y);
         }
-        o[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                          pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        *o = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
       }
     }
+    __syncwarp();   // every lane has read the chunk before the next one overwrites it
   }
 }
 
@@ -912,7 +913,8 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
         epi_swiglu_bwd<MX>(p, t, tbase, lrow, lane, h, hp);
         release_acc(&tempty[acc], lane);
       } else {
-        epi_wgrad_direct(p, t, tbase, lrow, h, 64);
+        epi_wgrad_direct(p, t, tbase, q, lane, h, 64,
+                         reinterpret_cast<float*>(staging + grp * 32768 + (gtid >> 5) * 4096));
         release_acc(&tempty[acc], lane);
       }
     }
