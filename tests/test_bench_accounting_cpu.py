@@ -42,3 +42,16 @@ def test_sample_experts_are_a_nested_seeded_prefix():
     assert b[:6] == a and len(set(b)) == 16
     present = set(int(e) for e in np.asarray(ids).reshape(-1) if e >= 0)
     assert set(b) <= present
+
+
+def test_accumulated_fp32_weight_gradients_count_a_read_and_a_write():
+    w = synth.WORKLOADS["ten_layer_graph"]
+    Rp, R = 40000, 32768
+    _, bf = bench.stage_bytes(w, Rp, R, w.precision, True)
+    _, acc = bench.stage_bytes(w, Rp, R, w.precision, True, dw_bytes=8)
+    D, F, E = w.D, w.F, w.E
+    assert acc["gemm_w13_wgrad"] - bf["gemm_w13_wgrad"] == E * 2 * F * D * (8 - 2)
+    assert acc["gemm_w2_wgrad"] - bf["gemm_w2_wgrad"] == E * D * F * (8 - 2)
+    for k in bf:     # nothing else depends on the weight-gradient format
+        if "wgrad" not in k:
+            assert acc[k] == bf[k]
