@@ -308,8 +308,8 @@ MOE_API moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int
  *           those of a full-state backward bit for bit.  The flag must
  *           match the forward's MOE_SAVE_INPUT_ONLY (moe_slot keeps it): the
  *           context remembers, per `saved` pointer, the last of its
- *           forwards that wrote there, and a mismatch returns
- *           MOE_ERR_INVALID_ARG.
+ *           forwards that wrote there (up to 4096 pointers; past that it
+ *           starts over), and a mismatch returns MOE_ERR_INVALID_ARG.
  */
 MOE_API moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout,
                         const moe_weight* W13, const moe_weight* W2, void* dx, void* dW13,

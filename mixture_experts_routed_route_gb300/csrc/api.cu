@@ -740,7 +740,12 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
 
   const SavedLayout SL = saved_layout(&c, input_only);
   uint8_t* sv = static_cast<uint8_t*>(saved);
-  if (train) ctx->saved_input_only[saved] = input_only;
+  if (train) {
+    // bounded: a caller cycling through fresh buffers forgets the oldest
+    // modes (their backwards are then taken at their word) instead of growing
+    if (ctx->saved_input_only.size() >= 4096 && !ctx->saved_input_only.count(saved)) ctx->saved_input_only.clear();
+    ctx->saved_input_only[saved] = input_only;
+  }
   if (input_only)   // the backward replays from this copy of x
     MOE_TRY(cudaMemcpyAsync(sv + SL.off[MOE_SAVED_X], x, static_cast<size_t>(T) * D * 2, cudaMemcpyDeviceToDevice,
                             stream));
