@@ -504,3 +504,36 @@ def test_post_norm_rounds_outputs_to_bf16():
     np.testing.assert_array_equal(y, fm.round_bf16(y))
     yx, _ = pn.forward(x, gamma, 1e-6, rounding=False)
     assert np.max(np.abs(y - yx) / np.maximum(np.abs(yx), 1e-30)) <= 2.0 ** -8
+
+
+# ------------------------------------------------------------ bounded samples
+
+@pytest.mark.parametrize("precision", ["bf16", "mxfp8"])
+def test_sample_reproduces_the_full_problem_for_its_experts(precision):
+    """oracle/sample.py, against the full oracle by brute force: with the
+    routes restricted to chosen experts, each chosen expert keeps its rows,
+    its h1 and its weight gradients exactly, and a token whose active routes
+    all reach chosen experts keeps its out, dX and score gradients."""
+    from oracle import sample as osample
+    T, D, F, E, K = 96, 128, 128, 8, 2
+    x, ids, s, w13, w2 = _case(T, D, F, E, K, 41)
+    dY = fm.round_bf16(np.random.default_rng(42).standard_normal((T, D)))
+    full = moe.forward(x, ids, s, w13, w2, precision)
+    fg = moe.backward(full, dY, w13, w2)
+    experts = [5, 1, 6]
+    res = osample.run(x, ids, s, w13[experts], w2[experts], experts, precision, dY=dY)
+    st, g = res["state"], res["grads"]
+    assert np.array_equal(res["ids"] >= 0, np.isin(ids, experts))
+    for i, e in enumerate(experts):
+        a, b = full["routing"].poffsets[e], full["routing"].poffsets[e + 1]
+        c, d = st["routing"].poffsets[i], st["routing"].poffsets[i + 1]
+        assert b - a == d - c
+        np.testing.assert_array_equal(st["h1"][c:d], full["h1"][a:b])
+        np.testing.assert_array_equal(g["dW13"][i], fg["dW13"][e])
+        np.testing.assert_array_equal(g["dW2"][i], fg["dW2"][e])
+    whole = np.all((ids < 0) | np.isin(ids, experts), axis=1) & np.any(np.isin(ids, experts), axis=1)
+    assert whole.sum() >= 5
+    np.testing.assert_array_equal(st["out"][whole], full["out"][whole])
+    np.testing.assert_array_equal(g["dX"][whole], fg["dX"][whole])
+    np.testing.assert_array_equal(g["dp"][whole], fg["dp"][whole])
+    assert osample.useful_flops(res["ids"], D, F, True) == 18.0 * np.isin(ids, experts).sum() * D * F
