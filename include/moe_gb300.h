@@ -254,6 +254,22 @@ MOE_API int64_t moe_row_capacity(const moe_config* cfg);
  *           transpose used by the input-gradient GEMMs.
  * The outputs are caller-owned device buffers.  Enqueued on `stream`.
  */
+/*
+ * Bytes of the buffers prepare_block_scaled_weight fills for one [E, N, K]
+ * weight, written to bytes[0..3] = data, scale, data_t, scale_t (0 for a
+ * buffer the precision does not use).  `with_transpose` asks for the
+ * backward's transposed copies (not for MOE_MXFP8_1X32).
+ *   MXFP8, MXFP8_1X32: data E*N*K, scale E*N*K/32 + 16, data_t E*K*N,
+ *                      scale_t E*K*N/32 + 16 (16 bytes of slack after the
+ *                      atoms); N % 128 == 0 and K % 128 == 0.
+ *   BF16:              data E*N*K*2 (the caller's own tensor, which the
+ *                      layer reads in place), data_t E*K*N*2.
+ * Host-only, no CUDA call.  Errors: MOE_ERR_INVALID_ARG (null bytes, shapes
+ * prepare_block_scaled_weight rejects, with_transpose for MXFP8_1X32).
+ */
+MOE_API moe_status moe_weight_bytes(moe_precision precision, int32_t E, int32_t N, int32_t K, int with_transpose,
+                                    size_t* bytes);
+
 MOE_API moe_status prepare_block_scaled_weight(const void* w, int32_t E, int32_t N, int32_t K,
                                        moe_precision precision, void* data, uint8_t* scale,
                                        void* data_t, uint8_t* scale_t, cudaStream_t stream);

@@ -112,6 +112,8 @@ _SIGNATURES = {
     "moe_ctx_set_max_ctas": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_ctx_set_post_norm": (ctypes.c_int, [_P, _P, ctypes.c_float]),
     "moe_post_norm_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
+    "moe_weight_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
+                                        ctypes.POINTER(ctypes.c_size_t)]),
     "moe_saved_input_bytes": (ctypes.c_size_t, [ctypes.POINTER(moe_config)]),
     "moe_saved_input_field": (ctypes.c_int, [ctypes.POINTER(moe_config), ctypes.c_int,
                                              ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]),
@@ -194,6 +196,13 @@ def moe_saved_state_field(cfg, field):
     _check("moe_saved_state_field", LIB.moe_saved_state_field(ctypes.byref(cfg), field, ctypes.byref(off),
                                                               ctypes.byref(nb)))
     return off.value, nb.value
+
+
+def moe_weight_bytes(precision, E, N, K, with_transpose):
+    """(data, scale, data_t, scale_t) byte counts of one prepared weight."""
+    out = (ctypes.c_size_t * 4)()
+    _check("moe_weight_bytes", LIB.moe_weight_bytes(precision, E, N, K, int(with_transpose), out))
+    return tuple(int(v) for v in out)
 
 
 def moe_saved_input_bytes(cfg):

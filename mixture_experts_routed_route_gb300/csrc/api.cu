@@ -695,6 +695,29 @@ moe_status moe_debug_copy_to_host(void* host_dst, const void* dev_src, size_t by
   return MOE_OK;
 }
 
+moe_status moe_weight_bytes(moe_precision precision, int32_t E, int32_t N, int32_t K, int with_transpose,
+                            size_t* bytes) {
+  if (!bytes || E < 1 || N < 32 || K < 32 || N % 32 || K % 32) return MOE_ERR_INVALID_ARG;
+  const size_t e = static_cast<size_t>(E), n = static_cast<size_t>(N), k = static_cast<size_t>(K);
+  bytes[0] = bytes[1] = bytes[2] = bytes[3] = 0;
+  if (precision == MOE_MXFP8 || precision == MOE_MXFP8_1X32) {
+    if (N % 128 || K % 128 || (precision == MOE_MXFP8_1X32 && with_transpose)) return MOE_ERR_INVALID_ARG;
+    bytes[0] = e * n * k;
+    bytes[1] = e * n * (k / 32) + 16;
+    if (with_transpose) {
+      bytes[2] = e * k * n;
+      bytes[3] = e * k * (n / 32) + 16;
+    }
+    return MOE_OK;
+  }
+  if (precision == MOE_BF16) {
+    bytes[0] = e * n * k * 2;
+    if (with_transpose) bytes[2] = e * k * n * 2;
+    return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
 moe_status prepare_block_scaled_weight(const void* w, int32_t E, int32_t N, int32_t K, moe_precision precision,
                                        void* data, uint8_t* scale, void* data_t, uint8_t* scale_t,
                                        cudaStream_t stream) {

@@ -97,3 +97,21 @@ def test_context_setters_reject_null_context(lib):
     from mixture_experts_routed_route_gb300 import abi
     assert abi.LIB.moe_ctx_set_max_ctas(None, 4) == abi.MOE_ERR_INVALID_ARG
     assert abi.LIB.moe_ctx_enable_stage_timing(None, 1) == abi.MOE_ERR_INVALID_ARG
+
+
+def test_weight_bytes_without_gpu(lib):
+    from mixture_experts_routed_route_gb300 import abi
+    E, N, K = 6, 256, 384
+    atoms = (E * N // 128) * (K // 128) * 512            # one 512-byte atom per 128 x 128 block
+    assert abi.moe_weight_bytes(abi.MOE_MXFP8, E, N, K, True) == (E * N * K, atoms + 16, E * K * N, atoms + 16)
+    assert abi.moe_weight_bytes(abi.MOE_MXFP8, E, N, K, False) == (E * N * K, atoms + 16, 0, 0)
+    assert abi.moe_weight_bytes(abi.MOE_MXFP8_1X32, E, N, K, False) == (E * N * K, atoms + 16, 0, 0)
+    assert abi.moe_weight_bytes(abi.MOE_BF16, E, 96, 64, True) == (E * 96 * 64 * 2, 0, E * 64 * 96 * 2, 0)
+    for bad in ((abi.MOE_MXFP8, E, 96, K, True),        # MXFP8 tiles N and K by 128
+                (abi.MOE_MXFP8_1X32, E, N, K, True),    # inference weights have no transpose
+                (abi.MOE_BF16, 0, 64, 64, True),
+                (abi.MOE_BF16, E, 48, 64, True),
+                (7, E, N, K, False)):
+        with pytest.raises(abi.MoEError) as ei:
+            abi.moe_weight_bytes(*bad)
+        assert ei.value.status == abi.MOE_ERR_INVALID_ARG
