@@ -188,3 +188,29 @@ def test_replay_needs_a_training_context(abi):
     ctx = ctypes.c_void_p()
     # rejected on the host before any CUDA call
     assert abi.LIB.moe_ctx_create(ctypes.byref(cfg), ctypes.byref(ctx)) == abi.MOE_ERR_INVALID_ARG
+
+
+def test_activation_slot_wrapper_on_a_host_buffer(abi):
+    """layer.ActivationSlot: views at the planner's offsets, sized for the
+    decision, given back in reverse order (a CPU buffer stands in for HBM)."""
+    import types
+    import torch
+    from mixture_experts_routed_route_gb300.layer import ActivationSlot
+    cfg = abi.make_config(64, 256, 256, 8, 2, abi.MOE_MXFP8, abi.MOE_TRAINING | abi.MOE_REPLAY)
+    layer = types.SimpleNamespace(cfg=cfg)
+    full, inp = abi.moe_saved_state_bytes(cfg), abi.moe_saved_input_bytes(cfg)
+    cap = sp.align128(full) * 2 + sp.align128(inp) * 2
+    slot = ActivationSlot(cap, max_layers=4, device="cpu")
+    want = sp.plan_stack([(full, inp)] * 4, cap)
+    got = [slot.push(layer, 3 - l) for l in range(4)]
+    base = slot.buf.data_ptr()
+    for (view, input_only), p in zip(got, want):
+        assert input_only == (p["decision"] == sp.INPUT)
+        assert view.data_ptr() - base == p["offset"]
+        assert view.numel() == (inp if input_only else full)
+    assert [d for _, d in got] == [False, False, True, True]
+    with pytest.raises(abi.MoEError):
+        slot.pop(got[0][0])            # not the most recent
+    for view, _ in reversed(got):
+        slot.pop(view)
+    assert slot.slot.layers == 0 and slot.slot.cursor == 0
