@@ -115,3 +115,28 @@ def test_weight_bytes_without_gpu(lib):
         with pytest.raises(abi.MoEError) as ei:
             abi.moe_weight_bytes(*bad)
         assert ei.value.status == abi.MOE_ERR_INVALID_ARG
+
+
+def test_binding_constants_match_the_header():
+    """Every #define and enum value of the header that the binding restates
+    has the same value there (the binding is written by hand)."""
+    from mixture_experts_routed_route_gb300 import abi
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    values = {}
+    for name, val in re.findall(r"^#define\s+(MOE_[A-Z0-9_]+)\s+\(?([0-9xa-fA-F]+)(?:u|ull)?", text, flags=re.M):
+        values[name] = int(val, 0)
+    for m in re.finditer(r"^#define\s+(MOE_[A-Z0-9_]+)\s+\(([0-9]+)ull\s*<<\s*([0-9]+)\)", text, flags=re.M):
+        values[m.group(1)] = int(m.group(2)) << int(m.group(3))
+    for body in re.findall(r"typedef enum\s*\{(.*?)\}", text, flags=re.S):
+        for name, val in re.findall(r"(MOE_[A-Z0-9_]+)\s*=\s*([0-9]+)", body):
+            values[name] = int(val)
+    checked = 0
+    for name, val in values.items():
+        if hasattr(abi, name):
+            assert getattr(abi, name) == val, name
+            checked += 1
+    assert checked >= 60
+    for required in ("MOE_REPLAY", "MOE_SAVE_INPUT_ONLY", "MOE_REPLAY_FORWARD", "MOE_SAVED_X", "MOE_BUF_REPLAY",
+                     "MOE_SLOT_MAX_LAYERS", "MOE_SAVED_NUM_FIELDS", "MOE_BUF_NUM", "MOE_STATIC_SCRATCH_BYTES"):
+        assert required in values and hasattr(abi, required), required
