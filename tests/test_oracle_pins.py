@@ -537,3 +537,26 @@ def test_sample_reproduces_the_full_problem_for_its_experts(precision):
     np.testing.assert_array_equal(g["dX"][whole], fg["dX"][whole])
     np.testing.assert_array_equal(g["dp"][whole], fg["dp"][whole])
     assert osample.useful_flops(res["ids"], D, F, True) == 18.0 * np.isin(ids, experts).sum() * D * F
+
+
+@pytest.mark.parametrize("case", ["all_to_one", "all_inactive"])
+def test_route_degenerate_distributions(case):
+    """The routing matrix's degenerate corners: every route to one expert of
+    eight (the others empty), and no active route at all."""
+    T, K, E = 300, 2, 8
+    ids = np.full((T, K), 5 if case == "all_to_one" else -1, dtype=np.int64)
+    rt = moe.route(ids, E)
+    n = T * K if case == "all_to_one" else 0
+    assert rt.num_active == n and rt.counts.tolist() == [n if e == 5 else 0 for e in range(E)]
+    pad = -(-n // 32) * 32
+    assert rt.poffsets.tolist() == [0] * 6 + [pad] * 3
+    np.testing.assert_array_equal(rt.perm[:n], np.arange(n))          # flat order kept
+    assert np.all(rt.perm[n:pad] == -1)
+    np.testing.assert_array_equal(rt.inv, np.arange(T * K) if n else np.full(T * K, -1))
+    x, _, s, w13, w2 = _case(T, 32, 32, E, K, 43, inactive=0.0)
+    out = moe.forward(x, ids, s, w13, w2, "f64")["out"]
+    if case == "all_inactive":
+        assert np.all(out == 0.0)
+    else:
+        ref = moe.forward_per_token(x, ids, s, w13, w2, "f64")
+        np.testing.assert_allclose(out, np.stack([ref[t] for t in range(T)]), rtol=1e-12, atol=1e-12)
