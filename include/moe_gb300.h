@@ -488,7 +488,8 @@ MOE_API moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t T, 
  * Activation slots: several layers' saved states packed into one buffer,
  * with save-or-replay decisions ("Dist-MoE: Speed-of-light distributed
  * Mixture-of-Experts kernels", section 04 "Activation Packing and Dynamic
- * Recompute").  The caller allocates one device buffer of `capacity` bytes;
+ * Recompute").  The caller allocates one device buffer of `capacity` bytes
+ * (base 16-byte aligned, as every saved state; offsets are multiples of 128);
  * each training forward of a stack takes its saved state at
  * base + offset from moe_slot_push, and the backwards, in reverse order,
  * give the offsets back with moe_slot_pop.
