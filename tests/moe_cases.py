@@ -148,13 +148,38 @@ def _mx_col_spread(cands, eps):
     return hi - lo
 
 
+def mx_wgrad_allowance(state, grads, i):
+    """(allow13, allow2, undecided13, undecided2) of oracle expert i: the
+    per-element allowance on top of the tolerance for dW13 and dW2 (twice
+    the spread of the undecided column-bundle codes times the other
+    operand's magnitudes), and the fractions of undecided codes in the dh1
+    and h2 column bundles.  Zero arrays for an expert without rows."""
+    from oracle import moe as omoe
+    rt = state["routing"]
+    F = state["F"]
+    a, b = int(rt.poffsets[i]), int(rt.poffsets[i + 1])
+    if a == b:
+        return np.zeros_like(grads["dW13"][i]), np.zeros_like(grads["dW2"][i]), 0.0, 0.0
+    h1x = state["h1_exact"][a:b]
+    g, ga = _bf16_candidates(h1x[:, :F], EPS_ACC)
+    u, ua = _bf16_candidates(h1x[:, F:], EPS_ACC)
+    dh2 = grads["dh2"][a:b]
+    lim = state.get("swiglu_limit", 0.0)
+    combos = [(g, u), (ga, u), (g, ua), (ga, ua)]
+    dh1_c = [np.concatenate(omoe.swiglu_grad(gg, uu, dh2, lim), axis=1) for gg, uu in combos]
+    h2_c = [omoe.swiglu(gg, uu, lim) for gg, uu in combos]
+    s13 = _mx_col_spread(dh1_c, EPS_ACC)
+    s2 = _mx_col_spread(h2_c, EPS_ACC)
+    allow13 = 2.0 * s13.T @ np.abs(grads["x_col"][a:b])
+    allow2 = 2.0 * np.abs(grads["dh3_col"][a:b]).T @ s2
+    return allow13, allow2, float((s13 > 0).mean()), float((s2 > 0).mean())
+
+
 def check_mx_wgrad(dW13_gpu, dW2_gpu, state, grads, experts=None, tol=TOL["mxfp8"], max_undecided=5e-3):
     """Assert dW13/dW2 of the listed experts (indices into the oracle's
     expert axis; dW*_gpu indexed the same way) against the oracle with the
     undecided-code allowance.  Returns the per-expert plain errors."""
-    from oracle import moe as omoe
     rt = state["routing"]
-    F = state["F"]
     experts = range(len(grads["dW13"])) if experts is None else experts
     errs = []
     for i in experts:
@@ -165,19 +190,8 @@ def check_mx_wgrad(dW13_gpu, dW2_gpu, state, grads, experts=None, tol=TOL["mxfp8
             assert np.all(got13 == 0) and np.all(got2 == 0)
             errs.append((0.0, 0.0))
             continue
-        h1x = state["h1_exact"][a:b]
-        g, ga = _bf16_candidates(h1x[:, :F], EPS_ACC)
-        u, ua = _bf16_candidates(h1x[:, F:], EPS_ACC)
-        dh2 = grads["dh2"][a:b]
-        lim = state.get("swiglu_limit", 0.0)
-        combos = [(g, u), (ga, u), (g, ua), (ga, ua)]
-        dh1_c = [np.concatenate(omoe.swiglu_grad(gg, uu, dh2, lim), axis=1) for gg, uu in combos]
-        h2_c = [omoe.swiglu(gg, uu, lim) for gg, uu in combos]
-        s13 = _mx_col_spread(dh1_c, EPS_ACC)
-        s2 = _mx_col_spread(h2_c, EPS_ACC)
-        assert (s13 > 0).mean() <= max_undecided and (s2 > 0).mean() <= max_undecided
-        allow13 = 2.0 * s13.T @ np.abs(grads["x_col"][a:b])
-        allow2 = 2.0 * np.abs(grads["dh3_col"][a:b]).T @ s2
+        allow13, allow2, u13, u2 = mx_wgrad_allowance(state, grads, i)
+        assert u13 <= max_undecided and u2 <= max_undecided
         for got, ref, allow, name in ((got13, ref13, allow13, "dW13"), (got2, ref2, allow2, "dW2")):
             bound = tol * np.max(np.abs(ref)) + allow
             bad = np.abs(got - ref) > bound

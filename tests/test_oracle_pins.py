@@ -134,6 +134,60 @@ def test_mx_weight_32x32_single_scale_per_tile():
     np.testing.assert_array_equal(eT, np.swapaxes(e, 1, 2))
 
 
+def _tile_scaled_weight(E=2, NT=3, KT=5, seed=9):
+    """Weights [E, 32 NT, 32 KT] whose tile (i, j) of expert x holds values
+    in [-1, 1] with one element exactly 1, times 2^(3i - 5j + x): every tile
+    has its own power-of-two scale, and the known maximum fixes its
+    exponent 3i - 5j + x - 8 in closed form."""
+    rng = np.random.default_rng(seed)
+    w = rng.uniform(-1.0, 1.0, (E, 32 * NT, 32 * KT))
+    for x in range(E):
+        for i in range(NT):
+            for j in range(KT):
+                t = w[x, 32 * i:32 * i + 32, 32 * j:32 * j + 32]
+                t[(7 * i + j) % 32, (5 * j + i) % 32] = 1.0
+                t *= 2.0 ** (3 * i - 5 * j + x)
+    return w
+
+
+def test_mx_weight_32x32_dequantise_tile_by_tile():
+    """Quantise then dequantise tiles whose scales differ by powers of two:
+    the exponents take their closed form, the dequantised tensor equals a
+    loop over tiles that multiplies each tile's codes by its own 2^e, and
+    every element that did not saturate is within half an E4M3 step (in its
+    own binade) of the input.  A broadcast over the wrong axis, or the N and
+    K tile axes exchanged (3 x 5 tiles), changes scales by powers of two and
+    fails the loop and the half-step bound."""
+    E, NT, KT = 2, 3, 5
+    w = _tile_scaled_weight(E, NT, KT)
+    q, e = fm.mx_quantize_weight_32x32(w)
+    assert e.shape == (E, NT, KT)
+    for x in range(E):
+        for i in range(NT):
+            for j in range(KT):
+                assert e[x, i, j] == 3 * i - 5 * j + x - 8
+    deq = fm.mx_dequantize_weight_32x32(q, e)
+    loop = np.empty_like(w)
+    for x in range(E):
+        for i in range(NT):
+            for j in range(KT):
+                sl = (x, slice(32 * i, 32 * i + 32), slice(32 * j, 32 * j + 32))
+                loop[sl] = q[sl] * 2.0 ** int(e[x, i, j])
+    np.testing.assert_array_equal(deq, loop)
+    # half an E4M3 step of the scaled value, in its own binade (subnormal
+    # quantum 2^-9 below 2^-6), times the tile scale
+    s = np.repeat(np.repeat(np.ldexp(1.0, e), 32, axis=1), 32, axis=2)
+    y = np.abs(w) / s
+    binade = np.floor(np.log2(np.maximum(y, 2.0 ** -6)))
+    half_step = np.ldexp(1.0, (binade - 4).astype(int)) * s
+    ok = y <= 448.0
+    assert ok.mean() > 0.8
+    assert np.all(np.abs(deq - w)[ok] <= half_step[ok])
+    # saturated elements keep their sign at the largest code
+    assert np.all(np.abs(deq[~ok]) == 448.0 * s[~ok])
+
+
+
 # -------------------------------------------------------------------- SiLU
 
 def test_silu_closed_form(golden_dir):
