@@ -345,37 +345,6 @@ MOE_API moe_status moe_ctx_get_error(moe_ctx* ctx, uint32_t* bits);
  * counters.  Not for use inside graph capture. */
 MOE_API moe_status moe_ctx_clip_stats(moe_ctx* ctx, uint64_t* counts);
 
-/* Copy `bytes` from device memory to host memory (synchronous).  A helper
- * for tests that inspect scratch; not part of the hot path. */
-MOE_API moe_status moe_debug_copy_to_host(void* host_dst, const void* dev_src, size_t bytes);
-
-/* Scratch regions of a context, for inspection by tests. */
-typedef enum {
-  MOE_BUF_XROW = 0,        /* gathered x row bundle: bf16 [R_cap, D] or e4m3  */
-  MOE_BUF_XROW_SCALE = 1,  /* e8m0 row-bundle atoms [B_cap][D/128]             */
-  MOE_BUF_H2ROW = 2,       /* h2 row bundle: bf16 [R_cap, F] or e4m3           */
-  MOE_BUF_H2ROW_SCALE = 3, /* e8m0 row-bundle atoms [B_cap][F/128]             */
-  MOE_BUF_H3 = 4,          /* bf16 [R_cap, D]                                  */
-  MOE_BUF_DH3ROW = 5,      /* bf16 [R_cap, D] or e4m3                          */
-  MOE_BUF_DH3ROW_SCALE = 6,/* e8m0 row-bundle atoms [B_cap][D/128]            */
-  MOE_BUF_DH3COL = 7,      /* bf16 [D, R_cap] or e4m3                          */
-  MOE_BUF_DH3COL_SCALE = 8,/* e8m0 column-bundle atoms [D/128][B_cap]         */
-  MOE_BUF_DH1ROW = 9,      /* bf16 [R_cap, 2F] or e4m3                         */
-  MOE_BUF_DH1ROW_SCALE = 10,/* e8m0 row-bundle atoms [B_cap][2F/128]          */
-  MOE_BUF_DH1COL = 11,     /* bf16 [2F, R_cap] or e4m3                         */
-  MOE_BUF_DH1COL_SCALE = 12,/* e8m0 column-bundle atoms [2F/128][B_cap]       */
-  MOE_BUF_DXR = 13,        /* bf16 [R_cap, D]                                  */
-  MOE_BUF_ROUTING = 14,    /* inference routing state (same layout as saved)   */
-  MOE_BUF_ERROR = 15,      /* uint32 error word                                */
-  MOE_BUF_NORM = 16,       /* MOE_POST_NORM training: float r[T_max], then the
-                              dgamma partial sums [ceil(T_max/64)][D]          */
-  MOE_BUF_REPLAY = 17,     /* MOE_REPLAY: a full saved state (same layout) that
-                              a backward with MOE_REPLAY_FORWARD rebuilds       */
-  MOE_BUF_NUM = 18
-} moe_buffer;
-
-MOE_API moe_status moe_ctx_buffer(moe_ctx* ctx, int which, void** dev_ptr, size_t* bytes);
-
 /*
  * Stage timing, for measurement.  When enabled, moe_forward and moe_backward
  * record a CUDA event on their stream before their first launch and after

@@ -18,6 +18,7 @@
 
 #include "kernels.cuh"
 #include "moe_gb300.h"
+#include "moe_gb300_testing.h"
 
 using namespace moe;
 

@@ -207,12 +207,10 @@ template <bool SCALE>
 cudaError_t both_impl(const void* src, int D, int K, const RoutingPtrs& rp, void* dst, void* dstT, int r_cap,
                       cudaStream_t stream) {
   auto kern = gather_both_kernel<SCALE>;
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBothSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce setup;
+  const cudaError_t se =
+      setup.once([&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBothSmem); });
+  if (se != cudaSuccess) return se;
   dim3 grid((D + kBothCols - 1) / kBothCols, (r_cap + kBothRows - 1) / kBothRows);
   kern<<<grid, 256, kBothSmem, stream>>>(static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr, rp.perm, rp.scores,
                                          static_cast<__nv_bfloat16*>(dst), static_cast<__nv_bfloat16*>(dstT), r_cap);
@@ -382,12 +380,10 @@ cudaError_t both_mx_impl(const CUtensorMap* tm_row, const CUtensorMap* tm_col, c
                          const RoutingPtrs& rp, uint8_t* dst_sf, uint8_t* dstT_sf, int r_cap, int b_cap,
                          cudaStream_t stream) {
   auto kern = gather_both_mx_kernel<SCALE>;
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce setup;
+  const cudaError_t se =
+      setup.once([&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem); });
+  if (se != cudaSuccess) return se;
   dim3 grid(D / kBothCols, r_cap / kBothRows);
   kern<<<grid, 256, kMxSmem, stream>>>(*tm_row, *tm_col, static_cast<const __nv_bfloat16*>(src), D, K, rp.hdr,
                                        rp.perm, rp.scores, dst_sf, dstT_sf, b_cap, rp.row_block, rp.blocks);

@@ -934,12 +934,10 @@ template <bool MX, int NA, int EPI, int MODE>
 cudaError_t launch_impl(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   using C = Cfg<MX, NA, MODE>;
   auto kern = gemm_kernel<MX, NA, EPI, MODE>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce setup;
+  const cudaError_t se =
+      setup.once([&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM); });
+  if (se != cudaSuccess) return se;
   const int grid = max(1, min(num_sms, g.max_tiles));
   GemmParams p = g.p;
   const int q = grid / p.n_tiles;

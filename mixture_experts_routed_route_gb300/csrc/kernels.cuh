@@ -1,9 +1,42 @@
 // Launch interface of the MoE kernels (internal to the library).
 #pragma once
 
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
+
+// ------------------------------------------------ per-device kernel set-up
+
+// Devices a process may drive (device ordinals 0 .. kMaxDevices - 1).
+constexpr int kMaxDevices = 64;
+
+// A kernel attribute such as the dynamic shared-memory opt-in belongs to
+// the context of the device that was current when it was set, so each
+// device needs its own set-up.  once() runs `fn` the first time it is
+// called with a device current, under a lock (host threads may race on
+// the first launch), and remembers success per device; a failed set-up is
+// tried again on the next call.
+struct PerDeviceOnce {
+  std::atomic<int> done[kMaxDevices] = {};
+  std::mutex mu;
+
+  template <typename Fn>
+  cudaError_t once(Fn&& fn) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = fn();
+    if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+    return e;
+  }
+};
 
 // Device view of one routing state (the saved-state prefix or the
 // context's inference copy).  Layout and meaning of every array are those of

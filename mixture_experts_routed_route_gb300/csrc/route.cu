@@ -259,12 +259,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_route(const int32_t* ids, const float* scores, int T, int K, int E, int r_cap, int debug,
                          const RoutingPtrs& rp, uint32_t* err, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(kWarps * E + E + E + 1) * sizeof(int);
-  static size_t configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = smem;
+  // the opt-in covers the largest expert count a context accepts (1024), so
+  // one set-up per device serves every launch
+  static PerDeviceOnce setup;
+  if (smem > 48 * 1024) {
+    const int max_smem = (kWarps * 1024 + 1024 + 1024 + 1) * static_cast<int>(sizeof(int));
+    const cudaError_t se = setup.once(
+        [&] { return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem); });
+    if (se != cudaSuccess) return se;
   }
   route_kernel<<<1, kThreads, smem, stream>>>(ids, scores, T, K, E, r_cap, debug, rp, err);
   return cudaGetLastError();

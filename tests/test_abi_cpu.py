@@ -1,5 +1,6 @@
-"""The C-ABI library loads and exports every function include/moe_gb300.h
-declares, and the binding's structs match the header (no GPU needed: no
+"""The C-ABI library loads and exports every function include/*.h declare
+(the boundary, moe_gb300.h, and the test inspection calls,
+moe_gb300_testing.h), and the binding's structs match the header (no GPU needed: no
 compute call is made)."""
 
 import ctypes
@@ -10,6 +11,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+TESTING_HEADER = os.path.join(ROOT, "include", "moe_gb300_testing.h")
 
 
 def _declared_functions():
@@ -36,6 +38,15 @@ def test_header_declares_the_boundary():
     for required in ("moe_ctx_create", "moe_ctx_destroy", "moe_forward", "moe_backward",
                      "prepare_block_scaled_weight", "moe_saved_state_bytes", "moe_ctx_get_error"):
         assert required in names
+
+
+def test_product_header_holds_no_test_inspection_calls():
+    """Scratch inspection and host copies live in the testing header only."""
+    text = open(HEADER).read()
+    for name in ("moe_debug_copy_to_host", "moe_ctx_buffer", "MOE_BUF_XROW"):
+        assert name not in text, name
+    testing = open(TESTING_HEADER).read()
+    assert "moe_debug_copy_to_host" in testing and "moe_ctx_buffer" in testing
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -121,7 +132,7 @@ def test_binding_constants_match_the_header():
     """Every #define and enum value of the header that the binding restates
     has the same value there (the binding is written by hand)."""
     from mixture_experts_routed_route_gb300 import abi
-    text = open(HEADER).read()
+    text = open(HEADER).read() + open(TESTING_HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     values = {}
     for name, val in re.findall(r"^#define\s+(MOE_[A-Z0-9_]+)\s+\(?([0-9xa-fA-F]+)(?:u|ull)?", text, flags=re.M):

@@ -56,3 +56,13 @@ def test_every_polling_loop_is_bounded():
                 f"{name}: polling loop without a deadline: {m.group(0)}"
             found += 1
     assert found >= 2      # the mbarrier wait and the drain wait
+
+
+def test_kernel_setup_is_per_device():
+    """Kernel attributes (the dynamic shared-memory opt-in) belong to the
+    context of the current device: their one-time set-up is kept per device
+    and under a lock, never in a process-wide flag."""
+    for name, text in _sources():
+        assert not re.search(r"static\s+bool\s+\w*configured", text), name
+        if "cudaFuncSetAttribute" in text:
+            assert "PerDeviceOnce" in text or "g_setup" in text, name
