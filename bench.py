@@ -459,6 +459,7 @@ def run_ours(args, rank, world):
     # ---------------- per-stage durations (CUDA events inside the graph)
     fwd_t = {n: [] for n in abi.FWD_STAGE_NAMES}
     bwd_t = {n: [] for n in abi.BWD_STAGE_NAMES}
+    shared_t = []   # the shared expert's own time per step: its forward (+ backward) stages
     for _ in range(max(3, min(args.steps, 10))):
         st.stage_graph.replay()
         torch.cuda.synchronize(dev)
@@ -467,6 +468,11 @@ def run_ours(args, rank, world):
         if st.train:
             for n, v in zip(abi.BWD_STAGE_NAMES, abi.moe_ctx_stage_times(st.layer.ctx, 1)):
                 bwd_t[n].append(v)
+        if st.shared:
+            t_sh = sum(abi.moe_ctx_stage_times(st.shared.ctx, 0))
+            if st.train:
+                t_sh += sum(abi.moe_ctx_stage_times(st.shared.ctx, 1))
+            shared_t.append(t_sh)
     stage_ms = {k: statistics.mean(v) for k, v in list(fwd_t.items()) + list(bwd_t.items()) if v}
     ids = np.asarray(st.ids_np)
     used = int(np.unique(ids[(ids >= 0) & (ids < w.E)]).size)
@@ -559,7 +565,8 @@ def run_ours(args, rank, world):
         experts, s13, s2, xc, dyc = sample
         dt, sflops, sroutes, n = timed_cpu_sample(w, st.ids_np, st.scores_np, xc, dyc, s13, s2, experts,
                                                   args.cpu_sample_seconds)
-        cpu = {"value": round(sflops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+        cpu = {"value": round(sflops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(),
+               "host_cores": os.cpu_count(), "kind": "oracle",
                "sample": f"fp64 numpy oracle, {'forward+backward' if w.train else 'forward'} of the {sroutes} "
                          f"routes of {n} of {w.E} experts, one oracle call per expert (all {w.T} tokens), {dt:.1f} s"}
 
@@ -580,7 +587,11 @@ def run_ours(args, rank, world):
                                        "(their FLOPs not counted as useful)") if st.replay else "full"}
                       if st.train else {})},
         "roofline": roof, "stages": stages,
-        "shared_expert_tflops": round(shared_flops / (ms * 1e-3) / 1e12, 3) if shared_flops else None,
+        # the BF16 shared expert over its own stage time (not counted in `value`)
+        "shared_expert": ({"ms": round(statistics.mean(shared_t), 4),
+                           "tflops": round(shared_flops / (statistics.mean(shared_t) * 1e-3) / 1e12, 3),
+                           "bf16_frac": round(shared_flops / (statistics.mean(shared_t) * 1e-3) / 1e12
+                                              / pk["bf16_tflops"], 4)} if shared_t else None),
         "clocks": clk, "gpu_launches": int(st.launches_per_step * args.steps),
         "e2e": e2e, "cpu_baseline": cpu,
     }
@@ -728,7 +739,8 @@ def run_reference(args, rank, world):
         "steps": steps, "warmup": min(args.warmup, 1), "ms_per_step": round(dt * 1e3, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "K": w.K, "train": w.train},
-        "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": blas_threads(),
+                         "host_cores": os.cpu_count(), "kind": "oracle",
                          "sample": f"fp64 numpy oracle, routes of {len(experts)} of {w.E} experts per step "
                                    f"({sroutes} routes, all {w.T} tokens)"},
         "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
