@@ -89,6 +89,8 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_MXFP8_1X32 = 2 } moe_precision;
 
 /* call_flags of moe_forward */
 #define MOE_ACCUMULATE_OUT 0x1u /* out = round(out + sum_k s*h3) (shared expert first) */
+#define MOE_FUSED_LAUNCH   0x4u /* inference, MXFP8: the whole forward in one
+                                   launch (see moe_forward)                    */
 #define MOE_SAVE_INPUT_ONLY 0x2u /* training: `saved` is an input-only state of
                                     moe_saved_input_bytes (routing, scores, a
                                     copy of x); needs a MOE_REPLAY context    */
@@ -292,6 +294,19 @@ MOE_API moe_status prepare_block_scaled_weight(const void* w, int32_t E, int32_t
  *              scores and a copy of x there and nothing of the expert
  *              state, which the backward rebuilds.
  * T may be 0 (nothing is enqueued).  T > max_tokens gives MOE_ERR_CAPACITY.
+ *
+ * MOE_FUSED_LAUNCH ([DM] section 05, "Kernel Pipelines: Staged and Mega":
+ * the Mega forward joins W13 and W2 in one grid with readiness counters):
+ * the routing, gather, W13 + SwiGLU GEMM, W2 GEMM and combine run as one
+ * persistent cooperative launch (at most one CTA per SM) whose CTAs wait on
+ * counters in the context's scratch for the records they consume; a
+ * decode-sized step pays one launch instead of five, and the W2 weights
+ * stream while W13 runs.  The result equals the staged forward's bit for
+ * bit.  Inference only (saved == NULL), MXFP8 contexts, d_model % 256 == 0,
+ * T*top_k <= 1024 and T*top_k/128 + min(num_experts, T*top_k) < 1024;
+ * otherwise MOE_ERR_UNSUPPORTED (MOE_POST_NORM too).  A wait that runs past
+ * its deadline sets MOE_DEV_ERR_TIMEOUT and the kernel returns; the
+ * context stays usable.  Stage timing records one stage (the whole launch).
  */
 MOE_API moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* topk_ids,
                        const float* topk_scores, const moe_weight* W13, const moe_weight* W2,
@@ -424,22 +439,27 @@ MOE_API moe_status moe_ctx_set_max_ctas(moe_ctx* ctx, int max_ctas);
  * KV cache at start-up, a plugin handed a stream but no allocator, or a
  * latency-critical loop that must not call cudaMalloc because it can
  * synchronise the whole device.  It runs the same kernels as an inference
- * moe_forward (no saved state) without a context: every intermediate lives
- * in one file-scope device array of MOE_STATIC_SCRATCH_BYTES, which every GPU
- * that loads this library holds until the process exits.  It calls no
- * cudaMalloc/cudaFree and no allocating library routine.
+ * moe_forward (no saved state), in the same launch configuration, so its
+ * output equals moe_forward's bit for bit; it needs no context: every
+ * intermediate lives in one file-scope device array of
+ * MOE_STATIC_SCRATCH_BYTES, which every GPU that loads this library holds
+ * until the process exits.  It calls no cudaMalloc/cudaFree and no
+ * allocating library routine.
  *   cfg         host struct: d_model, d_ff, num_experts, top_k, precision
  *               (max_tokens and MOE_TRAINING are ignored; MOE_DEBUG_CHECKS
  *               is honoured; MOE_POST_NORM, whose gamma lives in a context,
  *               returns MOE_ERR_UNSUPPORTED)
  *   T, x, topk_ids, topk_scores, W13, W2, out, call_flags: as moe_forward
- *   device_error_word  device uint32 that receives the MOE_DEV_ERR_* bits
- *               (ORed in, never cleared here); NULL uses a word inside the
- *               static array that each call clears and nobody reads.
+ *               (W13/W2 prepared 32x32 or 1x32 for MXFP8)
+ *   device_error_word  required: a 4-byte aligned device uint32 owned by
+ *               the caller that receives the MOE_DEV_ERR_* bits of the call
+ *               (ORed in, never cleared here: the caller reads and clears
+ *               it).  NULL returns MOE_ERR_INVALID_ARG.
  * Returns MOE_ERR_CAPACITY when the call's buffers do not fit the array.
  * They need about R*(D + F + 2D) bytes for MXFP8 (R*(2D + 2F + 2D) for BF16),
- * with R = T*top_k + 31*num_experts rounded up to 128, plus 128, plus
- * routing arrays of a few bytes per route.
+ * with R = T*top_k + 31*min(num_experts, T*top_k) rounded up to 128, plus
+ * 128, plus routing arrays of a few bytes per route: a decode step of up to
+ * 8 tokens fits at D = 7168, F = 2048, E = 384, top_k = 6 in MXFP8.
  * The first call on a device takes the array's device address
  * (cudaGetSymbolAddress) and sets kernel attributes, so make it before any
  * stream capture.  Every call shares the array and finds the previous call's

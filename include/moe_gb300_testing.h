@@ -44,10 +44,20 @@ typedef enum {
                               dgamma partial sums [ceil(T_max/64)][D]          */
   MOE_BUF_REPLAY = 17,     /* MOE_REPLAY: a full saved state (same layout) that
                               a backward with MOE_REPLAY_FORWARD rebuilds       */
-  MOE_BUF_NUM = 18
+  MOE_BUF_SYNC = 18,       /* int32 counters of the single-launch forward:
+                              3 + 2*B_cap words, zero between launches          */
+  MOE_BUF_NUM = 19
 } moe_buffer;
 
 MOE_API moe_status moe_ctx_buffer(moe_ctx* ctx, int which, void** dev_ptr, size_t* bytes);
+
+/* Failure test of the single-launch forward (MOE_FUSED_LAUNCH): with
+ * stall != 0 its W2 tiles wait for one more finished W13 tile than exists
+ * (a count nothing reaches), so their waits run out; every counter wait of
+ * that launch gives up after wait_cycles SM cycles (> 0; the default is
+ * about 2 s) and sets MOE_DEV_ERR_TIMEOUT.  stall = 0 and wait_cycles = 0
+ * restore the defaults.  Applies to later calls; no device access. */
+MOE_API moe_status moe_ctx_test_fused_stall(moe_ctx* ctx, int stall, int64_t wait_cycles);
 
 #ifdef __cplusplus
 }

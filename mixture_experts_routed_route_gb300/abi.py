@@ -38,6 +38,7 @@ MOE_POST_NORM = 0x4
 MOE_REPLAY = 0x8
 MOE_ACCUMULATE_OUT = 0x1
 MOE_SAVE_INPUT_ONLY = 0x2
+MOE_FUSED_LAUNCH = 0x4
 MOE_ACCUMULATE_DX = 0x1
 MOE_DW_FP32 = 0x2
 MOE_DW_ACCUMULATE = 0x4
@@ -54,8 +55,8 @@ MOE_SAVED_NUM_FIELDS = 18
 (MOE_BUF_XROW, MOE_BUF_XROW_SCALE, MOE_BUF_H2ROW, MOE_BUF_H2ROW_SCALE, MOE_BUF_H3, MOE_BUF_DH3ROW,
  MOE_BUF_DH3ROW_SCALE, MOE_BUF_DH3COL, MOE_BUF_DH3COL_SCALE, MOE_BUF_DH1ROW, MOE_BUF_DH1ROW_SCALE,
  MOE_BUF_DH1COL, MOE_BUF_DH1COL_SCALE, MOE_BUF_DXR, MOE_BUF_ROUTING, MOE_BUF_ERROR, MOE_BUF_NORM,
- MOE_BUF_REPLAY) = range(18)
-MOE_BUF_NUM = 18
+ MOE_BUF_REPLAY, MOE_BUF_SYNC) = range(19)
+MOE_BUF_NUM = 19
 
 
 class moe_config(ctypes.Structure):
@@ -110,6 +111,7 @@ _SIGNATURES = {
     "moe_ctx_stage_times": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.c_int]),
     "moe_ctx_launch_count": (ctypes.c_uint64, [_P]),
     "moe_ctx_set_max_ctas": (ctypes.c_int, [_P, ctypes.c_int]),
+    "moe_ctx_test_fused_stall": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64]),
     "moe_ctx_set_post_norm": (ctypes.c_int, [_P, _P, ctypes.c_float]),
     "moe_post_norm_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "moe_weight_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
@@ -302,6 +304,10 @@ def moe_ctx_set_max_ctas(ctx, max_ctas):
     _check("moe_ctx_set_max_ctas", LIB.moe_ctx_set_max_ctas(ctx, max_ctas))
 
 
+def moe_ctx_test_fused_stall(ctx, stall, wait_cycles=0):
+    _check("moe_ctx_test_fused_stall", LIB.moe_ctx_test_fused_stall(ctx, int(stall), int(wait_cycles)))
+
+
 def moe_ctx_set_post_norm(ctx, gamma, eps):
     _check("moe_ctx_set_post_norm", LIB.moe_ctx_set_post_norm(ctx, _ptr(gamma), eps))
 
@@ -311,8 +317,8 @@ def moe_post_norm_backward(ctx, saved, dout, dx_pre, dgamma, stream=None):
            LIB.moe_post_norm_backward(ctx, _ptr(saved), _ptr(dout), _ptr(dx_pre), _ptr(dgamma), _stream(stream)))
 
 
-def moe_forward_static_scratch(cfg, T, x, topk_ids, topk_scores, W13, W2, out, call_flags=0,
-                               device_error_word=None, stream=None):
+def moe_forward_static_scratch(cfg, T, x, topk_ids, topk_scores, W13, W2, out, device_error_word, call_flags=0,
+                               stream=None):
     _check("moe_forward_static_scratch",
            LIB.moe_forward_static_scratch(ctypes.byref(cfg), T, _ptr(x), _ptr(topk_ids), _ptr(topk_scores),
                                           ctypes.byref(W13), ctypes.byref(W2), _ptr(out), call_flags,

@@ -27,6 +27,8 @@ struct moe_ctx {
   int device;
   int num_sms;
   int max_ctas = 0;   // moe_ctx_set_max_ctas (0: num_sms)
+  int fused_stall = 0;             // moe_ctx_test_fused_stall
+  long long fused_wait = 0;        // counter-wait limit of the single-launch forward (0: default)
   const void* norm_gamma = nullptr;   // moe_ctx_set_post_norm (MOE_POST_NORM)
   float norm_eps = 0.0f;
   int64_t r_cap;
@@ -171,6 +173,7 @@ ScratchLayout scratch_layout(const moe_config* c) {
   }
   if (train && (c->flags & MOE_REPLAY)) sz[MOE_BUF_REPLAY] = saved_layout(c).total;
   sz[MOE_BUF_ROUTING] = saved_layout(c).routing_bytes;
+  if (!train && mx) sz[MOE_BUF_SYNC] = (3 + 2 * B) * sizeof(int);   // single-launch forward counters
   sz[MOE_BUF_ERROR] = 32;   // error word at 0, clip counters at 16
   size_t off = 0;
   for (int i = 0; i < MOE_BUF_NUM; ++i) {
@@ -198,127 +201,6 @@ RoutingPtrs routing_ptrs(uint8_t* base, const SavedLayout& L) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
-// ------------------------------------------------------------ tensor maps
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// 2D operand map over a row-major [rows, cols] matrix; boxes are
-// `row_bytes` (128, 64 or 32) wide with the matching swizzle and `box_rows`
-// tall.
-bool make_tmap(CUtensorMap* tm, const void* base, bool mx, int64_t rows, int64_t cols, int box_rows,
-               int row_bytes = 128) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const int esz = mx ? 1 : 2;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esz)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes / esz), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                : (row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
-  const CUresult r = fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// Weight tiles per stage of a grouped-M store GEMM whose output has `n`
-// features: two adjacent 128-row tiles share each loaded
-// activation box and its scales (half the activation traffic per weight
-// byte) when n is a multiple of 256, else one.
-int pair_tiles(int64_t n) { return n % 256 == 0 ? 2 : 1; }
-
-// The narrow-box maps a weight-gradient GEMM uses for a short last stage.
-bool make_narrow_tmaps(GemmLaunch* g, const void* a, int64_t a_rows, const void* b, int64_t b_rows, bool mx,
-                       int64_t cols) {
-  return make_tmap(&g->aux[0], a, mx, a_rows, cols, 128, 64) && make_tmap(&g->aux[1], b, mx, b_rows, cols, 128, 64) &&
-         make_tmap(&g->aux[2], a, mx, a_rows, cols, 128, 32) && make_tmap(&g->aux[3], b, mx, b_rows, cols, 128, 32);
-}
-
-// A tensor map of any rank (dims / box innermost first, byte strides of
-// dims 1..rank-1), no interleave.
-bool make_tmap_nd(CUtensorMap* tm, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
-                  const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return fn(tm, dt, rank, const_cast<void*>(base), const_cast<cuuint64_t*>(dims), const_cast<cuuint64_t*>(strides),
-            const_cast<cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// The larger boxes a grouped-M GEMM loads with (fewer copies per stage for
-// the producer thread to issue):
-//  * both A tiles of a stage in one copy: a 256-row box when they are
-//    adjacent (store GEMMs with two tiles per stage), a 3D box over
-//    [2E halves][F rows][K] when they are W13's gate and up halves
-//    (`halves_f` = F), and likewise their two MXFP8 scale atoms, read as
-//    [row tiles][K/128][128 words] (adjacent) or [2E][F/128][K/128][128]
-//    (halves) from `a_sf`;
-//  * a full 128-row routing block of B in one box.
-bool make_grouped_m_boxes(GemmLaunch* g, const void* a, int64_t a_rows, const void* a_sf, const void* b,
-                          int64_t b_rows, bool mx, int64_t cols, int64_t halves_f = 0) {
-  const int esz = mx ? 1 : 2;
-  const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const cuuint64_t ks = static_cast<cuuint64_t>(cols / 128), atom = 512;
-  if (g->na == 2 && g->epi == kEpiStore) {
-    if (!make_tmap(&g->aux[0], a, mx, a_rows, cols, 256)) return false;
-    if (mx) {
-      const cuuint64_t d[3] = {128, ks, static_cast<cuuint64_t>(a_rows / 128)};
-      const cuuint64_t st[2] = {atom, ks * atom};
-      const cuuint32_t bx[3] = {128, 1, 2};
-      if (!make_tmap_nd(&g->aux[2], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a_sf, d, st, bx, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return false;
-    }
-    g->p.a_pair_box = 1;
-  } else if (g->na == 2 && g->epi == kEpiSwigluFwd && halves_f > 0 && halves_f % 128 == 0) {
-    const cuuint64_t d[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(halves_f),
-                             static_cast<cuuint64_t>(a_rows / halves_f)};
-    const cuuint64_t st[2] = {static_cast<cuuint64_t>(cols * esz), static_cast<cuuint64_t>(halves_f * cols * esz)};
-    const cuuint32_t bx[3] = {static_cast<cuuint32_t>(128 / esz), 128, 2};
-    if (!make_tmap_nd(&g->aux[0], dt, 3, a, d, st, bx, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
-    if (mx) {
-      const cuuint64_t ft = static_cast<cuuint64_t>(halves_f / 128);
-      const cuuint64_t d4[4] = {128, ks, ft, static_cast<cuuint64_t>(a_rows / halves_f)};
-      const cuuint64_t st4[3] = {atom, ks * atom, ft * ks * atom};
-      const cuuint32_t bx4[4] = {128, 1, 1, 2};
-      if (!make_tmap_nd(&g->aux[2], CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, a_sf, d4, st4, bx4,
-                        CU_TENSOR_MAP_SWIZZLE_NONE))
-        return false;
-    }
-    g->p.a_pair_box = 2;
-  }
-  if (!make_tmap(&g->aux[1], b, mx, b_rows, cols, 128)) return false;
-  g->p.b_full_box = 1;
-  return true;
-}
-
-// Output map of a BF16 weight gradient [rows, cols]: boxes of 64 columns
-// (128 bytes) x 128 rows in the 128-byte swizzle the epilogue stages.
-bool make_out_tmap(CUtensorMap* tm, void* base, int64_t rows, int64_t cols) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-  cuuint32_t box[2] = {64, 128};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -361,46 +243,26 @@ cudaError_t stage_mark(moe_ctx* c, int pass, int idx, cudaStream_t s) {
   return cudaEventRecord(c->ev[pass][idx], s);
 }
 
-// Gather x (the row bundle; with `act`, also the column bundle into act's
-// XCOL fields) and run the W13 + SwiGLU GEMM (with `act`, h1 and the h2
-// column bundle into act's fields).  `act` is a full saved state (a
-// training forward's, or the context's replay scratch) or null (inference,
-// input-only states).  `marks`: record the forward's stage events and count
-// clip statistics (off when a backward replays these stages).
-moe_status run_gather_w13(moe_ctx* ctx, const void* x, const RoutingPtrs& rp, const moe_weight* W13, uint8_t* act,
-                          const SavedLayout& SL, bool marks, int sms, cudaStream_t stream) {
+// The W13 + SwiGLU GEMM of a forward (or replay) into *g1: x row bundle
+// from scratch, h2 row bundle to scratch; with `act` (a full saved state),
+// also h1 and the h2 column bundle into act's fields.  False if a tensor map
+// cannot be encoded.
+bool fill_w13(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W13, uint8_t* act, const SavedLayout& SL,
+              bool marks, GemmLaunch* g1) {
   const moe_config& c = ctx->cfg;
-  const int D = c.d_model, F = c.d_ff, E = c.num_experts, K = c.top_k;
+  const int D = c.d_model, F = c.d_ff, E = c.num_experts;
   const bool mx = c.precision == MOE_MXFP8;
   const int64_t R = ctx->r_cap;
-  if (act) {
-    // row bundle (W13 operand) and column bundle (W13 WGRAD operand) in one pass
-    CUtensorMap tr, tc;
-    if (mx && (!make_tmap(&tr, B(ctx, MOE_BUF_XROW), true, R, D, 128) ||
-               !make_tmap(&tc, act + SL.off[MOE_SAVED_XCOL], true, D, R, 128)))
-      return MOE_ERR_CUDA;
-    MOE_TRY(launch_gather_both(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
-                               act + SL.off[MOE_SAVED_XCOL], mx ? act + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr,
-                               static_cast<int>(R), static_cast<int>(ctx->b_cap), sms, stream, &tr, &tc));
-  } else {
-    MOE_TRY(launch_gather_rows(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
-                               static_cast<int>(R), sms, stream));
-  }
-  ctx->launches += 1;
-  if (marks) MOE_TRY(stage_mark(ctx, 0, 2, stream));
-
-  // ---- W13 + SwiGLU
-  GemmLaunch g1{};
-  g1.mx = mx;
-  g1.na = 2;
-  g1.epi = kEpiSwigluFwd;
-  g1.mode = kGroupedM;
-  if (!make_tmap(&g1.tmA, W13->data, mx, static_cast<int64_t>(E) * 2 * F, D, 128) ||
-      !make_tmap(&g1.tmB, B(ctx, MOE_BUF_XROW), mx, R, D, 32) ||
-      !make_grouped_m_boxes(&g1, W13->data, static_cast<int64_t>(E) * 2 * F, W13->scale, B(ctx, MOE_BUF_XROW), R,
+  g1->mx = mx;
+  g1->na = 2;
+  g1->epi = kEpiSwigluFwd;
+  g1->mode = kGroupedM;
+  if (!make_tmap(&g1->tmA, W13->data, mx, static_cast<int64_t>(E) * 2 * F, D, 128) ||
+      !make_tmap(&g1->tmB, B(ctx, MOE_BUF_XROW), mx, R, D, 32) ||
+      !make_grouped_m_boxes(g1, W13->data, static_cast<int64_t>(E) * 2 * F, W13->scale, B(ctx, MOE_BUF_XROW), R,
                             mx, D, F))
-    return MOE_ERR_CUDA;
-  GemmParams& p1 = g1.p;
+    return false;
+  GemmParams& p1 = g1->p;
   p1.hdr = rp.hdr;
   p1.blocks = rp.blocks;
   p1.poffsets = rp.poffsets;
@@ -432,7 +294,76 @@ moe_status run_gather_w13(moe_ctx* ctx, const void* x, const RoutingPtrs& rp, co
   p1.swiglu_limit = c.swiglu_limit;
   p1.clip = (marks && c.swiglu_limit > 0.0f) ? ctx->clip : nullptr;   // a replay counts no clips again
   p1.err = ctx->err;
-  g1.max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
+  g1->max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
+  return true;
+}
+
+// The W2 GEMM into *g2: h3 = h2 W2[e]^T from the h2 row bundle in scratch.
+bool fill_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uint8_t* h3, GemmLaunch* g2) {
+  const moe_config& c = ctx->cfg;
+  const int D = c.d_model, F = c.d_ff, E = c.num_experts;
+  const bool mx = c.precision == MOE_MXFP8;
+  const int64_t R = ctx->r_cap;
+  g2->mx = mx;
+  g2->na = pair_tiles(D);
+  g2->epi = kEpiStore;
+  g2->mode = kGroupedM;
+  if (!make_tmap(&g2->tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128) ||
+      !make_tmap(&g2->tmB, B(ctx, MOE_BUF_H2ROW), mx, R, F, 32) ||
+      !make_grouped_m_boxes(g2, W2->data, static_cast<int64_t>(E) * D, W2->scale, B(ctx, MOE_BUF_H2ROW), R, mx, F))
+    return false;
+  GemmParams& p2 = g2->p;
+  p2.hdr = rp.hdr;
+  p2.blocks = rp.blocks;
+  p2.poffsets = rp.poffsets;
+  p2.E = E;
+  p2.b_box_rows = 32;
+  p2.n_tiles = D / (128 * g2->na);
+  p2.K = F;
+  p2.a_rows_per_expert = D;
+  p2.sfa = W2->scale;
+  p2.sfa_ts = F / 128;
+  p2.sfb = B(ctx, MOE_BUF_H2ROW_SCALE);
+  p2.sfb_ts = F / 128;
+  p2.out0 = h3;
+  p2.out0_pitch = D;
+  p2.F = F;
+  p2.err = ctx->err;
+  g2->max_tiles = static_cast<int>(ctx->b_cap * p2.n_tiles);
+  return true;
+}
+
+// Gather x (the row bundle; with `act`, also the column bundle into act's
+// XCOL fields) and run the W13 + SwiGLU GEMM (with `act`, h1 and the h2
+// column bundle into act's fields).  `act` is a full saved state (a
+// training forward's, or the context's replay scratch) or null (inference,
+// input-only states).  `marks`: record the forward's stage events and count
+// clip statistics (off when a backward replays these stages).
+moe_status run_gather_w13(moe_ctx* ctx, const void* x, const RoutingPtrs& rp, const moe_weight* W13, uint8_t* act,
+                          const SavedLayout& SL, bool marks, int sms, cudaStream_t stream) {
+  const moe_config& c = ctx->cfg;
+  const int D = c.d_model, F = c.d_ff, E = c.num_experts, K = c.top_k;
+  const bool mx = c.precision == MOE_MXFP8;
+  const int64_t R = ctx->r_cap;
+  if (act) {
+    // row bundle (W13 operand) and column bundle (W13 WGRAD operand) in one pass
+    CUtensorMap tr, tc;
+    if (mx && (!make_tmap(&tr, B(ctx, MOE_BUF_XROW), true, R, D, 128) ||
+               !make_tmap(&tc, act + SL.off[MOE_SAVED_XCOL], true, D, R, 128)))
+      return MOE_ERR_CUDA;
+    MOE_TRY(launch_gather_both(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
+                               act + SL.off[MOE_SAVED_XCOL], mx ? act + SL.off[MOE_SAVED_XCOL_SCALE] : nullptr,
+                               static_cast<int>(R), static_cast<int>(ctx->b_cap), sms, stream, &tr, &tc));
+  } else {
+    MOE_TRY(launch_gather_rows(mx, false, x, D, K, rp, B(ctx, MOE_BUF_XROW), B(ctx, MOE_BUF_XROW_SCALE),
+                               static_cast<int>(R), sms, stream));
+  }
+  ctx->launches += 1;
+  if (marks) MOE_TRY(stage_mark(ctx, 0, 2, stream));
+
+  // ---- W13 + SwiGLU
+  GemmLaunch g1{};
+  if (!fill_w13(ctx, rp, W13, act, SL, marks, &g1)) return MOE_ERR_CUDA;
   MOE_TRY(launch_gemm(g1, sms, stream));
   ctx->launches += 1;
   if (marks) MOE_TRY(stage_mark(ctx, 0, 3, stream));
@@ -448,36 +379,62 @@ moe_status run_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uin
   const int64_t R = ctx->r_cap;
   // ---- W2
   GemmLaunch g2{};
-  g2.mx = mx;
-  g2.na = pair_tiles(D);
-  g2.epi = kEpiStore;
-  g2.mode = kGroupedM;
-  if (!make_tmap(&g2.tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128) ||
-      !make_tmap(&g2.tmB, B(ctx, MOE_BUF_H2ROW), mx, R, F, 32) ||
-      !make_grouped_m_boxes(&g2, W2->data, static_cast<int64_t>(E) * D, W2->scale, B(ctx, MOE_BUF_H2ROW), R, mx, F))
-    return MOE_ERR_CUDA;
-  GemmParams& p2 = g2.p;
-  p2.hdr = rp.hdr;
-  p2.blocks = rp.blocks;
-  p2.poffsets = rp.poffsets;
-  p2.E = E;
-  p2.b_box_rows = 32;
-  p2.n_tiles = D / (128 * g2.na);
-  p2.K = F;
-  p2.a_rows_per_expert = D;
-  p2.sfa = W2->scale;
-  p2.sfa_ts = F / 128;
-  p2.sfb = B(ctx, MOE_BUF_H2ROW_SCALE);
-  p2.sfb_ts = F / 128;
-  p2.out0 = h3;
-  p2.out0_pitch = D;
-  p2.F = F;
-  p2.err = ctx->err;
-  g2.max_tiles = static_cast<int>(ctx->b_cap * p2.n_tiles);
+  if (!fill_w2(ctx, rp, W2, h3, &g2)) return MOE_ERR_CUDA;
   MOE_TRY(launch_gemm(g2, sms, stream));
   ctx->launches += 1;
   return MOE_OK;
 }
+// The whole inference forward as one launch (MOE_FUSED_LAUNCH): the same
+// tensor maps and GEMM parameters as the staged launches, and the counters
+// in the context's sync buffer.
+moe_status run_fused_forward(moe_ctx* ctx, int T, const void* x, const int32_t* ids, const float* scores,
+                             const RoutingPtrs& rp, const moe_weight* W13, const moe_weight* W2, void* out,
+                             bool accumulate, int sms, cudaStream_t stream) {
+  const moe_config& c = ctx->cfg;
+  const SavedLayout SL = saved_layout(&c);
+  GemmLaunch g1{}, g2{};
+  if (!fill_w13(ctx, rp, W13, nullptr, SL, true, &g1) || !fill_w2(ctx, rp, W2, B(ctx, MOE_BUF_H3), &g2))
+    return MOE_ERR_CUDA;
+  if (g1.p.a_pair_box != 2 || g2.p.a_pair_box != 1 || !g1.p.b_full_box || !g2.p.b_full_box)
+    return MOE_ERR_UNSUPPORTED;
+  FusedLaunch L{};
+  L.a13 = g1.aux[0];
+  L.sf13 = g1.aux[2];
+  L.bx32 = g1.tmB;
+  L.bx128 = g1.aux[1];
+  L.a2 = g2.aux[0];
+  L.sf2 = g2.aux[2];
+  L.bh32 = g2.tmB;
+  L.bh128 = g2.aux[1];
+  FusedArgs& a = L.args;
+  a.ids = ids;
+  a.scores = scores;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.T = T;
+  a.K = c.top_k;
+  a.E = c.num_experts;
+  a.D = c.d_model;
+  a.F = c.d_ff;
+  a.debug = (c.flags & MOE_DEBUG_CHECKS) ? 1 : 0;
+  a.accumulate = accumulate ? 1 : 0;
+  a.rp = rp;
+  a.xrow = B(ctx, MOE_BUF_XROW);
+  a.xsf = B(ctx, MOE_BUF_XROW_SCALE);
+  a.w2 = static_cast<const uint8_t*>(W2->data);
+  a.sync = reinterpret_cast<int*>(B(ctx, MOE_BUF_SYNC));
+  a.b_cap = static_cast<int>(ctx->b_cap);
+  a.wait_cycles = ctx->fused_wait > 0 ? ctx->fused_wait : kWaitTimeoutCycles;
+  a.stall = ctx->fused_stall;
+  a.g13 = g1.p;
+  a.g2 = g2.p;
+  const int64_t tk = static_cast<int64_t>(T) * c.top_k;
+  L.max_blocks = static_cast<int>(tk / 128 + std::min<int64_t>(c.num_experts, tk) + 1);
+  MOE_TRY(launch_fused_forward(L, sms, stream));
+  ctx->launches += 1;
+  return MOE_OK;
+}
+
 }  // namespace
 
 // =================================================================== ABI
@@ -647,6 +604,13 @@ moe_status moe_post_norm_backward(moe_ctx* ctx, const void* saved, const void* d
   return MOE_OK;
 }
 
+moe_status moe_ctx_test_fused_stall(moe_ctx* ctx, int stall, int64_t wait_cycles) {
+  if (!ctx || wait_cycles < 0) return MOE_ERR_INVALID_ARG;
+  ctx->fused_stall = stall ? 1 : 0;
+  ctx->fused_wait = wait_cycles;
+  return MOE_OK;
+}
+
 moe_status moe_ctx_set_max_ctas(moe_ctx* ctx, int max_ctas) {
   if (!ctx || max_ctas < 0) return MOE_ERR_INVALID_ARG;
   ctx->max_ctas = max_ctas;
@@ -753,7 +717,15 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   if (train && !(c.flags & MOE_TRAINING)) return MOE_ERR_INVALID_ARG;
   if (!weight_ok(W13, c.precision, E, 2 * F, D, false) || !weight_ok(W2, c.precision, E, D, F, false))
     return MOE_ERR_INVALID_ARG;
-  if (call_flags & ~(MOE_ACCUMULATE_OUT | MOE_SAVE_INPUT_ONLY)) return MOE_ERR_INVALID_ARG;
+  if (call_flags & ~(MOE_ACCUMULATE_OUT | MOE_SAVE_INPUT_ONLY | MOE_FUSED_LAUNCH)) return MOE_ERR_INVALID_ARG;
+  const bool fused = (call_flags & MOE_FUSED_LAUNCH) != 0;
+  if (fused) {
+    const int64_t tk = static_cast<int64_t>(T) * K;
+    const int64_t max_blocks = tk / 128 + std::min<int64_t>(E, tk) + 1;
+    if (train || c.precision != MOE_MXFP8 || (c.flags & MOE_POST_NORM) || pair_tiles(D) != 2 ||
+        tk > kFusedMaxRoutes || max_blocks >= 1024 || !ctx->buf[MOE_BUF_SYNC])
+      return MOE_ERR_UNSUPPORTED;
+  }
   const bool input_only = (call_flags & MOE_SAVE_INPUT_ONLY) != 0;
   if (input_only && (!train || !(c.flags & MOE_REPLAY))) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
@@ -778,6 +750,12 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   const int sms = ctx->max_ctas > 0 ? std::min(ctx->max_ctas, ctx->num_sms) : ctx->num_sms;
 
   MOE_TRY(stage_mark(ctx, 0, 0, stream));
+  if (fused) {
+    MOE_PASS(run_fused_forward(ctx, T, x, topk_ids, topk_scores, rp, W13, W2, out,
+                               (call_flags & MOE_ACCUMULATE_OUT) != 0, sms, stream));
+    for (int i = 1; i <= MOE_FWD_STAGES; ++i) MOE_TRY(stage_mark(ctx, 0, i, stream));
+    return MOE_OK;
+  }
   MOE_TRY(launch_route(topk_ids, topk_scores, T, K, E, static_cast<int>(R), (c.flags & MOE_DEBUG_CHECKS) ? 1 : 0,
                        rp, ctx->err, stream));
   ctx->launches += 1;
@@ -823,6 +801,9 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   const int sms = ctx->max_ctas > 0 ? std::min(ctx->max_ctas, ctx->num_sms) : ctx->num_sms;
   const int dw_fp32 = (call_flags & MOE_DW_FP32) ? 1 : 0;
   const int dw_acc = (call_flags & MOE_DW_ACCUMULATE) ? 1 : 0;
+  // dW leaves through shared memory and TMA, except a BF16 accumulation
+  // (which rounds old + new once, in the epilogue)
+  const int dw_store = dw_fp32 ? (dw_acc ? kDwAddF32 : kDwStoreF32) : (dw_acc ? kDwDirect : kDwStoreBf16);
 
   // ---- replay: rebuild the expert state of an input-only forward from its
   // saved x and routing, with the forward's own kernels, in the context's
@@ -917,8 +898,8 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p2.out0_pitch = F;
   p2.dw_fp32 = dw_fp32;
   p2.dw_accum = dw_acc;
-  p2.tma_store = (!dw_fp32 && !dw_acc) ? 1 : 0;
-  if (p2.tma_store && !make_out_tmap(&g2.tmC, dW2, static_cast<int64_t>(E) * D, F)) return MOE_ERR_CUDA;
+  p2.tma_store = dw_store;
+  if (dw_store != kDwDirect && !make_out_tmap(&g2.tmC, dW2, static_cast<int64_t>(E) * D, F, dw_fp32 != 0)) return MOE_ERR_CUDA;
   p2.err = ctx->err;
   g2.max_tiles = E * (D / 128) * (F / 128);
   MOE_TRY(launch_gemm(g2, sms, stream));
@@ -985,8 +966,8 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p4.out0_pitch = D;
   p4.dw_fp32 = dw_fp32;
   p4.dw_accum = dw_acc;
-  p4.tma_store = (!dw_fp32 && !dw_acc) ? 1 : 0;
-  if (p4.tma_store && !make_out_tmap(&g4.tmC, dW13, static_cast<int64_t>(E) * 2 * F, D)) return MOE_ERR_CUDA;
+  p4.tma_store = dw_store;
+  if (dw_store != kDwDirect && !make_out_tmap(&g4.tmC, dW13, static_cast<int64_t>(E) * 2 * F, D, dw_fp32 != 0)) return MOE_ERR_CUDA;
   p4.err = ctx->err;
   g4.max_tiles = E * (2 * F / 128) * (D / 128);
   MOE_TRY(launch_gemm(g4, sms, stream));

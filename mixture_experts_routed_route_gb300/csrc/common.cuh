@@ -125,6 +125,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* 
                : "memory");
 }
 
+// 2D tiled reduce-add of the box at (x, y) from shared memory into global
+// memory: each element of the box is added to the global element (in the
+// tensor map's type) by the memory system, once (bulk-group completion).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* tm, const void* smem_src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N committed bulk groups still read shared memory.
@@ -147,6 +157,56 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// -------------------------------------------- grid-level progress counters
+// (the single-launch forward: CTAs publish finished work records in global
+// memory and others wait for them)
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_add_release_gpu(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Order this thread's generic-proxy global accesses with its async-proxy
+// (TMA) accesses: a writer's stores before the release that publishes them,
+// a reader's acquire before the tensor loads that read them.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Ask L2 to fetch `bytes` (a multiple of 16) from global memory.
+__device__ __forceinline__ void prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
+               : "memory");
+}
+
+// Wait until *counter >= target (acquire), for at most `limit` SM cycles;
+// then set kErrTimeout and the CTA's abort flag and return false.  Also
+// returns false once another role of the CTA gave up.
+__device__ __forceinline__ bool wait_counter(const int* counter, int target, long long limit,
+                                             volatile int* abort_flag, uint32_t* err) {
+  if (ld_acquire_gpu(counter) >= target) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (ld_acquire_gpu(counter) >= target) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      *abort_flag = 1;
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+    __nanosleep(128);
+  }
 }
 
 // ------------------------------------------------------------------- tcgen05

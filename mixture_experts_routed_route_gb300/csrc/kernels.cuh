@@ -1,6 +1,8 @@
 // Launch interface of the MoE kernels (internal to the library).
 #pragma once
 
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <mutex>
 
@@ -117,6 +119,11 @@ cudaError_t launch_transpose_bf16(const void* w, int E, int N, int K, void* wT, 
 // ------------------------------------------------------------- grouped GEMM
 
 enum GemmMode { kGroupedM = 0, kGroupedK = 1 };
+// How a weight-gradient epilogue writes dW: plain stores (BF16 accumulate),
+// or staged in shared memory and moved by TMA: a BF16 store, an FP32 store,
+// or an FP32 reduce-add into the existing dW (one FP32 add per element,
+// formed in L2).
+enum DwStore { kDwDirect = 0, kDwStoreBf16 = 1, kDwStoreF32 = 2, kDwAddF32 = 3 };
 enum GemmEpi { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2, kEpiWgrad = 3 };
 
 struct GemmParams {
@@ -156,7 +163,7 @@ struct GemmParams {
   int want_col;
   int dw_fp32;
   int dw_accum;
-  int tma_store;          // weight gradient written through shared memory + TMA
+  int tma_store;          // weight gradient through shared memory + TMA (kDwStore*)
   // grouped-M, both A tiles of a stage in one copy: aux[0] holds their data
   // (1: adjacent 128-row tiles, a 256-row box; 2: gate and up halves F rows
   // apart, a 3D [halves][F][K] box) and aux[2] their two scale atoms (1:
@@ -191,5 +198,81 @@ struct GemmLaunch {
 };
 
 cudaError_t launch_gemm(const GemmLaunch& g, int num_sms, cudaStream_t stream);
+
+// ------------------------------------------------- single-launch forward
+// MXFP8 inference forward in one persistent cooperative grid (fused.cu):
+// routing, gather, W13 + SwiGLU, W2, combine, coordinated by counters in
+// `sync` ((3 + 2 b_cap) ints, zero before the first launch).
+
+// Largest T*K the single-launch forward takes (the routing runs in one CTA
+// and every row block must fit the GEMMs' shared-memory block cache).
+constexpr int kFusedMaxRoutes = 1024;
+
+struct FusedArgs {
+  const int32_t* ids;
+  const float* scores;
+  const __nv_bfloat16* x;
+  __nv_bfloat16* out;
+  int T, K, E, D, F;
+  int debug;        // flag ID -1 routes with a nonzero score
+  int accumulate;   // out = bf16(out + routed sum)
+  RoutingPtrs rp;   // routing arrays, written by CTA 0
+  uint8_t* xrow;    // x row bundle [r_cap, D] and its scale atoms [b_cap][D/128]
+  uint8_t* xsf;
+  const uint8_t* w2;   // W2 codes [E*D, F] (L2 prefetch of a W2 tile's weights)
+  int* sync;
+  int b_cap;
+  long long wait_cycles;   // limit of every counter wait (SM cycles)
+  int stall;               // test only: W2 tiles wait for one W13 tile more than exist
+  GemmParams g13, g2;      // the two GEMMs (g13.out0 = h2 row bundle, g2.out0 = h3)
+};
+
+struct FusedLaunch {
+  CUtensorMap a13, sf13, bx32, bx128;   // W13 gate/up box, their atoms, x bundle 32/128-row boxes
+  CUtensorMap a2, sf2, bh32, bh128;     // W2 256-row box, its atoms, h2 bundle 32/128-row boxes
+  FusedArgs args;
+  int max_blocks;   // bound on the routing's row blocks (grid sizing)
+};
+
+cudaError_t launch_fused_forward(const FusedLaunch& L, int num_sms, cudaStream_t stream);
+
+// ------------------------------------------------------------- tensor maps
+// (host side, tmaps.cu; each returns false when the driver rejects the map)
+
+// The driver's cuTensorMapEncodeTiled, looked up once (null if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
+
+// 2D operand map over a row-major [rows, cols] matrix (E4M3 bytes when mx,
+// else BF16): boxes `row_bytes` (128, 64 or 32) wide with the matching
+// swizzle and `box_rows` tall.
+bool make_tmap(CUtensorMap* tm, const void* base, bool mx, int64_t rows, int64_t cols, int box_rows,
+               int row_bytes = 128);
+
+// A tensor map of any rank (dims / box innermost first, byte strides of
+// dims 1..rank-1), no interleave.
+bool make_tmap_nd(CUtensorMap* tm, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+                  const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw);
+
+// Weight tiles per stage of a grouped-M store GEMM with an n-feature output:
+// 2 when n is a multiple of 256 (two adjacent tiles share each activation
+// box), else 1.
+int pair_tiles(int64_t n);
+
+// The narrow-box maps (64- and 32-byte rows) a weight-gradient GEMM uses for
+// a short last stage, into g->aux[0..3].
+bool make_narrow_tmaps(GemmLaunch* g, const void* a, int64_t a_rows, const void* b, int64_t b_rows, bool mx,
+                       int64_t cols);
+
+// The larger boxes of a grouped-M GEMM (both A tiles of a stage in one
+// copy, their scale atoms in one copy, a full 128-row block of B in one
+// box), into g->aux[0..2]; sets g->p.a_pair_box and g->p.b_full_box.
+// `halves_f` = F for W13's gate and up halves, else 0.
+bool make_grouped_m_boxes(GemmLaunch* g, const void* a, int64_t a_rows, const void* a_sf, const void* b,
+                          int64_t b_rows, bool mx, int64_t cols, int64_t halves_f = 0);
+
+// Output map of a weight gradient [rows, cols], BF16 or FP32: boxes of 128
+// bytes (64 BF16 or 32 FP32 columns) x 128 rows in the 128-byte swizzle the
+// epilogue stages.
+bool make_out_tmap(CUtensorMap* tm, void* base, int64_t rows, int64_t cols, bool fp32 = false);
 
 }  // namespace moe

@@ -8,15 +8,16 @@
 // (route, gather, W13 + SwiGLU, W2, combine) but keeps every intermediate in
 // one file-scope device array instead of a context's cudaMalloc'd scratch.
 //
+// The GEMMs get the same tensor maps, tile pairing and grids as in
+// moe_forward, so the output equals an inference moe_forward's bit for bit.
+//
 // The array (kStaticScratchBytes) exists on every GPU that loads the library
 // and stays allocated until the process exits.  Every call shares it and it
 // keeps the previous call's contents; the routing kernel rewrites every
 // routing array it reads and the gather rewrites every row the GEMMs read, so
-// only the error word has to be cleared, which each call does.  Calls that
-// may overlap on the GPU (different streams, or different host threads
-// without ordering) race on the array.
-#include <cudaTypedefs.h>
-
+// nothing in it needs clearing.  Device errors go to the caller's error word.
+// Calls that may overlap on the GPU (different streams, or different host
+// threads without ordering) race on the array.
 #include <mutex>
 
 #include "kernels.cuh"
@@ -28,7 +29,6 @@ namespace {
 
 constexpr size_t kStaticScratchBytes = 64ull << 20;  // 64 MiB, see MOE_STATIC_SCRATCH_BYTES
 constexpr size_t kAl = 256;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
@@ -63,33 +63,6 @@ moe_status setup_device(DeviceSetup** out) {
   return MOE_OK;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-bool operand_map(CUtensorMap* tm, const void* base, bool mx, int64_t rows, int64_t cols, int box_rows) {
-  auto fn = tmap_encoder();
-  if (!fn) return false;
-  const int esz = mx ? 1 : 2;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esz)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(tm, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool is16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 bool weight_matches(const moe_weight* w, moe_precision prec, int E, int N, int K) {
@@ -101,16 +74,22 @@ bool weight_matches(const moe_weight* w, moe_precision prec, int E, int N, int K
 // Offsets of the call's buffers inside the static array.
 struct StaticLayout {
   size_t hdr, counts, offsets, poffsets, perm, inv, blocks, scores, bstart, row_block;
-  size_t xrow, xrow_sf, h2row, h2row_sf, h3, err, total;
+  size_t xrow, xrow_sf, h2row, h2row_sf, h3, total;
   int64_t r_cap, b_cap;
 };
 
+// At most min(E, T*K) experts receive rows, and each pads its rows to a
+// multiple of 32, so T*K + 31*min(E, T*K) rows hold every routing of T
+// tokens (a one-token decode step at E = 384, K = 6 needs 192 rows, not
+// the 11,910 a bound with 31*E would reserve); each receiving expert adds
+// at most one partial 128-row block.
 StaticLayout static_layout(int T, int D, int F, int E, int K, bool mx) {
   StaticLayout L{};
   const int64_t routes = static_cast<int64_t>(T) * K;
-  const int64_t rows = routes + 31LL * E;
+  const int64_t busy = routes < E ? routes : E;
+  const int64_t rows = routes + 31LL * busy;
   L.r_cap = (rows + 127) / 128 * 128 + 128;
-  L.b_cap = rows / 128 + E + 1;
+  L.b_cap = rows / 128 + busy + 1;
   const size_t esz = mx ? 1 : 2;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -133,7 +112,6 @@ StaticLayout static_layout(int T, int D, int F, int E, int K, bool mx) {
   L.h2row = take(L.r_cap * F * esz);
   L.h2row_sf = mx ? take(L.b_cap * (F / 128) * 512) : 0;
   L.h3 = take(L.r_cap * D * 2);
-  L.err = take(16);
   L.total = o;
   return L;
 }
@@ -156,6 +134,7 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   const bool mx = cfg->precision == MOE_MXFP8;
   if (!weight_matches(W13, cfg->precision, E, 2 * F, D) || !weight_matches(W2, cfg->precision, E, D, F))
     return MOE_ERR_INVALID_ARG;
+  if (!device_error_word || (reinterpret_cast<uintptr_t>(device_error_word) & 3)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !topk_ids || !topk_scores || !out || !is16(x) || !is16(out)) return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(T) * K + 31LL * E > (1LL << 28)) return MOE_ERR_CAPACITY;
@@ -167,10 +146,6 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   if (st != MOE_OK) return st;
   uint8_t* S = dev->scratch;
   uint32_t* err = device_error_word;
-  if (!err) {
-    err = reinterpret_cast<uint32_t*>(S + L.err);
-    if (cudaMemsetAsync(err, 0, sizeof(uint32_t), stream) != cudaSuccess) return MOE_ERR_CUDA;
-  }
   RoutingPtrs rp;
   rp.hdr = reinterpret_cast<int*>(S + L.hdr);
   rp.counts = reinterpret_cast<int*>(S + L.counts);
@@ -199,8 +174,9 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   g1.na = 2;
   g1.epi = kEpiSwigluFwd;
   g1.mode = kGroupedM;
-  if (!operand_map(&g1.tmA, W13->data, mx, static_cast<int64_t>(E) * 2 * F, D, 128) ||
-      !operand_map(&g1.tmB, xrow, mx, R, D, 32))
+  if (!make_tmap(&g1.tmA, W13->data, mx, static_cast<int64_t>(E) * 2 * F, D, 128) ||
+      !make_tmap(&g1.tmB, xrow, mx, R, D, 32) ||
+      !make_grouped_m_boxes(&g1, W13->data, static_cast<int64_t>(E) * 2 * F, W13->scale, xrow, R, mx, D, F))
     return MOE_ERR_CUDA;
   g1.p.hdr = rp.hdr;
   g1.p.blocks = rp.blocks;
@@ -228,18 +204,19 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
 
   GemmLaunch g2{};
   g2.mx = mx;
-  g2.na = 1;
+  g2.na = pair_tiles(D);
   g2.epi = kEpiStore;
   g2.mode = kGroupedM;
-  if (!operand_map(&g2.tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128) ||
-      !operand_map(&g2.tmB, h2, mx, R, F, 32))
+  if (!make_tmap(&g2.tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128) ||
+      !make_tmap(&g2.tmB, h2, mx, R, F, 32) ||
+      !make_grouped_m_boxes(&g2, W2->data, static_cast<int64_t>(E) * D, W2->scale, h2, R, mx, F))
     return MOE_ERR_CUDA;
   g2.p.hdr = rp.hdr;
   g2.p.blocks = rp.blocks;
   g2.p.poffsets = rp.poffsets;
   g2.p.E = E;
   g2.p.b_box_rows = 32;
-  g2.p.n_tiles = D / 128;
+  g2.p.n_tiles = D / (128 * g2.na);
   g2.p.K = F;
   g2.p.a_rows_per_expert = D;
   g2.p.sfa = W2->scale;
@@ -250,7 +227,7 @@ extern "C" moe_status moe_forward_static_scratch(const moe_config* cfg, int32_t 
   g2.p.out0_pitch = D;
   g2.p.F = F;
   g2.p.err = err;
-  g2.max_tiles = static_cast<int>(L.b_cap * (D / 128));
+  g2.max_tiles = static_cast<int>(L.b_cap * g2.p.n_tiles);
   if (launch_gemm(g2, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   if (launch_combine(h3, D, K, rp.inv, rp.scores, out, T, (call_flags & MOE_ACCUMULATE_OUT) != 0, sms, stream) !=

@@ -9,8 +9,10 @@ kernels", section 05: the weight gradients are stored in BF16 or FP32):
 * an expert no route reaches gets zeros, or keeps its old values when
   accumulating.
 
-All four go through the same GEMM; the last three use the plain-store
-epilogue, the first the staged tensor store."""
+All four go through the same GEMM and differ in the epilogue: BF16 and FP32
+overwrite stage the tile in shared memory and store it with TMA, FP32
+accumulate stages it and adds it with a TMA reduce-add (the one FP32 add is
+formed in L2), BF16 accumulate uses plain stores (it rounds old + new once)."""
 
 import numpy as np
 import pytest
