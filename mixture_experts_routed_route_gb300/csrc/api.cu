@@ -421,7 +421,6 @@ moe_status run_fused_forward(moe_ctx* ctx, int T, const void* x, const int32_t* 
   a.rp = rp;
   a.xrow = B(ctx, MOE_BUF_XROW);
   a.xsf = B(ctx, MOE_BUF_XROW_SCALE);
-  a.w2 = static_cast<const uint8_t*>(W2->data);
   a.sync = reinterpret_cast<int*>(B(ctx, MOE_BUF_SYNC));
   a.b_cap = static_cast<int>(ctx->b_cap);
   a.wait_cycles = ctx->fused_wait > 0 ? ctx->fused_wait : kWaitTimeoutCycles;

@@ -107,6 +107,22 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* t
       : "memory");
 }
 
+// Ask L2 to fetch the box at (x, y[, z]) of a tensor map (no shared memory
+// is written and nothing waits for it).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* tm, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* tm, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // 1D bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
 // from global to shared memory, completion counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
@@ -182,12 +198,6 @@ __device__ __forceinline__ void red_add_release_gpu(int* p, int v) {
 // a reader's acquire before the tensor loads that read them.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Ask L2 to fetch `bytes` (a multiple of 16) from global memory.
-__device__ __forceinline__ void prefetch_l2(const void* gsrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
-               : "memory");
 }
 
 // Wait until *counter >= target (acquire), for at most `limit` SM cycles;

@@ -6,19 +6,18 @@
 // launches; the Mega forward joins W13 and W2 in one grid whose resident
 // CTAs repeat work records on fixed warp roles (the same TMA, MMA and
 // epilogue roles serve W13 and W2) and coordinate through readiness
-// counters in global memory.  Here the grid also takes the routing (first,
-// on CTA 0), the gather and the combine, so a decode-sized step is one
-// launch.  "Mixture of Experts: How Routing Becomes GPU Computation",
+// counters in global memory.  Here the grid also takes the routing, the
+// gather and the combine, so a decode-sized step is one launch.  "Mixture of Experts: How Routing Becomes GPU Computation",
 // section 6: with few tokens, W13 has too few output tiles to fill the GPU;
-// the CTAs that hold W2 tiles ask L2 for their weight slabs while the W13
-// tiles they depend on are still running, so the W2 weights stream beside
-// W13's instead of after them.
+// the CTAs that hold W2 tiles ask L2 for their first weight stages while
+// the W13 tiles they depend on are still running, and every producer asks
+// L2 for the weight stages a few ahead of the ones it loads.
 //
 // Work records, numbered once the routing is known (nblk row blocks):
-//   [0, nblk)                      gather block b (x rows -> MXFP8 row bundle)
-//   [nblk, nblk (1 + n13))         W13 + SwiGLU tile (b, n), block-major
+//   [0, nblk gp)                   gather block b, column part p (x rows -> MXFP8 row bundle)
+//   [.., + nblk n13)               W13 + SwiGLU tile (b, n), block-major
 //   [.., + nblk n2)                W2 tile (b, n), block-major
-//   [.., + T)                      combine token t
+//   [.., + 4 T)                    combine: a quarter of token t's columns
 // CTA i takes records i, i + grid, ... in increasing order, and every role
 // of a CTA walks that sequence in order.  A record waits only for records
 // numbered below it: a W13 tile for its block's gather, a W2 tile for its
@@ -32,12 +31,16 @@
 // the same row-bundle codes, the same GEMM stages and MMA order, the same
 // epilogues, the same fixed-order FP32 combine.
 //
+// Every CTA computes the routing's row blocks (its work records) from the
+// IDs itself, and a gather record ranks its block's routes from the IDs, so
+// no record waits for the routing arrays; the last CTA writes those arrays
+// (the routing kernel's layout), which only the combine reads.
+//
 // Counters (ints in the context's scratch, zero between launches):
-//   [0] routing published   [1] CTAs finished   [2] W2 tiles finished
+//   [0] routing arrays published   [1] CTAs finished   [2] W2 tiles finished
 //   [3 + b]                 gather of block b finished
 //   [3 + b_cap + b]         W13 tiles of block b finished
-// CTA 0 zeroes the per-block words and [2] before it publishes the routing;
-// the last CTA to finish returns [0] and [1] to zero for the next launch.
+// The last CTA to finish returns them all to zero for the next launch.
 #include <algorithm>
 
 #include "gemm_core.cuh"
@@ -47,22 +50,33 @@ namespace moe {
 namespace {
 
 using CF = Cfg<true, 2, kGroupedM>;
-constexpr int kFusedThreads = CF::THREADS;     // producer, MMA, 8 epilogue warps, scale copier
+constexpr int kFusedThreads = CF::THREADS;     // producer, MMA (and scale copies), 8 epilogue warps, one idle warp
 constexpr int kEpiThreads = CF::EPI_THREADS;
+constexpr int kFusedSmem = CF::SMEM + kBlockRows * 4;   // + a gather record's routes
+constexpr int kPrefetch = 8;   // weight stages asked of L2 ahead of their loads
+constexpr int kCombineParts = 4;   // combine records per token (D % (8 kCombineParts) == 0)
+
+// Gather records per row block: column parts of D / gp columns, a multiple
+// of 128 (whole scale atoms), so one block's gather spreads over gp CTAs.
+__host__ __device__ __forceinline__ int gather_parts(int D) {
+  const int atoms = D / 128;
+  return atoms % 8 == 0 ? 8 : (atoms % 4 == 0 ? 4 : (atoms % 2 == 0 ? 2 : 1));
+}
 
 struct Rec {
   int kind;   // 0 gather, 1 W13 tile, 2 W2 tile, 3 combine
-  int b, n;   // block and slice (tiles), block (gather), token (combine: b)
+  int b, n;   // block and slice (tiles), block and column part (gather), combine part (b)
 };
 
-__device__ __forceinline__ Rec record(int u, int nblk, int n13, int n2) {
+__device__ __forceinline__ Rec record(int u, int nblk, int gp, int n13, int n2) {
   Rec r{};
-  if (u < nblk) {
+  if (u < nblk * gp) {
     r.kind = 0;
-    r.b = u;
+    r.b = u / gp;
+    r.n = u - r.b * gp;   // column part
     return r;
   }
-  u -= nblk;
+  u -= nblk * gp;
   if (u < nblk * n13) {
     r.kind = 1;
     r.b = u / n13;
@@ -91,8 +105,52 @@ __device__ __forceinline__ Tile tile_of(const FusedArgs& fa, const Rec& r, const
                      : decode_tile<kGroupedM, CF::BK, 256>(fa.g2, w, mc);
 }
 
+// ------------------------------------------------------- local block list
+// Every CTA, all threads: the row blocks of the routing, computed from the
+// IDs into the CTA's block cache (the same blocks, in the same order, as the
+// routing kernel's list; the fourth field holds the rank of the block's
+// first row among its expert's routes), so no CTA waits for another to
+// learn its work records.  `ws` is shared scratch of E ints.
+__device__ void local_blocks(const FusedArgs& fa, int* ws, int4* cache, volatile int* s_nblk) {
+  const int E = fa.E, TK = fa.T * fa.K;
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int e = tid; e < E; e += blockDim.x) ws[e] = 0;
+  __syncthreads();
+  for (int i = tid; i < TK; i += blockDim.x) {
+    const int id = __ldg(fa.ids + i);
+    if (id >= 0 && id < E) atomicAdd(&ws[id], 1);
+  }
+  __syncthreads();
+  if (tid < 32) {
+    int cp = 0, cb = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int c = e < E ? ws[e] : 0;
+      const int pc = (c + kPad - 1) / kPad * kPad;
+      const int nb = (pc + kBlockRows - 1) / kBlockRows;
+      int ip = pc, ib = nb;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int b = __shfl_up_sync(0xFFFFFFFFu, ip, o);
+        const int d = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+        if (lane >= o) {
+          ip += b;
+          ib += d;
+        }
+      }
+      const int ep = cp + ip - pc, eb = cb + ib - nb;
+      for (int j = 0; j < nb; ++j)
+        cache[eb + j] = make_int4(e, ep + j * kBlockRows, min(kBlockRows, pc - j * kBlockRows), j * kBlockRows);
+      cp += __shfl_sync(0xFFFFFFFFu, ip, 31);
+      cb += __shfl_sync(0xFFFFFFFFu, ib, 31);
+    }
+    if (lane == 0) *s_nblk = cb;
+  }
+  __syncthreads();
+}
+
 // ------------------------------------------------------------------ routing
-// CTA 0, all threads: the same arrays as the routing kernel (counts,
+// One CTA, all threads: the same arrays as the routing kernel (counts,
 // exclusive prefixes plain and padded to 32 rows, stable expert-major
 // permutation and inverse, row blocks, the routing copy of the scores).
 // `ws` is shared scratch of 3 E + 2 ints.
@@ -197,61 +255,101 @@ __device__ void fused_route(const FusedArgs& fa, int* ws) {
 }
 
 // ----------------------------------------------------------- gather block b
-// The 8 epilogue warps, one row at a time each: the row bundle of the
-// block's rows exactly as the inference gather writes it (4 lanes per
-// 32-value block, E8M0 scale into the block's atoms, pad rows zero).
-__device__ void fused_gather(const FusedArgs& fa, int b, const int4 blk, int ew, int lane) {
+// The 8 epilogue warps: the columns [part D/gp, (part+1) D/gp) of the
+// row bundle of the block's routed rows, exactly as the inference gather
+// writes them (4 lanes per 32-value block, E8M0 scale into the block's
+// atoms).  Work items are (row, 8-value chunk)
+// pairs spread over all 256 threads, four at a time with every load in
+// flight before the first is used, so a block with a single routed row
+// (one-token decode) still has all its loads in flight at once.
+__device__ void fused_gather(const FusedArgs& fa, int b, int part, int gp, const int4 blk, int gtid, int* s_route) {
+  // the routes of this block's rows: expert blk.x's routes of rank blk.w ..
+  // blk.w + blk.z - 1 in flat order (one warp ranks them with ballots);
+  // rows past the expert's routes are pad rows (-1)
+  if (gtid < kBlockRows) s_route[gtid] = -1;
+  named_bar_sync(kEpiBarrier, kEpiThreads);
+  if (gtid < 32) {
+    const int TK = fa.T * fa.K;
+    int run = 0;
+    for (int i0 = 0; i0 < TK; i0 += 32) {
+      const int i = i0 + gtid;
+      const bool mine = i < TK && __ldg(fa.ids + i) == blk.x;
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, mine);
+      const int rank = run + __popc(m & ((1u << gtid) - 1u)) - blk.w;
+      if (mine && rank >= 0 && rank < blk.z) s_route[rank] = i;
+      run += __popc(m);
+    }
+  }
+  named_bar_sync(kEpiBarrier, kEpiThreads);
   const int D = fa.D, K = fa.K;
+  // the block's routed rows come first (ranks in order); the rest are pad
+  // rows, which this gather leaves as they are: an MMA output row depends
+  // only on its own B row, so whatever (finite) codes a pad row holds reach
+  // only pad rows of h1, h2 and h3, which the combine never reads
+  int nreal = 0;
+  for (int i = 0; i < blk.z; ++i) nreal += s_route[i] >= 0 ? 1 : 0;
   const long long atom_row = static_cast<long long>(b) * (D / 128);
-  for (int r = blk.y + ew; r < blk.y + blk.z; r += CF::EPI_WARPS) {
-    const int route = __ldcg(fa.rp.perm + r);
-    const __nv_bfloat16* srow = route >= 0 ? fa.x + static_cast<long long>(route / K) * D : nullptr;
-    const int p = r - blk.y;
-    for (int base = 0; base < D; base += 1024) {
-      uint4 ub[4];
+  const int cols = D / gp, c0 = part * cols;   // this record's columns: whole scale atoms
+  const int chunks = cols / 8;         // a multiple of 4: a 4-lane group never straddles two rows
+  const int items = nreal * chunks;
+  constexpr int kBatch = 4;
+  for (int i0 = 0; i0 < items; i0 += kBatch * kEpiThreads) {
+    uint4 ub[kBatch];
+    int rr[kBatch], cc[kBatch];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int cq = base + q * 256 + lane * 8;
-        ub[q] = make_uint4(0, 0, 0, 0);
-        if (cq < D && srow) ub[q] = __ldg(reinterpret_cast<const uint4*>(srow + cq));
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * kEpiThreads + gtid;
+      const int rl = i / chunks;
+      rr[j] = blk.y + rl;
+      cc[j] = c0 + (i - rl * chunks) * 8;
+      ub[j] = make_uint4(0, 0, 0, 0);
+      if (i < items) {
+        const int route = s_route[rr[j] - blk.y];
+        if (route >= 0)
+          ub[j] = __ldg(reinterpret_cast<const uint4*>(fa.x + static_cast<long long>(route / K) * D + cc[j]));
       }
+    }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int c = base + q * 256 + lane * 8;
-        const uint4 u = ub[q];
-        float v[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                      bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
-        float amax = 0.0f;
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * kEpiThreads + gtid;   // uniform per 4-lane group (items is a multiple of 4)
+      const uint4 u = ub[j];
+      float v[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                    bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+      float amax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-        const int e = mx_shared_exp(amax);
-        const float inv = exp2_int(-e);
-        uint2 qv;
-        qv.x = cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
-        qv.y = cvt_e4m3x2(v[4] * inv, v[5] * inv) | (cvt_e4m3x2(v[6] * inv, v[7] * inv) << 16);
-        if (c < D) {
-          *reinterpret_cast<uint2*>(fa.xrow + static_cast<long long>(r) * D + c) = qv;
-          if ((lane & 3) == 0) {
-            const int kb = c >> 5;
-            fa.xsf[(atom_row + (kb >> 2)) * 512 + sf_atom_byte(p, kb & 3)] = static_cast<uint8_t>(e + 127);
-          }
+      for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+      const int e = mx_shared_exp(amax);
+      const float inv = exp2_int(-e);
+      uint2 qv;
+      qv.x = cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
+      qv.y = cvt_e4m3x2(v[4] * inv, v[5] * inv) | (cvt_e4m3x2(v[6] * inv, v[7] * inv) << 16);
+      if (i < items) {
+        *reinterpret_cast<uint2*>(fa.xrow + static_cast<long long>(rr[j]) * D + cc[j]) = qv;
+        if ((gtid & 3) == 0) {
+          const int kb = cc[j] >> 5;
+          fa.xsf[(atom_row + (kb >> 2)) * 512 + sf_atom_byte(rr[j] - blk.y, kb & 3)] = static_cast<uint8_t>(e + 127);
         }
       }
     }
   }
 }
 
-// ------------------------------------------------------------ combine token
+// ------------------------------------------------------------ combine part
+// Record q: token q / kCombineParts, the part q % kCombineParts of its D
+// columns (a one-token step spreads over kCombineParts CTAs).
 // out[t] = bf16((accumulate ? out[t] : 0) + sum_k s h3[inv]) in FP32, k in
 // order: the combine kernel's arithmetic, with h3 read through L2 (other
-// CTAs wrote it in this launch).
-__device__ void fused_combine(const FusedArgs& fa, int t, int gtid) {
+// CTAs wrote it in this launch).  Up to 8 routes at a time: their rows,
+// scores and h3 chunks are all in flight before the ordered FMAs.
+__device__ void fused_combine(const FusedArgs& fa, int q, int gtid) {
   const int D = fa.D, K = fa.K;
+  const int t = q / kCombineParts, part = q - t * kCombineParts;
+  const int c_end = (part + 1) * (D / kCombineParts);
   __nv_bfloat16* orow = fa.out + static_cast<long long>(t) * D;
   const __nv_bfloat16* h3 = static_cast<const __nv_bfloat16*>(fa.g2.out0);
-  for (int c = gtid * 8; c < D; c += kEpiThreads * 8) {
+  for (int c = part * (D / kCombineParts) + gtid * 8; c < c_end; c += kEpiThreads * 8) {
     float acc[8];
     if (fa.accumulate) {
       const uint4 u = *reinterpret_cast<const uint4*>(orow + c);
@@ -267,19 +365,33 @@ __device__ void fused_combine(const FusedArgs& fa, int t, int gtid) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
     }
-    for (int k = 0; k < K; ++k) {
-      const int r = __ldcg(fa.rp.inv + t * K + k);
-      if (r < 0) continue;
-      const float s = __ldcg(fa.rp.scores + t * K + k);
-      const uint4 u = __ldcg(reinterpret_cast<const uint4*>(h3 + static_cast<long long>(r) * D + c));
-      acc[0] = fmaf(s, bf16_lo(u.x), acc[0]);
-      acc[1] = fmaf(s, bf16_hi(u.x), acc[1]);
-      acc[2] = fmaf(s, bf16_lo(u.y), acc[2]);
-      acc[3] = fmaf(s, bf16_hi(u.y), acc[3]);
-      acc[4] = fmaf(s, bf16_lo(u.z), acc[4]);
-      acc[5] = fmaf(s, bf16_hi(u.z), acc[5]);
-      acc[6] = fmaf(s, bf16_lo(u.w), acc[6]);
-      acc[7] = fmaf(s, bf16_hi(u.w), acc[7]);
+    for (int k0 = 0; k0 < K; k0 += 8) {
+      int r[8];
+      float sc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        r[j] = k0 + j < K ? __ldcg(fa.rp.inv + t * K + k0 + j) : -1;
+        sc[j] = k0 + j < K ? __ldcg(fa.rp.scores + t * K + k0 + j) : 0.0f;
+      }
+      uint4 u[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        u[j] = make_uint4(0, 0, 0, 0);
+        if (r[j] >= 0) u[j] = __ldcg(reinterpret_cast<const uint4*>(h3 + static_cast<long long>(r[j]) * D + c));
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (r[j] < 0) continue;
+        const float s = sc[j];
+        acc[0] = fmaf(s, bf16_lo(u[j].x), acc[0]);
+        acc[1] = fmaf(s, bf16_hi(u[j].x), acc[1]);
+        acc[2] = fmaf(s, bf16_lo(u[j].y), acc[2]);
+        acc[3] = fmaf(s, bf16_hi(u[j].y), acc[3]);
+        acc[4] = fmaf(s, bf16_lo(u[j].z), acc[4]);
+        acc[5] = fmaf(s, bf16_hi(u[j].z), acc[5]);
+        acc[6] = fmaf(s, bf16_lo(u[j].w), acc[6]);
+        acc[7] = fmaf(s, bf16_hi(u[j].w), acc[7]);
+      }
     }
     *reinterpret_cast<uint4*>(orow + c) = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                                                      pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
@@ -300,9 +412,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
-  uint64_t* sf_full = drain + 1;   // [S]
-  uint64_t* sf_drain = sf_full + S;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_abort = abort_flag + 1;
   volatile int* s_nblk = abort_flag + 2;
@@ -317,12 +427,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_full[s], 1);
     }
     mbar_init(tfull, 1);
     mbar_init(tempty, CF::EPI_WARPS);
     mbar_init(drain, 1);
-    mbar_init(sf_drain, 1);
     *abort_flag = 0;
     *epi_abort = 0;
     *s_nblk = 0;
@@ -345,44 +453,31 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // ---- routing (CTA 0), then every CTA waits for it to be published
-  if (blockIdx.x == 0) {
+  // ---- every CTA: the row blocks (its work records) from the IDs; the
+  // last CTA also writes the routing arrays (the combine reads the inverse
+  // permutation and scores from them, once every W2 tile is done)
+  local_blocks(fa, reinterpret_cast<int*>(smem), reinterpret_cast<int4*>(cache), s_nblk);
+  if (blockIdx.x == gridDim.x - 1) {
     fused_route(fa, reinterpret_cast<int*>(smem));   // the stage buffers are idle until the routing is out
     __syncthreads();
-    if (threadIdx.x == 0) {
-      const int nb = fa.rp.hdr[1];
-      for (int b = 0; b < nb; ++b) {
-        gather_done[b] = 0;
-        w13_done[b] = 0;
-      }
-      sync[2] = 0;
-      __threadfence();
-      st_release_gpu(&sync[0], 1);
-    }
+    if (threadIdx.x == 0) st_release_gpu(&sync[0], 1);   // cumulative over the CTA's stores (barrier above)
   }
-  if (threadIdx.x == 0) {
-    if (wait_counter(&sync[0], 1, fa.wait_cycles, abort_flag, err)) *s_nblk = __ldcg(fa.rp.hdr + 1);
-  }
-  __syncthreads();
   const int nblk = *s_nblk;
   const int n13 = fa.g13.n_tiles, n2 = fa.g2.n_tiles;
-  const int U = *abort_flag ? 0 : nblk * (1 + n13 + n2) + fa.T;
+  const int gp = gather_parts(fa.D);
+  const int U = nblk * (gp + n13 + n2) + fa.T * kCombineParts;
   MetaCache mc;
   mc.blocks = reinterpret_cast<const int4*>(cache);
   mc.poff = nullptr;
   mc.bstart = nullptr;
-  {
-    int4* sb = reinterpret_cast<int4*>(cache);
-    for (int i = threadIdx.x; i < min(nblk, kCacheBlocks); i += blockDim.x) sb[i] = __ldcg(fa.rp.blocks + i);
-  }
-  __syncthreads();
+  int* s_route = reinterpret_cast<int*>(cache + kCacheBytes);   // [kBlockRows]: a gather record's routes
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
-      const Rec r = record(u, nblk, n13, n2);
+      const Rec r = record(u, nblk, gp, n13, n2);
       if (r.kind != 1 && r.kind != 2) continue;
       const bool is13 = r.kind == 1;
       const Tile t = tile_of(fa, r, mc);
@@ -391,18 +486,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       // h2 rows from all n13 W13 tiles (W2)
       int ready = 1;
       if (lane == 0) {
-        const int* dep = is13 ? gather_done + r.b : w13_done + r.b;
-        const int need = is13 ? 1 : n13 + fa.stall;
-        if (!is13 && ld_acquire_gpu(dep) < need) {
-          // while waiting, have L2 fetch this tile's two weight slabs (256
-          // adjacent rows of F bytes) and their scale atoms
-          const uint8_t* slab = fa.w2 + static_cast<long long>(t.a_row[0]) * p.K;
-          const uint32_t bytes = 256u * static_cast<uint32_t>(p.K);
-          for (uint32_t o = 0; o < bytes; o += 32768u) prefetch_l2(slab + o, min(32768u, bytes - o));
-          prefetch_l2(p.sfa + t.sfa_atom[0] * kAtom, static_cast<uint32_t>(2 * p.sfa_ts * kAtom));
+        // the block's gather first (a W13 tile's input; a W2 tile asks for
+        // its weights no earlier, so the gathers' loads do not queue behind
+        // weight traffic); a W2 tile whose W13 tiles are still running asks
+        // L2 for its first kPrefetch weight stages and waits for them
+        bool got = wait_counter(gather_done + r.b, gp, fa.wait_cycles, abort_flag, err);
+        if (got && !is13 && ld_acquire_gpu(w13_done + r.b) < n13 + fa.stall) {
+          for (int ks = 0; ks < min(kPrefetch, t.kstages); ++ks) tma_prefetch_l2_2d(&a2, ks * CF::BK, t.a_row[0]);
+          got = wait_counter(w13_done + r.b, n13 + fa.stall, fa.wait_cycles, abort_flag, err);
         }
-        ready = wait_counter(dep, need, fa.wait_cycles, abort_flag, err) ? 1 : 0;
+        // the acquires before this thread's tensor loads of what they guard
         fence_proxy_async_global();
+        ready = got ? 1 : 0;
       }
       if (!__shfl_sync(0xFFFFFFFFu, ready, 0)) {
         ok = false;
@@ -420,6 +515,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           uint8_t* ssf = sb + kBBytes;
           mbar_arrive_expect_tx(&full[slot], (2 * 128 + t.b_rows) * 128 + CF::SF_BYTES);
           const int kx = ks * CF::BK;
+          // the weight boxes kPrefetch stages ahead go to L2 now, so the
+          // loads that will fetch them wait for L2, not HBM: one SM's loads
+          // in flight bound its weight stream when few tiles share the GPU
+          if (ks + kPrefetch < t.kstages) {
+            const int px = kx + kPrefetch * CF::BK;
+            if (is13) tma_prefetch_l2_3d(&a13, px, t.out_col0, 2 * t.e);
+            else tma_prefetch_l2_2d(&a2, px, t.a_row[0]);
+          }
           if (is13) {
             tma_load_3d(sa, &a13, &full[slot], kx, t.out_col0, 2 * t.e);   // gate, then up
             tma_load_4d(ssf, &sf13, &full[slot], 0, ks, t.out_col0 >> 7, 2 * t.e);
@@ -451,7 +554,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     uint32_t it = 0, tc = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
-      const Rec r = record(u, nblk, n13, n2);
+      const Rec r = record(u, nblk, gp, n13, n2);
       if (r.kind != 1 && r.kind != 2) continue;
       const Tile t = tile_of(fa, r, mc);
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty, (tc & 1) ^ 1, abort_flag, err))) break;
@@ -459,7 +562,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const uint32_t idesc = idesc_mxf8(t.b_rows, 0, 0);
       for (int ks = 0; ks < t.kstages; ++ks, ++it) {
         const uint32_t slot = it % S, ph = (it / S) & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_full[slot], ph, abort_flag, err))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], ph, abort_flag, err))) {
           ok = false;
           break;
         }
@@ -470,6 +573,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const uint64_t bdesc0 = sdesc_k_sw128(sb);
         const uint64_t adesc0[2] = {sdesc_k_sw128(sa), sdesc_k_sw128(sa + kABytes)};
         if (lane == 0) {
+          // the stage's scale atoms go to its TMEM columns first (this
+          // thread's tcgen05 operations run in order); the decode-sized
+          // tiles this kernel serves are bound by how fast a stage cycles,
+          // not by MMA issue
+          const uint32_t ssf = sb + kBBytes;
+#pragma unroll
+          for (int j = 0; j <= 2; ++j) tc_cp_sf(sfcol + j * 4, sdesc_sf_atom(ssf + j * kAtom));
 #pragma unroll
           for (int k = 0; k < CF::MMAS; ++k) {
             const uint64_t koff = static_cast<uint64_t>(2 * k);
@@ -495,35 +605,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     __syncwarp();
   } else if (warp == 2 + CF::EPI_WARPS) {
-    // ------------------------------------------------- scale-atom copier
-    uint32_t it = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
-      const Rec r = record(u, nblk, n13, n2);
-      if (r.kind != 1 && r.kind != 2) continue;
-      const Tile t = tile_of(fa, r, mc);
-      for (int ks = 0; ks < t.kstages; ++ks, ++it) {
-        const uint32_t slot = it % S, ph = (it / S) & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], ph, abort_flag, err))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t sfcol = tmem + CF::SF_COL0 + slot * CF::SF_COLS;
-          const uint32_t ssf = smem_u32(smem + slot * CF::STAGE) + 2 * kABytes + kBBytes;
-#pragma unroll
-          for (int j = 0; j <= 2; ++j) tc_cp_sf(sfcol + j * 4, sdesc_sf_atom(ssf + j * kAtom));
-          tc_commit(&sf_full[slot]);
-        }
-        __syncwarp();
-      }
-    }
-    if (lane == 0) {
-      tc_commit(sf_drain);
-      drain_wait(sf_drain, 0);
-    }
-    __syncwarp();
+    // (the MMA thread copies the scale atoms itself here: this warp idles)
   } else {
     // -------------------------------------------- epilogue warps (8)
     // Every epilogue warp walks every record and reaches the end-of-record
@@ -537,7 +619,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const int gtid = threadIdx.x - 64;
     uint32_t tc = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
-      const Rec r = record(u, nblk, n13, n2);
+      const Rec r = record(u, nblk, gp, n13, n2);
       bool ok = true;
       if (r.kind == 1 || r.kind == 2) {
         const Tile t = tile_of(fa, r, mc);
@@ -550,10 +632,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
         ++tc;
       } else if (r.kind == 0) {
-        const int4 blk = r.b < kCacheBlocks ? mc.blocks[r.b] : __ldcg(fa.rp.blocks + r.b);
-        fused_gather(fa, r.b, blk, ew, lane);
+        const int4 blk = mc.blocks[r.b];   // nblk < kCacheBlocks (checked on the host)
+        fused_gather(fa, r.b, r.n, gp, blk, gtid, s_route);
       } else {
-        if (gtid == 0 && !wait_counter(&sync[2], nblk * n2, fa.wait_cycles, abort_flag, err)) *epi_abort = 1;
+        if (gtid == 0 && (!wait_counter(&sync[2], nblk * n2, fa.wait_cycles, abort_flag, err) ||
+                          !wait_counter(&sync[0], 1, fa.wait_cycles, abort_flag, err)))
+          *epi_abort = 1;
         named_bar_sync(kEpiBarrier, kEpiThreads);
         if (*epi_abort) break;
         fused_combine(fa, r.b, gtid);
@@ -562,10 +646,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       fence_proxy_async_global();   // this record's stores, before their release below
       named_bar_sync(kEpiBarrier, kEpiThreads);
       if (*epi_abort) break;
+      // the release is cumulative: it covers every epilogue thread's stores,
+      // ordered before it by the barrier above
       if (gtid == 0 && r.kind != 3) {
-        __threadfence();
-        if (r.kind == 0) st_release_gpu(gather_done + r.b, 1);
-        else red_add_release_gpu(r.kind == 1 ? w13_done + r.b : &sync[2], 1);
+        red_add_release_gpu(r.kind == 0 ? gather_done + r.b : (r.kind == 1 ? w13_done + r.b : &sync[2]), 1);
       }
     }
   }
@@ -577,12 +661,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  // the last CTA to finish returns the routing flag to zero for the next
-  // launch (every CTA read it, once, at its start)
+  // the last CTA to finish returns every counter of this launch to zero for
+  // the next one (every other CTA is past its last use of them)
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(&sync[1], 1) == static_cast<int>(gridDim.x) - 1) {
+      for (int b = 0; b < nblk; ++b) {
+        gather_done[b] = 0;
+        w13_done[b] = 0;
+      }
       sync[0] = 0;
+      sync[2] = 0;
       sync[1] = 0;
       __threadfence();
     }
@@ -594,15 +683,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 cudaError_t launch_fused_forward(const FusedLaunch& L, int num_sms, cudaStream_t stream) {
   static PerDeviceOnce setup;
   const cudaError_t se = setup.once(
-      [] { return cudaFuncSetAttribute(fused_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM); });
+      [] { return cudaFuncSetAttribute(fused_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmem); });
   if (se != cudaSuccess) return se;
   const FusedArgs& fa = L.args;
-  const long long recs = static_cast<long long>(L.max_blocks) * (1 + fa.g13.n_tiles + fa.g2.n_tiles) + fa.T;
+  const long long recs =
+      static_cast<long long>(L.max_blocks) * (gather_parts(fa.D) + fa.g13.n_tiles + fa.g2.n_tiles) +
+      static_cast<long long>(fa.T) * kCombineParts;
   const int grid = static_cast<int>(std::max(1LL, std::min<long long>(num_sms, recs)));
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kFusedThreads);
-  cfg.dynamicSmemBytes = CF::SMEM;
+  cfg.dynamicSmemBytes = kFusedSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident at once (the records wait on one another)

@@ -219,7 +219,6 @@ struct FusedArgs {
   RoutingPtrs rp;   // routing arrays, written by CTA 0
   uint8_t* xrow;    // x row bundle [r_cap, D] and its scale atoms [b_cap][D/128]
   uint8_t* xsf;
-  const uint8_t* w2;   // W2 codes [E*D, F] (L2 prefetch of a W2 tile's weights)
   int* sync;
   int b_cap;
   long long wait_cycles;   // limit of every counter wait (SM cycles)

@@ -127,11 +127,13 @@ class MoELayer:
 
     # ----------------------------------------------------------- compute
     def forward(self, x, ids, scores, W13, W2, out=None, saved=None, accumulate=False, save_input_only=False,
-                stream=None):
+                fused=False, stream=None):
+        """fused: the whole inference forward as one launch (MOE_FUSED_LAUNCH)."""
         T = x.shape[0]
         if out is None:
             out = torch.empty((T, self.D), dtype=torch.bfloat16, device=self.device)
-        flags = (abi.MOE_ACCUMULATE_OUT if accumulate else 0) | (abi.MOE_SAVE_INPUT_ONLY if save_input_only else 0)
+        flags = ((abi.MOE_ACCUMULATE_OUT if accumulate else 0) | (abi.MOE_SAVE_INPUT_ONLY if save_input_only else 0)
+                 | (abi.MOE_FUSED_LAUNCH if fused else 0))
         abi.moe_forward(self.ctx, T, x, ids, scores, W13.struct, W2.struct, out, saved, flags, stream)
         return out
 

@@ -106,6 +106,33 @@ def run_oracle(case, precision=None, out_init=None, dx_init=None, dw_fp32=False,
     return res
 
 
+def ctx_routing(layer, T):
+    """Routing arrays of the last inference forward (the context's copy,
+    laid out like the routing prefix of a saved state)."""
+    from mixture_experts_routed_route_gb300 import abi
+    _, nbytes = abi.moe_ctx_buffer(layer.ctx, abi.MOE_BUF_ROUTING)
+    raw = layer.read_buffer(abi.MOE_BUF_ROUTING, np.uint8, (nbytes,))
+
+    def field(f, n):
+        off, _ = abi.moe_saved_state_field(layer.cfg, f)
+        return raw[off:off + 4 * n].view(np.int32)
+
+    hdr = field(abi.MOE_SAVED_HEADER, 16)
+    return {"hdr": hdr, "counts": field(abi.MOE_SAVED_COUNTS, layer.E),
+            "poffsets": field(abi.MOE_SAVED_POFFSETS, layer.E + 1), "perm": field(abi.MOE_SAVED_PERM, int(hdr[2])),
+            "inv": field(abi.MOE_SAVED_INV, T * layer.K)}
+
+
+def assert_routing(got, ids, E):
+    from oracle import moe as omoe
+    rt = omoe.route(ids, E)
+    assert got["hdr"][0] == ids.shape[0] and got["hdr"][2] == rt.poffsets[-1] and got["hdr"][3] == rt.num_active
+    np.testing.assert_array_equal(got["counts"], rt.counts)
+    np.testing.assert_array_equal(got["poffsets"], rt.poffsets)
+    np.testing.assert_array_equal(got["perm"], rt.perm)
+    np.testing.assert_array_equal(got["inv"], rt.inv)
+
+
 # ------------------------------------------------------------------------
 # MXFP8 weight gradients: codes that two correct computations may round
 # differently.

@@ -21,42 +21,16 @@ from mixture_experts_routed_route_gb300 import synth
 from oracle import moe as omoe
 from oracle import sample as osample
 
-from moe_cases import TOL, Case, rel_err, run_gpu, run_oracle, to_f64
+from moe_cases import TOL, Case, assert_routing, ctx_routing, rel_err, run_gpu, run_oracle, to_f64
 
 pytestmark = pytest.mark.gpu
-
-
-def _routing_from_ctx(layer, T):
-    """Routing arrays of the last inference forward (the context's copy,
-    laid out like the routing prefix of a saved state)."""
-    from mixture_experts_routed_route_gb300 import abi
-    _, nbytes = abi.moe_ctx_buffer(layer.ctx, abi.MOE_BUF_ROUTING)
-    raw = layer.read_buffer(abi.MOE_BUF_ROUTING, np.uint8, (nbytes,))
-
-    def field(f, n):
-        off, _ = abi.moe_saved_state_field(layer.cfg, f)
-        return raw[off:off + 4 * n].view(np.int32)
-
-    hdr = field(abi.MOE_SAVED_HEADER, 16)
-    return {"hdr": hdr, "counts": field(abi.MOE_SAVED_COUNTS, layer.E),
-            "poffsets": field(abi.MOE_SAVED_POFFSETS, layer.E + 1), "perm": field(abi.MOE_SAVED_PERM, int(hdr[2])),
-            "inv": field(abi.MOE_SAVED_INV, T * layer.K)}
-
-
-def _assert_routing(got, ids, E):
-    rt = omoe.route(ids, E)
-    assert got["hdr"][0] == ids.shape[0] and got["hdr"][2] == rt.poffsets[-1] and got["hdr"][3] == rt.num_active
-    np.testing.assert_array_equal(got["counts"], rt.counts)
-    np.testing.assert_array_equal(got["poffsets"], rt.poffsets)
-    np.testing.assert_array_equal(got["perm"], rt.perm)
-    np.testing.assert_array_equal(got["inv"], rt.inv)
 
 
 def test_e64_bf16_inference_forward_matches_oracle():
     case = Case(synth.WORKLOADS["e64_bf16"])
     g = run_gpu(case, training=False, backward=False)
     assert g["err_bits"] == 0
-    _assert_routing(_routing_from_ctx(g["layer"], case.T), case.ids.astype(np.int64), case.w.E)
+    assert_routing(ctx_routing(g["layer"], case.T), case.ids.astype(np.int64), case.w.E)
     o = run_oracle(case, backward=False)
     assert rel_err(g["out"], o["out"]) <= TOL["bf16"]
     g["layer"].close()
@@ -96,7 +70,7 @@ def test_e384_mxfp8_inference_shared_then_routed():
                   accumulate=True)
     torch.cuda.synchronize()
     assert layer.error_bits() == 0 and shared.error_bits() == 0
-    _assert_routing(_routing_from_ctx(layer, T), ids.astype(np.int64), E)
+    assert_routing(ctx_routing(layer, T), ids.astype(np.int64), E)
 
     rng = np.random.default_rng(77)
     tokens = sorted(rng.choice(T, size=4, replace=False).tolist())
@@ -132,7 +106,7 @@ def test_small_inference_forward_matches_oracle(name):
     p = case.w.precision
     g = run_gpu(case, training=False, backward=False)
     assert g["err_bits"] == 0
-    _assert_routing(_routing_from_ctx(g["layer"], case.T), case.ids.astype(np.int64), case.w.E)
+    assert_routing(ctx_routing(g["layer"], case.T), case.ids.astype(np.int64), case.w.E)
     o = run_oracle(case, backward=False)
     assert rel_err(g["out"], o["out"]) <= TOL[p]
     dead = np.all(case.ids < 0, axis=1)
