@@ -161,14 +161,22 @@ def stage_bytes(w, rows_padded, routes, precision, train, experts_used=None, dw_
     return fwd, bwd
 
 
+def gemm_source_digest():
+    """SHA-256 prefix of the GEMM kernels' sources (gemm.cu, gemm_core.cuh,
+    common.cuh): a traffic record holds only for the code it was taken on."""
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "gemm_core.cuh", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "mixture_experts_routed_route_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel, workload):
     """DRAM bytes per launch from a committed ncu summary, if its kernel
     source is unchanged since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, "mixture_experts_routed_route_gb300", "csrc", "gemm.cu")
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    digest = gemm_source_digest()
     for line in open(path):
         line = line.strip()
         if not line.startswith("{"):

@@ -191,3 +191,107 @@ def mx_dequantize_weight_32x32(q, e):
     *lead, n, k = q.shape
     s = np.ldexp(1.0, e)[..., :, None, :, None]
     return (q.reshape(tuple(lead) + (n // 32, 32, k // 32, 32)) * s).reshape(q.shape)
+
+
+# ---------------------------------------------------------------- E2M1, NVFP4
+#
+# Dist-MoE explainer, section 02, "Expert Computation and Tensor Precision":
+# E2M1 holds a sign, two exponent bits and one fraction bit in four bits;
+# NVFP4 packs two E2M1 values per byte and uses E4M3 block scales plus
+# global scales; NVFP4 inference quantises on the source side and publishes
+# packed data, block scales and the row's inverse global scale.
+#
+# Readings where the pages leave a step open (the NVFP4 format's own
+# conventions):
+# * E2M1: exponent bias 1, no infinities or NaN; magnitudes 0, 0.5, 1, 1.5,
+#   2, 3, 4, 6; round to nearest even, saturating to +-6.
+# * Blocks of 16 consecutive values along the contraction axis, one E4M3
+#   block scale each (a positive value, rounded to nearest even, saturating
+#   to 448), and one FP32 global scale per row: g = amax(row) / (6 * 448), so
+#   the largest block scale lands at 448 and the largest value at 6.
+# * Every step is one FP32 operation, rounded to nearest even, in this order
+#   (both sides of a parity test decide the codes with the same FP32 values):
+#     g   = fp32(a_row / 2688)
+#     s6g = fp32(6 * g)
+#     sb  = E4M3(fp32(a_block / s6g))
+#     d   = fp32(sb * g)
+#     q   = E2M1(fp32(v / d))          (q = 0 where d = 0)
+#   and v is represented by q * sb * g.  A zero row has g = 0 and all codes 0.
+
+E2M1_MAX = 6.0
+NVFP4_BLOCK = 16
+NVFP4_GLOBAL_DIV = 6.0 * E4M3_MAX     # 2688: the largest E2M1 times the largest E4M3
+
+
+def round_e2m1(x):
+    """Nearest-even E2M1 value of ``x``, saturating to +-6."""
+    return round_to_binary(x, 1, 0, E2M1_MAX, saturate=True)
+
+
+def e2m1_decode(codes):
+    """Value of each 4-bit E2M1 code (bit 3 sign, bits 2-1 exponent, bit 0
+    fraction; exponent 0 is subnormal: 0 or 0.5)."""
+    c = np.asarray(codes, dtype=np.int64) & 0xF
+    sign = np.where(c & 0x8, -1.0, 1.0)
+    exp = (c >> 1) & 0x3
+    man = c & 0x1
+    return sign * np.where(exp == 0, man * 0.5, np.ldexp(1.0 + man / 2.0, exp - 1))
+
+
+def e2m1_encode(values):
+    """4-bit code of each E2M1-representable value (input on the grid)."""
+    v = np.asarray(values, dtype=np.float64)
+    sign = np.where(np.signbit(v), 0x8, 0)
+    a = np.abs(v)
+    _, e = np.frexp(a)
+    e = e - 1                                   # floor(log2 a) for a > 0
+    sub = a < 1.0
+    exp_field = np.where(sub, 0, e + 1)
+    man = np.where(sub, a / 0.5, (a / np.ldexp(1.0, e) - 1.0) * 2.0)
+    code = sign | (exp_field.astype(np.int64) << 1) | np.rint(man).astype(np.int64)
+    return np.where(a == 0, sign, code).astype(np.uint8)
+
+
+def _f32(x):
+    return np.asarray(x, dtype=np.float32)
+
+
+def nvfp4_quantize(v, axis=-1):
+    """NVFP4 quantisation of ``v`` (values exactly representable in FP32)
+    in blocks of 16 along ``axis``, with one global scale per row (all other
+    axes).  Returns ``(q, sb, g)``: E2M1 values (shape of v), E4M3 block
+    scales (the blocked axis shortened 16x) and FP32 row scales (the blocked
+    axis removed), all as float64."""
+    v = np.moveaxis(np.asarray(v, dtype=np.float64), axis, -1)
+    n = v.shape[-1]
+    assert n % NVFP4_BLOCK == 0, "NVFP4 axis must be a multiple of 16"
+    v32 = _f32(v)
+    assert np.array_equal(v32.astype(np.float64), v), "inputs must be FP32 values"
+    a_row = np.max(np.abs(v32), axis=-1)
+    g = _f32(a_row / np.float32(NVFP4_GLOBAL_DIV))
+    s6g = _f32(np.float32(6.0) * g)
+    blk = v32.reshape(v32.shape[:-1] + (n // NVFP4_BLOCK, NVFP4_BLOCK))
+    a_blk = np.max(np.abs(blk), axis=-1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(s6g[..., None] > 0, _f32(a_blk / s6g[..., None]), np.float32(0.0))
+    sb = _f32(round_e4m3(ratio.astype(np.float64)))
+    d = _f32(sb * g[..., None])
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = np.where(d[..., None] > 0, _f32(blk / d[..., None]), np.float32(0.0))
+    q = round_e2m1(y.astype(np.float64)).reshape(v.shape)
+    return (np.moveaxis(q, -1, axis), np.moveaxis(sb.astype(np.float64), -1, axis),
+            g.astype(np.float64))
+
+
+def nvfp4_dequantize(q, sb, g, axis=-1):
+    """q * sb * g with each block scale broadcast over its 16 values and the
+    row scale over the row."""
+    q = np.moveaxis(np.asarray(q, dtype=np.float64), axis, -1)
+    sb = np.moveaxis(np.asarray(sb, dtype=np.float64), axis, -1)
+    return np.moveaxis(q * np.repeat(sb, NVFP4_BLOCK, axis=-1) * np.asarray(g)[..., None], -1, axis)
+
+
+def nvfp4_fake_quant(v, axis=-1):
+    """Dequantised NVFP4 copy of ``v`` (FP32 values) along ``axis``."""
+    q, sb, g = nvfp4_quantize(v, axis)
+    return nvfp4_dequantize(q, sb, g, axis)

@@ -55,6 +55,11 @@ Readings of the pages (each also listed in the design notes)
 * Inference weights with 1x32 blocks (same section: "32x32 blocks for MXFP8
   training-compatible values or 1x32 for inference"): one scale per 32
   consecutive values of a weight row along the contraction axis.
+* NVFP4 (inference only; Dist-MoE explainer, section 08, "Public API and
+  Supported Modes": NVFP4 inference with prepared weights): weights, x rows
+  and h2 rows quantised along their contraction axis in blocks of 16 with
+  E4M3 block scales and one FP32 global scale per row (``formats``); h1 and
+  h3 are rounded to BF16 as in the other modes.
 """
 
 from collections import namedtuple
@@ -128,7 +133,7 @@ def route(ids, num_experts, pad=PAD):
 
 # ------------------------------------------------------- precision helpers
 
-PRECISIONS = ("f64", "bf16", "mxfp8")
+PRECISIONS = ("f64", "bf16", "mxfp8", "nvfp4")
 
 
 def _round_out(v, precision):
@@ -137,11 +142,15 @@ def _round_out(v, precision):
 
 
 def _q_row(v, precision):
-    """Activation quantiser along the last (feature) axis: FPROP/DGRAD operand."""
+    """Activation quantiser along the last (feature) axis: FPROP/DGRAD operand.
+    NVFP4 (inference): the value is first rounded to FP32, the precision in
+    which the GPU holds it, then quantised by the FP32 steps of the format."""
     if precision == "f64":
         return v
     if precision == "bf16":
         return fm.round_bf16(v)
+    if precision == "nvfp4":
+        return fm.nvfp4_fake_quant(fm.round_fp32(v), axis=-1)
     return fm.mx_fake_quant(v, axis=-1)
 
 
@@ -158,6 +167,8 @@ def prepare_weight(w_e, precision, blocks="32x32"):
     """One expert's weight [N, K] as the GEMMs consume it: MXFP8 with 32x32
     blocks (training) or 1x32 blocks along K (inference)."""
     w_e = np.asarray(w_e, dtype=np.float64)
+    if precision == "nvfp4":
+        return fm.nvfp4_fake_quant(w_e, axis=-1)      # 1x16 blocks along K, a global scale per row
     if precision == "mxfp8":
         if blocks == "1x32":
             return fm.mx_fake_quant(w_e, axis=-1)
@@ -262,6 +273,7 @@ def backward(state, dY, w13, w2, dx_init=None, dw_fp32=False):
     dW2 [E,D,F] and the intermediates dh3/dh2/dh1/dxr per padded row.
     """
     p = state["precision"]
+    assert p != "nvfp4", "NVFP4 is an inference format here (no backward)"
     rt = state["routing"]
     T, D, F, E, K = (state[k] for k in ("T", "D", "F", "E", "K"))
     Rp = int(rt.poffsets[E])
