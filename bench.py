@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--fused", action="store_true")    # MXFP8 inference: the routed forward as one launch
     ap.add_argument("--replay", action="store_true")   # training: the routed layer saves only its input and
                                                        # its backward replays the forward (activation slots)
+    ap.add_argument("--tied", action="store_true")     # layer stacks: one weight set shared by the layers
     ap.add_argument("--slot-gb", type=float, default=0.0)   # layer stacks: one activation slot of this size
                                                             # holds every layer's saved state (0: full states)
     ap.add_argument("--cpu-sample-experts", type=int, default=3)        # reference arm: experts per step
@@ -293,25 +294,37 @@ class Step:
 
 
 class StackStep:
-    """A stack of `w.layers` training layers on one context with one (tied)
-    expert weight set: every layer's forward in order, then the backwards in
-    reverse, captured as one CUDA graph.  Each layer has its own routing
-    (Zipf with a per-layer exponent), tokens and output gradient.  The weight
-    gradients of the layers accumulate in one FP32 buffer (the first backward
-    writes it).  With `slot_bytes`, the saved states share one activation
-    slot and the planner decides which layers keep only their input."""
+    """A stack of `w.layers` training layers on one context: every layer's
+    forward in order, then the backwards in reverse, captured as one CUDA
+    graph.  Each layer has its own routing (Zipf with a per-layer exponent),
+    tokens and output gradient.
 
-    def __init__(self, w, device, slot_bytes=0):
+    Independent weights (the default): each layer has its own MXFP8 weight
+    set, prepared without transposed codes (the input-gradient GEMMs read the
+    forward codes MN-major), and each backward writes its layer's BF16 weight
+    gradients into one pair of buffers that the next backward overwrites (a
+    framework consumes each layer's gradient as it is produced).  Tied
+    weights: one weight set shared by the layers, whose weight gradients
+    accumulate in one FP32 buffer (the first backward writes it).  With
+    `slot_bytes`, the saved states share one activation slot and the planner
+    decides which layers keep only their input."""
+
+    def __init__(self, w, device, slot_bytes=0, tied=False):
         import torch
         from mixture_experts_routed_route_gb300 import synth
         from mixture_experts_routed_route_gb300.layer import ActivationSlot, MoELayer, PreparedWeight
 
         self.w, self.dev, self.train = w, device, True
         T, D, F, E, K, L = w.T, w.D, w.F, w.E, w.K, w.layers
-        w13, w2 = synth.make_weights(w, device)
-        self.W13 = PreparedWeight(w13, w.precision, with_transpose=True)
-        self.W2 = PreparedWeight(w2, w.precision, with_transpose=True)
-        del w13, w2
+        self.tied = tied
+        self.W13, self.W2 = [], []
+        for l in range(1 if tied else L):
+            w13, w2 = synth.make_weights(w, device, layer=l)
+            mn = not tied and w.precision == "mxfp8"
+            self.W13.append(PreparedWeight(w13, w.precision, with_transpose=True, mn_major=mn))
+            self.W2.append(PreparedWeight(w2, w.precision, with_transpose=True, mn_major=mn))
+            del w13, w2
+            torch.cuda.empty_cache()
         self.layer = MoELayer(T, D, F, E, K, w.precision, training=True, device=device, replay=slot_bytes > 0)
         self.ids_np, self.io = [], []
         for l in range(L):
@@ -321,8 +334,9 @@ class StackStep:
                             "x": synth.make_tokens(w, device, layer=l), "dy": synth.make_grad_out(w, device, layer=l),
                             "out": torch.empty((T, D), dtype=torch.bfloat16, device=device),
                             "dx": torch.empty((T, D), dtype=torch.bfloat16, device=device)})
-        self.dW13 = torch.empty((E, 2 * F, D), dtype=torch.float32, device=device)
-        self.dW2 = torch.empty((E, D, F), dtype=torch.float32, device=device)
+        dt = torch.float32 if tied else torch.bfloat16
+        self.dW13 = torch.empty((E, 2 * F, D), dtype=dt, device=device)
+        self.dW2 = torch.empty((E, D, F), dtype=dt, device=device)
         self.slot = None
         if slot_bytes > 0:
             # the decisions depend only on the sizes, so they are taken once
@@ -336,15 +350,20 @@ class StackStep:
     def layers(self):
         return [self.layer]
 
+    def weights(self, l):
+        return (self.W13[0], self.W2[0]) if self.tied else (self.W13[l], self.W2[l])
+
     def enqueue(self):
         for l, io in enumerate(self.io):
             saved, input_only = self.states[l]
-            self.layer.forward(io["x"], io["ids"], io["scores"], self.W13, self.W2, out=io["out"], saved=saved,
+            W13, W2 = self.weights(l)
+            self.layer.forward(io["x"], io["ids"], io["scores"], W13, W2, out=io["out"], saved=saved,
                                save_input_only=input_only)
         for n, l in enumerate(reversed(range(len(self.io)))):
             saved, input_only = self.states[l]
-            self.layer.backward(saved, self.io[l]["dy"], self.W13, self.W2, dx=self.io[l]["dx"], dW13=self.dW13,
-                                dW2=self.dW2, dw_fp32=True, dw_accumulate=n > 0, replay=input_only)
+            W13, W2 = self.weights(l)
+            self.layer.backward(saved, self.io[l]["dy"], W13, W2, dx=self.io[l]["dx"], dW13=self.dW13, dW2=self.dW2,
+                                dw_fp32=self.tied, dw_accumulate=self.tied and n > 0, replay=input_only)
 
     capture = Step.capture
 
@@ -626,7 +645,7 @@ def run_stack(args, rank, world):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk = peaks()
-    st = StackStep(w, dev, slot_bytes=int(args.slot_gb * 1e9))
+    st = StackStep(w, dev, slot_bytes=int(args.slot_gb * 1e9), tied=args.tied)
     st.enqueue()
     torch.cuda.synchronize(dev)
     bits = st.layer.error_bits()
@@ -683,7 +702,8 @@ def run_stack(args, rank, world):
         return int(np.unique(ids[(ids >= 0) & (ids < w.E)]).size)
 
     fb, _ = stage_bytes(w, rows[-1][0], rows[-1][1], w.precision, True, experts_used=used(len(rows) - 1))
-    _, bb = stage_bytes(w, rows[0][0], rows[0][1], w.precision, True, experts_used=used(0), dw_bytes=8)
+    _, bb = stage_bytes(w, rows[0][0], rows[0][1], w.precision, True, experts_used=used(0),
+                        dw_bytes=8 if st.tied else 2)
     sbytes = {**fb, **bb}
     dom = max(stage_ms, key=lambda k: stage_ms[k])
     achieved = sbytes[dom] / (stage_ms[dom] * 1e-3) / 1e9
@@ -707,8 +727,11 @@ def run_stack(args, rank, world):
         "config": {"workload": w.name, "layers": w.layers, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "K": w.K,
                    "routing": "Zipf, exponent per layer in [0.8, 1.5]", "active_routes": routes,
                    "padded_rows": [r for r, _ in rows], "train": True,
-                   "weights": "one MXFP8 weight set shared by the layers (tied); dW13/dW2 FP32, accumulated "
-                              "over the layers",
+                   "weights": ("one MXFP8 weight set shared by the layers (tied); dW13/dW2 FP32, accumulated "
+                               "over the layers" if st.tied else
+                               "an independent MXFP8 weight set per layer (input-gradient GEMMs read the forward "
+                               "codes MN-major); each layer's dW13/dW2 BF16, written into one reused pair of "
+                               "buffers"),
                    "saved_state": ("full, one buffer per layer" if st.slot is None else
                                    f"one {args.slot_gb:g} GB activation slot; layers {replayed} keep only their "
                                    f"input and replay (their replay FLOPs not counted as useful)"),

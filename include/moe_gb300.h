@@ -135,8 +135,13 @@ typedef struct {
  * BF16:  data = the caller's BF16 tensor; scale = scale_t = NULL; data_t =
  *        BF16 [E, K, N] transposed copy (needed by moe_backward only).
  * MXFP8: data = E4M3 codes [E, N, K], scale = E8M0 atoms [E*N/128][K/128];
- *        data_t = E4M3 codes [E, K, N], scale_t = E8M0 atoms [E*K/128][N/128]
- *        (backward only; both E*N*K/32 bytes, see the atom layout below).
+ *        scale_t = E8M0 atoms [E*K/128][N/128] (backward only), and
+ *        optionally data_t = E4M3 codes [E, K, N] (backward only).  With
+ *        data_t == NULL the input-gradient GEMMs read `data` itself,
+ *        MN-major ([DM] section 02, "Quantization Axes for Forward and
+ *        Backward": static 32x32 weights let FPROP and DGRAD share qdata),
+ *        which saves E*N*K bytes; with data_t they read the K-major copy.
+ *        Both give the same results.  Atoms: E*N*K/32 bytes, see below.
  *        N % 128 == 0 and K % 128 == 0.  Filled by prepare_block_scaled_weight.
  * The struct is read on the host at call time; the pointers are not owned.
  */
@@ -246,8 +251,10 @@ MOE_API int64_t moe_row_capacity(const moe_config* cfg);
  *   MXFP8:  one E8M0 scale per 32x32 tile (OCP MX rule: floor(log2 amax) - 8,
  *           values rounded to nearest-even E4M3 and saturated at 448) is
  *           written to the scale atoms [E*N/128][K/128] and, when
- *           data_t != NULL, the transposed codes to data_t [E,K,N] with
- *           scale atoms [E*K/128][N/128] in scale_t.  data may not be NULL.
+ *           scale_t != NULL, the input-gradient orientation's atoms
+ *           [E*K/128][N/128]; if data_t != NULL too, the transposed codes
+ *           [E,K,N] (data_t without scale_t is rejected).  data may not be
+ *           NULL.
  *   MXFP8_1X32: inference weights, one E8M0 scale per 32 consecutive values
  *           of a row along K (same rule), codes to data [E,N,K] and scales
  *           to the atoms [E*N/128][K/128]; data_t and scale_t must be NULL.
@@ -260,10 +267,13 @@ MOE_API int64_t moe_row_capacity(const moe_config* cfg);
  * Bytes of the buffers prepare_block_scaled_weight fills for one [E, N, K]
  * weight, written to bytes[0..3] = data, scale, data_t, scale_t (0 for a
  * buffer the precision does not use).  `with_transpose` asks for the
- * backward's transposed copies (not for MOE_MXFP8_1X32).
- *   MXFP8, MXFP8_1X32: data E*N*K, scale E*N*K/32 + 16, data_t E*K*N,
- *                      scale_t E*K*N/32 + 16 (16 bytes of slack after the
- *                      atoms); N % 128 == 0 and K % 128 == 0.
+ * backward's orientation (not for MOE_MXFP8_1X32): 0 none, 1 the transposed
+ * codes and their scales, 2 (MXFP8) the scales only, for MN-major
+ * input-gradient GEMMs that read the forward codes.
+ *   MXFP8, MXFP8_1X32: data E*N*K, scale E*N*K/32 + 16, data_t E*K*N
+ *                      (with_transpose 1), scale_t E*K*N/32 + 16 (1 or 2;
+ *                      16 bytes of slack after the atoms); N % 128 == 0
+ *                      and K % 128 == 0.
  *   BF16:              data E*N*K*2 (the caller's own tensor, which the
  *                      layer reads in place), data_t E*K*N*2.
  * Host-only, no CUDA call.  Errors: MOE_ERR_INVALID_ARG (null bytes, shapes
@@ -319,7 +329,8 @@ MOE_API moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int
  * WGRAD, then the K-reduction of the input gradients):
  *   saved   the state written by the matching training forward
  *   dout    bf16 [T, D]   gradient of out (T as in that forward)
- *   W13,W2  prepared weights including data_t (and scale_t for MXFP8)
+ *   W13,W2  prepared weights with the backward orientation: data_t (BF16);
+ *           scale_t, with or without data_t (MXFP8)
  *   dx      bf16 [T, D]   dx[t] = bf16(sum_k dxr); MOE_ACCUMULATE_DX adds the
  *                         old dx first
  *   dW13    [E, 2F, D], dW2 [E, D, F]: BF16, or float with MOE_DW_FP32;

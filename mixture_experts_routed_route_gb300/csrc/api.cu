@@ -225,8 +225,14 @@ bool weight_ok(const moe_weight* w, moe_precision prec, int E, int N, int K, boo
   if (!w->data || !aligned16(w->data)) return false;
   if (prec == MOE_MXFP8 && (!w->scale || !aligned16(w->scale))) return false;
   if (need_t) {
-    if (!w->data_t || !aligned16(w->data_t)) return false;
-    if (prec == MOE_MXFP8 && (!w->scale_t || !aligned16(w->scale_t))) return false;
+    // MXFP8: the input-gradient scale atoms, and either the transposed codes
+    // (a K-major input-gradient operand) or none (the GEMM reads the
+    // forward's codes MN-major); BF16: the transposed copy
+    if (prec == MOE_MXFP8) {
+      if (!w->scale_t || !aligned16(w->scale_t) || (w->data_t && !aligned16(w->data_t))) return false;
+    } else if (!w->data_t || !aligned16(w->data_t)) {
+      return false;
+    }
   }
   return true;
 }
@@ -665,16 +671,19 @@ moe_status moe_weight_bytes(moe_precision precision, int32_t E, int32_t N, int32
   const size_t e = static_cast<size_t>(E), n = static_cast<size_t>(N), k = static_cast<size_t>(K);
   bytes[0] = bytes[1] = bytes[2] = bytes[3] = 0;
   if (precision == MOE_MXFP8 || precision == MOE_MXFP8_1X32) {
-    if (N % 128 || K % 128 || (precision == MOE_MXFP8_1X32 && with_transpose)) return MOE_ERR_INVALID_ARG;
+    if (N % 128 || K % 128 || (precision == MOE_MXFP8_1X32 && with_transpose) || with_transpose < 0 ||
+        with_transpose > 2)
+      return MOE_ERR_INVALID_ARG;
     bytes[0] = e * n * k;
     bytes[1] = e * n * (k / 32) + 16;
     if (with_transpose) {
-      bytes[2] = e * k * n;
+      bytes[2] = with_transpose == 1 ? e * k * n : 0;   // 2: scales only (MN-major input gradients)
       bytes[3] = e * k * (n / 32) + 16;
     }
     return MOE_OK;
   }
   if (precision == MOE_BF16) {
+    if (with_transpose < 0 || with_transpose > 1) return MOE_ERR_INVALID_ARG;
     bytes[0] = e * n * k * 2;
     if (with_transpose) bytes[2] = e * k * n * 2;
     return MOE_OK;
@@ -692,7 +701,7 @@ moe_status prepare_block_scaled_weight(const void* w, int32_t E, int32_t N, int3
   }
   if (precision == MOE_MXFP8) {
     if (N % 128 || K % 128 || !data || !scale || !aligned16(data)) return MOE_ERR_INVALID_ARG;
-    if ((data_t == nullptr) != (scale_t == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (data_t && !scale_t) return MOE_ERR_INVALID_ARG;   // transposed codes come with their scales
     if (data_t && !aligned16(data_t)) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_prep_mx_weight(w, E, N, K, static_cast<uint8_t*>(data), scale,
                                              static_cast<uint8_t*>(data_t), scale_t, stream));
@@ -834,11 +843,16 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g1.na = 1;   // the SwiGLU-backward epilogue needs two accumulator buffers
   g1.epi = kEpiSwigluBwd;
   g1.mode = kGroupedM;
-  if (!make_tmap(&g1.tmA, W2->data_t, mx, static_cast<int64_t>(E) * F, D, 128) ||
+  // MXFP8 weights prepared without transposed codes: A is W2's forward codes
+  // [E*D rows (K), F columns (M)], read MN-major
+  const bool mn2 = mx && W2->data_t == nullptr;
+  if (!(mn2 ? make_tmap(&g1.tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128)
+            : make_tmap(&g1.tmA, W2->data_t, mx, static_cast<int64_t>(E) * F, D, 128)) ||
       !make_tmap(&g1.tmB, B(ctx, MOE_BUF_DH3ROW), mx, R, D, 32) ||
-      !make_grouped_m_boxes(&g1, W2->data_t, static_cast<int64_t>(E) * F, W2->scale_t, B(ctx, MOE_BUF_DH3ROW), R,
-                            mx, D))
+      !make_grouped_m_boxes(&g1, mn2 ? W2->data : W2->data_t, static_cast<int64_t>(E) * F, W2->scale_t,
+                            B(ctx, MOE_BUF_DH3ROW), R, mx, D))
     return MOE_ERR_CUDA;
+  g1.p.a_mn = mn2 ? 1 : 0;
   GemmParams& p1 = g1.p;
   p1.hdr = rp.hdr;
   p1.blocks = rp.blocks;
@@ -911,11 +925,19 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g3.na = pair_tiles(D);
   g3.epi = kEpiStore;
   g3.mode = kGroupedM;
-  if (!make_tmap(&g3.tmA, W13->data_t, mx, static_cast<int64_t>(E) * D, 2 * F, 128) ||
+  // MXFP8 without transposed codes: A is W13's forward codes [E*2F rows (K),
+  // D columns (M)], read MN-major, one box per 128-column weight tile
+  const bool mn13 = mx && W13->data_t == nullptr;
+  if (!(mn13 ? make_tmap(&g3.tmA, W13->data, mx, static_cast<int64_t>(E) * 2 * F, D, 128)
+             : make_tmap(&g3.tmA, W13->data_t, mx, static_cast<int64_t>(E) * D, 2 * F, 128)) ||
       !make_tmap(&g3.tmB, B(ctx, MOE_BUF_DH1ROW), mx, R, 2 * F, 32) ||
-      !make_grouped_m_boxes(&g3, W13->data_t, static_cast<int64_t>(E) * D, W13->scale_t, B(ctx, MOE_BUF_DH1ROW), R,
-                            mx, 2 * F))
+      !make_grouped_m_boxes(&g3, mn13 ? W13->data : W13->data_t, static_cast<int64_t>(E) * D, W13->scale_t,
+                            B(ctx, MOE_BUF_DH1ROW), R, mx, 2 * F))
     return MOE_ERR_CUDA;
+  if (mn13) {
+    g3.p.a_mn = 1;
+    g3.p.a_pair_box = 0;   // one box and one scale atom per weight tile
+  }
   GemmParams& p3 = g3.p;
   p3.hdr = rp.hdr;
   p3.blocks = rp.blocks;

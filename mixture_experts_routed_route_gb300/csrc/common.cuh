@@ -281,6 +281,22 @@ __device__ __forceinline__ uint64_t sdesc_k_sw(uint32_t saddr, int row_bytes) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major 8-bit operand tile as TMA's
+// SWIZZLE_128B writes a box whose inner 128 bytes run along M (or N) and
+// whose rows are consecutive K indices: swizzle atoms of 8 K-rows x 128
+// bytes, 1024 bytes apart along K (stride byte offset).  A 128-element tile
+// is one atom wide along M, so the leading byte offset (the stride from one
+// atom to the next along M) is never used; it is set to the same 1024.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1024 >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Shared-memory descriptor of one scale atom for tcgen05.cp: a K-major
 // matrix of 32 rows x 16 bytes without swizzle, i.e. four 8-row x 16-byte
 // core matrices 128 bytes apart (stride byte offset 128).
@@ -313,6 +329,10 @@ __device__ __forceinline__ uint32_t idesc_bf16(uint32_t n) {
 __device__ __forceinline__ uint32_t idesc_mxf8(uint32_t n, uint32_t sfa_id, uint32_t sfb_id) {
   return (sfb_id << 4) | ((n >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) | (sfa_id << 29);
 }
+
+// Bit 15 of the instruction descriptor: A is MN-major (transposed) rather
+// than K-major.
+constexpr uint32_t kIdescAMnMajor = 1u << 15;
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {

@@ -191,7 +191,14 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
           } else {
             // fewer, larger copies: the issue rate of the producer thread
             // bounds compute-bound shapes
-            if (NA == 2 && p.a_pair_box == 1) {
+            if (MX && p.a_mn) {
+              // MN-major A: box (M columns of this tile, K rows of this
+              // stage) of the weight as prepared for the forward, [E * K, M]
+#pragma unroll
+              for (int j = 0; j < NA; ++j)
+                tma_load_2d(sa + j * kABytes, &tmA, &full[slot], t.a_row[j] - t.e * p.a_rows_per_expert,
+                            t.e * p.K + kx);
+            } else if (NA == 2 && p.a_pair_box == 1) {
               tma_load_2d(sa, &aux0, &full[slot], kx, t.a_row[0]);   // rows a_row[0] .. +255
             } else if (NA == 2 && p.a_pair_box == 2) {
               tma_load_3d(sa, &aux0, &full[slot], kx, t.out_col0, 2 * t.e);   // gate, then up
@@ -248,7 +255,8 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty[acc], aph ^ 1, abort_flag, p.err))) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem + acc * C::ACC_COLS;
-      const uint32_t idesc = MX ? idesc_mxf8(t.b_rows, 0, 0) : idesc_bf16(t.b_rows);
+      const uint32_t idesc = MX ? (idesc_mxf8(t.b_rows, 0, 0) | (MODE == kGroupedM && p.a_mn ? kIdescAMnMajor : 0u))
+                                : idesc_bf16(t.b_rows);
       for (int ks = 0; ks < t.kstages; ++ks, ++it) {
         const uint32_t slot = it % S, ph = (it / S) & 1;
         // MXFP8: the scale warp's commit for this stage follows its own wait
@@ -263,9 +271,12 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
         const uint32_t sfcol = tmem + C::SF_COL0 + slot * C::SF_COLS;
         const int rb = stage_row_bytes<MODE, C::BK, MX ? 1 : 2>(t, ks);
         const uint64_t bdesc0 = sdesc_k_sw(sb, rb);
+        // MN-major A (grouped-M MXFP8 with p.a_mn): a K step of 32 rows is 4 KB on
+        const bool amn = MX && MODE == kGroupedM && p.a_mn;
         uint64_t adesc0[NA];
 #pragma unroll
-        for (int j = 0; j < NA; ++j) adesc0[j] = sdesc_k_sw(sa + j * kABytes, rb);
+        for (int j = 0; j < NA; ++j) adesc0[j] = amn ? sdesc_mn_sw128(sa + j * kABytes) : sdesc_k_sw(sa + j * kABytes, rb);
+        const uint64_t astep = amn ? (4096 >> 4) : 2;
         const int nmma = (ks == t.kstages - 1) ? t.klast / C::KMMA : C::MMAS;
         if (lane == 0) {
 #pragma unroll
@@ -277,7 +288,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
               for (int j = 0; j < NA; ++j) {
                 if (MX) {
                   // scale byte k of the 4 per row (one per 32-element block)
-                  mma_mxf8(d_tmem + j * 128, adesc0[j] + koff, bdesc0 + koff,
+                  mma_mxf8(d_tmem + j * 128, adesc0[j] + static_cast<uint64_t>(k) * astep, bdesc0 + koff,
                            idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29), sfcol + j * 4,
                            sfcol + NA * 4, accum);
                 } else {

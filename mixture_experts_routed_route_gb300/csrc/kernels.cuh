@@ -172,6 +172,10 @@ struct GemmParams {
   float swiglu_limit;     // SwiGLU epilogues: clamp g <= L and |u| <= L when L > 0
   unsigned long long* clip;  // SwiGLU forward with a limit: [2] counts of clamped g, u (or null)
   int b_full_box;         // grouped-M: aux[1] loads a full 128-row block in one box
+  // grouped-M, MXFP8: A is read MN-major from the weight as prepared for the
+  // forward (tmA over [E * K rows, M cols], 128 M-bytes x 128 K-rows boxes):
+  // the input-gradient GEMMs need no transposed copy of the codes
+  int a_mn;
   // Set by the launcher from the grid size: the step of one grid in tile
   // coordinates (tile, n, m, e), by which the producer, MMA and scale-copy
   // roles advance their tiles.

@@ -25,10 +25,14 @@ class PreparedWeight:
 
     BF16: ``data`` is the caller's tensor, ``data_t`` its transpose
     [E, K, N] (for the input-gradient GEMMs).  MXFP8: E4M3 codes with one
-    E8M0 scale per 32x32 tile, in both orientations.  "mxfp8_1x32": forward
-    only, one scale per 1x32 block of a row along K."""
+    E8M0 scale per 32x32 tile, in both orientations (the transposed codes
+    too unless mn_major).  "mxfp8_1x32": forward only, one scale per 1x32
+    block of a row along K."""
 
-    def __init__(self, w, precision, with_transpose=True, stream=None):
+    def __init__(self, w, precision, with_transpose=True, stream=None, mn_major=False):
+        """mn_major (MXFP8 with_transpose): keep only the input-gradient scale
+        atoms; the input-gradient GEMMs then read the forward codes MN-major
+        instead of a transposed copy (E*N*K bytes less)."""
         assert w.dtype == torch.bfloat16 and w.is_cuda and w.dim() == 3
         w = w.contiguous()
         self.precision = precision_code(precision)
@@ -44,7 +48,8 @@ class PreparedWeight:
             self.data = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
             self.scale = torch.empty(E * N * (K // 32) + 16, dtype=torch.uint8, device=dev)
             if with_transpose:
-                self.data_t = torch.empty((E, K, N), dtype=torch.uint8, device=dev)
+                if not mn_major:
+                    self.data_t = torch.empty((E, K, N), dtype=torch.uint8, device=dev)
                 self.scale_t = torch.empty(E * K * (N // 32) + 16, dtype=torch.uint8, device=dev)
             abi.prepare_block_scaled_weight(w, E, N, K, self.precision, self.data, self.scale, self.data_t,
                                             self.scale_t, stream)

@@ -117,11 +117,15 @@ def test_weight_bytes_without_gpu(lib):
     assert abi.moe_weight_bytes(abi.MOE_MXFP8, E, N, K, True) == (E * N * K, atoms + 16, E * K * N, atoms + 16)
     assert abi.moe_weight_bytes(abi.MOE_MXFP8, E, N, K, False) == (E * N * K, atoms + 16, 0, 0)
     assert abi.moe_weight_bytes(abi.MOE_MXFP8_1X32, E, N, K, False) == (E * N * K, atoms + 16, 0, 0)
+    # 2: the input-gradient scales only (MN-major input-gradient GEMMs)
+    assert abi.moe_weight_bytes(abi.MOE_MXFP8, E, N, K, 2) == (E * N * K, atoms + 16, 0, atoms + 16)
     assert abi.moe_weight_bytes(abi.MOE_BF16, E, 96, 64, True) == (E * 96 * 64 * 2, 0, E * 64 * 96 * 2, 0)
     for bad in ((abi.MOE_MXFP8, E, 96, K, True),        # MXFP8 tiles N and K by 128
                 (abi.MOE_MXFP8_1X32, E, N, K, True),    # inference weights have no transpose
                 (abi.MOE_BF16, 0, 64, 64, True),
                 (abi.MOE_BF16, E, 48, 64, True),
+                (abi.MOE_BF16, E, 96, 64, 2),           # BF16 has no scales-only orientation
+                (abi.MOE_MXFP8, E, N, K, 3),
                 (7, E, N, K, False)):
         with pytest.raises(abi.MoEError) as ei:
             abi.moe_weight_bytes(*bad)
