@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fused", action="store_true")    # MXFP8 inference: the routed forward as one launch
+    ap.add_argument("--mn-major", action="store_true")  # MXFP8 training: no transposed weight codes; the
+                                                        # input-gradient GEMMs read the forward codes MN-major
     ap.add_argument("--replay", action="store_true")   # training: the routed layer saves only its input and
                                                        # its backward replays the forward (activation slots)
     ap.add_argument("--tied", action="store_true")     # layer stacks: one weight set shared by the layers
@@ -193,7 +195,7 @@ def traffic_record(kernel, workload):
 class Step:
     """Inputs, weights, contexts and the captured CUDA graph of one step."""
 
-    def __init__(self, w, device, replay=False, fused=False):
+    def __init__(self, w, device, replay=False, fused=False, mn_major=False):
         import torch
         from mixture_experts_routed_route_gb300 import synth
         from mixture_experts_routed_route_gb300.layer import MoELayer, PreparedWeight
@@ -210,8 +212,10 @@ class Step:
         self.scores = torch.from_numpy(scores).to(device)
         w13, w2 = synth.make_weights(w, device)
         self.sample_experts = None
-        self.W13 = PreparedWeight(w13, w.precision, with_transpose=self.train)
-        self.W2 = PreparedWeight(w2, w.precision, with_transpose=self.train)
+        mn = bool(mn_major and self.train and w.precision == "mxfp8")
+        self.mn_major = mn
+        self.W13 = PreparedWeight(w13, w.precision, with_transpose=self.train, mn_major=mn)
+        self.W2 = PreparedWeight(w2, w.precision, with_transpose=self.train, mn_major=mn)
         self.w13_bf16, self.w2_bf16 = w13, w2   # kept only until the oracle sample is taken
         self.replay = bool(replay and self.train)
         self.fused = bool(fused and not self.train and w.precision == "mxfp8")
@@ -435,7 +439,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk = peaks()
-    st = Step(w, dev, replay=args.replay, fused=args.fused)
+    st = Step(w, dev, replay=args.replay, fused=args.fused, mn_major=args.mn_major)
 
     # eager warm-up (configures kernels), then correctness guard: no device error
     st.enqueue()
@@ -618,6 +622,8 @@ def run_ours(args, rank, world):
                    "l2": "inputs larger than L2 (expert weights stream from HBM every step)",
                    "graph": "one CUDA graph per step, replayed",
                    **({"forward": "single launch (MOE_FUSED_LAUNCH)"} if st.fused else {}),
+                   **({"weights": "MXFP8 without transposed codes (input-gradient GEMMs read them MN-major)"}
+                      if st.mn_major else {}),
                    **({"saved_state": ("input only: the backward replays the gather, W13 and W2 GEMMs "
                                        "(their FLOPs not counted as useful)") if st.replay else "full"}
                       if st.train else {})},

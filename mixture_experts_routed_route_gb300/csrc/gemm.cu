@@ -49,7 +49,11 @@ namespace moe {
 
 namespace {
 
-template <bool MX, int NA, int EPI, int MODE>
+// DWF (weight gradient only): the FP32 staged modes (TMA store or TMA
+// reduce-add) are compiled into this instance; the other instance holds the
+// BF16 staged store and the plain-store epilogue, so neither carries the
+// other's registers.
+template <bool MX, int NA, int EPI, int MODE, bool DWF = false>
 __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap aux0,
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
         //    64 hh + 32 h into box h.  A reduce-add into an expert without
         //    rows is skipped (its dW stays as it was).
         uint8_t* stg = staging + grp * 32768;
-        const bool f32 = p.tma_store != kDwStoreBf16;
+        constexpr bool f32 = DWF;
         const bool has = ok && t.kstages > 0;
         uint32_t r[32];
         if (has) tmem_ld32(tbase + 32 * h, r);
@@ -491,10 +495,10 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   }
 }
 
-template <bool MX, int NA, int EPI, int MODE>
+template <bool MX, int NA, int EPI, int MODE, bool DWF = false>
 cudaError_t launch_impl(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   using C = Cfg<MX, NA, MODE>;
-  auto kern = gemm_kernel<MX, NA, EPI, MODE>;
+  auto kern = gemm_kernel<MX, NA, EPI, MODE, DWF>;
   static PerDeviceOnce setup;
   const cudaError_t se =
       setup.once([&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM); });
@@ -527,6 +531,10 @@ cudaError_t launch_gemm(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   MOE_GEMM_CASE(true, 2, kEpiStore, kGroupedM)
   MOE_GEMM_CASE(false, 1, kEpiSwigluBwd, kGroupedM)
   MOE_GEMM_CASE(true, 1, kEpiSwigluBwd, kGroupedM)
+  if (g.epi == kEpiWgrad && g.mode == kGroupedK &&
+      (g.p.tma_store == kDwStoreF32 || g.p.tma_store == kDwAddF32))
+    return g.mx ? launch_impl<true, 1, kEpiWgrad, kGroupedK, true>(g, num_sms, stream)
+                : launch_impl<false, 1, kEpiWgrad, kGroupedK, true>(g, num_sms, stream);
   MOE_GEMM_CASE(false, 1, kEpiWgrad, kGroupedK)
   MOE_GEMM_CASE(true, 1, kEpiWgrad, kGroupedK)
 #undef MOE_GEMM_CASE
