@@ -164,6 +164,25 @@ def stage_bytes(w, rows_padded, routes, precision, train, experts_used=None, dw_
     return fwd, bwd
 
 
+# useful FLOPs of each grouped GEMM per active route, in units of D * F
+GEMM_FLOPS = {"gemm_w13_swiglu": 4.0, "gemm_w2": 2.0, "gemm_w2_dgrad_swiglu_bwd": 2.0, "gemm_w2_wgrad": 2.0,
+              "gemm_w13_dgrad": 4.0, "gemm_w13_wgrad": 4.0}
+
+
+def gemm_tensor(stage_ms, routes, w, peak_t):
+    """The grouped GEMMs alone: their useful FLOPs over their own stage
+    times against the tensor peak, in total and per GEMM (the step's
+    tensor_frac also carries the HBM-bound routing, gather and combine)."""
+    ms = {k: v for k, v in stage_ms.items() if k in GEMM_FLOPS and v > 0}
+    if not ms:
+        return None
+    per = {k: round(GEMM_FLOPS[k] * routes * w.D * w.F / (v * 1e-3) / 1e12 / peak_t, 4) for k, v in ms.items()}
+    total = sum(GEMM_FLOPS[k] * routes * w.D * w.F for k in ms)
+    t = sum(ms.values())
+    return {"ms": round(t, 4), "tflops": round(total / (t * 1e-3) / 1e12, 1),
+            "tensor_frac": round(total / (t * 1e-3) / 1e12 / peak_t, 4), "per_gemm_tensor_frac": per}
+
+
 def gemm_source_digest():
     """SHA-256 prefix of the GEMM kernels' sources (gemm.cu, gemm_core.cuh,
     common.cuh): a traffic record holds only for the code it was taken on."""
@@ -615,6 +634,7 @@ def run_ours(args, rank, world):
         "tokens_per_s": round(w.T * world / (ms * 1e-3), 1),
         "tensor_frac": round(tflops / world / peak_t, 4),
         "tensor_peak_tflops": round(peak_t, 1),
+        "gemms": None if st.fused else gemm_tensor(stage_ms, routes, w, peak_t),
         "config": {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "K": w.K,
                    "routing": w.routing, "inactive_frac": w.inactive_frac, "shared_F": w.shared_F,
                    "train": w.train, "active_routes": routes, "padded_rows": rows_padded,

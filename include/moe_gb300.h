@@ -208,14 +208,20 @@ MOE_API size_t moe_saved_state_bytes(const moe_config* cfg);
  * bundles and H3 of a full state or X of an input-only state.  The routing
  * fields and PRENORM sit at the same offsets in both layouts. */
 typedef enum {
-  MOE_SAVED_HEADER = 0,     /* int32[16]: [0] T, [1] row blocks, [2] rows used, [3] active routes */
+  MOE_SAVED_HEADER = 0,     /* int32[16]: [0] T, [1] row blocks, [2] rows used, [3] active routes,
+                               [4] row-block pairs                             */
   MOE_SAVED_COUNTS = 1,     /* int32[E]     active routes per expert           */
   MOE_SAVED_OFFSETS = 2,    /* int32[E+1]   exclusive prefix of counts         */
   MOE_SAVED_POFFSETS = 3,   /* int32[E+1]   same with counts padded to 32      */
   MOE_SAVED_PERM = 4,       /* int32[R_cap] route t*K+k of each row, -1 = pad  */
   MOE_SAVED_INV = 5,        /* int32[T_max*K] row of each route, -1 = inactive */
-  MOE_SAVED_BLOCKS = 6,     /* int32[4*B_cap] (expert, first row, rows, 0): each
-                               expert's padded rows cut into blocks of <=128   */
+  MOE_SAVED_BLOCKS = 6,     /* int32[4*B_cap] (expert, first row, rows, pair):
+                               each expert's padded rows cut into blocks of
+                               <=128.  Word 3 of entry p < header[4] describes
+                               row-block pair p, consecutive blocks of one
+                               expert taken two at a time (the last alone):
+                               (first block << 1) | (second block present);
+                               0 in the other entries                          */
   MOE_SAVED_SCORES = 7,     /* float[T_max*K] scores, 0 for inactive routes    */
   MOE_SAVED_H1 = 8,         /* bf16[R_cap, 2F]                                 */
   MOE_SAVED_XCOL = 9,       /* x column bundle: bf16 [D, R_cap] or e4m3 codes  */

@@ -112,6 +112,7 @@ _SIGNATURES = {
     "moe_ctx_launch_count": (ctypes.c_uint64, [_P]),
     "moe_ctx_set_max_ctas": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_ctx_test_fused_stall": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64]),
+    "moe_ctx_test_tile_mode": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_ctx_set_post_norm": (ctypes.c_int, [_P, _P, ctypes.c_float]),
     "moe_post_norm_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "moe_weight_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
@@ -306,6 +307,11 @@ def moe_ctx_set_max_ctas(ctx, max_ctas):
 
 def moe_ctx_test_fused_stall(ctx, stall, wait_cycles=0):
     _check("moe_ctx_test_fused_stall", LIB.moe_ctx_test_fused_stall(ctx, int(stall), int(wait_cycles)))
+
+
+def moe_ctx_test_tile_mode(ctx, mode):
+    """0: row-block pairs when the capacity is dense enough, 1: row blocks, 2: pairs."""
+    _check("moe_ctx_test_tile_mode", LIB.moe_ctx_test_tile_mode(ctx, int(mode)))
 
 
 def moe_ctx_set_post_norm(ctx, gamma, eps):

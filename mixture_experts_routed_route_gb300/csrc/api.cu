@@ -28,6 +28,11 @@ struct moe_ctx {
   int num_sms;
   int max_ctas = 0;   // moe_ctx_set_max_ctas (0: num_sms)
   int fused_stall = 0;             // moe_ctx_test_fused_stall
+  // grouped-M GEMM tiles over row-block pairs (B up to 256 rows): chosen at
+  // creation when the capacity gives the experts 128 routes each on average
+  // (max_tokens * top_k >= 128 E); moe_ctx_test_tile_mode overrides it
+  bool pair_tiles_auto = false;
+  int tile_mode = 0;               // 0: pair_tiles_auto, 1: row blocks, 2: pairs
   long long fused_wait = 0;        // counter-wait limit of the single-launch forward (0: default)
   const void* norm_gamma = nullptr;   // moe_ctx_set_post_norm (MOE_POST_NORM)
   float norm_eps = 0.0f;
@@ -67,6 +72,8 @@ bool config_ok(const moe_config* c) {
 }
 
 bool config_tileable(const moe_config* c) { return c->d_model % 128 == 0 && c->d_ff % 128 == 0; }
+
+bool use_pairs(const moe_ctx* c) { return c->tile_mode == 2 || (c->tile_mode == 0 && c->pair_tiles_auto); }
 
 int64_t row_cap(const moe_config* c) {
   const int64_t r = static_cast<int64_t>(c->max_tokens) * c->top_k + 31LL * c->num_experts;
@@ -254,15 +261,15 @@ cudaError_t stage_mark(moe_ctx* c, int pass, int idx, cudaStream_t s) {
 // also h1 and the h2 column bundle into act's fields.  False if a tensor map
 // cannot be encoded.
 bool fill_w13(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W13, uint8_t* act, const SavedLayout& SL,
-              bool marks, GemmLaunch* g1) {
+              bool marks, GemmLaunch* g1, bool pairs) {
   const moe_config& c = ctx->cfg;
   const int D = c.d_model, F = c.d_ff, E = c.num_experts;
   const bool mx = c.precision == MOE_MXFP8;
   const int64_t R = ctx->r_cap;
   g1->mx = mx;
-  g1->na = 2;
+  g1->na = pairs ? 1 : 2;
   g1->epi = kEpiSwigluFwd;
-  g1->mode = kGroupedM;
+  g1->mode = pairs ? kGroupedMP : kGroupedM;
   if (!make_tmap(&g1->tmA, W13->data, mx, static_cast<int64_t>(E) * 2 * F, D, 128) ||
       !make_tmap(&g1->tmB, B(ctx, MOE_BUF_XROW), mx, R, D, 32) ||
       !make_grouped_m_boxes(g1, W13->data, static_cast<int64_t>(E) * 2 * F, W13->scale, B(ctx, MOE_BUF_XROW), R,
@@ -274,7 +281,7 @@ bool fill_w13(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W13, uint8_
   p1.poffsets = rp.poffsets;
   p1.E = E;
   p1.b_box_rows = 32;
-  p1.n_tiles = F / 128;
+  p1.n_tiles = F / (pairs ? 64 : 128);
   p1.K = D;
   p1.a_rows_per_expert = 2 * F;
   p1.a_up_offset = F;
@@ -300,20 +307,20 @@ bool fill_w13(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W13, uint8_
   p1.swiglu_limit = c.swiglu_limit;
   p1.clip = (marks && c.swiglu_limit > 0.0f) ? ctx->clip : nullptr;   // a replay counts no clips again
   p1.err = ctx->err;
-  g1->max_tiles = static_cast<int>(ctx->b_cap * (F / 128));
+  g1->max_tiles = static_cast<int>(ctx->b_cap * p1.n_tiles);
   return true;
 }
 
 // The W2 GEMM into *g2: h3 = h2 W2[e]^T from the h2 row bundle in scratch.
-bool fill_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uint8_t* h3, GemmLaunch* g2) {
+bool fill_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uint8_t* h3, GemmLaunch* g2, bool pairs) {
   const moe_config& c = ctx->cfg;
   const int D = c.d_model, F = c.d_ff, E = c.num_experts;
   const bool mx = c.precision == MOE_MXFP8;
   const int64_t R = ctx->r_cap;
   g2->mx = mx;
-  g2->na = pair_tiles(D);
+  g2->na = pairs ? 1 : pair_tiles(D);
   g2->epi = kEpiStore;
-  g2->mode = kGroupedM;
+  g2->mode = pairs ? kGroupedMP : kGroupedM;
   if (!make_tmap(&g2->tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128) ||
       !make_tmap(&g2->tmB, B(ctx, MOE_BUF_H2ROW), mx, R, F, 32) ||
       !make_grouped_m_boxes(g2, W2->data, static_cast<int64_t>(E) * D, W2->scale, B(ctx, MOE_BUF_H2ROW), R, mx, F))
@@ -369,7 +376,7 @@ moe_status run_gather_w13(moe_ctx* ctx, const void* x, const RoutingPtrs& rp, co
 
   // ---- W13 + SwiGLU
   GemmLaunch g1{};
-  if (!fill_w13(ctx, rp, W13, act, SL, marks, &g1)) return MOE_ERR_CUDA;
+  if (!fill_w13(ctx, rp, W13, act, SL, marks, &g1, use_pairs(ctx))) return MOE_ERR_CUDA;
   MOE_TRY(launch_gemm(g1, sms, stream));
   ctx->launches += 1;
   if (marks) MOE_TRY(stage_mark(ctx, 0, 3, stream));
@@ -385,7 +392,7 @@ moe_status run_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uin
   const int64_t R = ctx->r_cap;
   // ---- W2
   GemmLaunch g2{};
-  if (!fill_w2(ctx, rp, W2, h3, &g2)) return MOE_ERR_CUDA;
+  if (!fill_w2(ctx, rp, W2, h3, &g2, use_pairs(ctx))) return MOE_ERR_CUDA;
   MOE_TRY(launch_gemm(g2, sms, stream));
   ctx->launches += 1;
   return MOE_OK;
@@ -399,7 +406,8 @@ moe_status run_fused_forward(moe_ctx* ctx, int T, const void* x, const int32_t* 
   const moe_config& c = ctx->cfg;
   const SavedLayout SL = saved_layout(&c);
   GemmLaunch g1{}, g2{};
-  if (!fill_w13(ctx, rp, W13, nullptr, SL, true, &g1) || !fill_w2(ctx, rp, W2, B(ctx, MOE_BUF_H3), &g2))
+  if (!fill_w13(ctx, rp, W13, nullptr, SL, true, &g1, false) ||
+      !fill_w2(ctx, rp, W2, B(ctx, MOE_BUF_H3), &g2, false))
     return MOE_ERR_CUDA;
   if (g1.p.a_pair_box != 2 || g2.p.a_pair_box != 1 || !g1.p.b_full_box || !g2.p.b_full_box)
     return MOE_ERR_UNSUPPORTED;
@@ -539,6 +547,7 @@ moe_status moe_ctx_create(const moe_config* cfg, moe_ctx** out) {
   }
   c->r_cap = row_cap(cfg);
   c->b_cap = block_cap(cfg);
+  c->pair_tiles_auto = static_cast<int64_t>(cfg->max_tokens) * cfg->top_k >= 128LL * cfg->num_experts;
   const ScratchLayout L = scratch_layout(cfg);
   c->bytes = L.total;
   if (cudaMalloc(&c->base, c->bytes) != cudaSuccess) {
@@ -613,6 +622,12 @@ moe_status moe_ctx_test_fused_stall(moe_ctx* ctx, int stall, int64_t wait_cycles
   if (!ctx || wait_cycles < 0) return MOE_ERR_INVALID_ARG;
   ctx->fused_stall = stall ? 1 : 0;
   ctx->fused_wait = wait_cycles;
+  return MOE_OK;
+}
+
+moe_status moe_ctx_test_tile_mode(moe_ctx* ctx, int mode) {
+  if (!ctx || mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
+  ctx->tile_mode = mode;
   return MOE_OK;
 }
 
@@ -921,10 +936,11 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
 
   // ---- W13 DGRAD: dxr = dh1 W13[e]
   GemmLaunch g3{};
+  const bool pairs3 = use_pairs(ctx);
   g3.mx = mx;
-  g3.na = pair_tiles(D);
+  g3.na = pairs3 ? 1 : pair_tiles(D);
   g3.epi = kEpiStore;
-  g3.mode = kGroupedM;
+  g3.mode = pairs3 ? kGroupedMP : kGroupedM;
   // MXFP8 without transposed codes: A is W13's forward codes [E*2F rows (K),
   // D columns (M)], read MN-major, one box per 128-column weight tile
   const bool mn13 = mx && W13->data_t == nullptr;

@@ -17,6 +17,15 @@
 //    Experts get only ~32 rows at the 384-expert shape, so putting weights
 //    on the 128-wide M side keeps the MMA from computing padding and reads
 //    each weight tile once per row block.
+//  * grouped-M over row-block pairs (kGroupedMP), for routings dense enough
+//    that experts have two or more blocks: B is two consecutive blocks of
+//    one expert (N up to 256).  A tensor-core instruction of N = 128 takes
+//    about as long as one of N = 256 on this part, so at the compute-bound
+//    shapes 256-wide instructions double the rate.  One A tile of 128 rows
+//    per stage (a 256-column accumulator: single-buffered in MXFP8, whose
+//    scale columns need the rest of TMEM); the SwiGLU forward's A tile is 64
+//    gate rows followed by the 64 up rows of the same features, and its
+//    epilogue pairs them up through shared memory.
 //  * grouped-K (WGRAD): dW_e[m, n] = sum over the expert's rows of
 //    colA[m, r] colB[n, r]; both operands are column bundles stored
 //    [features, rows], so the contraction runs over the expert's row range.
@@ -61,12 +70,14 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
                 const __grid_constant__ CUtensorMap aux3, const GemmParams p) {
   using C = Cfg<MX, NA, MODE>;
   constexpr int S = C::S;
-  constexpr int kStep = (NA == 2 && EPI != kEpiSwigluFwd) ? 256 : 128;
+  constexpr bool PAIR = C::PAIR;
+  constexpr int kStep = PAIR ? (EPI == kEpiSwigluFwd ? 64 : 128) : ((NA == 2 && EPI != kEpiSwigluFwd) ? 256 : 128);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + S * C::STAGE;
   uint8_t* sfg = staging + C::STAGING;     // [SFR][GROUP_BYTES]: scale-atom groups (SFG)
-  uint64_t* full = reinterpret_cast<uint64_t*>(sfg + C::SFG_BYTES);
+  uint8_t* xbuf = sfg + C::SFG_BYTES;      // [EXCH]: the pair SwiGLU epilogue's exchange
+  uint64_t* full = reinterpret_cast<uint64_t*>(xbuf + C::EXCH);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + C::ACC_BUFS;
@@ -78,7 +89,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfg_empty + C::SFR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_abort = abort_flag + 1;  // [EPI_GROUPS]: a group's warps leave together
-  uint8_t* cache = staging + C::STAGING + C::SFG_BYTES + 256;
+  uint8_t* cache = xbuf + C::EXCH + 256;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -125,15 +136,18 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int nblk = (MODE == kGroupedM) ? p.hdr[1] : 0;
-  const int num_tiles = (MODE == kGroupedM) ? nblk * p.n_tiles : p.E * p.m_tiles * p.n_tiles;
+  const int nblk = (MODE != kGroupedK) ? p.hdr[1] : 0;
+  const int num_tiles = (MODE == kGroupedM)    ? nblk * p.n_tiles
+                        : (MODE == kGroupedMP) ? p.hdr[4] * p.n_tiles
+                                               : p.E * p.m_tiles * p.n_tiles;
   MetaCache mc;
   mc.blocks = reinterpret_cast<const int4*>(cache);
+  mc.ncache = C::CACHE / 16;
   mc.poff = reinterpret_cast<const int*>(cache);
   mc.bstart = reinterpret_cast<const int*>(cache) + 1028;
-  if (MODE == kGroupedM) {
+  if (MODE != kGroupedK) {
     int4* sb = reinterpret_cast<int4*>(cache);
-    for (int i = threadIdx.x; i < min(nblk, kCacheBlocks); i += blockDim.x) sb[i] = p.blocks[i];
+    for (int i = threadIdx.x; i < min(nblk, mc.ncache); i += blockDim.x) sb[i] = p.blocks[i];
   } else {
     int* sp = reinterpret_cast<int*>(cache);
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
@@ -181,10 +195,31 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
         if (lane == 0) {
           uint8_t* sa = smem + slot * C::STAGE;
           uint8_t* sb = sa + NA * kABytes;
-          uint8_t* ssf = sb + kBBytes;
+          uint8_t* ssf = sa + C::SF_OFF;
           const int rb = stage_row_bytes<MODE, C::BK, MX ? 1 : 2>(t, ks);
-          mbar_arrive_expect_tx(&full[slot], (NA * 128 + t.b_rows) * rb + (C::SFG ? 0 : C::SF_BYTES));
           const int kx = t.k0 + ks * C::BK;
+          if (PAIR) {
+            // one A tile (SwiGLU: its gate and up halves in one 3D box), B as
+            // full 128-row boxes then 32-row boxes; MXFP8: the weight's atom
+            // (two for the halves) and one atom per routing block of the pair
+            const bool two = t.b_rows > 128;
+            mbar_arrive_expect_tx(&full[slot], (128 + t.b_rows) * rb +
+                                                   (MX ? ((EPI == kEpiSwigluFwd ? 2 : 1) + (two ? 2 : 1)) * kAtom : 0));
+            if (EPI == kEpiSwigluFwd) tma_load_3d(sa, &aux0, &full[slot], kx, t.out_col0, 2 * t.e);
+            else if (MX && p.a_mn) tma_load_2d(sa, &tmA, &full[slot], t.a_row[0] - t.e * p.a_rows_per_expert, t.e * p.K + kx);
+            else tma_load_2d(sa, &tmA, &full[slot], kx, t.a_row[0]);
+            int r = 0;
+            if (p.b_full_box)
+              for (; r + 128 <= t.b_rows; r += 128) tma_load_2d(sb + r * 128, &aux1, &full[slot], kx, t.b_row0 + r);
+            for (; r < t.b_rows; r += 32) tma_load_2d(sb + r * 128, &tmB, &full[slot], kx, t.b_row0 + r);
+            if (MX) {
+              if (EPI == kEpiSwigluFwd) tma_load_4d(ssf, &aux2, &full[slot], 0, ks, t.out_col0 >> 7, 2 * t.e);
+              else bulk_load(ssf, p.sfa + (t.sfa_atom[0] + ks) * kAtom, kAtom, &full[slot]);
+              bulk_load(ssf + 2 * kAtom, p.sfb + (t.sfb_atom + ks) * kAtom, kAtom, &full[slot]);
+              if (two) bulk_load(ssf + 3 * kAtom, p.sfb + (t.sfb_atom + p.sfb_ts + ks) * kAtom, kAtom, &full[slot]);
+            }
+          } else {
+          mbar_arrive_expect_tx(&full[slot], (NA * 128 + t.b_rows) * rb + (C::SFG ? 0 : C::SF_BYTES));
           if (MODE == kGroupedK) {
             const CUtensorMap* ta = rb == 128 ? &tmA : (rb == 64 ? &aux0 : &aux2);
             const CUtensorMap* tb = rb == 128 ? &tmB : (rb == 64 ? &aux1 : &aux3);
@@ -229,6 +264,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
             }
             bulk_load(ssf + NA * kAtom, p.sfb + (t.sfb_atom + ks) * kAtom, kAtom, &full[slot]);
           }
+          }
         }
         __syncwarp();
       }
@@ -259,7 +295,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty[acc], aph ^ 1, abort_flag, p.err))) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem + acc * C::ACC_COLS;
-      const uint32_t idesc = MX ? (idesc_mxf8(t.b_rows, 0, 0) | (MODE == kGroupedM && p.a_mn ? kIdescAMnMajor : 0u))
+      const uint32_t idesc = MX ? (idesc_mxf8(t.b_rows, 0, 0) | (MODE != kGroupedK && p.a_mn ? kIdescAMnMajor : 0u))
                                 : idesc_bf16(t.b_rows);
       for (int ks = 0; ks < t.kstages; ++ks, ++it) {
         const uint32_t slot = it % S, ph = (it / S) & 1;
@@ -276,7 +312,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
         const int rb = stage_row_bytes<MODE, C::BK, MX ? 1 : 2>(t, ks);
         const uint64_t bdesc0 = sdesc_k_sw(sb, rb);
         // MN-major A (grouped-M MXFP8 with p.a_mn): a K step of 32 rows is 4 KB on
-        const bool amn = MX && MODE == kGroupedM && p.a_mn;
+        const bool amn = MX && MODE != kGroupedK && p.a_mn;
         uint64_t adesc0[NA];
 #pragma unroll
         for (int j = 0; j < NA; ++j) adesc0[j] = amn ? sdesc_mn_sw128(sa + j * kABytes) : sdesc_k_sw(sa + j * kABytes, rb);
@@ -341,6 +377,21 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
             break;
           }
         }
+        if (PAIR && EPI == kEpiSwigluFwd) {
+          // The A tile is rows f0..f0+63 of the gate half, then of the up
+          // half: its atom (row p at byte (p%32)*16 + (p/32)*4 + l) takes
+          // rows 64a..64a+63 (a = (f0/64) % 2) of the gate half's 128-row
+          // atom, then the same rows of the up half's.  Lane r builds its
+          // 16 bytes from 8 of each, over the gate atom's place.
+          uint8_t* at = smem + slot * C::STAGE + C::SF_OFF;
+          const int a8 = ((t.out_col0 >> 6) & 1) * 8;
+          const uint2 g = *reinterpret_cast<const uint2*>(at + lane * 16 + a8);
+          const uint2 u = *reinterpret_cast<const uint2*>(at + kAtom + lane * 16 + a8);
+          __syncwarp();
+          *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(g.x, g.y, u.x, u.y);
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
         tc_fence_after();
         if (lane == 0) {
           const uint32_t sfcol = tmem + C::SF_COL0 + slot * C::SF_COLS;
@@ -350,6 +401,12 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
             tc_cp_sf(sfcol + 4, sdesc_sf_atom(grp + C::GS * kAtom));
             // the group's last stage: its buffer may be refilled once these copies completed
             if (ks % C::GS == C::GS - 1 || ks == t.kstages - 1) tc_commit(&sfg_empty[cur % C::SFR]);
+          } else if (PAIR) {
+            // the weight's atom (SwiGLU: built below), then the pair's B atoms
+            const uint32_t ssf = smem_u32(smem + slot * C::STAGE) + C::SF_OFF;
+            tc_cp_sf(sfcol, sdesc_sf_atom(ssf));
+            tc_cp_sf(sfcol + 4, sdesc_sf_atom(ssf + 2 * kAtom));
+            if (t.b_rows > 128) tc_cp_sf(sfcol + 8, sdesc_sf_atom(ssf + 3 * kAtom));
           } else {
             const uint32_t ssf = smem_u32(smem + slot * C::STAGE) + NA * kABytes + kBBytes;
 #pragma unroll
@@ -387,7 +444,8 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       uint32_t hp[32];
       if (EPI == kEpiSwigluBwd && 32 * h < t.b_rows) load_h1_chunk(p, t, t.out_col0 + lrow, 32 * h, hp);
       const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&tfull[acc], aph, abort_flag, p.err));
-      if (!staged && !ok) break;
+      constexpr bool pair_swiglu = PAIR && EPI == kEpiSwigluFwd;   // leaves through its own barrier
+      if (!staged && !pair_swiglu && !ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
       if (staged) {
@@ -471,8 +529,12 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
         }
         continue;
       }
-      if (EPI == kEpiStore) epi_store<NA>(p, t, tbase, lrow, lane, h, &tempty[acc]);
-      else if (EPI == kEpiSwigluFwd) epi_swiglu_fwd<MX>(p, t, tbase, lrow, lane, h, &tempty[acc]);
+      if (EPI == kEpiStore) epi_store<NA, PAIR ? 4 : 2>(p, t, tbase, lrow, lane, h, &tempty[acc]);
+      else if (pair_swiglu) {
+        if (!epi_swiglu_fwd_pair<MX>(p, t, tbase, q, lane, h, ok, &tempty[acc], xbuf, epi_abort, kEpiBarrier,
+                                     C::EPI_THREADS))
+          break;
+      } else if (EPI == kEpiSwigluFwd) epi_swiglu_fwd<MX>(p, t, tbase, lrow, lane, h, &tempty[acc]);
       else if (EPI == kEpiSwigluBwd) {
         // its two accumulator buffers cover this (heavier) epilogue: release at the end
         epi_swiglu_bwd<MX>(p, t, tbase, lrow, lane, h, hp);
@@ -508,8 +570,8 @@ cudaError_t launch_impl(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   const int q = grid / p.n_tiles;
   p.walk[0] = grid;
   p.walk[1] = grid % p.n_tiles;
-  p.walk[2] = MODE == kGroupedM ? q : q % p.m_tiles;
-  p.walk[3] = MODE == kGroupedM ? 0 : q / p.m_tiles;
+  p.walk[2] = MODE != kGroupedK ? q : q % p.m_tiles;
+  p.walk[3] = MODE != kGroupedK ? 0 : q / p.m_tiles;
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.tmC, g.aux[0], g.aux[1], g.aux[2], g.aux[3], p);
   return cudaGetLastError();
 }
@@ -531,6 +593,10 @@ cudaError_t launch_gemm(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   MOE_GEMM_CASE(true, 2, kEpiStore, kGroupedM)
   MOE_GEMM_CASE(false, 1, kEpiSwigluBwd, kGroupedM)
   MOE_GEMM_CASE(true, 1, kEpiSwigluBwd, kGroupedM)
+  MOE_GEMM_CASE(false, 1, kEpiSwigluFwd, kGroupedMP)
+  MOE_GEMM_CASE(true, 1, kEpiSwigluFwd, kGroupedMP)
+  MOE_GEMM_CASE(false, 1, kEpiStore, kGroupedMP)
+  MOE_GEMM_CASE(true, 1, kEpiStore, kGroupedMP)
   if (g.epi == kEpiWgrad && g.mode == kGroupedK &&
       (g.p.tma_store == kDwStoreF32 || g.p.tma_store == kDwAddF32))
     return g.mx ? launch_impl<true, 1, kEpiWgrad, kGroupedK, true>(g, num_sms, stream)

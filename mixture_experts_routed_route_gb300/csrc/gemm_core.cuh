@@ -39,14 +39,16 @@ struct Tile {
 };
 
 struct MetaCache {
-  const int4* blocks;   // grouped-M: s_blocks[b] for b < kCacheBlocks
+  const int4* blocks;   // grouped-M: s_blocks[b] for b < ncache
+  int ncache = kCacheBlocks;
   const int* poff;      // grouped-K: poffsets[0..E]
   const int* bstart;    // grouped-K: bstart[0..E]
 };
 
 // STEP: weight rows per grouped-M output tile: 128, or 256 when the two A
 // tiles of an NA = 2 store tile are adjacent 128-row blocks (the SwiGLU
-// forward's second A tile is the up half, F rows on).
+// forward's second A tile is the up half, F rows on); over row-block pairs,
+// 128 (store) or 64 (SwiGLU forward: 64 features, their gate and up rows).
 //
 // Grouped-M tiles run routing block by routing block, all output slices of
 // a block together: the resident CTAs then cover a few blocks at a time,
@@ -70,8 +72,8 @@ struct TileWalk {
     tile = tile0;
     n = tile0 % p.n_tiles;
     const int q = tile0 / p.n_tiles;
-    m = MODE == kGroupedM ? q : q % p.m_tiles;
-    e = MODE == kGroupedM ? 0 : q / p.m_tiles;
+    m = MODE != kGroupedK ? q : q % p.m_tiles;
+    e = MODE != kGroupedK ? 0 : q / p.m_tiles;
   }
   __device__ __forceinline__ void advance(const GemmParams& p) {
     tile += p.walk[0];
@@ -92,7 +94,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const TileWalk<
   Tile t;
   if (MODE == kGroupedM) {
     const int b = w.m, n = w.n;
-    const int4 blk = (b < kCacheBlocks) ? mc.blocks[b] : p.blocks[b];
+    const int4 blk = (b < mc.ncache) ? mc.blocks[b] : p.blocks[b];
     t.e = blk.x;
     t.blk = b;
     t.a_row[0] = blk.x * p.a_rows_per_expert + n * STEP;
@@ -107,6 +109,27 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const TileWalk<
     t.sfa_atom[0] = static_cast<long long>(t.a_row[0] >> 7) * p.sfa_ts;
     t.sfa_atom[1] = static_cast<long long>(t.a_row[1] >> 7) * p.sfa_ts;
     t.sfb_atom = static_cast<long long>(b) * p.sfb_ts;
+  } else if (MODE == kGroupedMP) {
+    // pair m: word 3 of blocks[m] = (first block << 1) | second present;
+    // the first block of a two-block pair is a full 128 rows
+    const int m = w.m, n = w.n;
+    const int desc = ((m < mc.ncache) ? mc.blocks[m] : p.blocks[m]).w;
+    const int fb = desc >> 1;
+    const int4 b0 = (fb < mc.ncache) ? mc.blocks[fb] : p.blocks[fb];
+    t.e = b0.x;
+    t.blk = fb;
+    t.a_row[0] = b0.x * p.a_rows_per_expert + n * STEP;
+    t.a_row[1] = t.a_row[0] + (STEP == 64 ? p.a_up_offset : 0);
+    t.b_row0 = b0.y;
+    t.b_rows = (desc & 1) ? 128 + ((fb + 1 < mc.ncache) ? mc.blocks[fb + 1] : p.blocks[fb + 1]).z : b0.z;
+    t.k0 = 0;
+    t.kstages = p.K / BK;
+    t.klast = BK;
+    t.out_row0 = b0.y;
+    t.out_col0 = n * STEP;
+    t.sfa_atom[0] = static_cast<long long>(t.a_row[0] >> 7) * p.sfa_ts;
+    t.sfa_atom[1] = static_cast<long long>(t.a_row[1] >> 7) * p.sfa_ts;
+    t.sfb_atom = static_cast<long long>(fb) * p.sfb_ts;
   } else {
     const int e = w.e, m = w.m, n = w.n;
     const int k0 = mc.poff[e], klen = mc.poff[e + 1] - k0;
@@ -218,16 +241,17 @@ __device__ __forceinline__ void release_acc(uint64_t* tempty, int lane) {
 
 // h3 / input-gradient rows: out[row][feature] = bf16(acc).
 // With NA = 2 the two accumulators hold features out_col0 + [0, 128) and
-// out_col0 + [128, 256).  Every chunk is read from TMEM first, rounded to
-// BF16 pairs at once (the stored value), and the accumulator handed back
+// out_col0 + [128, 256).  NC: chunks per warp (2: up to 128 token columns,
+// 4: a row-block pair's 256).  Every chunk is read from TMEM first, rounded
+// to BF16 pairs at once (the stored value), and the accumulator handed back
 // before the first store.
-template <int NA>
+template <int NA, int NC = 2>
 __device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, uint32_t tbase, int lrow, int lane,
                                           int h, uint64_t* tempty) {
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0);
-  uint32_t pk[NA][2][16];
+  uint32_t pk[NA][NC][16];
 #pragma unroll
-  for (int ci = 0; ci < 2; ++ci) {
+  for (int ci = 0; ci < NC; ++ci) {
     const int c0 = 32 * h + 64 * ci;
     if (c0 < t.b_rows) {
       uint32_t v[NA][32];   // both accumulators' chunk, one wait
@@ -244,7 +268,7 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, ui
 #pragma unroll
   for (int j = 0; j < NA; ++j)
 #pragma unroll
-    for (int ci = 0; ci < 2; ++ci) {
+    for (int ci = 0; ci < NC; ++ci) {
       const int c0 = 32 * h + 64 * ci;
       if (c0 < t.b_rows) {
         __nv_bfloat16* o = out + static_cast<long long>(t.out_row0 + c0) * p.out0_pitch + t.out_col0 + j * 128 + lrow;
@@ -256,6 +280,45 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const Tile& t, ui
         }
       }
     }
+}
+
+// One 32-token chunk of feature f: gu[i] = (g, u) of token row row0 + i as
+// a BF16 pair; the rows lie in routing block blk from its row prow0 on.
+template <bool MX>
+__device__ __forceinline__ void swiglu_fwd_chunk(const GemmParams& p, long long row0, int f, int blk, int prow0,
+                                                 const uint32_t (&gu)[32], int lane) {
+  float hv[32];
+  const float L = p.swiglu_limit;
+  int cg = 0, cu = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const long long row = row0 + i;
+    const uint32_t w = gu[i];
+    if (p.save_h1) {
+      p.h1[row * p.h1_pitch + f] = __ushort_as_bfloat16(static_cast<unsigned short>(w & 0xFFFFu));
+      p.h1[row * p.h1_pitch + p.F + f] = __ushort_as_bfloat16(static_cast<unsigned short>(w >> 16));
+    }
+    float g = bf16_lo(w), u = bf16_hi(w);
+    if (L > 0.0f) {
+      cg += g > L;
+      cu += fabsf(u) > L;
+      g = fminf(g, L);
+      u = fminf(fmaxf(u, -L), L);
+    }
+    hv[i] = silu_f(g) * u;
+  }
+  if (L > 0.0f && p.clip != nullptr) {
+    cg = __reduce_add_sync(0xFFFFFFFFu, cg);
+    cu = __reduce_add_sync(0xFFFFFFFFu, cu);
+    if (lane == 0) {
+      if (cg) atomicAdd(&p.clip[0], static_cast<unsigned long long>(cg));
+      if (cu) atomicAdd(&p.clip[1], static_cast<unsigned long long>(cu));
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    store_row_val<MX>(p, p.out0, p.out0_pitch, row0 + i, f, hv[i], lane, blk, prow0 + i);
+  if (p.want_col) store_col32<MX>(p, f, row0, blk, prow0 >> 5, hv);
 }
 
 // Fused SwiGLU forward: g, u from the two accumulators, rounded to BF16
@@ -289,40 +352,92 @@ __device__ __forceinline__ void epi_swiglu_fwd(const GemmParams& p, const Tile& 
 #pragma unroll
   for (int ci = 0; ci < 2; ++ci) {
     const int c0 = 32 * h + 64 * ci;
-    if (c0 >= t.b_rows) continue;
-    float hv[32];
-    const float L = p.swiglu_limit;
-    int cg = 0, cu = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const long long row = t.out_row0 + c0 + i;
-      const uint32_t w = gu[ci][i];
-      if (p.save_h1) {
-        p.h1[row * p.h1_pitch + f] = __ushort_as_bfloat16(static_cast<unsigned short>(w & 0xFFFFu));
-        p.h1[row * p.h1_pitch + p.F + f] = __ushort_as_bfloat16(static_cast<unsigned short>(w >> 16));
-      }
-      float g = bf16_lo(w), u = bf16_hi(w);
-      if (L > 0.0f) {
-        cg += g > L;
-        cu += fabsf(u) > L;
-        g = fminf(g, L);
-        u = fminf(fmaxf(u, -L), L);
-      }
-      hv[i] = silu_f(g) * u;
-    }
-    if (L > 0.0f && p.clip != nullptr) {
-      cg = __reduce_add_sync(0xFFFFFFFFu, cg);
-      cu = __reduce_add_sync(0xFFFFFFFFu, cu);
-      if (lane == 0) {
-        if (cg) atomicAdd(&p.clip[0], static_cast<unsigned long long>(cg));
-        if (cu) atomicAdd(&p.clip[1], static_cast<unsigned long long>(cu));
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      store_row_val<MX>(p, p.out0, p.out0_pitch, t.out_row0 + c0 + i, f, hv[i], lane, t.blk, c0 + i);
-    if (p.want_col) store_col32<MX>(p, f, t.out_row0 + c0, t.blk, c0 >> 5, hv);
+    if (c0 < t.b_rows) swiglu_fwd_chunk<MX>(p, t.out_row0 + c0, f, t.blk, c0, gu[ci], lane);
   }
+}
+
+// Fused SwiGLU forward over a row-block pair.  The A tile is 64 gate rows
+// and then the 64 up rows of the same features, so TMEM lanes 0..63 hold g
+// and lanes 64..127 u: the warp of lane quadrant q < 2 and the warp of
+// quadrant q + 2 with the same chunk set h hold g and u of the same 32
+// features (feature out_col0 + 32 q + lane).  Of their four 32-token chunks
+// (columns 32 h + 64 ci), the gate warp finishes ci = 0 and 2 and the up
+// warp ci = 1 and 3; each hands the other its BF16 values (the stored h1) of
+// the partner's chunks through `xbuf`, 16 KB per round, two rounds.  Every
+// epilogue warp passes the same named barriers; if any warp's accumulator
+// wait gave up (`ok` false), all leave together and it returns false.
+template <bool MX>
+__device__ __forceinline__ bool epi_swiglu_fwd_pair(const GemmParams& p, const Tile& t, uint32_t tbase, int q,
+                                                    int lane, int h, bool ok, uint64_t* tempty, uint8_t* xbuf,
+                                                    volatile int* abort_flag, int bar_id, int bar_threads) {
+  const int up = q >> 1, qg = q & 1;
+  const int f = t.out_col0 + 32 * qg + lane;
+  uint4* mine = reinterpret_cast<uint4*>(xbuf + (((qg * 2 + h) * 2 + up) << 11));
+  const uint4* theirs = reinterpret_cast<const uint4*>(xbuf + (((qg * 2 + h) * 2 + (up ^ 1)) << 11));
+  if (!ok && lane == 0) *abort_flag = 1;
+  named_bar_sync(bar_id, bar_threads);
+  if (*abort_flag) return false;
+  uint32_t own[2][16], oth[16], par[2][16];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int co = 32 * h + 64 * (2 * k + up), cx = 32 * h + 64 * (2 * k + (up ^ 1));
+    uint32_t vo[32], vx[32];
+    if (co < t.b_rows) tmem_ld32(tbase + co, vo);
+    if (cx < t.b_rows) tmem_ld32(tbase + cx, vx);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      own[k][i] = pack_bf16x2(u2f(vo[2 * i]), u2f(vo[2 * i + 1]));
+      oth[i] = pack_bf16x2(u2f(vx[2 * i]), u2f(vx[2 * i + 1]));
+    }
+    if (k == 0 && cx < t.b_rows) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mine[j * 32 + lane] = make_uint4(oth[4 * j], oth[4 * j + 1], oth[4 * j + 2], oth[4 * j + 3]);
+    }
+  }
+  release_acc(tempty, lane);
+  const int co0 = 32 * h + 64 * up, co1 = co0 + 128, cx1 = 32 * h + 64 * (2 + (up ^ 1));
+  named_bar_sync(bar_id, bar_threads);   // round 0 written
+  if (co0 < t.b_rows) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 w = theirs[j * 32 + lane];
+      par[0][4 * j] = w.x;
+      par[0][4 * j + 1] = w.y;
+      par[0][4 * j + 2] = w.z;
+      par[0][4 * j + 3] = w.w;
+    }
+  }
+  named_bar_sync(bar_id, bar_threads);   // round 0 read
+  if (cx1 < t.b_rows) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mine[j * 32 + lane] = make_uint4(oth[4 * j], oth[4 * j + 1], oth[4 * j + 2], oth[4 * j + 3]);
+  }
+  named_bar_sync(bar_id, bar_threads);   // round 1 written
+  if (co1 < t.b_rows) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 w = theirs[j * 32 + lane];
+      par[1][4 * j] = w.x;
+      par[1][4 * j + 1] = w.y;
+      par[1][4 * j + 2] = w.z;
+      par[1][4 * j + 3] = w.w;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int co = k ? co1 : co0;
+    if (co >= t.b_rows) continue;
+    uint32_t gu[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t g2 = up ? par[k][i] : own[k][i], u2 = up ? own[k][i] : par[k][i];
+      gu[2 * i] = __byte_perm(g2, u2, 0x5410);       // (g, u) of token 2i
+      gu[2 * i + 1] = __byte_perm(g2, u2, 0x7632);   // of token 2i + 1
+    }
+    swiglu_fwd_chunk<MX>(p, t.out_row0 + co, f, t.blk + (co >> 7), co & 127, gu, lane);
+  }
+  return true;
 }
 
 // Fused SwiGLU backward: dh2 from the accumulator (W2 DGRAD), g and u from
@@ -479,7 +594,11 @@ __device__ __forceinline__ void stage_chunk_f32(const uint32_t (&r)[32], bool ze
 template <bool MX, int NA, int MODE>
 struct Cfg {
   static constexpr bool WGRAD = MODE == kGroupedK;
-  static constexpr int SF_BYTES = MX ? (NA + 1) * kAtom : 0;
+  // over row-block pairs: one A tile, a B operand of up to 256 rows (two
+  // 128-row boxes), scale atoms of two A halves (gate, up) and two B blocks
+  static constexpr bool PAIR = MODE == kGroupedMP;
+  static_assert(!PAIR || NA == 1, "one A tile per stage over row-block pairs");
+  static constexpr int SF_BYTES = MX ? (PAIR ? 4 : NA + 1) * kAtom : 0;
   // Scale-atom groups (MXFP8, grouped-M, one A tile): the atoms of GS
   // consecutive stages of a tile are consecutive in memory for the weight
   // and for the row block, so they come in two copies per group into a
@@ -490,14 +609,20 @@ struct Cfg {
   static constexpr int GS = 4, SFR = 2;
   static constexpr int GROUP_BYTES = GS * (NA + 1) * kAtom;
   static constexpr int SFG_BYTES = SFG ? SFR * GROUP_BYTES : 0;
-  static constexpr int STAGE = ((NA * kABytes + kBBytes + (SFG ? 0 : SF_BYTES)) + 1023) / 1024 * 1024;
-  static constexpr int S = WGRAD ? 4 : ((NA == 2) ? 4 : 6);  // pipeline stages
+  static constexpr int B_BYTES = PAIR ? 2 * kBBytes : kBBytes;
+  static constexpr int SF_OFF = NA * kABytes + B_BYTES;      // a stage's scale atoms
+  static constexpr int STAGE = ((SF_OFF + (SFG ? 0 : SF_BYTES)) + 1023) / 1024 * 1024;
+  static constexpr int S = WGRAD ? 4 : ((NA == 2 || PAIR) ? 4 : 6);  // pipeline stages
   static constexpr int STAGING = WGRAD ? 2 * 32768 : 0;    // weight-gradient store buffers
-  // accumulator buffers: two, except with two MXFP8 A tiles (2 x 256
-  // columns leave no room in TMEM's 512 for the stages' scale columns)
-  static constexpr int ACC_BUFS = (NA == 1 || !MX) ? 2 : 1;
-  static constexpr int ACC_COLS = NA * 128;
-  static constexpr int SF_COLS = (NA + 1) * 4;             // scale columns per stage
+  // accumulator buffers: two, except with two MXFP8 A tiles or a 256-wide
+  // MXFP8 pair tile (2 x 256 columns leave no room in TMEM's 512 for the
+  // stages' scale columns)
+  static constexpr int ACC_BUFS = PAIR ? (MX ? 1 : 2) : ((NA == 1 || !MX) ? 2 : 1);
+  static constexpr int ACC_COLS = PAIR ? 256 : NA * 128;
+  static constexpr int SF_COLS = PAIR ? 12 : (NA + 1) * 4;  // scale columns per stage (B: 8 over pairs)
+  // the pair SwiGLU epilogue's exchange buffer; a smaller metadata cache
+  static constexpr int EXCH = PAIR ? 16384 : 0;
+  static constexpr int CACHE = PAIR ? 8192 : kCacheBytes;
   static constexpr uint32_t SF_COL0 = ACC_BUFS * ACC_COLS;
   static constexpr int BK = MX ? 128 : 64;                 // contraction elements per stage
   static constexpr int KMMA = MX ? 32 : 16;                // contraction elements per MMA
@@ -516,7 +641,9 @@ struct Cfg {
   // MMA thread issues nothing but MMAs and commits
   static constexpr int SF_WARPS = MX ? 1 : 0;
   static constexpr int THREADS = 64 + EPI_THREADS + 32 * SF_WARPS;
-  static constexpr int SMEM = 1024 + S * STAGE + STAGING + SFG_BYTES + 256 + kCacheBytes;
+  static constexpr int SMEM = 1024 + S * STAGE + STAGING + SFG_BYTES + EXCH + 256 + CACHE;
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+  static_assert(ACC_BUFS * ACC_COLS + S * (MX ? SF_COLS : 0) <= 512, "tensor memory columns");
 };
 
 }  // namespace

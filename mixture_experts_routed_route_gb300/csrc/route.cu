@@ -11,6 +11,14 @@
 // (each expert padded to its row multiple) gather zeros and scatter nowhere;
 // ID -1 is an inactive route.
 //
+// Row-block pairs: the grouped GEMMs of dense enough routings take two
+// consecutive blocks of one expert (up to 256 rows) as one B operand, so
+// every tensor-core instruction is 256 wide.  Pair p of the routing is
+// described in the fourth word of blocks[p]: (first block << 1) | (1 if the
+// pair has a second block); the header's word 4 counts the pairs.  Each
+// expert's blocks pair up in order: blocks 0+1, 2+3, ..., the last alone
+// when the expert has an odd number.
+//
 // One CTA of 32 warps.  Warp w owns the contiguous route segment
 // [w*seg, (w+1)*seg); within a warp, routes are taken 32 at a time in
 // order, and lanes holding the same expert are grouped (one ballot per bit
@@ -179,8 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int pc = (c + kPad - 1) / kPad * kPad;
   const int nb = (pc + kBlockRows - 1) / kBlockRows;
-  int eo, ep, eb, to, tp, tb;
+  int eo, ep, eb, to, tp, tb, epr, tpr, d0, d1, d2, d3;
   block_scan3(tid < E ? c : 0, tid < E ? pc : 0, tid < E ? nb : 0, eo, ep, eb, to, tp, tb, ws);
+  const int np = (nb + 1) / 2;
+  block_scan3(tid < E ? np : 0, 0, 0, epr, d0, d1, tpr, d2, d3, ws);
   if (tid < E) {
     rp.counts[tid] = c;
     rp.offsets[tid] = eo;
@@ -210,8 +220,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     rp.hdr[1] = tb;
     rp.hdr[2] = tp;
     rp.hdr[3] = to;
+    rp.hdr[4] = tpr;
   }
   __syncthreads();
+  // pair descriptors, once every block entry is written
+  if (tid < E) {
+    for (int q = 0; q < np; ++q)
+      reinterpret_cast<int*>(rp.blocks + epr + q)[3] = ((eb + 2 * q) << 1) | (2 * q + 1 < nb ? 1 : 0);
+  }
 
   // ---- pass 3: stable scatter of each route to its row
   const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;

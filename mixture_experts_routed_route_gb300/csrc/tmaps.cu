@@ -78,6 +78,9 @@ bool make_tmap_nd(CUtensorMap* tm, CUtensorMapDataType dt, int rank, const void*
 //    [row tiles][K/128][128 words] (adjacent) or [2E][F/128][K/128][128]
 //    (halves) from `a_sf`;
 //  * a full 128-row routing block of B in one box.
+// Over row-block pairs (kGroupedMP) the SwiGLU forward's one A tile is the
+// same 3D box 64 rows high: 64 gate rows, then the up rows of the same
+// features.
 bool make_grouped_m_boxes(GemmLaunch* g, const void* a, int64_t a_rows, const void* a_sf, const void* b,
                           int64_t b_rows, bool mx, int64_t cols, int64_t halves_f) {
   const int esz = mx ? 1 : 2;
@@ -93,11 +96,12 @@ bool make_grouped_m_boxes(GemmLaunch* g, const void* a, int64_t a_rows, const vo
         return false;
     }
     g->p.a_pair_box = 1;
-  } else if (g->na == 2 && g->epi == kEpiSwigluFwd && halves_f > 0 && halves_f % 128 == 0) {
+  } else if ((g->na == 2 || g->mode == kGroupedMP) && g->epi == kEpiSwigluFwd && halves_f > 0 &&
+             halves_f % 128 == 0) {
     const cuuint64_t d[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(halves_f),
                              static_cast<cuuint64_t>(a_rows / halves_f)};
     const cuuint64_t st[2] = {static_cast<cuuint64_t>(cols * esz), static_cast<cuuint64_t>(halves_f * cols * esz)};
-    const cuuint32_t bx[3] = {static_cast<cuuint32_t>(128 / esz), 128, 2};
+    const cuuint32_t bx[3] = {static_cast<cuuint32_t>(128 / esz), g->mode == kGroupedMP ? 64u : 128u, 2};
     if (!make_tmap_nd(&g->aux[0], dt, 3, a, d, st, bx, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
     if (mx) {
       const cuuint64_t ft = static_cast<cuuint64_t>(halves_f / 128);

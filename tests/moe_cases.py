@@ -50,11 +50,15 @@ class Case:
 
 
 def run_gpu(case, precision=None, training=True, debug=False, out_init=None, max_tokens=None,
-            dx_init=None, dw_fp32=False, backward=True, swiglu_limit=0.0, weight_prec=None, max_ctas=0):
+            dx_init=None, dw_fp32=False, backward=True, swiglu_limit=0.0, weight_prec=None, max_ctas=0,
+            tile_mode=0, mn_major=False):
     """Forward (and backward) of a case through the C ABI; returns a dict of
     host arrays plus the layer object for further inspection.  weight_prec
     overrides the weights' preparation (e.g. "mxfp8_1x32"); max_ctas caps
-    the persistent grids (moe_ctx_set_max_ctas)."""
+    the persistent grids (moe_ctx_set_max_ctas); tile_mode picks the
+    grouped GEMMs' B tiles (moe_ctx_test_tile_mode: 1 row blocks, 2
+    row-block pairs, 0 the context's default); mn_major: MXFP8 weights
+    without transposed codes."""
     from mixture_experts_routed_route_gb300 import abi
     from mixture_experts_routed_route_gb300.layer import MoELayer, PreparedWeight
 
@@ -66,8 +70,10 @@ def run_gpu(case, precision=None, training=True, debug=False, out_init=None, max
                      swiglu_limit=swiglu_limit)
     if max_ctas:
         abi.moe_ctx_set_max_ctas(layer.ctx, max_ctas)
-    W13 = PreparedWeight(case.w13.to(dev), weight_prec or precision, with_transpose=training)
-    W2 = PreparedWeight(case.w2.to(dev), weight_prec or precision, with_transpose=training)
+    if tile_mode:
+        abi.moe_ctx_test_tile_mode(layer.ctx, tile_mode)
+    W13 = PreparedWeight(case.w13.to(dev), weight_prec or precision, with_transpose=training, mn_major=mn_major)
+    W2 = PreparedWeight(case.w2.to(dev), weight_prec or precision, with_transpose=training, mn_major=mn_major)
     x = case.x.to(dev)
     ids = torch.from_numpy(case.ids).to(dev)
     sc = torch.from_numpy(case.scores).to(dev)

@@ -55,3 +55,19 @@ def test_accumulated_fp32_weight_gradients_count_a_read_and_a_write():
     for k in bf:     # nothing else depends on the weight-gradient format
         if "wgrad" not in k:
             assert acc[k] == bf[k]
+
+
+def test_gemm_flops_add_up_to_the_step():
+    """The per-GEMM useful FLOPs sum to the step's: 6 R D F forward (W13 is
+    2F wide, W2 F deep), 12 R D F more for the four backward GEMMs."""
+    fwd = bench.GEMM_FLOPS["gemm_w13_swiglu"] + bench.GEMM_FLOPS["gemm_w2"]
+    assert fwd == 6.0
+    assert sum(bench.GEMM_FLOPS.values()) == 18.0
+    w = synth.WORKLOADS["e6_dense"]
+    R = w.T * w.K
+    ms = {"route": 0.02, "gemm_w13_swiglu": 0.3, "gemm_w2": 0.15, "combine": 0.04}
+    g = bench.gemm_tensor(ms, R, w, 1000.0)
+    want = 6.0 * R * w.D * w.F / 0.45e-3 / 1e12
+    assert abs(g["tflops"] - want) < 0.1 and abs(g["tensor_frac"] - want / 1000.0) < 1e-4
+    assert set(g["per_gemm_tensor_frac"]) == {"gemm_w13_swiglu", "gemm_w2"}
+    assert bench.gemm_tensor({"route": 0.02}, R, w, 1000.0) is None

@@ -1,0 +1,91 @@
+"""Grouped GEMMs over row-block pairs (B operands of two consecutive routing
+blocks of one expert, up to 256 rows) against the same GEMMs over single
+row blocks, and against the oracle.
+
+The two tilings contract every output element over the same K order, so the
+forward output, the input gradient, both weight gradients and the score
+gradient must agree bit for bit.  The cases mix full pairs (256 rows), pairs
+whose second block is short, experts with an odd number of blocks (a last
+block alone) and experts with a single short block; the SwiGLU forward's
+64-feature tiles start on both halves of the weight's 128-row scale atoms
+(F = 256, 384).  ("Mixture of Experts: How Routing Becomes GPU
+Computation", section 2, "Grouped GEMM": C_e = A_e B_e^T over each expert's
+ragged rows; Dist-MoE explainer section 05, "GPU Kernels: Tiles and Warp
+Roles": expert row tiles with masked tails.)"""
+
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_routed_route_gb300 import synth
+
+from moe_cases import TOL, Case, check_mx_wgrad, rel_err, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # 1200 routes over 4 experts, Zipf-skewed: 1 to 5 blocks per expert
+    "mx_ragged": lambda: synth.Workload("pair_mx", 600, 256, 256, 4, 2, "mxfp8", "zipf", inactive_frac=0.05,
+                                        zipf_s=0.8, seed=81),
+    "bf16_ragged": lambda: synth.Workload("pair_bf16", 600, 256, 384, 4, 2, "bf16", "zipf", inactive_frac=0.05,
+                                          zipf_s=0.8, seed=82),
+    # uniform: every expert about 2 full blocks
+    "mx_full": lambda: synth.Workload("pair_full", 512, 512, 384, 4, 2, "mxfp8", "uniform", seed=83),
+}
+
+FIELDS = ("out", "dx", "dW13", "dW2", "dp")
+
+
+def _both(w, **kw):
+    case = Case(w)
+    a = run_gpu(case, tile_mode=1, **kw)
+    b = run_gpu(case, tile_mode=2, **kw)
+    for r in (a, b):
+        assert r["err_bits"] == 0
+    return case, a, b
+
+
+def _pairs_in(r):
+    hdr = r["layer"].saved_field(r["saved"], 0, torch.int32, (16,)).cpu().numpy()
+    return int(hdr[1]), int(hdr[4])
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_pairs_equal_row_blocks_bitwise(name):
+    w = CASES[name]()
+    case, a, b = _both(w)
+    nblk, npair = _pairs_in(b)
+    assert npair < nblk      # some experts do have two or more blocks
+    for f in FIELDS:
+        np.testing.assert_array_equal(a[f], b[f], err_msg=f)
+    o = run_oracle(case)
+    tol = TOL[w.precision]
+    assert rel_err(b["out"], o["out"]) <= tol
+    assert rel_err(b["dx"], o["dx"]) <= tol
+    if w.precision == "bf16":
+        assert rel_err(b["dW13"], o["dW13"]) <= tol and rel_err(b["dW2"], o["dW2"]) <= tol
+    else:
+        check_mx_wgrad(b["dW13"], b["dW2"], o["state"], o["grads"])
+
+
+def test_pairs_mn_major_input_gradient():
+    """MXFP8 weights without transposed codes: the W13 input-gradient GEMM
+    over pairs reads the forward codes MN-major; same bits as row blocks."""
+    w = CASES["mx_full"]()
+    case, a, b = _both(w, mn_major=True)
+    for f in FIELDS:
+        np.testing.assert_array_equal(a[f], b[f], err_msg=f)
+
+
+def test_pairs_inference_and_clamped_swiglu():
+    """Inference (no saved state: h1 and column bundles not written) and the
+    clamped SwiGLU with its clip counts, pairs against row blocks."""
+    w = CASES["mx_ragged"]()
+    case = Case(w)
+    res = []
+    for mode in (1, 2):
+        r = run_gpu(case, training=False, swiglu_limit=0.75, tile_mode=mode)
+        assert r["err_bits"] == 0
+        res.append((r["out"], r["layer"].clip_stats()))
+    np.testing.assert_array_equal(res[0][0], res[1][0])
+    assert list(res[0][1]) == list(res[1][1]) and res[0][1][0] > 0

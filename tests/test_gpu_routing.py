@@ -83,6 +83,17 @@ def test_routing_bit_exact(name):
         pc = int(rt.poffsets[e + 1] - rt.poffsets[e])
         for b in range((pc + 127) // 128):
             exp.append([e, int(rt.poffsets[e]) + 128 * b, min(128, pc - 128 * b), 0])
+    # pairs of consecutive blocks of one expert (the last alone when odd), in
+    # word 3 of the first entries
+    pairs = []
+    b0 = 0
+    for e in range(E):
+        nbe = (int(rt.poffsets[e + 1] - rt.poffsets[e]) + 127) // 128
+        pairs += [((b0 + j) << 1) | int(j + 1 < nbe) for j in range(0, nbe, 2)]
+        b0 += nbe
+    assert hdr[4] == len(pairs)
+    for i, d in enumerate(pairs):
+        exp[i][3] = d
     np.testing.assert_array_equal(blocks, np.array(exp, dtype=np.int32).reshape(-1, 4))
     # first block of each expert, and the block of every 32-row group
     nb = np.array([(int(rt.poffsets[e + 1] - rt.poffsets[e]) + 127) // 128 for e in range(E)])
