@@ -857,7 +857,9 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g1.mx = mx;
   g1.na = 1;   // the SwiGLU-backward epilogue needs two accumulator buffers
   g1.epi = kEpiSwigluBwd;
-  g1.mode = kGroupedM;
+  // over row-block pairs in BF16 only: a 256-wide MXFP8 accumulator is
+  // single-buffered, and this epilogue reads it to the end of its work
+  g1.mode = (use_pairs(ctx) && !mx) ? kGroupedMP : kGroupedM;
   // MXFP8 weights prepared without transposed codes: A is W2's forward codes
   // [E*D rows (K), F columns (M)], read MN-major
   const bool mn2 = mx && W2->data_t == nullptr;

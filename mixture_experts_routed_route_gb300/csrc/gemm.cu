@@ -596,6 +596,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   MOE_GEMM_CASE(false, 1, kEpiSwigluFwd, kGroupedMP)
   MOE_GEMM_CASE(true, 1, kEpiSwigluFwd, kGroupedMP)
   MOE_GEMM_CASE(false, 1, kEpiStore, kGroupedMP)
+  MOE_GEMM_CASE(false, 1, kEpiSwigluBwd, kGroupedMP)
   MOE_GEMM_CASE(true, 1, kEpiStore, kGroupedMP)
   if (g.epi == kEpiWgrad && g.mode == kGroupedK &&
       (g.p.tma_store == kDwStoreF32 || g.p.tma_store == kDwAddF32))

@@ -488,14 +488,16 @@ __device__ __forceinline__ void epi_swiglu_bwd(const GemmParams& p, const Tile& 
       dg[i] = dh2 * u * (s * (1.0f + g * (1.0f - s))) * mg;
       du[i] = dh2 * (g * s) * mu;
     }
+    // over a row-block pair, rows 128.. of the tile are the second block's
+    const int blk = t.blk + (c0 >> 7), prow = c0 & 127;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const long long row = t.out_row0 + c0 + i;
-      store_row_val<MX>(p, p.out0, p.out0_pitch, row, f, dg[i], lane, t.blk, c0 + i);
-      store_row_val<MX>(p, p.out0, p.out0_pitch, row, p.F + f, du[i], lane, t.blk, c0 + i);
+      store_row_val<MX>(p, p.out0, p.out0_pitch, row, f, dg[i], lane, blk, prow + i);
+      store_row_val<MX>(p, p.out0, p.out0_pitch, row, p.F + f, du[i], lane, blk, prow + i);
     }
-    store_col32<MX>(p, f, t.out_row0 + c0, t.blk, c0 >> 5, dg);
-    store_col32<MX>(p, p.F + f, t.out_row0 + c0, t.blk, c0 >> 5, du);
+    store_col32<MX>(p, f, t.out_row0 + c0, blk, prow >> 5, dg);
+    store_col32<MX>(p, p.F + f, t.out_row0 + c0, blk, prow >> 5, du);
   }
 }
 
