@@ -63,7 +63,8 @@ MOE_API moe_status moe_ctx_test_fused_stall(moe_ctx* ctx, int stall, int64_t wai
  * W2, W13 input gradient): mode 1 takes one routing row block (<= 128 rows)
  * as the B operand; mode 2 takes row-block pairs (two consecutive blocks of
  * one expert, <= 256 rows, the pairs of MOE_SAVED_BLOCKS word 3); mode 0
- * (the default) takes pairs when max_tokens * top_k >= 128 * num_experts.
+ * (the default) takes pairs in BF16 when max_tokens * top_k >= 128 *
+ * num_experts.
  * Both give the same results bit for bit, and a forward and its backward
  * may run in different modes (both read the same saved state).  Applies to
  * later calls; no device access. */
