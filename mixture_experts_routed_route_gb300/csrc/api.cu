@@ -29,8 +29,8 @@ struct moe_ctx {
   int max_ctas = 0;   // moe_ctx_set_max_ctas (0: num_sms)
   int fused_stall = 0;             // moe_ctx_test_fused_stall
   // grouped-M GEMM tiles over row-block pairs (B up to 256 rows): chosen at
-  // creation when the capacity gives the experts 128 routes each on average
-  // (max_tokens * top_k >= 128 E); moe_ctx_test_tile_mode overrides it
+  // creation for BF16 when the capacity gives the experts 128 routes each on
+  // average (max_tokens * top_k >= 128 E); moe_ctx_test_tile_mode overrides it
   bool pair_tiles_auto = false;
   int tile_mode = 0;               // 0: pair_tiles_auto, 1: row blocks, 2: pairs
   long long fused_wait = 0;        // counter-wait limit of the single-launch forward (0: default)
@@ -547,7 +547,10 @@ moe_status moe_ctx_create(const moe_config* cfg, moe_ctx** out) {
   }
   c->r_cap = row_cap(cfg);
   c->b_cap = block_cap(cfg);
-  c->pair_tiles_auto = static_cast<int64_t>(cfg->max_tokens) * cfg->top_k >= 128LL * cfg->num_experts;
+  // BF16 only: MXFP8 pair tiles, single-buffered and bound by their operand
+  // loads, measured no faster than two row-block tiles
+  c->pair_tiles_auto = cfg->precision == MOE_BF16 &&
+                       static_cast<int64_t>(cfg->max_tokens) * cfg->top_k >= 128LL * cfg->num_experts;
   const ScratchLayout L = scratch_layout(cfg);
   c->bytes = L.total;
   if (cudaMalloc(&c->base, c->bytes) != cudaSuccess) {
