@@ -355,7 +355,7 @@ bool fill_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uint8_t*
 moe_status run_gather_w13(moe_ctx* ctx, const void* x, const RoutingPtrs& rp, const moe_weight* W13, uint8_t* act,
                           const SavedLayout& SL, bool marks, int sms, cudaStream_t stream) {
   const moe_config& c = ctx->cfg;
-  const int D = c.d_model, F = c.d_ff, E = c.num_experts, K = c.top_k;
+  const int D = c.d_model, K = c.top_k;
   const bool mx = c.precision == MOE_MXFP8;
   const int64_t R = ctx->r_cap;
   if (act) {
@@ -386,11 +386,6 @@ moe_status run_gather_w13(moe_ctx* ctx, const void* x, const RoutingPtrs& rp, co
 // The W2 GEMM: h3 = h2 W2[e]^T from the h2 row bundle in scratch.
 moe_status run_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uint8_t* h3, int sms,
                   cudaStream_t stream) {
-  const moe_config& c = ctx->cfg;
-  const int D = c.d_model, F = c.d_ff, E = c.num_experts;
-  const bool mx = c.precision == MOE_MXFP8;
-  const int64_t R = ctx->r_cap;
-  // ---- W2
   GemmLaunch g2{};
   if (!fill_w2(ctx, rp, W2, h3, &g2, use_pairs(ctx))) return MOE_ERR_CUDA;
   MOE_TRY(launch_gemm(g2, sms, stream));
