@@ -32,7 +32,11 @@ struct moe_ctx {
   // creation for BF16 when the capacity gives the experts 128 routes each on
   // average (max_tokens * top_k >= 128 E); moe_ctx_test_tile_mode overrides it
   bool pair_tiles_auto = false;
-  int tile_mode = 0;               // 0: pair_tiles_auto, 1: row blocks, 2: pairs
+  // MXFP8: the forward's GEMMs over row-block pairs on CTA pairs, chosen at
+  // creation when experts hold two or more full row blocks on average
+  // (max_tokens * top_k >= 256 E); moe_ctx_test_tile_mode overrides it
+  bool cta_pairs_auto = false;
+  int tile_mode = 0;               // 0: automatic, 1: row blocks, 2: pairs, 3: pairs on CTA pairs
   long long fused_wait = 0;        // counter-wait limit of the single-launch forward (0: default)
   const void* norm_gamma = nullptr;   // moe_ctx_set_post_norm (MOE_POST_NORM)
   float norm_eps = 0.0f;
@@ -73,7 +77,21 @@ bool config_ok(const moe_config* c) {
 
 bool config_tileable(const moe_config* c) { return c->d_model % 128 == 0 && c->d_ff % 128 == 0; }
 
-bool use_pairs(const moe_ctx* c) { return c->tile_mode == 2 || (c->tile_mode == 0 && c->pair_tiles_auto); }
+bool use_pairs(const moe_ctx* c) { return c->tile_mode >= 2 || (c->tile_mode == 0 && c->pair_tiles_auto); }
+
+// Tiles of the forward's grouped-M GEMMs (W13 + SwiGLU, W2): row blocks, row-
+// block pairs, or (MXFP8) row-block pairs on CTA pairs.
+GemmMode forward_tiles(const moe_ctx* c) {
+  const bool mx = c->cfg.precision == MOE_MXFP8;
+  switch (c->tile_mode) {
+    case 1: return kGroupedM;
+    case 2: return kGroupedMP;
+    case 3: return mx ? kGroupedMC : kGroupedMP;
+    default:
+      if (mx) return c->cta_pairs_auto ? kGroupedMC : kGroupedM;
+      return c->pair_tiles_auto ? kGroupedMP : kGroupedM;
+  }
+}
 
 int64_t row_cap(const moe_config* c) {
   const int64_t r = static_cast<int64_t>(c->max_tokens) * c->top_k + 31LL * c->num_experts;
@@ -261,15 +279,16 @@ cudaError_t stage_mark(moe_ctx* c, int pass, int idx, cudaStream_t s) {
 // also h1 and the h2 column bundle into act's fields.  False if a tensor map
 // cannot be encoded.
 bool fill_w13(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W13, uint8_t* act, const SavedLayout& SL,
-              bool marks, GemmLaunch* g1, bool pairs) {
+              bool marks, GemmLaunch* g1, GemmMode mode) {
   const moe_config& c = ctx->cfg;
   const int D = c.d_model, F = c.d_ff, E = c.num_experts;
   const bool mx = c.precision == MOE_MXFP8;
   const int64_t R = ctx->r_cap;
+  if (mode == kGroupedMC && D % 256 != 0) mode = kGroupedMP;   // a CTA pair's stage is 256 of K
   g1->mx = mx;
-  g1->na = pairs ? 1 : 2;
+  g1->na = mode == kGroupedM ? 2 : 1;
   g1->epi = kEpiSwigluFwd;
-  g1->mode = pairs ? kGroupedMP : kGroupedM;
+  g1->mode = mode;
   if (!make_tmap(&g1->tmA, W13->data, mx, static_cast<int64_t>(E) * 2 * F, D, 128) ||
       !make_tmap(&g1->tmB, B(ctx, MOE_BUF_XROW), mx, R, D, 32) ||
       !make_grouped_m_boxes(g1, W13->data, static_cast<int64_t>(E) * 2 * F, W13->scale, B(ctx, MOE_BUF_XROW), R,
@@ -281,7 +300,7 @@ bool fill_w13(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W13, uint8_
   p1.poffsets = rp.poffsets;
   p1.E = E;
   p1.b_box_rows = 32;
-  p1.n_tiles = F / (pairs ? 64 : 128);
+  p1.n_tiles = F / (mode == kGroupedMP ? 64 : 128);   // (CTA pairs: 2 x 64 features)
   p1.K = D;
   p1.a_rows_per_expert = 2 * F;
   p1.a_up_offset = F;
@@ -312,15 +331,18 @@ bool fill_w13(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W13, uint8_
 }
 
 // The W2 GEMM into *g2: h3 = h2 W2[e]^T from the h2 row bundle in scratch.
-bool fill_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uint8_t* h3, GemmLaunch* g2, bool pairs) {
+bool fill_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uint8_t* h3, GemmLaunch* g2,
+             GemmMode mode) {
   const moe_config& c = ctx->cfg;
   const int D = c.d_model, F = c.d_ff, E = c.num_experts;
   const bool mx = c.precision == MOE_MXFP8;
   const int64_t R = ctx->r_cap;
+  // a CTA pair's tile is 256 features, its stage 256 of K
+  if (mode == kGroupedMC && (D % 256 != 0 || F % 256 != 0)) mode = kGroupedMP;
   g2->mx = mx;
-  g2->na = pairs ? 1 : pair_tiles(D);
+  g2->na = mode == kGroupedM ? pair_tiles(D) : 1;
   g2->epi = kEpiStore;
-  g2->mode = pairs ? kGroupedMP : kGroupedM;
+  g2->mode = mode;
   if (!make_tmap(&g2->tmA, W2->data, mx, static_cast<int64_t>(E) * D, F, 128) ||
       !make_tmap(&g2->tmB, B(ctx, MOE_BUF_H2ROW), mx, R, F, 32) ||
       !make_grouped_m_boxes(g2, W2->data, static_cast<int64_t>(E) * D, W2->scale, B(ctx, MOE_BUF_H2ROW), R, mx, F))
@@ -331,7 +353,7 @@ bool fill_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uint8_t*
   p2.poffsets = rp.poffsets;
   p2.E = E;
   p2.b_box_rows = 32;
-  p2.n_tiles = D / (128 * g2->na);
+  p2.n_tiles = D / (mode == kGroupedMC ? 256 : 128 * g2->na);   // (CTA pairs: 2 x 128 features)
   p2.K = F;
   p2.a_rows_per_expert = D;
   p2.sfa = W2->scale;
@@ -376,7 +398,7 @@ moe_status run_gather_w13(moe_ctx* ctx, const void* x, const RoutingPtrs& rp, co
 
   // ---- W13 + SwiGLU
   GemmLaunch g1{};
-  if (!fill_w13(ctx, rp, W13, act, SL, marks, &g1, use_pairs(ctx))) return MOE_ERR_CUDA;
+  if (!fill_w13(ctx, rp, W13, act, SL, marks, &g1, forward_tiles(ctx))) return MOE_ERR_CUDA;
   MOE_TRY(launch_gemm(g1, sms, stream));
   ctx->launches += 1;
   if (marks) MOE_TRY(stage_mark(ctx, 0, 3, stream));
@@ -387,7 +409,7 @@ moe_status run_gather_w13(moe_ctx* ctx, const void* x, const RoutingPtrs& rp, co
 moe_status run_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uint8_t* h3, int sms,
                   cudaStream_t stream) {
   GemmLaunch g2{};
-  if (!fill_w2(ctx, rp, W2, h3, &g2, use_pairs(ctx))) return MOE_ERR_CUDA;
+  if (!fill_w2(ctx, rp, W2, h3, &g2, forward_tiles(ctx))) return MOE_ERR_CUDA;
   MOE_TRY(launch_gemm(g2, sms, stream));
   ctx->launches += 1;
   return MOE_OK;
@@ -401,8 +423,8 @@ moe_status run_fused_forward(moe_ctx* ctx, int T, const void* x, const int32_t* 
   const moe_config& c = ctx->cfg;
   const SavedLayout SL = saved_layout(&c);
   GemmLaunch g1{}, g2{};
-  if (!fill_w13(ctx, rp, W13, nullptr, SL, true, &g1, false) ||
-      !fill_w2(ctx, rp, W2, B(ctx, MOE_BUF_H3), &g2, false))
+  if (!fill_w13(ctx, rp, W13, nullptr, SL, true, &g1, kGroupedM) ||
+      !fill_w2(ctx, rp, W2, B(ctx, MOE_BUF_H3), &g2, kGroupedM))
     return MOE_ERR_CUDA;
   if (g1.p.a_pair_box != 2 || g2.p.a_pair_box != 1 || !g1.p.b_full_box || !g2.p.b_full_box)
     return MOE_ERR_UNSUPPORTED;
@@ -546,6 +568,10 @@ moe_status moe_ctx_create(const moe_config* cfg, moe_ctx** out) {
   // loads, measured no faster than two row-block tiles
   c->pair_tiles_auto = cfg->precision == MOE_BF16 &&
                        static_cast<int64_t>(cfg->max_tokens) * cfg->top_k >= 128LL * cfg->num_experts;
+  // MXFP8 dense enough for full pairs: CTA pairs (one 256 x 256 MMA over two
+  // SMs, each loading half the operands, in 68 KB two-K-chunk stages)
+  c->cta_pairs_auto = cfg->precision == MOE_MXFP8 &&
+                      static_cast<int64_t>(cfg->max_tokens) * cfg->top_k >= 256LL * cfg->num_experts;
   const ScratchLayout L = scratch_layout(cfg);
   c->bytes = L.total;
   if (cudaMalloc(&c->base, c->bytes) != cudaSuccess) {
@@ -624,7 +650,7 @@ moe_status moe_ctx_test_fused_stall(moe_ctx* ctx, int stall, int64_t wait_cycles
 }
 
 moe_status moe_ctx_test_tile_mode(moe_ctx* ctx, int mode) {
-  if (!ctx || mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
+  if (!ctx || mode < 0 || mode > 3) return MOE_ERR_INVALID_ARG;
   ctx->tile_mode = mode;
   return MOE_OK;
 }

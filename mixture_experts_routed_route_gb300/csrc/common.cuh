@@ -53,15 +53,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same for a phase that arrivals from the other CTA of a cluster (or its
+// tensor-core commits) complete: the thread is suspended for at most
+// kClusterWaitNs per try.
+constexpr uint32_t kClusterWaitNs = 64;
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kClusterWaitNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete.  Returns
 // false (and leaves the CTA-wide abort flag set) if the wait ran out of time
-// or another role of the CTA already gave up.
+// or another role of the CTA already gave up.  CLUSTER: the phase is
+// completed from the other CTA of a pair (short suspends per try).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto probe = [&] { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (probe()) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (probe()) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitTimeoutCycles) {
       *abort_flag = 1;
@@ -251,6 +270,83 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                : "memory");
 }
 
+// ------------------------------------------------ CTA pairs (cta_group::2)
+// A cluster of two CTAs on two SMs shares one tensor-core instruction of
+// M = 256: each CTA holds 128 rows of A and half of B's rows in its own
+// shared memory, and 128 accumulator lanes in its own TMEM.  Every tcgen05
+// instruction of such a kernel names cta_group::2 (alloc and dealloc by one
+// warp of each CTA together; MMA, scale copies and commits by one thread of
+// the lower-ranked CTA, on both CTAs' memories at the same addresses).
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs: release and acquire at cluster scope.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of `p`'s counterpart in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier in another CTA of the cluster.  Release at CTA scope
+// only: what such an arrival reports (a stage landed in this CTA's shared
+// memory, this CTA's accumulator lanes drained) is then read by this SM's
+// own tensor core, never across SMs.  (A cluster-scope release stalls the
+// arriving thread about 600 ns on this part.)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_alloc_cg(uint32_t* smem_dst, uint32_t ncols) {
+  if constexpr (CG == 2)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_dst)),
+                 "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_relinquish_cg() {
+  if constexpr (CG == 2) asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc_cg(uint32_t taddr, uint32_t ncols) {
+  if constexpr (CG == 2)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// tc_commit for a CTA-pair kernel: one barrier (here or in the other CTA).
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// ... and the barrier at the same offset in each CTA of `cta_mask`.
+__device__ __forceinline__ void tc_commit_pair_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
 // 128-byte swizzle that TMA's SWIZZLE_128B writes: rows of 128 bytes, groups
 // of 8 rows 1024 bytes apart.  Fields: start address >> 4 (bits 0-13),
@@ -315,6 +411,11 @@ __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// The same in a CTA-pair kernel: each CTA's atom at `sdesc` into its own TMEM.
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = BF16
 // (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at
 // bits 24-28 (M = 128).
@@ -326,8 +427,8 @@ __device__ __forceinline__ uint32_t idesc_bf16(uint32_t n) {
 // (format 0), both K-major, scale type UE8M0 (bit 23), N >> 3 at 17-22,
 // M >> 4 at 24-28, scale-factor byte selectors for B (bits 4-5) and A
 // (bits 29-30).
-__device__ __forceinline__ uint32_t idesc_mxf8(uint32_t n, uint32_t sfa_id, uint32_t sfb_id) {
-  return (sfb_id << 4) | ((n >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) | (sfa_id << 29);
+__device__ __forceinline__ uint32_t idesc_mxf8(uint32_t n, uint32_t sfa_id, uint32_t sfb_id, uint32_t m = 128) {
+  return (sfb_id << 4) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24) | (sfa_id << 29);
 }
 
 // Bit 15 of the instruction descriptor: A is MN-major (transposed) rather
@@ -350,6 +451,20 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.u32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+          "r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// A CTA pair's block-scaled MMA (M = 256 over both CTAs, issued by the
+// lower-ranked one): D (each CTA's 128 lanes) += A (each CTA's 128 rows) x B
+// (N rows, the first N/2 in this CTA's shared memory, the rest in the other's).
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
           "r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");

@@ -26,6 +26,17 @@
 //    scale columns need the rest of TMEM); the SwiGLU forward's A tile is 64
 //    gate rows followed by the 64 up rows of the same features, and its
 //    epilogue pairs them up through shared memory.
+//  * the same pair tiles on CTA pairs (kGroupedMC, MXFP8): a cluster of two
+//    CTAs on two SMs takes two adjacent A tiles (SwiGLU: features f..f+63
+//    and f+64..f+127) against one row-block pair, each CTA loading its own
+//    A tile and one block of the pair.  The lower-ranked CTA issues one
+//    tcgen05.mma.cta_group::2 of M = 256, N = 256 per K step over both; each
+//    CTA's 128 accumulator lanes hold its A tile's rows against all 256
+//    columns, and each CTA drains its own.  Per SM a stage then carries 32 KB
+//    of operands instead of 48 for the same tensor-core work.  Rank 1 reports
+//    each stage's operands in place (and each accumulator drained) to rank 0
+//    through mbarriers in rank 0's shared memory; rank 0's commits release
+//    the stages and hand over the accumulators in both CTAs (multicast).
 //  * grouped-K (WGRAD): dW_e[m, n] = sum over the expert's rows of
 //    colA[m, r] colB[n, r]; both operands are column bundles stored
 //    [features, rows], so the contraction runs over the expert's row range.
@@ -35,7 +46,11 @@
 // (the one-A-tile grouped-M GEMMs: four stages' atoms per copy, into a ring
 // of their own), a scale warp moves them to tensor memory with tcgen05.cp
 // and commits them to the stage's sf_full barrier, and the MMA thread,
-// which waits on that barrier, issues the block-scaled MMAs.
+// which waits on that barrier, issues the block-scaled MMAs.  On CTA pairs
+// the MMA thread issues the copies itself, just before the stage's MMAs (a
+// copy and the MMAs after it from one thread run in issue order with no
+// wait between them, and next to 256-wide MMAs the copies cost no tensor
+// time), so the stage's chain has one hop less.
 //
 // Epilogues: fused SwiGLU forward (h1 -> h2 row/column bundles), plain BF16
 // store (h3, input-gradient rows), fused SwiGLU backward (dh2 -> dh1 row and
@@ -45,13 +60,16 @@
 // Warp roles (one CTA per SM, persistent over tiles; warps 0, 1 and the
 // scale warp run their loops converged and lane 0 issues):
 //   warp 0      TMA producer
-//   warp 1      TMEM allocator and MMA issuer
+//   warp 1      TMEM allocator and MMA issuer (CTA pairs, rank 1: tells
+//               rank 0 when its epilogue has drained the accumulator)
 //   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and the
 //               32-column chunks 32h and 32h + 64 (h = (w-2)/4) of the
 //               accumulator
 //   warps 10..17  weight gradient only: a second epilogue group of 8 warps;
 //               the two groups take alternate tiles
-//   last warp   MXFP8 only: scale-atom copier (tcgen05.cp)
+//   last warp   MXFP8 only: over row-block pairs, builds the SwiGLU
+//               forward's weight atom of each stage; CTA pairs: tells rank
+//               0's MMA thread when a stage's operands are in place
 #include "gemm_core.cuh"
 
 namespace moe {
@@ -71,6 +89,8 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   using C = Cfg<MX, NA, MODE>;
   constexpr int S = C::S;
   constexpr bool PAIR = C::PAIR;
+  constexpr bool CG2 = C::CG2;
+  constexpr int CG = CG2 ? 2 : 1;
   constexpr int kStep = PAIR ? (EPI == kEpiSwigluFwd ? 64 : 128) : ((NA == 2 && EPI != kEpiSwigluFwd) ? 256 : 128);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -86,12 +106,19 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
   uint64_t* sf_drain = sf_full + S;
   uint64_t* sfg_full = sf_drain + 1;        // [SFR]: a scale-atom group has landed
   uint64_t* sfg_empty = sfg_full + C::SFR;  // [SFR]: its atoms are in TMEM
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfg_empty + C::SFR);
+  uint64_t* ready = sfg_empty + C::SFR;     // CTA pairs [S]: both CTAs' operands of a stage are in place
+  uint64_t* ptempty = ready + (CG2 ? S : 0);   // CTA pairs [ACC_BUFS]: the other CTA drained its accumulator
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ptempty + (CG2 ? C::ACC_BUFS : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_abort = abort_flag + 1;  // [EPI_GROUPS]: a group's warps leave together
-  uint8_t* cache = xbuf + C::EXCH + 256;
+  uint8_t* cache = xbuf + C::EXCH + C::BARS;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA pairs: both CTAs of a cluster walk the same tiles (cluster index cid
+  // of ncl), rank 0 issuing the MMAs for both
+  const uint32_t rank = CG2 ? cluster_ctarank() : 0u;
+  const int cid = CG2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ncl = CG2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -107,6 +134,10 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     for (int g = 0; g < C::SFR; ++g) {
       mbar_init(&sfg_full[g], 1);
       mbar_init(&sfg_empty[g], 1);
+    }
+    if (CG2) {
+      for (int s = 0; s < S; ++s) mbar_init(&ready[s], 2);
+      for (int a = 0; a < C::ACC_BUFS; ++a) mbar_init(&ptempty[a], 1);
     }
     *abort_flag = 0;
     for (int g = 0; g < C::EPI_GROUPS; ++g) epi_abort[g] = 0;
@@ -128,17 +159,20 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+    // CTA pairs: one warp of each CTA together, the same columns in both
+    tmem_alloc_cg<CG>(tmem_slot, 512);
+    tmem_relinquish_cg<CG>();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the other CTA's barriers are initialised before anything arrives on them
+  if (CG2) cluster_sync();
 
   const int nblk = (MODE != kGroupedK) ? p.hdr[1] : 0;
   const int num_tiles = (MODE == kGroupedM)    ? nblk * p.n_tiles
-                        : (MODE == kGroupedMP) ? p.hdr[4] * p.n_tiles
+                        : (MODE == kGroupedMP || MODE == kGroupedMC) ? p.hdr[4] * p.n_tiles
                                                : p.E * p.m_tiles * p.n_tiles;
   MetaCache mc;
   mc.blocks = reinterpret_cast<const int4*>(cache);
@@ -156,6 +190,11 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     }
   }
   __syncthreads();
+  // A tile of the walk; CTA pairs: this CTA's half (A tile 2n + rank)
+  auto tile_at = [&](TileWalk<MODE> w) {
+    if (CG2) w.n = 2 * w.n + static_cast<int>(rank);
+    return decode_tile<MODE, C::BK, kStep>(p, w, mc);
+  };
 
   // The producer and MMA warps walk their loops with all 32 lanes, so the
   // loop state and the descriptors stay warp-uniform; lane 0 alone issues
@@ -166,9 +205,9 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     uint32_t it = 0, gc = 0;   // gc: scale-atom groups issued (SFG)
     bool ok = true;
     TileWalk<MODE> w;
-    w.start(p, blockIdx.x);
+    w.start(p, cid);
     for (; ok && w.tile < num_tiles; w.advance(p)) {
-      const Tile t = decode_tile<MODE, C::BK, kStep>(p, w, mc);
+      const Tile t = tile_at(w);
       for (int ks = 0; ks < t.kstages; ++ks, ++it) {
         const uint32_t slot = it % S, ph = (it / S) & 1;
         if (C::SFG && ks % C::GS == 0) {
@@ -188,17 +227,34 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
           }
           ++gc;
         }
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[slot], ph ^ 1, abort_flag, p.err))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait<CG2>(&empty[slot], ph ^ 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
         if (lane == 0) {
           uint8_t* sa = smem + slot * C::STAGE;
-          uint8_t* sb = sa + NA * kABytes;
+          uint8_t* sb = sa + C::A_BYTES;
           uint8_t* ssf = sa + C::SF_OFF;
           const int rb = stage_row_bytes<MODE, C::BK, MX ? 1 : 2>(t, ks);
           const int kx = t.k0 + ks * C::BK;
-          if (PAIR) {
+          if (CG2) {
+            // two K-chunks (kc, kc + 1): the A tile (SwiGLU: gate and up
+            // halves) and this CTA's block of the pair in one box each (none
+            // for rank 1 of a lone block), the weight's atoms of both chunks
+            // (SwiGLU: of both halves) at ssf, then each block's two atoms
+            const bool two = t.b_rows > 128;
+            const bool mine = rank == 0 || two;
+            const int kc = kx >> 7;
+            mbar_arrive_expect_tx(&full[slot], C::A_BYTES + (mine ? C::B_BYTES : 0) +
+                                                   ((EPI == kEpiSwigluFwd ? 4 : 2) + (two ? 4 : 2)) * kAtom);
+            if (EPI == kEpiSwigluFwd) tma_load_4d(sa, &aux0, &full[slot], 0, t.out_col0, 2 * t.e, kc);
+            else tma_load_3d(sa, &aux0, &full[slot], 0, t.a_row[0], kc);
+            if (mine) tma_load_3d(sb, &aux1, &full[slot], 0, t.b_row0 + 128 * static_cast<int>(rank), kc);
+            if (EPI == kEpiSwigluFwd) tma_load_4d(ssf, &aux2, &full[slot], 0, kc, t.out_col0 >> 7, 2 * t.e);
+            else bulk_load(ssf, p.sfa + (t.sfa_atom[0] + kc) * kAtom, 2 * kAtom, &full[slot]);
+            bulk_load(ssf + 4 * kAtom, p.sfb + (t.sfb_atom + kc) * kAtom, 2 * kAtom, &full[slot]);
+            if (two) bulk_load(ssf + 6 * kAtom, p.sfb + (t.sfb_atom + p.sfb_ts + kc) * kAtom, 2 * kAtom, &full[slot]);
+          } else if (PAIR) {
             // one A tile (SwiGLU: its gate and up halves in one 3D box), B as
             // full 128-row boxes then 32-row boxes; MXFP8: the weight's atom
             // (two for the halves) and one atom per routing block of the pair
@@ -283,31 +339,52 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (CG2 && warp == 1 && rank != 0) {
+    // ------------------------------------ CTA pairs, rank 1: accumulator relay
+    // Rank 0's MMA thread reuses the accumulator once this CTA's epilogue
+    // has drained its lanes as well.
+    const uint32_t peer_ptempty = cluster_addr(ptempty, 0);
+    uint32_t tc = 0;
+    TileWalk<MODE> w;
+    w.start(p, cid);
+    for (; w.tile < num_tiles; w.advance(p), ++tc) {
+      const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait<true>(&tempty[acc], aph, abort_flag, p.err))) break;
+      if (lane == 0) mbar_arrive_cluster(peer_ptempty + 8 * acc);
+      __syncwarp();
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     uint32_t it = 0, tc = 0;
     bool ok = true;
     TileWalk<MODE> w;
-    w.start(p, blockIdx.x);
+    w.start(p, cid);
     for (; ok && w.tile < num_tiles; w.advance(p), ++tc) {
-      const Tile t = decode_tile<MODE, C::BK, kStep>(p, w, mc);
+      const Tile t = tile_at(w);
       const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty[acc], aph ^ 1, abort_flag, p.err))) break;
+      if (CG2 && !__all_sync(0xFFFFFFFFu, mbar_wait<true>(&ptempty[acc], aph ^ 1, abort_flag, p.err))) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem + acc * C::ACC_COLS;
-      const uint32_t idesc = MX ? (idesc_mxf8(t.b_rows, 0, 0) | (MODE != kGroupedK && p.a_mn ? kIdescAMnMajor : 0u))
+      // CTA pairs: M = 256 over both CTAs and N = 256 (a lone block's other
+      // half is whatever the other CTA's stage holds; its columns are never read)
+      const uint32_t idesc = MX ? (idesc_mxf8(CG2 ? 256 : t.b_rows, 0, 0, CG2 ? 256 : 128) |
+                                   (MODE != kGroupedK && p.a_mn ? kIdescAMnMajor : 0u))
                                 : idesc_bf16(t.b_rows);
       for (int ks = 0; ks < t.kstages; ++ks, ++it) {
         const uint32_t slot = it % S, ph = (it / S) & 1;
         // MXFP8: the scale warp's commit for this stage follows its own wait
-        // for the stage's data, so it covers both
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(MX ? &sf_full[slot] : &full[slot], ph, abort_flag, p.err))) {
+        // for the stage's data, so it covers both.  CTA pairs: both CTAs'
+        // scale warps report the stage in place (weight atom built), and this
+        // thread copies the atoms itself, just before the stage's MMAs.
+        uint64_t* in_place = CG2 ? &ready[slot] : (MX ? &sf_full[slot] : &full[slot]);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait<CG2>(in_place, ph, abort_flag, p.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + slot * C::STAGE);
-        const uint32_t sb = sa + NA * kABytes;
+        const uint32_t sb = sa + C::A_BYTES;
         const uint32_t sfcol = tmem + C::SF_COL0 + slot * C::SF_COLS;
         const int rb = stage_row_bytes<MODE, C::BK, MX ? 1 : 2>(t, ks);
         const uint64_t bdesc0 = sdesc_k_sw(sb, rb);
@@ -318,7 +395,28 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
         for (int j = 0; j < NA; ++j) adesc0[j] = amn ? sdesc_mn_sw128(sa + j * kABytes) : sdesc_k_sw(sa + j * kABytes, rb);
         const uint64_t astep = amn ? (4096 >> 4) : 2;
         const int nmma = (ks == t.kstages - 1) ? t.klast / C::KMMA : C::MMAS;
-        if (lane == 0) {
+        if (lane == 0 && CG2) {
+          // per K-chunk c: the weight's atom, then the pair's B atoms (every
+          // SM's MMA reads the scales of all 256 columns) into columns
+          // 12c .. 12c + 11 of the stage, then the chunk's four MMAs
+          const uint32_t ssf = sa + C::SF_OFF;
+          const bool two = t.b_rows > 128;
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c) {
+            const uint32_t sfc = sfcol + 12 * c;
+            tc_cp_sf_pair(sfc, sdesc_sf_atom(ssf + c * kAtom));
+            tc_cp_sf_pair(sfc + 4, sdesc_sf_atom(ssf + (4 + c) * kAtom));
+            if (two) tc_cp_sf_pair(sfc + 8, sdesc_sf_atom(ssf + (6 + c) * kAtom));
+            const uint64_t ad = sdesc_k_sw(sa + c * kABytes, 128), bd = sdesc_k_sw(sb + c * kBBytes, 128);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_mxf8_pair(d_tmem, ad + 2 * k, bd + 2 * k,
+                            idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29), sfc, sfc + 4,
+                            (ks | c | k) ? 1u : 0u);
+          }
+          // the stage is free in both CTAs
+          tc_commit_pair_mc(&empty[slot], 3);
+        } else if (lane == 0) {
 #pragma unroll
           for (int k = 0; k < C::MMAS; ++k) {
             if (k < nmma) {
@@ -342,12 +440,16 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(&tfull[acc]);
+      if (lane == 0) {
+        if (CG2) tc_commit_pair_mc(&tfull[acc], 3);
+        else tc_commit(&tfull[acc]);
+      }
       __syncwarp();
     }
-    // every MMA issued here must be complete before TMEM is released
+    // every MMA (and scale copy) issued here must be complete before TMEM is released
     if (lane == 0) {
-      tc_commit(drain);
+      if (CG2) tc_commit_pair(drain);
+      else tc_commit(drain);
       drain_wait(drain, 0);
     }
     __syncwarp();
@@ -356,16 +458,18 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     // Each stage's scale atoms go from shared memory to the stage's TMEM
     // columns once its data has landed; the commit tells the MMA thread.
     // A slot's columns are rewritten only after the producer refilled the
-    // slot, i.e. after the MMAs that read them completed.
+    // slot, i.e. after the MMAs that read them completed.  CTA pairs: the
+    // MMA thread copies the atoms; this warp builds the SwiGLU weight atom
+    // and reports each stage in place to rank 0 (both CTAs).
     uint32_t it = 0, gc = 0, cur = 0;   // scale-atom groups (SFG): next, and the current one
     bool ok = true;
     TileWalk<MODE> w;
-    w.start(p, blockIdx.x);
+    w.start(p, cid);
     for (; ok && w.tile < num_tiles; w.advance(p)) {
-      const Tile t = decode_tile<MODE, C::BK, kStep>(p, w, mc);
+      const Tile t = tile_at(w);
       for (int ks = 0; ks < t.kstages; ++ks, ++it) {
         const uint32_t slot = it % S, ph = (it / S) & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], ph, abort_flag, p.err))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait<CG2>(&full[slot], ph, abort_flag, p.err))) {
           ok = false;
           break;
         }
@@ -383,14 +487,27 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
           // rows 64a..64a+63 (a = (f0/64) % 2) of the gate half's 128-row
           // atom, then the same rows of the up half's.  Lane r builds its
           // 16 bytes from 8 of each, over the gate atom's place.
-          uint8_t* at = smem + slot * C::STAGE + C::SF_OFF;
+          // (CTA pairs: for each of the stage's two K-chunks; the up half's
+          // atoms follow the gate half's)
           const int a8 = ((t.out_col0 >> 6) & 1) * 8;
-          const uint2 g = *reinterpret_cast<const uint2*>(at + lane * 16 + a8);
-          const uint2 u = *reinterpret_cast<const uint2*>(at + kAtom + lane * 16 + a8);
-          __syncwarp();
-          *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(g.x, g.y, u.x, u.y);
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c) {
+            uint8_t* at = smem + slot * C::STAGE + C::SF_OFF + c * kAtom;
+            const uint2 g = *reinterpret_cast<const uint2*>(at + lane * 16 + a8);
+            const uint2 u = *reinterpret_cast<const uint2*>(at + C::KCH * kAtom + lane * 16 + a8);
+            __syncwarp();
+            *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(g.x, g.y, u.x, u.y);
+          }
           fence_proxy_async_smem();
           __syncwarp();
+        }
+        if (CG2) {
+          if (lane == 0) {
+            if (rank == 0) mbar_arrive(&ready[slot]);
+            else mbar_arrive_cluster(cluster_addr(&ready[slot], 0));
+          }
+          __syncwarp();
+          continue;
         }
         tc_fence_after();
         if (lane == 0) {
@@ -402,7 +519,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
             // the group's last stage: its buffer may be refilled once these copies completed
             if (ks % C::GS == C::GS - 1 || ks == t.kstages - 1) tc_commit(&sfg_empty[cur % C::SFR]);
           } else if (PAIR) {
-            // the weight's atom (SwiGLU: built below), then the pair's B atoms
+            // the weight's atom (SwiGLU: built above), then the pair's B atoms
             const uint32_t ssf = smem_u32(smem + slot * C::STAGE) + C::SF_OFF;
             tc_cp_sf(sfcol, sdesc_sf_atom(ssf));
             tc_cp_sf(sfcol + 4, sdesc_sf_atom(ssf + 2 * kAtom));
@@ -418,7 +535,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       }
     }
     // every copy issued here must be complete before TMEM is released
-    if (lane == 0) {
+    if (lane == 0 && !CG2) {
       tc_commit(sf_drain);
       drain_wait(sf_drain, 0);
     }
@@ -435,15 +552,14 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
     uint32_t tc = grp;
     // (the epilogue has slack: it decodes each tile from its index, which
     // keeps the walk's registers out of its register-bound loop)
-    for (int tile = blockIdx.x + grp * gridDim.x; tile < num_tiles;
-         tile += C::EPI_GROUPS * gridDim.x, tc += C::EPI_GROUPS) {
+    for (int tile = cid + grp * ncl; tile < num_tiles; tile += C::EPI_GROUPS * ncl, tc += C::EPI_GROUPS) {
       TileWalk<MODE> w;
       w.start(p, tile);
-      const Tile t = decode_tile<MODE, C::BK, kStep>(p, w, mc);
+      const Tile t = tile_at(w);
       const uint32_t acc = tc % C::ACC_BUFS, aph = (tc / C::ACC_BUFS) & 1;
       uint32_t hp[32];
       if (EPI == kEpiSwigluBwd && 32 * h < t.b_rows) load_h1_chunk(p, t, t.out_col0 + lrow, 32 * h, hp);
-      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&tfull[acc], aph, abort_flag, p.err));
+      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait<CG2>(&tfull[acc], aph, abort_flag, p.err));
       constexpr bool pair_swiglu = PAIR && EPI == kEpiSwigluFwd;   // leaves through its own barrier
       if (!staged && !pair_swiglu && !ok) break;
       tc_fence_after();
@@ -550,10 +666,13 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // CTA pairs: neither CTA leaves (nor frees TMEM) while the other may still
+  // touch its shared memory, barriers or tensor memory
+  if (CG2) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_cg<CG>(tmem, 512);
   }
 }
 
@@ -562,17 +681,47 @@ cudaError_t launch_impl(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   using C = Cfg<MX, NA, MODE>;
   auto kern = gemm_kernel<MX, NA, EPI, MODE, DWF>;
   static PerDeviceOnce setup;
-  const cudaError_t se =
-      setup.once([&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM); });
+  static int pair_slots[kMaxDevices];   // CTA pairs: clusters of two that fit on the device at once
+  int dev = 0;
+  cudaError_t se = cudaGetDevice(&dev);
   if (se != cudaSuccess) return se;
-  const int grid = max(1, min(num_sms, g.max_tiles));
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute la[1];
+  la[0].id = cudaLaunchAttributeClusterDimension;
+  la[0].val.clusterDim.x = 2;
+  la[0].val.clusterDim.y = 1;
+  la[0].val.clusterDim.z = 1;
+  lc.blockDim = dim3(C::THREADS);
+  lc.dynamicSmemBytes = C::SMEM;
+  lc.stream = stream;
+  lc.attrs = la;
+  lc.numAttrs = 1;
+  se = setup.once([&] {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess || !C::CG2) return e;
+    int n = 0;
+    lc.gridDim = dim3(2);
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &lc);
+    if (e == cudaSuccess && n < 1) e = cudaErrorInvalidConfiguration;
+    pair_slots[dev] = n;
+    return e;
+  });
+  if (se != cudaSuccess) return se;
+  // CTA pairs: the walk is over clusters (both CTAs of one take the same tiles)
+  const int units = C::CG2 ? max(1, min(min(num_sms / 2, pair_slots[dev]), g.max_tiles))
+                           : max(1, min(num_sms, g.max_tiles));
   GemmParams p = g.p;
-  const int q = grid / p.n_tiles;
-  p.walk[0] = grid;
-  p.walk[1] = grid % p.n_tiles;
+  const int q = units / p.n_tiles;
+  p.walk[0] = units;
+  p.walk[1] = units % p.n_tiles;
   p.walk[2] = MODE != kGroupedK ? q : q % p.m_tiles;
   p.walk[3] = MODE != kGroupedK ? 0 : q / p.m_tiles;
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.tmC, g.aux[0], g.aux[1], g.aux[2], g.aux[3], p);
+  if (C::CG2) {
+    lc.gridDim = dim3(2 * units);
+    return cudaLaunchKernelEx(&lc, kern, g.tmA, g.tmB, g.tmC, g.aux[0], g.aux[1], g.aux[2], g.aux[3], p);
+  }
+  kern<<<units, C::THREADS, C::SMEM, stream>>>(g.tmA, g.tmB, g.tmC, g.aux[0], g.aux[1], g.aux[2], g.aux[3], p);
   return cudaGetLastError();
 }
 
@@ -598,6 +747,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   MOE_GEMM_CASE(false, 1, kEpiStore, kGroupedMP)
   MOE_GEMM_CASE(false, 1, kEpiSwigluBwd, kGroupedMP)
   MOE_GEMM_CASE(true, 1, kEpiStore, kGroupedMP)
+  MOE_GEMM_CASE(true, 1, kEpiSwigluFwd, kGroupedMC)
+  MOE_GEMM_CASE(true, 1, kEpiStore, kGroupedMC)
   if (g.epi == kEpiWgrad && g.mode == kGroupedK &&
       (g.p.tma_store == kDwStoreF32 || g.p.tma_store == kDwAddF32))
     return g.mx ? launch_impl<true, 1, kEpiWgrad, kGroupedK, true>(g, num_sms, stream)

@@ -109,7 +109,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const TileWalk<
     t.sfa_atom[0] = static_cast<long long>(t.a_row[0] >> 7) * p.sfa_ts;
     t.sfa_atom[1] = static_cast<long long>(t.a_row[1] >> 7) * p.sfa_ts;
     t.sfb_atom = static_cast<long long>(b) * p.sfb_ts;
-  } else if (MODE == kGroupedMP) {
+  } else if (MODE == kGroupedMP || MODE == kGroupedMC) {
     // pair m: word 3 of blocks[m] = (first block << 1) | second present;
     // the first block of a two-block pair is a full 128 rows
     const int m = w.m, n = w.n;
@@ -598,9 +598,20 @@ struct Cfg {
   static constexpr bool WGRAD = MODE == kGroupedK;
   // over row-block pairs: one A tile, a B operand of up to 256 rows (two
   // 128-row boxes), scale atoms of two A halves (gate, up) and two B blocks
-  static constexpr bool PAIR = MODE == kGroupedMP;
+  static constexpr bool PAIR = MODE == kGroupedMP || MODE == kGroupedMC;
+  // over row-block pairs on a CTA pair: this CTA's B is one block (128 rows)
+  // of the pair; both B atoms, as every SM's MMA reads the scales of all 256.
+  // A stage holds two K-chunks (K = 256): the operands come in one box each
+  // (two 16 KB chunk tiles) and the scale atoms of both chunks in one copy
+  // per operand, so each SM fills three 68 KB stages with five copies per
+  // stage (large stages and few copies are what keeps the L2-to-shared-
+  // memory stream near 24 TB/s for the whole GPU; 32 KB stages of two boxes
+  // and three small copies reach about 10).
+  static constexpr bool CG2 = MODE == kGroupedMC;
   static_assert(!PAIR || NA == 1, "one A tile per stage over row-block pairs");
-  static constexpr int SF_BYTES = MX ? (PAIR ? 4 : NA + 1) * kAtom : 0;
+  static_assert(!CG2 || MX, "CTA pairs: MXFP8");
+  static constexpr int KCH = CG2 ? 2 : 1;                  // 128-element K-chunks per stage
+  static constexpr int SF_BYTES = MX ? (PAIR ? 4 * KCH : NA + 1) * kAtom : 0;
   // Scale-atom groups (MXFP8, grouped-M, one A tile): the atoms of GS
   // consecutive stages of a tile are consecutive in memory for the weight
   // and for the row block, so they come in two copies per group into a
@@ -611,22 +622,27 @@ struct Cfg {
   static constexpr int GS = 4, SFR = 2;
   static constexpr int GROUP_BYTES = GS * (NA + 1) * kAtom;
   static constexpr int SFG_BYTES = SFG ? SFR * GROUP_BYTES : 0;
-  static constexpr int B_BYTES = PAIR ? 2 * kBBytes : kBBytes;
-  static constexpr int SF_OFF = NA * kABytes + B_BYTES;      // a stage's scale atoms
+  static constexpr int A_BYTES = NA * KCH * kABytes;
+  static constexpr int B_BYTES = (PAIR && !CG2) ? 2 * kBBytes : KCH * kBBytes;
+  static constexpr int SF_OFF = A_BYTES + B_BYTES;           // a stage's scale atoms
   static constexpr int STAGE = ((SF_OFF + (SFG ? 0 : SF_BYTES)) + 1023) / 1024 * 1024;
-  static constexpr int S = WGRAD ? 4 : ((NA == 2 || PAIR) ? 4 : 6);  // pipeline stages
+  static constexpr int S = CG2 ? 3 : (WGRAD ? 4 : ((NA == 2 || PAIR) ? 4 : 6));  // pipeline stages
   static constexpr int STAGING = WGRAD ? 2 * 32768 : 0;    // weight-gradient store buffers
   // accumulator buffers: two, except with two MXFP8 A tiles or a 256-wide
   // MXFP8 pair tile (2 x 256 columns leave no room in TMEM's 512 for the
   // stages' scale columns)
   static constexpr int ACC_BUFS = PAIR ? (MX ? 1 : 2) : ((NA == 1 || !MX) ? 2 : 1);
   static constexpr int ACC_COLS = PAIR ? 256 : NA * 128;
-  static constexpr int SF_COLS = PAIR ? 12 : (NA + 1) * 4;  // scale columns per stage (B: 8 over pairs)
+  static constexpr int SF_COLS = PAIR ? 12 * KCH : (NA + 1) * 4;  // scale columns per stage (B: 8 over pairs)
   // the pair SwiGLU epilogue's exchange buffer; a smaller metadata cache
   static constexpr int EXCH = PAIR ? 16384 : 0;
-  static constexpr int CACHE = PAIR ? 8192 : kCacheBytes;
+  static constexpr int CACHE = CG2 ? 4096 : (PAIR ? 8192 : kCacheBytes);
+  // mbarriers, the TMEM address and the abort flags (CTA pairs: also each
+  // stage's "both CTAs' operands are ready" and the other CTA's accumulator
+  // release)
+  static constexpr int BARS = CG2 ? 512 : 256;
   static constexpr uint32_t SF_COL0 = ACC_BUFS * ACC_COLS;
-  static constexpr int BK = MX ? 128 : 64;                 // contraction elements per stage
+  static constexpr int BK = MX ? 128 * KCH : 64;           // contraction elements per stage
   static constexpr int KMMA = MX ? 32 : 16;                // contraction elements per MMA
   static constexpr int MMAS = BK / KMMA;
   // epilogue warps: 8 (two per TMEM lane quadrant, alternate 32-column
@@ -643,7 +659,7 @@ struct Cfg {
   // MMA thread issues nothing but MMAs and commits
   static constexpr int SF_WARPS = MX ? 1 : 0;
   static constexpr int THREADS = 64 + EPI_THREADS + 32 * SF_WARPS;
-  static constexpr int SMEM = 1024 + S * STAGE + STAGING + SFG_BYTES + EXCH + 256 + CACHE;
+  static constexpr int SMEM = 1024 + S * STAGE + STAGING + SFG_BYTES + EXCH + BARS + CACHE;
   static_assert(SMEM <= 232448, "shared memory per CTA");
   static_assert(ACC_BUFS * ACC_COLS + S * (MX ? SF_COLS : 0) <= 512, "tensor memory columns");
 };

@@ -120,8 +120,11 @@ cudaError_t launch_transpose_bf16(const void* w, int E, int N, int K, void* wT, 
 
 // kGroupedMP: grouped-M over row-block pairs (B up to 256 rows, one A tile
 // of 128 rows per stage; the SwiGLU forward's A tile is 64 gate rows then the
-// 64 up rows of the same features).
-enum GemmMode { kGroupedM = 0, kGroupedK = 1, kGroupedMP = 2 };
+// 64 up rows of the same features).  kGroupedMC: the same tiles on CTA
+// pairs (clusters of two): the pair's two CTAs take adjacent A tiles and one
+// routing block each of the same row-block pair, and one 256 x 256 MMA
+// (cta_group::2) covers both, so each SM loads 128 B rows instead of 256.
+enum GemmMode { kGroupedM = 0, kGroupedK = 1, kGroupedMP = 2, kGroupedMC = 3 };
 // How a weight-gradient epilogue writes dW: plain stores (BF16 accumulate),
 // or staged in shared memory and moved by TMA: a BF16 store, an FP32 store,
 // or an FP32 reduce-add into the existing dW (one FP32 add per element,

@@ -81,11 +81,50 @@ bool make_tmap_nd(CUtensorMap* tm, CUtensorMapDataType dt, int rank, const void*
 // Over row-block pairs (kGroupedMP) the SwiGLU forward's one A tile is the
 // same 3D box 64 rows high: 64 gate rows, then the up rows of the same
 // features.
+//
+// On CTA pairs (kGroupedMC, MXFP8) a stage is two 128-byte K-chunks, and each
+// box covers both: the K axis is split into [K/128 chunks][128 bytes] (the
+// chunk axis outermost in the box), so a box lands as [chunk][rows][128 B],
+// one 128-row (or 2 x 64-row) tile per chunk.  aux[0]: A (W13: [chunks]
+// [gate, up][64 rows]; W2: [chunks][128 rows]); aux[1]: B, one routing block
+// ([chunks][128 rows]); aux[2] (W13): both chunks' atoms of the gate and up
+// halves.
 bool make_grouped_m_boxes(GemmLaunch* g, const void* a, int64_t a_rows, const void* a_sf, const void* b,
                           int64_t b_rows, bool mx, int64_t cols, int64_t halves_f) {
   const int esz = mx ? 1 : 2;
   const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const cuuint64_t ks = static_cast<cuuint64_t>(cols / 128), atom = 512;
+  if (g->mode == kGroupedMC) {
+    if (!mx || cols % 256 != 0) return false;
+    const cuuint64_t c = static_cast<cuuint64_t>(cols);
+    if (g->epi == kEpiSwigluFwd) {
+      if (halves_f <= 0 || halves_f % 128 != 0) return false;
+      const cuuint64_t hf = static_cast<cuuint64_t>(halves_f);
+      const cuuint64_t d[4] = {128, hf, static_cast<cuuint64_t>(a_rows) / hf, ks};
+      const cuuint64_t st[3] = {c, hf * c, 128};
+      const cuuint32_t bx[4] = {128, 64, 2, 2};
+      if (!make_tmap_nd(&g->aux[0], dt, 4, a, d, st, bx, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
+      const cuuint64_t ft = hf / 128;
+      const cuuint64_t d4[4] = {128, ks, ft, static_cast<cuuint64_t>(a_rows) / hf};
+      const cuuint64_t st4[3] = {atom, ks * atom, ft * ks * atom};
+      const cuuint32_t bx4[4] = {128, 2, 1, 2};
+      if (!make_tmap_nd(&g->aux[2], CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, a_sf, d4, st4, bx4,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+        return false;
+    } else {
+      const cuuint64_t d[3] = {128, static_cast<cuuint64_t>(a_rows), ks};
+      const cuuint64_t st[2] = {c, 128};
+      const cuuint32_t bx[3] = {128, 128, 2};
+      if (!make_tmap_nd(&g->aux[0], dt, 3, a, d, st, bx, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
+    }
+    const cuuint64_t d[3] = {128, static_cast<cuuint64_t>(b_rows), ks};
+    const cuuint64_t st[2] = {c, 128};
+    const cuuint32_t bx[3] = {128, 128, 2};
+    if (!make_tmap_nd(&g->aux[1], dt, 3, b, d, st, bx, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
+    g->p.a_pair_box = 0;
+    g->p.b_full_box = 0;
+    return true;
+  }
   if (g->na == 2 && g->epi == kEpiStore) {
     if (!make_tmap(&g->aux[0], a, mx, a_rows, cols, 256)) return false;
     if (mx) {
@@ -101,7 +140,7 @@ bool make_grouped_m_boxes(GemmLaunch* g, const void* a, int64_t a_rows, const vo
     const cuuint64_t d[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(halves_f),
                              static_cast<cuuint64_t>(a_rows / halves_f)};
     const cuuint64_t st[2] = {static_cast<cuuint64_t>(cols * esz), static_cast<cuuint64_t>(halves_f * cols * esz)};
-    const cuuint32_t bx[3] = {static_cast<cuuint32_t>(128 / esz), g->mode == kGroupedMP ? 64u : 128u, 2};
+    const cuuint32_t bx[3] = {static_cast<cuuint32_t>(128 / esz), g->na == 1 ? 64u : 128u, 2};
     if (!make_tmap_nd(&g->aux[0], dt, 3, a, d, st, bx, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
     if (mx) {
       const cuuint64_t ft = static_cast<cuuint64_t>(halves_f / 128);

@@ -89,3 +89,67 @@ def test_pairs_inference_and_clamped_swiglu():
         res.append((r["out"], r["layer"].clip_stats()))
     np.testing.assert_array_equal(res[0][0], res[1][0])
     assert list(res[0][1]) == list(res[1][1]) and res[0][1][0] > 0
+
+
+# ---------------------------------------------------------------- CTA pairs
+# Mode 3: the MXFP8 forward's pair tiles on clusters of two CTAs, one
+# 256 x 256 block-scaled MMA (cta_group::2) per K step over both: each CTA
+# holds its own 128 weight rows (SwiGLU: 64 gate + 64 up rows of its own 64
+# features) and one routing block of the pair, and drains its own 128
+# accumulator lanes; a stage is two 128-element K-chunks.  The contraction
+# order per output element is that of the row-block tiles, so the bits must
+# match.  The backward's GEMMs keep their usual tiles; a saved state is the
+# same whichever tiles wrote it.
+
+CTA_CASES = {
+    # D = F = 256: one stage per tile; lone last blocks (the second CTA of the
+    # cluster loads no rows) and short second blocks
+    "mx_ragged": CASES["mx_ragged"],
+    # D = 1024, F = 512: four stages per W13 tile, two per W2 tile (stage ring
+    # phases wrap within a tile), two W2 cluster tiles along the features
+    "mx_deep": lambda: synth.Workload("pair_deep", 600, 1024, 512, 4, 2, "mxfp8", "zipf", inactive_frac=0.05,
+                                      zipf_s=0.8, seed=85),
+}
+
+
+@pytest.mark.parametrize("max_ctas", [0, 6])
+@pytest.mark.parametrize("name", list(CTA_CASES))
+def test_cta_pairs_equal_row_blocks_bitwise(name, max_ctas):
+    """max_ctas = 6 (three clusters) makes every cluster walk many tiles."""
+    w = CTA_CASES[name]()
+    case = Case(w)
+    a = run_gpu(case, tile_mode=1, max_ctas=max_ctas)
+    b = run_gpu(case, tile_mode=3, max_ctas=max_ctas)
+    for r in (a, b):
+        assert r["err_bits"] == 0
+    for f in FIELDS:
+        np.testing.assert_array_equal(a[f], b[f], err_msg=f)
+    o = run_oracle(case, backward=False)
+    assert rel_err(b["out"], o["out"]) <= TOL[w.precision]
+
+
+def test_cta_pairs_inference_and_clamped_swiglu():
+    """Inference through CTA pairs with the clamped SwiGLU: output and clip
+    counts equal to row blocks."""
+    w = CTA_CASES["mx_deep"]()
+    case = Case(w)
+    res = []
+    for mode in (1, 3):
+        r = run_gpu(case, training=False, swiglu_limit=0.75, tile_mode=mode)
+        assert r["err_bits"] == 0
+        res.append((r["out"], r["layer"].clip_stats()))
+    np.testing.assert_array_equal(res[0][0], res[1][0])
+    assert list(res[0][1]) == list(res[1][1]) and res[0][1][0] > 0
+
+
+@pytest.mark.parametrize("D,F", [(384, 256), (512, 384)])
+def test_cta_pairs_fall_back_where_k_is_not_a_multiple_of_256(D, F):
+    """A CTA pair's stage is 256 elements of K and its W2 tile 256 features:
+    W13 (K = D) and W2 (K = F, 256-feature tiles of D) that do not divide
+    take one-CTA pair tiles instead, with the same bits."""
+    w = synth.Workload("pair_fallback", 300, D, F, 3, 2, "mxfp8", "uniform", seed=84)
+    case = Case(w)
+    a = run_gpu(case, training=False, tile_mode=1)
+    b = run_gpu(case, training=False, tile_mode=3)
+    assert a["err_bits"] == 0 and b["err_bits"] == 0
+    np.testing.assert_array_equal(a["out"], b["out"])
