@@ -153,3 +153,27 @@ def test_cta_pairs_fall_back_where_k_is_not_a_multiple_of_256(D, F):
     b = run_gpu(case, training=False, tile_mode=3)
     assert a["err_bits"] == 0 and b["err_bits"] == 0
     np.testing.assert_array_equal(a["out"], b["out"])
+
+
+def test_cta_pairs_at_the_dense_full_size():
+    """The compute-bound diagnostic shape (T=2048, D=7168, F=2048, E=6, K=6,
+    every token routed to every expert: 8 full pairs per expert, 28 stages
+    per W13 tile, more tiles than clusters).  CTA pairs, forced and by the
+    context's default at this density, equal row blocks bit for bit; sampled
+    tokens match the oracle (the MXFP8 oracle quantises each token row on its
+    own, so a token subset gives the same rows)."""
+    from oracle import moe as omoe
+    from moe_cases import to_f64
+    w = synth.WORKLOADS["e6_dense"]
+    case = Case(w)
+    a = run_gpu(case, training=False, tile_mode=1)
+    b = run_gpu(case, training=False, tile_mode=3)
+    c = run_gpu(case, training=False)
+    for r in (a, b, c):
+        assert r["err_bits"] == 0
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["out"], c["out"])
+    tokens = [0, 777, 1500, 2047]
+    st = omoe.forward(to_f64(case.x)[tokens], case.ids[tokens].astype(np.int64), case.scores[tokens],
+                      to_f64(case.w13), to_f64(case.w2), "mxfp8")
+    assert rel_err(b["out"][tokens], st["out"]) <= TOL["mxfp8"]
