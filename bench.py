@@ -183,6 +183,24 @@ def gemm_tensor(stage_ms, routes, w, peak_t):
             "tensor_frac": round(total / (t * 1e-3) / 1e12 / peak_t, 4), "per_gemm_tensor_frac": per}
 
 
+def roofline(kernel, ms, nbytes, routes, w, pk, peak_t, traffic):
+    """The dominant kernel against the roof that bounds it: its useful FLOPs
+    per algorithmic byte above the ridge (tensor peak / copy bandwidth) put
+    it under the tensor roof (TFLOP/s of the dtype's peak), else under HBM."""
+    base = {"kernel": kernel, "traffic": traffic, "algorithmic_bytes": int(nbytes), "avg_launch_ms": round(ms, 4),
+            "peak_source": pk["source"]}
+    flops = GEMM_FLOPS.get(kernel, 0.0) * routes * w.D * w.F
+    ridge = peak_t * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if flops > 0 and flops / nbytes > ridge:
+        achieved = flops / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak_t, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak_t, 4), "flop_per_byte": round(flops / nbytes, 1),
+                "ridge_flop_per_byte": round(ridge, 1), **base}
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4), **base}
+
+
 def gemm_source_digest():
     """SHA-256 prefix of the GEMM kernels' sources (gemm.cu, gemm_core.cuh,
     common.cuh): a traffic record holds only for the code it was taken on."""
@@ -536,19 +554,15 @@ def run_ours(args, rank, world):
         stage_ms = {"fused_forward": sum(statistics.mean(fwd_t[n]) for n in abi.FWD_STAGE_NAMES)}
         sbytes = {"fused_forward": sum(fb.values())}
     dom = max(stage_ms, key=lambda k: stage_ms[k])
-    achieved = sbytes[dom] / (stage_ms[dom] * 1e-3) / 1e9
-    roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic_record(dom, w.name),
-            "algorithmic_bytes": int(sbytes[dom]), "avg_launch_ms": round(stage_ms[dom], 4),
-            "peak_source": pk["source"]}
+    fp8_peak = pk["bf16_tflops"] * 2.0
+    peak_t = fp8_peak if w.precision == "mxfp8" else pk["bf16_tflops"]
+    roof = roofline(dom, stage_ms[dom], sbytes[dom], routes, w, pk, peak_t, traffic_record(dom, w.name))
     stages = {k: {"ms": round(v, 4), "GB/s": round(sbytes[k] / (v * 1e-3) / 1e9, 1) if v > 0 else None}
               for k, v in stage_ms.items()}
 
     # ---------------- metric
     flops = 6.0 * routes * w.D * w.F * (3.0 if st.train else 1.0)
     tflops = flops / (ms * 1e-3) / 1e12 * world
-    fp8_peak = pk["bf16_tflops"] * 2.0
-    peak_t = fp8_peak if w.precision == "mxfp8" else pk["bf16_tflops"]
     shared_flops = (6.0 * w.T * w.D * w.shared_F * (3.0 if st.train else 1.0)) if w.shared_F else 0.0
 
     # ---------------- end to end through the ABI with host buffers

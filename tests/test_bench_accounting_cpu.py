@@ -71,3 +71,28 @@ def test_gemm_flops_add_up_to_the_step():
     assert abs(g["tflops"] - want) < 0.1 and abs(g["tensor_frac"] - want / 1000.0) < 1e-4
     assert set(g["per_gemm_tensor_frac"]) == {"gemm_w13_swiglu", "gemm_w2"}
     assert bench.gemm_tensor({"route": 0.02}, R, w, 1000.0) is None
+
+
+def test_roofline_bound_follows_arithmetic_intensity():
+    """The dominant kernel is reported under the tensor roof when its useful
+    FLOPs per algorithmic byte exceed the ridge (peak FLOP/s over copy
+    bandwidth), else under HBM: the dense E=6 W13 (about 2400 FLOP/B) is
+    tensor-bound, the E=384 training step's W13 weight gradient (about 28) is
+    bound by its dW bytes."""
+    pk = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "measured"}
+    peak8 = 2 * pk["bf16_tflops"]
+    w = synth.WORKLOADS["e6_dense"]
+    R = w.T * w.K
+    fb, _ = bench.stage_bytes(w, R, R, w.precision, False)
+    r = bench.roofline("gemm_w13_swiglu", 0.25, fb["gemm_w13_swiglu"], R, w, pk, peak8, None)
+    flops = 4.0 * R * w.D * w.F
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - flops / 0.25e-3 / 1e12) < 0.1 and abs(r["frac"] - r["achieved"] / peak8) < 1e-4
+    assert r["flop_per_byte"] > r["ridge_flop_per_byte"]
+    w4 = synth.WORKLOADS["e384_mxfp8_zipf_train"]
+    _, bb = bench.stage_bytes(w4, 20000, 11059, w4.precision, True)
+    r4 = bench.roofline("gemm_w13_wgrad", 3.5, bb["gemm_w13_wgrad"], 11059, w4, pk, peak8, 123)
+    assert r4["bound"] == "hbm" and r4["unit"] == "GB/s" and r4["traffic"] == 123
+    assert abs(r4["achieved"] - bb["gemm_w13_wgrad"] / 3.5e-3 / 1e9) < 0.1
+    # a stage with no GEMM FLOPs (routing, gathers, combine) is always HBM
+    assert bench.roofline("combine", 0.04, 1e8, R, w, pk, peak8, None)["bound"] == "hbm"
