@@ -440,11 +440,13 @@ MOE_API uint64_t moe_ctx_launch_count(const moe_ctx* ctx);
 /*
  * Upper bound on the CTAs of each persistent launch of this context (the
  * grouped GEMMs, combine, score gradient): 0, the default, is one per SM.
- * The pages have no counterpart; a caller can leave SMs to work on other
- * streams, and a test can make each CTA walk many tiles of a small
- * problem.  Results do not depend on it: every output tile is computed by
- * one CTA with the same instruction sequence.  Applies to calls enqueued
- * after it (a captured graph keeps the grids it was captured with).
+ * GEMMs that run on CTA pairs (clusters of two) take max_ctas / 2 clusters,
+ * and at least one.  The pages have no counterpart; a caller can leave SMs
+ * to work on other streams, and a test can make each CTA walk many tiles of
+ * a small problem.  Results do not depend on it: every output tile is
+ * computed by one CTA (or CTA pair) with the same instruction sequence.
+ * Applies to calls enqueued after it (a captured graph keeps the grids it
+ * was captured with).
  * Errors: MOE_ERR_INVALID_ARG for a null context or max_ctas < 0.
  */
 MOE_API moe_status moe_ctx_set_max_ctas(moe_ctx* ctx, int max_ctas);
