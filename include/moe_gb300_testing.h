@@ -63,13 +63,13 @@ MOE_API moe_status moe_ctx_test_fused_stall(moe_ctx* ctx, int stall, int64_t wai
  * W2, W13 input gradient): mode 1 takes one routing row block (<= 128 rows)
  * as the B operand; mode 2 takes row-block pairs (two consecutive blocks of
  * one expert, <= 256 rows, the pairs of MOE_SAVED_BLOCKS word 3); mode 3
- * (MXFP8) runs the forward's pairs on CTA pairs (clusters of two CTAs, one
- * 256 x 256 tensor-core instruction over both: each CTA one A tile and one
- * block of the pair; where d_model or d_ff is not a multiple of 256 that
- * GEMM takes mode 2's tiles; the backward as mode 2); mode 0 (the default)
- * takes pairs in BF16 when max_tokens * top_k >= 128 * num_experts and, in
- * MXFP8, CTA pairs for the forward when max_tokens * top_k >= 256 *
- * num_experts.
+ * runs the forward's pairs on CTA pairs (clusters of two CTAs, one 256 x 256
+ * tensor-core instruction over both: each CTA one A tile and one block of
+ * the pair; a GEMM whose K is not a multiple of 256 bytes, or W2 where
+ * d_model is not a multiple of 256, takes mode 2's tiles; the backward as
+ * mode 2); mode 0 (the default) takes CTA pairs for the forward when
+ * max_tokens * top_k >= 256 * num_experts, and in BF16 pairs elsewhere when
+ * max_tokens * top_k >= 128 * num_experts.
  * All give the same results bit for bit, and a forward and its backward
  * may run in different modes (both read the same saved state).  Applies to
  * later calls; no device access. */

@@ -311,7 +311,7 @@ def moe_ctx_test_fused_stall(ctx, stall, wait_cycles=0):
 
 def moe_ctx_test_tile_mode(ctx, mode):
     """0: row-block pairs when the capacity is dense enough, 1: row blocks, 2: pairs,
-    3: MXFP8 forward pairs on CTA pairs."""
+    3: the forward's pairs on CTA pairs."""
     _check("moe_ctx_test_tile_mode", LIB.moe_ctx_test_tile_mode(ctx, int(mode)))
 
 

@@ -32,9 +32,9 @@ struct moe_ctx {
   // creation for BF16 when the capacity gives the experts 128 routes each on
   // average (max_tokens * top_k >= 128 E); moe_ctx_test_tile_mode overrides it
   bool pair_tiles_auto = false;
-  // MXFP8: the forward's GEMMs over row-block pairs on CTA pairs, chosen at
-  // creation when experts hold two or more full row blocks on average
-  // (max_tokens * top_k >= 256 E); moe_ctx_test_tile_mode overrides it
+  // the forward's GEMMs over row-block pairs on CTA pairs, chosen at creation
+  // when experts hold two or more full row blocks on average (max_tokens *
+  // top_k >= 256 E); moe_ctx_test_tile_mode overrides it
   bool cta_pairs_auto = false;
   int tile_mode = 0;               // 0: automatic, 1: row blocks, 2: pairs, 3: pairs on CTA pairs
   long long fused_wait = 0;        // counter-wait limit of the single-launch forward (0: default)
@@ -80,15 +80,14 @@ bool config_tileable(const moe_config* c) { return c->d_model % 128 == 0 && c->d
 bool use_pairs(const moe_ctx* c) { return c->tile_mode >= 2 || (c->tile_mode == 0 && c->pair_tiles_auto); }
 
 // Tiles of the forward's grouped-M GEMMs (W13 + SwiGLU, W2): row blocks, row-
-// block pairs, or (MXFP8) row-block pairs on CTA pairs.
+// block pairs, or row-block pairs on CTA pairs.
 GemmMode forward_tiles(const moe_ctx* c) {
-  const bool mx = c->cfg.precision == MOE_MXFP8;
   switch (c->tile_mode) {
     case 1: return kGroupedM;
     case 2: return kGroupedMP;
-    case 3: return mx ? kGroupedMC : kGroupedMP;
+    case 3: return kGroupedMC;
     default:
-      if (mx) return c->cta_pairs_auto ? kGroupedMC : kGroupedM;
+      if (c->cta_pairs_auto) return kGroupedMC;
       return c->pair_tiles_auto ? kGroupedMP : kGroupedM;
   }
 }
@@ -284,7 +283,7 @@ bool fill_w13(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W13, uint8_
   const int D = c.d_model, F = c.d_ff, E = c.num_experts;
   const bool mx = c.precision == MOE_MXFP8;
   const int64_t R = ctx->r_cap;
-  if (mode == kGroupedMC && D % 256 != 0) mode = kGroupedMP;   // a CTA pair's stage is 256 of K
+  if (mode == kGroupedMC && D % (mx ? 256 : 128) != 0) mode = kGroupedMP;   // a CTA pair's stage: 256 bytes of K
   g1->mx = mx;
   g1->na = mode == kGroupedM ? 2 : 1;
   g1->epi = kEpiSwigluFwd;
@@ -337,8 +336,8 @@ bool fill_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uint8_t*
   const int D = c.d_model, F = c.d_ff, E = c.num_experts;
   const bool mx = c.precision == MOE_MXFP8;
   const int64_t R = ctx->r_cap;
-  // a CTA pair's tile is 256 features, its stage 256 of K
-  if (mode == kGroupedMC && (D % 256 != 0 || F % 256 != 0)) mode = kGroupedMP;
+  // a CTA pair's tile is 256 features, its stage 256 bytes of K
+  if (mode == kGroupedMC && (D % 256 != 0 || F % (mx ? 256 : 128) != 0)) mode = kGroupedMP;
   g2->mx = mx;
   g2->na = mode == kGroupedM ? pair_tiles(D) : 1;
   g2->epi = kEpiStore;
@@ -568,10 +567,9 @@ moe_status moe_ctx_create(const moe_config* cfg, moe_ctx** out) {
   // loads, measured no faster than two row-block tiles
   c->pair_tiles_auto = cfg->precision == MOE_BF16 &&
                        static_cast<int64_t>(cfg->max_tokens) * cfg->top_k >= 128LL * cfg->num_experts;
-  // MXFP8 dense enough for full pairs: CTA pairs (one 256 x 256 MMA over two
-  // SMs, each loading half the operands, in 68 KB two-K-chunk stages)
-  c->cta_pairs_auto = cfg->precision == MOE_MXFP8 &&
-                      static_cast<int64_t>(cfg->max_tokens) * cfg->top_k >= 256LL * cfg->num_experts;
+  // dense enough for full pairs: CTA pairs (one 256 x 256 MMA over two SMs,
+  // each loading half the operands, in two-K-chunk stages)
+  c->cta_pairs_auto = static_cast<int64_t>(cfg->max_tokens) * cfg->top_k >= 256LL * cfg->num_experts;
   const ScratchLayout L = scratch_layout(cfg);
   c->bytes = L.total;
   if (cudaMalloc(&c->base, c->bytes) != cudaSuccess) {

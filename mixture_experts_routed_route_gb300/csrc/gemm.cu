@@ -26,14 +26,16 @@
 //    scale columns need the rest of TMEM); the SwiGLU forward's A tile is 64
 //    gate rows followed by the 64 up rows of the same features, and its
 //    epilogue pairs them up through shared memory.
-//  * the same pair tiles on CTA pairs (kGroupedMC, MXFP8): a cluster of two
+//  * the same pair tiles on CTA pairs (kGroupedMC): a cluster of two
 //    CTAs on two SMs takes two adjacent A tiles (SwiGLU: features f..f+63
 //    and f+64..f+127) against one row-block pair, each CTA loading its own
 //    A tile and one block of the pair.  The lower-ranked CTA issues one
 //    tcgen05.mma.cta_group::2 of M = 256, N = 256 per K step over both; each
 //    CTA's 128 accumulator lanes hold its A tile's rows against all 256
 //    columns, and each CTA drains its own.  Per SM a stage then carries 32 KB
-//    of operands instead of 48 for the same tensor-core work.  Rank 1 reports
+//    of operands instead of 48 for the same tensor-core work (stages hold two
+//    K-chunks: 64 KB per SM; BF16 double-buffers the accumulator, having no
+//    scale columns in TMEM).  Rank 1 reports
 //    each stage's operands in place (and each accumulator drained) to rank 0
 //    through mbarriers in rank 0's shared memory; rank 0's commits release
 //    the stages and hand over the accumulators in both CTAs (multicast).
@@ -67,9 +69,10 @@
 //               accumulator
 //   warps 10..17  weight gradient only: a second epilogue group of 8 warps;
 //               the two groups take alternate tiles
-//   last warp   MXFP8 only: over row-block pairs, builds the SwiGLU
-//               forward's weight atom of each stage; CTA pairs: tells rank
-//               0's MMA thread when a stage's operands are in place
+//   last warp   MXFP8 (and BF16 on CTA pairs): copies the scale atoms, or
+//               over row-block pairs builds the SwiGLU forward's weight atom
+//               of each stage; CTA pairs: tells rank 0's MMA thread when a
+//               stage's operands are in place
 #include "gemm_core.cuh"
 
 namespace moe {
@@ -244,16 +247,19 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
             // (SwiGLU: of both halves) at ssf, then each block's two atoms
             const bool two = t.b_rows > 128;
             const bool mine = rank == 0 || two;
-            const int kc = kx >> 7;
+            const int kc = kx / (MX ? 128 : 64);   // 128-byte chunks
             mbar_arrive_expect_tx(&full[slot], C::A_BYTES + (mine ? C::B_BYTES : 0) +
-                                                   ((EPI == kEpiSwigluFwd ? 4 : 2) + (two ? 4 : 2)) * kAtom);
+                                                   (MX ? ((EPI == kEpiSwigluFwd ? 4 : 2) + (two ? 4 : 2)) * kAtom : 0));
             if (EPI == kEpiSwigluFwd) tma_load_4d(sa, &aux0, &full[slot], 0, t.out_col0, 2 * t.e, kc);
             else tma_load_3d(sa, &aux0, &full[slot], 0, t.a_row[0], kc);
             if (mine) tma_load_3d(sb, &aux1, &full[slot], 0, t.b_row0 + 128 * static_cast<int>(rank), kc);
-            if (EPI == kEpiSwigluFwd) tma_load_4d(ssf, &aux2, &full[slot], 0, kc, t.out_col0 >> 7, 2 * t.e);
-            else bulk_load(ssf, p.sfa + (t.sfa_atom[0] + kc) * kAtom, 2 * kAtom, &full[slot]);
-            bulk_load(ssf + 4 * kAtom, p.sfb + (t.sfb_atom + kc) * kAtom, 2 * kAtom, &full[slot]);
-            if (two) bulk_load(ssf + 6 * kAtom, p.sfb + (t.sfb_atom + p.sfb_ts + kc) * kAtom, 2 * kAtom, &full[slot]);
+            if (MX) {
+              if (EPI == kEpiSwigluFwd) tma_load_4d(ssf, &aux2, &full[slot], 0, kc, t.out_col0 >> 7, 2 * t.e);
+              else bulk_load(ssf, p.sfa + (t.sfa_atom[0] + kc) * kAtom, 2 * kAtom, &full[slot]);
+              bulk_load(ssf + 4 * kAtom, p.sfb + (t.sfb_atom + kc) * kAtom, 2 * kAtom, &full[slot]);
+              if (two)
+                bulk_load(ssf + 6 * kAtom, p.sfb + (t.sfb_atom + p.sfb_ts + kc) * kAtom, 2 * kAtom, &full[slot]);
+            }
           } else if (PAIR) {
             // one A tile (SwiGLU: its gate and up halves in one 3D box), B as
             // full 128-row boxes then 32-row boxes; MXFP8: the weight's atom
@@ -370,7 +376,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       // half is whatever the other CTA's stage holds; its columns are never read)
       const uint32_t idesc = MX ? (idesc_mxf8(CG2 ? 256 : t.b_rows, 0, 0, CG2 ? 256 : 128) |
                                    (MODE != kGroupedK && p.a_mn ? kIdescAMnMajor : 0u))
-                                : idesc_bf16(t.b_rows);
+                                : idesc_bf16(CG2 ? 256 : t.b_rows, CG2 ? 256 : 128);
       for (int ks = 0; ks < t.kstages; ++ks, ++it) {
         const uint32_t slot = it % S, ph = (it / S) & 1;
         // MXFP8: the scale warp's commit for this stage follows its own wait
@@ -404,15 +410,21 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < C::KCH; ++c) {
             const uint32_t sfc = sfcol + 12 * c;
-            tc_cp_sf_pair(sfc, sdesc_sf_atom(ssf + c * kAtom));
-            tc_cp_sf_pair(sfc + 4, sdesc_sf_atom(ssf + (4 + c) * kAtom));
-            if (two) tc_cp_sf_pair(sfc + 8, sdesc_sf_atom(ssf + (6 + c) * kAtom));
+            if (MX) {
+              tc_cp_sf_pair(sfc, sdesc_sf_atom(ssf + c * kAtom));
+              tc_cp_sf_pair(sfc + 4, sdesc_sf_atom(ssf + (4 + c) * kAtom));
+              if (two) tc_cp_sf_pair(sfc + 8, sdesc_sf_atom(ssf + (6 + c) * kAtom));
+            }
             const uint64_t ad = sdesc_k_sw(sa + c * kABytes, 128), bd = sdesc_k_sw(sb + c * kBBytes, 128);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_mxf8_pair(d_tmem, ad + 2 * k, bd + 2 * k,
-                            idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29), sfc, sfc + 4,
-                            (ks | c | k) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {   // 32 bytes of K each (32 E4M3 or 16 BF16 values)
+              if (MX)
+                mma_mxf8_pair(d_tmem, ad + 2 * k, bd + 2 * k,
+                              idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29), sfc,
+                              sfc + 4, (ks | c | k) ? 1u : 0u);
+              else
+                mma_bf16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (ks | c | k) ? 1u : 0u);
+            }
           }
           // the stage is free in both CTAs
           tc_commit_pair_mc(&empty[slot], 3);
@@ -453,7 +465,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
       drain_wait(drain, 0);
     }
     __syncwarp();
-  } else if (MX && warp == 2 + C::EPI_WARPS) {
+  } else if ((MX || CG2) && warp == 2 + C::EPI_WARPS) {
     // ------------------------------------------------- scale-atom copier
     // Each stage's scale atoms go from shared memory to the stage's TMEM
     // columns once its data has landed; the commit tells the MMA thread.
@@ -481,7 +493,7 @@ __global__ void __launch_bounds__(Cfg<MX, NA, MODE>::THREADS, 1)
             break;
           }
         }
-        if (PAIR && EPI == kEpiSwigluFwd) {
+        if (MX && PAIR && EPI == kEpiSwigluFwd) {
           // The A tile is rows f0..f0+63 of the gate half, then of the up
           // half: its atom (row p at byte (p%32)*16 + (p/32)*4 + l) takes
           // rows 64a..64a+63 (a = (f0/64) % 2) of the gate half's 128-row
@@ -747,7 +759,9 @@ cudaError_t launch_gemm(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   MOE_GEMM_CASE(false, 1, kEpiStore, kGroupedMP)
   MOE_GEMM_CASE(false, 1, kEpiSwigluBwd, kGroupedMP)
   MOE_GEMM_CASE(true, 1, kEpiStore, kGroupedMP)
+  MOE_GEMM_CASE(false, 1, kEpiSwigluFwd, kGroupedMC)
   MOE_GEMM_CASE(true, 1, kEpiSwigluFwd, kGroupedMC)
+  MOE_GEMM_CASE(false, 1, kEpiStore, kGroupedMC)
   MOE_GEMM_CASE(true, 1, kEpiStore, kGroupedMC)
   if (g.epi == kEpiWgrad && g.mode == kGroupedK &&
       (g.p.tma_store == kDwStoreF32 || g.p.tma_store == kDwAddF32))

@@ -609,7 +609,6 @@ struct Cfg {
   // and three small copies reach about 10).
   static constexpr bool CG2 = MODE == kGroupedMC;
   static_assert(!PAIR || NA == 1, "one A tile per stage over row-block pairs");
-  static_assert(!CG2 || MX, "CTA pairs: MXFP8");
   static constexpr int KCH = CG2 ? 2 : 1;                  // 128-element K-chunks per stage
   static constexpr int SF_BYTES = MX ? (PAIR ? 4 * KCH : NA + 1) * kAtom : 0;
   // Scale-atom groups (MXFP8, grouped-M, one A tile): the atoms of GS
@@ -642,7 +641,7 @@ struct Cfg {
   // release)
   static constexpr int BARS = CG2 ? 512 : 256;
   static constexpr uint32_t SF_COL0 = ACC_BUFS * ACC_COLS;
-  static constexpr int BK = MX ? 128 * KCH : 64;           // contraction elements per stage
+  static constexpr int BK = (MX ? 128 : 64) * KCH;         // contraction elements per stage
   static constexpr int KMMA = MX ? 32 : 16;                // contraction elements per MMA
   static constexpr int MMAS = BK / KMMA;
   // epilogue warps: 8 (two per TMEM lane quadrant, alternate 32-column
@@ -656,8 +655,9 @@ struct Cfg {
   static constexpr int GROUP_THREADS = EPI_THREADS / EPI_GROUPS;
   static_assert(!WGRAD || (NA == 1 && ACC_BUFS == EPI_GROUPS), "one accumulator buffer per epilogue group");
   // MXFP8: one more warp copies each stage's scale atoms to TMEM, so the
-  // MMA thread issues nothing but MMAs and commits
-  static constexpr int SF_WARPS = MX ? 1 : 0;
+  // MMA thread issues nothing but MMAs and commits (CTA pairs, BF16 too: it
+  // reports each stage to rank 0)
+  static constexpr int SF_WARPS = (MX || CG2) ? 1 : 0;
   static constexpr int THREADS = 64 + EPI_THREADS + 32 * SF_WARPS;
   static constexpr int SMEM = 1024 + S * STAGE + STAGING + SFG_BYTES + EXCH + BARS + CACHE;
   static_assert(SMEM <= 232448, "shared memory per CTA");

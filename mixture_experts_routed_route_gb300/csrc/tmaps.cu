@@ -82,10 +82,10 @@ bool make_tmap_nd(CUtensorMap* tm, CUtensorMapDataType dt, int rank, const void*
 // same 3D box 64 rows high: 64 gate rows, then the up rows of the same
 // features.
 //
-// On CTA pairs (kGroupedMC, MXFP8) a stage is two 128-byte K-chunks, and each
-// box covers both: the K axis is split into [K/128 chunks][128 bytes] (the
-// chunk axis outermost in the box), so a box lands as [chunk][rows][128 B],
-// one 128-row (or 2 x 64-row) tile per chunk.  aux[0]: A (W13: [chunks]
+// On CTA pairs (kGroupedMC) a stage is two 128-byte K-chunks, and each box
+// covers both: the K axis is split into [chunks][128 bytes] (the chunk axis
+// outermost in the box), so a box lands as [chunk][rows][128 B], one 128-row
+// (or 2 x 64-row) tile per chunk.  aux[0]: A (W13: [chunks]
 // [gate, up][64 rows]; W2: [chunks][128 rows]); aux[1]: B, one routing block
 // ([chunks][128 rows]); aux[2] (W13): both chunks' atoms of the gate and up
 // halves.
@@ -95,31 +95,35 @@ bool make_grouped_m_boxes(GemmLaunch* g, const void* a, int64_t a_rows, const vo
   const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const cuuint64_t ks = static_cast<cuuint64_t>(cols / 128), atom = 512;
   if (g->mode == kGroupedMC) {
-    if (!mx || cols % 256 != 0) return false;
-    const cuuint64_t c = static_cast<cuuint64_t>(cols);
+    const cuuint64_t w = static_cast<cuuint64_t>(128 / esz);             // elements per chunk
+    if (cols % (2 * w) != 0) return false;
+    const cuuint64_t nch = static_cast<cuuint64_t>(cols) / w;           // chunks along K
+    const cuuint64_t rb = static_cast<cuuint64_t>(cols) * esz;          // row pitch in bytes
     if (g->epi == kEpiSwigluFwd) {
       if (halves_f <= 0 || halves_f % 128 != 0) return false;
       const cuuint64_t hf = static_cast<cuuint64_t>(halves_f);
-      const cuuint64_t d[4] = {128, hf, static_cast<cuuint64_t>(a_rows) / hf, ks};
-      const cuuint64_t st[3] = {c, hf * c, 128};
-      const cuuint32_t bx[4] = {128, 64, 2, 2};
+      const cuuint64_t d[4] = {w, hf, static_cast<cuuint64_t>(a_rows) / hf, nch};
+      const cuuint64_t st[3] = {rb, hf * rb, 128};
+      const cuuint32_t bx[4] = {static_cast<cuuint32_t>(w), 64, 2, 2};
       if (!make_tmap_nd(&g->aux[0], dt, 4, a, d, st, bx, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
-      const cuuint64_t ft = hf / 128;
-      const cuuint64_t d4[4] = {128, ks, ft, static_cast<cuuint64_t>(a_rows) / hf};
-      const cuuint64_t st4[3] = {atom, ks * atom, ft * ks * atom};
-      const cuuint32_t bx4[4] = {128, 2, 1, 2};
-      if (!make_tmap_nd(&g->aux[2], CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, a_sf, d4, st4, bx4,
-                        CU_TENSOR_MAP_SWIZZLE_NONE))
-        return false;
+      if (mx) {
+        const cuuint64_t ft = hf / 128;
+        const cuuint64_t d4[4] = {128, ks, ft, static_cast<cuuint64_t>(a_rows) / hf};
+        const cuuint64_t st4[3] = {atom, ks * atom, ft * ks * atom};
+        const cuuint32_t bx4[4] = {128, 2, 1, 2};
+        if (!make_tmap_nd(&g->aux[2], CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, a_sf, d4, st4, bx4,
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
+          return false;
+      }
     } else {
-      const cuuint64_t d[3] = {128, static_cast<cuuint64_t>(a_rows), ks};
-      const cuuint64_t st[2] = {c, 128};
-      const cuuint32_t bx[3] = {128, 128, 2};
+      const cuuint64_t d[3] = {w, static_cast<cuuint64_t>(a_rows), nch};
+      const cuuint64_t st[2] = {rb, 128};
+      const cuuint32_t bx[3] = {static_cast<cuuint32_t>(w), 128, 2};
       if (!make_tmap_nd(&g->aux[0], dt, 3, a, d, st, bx, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
     }
-    const cuuint64_t d[3] = {128, static_cast<cuuint64_t>(b_rows), ks};
-    const cuuint64_t st[2] = {c, 128};
-    const cuuint32_t bx[3] = {128, 128, 2};
+    const cuuint64_t d[3] = {w, static_cast<cuuint64_t>(b_rows), nch};
+    const cuuint64_t st[2] = {rb, 128};
+    const cuuint32_t bx[3] = {static_cast<cuuint32_t>(w), 128, 2};
     if (!make_tmap_nd(&g->aux[1], dt, 3, b, d, st, bx, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
     g->p.a_pair_box = 0;
     g->p.b_full_box = 0;

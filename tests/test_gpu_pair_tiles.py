@@ -92,8 +92,8 @@ def test_pairs_inference_and_clamped_swiglu():
 
 
 # ---------------------------------------------------------------- CTA pairs
-# Mode 3: the MXFP8 forward's pair tiles on clusters of two CTAs, one
-# 256 x 256 block-scaled MMA (cta_group::2) per K step over both: each CTA
+# Mode 3: the forward's pair tiles on clusters of two CTAs, one 256 x 256
+# MMA (cta_group::2; block-scaled in MXFP8) per K step over both: each CTA
 # holds its own 128 weight rows (SwiGLU: 64 gate + 64 up rows of its own 64
 # features) and one routing block of the pair, and drains its own 128
 # accumulator lanes; a stage is two 128-element K-chunks.  The contraction
@@ -109,6 +109,9 @@ CTA_CASES = {
     # phases wrap within a tile), two W2 cluster tiles along the features
     "mx_deep": lambda: synth.Workload("pair_deep", 600, 1024, 512, 4, 2, "mxfp8", "zipf", inactive_frac=0.05,
                                       zipf_s=0.8, seed=85),
+    # BF16: 128-value stages (eight per W13 tile), two accumulator buffers
+    "bf16_deep": lambda: synth.Workload("pair_bf16_deep", 600, 1024, 512, 4, 2, "bf16", "zipf",
+                                        inactive_frac=0.05, zipf_s=0.8, seed=86),
 }
 
 
@@ -142,12 +145,13 @@ def test_cta_pairs_inference_and_clamped_swiglu():
     assert list(res[0][1]) == list(res[1][1]) and res[0][1][0] > 0
 
 
-@pytest.mark.parametrize("D,F", [(384, 256), (512, 384)])
-def test_cta_pairs_fall_back_where_k_is_not_a_multiple_of_256(D, F):
-    """A CTA pair's stage is 256 elements of K and its W2 tile 256 features:
-    W13 (K = D) and W2 (K = F, 256-feature tiles of D) that do not divide
-    take one-CTA pair tiles instead, with the same bits."""
-    w = synth.Workload("pair_fallback", 300, D, F, 3, 2, "mxfp8", "uniform", seed=84)
+@pytest.mark.parametrize("prec,D,F", [("mxfp8", 384, 256), ("mxfp8", 512, 384), ("bf16", 384, 256)])
+def test_cta_pairs_fall_back_where_k_does_not_divide(prec, D, F):
+    """A CTA pair's stage is 256 bytes of K (256 MXFP8 or 128 BF16 values) and
+    its W2 tile 256 features: W13 (K = D) and W2 (K = F, 256-feature tiles of
+    D) that do not divide take one-CTA pair tiles instead, with the same
+    bits (BF16, D = 384: W13 on CTA pairs, W2 not)."""
+    w = synth.Workload("pair_fallback", 300, D, F, 3, 2, prec, "uniform", seed=84)
     case = Case(w)
     a = run_gpu(case, training=False, tile_mode=1)
     b = run_gpu(case, training=False, tile_mode=3)
