@@ -115,10 +115,11 @@ CTA_CASES = {
 }
 
 
-@pytest.mark.parametrize("max_ctas", [0, 6])
+@pytest.mark.parametrize("max_ctas", [0, 1, 6])
 @pytest.mark.parametrize("name", list(CTA_CASES))
 def test_cta_pairs_equal_row_blocks_bitwise(name, max_ctas):
-    """max_ctas = 6 (three clusters) makes every cluster walk many tiles."""
+    """max_ctas = 6 (three clusters) makes every cluster walk many tiles;
+    max_ctas = 1 still launches one cluster of two, which walks them all."""
     w = CTA_CASES[name]()
     case = Case(w)
     a = run_gpu(case, tile_mode=1, max_ctas=max_ctas)
