@@ -68,8 +68,8 @@ MOE_API moe_status moe_ctx_test_fused_stall(moe_ctx* ctx, int stall, int64_t wai
  * the pair; a GEMM whose K is not a multiple of 256 bytes, or W2 where
  * d_model is not a multiple of 256, takes mode 2's tiles; the backward as
  * mode 2); mode 0 (the default) takes CTA pairs for the forward when
- * max_tokens * top_k >= 256 * num_experts, and in BF16 pairs elsewhere when
- * max_tokens * top_k >= 128 * num_experts.
+ * max_tokens * top_k >= 192 * num_experts in MXFP8 or >= 128 * num_experts
+ * in BF16, and in BF16 pairs for the backward from the same density.
  * All give the same results bit for bit, and a forward and its backward
  * may run in different modes (both read the same saved state).  Applies to
  * later calls; no device access. */

@@ -33,8 +33,8 @@ struct moe_ctx {
   // average (max_tokens * top_k >= 128 E); moe_ctx_test_tile_mode overrides it
   bool pair_tiles_auto = false;
   // the forward's GEMMs over row-block pairs on CTA pairs, chosen at creation
-  // when experts hold two or more full row blocks on average (max_tokens *
-  // top_k >= 256 E); moe_ctx_test_tile_mode overrides it
+  // when the capacity gives the experts 192 (MXFP8) or 128 (BF16) routes on
+  // average; moe_ctx_test_tile_mode overrides it
   bool cta_pairs_auto = false;
   int tile_mode = 0;               // 0: automatic, 1: row blocks, 2: pairs, 3: pairs on CTA pairs
   long long fused_wait = 0;        // counter-wait limit of the single-launch forward (0: default)
@@ -567,9 +567,13 @@ moe_status moe_ctx_create(const moe_config* cfg, moe_ctx** out) {
   // loads, measured no faster than two row-block tiles
   c->pair_tiles_auto = cfg->precision == MOE_BF16 &&
                        static_cast<int64_t>(cfg->max_tokens) * cfg->top_k >= 128LL * cfg->num_experts;
-  // dense enough for full pairs: CTA pairs (one 256 x 256 MMA over two SMs,
-  // each loading half the operands, in two-K-chunk stages)
-  c->cta_pairs_auto = static_cast<int64_t>(cfg->max_tokens) * cfg->top_k >= 256LL * cfg->num_experts;
+  // dense enough for pairs: CTA pairs (one 256 x 256 MMA over two SMs, each
+  // loading half the operands, in two-K-chunk stages).  Measured against row
+  // blocks in MXFP8 (E = 128 / 96 / 64 / 48 at T = 2048, K = 6, D = 7168:
+  // -10 / -4 / +18 / +2 %; a lone block costs a pair twice the SM time) and
+  // against one-CTA pairs in BF16 (128 and 192 routes per expert: +2, +6 %).
+  c->cta_pairs_auto = static_cast<int64_t>(cfg->max_tokens) * cfg->top_k >=
+                      (cfg->precision == MOE_MXFP8 ? 192LL : 128LL) * cfg->num_experts;
   const ScratchLayout L = scratch_layout(cfg);
   c->bytes = L.total;
   if (cudaMalloc(&c->base, c->bytes) != cudaSuccess) {
