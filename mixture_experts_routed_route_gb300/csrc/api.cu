@@ -884,8 +884,11 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   g1.na = 1;   // the SwiGLU-backward epilogue needs two accumulator buffers
   g1.epi = kEpiSwigluBwd;
   // over row-block pairs in BF16 only: a 256-wide MXFP8 accumulator is
-  // single-buffered, and this epilogue reads it to the end of its work
-  g1.mode = (use_pairs(ctx) && !mx) ? kGroupedMP : kGroupedM;
+  // single-buffered, and this epilogue reads it to the end of its work.
+  // BF16 contexts whose forward runs on CTA pairs run this GEMM on them too
+  // (256-feature cluster tiles).
+  const bool cta1 = !mx && forward_tiles(ctx) == kGroupedMC && F % 256 == 0;
+  g1.mode = cta1 ? kGroupedMC : ((use_pairs(ctx) && !mx) ? kGroupedMP : kGroupedM);
   // MXFP8 weights prepared without transposed codes: A is W2's forward codes
   // [E*D rows (K), F columns (M)], read MN-major
   const bool mn2 = mx && W2->data_t == nullptr;
@@ -902,7 +905,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p1.poffsets = rp.poffsets;
   p1.E = E;
   p1.b_box_rows = 32;
-  p1.n_tiles = F / (128 * g1.na);
+  p1.n_tiles = F / (cta1 ? 256 : 128 * g1.na);
   p1.K = D;
   p1.a_rows_per_expert = F;
   p1.sfa = W2->scale_t;
@@ -965,10 +968,12 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   // ---- W13 DGRAD: dxr = dh1 W13[e]
   GemmLaunch g3{};
   const bool pairs3 = use_pairs(ctx);
+  // BF16 on CTA pairs as its forward (256-feature cluster tiles of D)
+  const bool cta3 = !mx && forward_tiles(ctx) == kGroupedMC && D % 256 == 0;
   g3.mx = mx;
-  g3.na = pairs3 ? 1 : pair_tiles(D);
+  g3.na = (pairs3 || cta3) ? 1 : pair_tiles(D);
   g3.epi = kEpiStore;
-  g3.mode = pairs3 ? kGroupedMP : kGroupedM;
+  g3.mode = cta3 ? kGroupedMC : (pairs3 ? kGroupedMP : kGroupedM);
   // MXFP8 without transposed codes: A is W13's forward codes [E*2F rows (K),
   // D columns (M)], read MN-major, one box per 128-column weight tile
   const bool mn13 = mx && W13->data_t == nullptr;
@@ -988,7 +993,7 @@ moe_status moe_backward(moe_ctx* ctx, const void* saved, const void* dout, const
   p3.poffsets = rp.poffsets;
   p3.E = E;
   p3.b_box_rows = 32;
-  p3.n_tiles = D / (128 * g3.na);
+  p3.n_tiles = D / (cta3 ? 256 : 128 * g3.na);
   p3.K = 2 * F;
   p3.a_rows_per_expert = D;
   p3.sfa = W13->scale_t;

@@ -763,6 +763,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, int num_sms, cudaStream_t stream) {
   MOE_GEMM_CASE(true, 1, kEpiSwigluFwd, kGroupedMC)
   MOE_GEMM_CASE(false, 1, kEpiStore, kGroupedMC)
   MOE_GEMM_CASE(true, 1, kEpiStore, kGroupedMC)
+  MOE_GEMM_CASE(false, 1, kEpiSwigluBwd, kGroupedMC)
   if (g.epi == kEpiWgrad && g.mode == kGroupedK &&
       (g.p.tma_store == kDwStoreF32 || g.p.tma_store == kDwAddF32))
     return g.mx ? launch_impl<true, 1, kEpiWgrad, kGroupedK, true>(g, num_sms, stream)
