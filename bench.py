@@ -804,10 +804,14 @@ def run_reference(args, rank, world):
     dy = synth.make_grad_out(w, "cpu")
     experts = pick_sample_experts(w, ids, args.cpu_sample_experts)
     w13s, w2s = synth.make_weights(w, "cpu", experts=experts)
-    for _ in range(min(args.warmup, 1)):
+    # at most 3 warm-up and 5 timed samples (a few seconds each), so the arm
+    # ends within about a minute whatever --steps / --warmup ask; the line
+    # reports the counts it ran
+    warm = max(0, min(args.warmup, 3))
+    for _ in range(warm):
         cpu_sample(w, ids, scores, x, dy, w13s, w2s, experts)
     times, fl = [], 0.0
-    steps = max(1, min(args.steps, 3))
+    steps = max(1, min(args.steps, 5))
     for _ in range(steps):
         dt, fl, sroutes = cpu_sample(w, ids, scores, x, dy, w13s, w2s, experts)
         times.append(dt)
@@ -815,7 +819,7 @@ def run_reference(args, rank, world):
     val = fl / dt / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": world,
-        "steps": steps, "warmup": min(args.warmup, 1), "ms_per_step": round(dt * 1e3, 1), "higher_is_better": True,
+        "steps": steps, "warmup": warm, "ms_per_step": round(dt * 1e3, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "K": w.K, "train": w.train},
         "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": blas_threads(),
