@@ -1,6 +1,7 @@
 """Grouped GEMMs over row-block pairs (B operands of two consecutive routing
-blocks of one expert, up to 256 rows) against the same GEMMs over single
-row blocks, and against the oracle.
+blocks of one expert, up to 256 rows), on one CTA or on CTA pairs (clusters
+of two sharing one 256 x 256 MMA), against the same GEMMs over single row
+blocks, and against the oracle.
 
 The two tilings contract every output element over the same K order, so the
 forward output, the input gradient, both weight gradients and the score
