@@ -139,17 +139,21 @@ def stage_bytes(w, rows_padded, routes, precision, train, experts_used=None, dw_
     rows_padded = sum of expert row counts padded to 32; routes = active
     routes; experts_used = experts with at least one route (the GEMMs read
     only their weights; the weight gradients write dW of every expert).
-    MXFP8 operands cost 1 + 1/32 bytes per element (E4M3 + E8M0).
+    MXFP8 operands cost 1 + 1/32 bytes per element (E4M3 + E8M0), NVFP4
+    operands 9/16 (E2M1 + one E4M3 scale per 16; inference only: its W13
+    stage also writes the FP32 h2 and its quantisation reads it back).
     dw_bytes = bytes moved per weight-gradient element: 2 (BF16 written),
     4 (FP32 written), 8 (FP32 read and written back when accumulating)."""
     T, D, F, E = w.T, w.D, w.F, w.E
     Eu = w.E if experts_used is None else experts_used
-    q = (1 + 1 / 32) if precision == "mxfp8" else 2.0
+    q = {"mxfp8": 1 + 1 / 32, "nvfp4": 9 / 16}.get(precision, 2.0)
     Rp, R = rows_padded, routes
+    h2_f32 = Rp * F * 8 if precision == "nvfp4" else 0
     fwd = {
         "route": T * w.K * 8 + (Rp + 2 * T * w.K) * 4,
         "gather_x": T * D * 2 + Rp * D * q * (2 if train else 1),
-        "gemm_w13_swiglu": Eu * 2 * F * D * q + Rp * D * q + Rp * F * q + (Rp * 2 * F * 2 + Rp * F * q if train else 0),
+        "gemm_w13_swiglu": Eu * 2 * F * D * q + Rp * D * q + Rp * F * q + h2_f32
+                           + (Rp * 2 * F * 2 + Rp * F * q if train else 0),
         "gemm_w2": Eu * D * F * q + Rp * F * q + Rp * D * 2,
         "combine": R * D * 2 + T * D * 2 * 2,
     }
@@ -555,6 +559,7 @@ def run_ours(args, rank, world):
         sbytes = {"fused_forward": sum(fb.values())}
     dom = max(stage_ms, key=lambda k: stage_ms[k])
     fp8_peak = pk["bf16_tflops"] * 2.0
+    # NVFP4 operands reach the tensor cores as FP16 (kind::f16): the 16-bit peak
     peak_t = fp8_peak if w.precision == "mxfp8" else pk["bf16_tflops"]
     roof = roofline(dom, stage_ms[dom], sbytes[dom], routes, w, pk, peak_t, traffic_record(dom, w.name))
     stages = {k: {"ms": round(v, 4), "GB/s": round(sbytes[k] / (v * 1e-3) / 1e9, 1) if v > 0 else None}

@@ -73,7 +73,17 @@ typedef enum {
  * Open-Source Fused MoE Kernels for Blackwell", "Supported modes": 32x32
  * blocks for training-compatible values, 1x32 for inference).  Such a
  * weight feeds moe_forward of an MXFP8 context; moe_backward rejects it. */
-typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_MXFP8_1X32 = 2 } moe_precision;
+/* MOE_NVFP4 is an inference precision ([DM] section 02, "Expert
+ * Computation and Tensor Precision": E2M1 values with E4M3 block scales and
+ * a global scale per row; section 08, "Public API and Supported Modes":
+ * NVFP4 inference with prepared weights): a context of this precision takes
+ * no MOE_TRAINING, MOE_REPLAY or MOE_POST_NORM flag (MOE_ERR_UNSUPPORTED)
+ * and its moe_forward runs without `saved` and without MOE_FUSED_LAUNCH.
+ * Weights, x rows and h2 rows are quantised along K in blocks of 16 values:
+ * g = amax(row) / 2688, sb = E4M3(amax(block) / (6 g)), q = E2M1(v / (sb g)),
+ * each step one FP32 operation rounded to nearest even (E4M3 and E2M1
+ * saturate); h1 and h3 are rounded to BF16 as in the other precisions. */
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_MXFP8_1X32 = 2, MOE_NVFP4 = 3 } moe_precision;
 
 /* moe_config.flags */
 #define MOE_TRAINING      0x1u  /* forward saves state; backward is allowed   */
@@ -110,6 +120,9 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_MXFP8_1X32 = 2 } moe_precision;
  *   MXFP8: E4M3 operands with one E8M0 scale per 32 values along the
  *          contraction axis ([DM] section 02, "Block-Scaled Quantization"),
  *          FP32 accumulation, BF16 h1/h3.
+ *   NVFP4: (inference) E2M1 operands with E4M3 scales per 16 values and an
+ *          FP32 scale per row (see moe_precision), FP32 accumulation of the
+ *          scaled codes, BF16 h1/h3; h2 formed in FP32, then quantised.
  */
 typedef struct {
   int32_t max_tokens;     /* T_max: largest T any call will pass            */
@@ -117,7 +130,7 @@ typedef struct {
   int32_t d_ff;           /* F (h1 has 2F columns: gate then up)            */
   int32_t num_experts;    /* E                                              */
   int32_t top_k;          /* K routes per token                             */
-  moe_precision precision; /* MOE_BF16 or MOE_MXFP8                         */
+  moe_precision precision; /* MOE_BF16, MOE_MXFP8 or MOE_NVFP4 (inference)  */
   uint32_t flags;         /* MOE_TRAINING | MOE_DEBUG_CHECKS                */
   float swiglu_limit;     /* 0: plain SwiGLU.  L > 0: clamped SwiGLU ("Meta
                            * Dist-MoE...", "Supported modes"), h2 =
@@ -143,6 +156,12 @@ typedef struct {
  *        which saves E*N*K bytes; with data_t they read the K-major copy.
  *        Both give the same results.  Atoms: E*N*K/32 bytes, see below.
  *        N % 128 == 0 and K % 128 == 0.  Filled by prepare_block_scaled_weight.
+ * NVFP4: data = chunks of 128 rows x 64 values (4096 bytes of E2M1 codes, row
+ *        m at byte 32 m, value k in byte k/2, low nibble for even k; then
+ *        512 bytes of E4M3 block scales, row m's four at 4096 + 4 m), the
+ *        chunk of rows 128 t .. 128 t + 127 of the stacked [E*N, K] weight
+ *        and values 64 s .. 64 s + 63 at (t * K/64 + s) * 4608;
+ *        scale = FP32 row scales g [E*N]; data_t = scale_t = NULL.
  * The struct is read on the host at call time; the pointers are not owned.
  */
 typedef struct {
@@ -267,6 +286,10 @@ MOE_API int64_t moe_row_capacity(const moe_config* cfg);
  *           Use the result with moe_weight.precision = MOE_MXFP8_1X32.
  *   BF16:   data and scale must be NULL; data_t (BF16 [E,K,N]) receives the
  *           transpose used by the input-gradient GEMMs.
+ *   NVFP4:  inference weights (the quantiser of MOE_NVFP4, blocks of 16
+ *           along K, one row scale per weight row): codes and block scales
+ *           to data, FP32 row scales to scale (see moe_weight); data_t and
+ *           scale_t must be NULL; N % 128 == 0 and K % 64 == 0.
  * The outputs are caller-owned device buffers.  Enqueued on `stream`.
  */
 /*
@@ -282,6 +305,9 @@ MOE_API int64_t moe_row_capacity(const moe_config* cfg);
  *                      and K % 128 == 0.
  *   BF16:              data E*N*K*2 (the caller's own tensor, which the
  *                      layer reads in place), data_t E*K*N*2.
+ *   NVFP4:             data E*N*K*9/16 (codes and block scales), scale
+ *                      E*N*4 (row scales); N % 128 == 0, K % 64 == 0,
+ *                      with_transpose 0.
  * Host-only, no CUDA call.  Errors: MOE_ERR_INVALID_ARG (null bytes, shapes
  * prepare_block_scaled_weight rejects, with_transpose for MXFP8_1X32).
  */

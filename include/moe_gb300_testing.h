@@ -24,10 +24,14 @@ MOE_API moe_status moe_debug_copy_to_host(void* host_dst, const void* dev_src, s
 /* Scratch regions of a context, for inspection by tests.  Sizes follow
  * R_cap (moe_row_capacity) and B_cap = (T_max*K + 31*E)/128 + E + 1. */
 typedef enum {
-  MOE_BUF_XROW = 0,        /* gathered x row bundle: bf16 [R_cap, D] or e4m3  */
-  MOE_BUF_XROW_SCALE = 1,  /* e8m0 row-bundle atoms [B_cap][D/128]             */
-  MOE_BUF_H2ROW = 2,       /* h2 row bundle: bf16 [R_cap, F] or e4m3           */
-  MOE_BUF_H2ROW_SCALE = 3, /* e8m0 row-bundle atoms [B_cap][F/128]             */
+  MOE_BUF_XROW = 0,        /* gathered x row bundle: bf16 [R_cap, D] or e4m3
+                              (MOE_NVFP4: chunks [B_cap][D/64] of 4608 bytes)  */
+  MOE_BUF_XROW_SCALE = 1,  /* e8m0 row-bundle atoms [B_cap][D/128]
+                              (MOE_NVFP4: FP32 row scales [R_cap])             */
+  MOE_BUF_H2ROW = 2,       /* h2 row bundle: bf16 [R_cap, F] or e4m3
+                              (MOE_NVFP4: chunks [B_cap][F/64])                */
+  MOE_BUF_H2ROW_SCALE = 3, /* e8m0 row-bundle atoms [B_cap][F/128]
+                              (MOE_NVFP4: FP32 row scales [R_cap])             */
   MOE_BUF_H3 = 4,          /* bf16 [R_cap, D]                                  */
   MOE_BUF_DH3ROW = 5,      /* bf16 [R_cap, D] or e4m3                          */
   MOE_BUF_DH3ROW_SCALE = 6,/* e8m0 row-bundle atoms [B_cap][D/128]            */
@@ -46,7 +50,8 @@ typedef enum {
                               a backward with MOE_REPLAY_FORWARD rebuilds       */
   MOE_BUF_SYNC = 18,       /* int32 counters of the single-launch forward:
                               3 + 2*B_cap words, zero between launches          */
-  MOE_BUF_NUM = 19
+  MOE_BUF_H2F = 19,        /* MOE_NVFP4: FP32 h2 [R_cap, F] (then quantised)   */
+  MOE_BUF_NUM = 20
 } moe_buffer;
 
 MOE_API moe_status moe_ctx_buffer(moe_ctx* ctx, int which, void** dev_ptr, size_t* bytes);

@@ -31,6 +31,7 @@ MOE_DEV_ERR_TIMEOUT = 0x4
 MOE_BF16 = 0
 MOE_MXFP8 = 1
 MOE_MXFP8_1X32 = 2    # weight preparation only: 1x32 inference blocks
+MOE_NVFP4 = 3         # inference only: E2M1 values, E4M3 1x16 block scales, FP32 row scales
 
 MOE_TRAINING = 0x1
 MOE_DEBUG_CHECKS = 0x2
@@ -55,8 +56,8 @@ MOE_SAVED_NUM_FIELDS = 18
 (MOE_BUF_XROW, MOE_BUF_XROW_SCALE, MOE_BUF_H2ROW, MOE_BUF_H2ROW_SCALE, MOE_BUF_H3, MOE_BUF_DH3ROW,
  MOE_BUF_DH3ROW_SCALE, MOE_BUF_DH3COL, MOE_BUF_DH3COL_SCALE, MOE_BUF_DH1ROW, MOE_BUF_DH1ROW_SCALE,
  MOE_BUF_DH1COL, MOE_BUF_DH1COL_SCALE, MOE_BUF_DXR, MOE_BUF_ROUTING, MOE_BUF_ERROR, MOE_BUF_NORM,
- MOE_BUF_REPLAY, MOE_BUF_SYNC) = range(19)
-MOE_BUF_NUM = 19
+ MOE_BUF_REPLAY, MOE_BUF_SYNC, MOE_BUF_H2F) = range(20)
+MOE_BUF_NUM = 20
 
 
 class moe_config(ctypes.Structure):

@@ -68,7 +68,7 @@ bool config_ok(const moe_config* c) {
   if (c->max_tokens < 1 || c->top_k < 1 || c->top_k > 32) return false;
   if (c->num_experts < 1 || c->num_experts > 1024) return false;
   if (c->d_model < 128 || c->d_ff < 128) return false;
-  if (c->precision != MOE_BF16 && c->precision != MOE_MXFP8) return false;
+  if (c->precision != MOE_BF16 && c->precision != MOE_MXFP8 && c->precision != MOE_NVFP4) return false;
   if (!(c->swiglu_limit >= 0.0f) || c->swiglu_limit > 3.0e38f) return false;   // also rejects NaN
   const int64_t routes = static_cast<int64_t>(c->max_tokens) * c->top_k;
   if (routes + 31LL * c->num_experts > (1LL << 28)) return false;
@@ -199,6 +199,15 @@ ScratchLayout scratch_layout(const moe_config* c) {
   sz[MOE_BUF_ROUTING] = saved_layout(c).routing_bytes;
   if (!train && mx) sz[MOE_BUF_SYNC] = (3 + 2 * B) * sizeof(int);   // single-launch forward counters
   sz[MOE_BUF_ERROR] = 32;   // error word at 0, clip counters at 16
+  if (c->precision == MOE_NVFP4) {
+    // inference only: chunks of the routing blocks' x and h2 rows with their
+    // FP32 row scales, and the FP32 h2 the W13 epilogue writes
+    sz[MOE_BUF_XROW] = nvfp4_chunk_bytes(B, static_cast<int>(D));
+    sz[MOE_BUF_XROW_SCALE] = R * sizeof(float);
+    sz[MOE_BUF_H2ROW] = nvfp4_chunk_bytes(B, static_cast<int>(F));
+    sz[MOE_BUF_H2ROW_SCALE] = R * sizeof(float);
+    sz[MOE_BUF_H2F] = R * F * sizeof(float);
+  }
   size_t off = 0;
   for (int i = 0; i < MOE_BUF_NUM; ++i) {
     L.off[i] = off;
@@ -247,7 +256,7 @@ bool weight_ok(const moe_weight* w, moe_precision prec, int E, int N, int K, boo
   const bool row32 = prec == MOE_MXFP8 && !need_t && w->precision == MOE_MXFP8_1X32;
   if (w->precision != prec && !row32) return false;
   if (!w->data || !aligned16(w->data)) return false;
-  if (prec == MOE_MXFP8 && (!w->scale || !aligned16(w->scale))) return false;
+  if ((prec == MOE_MXFP8 || prec == MOE_NVFP4) && (!w->scale || !aligned16(w->scale))) return false;
   if (need_t) {
     // MXFP8: the input-gradient scale atoms, and either the transposed codes
     // (a K-major input-gradient operand) or none (the GEMM reads the
@@ -413,6 +422,56 @@ moe_status run_w2(moe_ctx* ctx, const RoutingPtrs& rp, const moe_weight* W2, uin
   ctx->launches += 1;
   return MOE_OK;
 }
+// NVFP4 inference after routing (nvfp4.cu): the routed x rows quantised
+// into their routing blocks' chunks; the W13 + SwiGLU GEMM to FP32 h2 and
+// the h2 rows quantised (one stage); the W2 GEMM to BF16 h3.  Grids: one CTA
+// per SM at most, and no more than the tiles the token count allows.
+moe_status run_nvfp4(moe_ctx* ctx, int T, const void* x, const RoutingPtrs& rp, const moe_weight* W13,
+                     const moe_weight* W2, int sms, cudaStream_t stream) {
+  const moe_config& c = ctx->cfg;
+  const int D = c.d_model, F = c.d_ff, K = c.top_k;
+  const int R = static_cast<int>(ctx->r_cap);
+  float* gx = reinterpret_cast<float*>(B(ctx, MOE_BUF_XROW_SCALE));
+  float* gh = reinterpret_cast<float*>(B(ctx, MOE_BUF_H2ROW_SCALE));
+  MOE_TRY(launch_nvfp4_rows(false, x, D, K, rp, R, B(ctx, MOE_BUF_XROW), gx, sms, stream));
+  ctx->launches += 1;
+  MOE_TRY(stage_mark(ctx, 0, 2, stream));
+  const int64_t tk = static_cast<int64_t>(T) * K;
+  const int64_t max_blocks = tk / 128 + std::min<int64_t>(c.num_experts, tk) + 1;
+  Fp4GemmParams p{};
+  p.a = static_cast<const uint8_t*>(W13->data);
+  p.ga = reinterpret_cast<const float*>(W13->scale);
+  p.b = B(ctx, MOE_BUF_XROW);
+  p.gb = gx;
+  p.hdr = rp.hdr;
+  p.blocks = rp.blocks;
+  p.out = B(ctx, MOE_BUF_H2F);
+  p.ks = D / 64;
+  p.n_tiles = F / 128;
+  p.a_tiles_e = 2 * F / 128;
+  p.ld = F;
+  p.swiglu_limit = c.swiglu_limit;
+  p.clip = ctx->clip;
+  p.err = ctx->err;
+  MOE_TRY(launch_nvfp4_gemm(p, true, static_cast<int>(std::min<int64_t>(sms, max_blocks * p.n_tiles)), stream));
+  MOE_TRY(launch_nvfp4_rows(true, B(ctx, MOE_BUF_H2F), F, K, rp, R, B(ctx, MOE_BUF_H2ROW), gh, sms, stream));
+  ctx->launches += 2;
+  MOE_TRY(stage_mark(ctx, 0, 3, stream));
+  p.a = static_cast<const uint8_t*>(W2->data);
+  p.ga = reinterpret_cast<const float*>(W2->scale);
+  p.b = B(ctx, MOE_BUF_H2ROW);
+  p.gb = gh;
+  p.out = B(ctx, MOE_BUF_H3);
+  p.ks = F / 64;
+  p.n_tiles = D / 128;
+  p.a_tiles_e = D / 128;
+  p.ld = D;
+  p.clip = nullptr;
+  MOE_TRY(launch_nvfp4_gemm(p, false, static_cast<int>(std::min<int64_t>(sms, max_blocks * p.n_tiles)), stream));
+  ctx->launches += 1;
+  return MOE_OK;
+}
+
 // The whole inference forward as one launch (MOE_FUSED_LAUNCH): the same
 // tensor maps and GEMM parameters as the staged launches, and the counters
 // in the context's sync buffer.
@@ -553,6 +612,8 @@ moe_status moe_ctx_create(const moe_config* cfg, moe_ctx** out) {
   if (!out || !config_ok(cfg)) return MOE_ERR_INVALID_ARG;
   if ((cfg->flags & MOE_REPLAY) && !(cfg->flags & MOE_TRAINING)) return MOE_ERR_INVALID_ARG;
   if (!config_tileable(cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->precision == MOE_NVFP4 && (cfg->flags & (MOE_TRAINING | MOE_REPLAY | MOE_POST_NORM)))
+    return MOE_ERR_UNSUPPORTED;   // an inference format
   if (!encode_fn()) return MOE_ERR_CUDA;
   moe_ctx* c = new moe_ctx();
   c->cfg = *cfg;
@@ -723,6 +784,12 @@ moe_status moe_weight_bytes(moe_precision precision, int32_t E, int32_t N, int32
     }
     return MOE_OK;
   }
+  if (precision == MOE_NVFP4) {
+    if (N % 128 || K % 64 || with_transpose) return MOE_ERR_INVALID_ARG;
+    bytes[0] = nvfp4_chunk_bytes(static_cast<long long>(e * n / 128), K);
+    bytes[1] = e * n * sizeof(float);
+    return MOE_OK;
+  }
   if (precision == MOE_BF16) {
     if (with_transpose < 0 || with_transpose > 1) return MOE_ERR_INVALID_ARG;
     bytes[0] = e * n * k * 2;
@@ -746,6 +813,15 @@ moe_status prepare_block_scaled_weight(const void* w, int32_t E, int32_t N, int3
     if (data_t && !aligned16(data_t)) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_prep_mx_weight(w, E, N, K, static_cast<uint8_t*>(data), scale,
                                              static_cast<uint8_t*>(data_t), scale_t, stream));
+  }
+  if (precision == MOE_NVFP4) {
+    if (N % 128 || K % 64 || !data || !scale || !aligned16(data) || !aligned16(scale) || data_t || scale_t)
+      return MOE_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    MOE_TRY(cudaGetDevice(&dev));
+    MOE_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    return cuda_status(launch_nvfp4_prep_weight(w, E, N, K, static_cast<uint8_t*>(data), reinterpret_cast<float*>(scale),
+                                                sms, stream));
   }
   if (precision == MOE_BF16) {
     if (data || scale || scale_t || !data_t || !aligned16(data_t)) return MOE_ERR_INVALID_ARG;
@@ -777,6 +853,7 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   }
   const bool input_only = (call_flags & MOE_SAVE_INPUT_ONLY) != 0;
   if (input_only && (!train || !(c.flags & MOE_REPLAY))) return MOE_ERR_INVALID_ARG;
+  const bool nvfp4 = c.precision == MOE_NVFP4;   // inference only (no saved state, no single launch)
   if (T == 0) return MOE_OK;
   if (!x || !topk_ids || !topk_scores || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(out) || (saved && !aligned16(saved))) return MOE_ERR_INVALID_ARG;
@@ -810,9 +887,13 @@ moe_status moe_forward(moe_ctx* ctx, int32_t T, const void* x, const int32_t* to
   ctx->launches += 1;
   MOE_TRY(stage_mark(ctx, 0, 1, stream));
   uint8_t* act = (train && !input_only) ? sv : nullptr;   // where the expert state is saved
-  MOE_PASS(run_gather_w13(ctx, x, rp, W13, act, SL, true, sms, stream));
   uint8_t* h3 = act ? act + SL.off[MOE_SAVED_H3] : B(ctx, MOE_BUF_H3);   // saved for the score gradient
-  MOE_PASS(run_w2(ctx, rp, W2, h3, sms, stream));
+  if (nvfp4) {
+    MOE_PASS(run_nvfp4(ctx, T, x, rp, W13, W2, sms, stream));
+  } else {
+    MOE_PASS(run_gather_w13(ctx, x, rp, W13, act, SL, true, sms, stream));
+    MOE_PASS(run_w2(ctx, rp, W2, h3, sms, stream));
+  }
   MOE_TRY(stage_mark(ctx, 0, 4, stream));
 
   // ---- combine

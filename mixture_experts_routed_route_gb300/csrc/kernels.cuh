@@ -116,6 +116,46 @@ cudaError_t launch_prep_mx_weight_row32(const void* w, int E, int N, int K, uint
                                         cudaStream_t stream);
 cudaError_t launch_transpose_bf16(const void* w, int E, int N, int K, void* wT, cudaStream_t stream);
 
+// ------------------------------------------------------------------ NVFP4
+// (nvfp4.cu: format, chunk layout and GEMM design.)  Chunks are 128 rows x
+// 64 values of one operand: 4096 code bytes, then 512 block-scale bytes.
+
+// Bytes of the chunks of `row_tiles` 128-row tiles with K values per row.
+size_t nvfp4_chunk_bytes(long long row_tiles, int K);
+
+// Weight [E, N, K] BF16 -> chunks of its row tiles and FP32 row scales g
+// [E*N]; N % 128 == 0, K % 64 == 0.
+cudaError_t launch_nvfp4_prep_weight(const void* w, int E, int N, int K, uint8_t* chunks, float* g, int num_sms,
+                                     cudaStream_t stream);
+
+// Routed rows r < hdr[2] -> chunks of their routing blocks and g [r_cap]:
+// BF16 x[perm[r] / top_k] (zeros for pad rows) or, with f32_rows, the FP32
+// rows src[r] ([r_cap, K]).
+cudaError_t launch_nvfp4_rows(bool f32_rows, const void* src, int K, int top_k, const RoutingPtrs& rp, int r_cap,
+                              uint8_t* chunks, float* g, int num_sms, cudaStream_t stream);
+
+struct Fp4GemmParams {
+  const uint8_t* a;     // weight chunks
+  const float* ga;      // weight row scales [E * N]
+  const uint8_t* b;     // routed activation chunks (per routing block)
+  const float* gb;      // routed row scales [r_cap]
+  const int* hdr;       // routing header: hdr[1] routing blocks
+  const int4* blocks;   // (expert, first row, rows, -) per routing block
+  void* out;            // SwiGLU: FP32 h2 [r_cap, ld]; otherwise BF16 h3 [r_cap, ld]
+  int ks;               // K / 64 stages
+  int n_tiles;          // 128-wide output slices per routing block (F/128 or D/128)
+  int a_tiles_e;        // 128-row weight tiles per expert (2F/128 or D/128)
+  int ld;               // output row pitch in elements
+  float swiglu_limit;   // clamped SwiGLU (0: plain)
+  unsigned long long* clip;   // [2] clamped gate / up counts, or NULL
+  uint32_t* err;        // device error word
+};
+
+// Grouped-M GEMM over routing blocks x 128-feature slices; swiglu: W13 (gate
+// tile n and up tile n + F/128 of the block's expert) with the SwiGLU
+// epilogue, else W2 with the BF16 store.  `grid` persistent CTAs.
+cudaError_t launch_nvfp4_gemm(const Fp4GemmParams& p, bool swiglu, int grid, cudaStream_t stream);
+
 // ------------------------------------------------------------- grouped GEMM
 
 // kGroupedMP: grouped-M over row-block pairs (B up to 256 rows, one A tile

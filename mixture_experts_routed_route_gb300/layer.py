@@ -13,7 +13,7 @@ import torch
 
 from . import abi
 
-_DT = {"bf16": abi.MOE_BF16, "mxfp8": abi.MOE_MXFP8, "mxfp8_1x32": abi.MOE_MXFP8_1X32}
+_DT = {"bf16": abi.MOE_BF16, "mxfp8": abi.MOE_MXFP8, "mxfp8_1x32": abi.MOE_MXFP8_1X32, "nvfp4": abi.MOE_NVFP4}
 
 
 def precision_code(precision):
@@ -27,7 +27,9 @@ class PreparedWeight:
     [E, K, N] (for the input-gradient GEMMs).  MXFP8: E4M3 codes with one
     E8M0 scale per 32x32 tile, in both orientations (the transposed codes
     too unless mn_major).  "mxfp8_1x32": forward only, one scale per 1x32
-    block of a row along K."""
+    block of a row along K.  "nvfp4": inference only, E2M1 codes and E4M3
+    scales per 16 values along K in 128-row x 64-value chunks (``data``)
+    and one FP32 scale per row (``scale``)."""
 
     def __init__(self, w, precision, with_transpose=True, stream=None, mn_major=False):
         """mn_major (MXFP8 with_transpose): keep only the input-gradient scale
@@ -40,7 +42,12 @@ class PreparedWeight:
         self.shape = (E, N, K)
         dev = w.device
         self.data_t = self.scale = self.scale_t = None
-        if self.precision == abi.MOE_MXFP8_1X32:
+        if self.precision == abi.MOE_NVFP4:
+            nbytes = abi.moe_weight_bytes(self.precision, E, N, K, False)
+            self.data = torch.empty(nbytes[0], dtype=torch.uint8, device=dev)
+            self.scale = torch.empty(E * N, dtype=torch.float32, device=dev)
+            abi.prepare_block_scaled_weight(w, E, N, K, self.precision, self.data, self.scale, None, None, stream)
+        elif self.precision == abi.MOE_MXFP8_1X32:
             self.data = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
             self.scale = torch.empty(E * N * (K // 32) + 16, dtype=torch.uint8, device=dev)
             abi.prepare_block_scaled_weight(w, E, N, K, self.precision, self.data, self.scale, None, None, stream)

@@ -41,7 +41,7 @@ class Workload:
     F: int
     E: int
     K: int
-    precision: str            # "bf16" or "mxfp8"
+    precision: str            # "bf16", "mxfp8" or "nvfp4" (inference)
     routing: str              # "topk_logits", "uniform", "zipf"
     inactive_frac: float = 0.0
     zipf_s: float = 1.2
@@ -63,6 +63,9 @@ WORKLOADS = {
     "ten_layer_graph": Workload("ten_layer_graph", 4096, 7168, 2048, 384, 8, "mxfp8",
                                 "zipf", train=True, layers=10, seed=5),
     "e6_dense": Workload("e6_dense", 2048, 7168, 2048, 6, 6, "mxfp8", "uniform", seed=6),
+    # the e384 inference shape's routed layer with NVFP4 experts (inference
+    # only; no shared expert)
+    "e384_nvfp4": Workload("e384_nvfp4", 2048, 7168, 2048, 384, 6, "nvfp4", "uniform", seed=11),
     # profiling case: the e384 per-expert shape (about 32 rows per expert, D=7168,
     # F=2048) with 24 experts, so a full ncu capture holds a few GB, while the
     # weight gradients (1.4 GB for W13) still exceed L2

@@ -10,7 +10,11 @@ import torch
 
 from mixture_experts_routed_route_gb300 import synth
 
-TOL = {"bf16": 1e-2, "mxfp8": 3e-2}   # max|gpu - ref| / max|ref|
+# max|gpu - ref| / max|ref|.  NVFP4 takes the MXFP8 bound: both sides
+# quantise the same FP32 values with the same FP32 steps, so the operands are
+# the same codes except where the two accumulation orders move an FP32 value
+# across a rounding boundary.
+TOL = {"bf16": 1e-2, "mxfp8": 3e-2, "nvfp4": 3e-2}
 
 
 def rel_err(got, ref):

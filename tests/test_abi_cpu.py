@@ -132,6 +132,31 @@ def test_weight_bytes_without_gpu(lib):
         assert ei.value.status == abi.MOE_ERR_INVALID_ARG
 
 
+def test_nvfp4_host_side_checks_without_gpu(lib):
+    """NVFP4: weight sizes (codes and block scales 9/16 byte per value, one
+    FP32 scale per row), an inference-only context, no transposed weights."""
+    from mixture_experts_routed_route_gb300 import abi
+    E, N, K = 6, 256, 384
+    assert abi.moe_weight_bytes(abi.MOE_NVFP4, E, N, K, False) == (E * N * K * 9 // 16, E * N * 4, 0, 0)
+    assert abi.moe_weight_bytes(abi.MOE_NVFP4, 1, 128, 64, False) == (4608, 512, 0, 0)   # one chunk
+    for bad in ((abi.MOE_NVFP4, E, N, K, True),         # no backward orientation
+                (abi.MOE_NVFP4, E, 96, K, False),       # 128-row chunks
+                (abi.MOE_NVFP4, E, N, 96, False)):      # 64-value chunks
+        with pytest.raises(abi.MoEError) as ei:
+            abi.moe_weight_bytes(*bad)
+        assert ei.value.status == abi.MOE_ERR_INVALID_ARG
+    cfg = abi.make_config(2048, 7168, 2048, 384, 6, abi.MOE_NVFP4, 0)
+    assert abi.moe_row_capacity(cfg) > 0 and abi.moe_ctx_scratch_bytes(cfg) > 0
+    for flags in (abi.MOE_TRAINING, abi.MOE_TRAINING | abi.MOE_REPLAY, abi.MOE_POST_NORM):
+        with pytest.raises(abi.MoEError) as ei:
+            abi.moe_ctx_create(abi.make_config(2048, 7168, 2048, 384, 6, abi.MOE_NVFP4, flags))
+        assert ei.value.status == abi.MOE_ERR_UNSUPPORTED
+    # transposed outputs are rejected before any device work
+    fake = ctypes.c_void_p(256)
+    st = abi.LIB.prepare_block_scaled_weight(fake, E, N, K, abi.MOE_NVFP4, fake, fake, fake, None, None)
+    assert st == abi.MOE_ERR_INVALID_ARG
+
+
 def test_binding_constants_match_the_header():
     """Every #define and enum value of the header that the binding restates
     has the same value there (the binding is written by hand)."""
