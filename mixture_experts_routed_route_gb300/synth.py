@@ -78,6 +78,9 @@ WORKLOADS = {
     # profiling case for the row-sized kernels (gathers, combine): the e384
     # token count and width (T=2048, D=7168, K=6, so about 12 K routed rows)
     # with 32 experts, about 10 GB on the device
+    # profiling case of the NVFP4 GEMMs: the e384 token count and widths with
+    # 32 experts (about 3 routing blocks each), about 1 GB of NVFP4 weights
+    "profile_e32_nvfp4": Workload("profile_e32_nvfp4", 2048, 7168, 2048, 32, 6, "nvfp4", "uniform", seed=12),
     "profile_e32": Workload("profile_e32", 2048, 7168, 2048, 32, 6, "mxfp8", "zipf", inactive_frac=0.10,
                             zipf_s=1.2, train=True, seed=8),
 }
