@@ -11,7 +11,7 @@ from mixture_experts_routed_route_gb300 import synth
 from oracle import formats as fm
 from oracle import moe as omoe
 
-from moe_cases import (TOL, Case, rel_err, run_gpu, run_oracle, saved_blocks, to_f64, unpack_row_sf,
+from moe_cases import (TOL, Case, rel_err, run_gpu, run_oracle, saved_blocks, to_f64, unpack_col_sf, unpack_row_sf,
                         unpack_weight_sf)
 
 pytestmark = pytest.mark.gpu
@@ -74,6 +74,17 @@ def test_forward_stages(name):
         q, e = fm.mx_quantize(st["xg"], axis=-1)
         np.testing.assert_array_equal(fm.e4m3_decode(xr), q)
         np.testing.assert_array_equal(xs.astype(np.int64) - 127, e)
+        # the column bundle the same pass writes (the W13 weight gradient's
+        # operand): 32-row blocks from each expert's first row
+        sv = g["saved"].cpu().numpy()
+        off, nb = abi.moe_saved_state_field(layer.cfg, abi.MOE_SAVED_XCOL)
+        xc = sv[off:off + D * layer.r_cap].reshape(D, layer.r_cap)[:, :rows]
+        off, nb = abi.moe_saved_state_field(layer.cfg, abi.MOE_SAVED_XCOL_SCALE)
+        b_cap = nb // ((D // 128) * 512)
+        cs = unpack_col_sf(sv[off:off + nb], saved_blocks(layer, g["saved"]), D, rows, b_cap)
+        q, e = fm.mx_quantize(st["xg"], axis=0)
+        np.testing.assert_array_equal(fm.e4m3_decode(xc).T, q)
+        np.testing.assert_array_equal(cs.astype(np.int64).T - 127, e)
     # h1 (saved, BF16) within half a BF16 ulp plus the FP32 accumulation bound
     # of the exact product of the same quantised operands
     h1 = layer.saved_field(g["saved"], abi.MOE_SAVED_H1, torch.bfloat16, (layer.r_cap, 2 * F))
