@@ -250,46 +250,6 @@ __device__ __forceinline__ float amax32(const float (&v)[32]) {
   return a;
 }
 
-// Packed BF16 arithmetic on the raw row words, two values per instruction,
-// where it gives the FP32 path's codes exactly:
-//  * the block maximum: max(|a|, |b|) per half (the result's sign is the
-//    XOR of the inputs' and is masked off); a BF16 maximum is exact;
-//  * the power-of-two scaling v * 2^-e: exact in BF16 (same exponent range
-//    as FP32) while the result stays normal.  With the block maximum at
-//    least 2^-100 (|2^-e| <= 2^108), a value whose product or input is
-//    subnormal is below 2^-18 after scaling and gets code 0 either way,
-//    whether or not the BF16 unit flushes it.
-// Smaller maxima take the FP32 path.
-constexpr float kPackedMinAmax = 7.888609052210118e-31f;   // 2^-100
-
-__device__ __forceinline__ uint32_t bmax2_abs(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-// Per-half maximum magnitude of 16 words (32 BF16 values, even values in the
-// low halves), as a BF16 pair with clear sign bits.
-__device__ __forceinline__ uint32_t bmax16(const uint32_t (&w)[16]) {
-  uint32_t m[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = bmax2_abs(w[2 * i], w[2 * i + 1]);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) m[i] = bmax2_abs(m[i], m[i + 4]);
-  m[0] = bmax2_abs(m[0], m[2]);
-  m[1] = bmax2_abs(m[1], m[3]);
-  return bmax2_abs(m[0], m[1]) & 0x7FFF7FFFu;
-}
-
-// 2^-e as a BF16 value in the low half (e in [-127, 120]).
-__device__ __forceinline__ uint32_t bf16_exp2_neg(int e) { return static_cast<uint32_t>(127 - e) << 7; }
-
 template <bool SCALE>
 __global__ void __launch_bounds__(256, 3) gather_both_mx_kernel(const __grid_constant__ CUtensorMap tm_row,
                                                                 const __grid_constant__ CUtensorMap tm_col,
@@ -343,53 +303,24 @@ __global__ void __launch_bounds__(256, 3) gather_both_mx_kernel(const __grid_con
     sword = 0;
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
-      uint32_t ww[16];
+      float v[32];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint4 w4 = u[4 * blk + q];
-        ww[4 * q] = w4.x;
-        ww[4 * q + 1] = w4.y;
-        ww[4 * q + 2] = w4.z;
-        ww[4 * q + 3] = w4.w;
+        const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[8 * q + 2 * k] = bf16_lo(ww[k]);
+          v[8 * q + 2 * k + 1] = bf16_hi(ww[k]);
+        }
       }
-      // the block maximum of |sc v| is sc times that of |v|: rounding is
-      // monotone, so max |fp32(sc v)| = fp32(|sc| max |v|)
-      const uint32_t m2 = bmax16(ww);
-      float amax = fmaxf(bf16_lo(m2), bf16_hi(m2));
-      if (SCALE) amax *= fabsf(sc);
-      const int e = mx_shared_exp(amax);
+      if (SCALE) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= sc;
+      }
+      const int e = mx_shared_exp(amax32(v));
       uint32_t w[8];
-      if (amax >= kPackedMinAmax) {
-        if (SCALE) {
-          // fp32(fp32(sc v) 2^-e) = fp32(v (sc 2^-e)): scaling by a power of
-          // two commutes with rounding in the normal range, and sc 2^-e >=
-          // 2^-120 is exact
-          const float s2 = sc * exp2_int(-e);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            w[k] = cvt_e4m3x2(bf16_lo(ww[2 * k]) * s2, bf16_hi(ww[2 * k]) * s2) |
-                   (cvt_e4m3x2(bf16_lo(ww[2 * k + 1]) * s2, bf16_hi(ww[2 * k + 1]) * s2) << 16);
-        } else {
-          const uint32_t inv2 = bf16_exp2_neg(e) * 0x10001u;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t a = bmul2(ww[2 * k], inv2), b = bmul2(ww[2 * k + 1], inv2);
-            w[k] = cvt_e4m3x2(bf16_lo(a), bf16_hi(a)) | (cvt_e4m3x2(bf16_lo(b), bf16_hi(b)) << 16);
-          }
-        }
-      } else {
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          v[2 * i] = bf16_lo(ww[i]);
-          v[2 * i + 1] = bf16_hi(ww[i]);
-        }
-        if (SCALE) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= sc;
-        }
-        mx_codes32(v, e, w);
-      }
+      mx_codes32(v, e, w);
       // bytes 32 (2h + blk) .. +31 of the row's line: chunks 2 (2h + blk) and +1
       const int ch = 2 * (2 * h + blk);
       *reinterpret_cast<uint4*>(rb + row * 128 + ((ch ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -412,51 +343,17 @@ __global__ void __launch_bounds__(256, 3) gather_both_mx_kernel(const __grid_con
     uint32_t pr[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) pr[i] = *reinterpret_cast<const uint32_t*>(xcol + (rl + i) * kMxPitchB);
-    // without scores: both features' maxima and scalings on the packed
-    // words (feature 2q in the low halves, 2q + 1 in the high halves)
-    int ef[2] = {0, 0};
-    bool packed = false;
-    if (!SCALE) {
-      uint32_t m2 = 0;
-#pragma unroll
-      for (int i = 0; i < 32; i += 16) {
-        uint32_t part[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) part[j] = pr[i + j];
-        m2 = bmax2_abs(m2, bmax16(part)) & 0x7FFF7FFFu;
-      }
-      const float a0 = bf16_lo(m2), a1 = bf16_hi(m2);
-      ef[0] = mx_shared_exp(a0);
-      ef[1] = mx_shared_exp(a1);
-      packed = a0 >= kPackedMinAmax && a1 >= kPackedMinAmax;
-      if (packed) {
-        const uint32_t inv2 = bf16_exp2_neg(ef[0]) | (bf16_exp2_neg(ef[1]) << 16);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pr[i] = bmul2(pr[i], inv2);
-      }
-    }
 #pragma unroll
     for (int f = 0; f < 2; ++f) {
-      uint32_t w[8];
-      int e;
-      if (packed) {
-        e = ef[f];
+      float v[32];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t* p4 = pr + 4 * k;
-          w[k] = f == 0 ? cvt_e4m3x2(bf16_lo(p4[0]), bf16_lo(p4[1])) | (cvt_e4m3x2(bf16_lo(p4[2]), bf16_lo(p4[3])) << 16)
-                        : cvt_e4m3x2(bf16_hi(p4[0]), bf16_hi(p4[1])) | (cvt_e4m3x2(bf16_hi(p4[2]), bf16_hi(p4[3])) << 16);
-        }
-      } else {
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v[i] = f == 0 ? bf16_lo(pr[i]) : bf16_hi(pr[i]);
-          if (SCALE) v[i] *= s_row[rl + i];
-        }
-        e = mx_shared_exp(amax32(v));
-        mx_codes32(v, e, w);
+      for (int i = 0; i < 32; ++i) {
+        v[i] = f == 0 ? bf16_lo(pr[i]) : bf16_hi(pr[i]);
+        if (SCALE) v[i] *= s_row[rl + i];
       }
+      const int e = mx_shared_exp(amax32(v));
+      uint32_t w[8];
+      mx_codes32(v, e, w);
       const int cc = 2 * q + f;   // feature within the slab
       *reinterpret_cast<uint4*>(cb + cc * 128 + (((2 * g) ^ (cc & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       *reinterpret_cast<uint4*>(cb + cc * 128 + (((2 * g + 1) ^ (cc & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
