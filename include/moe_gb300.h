@@ -337,6 +337,11 @@ MOE_API moe_status prepare_block_scaled_weight(const void* w, int32_t E, int32_t
  *              state, which the backward rebuilds.
  * T may be 0 (nothing is enqueued).  T > max_tokens gives MOE_ERR_CAPACITY.
  *
+ * MOE_NVFP4 contexts: inference only (saved must be NULL), NVFP4 weights;
+ * the x rows are quantised into the routing blocks' chunks, the W13 +
+ * SwiGLU GEMM writes FP32 h2, whose rows are quantised in turn, and the W2
+ * GEMM writes BF16 h3 (six launches).
+ *
  * MOE_FUSED_LAUNCH ([DM] section 05, "Kernel Pipelines: Staged and Mega":
  * the Mega forward joins W13 and W2 in one grid with readiness counters):
  * the routing, gather, W13 + SwiGLU GEMM, W2 GEMM and combine run as one
