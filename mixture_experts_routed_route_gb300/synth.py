@@ -75,6 +75,7 @@ WORKLOADS = {
     # and 16 tokens, no shared expert; only the routed experts' weights stream
     "decode_e384_t1": Workload("decode_e384_t1", 1, 7168, 2048, 384, 6, "mxfp8", "uniform", seed=9),
     "decode_e384_t16": Workload("decode_e384_t16", 16, 7168, 2048, 384, 6, "mxfp8", "uniform", seed=10),
+    "decode_e384_t1_nvfp4": Workload("decode_e384_t1_nvfp4", 1, 7168, 2048, 384, 6, "nvfp4", "uniform", seed=9),
     # profiling case for the row-sized kernels (gathers, combine): the e384
     # token count and width (T=2048, D=7168, K=6, so about 12 K routed rows)
     # with 32 experts, about 10 GB on the device
