@@ -11,8 +11,10 @@
   on all but a few codes.
 * The forward: out within TOL["nvfp4"] of the oracle's NVFP4 forward on
   small ragged cases (several 128-row blocks, 32-row remainders, inactive
-  routes, a clamped SwiGLU), at the E=384, D=7168 inference shape on sampled
-  tokens, and at one token.
+  routes, a clamped SwiGLU, accumulation onto an existing out), at the
+  E=384, D=7168 inference shape on sampled tokens, and at one token; a
+  call whose routes are all inactive gives exact zeros, and T = 0 enqueues
+  nothing.
 """
 
 import json
@@ -198,3 +200,28 @@ def test_e384_inference_shape_sampled_tokens():
 
 def test_one_token_at_the_e384_shape():
     _sampled_parity(synth.WORKLOADS["e384_nvfp4"], 1, 1, 79)
+
+
+def test_inactive_routes_accumulate_and_empty_calls():
+    """Every route inactive: no routing block, so both GEMMs have no tile and
+    out is exactly zero (or the accumulated input, rounded once).  With
+    MOE_ACCUMULATE_OUT on a live case, out_init is added before the single
+    rounding, as the oracle does.  T = 0 enqueues nothing."""
+    case = Case(SMALL["zipf"]())
+    dead = Case(SMALL["zipf"](), ids=np.full_like(case.ids, -1), scores=np.zeros_like(case.scores))
+    g = run_gpu(dead, training=False, backward=False)
+    assert g["err_bits"] == 0 and np.all(g["out"] == 0.0)
+    g["layer"].close()
+    init = torch.randn((case.T, case.w.D), generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
+    g = run_gpu(case, training=False, backward=False, out_init=init.cuda())
+    assert g["err_bits"] == 0
+    o = run_oracle(case, backward=False, out_init=to_f64(init))
+    assert rel_err(g["out"], o["out"]) <= TOL["nvfp4"]
+    layer, W13, W2 = g["layer"], g["W13"], g["W2"]
+    dev = torch.device("cuda")
+    empty = torch.empty((0, case.w.D), dtype=torch.bfloat16, device=dev)
+    layer.forward(empty, torch.empty((0, case.w.K), dtype=torch.int32, device=dev),
+                  torch.empty((0, case.w.K), dtype=torch.float32, device=dev), W13, W2, out=empty)
+    torch.cuda.synchronize()
+    assert layer.error_bits() == 0
+    layer.close()
