@@ -225,3 +225,19 @@ def test_inactive_routes_accumulate_and_empty_calls():
     torch.cuda.synchronize()
     assert layer.error_bits() == 0
     layer.close()
+
+
+@pytest.mark.parametrize("name", ["zipf", "long_k"])
+def test_few_ctas_walk_many_tiles_bit_for_bit(name):
+    """With the persistent grids capped at 1 and 3 CTAs each CTA walks every
+    or every third tile, through both accumulator buffers and many passes of
+    the staging and operand rings; the output equals the uncapped run's bit
+    for bit (a tile's K sum does not depend on which CTA runs it)."""
+    case = Case(SMALL[name]())
+    ref = run_gpu(case, training=False, backward=False)
+    ref["layer"].close()
+    for ctas in (1, 3):
+        g = run_gpu(case, training=False, backward=False, max_ctas=ctas)
+        assert g["err_bits"] == 0
+        assert np.array_equal(g["out"], ref["out"]), ctas
+        g["layer"].close()
